@@ -1,0 +1,347 @@
+"""Pins of the fp64 oracle and of the layout writer against things other than themselves.
+
+Each check is chosen so that a plausible slip in the oracle (a dropped bias
+term, a wrong sign, a shifted bit, a transposed operand, a wrong group index)
+fails at least one of them; ``test_planted_mistakes_are_caught`` plants such
+slips in a copy of the oracle and confirms it.
+"""
+from fractions import Fraction
+import os
+
+import numpy as np
+import pytest
+
+from dequant_gemv_gemm_bt_b300 import synth
+import oracle.bt_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "layout_fixtures.txt")
+BITS = (2, 3, 4, 6, 8)
+
+
+# ------------------------------------------------------------------ fixtures
+def load_layout_fixtures():
+    out = []
+    cur = None
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, _, rest = line.partition(" ")
+        if key == "fixture":
+            cur = {"name": rest}
+        elif key == "bits":
+            cur["bits"] = int(rest)
+        elif key == "codes":
+            kind, _, spec = rest.partition(" ")
+            q = np.zeros(64, dtype=np.int64)
+            if kind == "ramp":
+                q = np.arange(64) % int(spec)
+            else:
+                for item in spec.split():
+                    j, v = item.split(":")
+                    q[int(j)] = int(v)
+            cur["codes"] = q
+        elif key == "words":
+            cur["words"] = np.array([int(h, 16) for h in rest.split()], dtype=np.uint32)
+        elif key == "end":
+            out.append(cur)
+    return out
+
+
+def brute_force_unpack(words: np.ndarray, bits: int, k: int):
+    """Bit-by-bit from the little-endian byte array, pure Python."""
+    by = bytes(np.ascontiguousarray(words, dtype="<u4").tobytes())
+    out = []
+    for j in range(k):
+        v = 0
+        for i in range(bits):
+            t = j * bits + i
+            bit = (by[t // 8] >> (t % 8)) & 1
+            v |= bit << i
+        out.append(v)
+    return out
+
+
+def frac_f16(u16) -> Fraction:
+    """Exact rational value of an fp16 bit pattern, decoded field by field."""
+    u = int(u16)
+    sign = -1 if u >> 15 else 1
+    e = (u >> 10) & 0x1F
+    m = u & 0x3FF
+    assert e != 31
+    if e == 0:
+        return sign * Fraction(m, 1 << 24)
+    return sign * Fraction(1024 + m, 1) * Fraction(2) ** (e - 25)
+
+
+def frac_bf16(u16) -> Fraction:
+    u = int(u16)
+    sign = -1 if u >> 15 else 1
+    e = (u >> 7) & 0xFF
+    m = u & 0x7F
+    assert e != 255
+    if e == 0:
+        return sign * Fraction(m, 1) * Fraction(2) ** (-133)
+    return sign * Fraction(128 + m, 1) * Fraction(2) ** (e - 134)
+
+
+# --------------------------------------------------------------- layout pins
+@pytest.mark.parametrize("fx", load_layout_fixtures(), ids=lambda f: f["name"])
+def test_layout_fixture(fx):
+    bits, q, words = fx["bits"], fx["codes"], fx["words"]
+    assert words.size == 2 * bits
+    packed = synth.pack_codes(q[None, :], bits)
+    np.testing.assert_array_equal(packed[0], words)
+    np.testing.assert_array_equal(O.unpack_codes(words[None, :], bits, 64)[0], q)
+    assert brute_force_unpack(words, bits, 64) == list(q)
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_all_ones_words_give_qmax(bits):
+    words = np.full((3, 2 * bits * 2), 0xFFFFFFFF, dtype=np.uint32)
+    q = O.unpack_codes(words, bits, 128)
+    assert np.all(q == 2**bits - 1)
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_codes_in_range_and_brute_unpack(bits):
+    r = synth.rng_for("pins", "range", bits)
+    qw = synth.make_qweight(r, 5, 192, bits)
+    q = O.unpack_codes(qw.codes, bits, 192)
+    assert q.min() >= 0 and q.max() <= 2**bits - 1
+    for n in range(5):
+        assert brute_force_unpack(qw.codes[n], bits, 192) == list(q[n])
+
+
+# --------------------------------------------------------- brute-force exact
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("k", [64, 128])
+def test_brute_force_exact(bits, k):
+    r = synth.rng_for("pins", "brute", bits, k)
+    n = 7
+    qw = synth.make_qweight(r, n, k, bits)
+    x16 = synth.draw_activations(r, 1, k, "f16")[0]
+    y, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x16))
+    xs = [frac_f16(v) for v in x16]
+    for row in range(n):
+        q = brute_force_unpack(qw.codes[row], bits, k)
+        acc = Fraction(0)
+        absacc = Fraction(0)
+        for j in range(k):
+            g = j // 64
+            w = frac_f16(qw.scales[row, g]) * q[j] + frac_f16(qw.biases[row, g])
+            acc += w * xs[j]
+            absacc += abs(w * xs[j])
+        assert abs(y[row] - float(acc)) <= 1e-12 * float(absacc) + 1e-300
+        assert abs(a[row] - float(absacc)) <= 1e-12 * float(absacc)
+
+
+def test_bf16_decode_exact():
+    r = synth.rng_for("pins", "bf16")
+    xb = synth.draw_activations(r, 1, 256, "bf16")[0]
+    got = O.decode_bf16(xb)
+    want = [float(frac_bf16(v)) for v in xb]
+    np.testing.assert_array_equal(got, np.array(want))
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    r = synth.rng_for("pins", "bf16-round")
+    a = r.standard_normal(4096).astype(np.float32)
+    a[:4] = [1.0 + 2**-8, 1.0 + 3 * 2**-8, -(1.0 + 2**-8), 0.0]  # ties to even
+    want = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(synth.f32_to_bf16_bits(a), want)
+
+
+# ------------------------------------------------------------- invariants
+@pytest.mark.parametrize("bits", BITS)
+def test_one_hot_returns_column(bits):
+    r = synth.rng_for("pins", "onehot", bits)
+    n, k = 9, 192
+    qw = synth.make_qweight(r, n, k, bits)
+    w = O.dequant_weight(qw.codes, qw.scales, qw.biases, bits, k)
+    for col in (0, 63, 64, 100, 191):
+        x = np.zeros(k)
+        x[col] = 1.0
+        y, _ = O.qgemv(qw.codes, qw.scales, qw.biases, bits, x)
+        np.testing.assert_array_equal(y, w[:, col])
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_grid_exact_roundtrip(bits):
+    r = synth.rng_for("pins", "grid", bits)
+    n, k = 6, 256
+    w, q_true, s, beta = synth.grid_exact_weights(r, n, k, bits)
+    q, s16, b16 = synth.quantize(w, bits)
+    np.testing.assert_array_equal(q, q_true)
+    np.testing.assert_array_equal(O.decode_f16(s16), s.astype(np.float64))
+    np.testing.assert_array_equal(O.decode_f16(b16), beta.astype(np.float64))
+    codes = synth.pack_codes(q, bits)
+    np.testing.assert_array_equal(O.unpack_codes(codes, bits, k), q_true)
+    wd = O.dequant_weight(codes, s16, b16, bits, k)
+    np.testing.assert_array_equal(wd, w.astype(np.float64))
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_closed_form_all_qmax(bits):
+    r = synth.rng_for("pins", "qmax", bits)
+    n, k = 4, 320
+    g = k // 64
+    codes = np.full((n, k * bits // 32), 0xFFFFFFFF, dtype=np.uint32)
+    s16 = synth.f32_to_f16_bits(r.uniform(0.001, 0.01, (n, g)))
+    b16 = synth.f32_to_f16_bits(r.uniform(-0.05, 0.0, (n, g)))
+    y, _ = O.qgemv(codes, s16, b16, bits, np.ones(k))
+    want = (64 * (O.decode_f16(s16) * (2**bits - 1) + O.decode_f16(b16))).sum(axis=1)
+    np.testing.assert_allclose(y, want, rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_closed_form_zero_scale(bits):
+    r = synth.rng_for("pins", "s0", bits)
+    n, k = 4, 256
+    g = k // 64
+    qw = synth.make_qweight(r, n, k, bits)
+    s16 = np.zeros((n, g), dtype=np.uint16)
+    x = O.decode_f16(synth.draw_activations(r, 1, k, "f16")[0])
+    y, _ = O.qgemv(qw.codes, s16, qw.biases, bits, x)
+    want = (O.decode_f16(qw.biases) * x.reshape(g, 64).sum(axis=1)[None, :]).sum(axis=1)
+    np.testing.assert_allclose(y, want, rtol=1e-13, atol=1e-15)
+
+
+def test_constant_group_quantizes_to_bias():
+    w = np.full((2, 128), 0.0123, dtype=np.float32)
+    for bits in BITS:
+        q, s16, b16 = synth.quantize(w, bits)
+        assert np.all(q == 0) and np.all(s16 == 0)
+        wd = O.dequant_weight(synth.pack_codes(q, bits), s16, b16, bits, 128)
+        np.testing.assert_array_equal(wd, np.float64(np.float16(0.0123)))
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_factored_form_matches_matmul(bits):
+    """The per-group factored form s*sum(q x) + b*sum(x) equals the matmul definition."""
+    r = synth.rng_for("pins", "factored", bits)
+    m, n, k = 3, 11, 384
+    g = k // 64
+    qw = synth.make_qweight(r, n, k, bits)
+    x = O.decode_bf16(synth.draw_activations(r, m, k, "bf16"))
+    y, a = O.qgemm(qw.codes, qw.scales, qw.biases, bits, x)
+    q = O.unpack_codes(qw.codes, bits, k).reshape(n, g, 64).astype(np.float64)
+    xs = x.reshape(m, g, 64)
+    qx = np.einsum("ngj,mgj->mng", q, xs)
+    sx = xs.sum(axis=2)
+    y2 = (O.decode_f16(qw.scales)[None] * qx + O.decode_f16(qw.biases)[None] * sx[:, None, :]).sum(2)
+    np.testing.assert_allclose(y, y2, rtol=1e-12, atol=1e-12)
+    assert np.all(a >= np.abs(y) - 1e-12)
+
+
+def test_quantizer_error_bound():
+    """Min/max quantization error is at most half a step (plus fp16 parameter rounding)."""
+    r = synth.rng_for("pins", "qerr")
+    w = synth.draw_weights(r, 16, 512)
+    for bits in BITS:
+        q, s16, b16 = synth.quantize(w, bits)
+        wd = O.dequant_weight(synth.pack_codes(q, bits), s16, b16, bits, 512)
+        step = np.repeat(O.decode_f16(s16), 64, axis=1)
+        err = np.abs(wd - w.astype(np.float64))
+        assert np.all(err <= 0.5 * step + 2e-3 * np.abs(w) + 1e-7)
+
+
+# ------------------------------------------------------------------ MoE pins
+def test_route_sort_stable_and_offsets():
+    ids = np.array([[3, 0], [0, 2], [3, 1], [2, 0]])
+    offsets, order = O.route_sort(ids, 5)
+    np.testing.assert_array_equal(offsets, [0, 3, 4, 6, 8, 8])
+    # expert 0: pairs (0,1)=1, (1,0)=2, (3,1)=7; expert 1: (2,1)=5; expert 2: 3, 6; expert 3: 0, 4
+    np.testing.assert_array_equal(order, [1, 2, 7, 5, 3, 6, 0, 4])
+
+
+def test_moe_qgemm_matches_per_expert_and_empty_experts():
+    r = synth.rng_for("pins", "moe")
+    e, n, k, bits = 4, 6, 128, 4
+    ws = [synth.make_qweight(r, n, k, bits) for _ in range(e)]
+    codes = np.stack([w.codes for w in ws])
+    sc = np.stack([w.scales for w in ws])
+    bi = np.stack([w.biases for w in ws])
+    offsets = np.array([0, 2, 2, 5, 5])  # experts 1 and 3 empty
+    x = O.decode_bf16(synth.draw_activations(r, 5, k, "bf16"))
+    y, _ = O.moe_qgemm(codes, sc, bi, bits, offsets, x)
+    for ex, (lo, hi) in enumerate(zip(offsets[:-1], offsets[1:])):
+        if hi > lo:
+            y_e, _ = O.qgemm(ws[ex].codes, ws[ex].scales, ws[ex].biases, bits, x[lo:hi])
+            np.testing.assert_array_equal(y[lo:hi], y_e)
+
+
+def test_moe_layer_single_slot_reduces_to_dense_chain():
+    r = synth.rng_for("pins", "moe-layer")
+    e, hdim, idim, bits, t = 3, 128, 64, 4, 5
+
+    def stack(n, k):
+        ws = [synth.make_qweight(r, n, k, bits) for _ in range(e)]
+        return (np.stack([w.codes for w in ws]), np.stack([w.scales for w in ws]),
+                np.stack([w.biases for w in ws]))
+    gw, uw, dw = stack(idim, hdim), stack(idim, hdim), stack(hdim, idim)
+    ids = np.array([[1], [0], [1], [2], [1]])
+    gates = np.ones((t, 1))
+    x = O.decode_bf16(synth.draw_activations(r, t, hdim, "bf16"))
+    out, _, _, _ = O.moe_layer(x, ids, gates, gw, uw, dw, bits)
+    for tok in range(t):
+        ex = ids[tok, 0]
+        g, _ = O.qgemv(gw[0][ex], gw[1][ex], gw[2][ex], bits, x[tok])
+        u, _ = O.qgemv(uw[0][ex], uw[1][ex], uw[2][ex], bits, x[tok])
+        hv = g / (1 + np.exp(-g)) * u
+        d, _ = O.qgemv(dw[0][ex], dw[1][ex], dw[2][ex], bits, hv)
+        np.testing.assert_allclose(out[tok], d, rtol=1e-12, atol=1e-14)
+
+
+def test_routing_draw_is_distinct_and_normalized():
+    r = synth.rng_for("pins", "routing")
+    ids, gates = synth.draw_routing(r, 64, 128, 8)
+    for row in ids:
+        assert len(set(row.tolist())) == 8
+    np.testing.assert_allclose(gates.sum(axis=1), 1.0, rtol=1e-6)
+
+
+# ------------------------------------------------------- planted mistakes
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Mutated oracles must fail the brute-force / invariant pins."""
+    r = synth.rng_for("pins", "mutants")
+    bits, n, k = 3, 5, 128
+    qw = synth.make_qweight(r, n, k, bits)
+    x = O.decode_f16(synth.draw_activations(r, 1, k, "f16")[0])
+    y_good, a_good = O.qgemv(qw.codes, qw.scales, qw.biases, bits, x)
+
+    def brute(row):
+        q = brute_force_unpack(qw.codes[row], bits, k)
+        return float(sum((frac_f16(qw.scales[row, j // 64]) * q[j] + frac_f16(qw.biases[row, j // 64]))
+                         * Fraction(float(x[j])) for j in range(k)))
+    want = np.array([brute(i) for i in range(n)])
+    assert np.allclose(y_good, want, rtol=1e-12, atol=1e-14)
+
+    real_unpack = O.unpack_codes
+    real_deq = O.dequantize
+    mutants = {
+        "msb_first": lambda c, b, kk, g=64: real_unpack(c, b, kk, g)[:, ::-1].copy(),
+        "dropped_bias": None,
+        "wrong_group": None,
+    }
+
+    def deq_no_bias(q, s, b, g=64):
+        return real_deq(q, s, np.zeros_like(b), g)
+
+    def deq_shifted_group(q, s, b, g=64):
+        return real_deq(q, np.roll(s, 1, axis=1), b, g)
+
+    caught = 0
+    for name in mutants:
+        with monkeypatch.context() as mp:
+            if name == "msb_first":
+                mp.setattr(O, "unpack_codes", mutants[name])
+            elif name == "dropped_bias":
+                mp.setattr(O, "dequantize", deq_no_bias)
+            else:
+                mp.setattr(O, "dequantize", deq_shifted_group)
+            y_bad, _ = O.qgemv(qw.codes, qw.scales, qw.biases, bits, x)
+            if not np.allclose(y_bad, want, rtol=1e-9, atol=1e-12):
+                caught += 1
+    assert caught == len(mutants)

@@ -1,0 +1,191 @@
+"""Python binding of libbt (ctypes; argument marshalling only).
+
+Each function has the name of the C entry point it calls and takes torch CUDA
+tensors; shapes are read from the tensors, outputs are allocated with torch
+when not given, and every product runs in libbt's CUDA kernels.  There is no
+fallback: importing this module raises when ``libbt.so`` is missing, and every
+call raises :class:`BTError` when the library returns an error status.
+
+Layout of a packed weight (see ``include/bt.h``): ``codes`` int32 (bit
+patterns of uint32) ``[N, K*bits/32]``, ``scales`` and ``biases`` float16
+``[N, K/64]``; grouped experts stack a leading ``[E]`` dimension.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbt.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libbt.so not found at {LIB_PATH}; build it with "
+        "`python -m dequant_gemv_gemm_bt_b300.build` (nvcc, sm_103a)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_MISALIGNED, BT_ERR_CUDA, BT_ERR_TIMEOUT = range(6)
+BT_F16, BT_BF16, BT_F32 = 0, 1, 2
+(BT_OPT_PDL, BT_OPT_CONST_WEIGHTS, BT_OPT_WAIT_TIMEOUT_US, BT_OPT_TEST_DROP_STAGE,
+ BT_OPT_GEMV_GENERIC, BT_OPT_GEMV_STAGES, BT_OPT_GEMM_PATH) = range(7)
+
+EXPORTS = ("bt_qgemv", "bt_qgemm", "bt_moe_qgemm", "bt_moe_route", "bt_swiglu", "bt_moe_combine",
+           "bt_status_string", "bt_last_device_error", "bt_set_option")
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_W = [_p, _p, _p, _i, _i]            # codes, scales, biases, bits, group_size
+lib.bt_qgemv.argtypes = _W + [_i, _i, _p, _i, _p, _i, _p]
+lib.bt_qgemm.argtypes = _W + [_i, _i, _i, _p, _i, _p, _i, _p]
+lib.bt_moe_qgemm.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
+lib.bt_moe_route.argtypes = [_p, _i, _i, _i, _p, _p, _p, _p]
+lib.bt_swiglu.argtypes = [_p, _i, _i, _i, _p, _i, _p]
+lib.bt_moe_combine.argtypes = [_p, _i, _p, _p, _i, _i, _i, _p, _i, _p]
+lib.bt_status_string.argtypes = [_i]
+lib.bt_status_string.restype = ctypes.c_char_p
+lib.bt_last_device_error.argtypes = [_p]
+lib.bt_set_option.argtypes = [_i, ctypes.c_longlong]
+for _name in EXPORTS:
+    if _name != "bt_status_string":
+        getattr(lib, _name).restype = _i
+
+_DT = {torch.float16: BT_F16, torch.bfloat16: BT_BF16, torch.float32: BT_F32}
+
+
+class BTError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bt_status_string(status)}")
+
+
+def bt_status_string(status: int) -> str:
+    return lib.bt_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != BT_OK:
+        raise BTError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def _weights(codes, scales, biases):
+    return _dev(codes, "codes"), _dev(scales, "scales"), _dev(biases, "biases")
+
+
+def bt_set_option(option: int, value: int) -> None:
+    _check(lib.bt_set_option(int(option), int(value)), "bt_set_option")
+
+
+def bt_last_device_error(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device error status."""
+    return lib.bt_last_device_error(_stream(stream))
+
+
+def bt_qgemv(codes, scales, biases, bits: int, x, y=None, *, group_size: int = 64,
+             out_dtype=torch.float32, stream=None):
+    """``y[n] = sum_k x[k] * w_deq[n, k]``; ``x`` [K] fp16/bf16, ``y`` [N]."""
+    n = codes.shape[0]
+    k = x.shape[-1]
+    if y is None:
+        y = torch.empty(n, dtype=out_dtype, device=x.device)
+    c, s, b = _weights(codes, scales, biases)
+    _check(lib.bt_qgemv(c, s, b, bits, group_size, n, k, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y),
+                        _stream(stream)), "bt_qgemv")
+    return y
+
+
+def bt_qgemm(codes, scales, biases, bits: int, x, y=None, *, group_size: int = 64,
+             out_dtype=torch.bfloat16, stream=None):
+    """``Y = X @ W_deq^T``; ``x`` [M, K] bf16/fp16, ``Y`` [M, N]."""
+    n = codes.shape[0]
+    m, k = x.shape
+    if y is None:
+        y = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    c, s, b = _weights(codes, scales, biases)
+    _check(lib.bt_qgemm(c, s, b, bits, group_size, m, n, k, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y),
+                        _stream(stream)), "bt_qgemm")
+    return y
+
+
+def bt_moe_qgemm(codes, scales, biases, bits: int, expert_offsets, x, y=None, *, total_rows=None,
+                 x_row_index=None, group_size: int = 64, out_dtype=torch.bfloat16, stream=None):
+    """Grouped expert product; ``codes`` [E, N, .], ``expert_offsets`` int32 [E+1] on the device.
+
+    ``total_rows`` defaults to ``len(x_row_index)`` when a gather index is given, else ``x.shape[0]``.
+    """
+    e, n = codes.shape[0], codes.shape[1]
+    k = x.shape[-1]
+    if total_rows is None:
+        total_rows = x_row_index.shape[0] if x_row_index is not None else x.shape[0]
+    if y is None:
+        y = torch.empty((total_rows, n), dtype=out_dtype, device=x.device)
+    c, s, b = _weights(codes, scales, biases)
+    ri = _dev(x_row_index, "x_row_index") if x_row_index is not None else None
+    _check(lib.bt_moe_qgemm(c, s, b, bits, group_size, e, n, k, _dev(expert_offsets, "expert_offsets"),
+                            total_rows, ri, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y), _stream(stream)),
+           "bt_moe_qgemm")
+    return y
+
+
+def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair_row=None, stream=None):
+    """Stable grouping of (token, slot) pairs by expert: returns (offsets, pair_index, pair_row)."""
+    t, top_k = topk_ids.shape
+    dev = topk_ids.device
+    if offsets is None:
+        offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    if pair_index is None:
+        pair_index = torch.empty(t * top_k, dtype=torch.int32, device=dev)
+    if pair_row is None:
+        pair_row = torch.empty(t * top_k, dtype=torch.int32, device=dev)
+    _check(lib.bt_moe_route(_dev(topk_ids, "topk_ids"), t, top_k, num_experts, _dev(offsets, "offsets"),
+                            _dev(pair_index, "pair_index"), _dev(pair_row, "pair_row"), _stream(stream)),
+           "bt_moe_route")
+    return offsets, pair_index, pair_row
+
+
+def bt_swiglu(gate_up, h=None, *, out_dtype=None, stream=None):
+    """``h = silu(gate_up[:, :I]) * gate_up[:, I:]``."""
+    rows, two_i = gate_up.shape
+    inter = two_i // 2
+    if h is None:
+        h = torch.empty((rows, inter), dtype=out_dtype or gate_up.dtype, device=gate_up.device)
+    _check(lib.bt_swiglu(_dev(gate_up, "gate_up"), _dt(gate_up), rows, inter, _dev(h, "h"), _dt(h),
+                         _stream(stream)), "bt_swiglu")
+    return h
+
+
+def bt_moe_combine(y_grouped, gates, pair_row, top_k: int, out=None, *, out_dtype=None, stream=None):
+    """``out[t] = sum_s gates[t, s] * y_grouped[pair_row[t*top_k + s]]``."""
+    hidden = y_grouped.shape[1]
+    tokens = gates.shape[0]
+    if out is None:
+        out = torch.empty((tokens, hidden), dtype=out_dtype or y_grouped.dtype, device=y_grouped.device)
+    _check(lib.bt_moe_combine(_dev(y_grouped, "y_grouped"), _dt(y_grouped), _dev(gates, "gates"),
+                              _dev(pair_row, "pair_row"), tokens, top_k, hidden, _dev(out, "out"), _dt(out),
+                              _stream(stream)), "bt_moe_combine")
+    return out

@@ -1,0 +1,233 @@
+// C ABI of libbt: argument validation, per-shape launch heuristics and the
+// device error word.  Every product is computed by the kernels in this
+// library; nothing here computes on the host.
+#include <cstdlib>
+#include <mutex>
+#include <vector>
+
+#include "bt_common.cuh"
+#include "moe.cuh"
+#include "qgemm.cuh"
+#include "qgemv.cuh"
+
+namespace bt {
+
+__device__ unsigned g_device_error = 0;
+
+LaunchOpts& opts() {
+  static LaunchOpts o;
+  return o;
+}
+
+namespace {
+std::mutex g_mu;
+std::vector<unsigned*> g_err_ptr;   // per device
+std::vector<int> g_sms;
+
+int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+}  // namespace
+
+unsigned* device_error_word() {
+  const int d = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_err_ptr.size() <= d) g_err_ptr.resize(d + 1, nullptr);
+  if (!g_err_ptr[d]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<unsigned*>(ptr);
+  }
+  return g_err_ptr[d];
+}
+
+int sm_count() {
+  const int d = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_sms.size() <= d) g_sms.resize(d + 1, 0);
+  if (!g_sms[d]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = v > 0 ? v : 1;
+  }
+  return g_sms[d];
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 6 || b == 8; }
+bool half_dtype(bt_dtype d) { return d == BT_F16 || d == BT_BF16; }
+bool out_dtype(bt_dtype d) { return d == BT_F16 || d == BT_BF16 || d == BT_F32; }
+
+bt_status check_weights(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                        int group_size, int N, int K) {
+  if (!codes || !scales || !biases) return BT_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0) return BT_ERR_INVALID_ARG;
+  if (!bits_ok(bits) || group_size != kGroup) return BT_ERR_UNSUPPORTED;
+  if (K % group_size) return BT_ERR_INVALID_ARG;
+  if (K > kMaxK) return BT_ERR_UNSUPPORTED;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(biases)) return BT_ERR_MISALIGNED;
+  return BT_OK;
+}
+
+bt_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) e = cudaGetLastError();
+  else cudaGetLastError();
+  return e == cudaSuccess ? BT_OK : BT_ERR_CUDA;
+}
+
+bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits, int N, int K,
+                   const void* x, bt_dtype xd, void* y, bt_dtype yd, int problems, const int32_t* offsets,
+                   const int32_t* row_index, int num_experts, cudaStream_t stream) {
+  GemvParams p{};
+  p.codes = codes;
+  p.scales = scales;
+  p.biases = biases;
+  p.x = x;
+  p.y = y;
+  p.N = N;
+  p.K = K;
+  p.G = K / kGroup;
+  p.moe_offsets = offsets;
+  p.row_index = row_index;
+  p.num_experts = offsets ? num_experts : 0;
+  p.total_rows = problems;
+  p.err = device_error_word();
+  p.timeout_ns = opts().wait_timeout_ns;
+  p.const_weights = opts().pdl && opts().const_weights;
+  p.drop_stage = opts().test_drop_stage;
+  opts().test_drop_stage = 0;
+  const GemvPlan pl = plan_gemv(bits, N, K, problems, p.num_experts, sm_count());
+  return cuda_status(launch_gemv(p, pl, bits, xd, yd, stream));
+}
+
+}  // namespace
+}  // namespace bt
+
+using namespace bt;
+
+extern "C" {
+
+const char* bt_status_string(bt_status s) {
+  switch (s) {
+    case BT_OK: return "BT_OK";
+    case BT_ERR_INVALID_ARG: return "BT_ERR_INVALID_ARG: invalid argument";
+    case BT_ERR_UNSUPPORTED: return "BT_ERR_UNSUPPORTED: unsupported bits, group size or size";
+    case BT_ERR_MISALIGNED: return "BT_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case BT_ERR_CUDA: return "BT_ERR_CUDA: CUDA call or launch failed";
+    case BT_ERR_TIMEOUT: return "BT_ERR_TIMEOUT: a device-side wait expired";
+  }
+  return "unknown bt_status";
+}
+
+bt_status bt_set_option(bt_option option, long long value) {
+  if (value < 0) return BT_ERR_INVALID_ARG;
+  switch (option) {
+    case BT_OPT_PDL: opts().pdl = value != 0; return BT_OK;
+    case BT_OPT_CONST_WEIGHTS: opts().const_weights = value != 0; return BT_OK;
+    case BT_OPT_WAIT_TIMEOUT_US: opts().wait_timeout_ns = (unsigned long long)value * 1000ull; return BT_OK;
+    case BT_OPT_TEST_DROP_STAGE: opts().test_drop_stage = value != 0; return BT_OK;
+    case BT_OPT_GEMV_GENERIC: opts().gemv_generic = value != 0; return BT_OK;
+    case BT_OPT_GEMV_STAGES: opts().gemv_stages = (int)value; return BT_OK;
+    case BT_OPT_GEMM_PATH: opts().gemm_path = (int)value; return BT_OK;
+  }
+  return BT_ERR_INVALID_ARG;
+}
+
+bt_status bt_last_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return BT_ERR_CUDA;
+  }
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return BT_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return BT_ERR_CUDA;
+  }
+  if (v & kErrTimeout) return BT_ERR_TIMEOUT;
+  if (v & kErrBadArg) return BT_ERR_INVALID_ARG;
+  return BT_OK;
+}
+
+bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                   int group_size, int N, int K, const void* x, bt_dtype x_dtype, void* y, bt_dtype y_dtype,
+                   cudaStream_t stream) {
+  bt_status s = check_weights(codes, scales, biases, bits, group_size, N, K);
+  if (s != BT_OK) return s;
+  if (!x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
+  if (!aligned16(x)) return BT_ERR_MISALIGNED;
+  return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0, stream);
+}
+
+bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                   int group_size, int M, int N, int K, const void* x, bt_dtype x_dtype, void* y,
+                   bt_dtype y_dtype, cudaStream_t stream) {
+  bt_status s = check_weights(codes, scales, biases, bits, group_size, N, K);
+  if (s != BT_OK) return s;
+  if (M <= 0 || !x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
+  if (!aligned16(x)) return BT_ERR_MISALIGNED;
+  if (M == 1) return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0, stream);
+  GemmParams p{};
+  p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
+  p.M = M; p.N = N; p.K = K;
+  p.err = device_error_word();
+  p.timeout_ns = opts().wait_timeout_ns;
+  return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
+}
+
+bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                       int group_size, int num_experts, int N, int K, const int32_t* expert_offsets,
+                       int total_rows, const int32_t* x_row_index, const void* x, bt_dtype x_dtype, void* y,
+                       bt_dtype y_dtype, cudaStream_t stream) {
+  bt_status s = check_weights(codes, scales, biases, bits, group_size, N, K);
+  if (s != BT_OK) return s;
+  if (num_experts <= 0 || num_experts > 4096 || total_rows < 0 || !expert_offsets || !x || !y ||
+      !half_dtype(x_dtype) || !out_dtype(y_dtype))
+    return BT_ERR_INVALID_ARG;
+  if (!aligned16(x)) return BT_ERR_MISALIGNED;
+  if (total_rows == 0) return BT_OK;
+  if (total_rows <= num_experts && opts().gemm_path != 1)
+    return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, total_rows, expert_offsets,
+                    x_row_index, num_experts, stream);
+  GemmParams p{};
+  p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
+  p.M = total_rows; p.N = N; p.K = K;
+  p.offsets = expert_offsets;
+  p.row_index = x_row_index;
+  p.num_experts = num_experts;
+  p.err = device_error_word();
+  p.timeout_ns = opts().wait_timeout_ns;
+  return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
+}
+
+bt_status bt_moe_route(const int32_t* topk_ids, int tokens, int top_k, int num_experts, int32_t* expert_offsets,
+                       int32_t* pair_index, int32_t* pair_row, cudaStream_t stream) {
+  if (tokens < 0 || top_k < 1 || top_k > 32 || num_experts < 1 || num_experts > 4096) return BT_ERR_INVALID_ARG;
+  if (!expert_offsets || (tokens > 0 && (!topk_ids || !pair_index || !pair_row))) return BT_ERR_INVALID_ARG;
+  if ((long long)tokens * top_k > (1LL << 30)) return BT_ERR_UNSUPPORTED;
+  return cuda_status(launch_moe_route(topk_ids, tokens, top_k, num_experts, expert_offsets, pair_index, pair_row,
+                                      stream));
+}
+
+bt_status bt_swiglu(const void* gate_up, bt_dtype in_dtype, int rows, int inter, void* h, bt_dtype h_dtype,
+                    cudaStream_t stream) {
+  if (rows < 0 || inter <= 0 || !out_dtype(in_dtype) || !out_dtype(h_dtype)) return BT_ERR_INVALID_ARG;
+  if (rows > 0 && (!gate_up || !h)) return BT_ERR_INVALID_ARG;
+  return cuda_status(launch_swiglu(gate_up, in_dtype, rows, inter, h, h_dtype, stream));
+}
+
+bt_status bt_moe_combine(const void* y_grouped, bt_dtype y_dtype, const float* gates, const int32_t* pair_row,
+                         int tokens, int top_k, int hidden, void* out, bt_dtype out_dtype_, cudaStream_t stream) {
+  if (tokens < 0 || top_k < 1 || top_k > 32 || hidden <= 0 || !out_dtype(y_dtype) || !out_dtype(out_dtype_))
+    return BT_ERR_INVALID_ARG;
+  if (tokens > 65535) return BT_ERR_UNSUPPORTED;
+  if (tokens > 0 && (!y_grouped || !gates || !pair_row || !out)) return BT_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(y_grouped, y_dtype, gates, pair_row, tokens, top_k, hidden, out, out_dtype_,
+                                    stream));
+}
+
+}  // extern "C"

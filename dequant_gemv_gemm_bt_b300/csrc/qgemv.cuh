@@ -1,0 +1,43 @@
+// Dequant-GEMV launch description shared by the dense and grouped-expert entry points.
+#pragma once
+#include <algorithm>
+#include "bt_common.cuh"
+
+namespace bt {
+
+// One launch streams `problems` independent GEMVs of the same [N, K] shape.
+// Dense: one problem.  Grouped experts at one row per expert (decode): problem
+// r is grouped row r, whose expert is found from the device offsets.
+struct GemvParams {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const void* x;
+  void* y;
+  int N, K, G;
+  // plan
+  int rows_per_unit, row_bytes, stage_bytes, stages, kw, units_per_problem;
+  long long num_units;
+  // grouped experts (null offsets = dense)
+  const int32_t* moe_offsets;
+  const int32_t* row_index;
+  int num_experts;
+  int total_rows;
+  // control
+  unsigned* err;
+  unsigned long long timeout_ns;
+  int const_weights;
+  int drop_stage;
+};
+
+struct GemvPlan {
+  int kw, cpl, rows_per_unit, row_bytes, stage_bytes, stages, units_per_problem, grid;
+  long long num_units;
+  size_t smem;
+};
+
+GemvPlan plan_gemv(int bits, int N, int K, int problems, int num_experts, int sms);
+cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,
+                        cudaStream_t stream);
+
+}  // namespace bt

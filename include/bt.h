@@ -1,0 +1,205 @@
+/*
+ * bt.h -- C ABI of libbt: matrix products over affine group-quantized weights
+ * with the dequantization done inside the compute loop (B300, sm_103a).
+ *
+ * What is computed.  The BaseRT pages describe "affine quantization Q2 to Q8"
+ * (thakicloud.com, "Apple Silicon 로컬 LLM 추론의 새 기준 BaseRT", section
+ * "BaseRT는 무엇인가") and "dedicated GEMV kernels for decode where M=1, GEMM
+ * kernels for prefill where M>1; dequantization happens inline in the compute
+ * loop rather than materializing full-precision weights to memory; memory
+ * traffic scales with the compression ratio" (thetesserapress.com, "BaseRT
+ * claims fastest Apple Silicon inference", section "What BaseRT does
+ * differently").  Every product here is
+ *
+ *     y[m, n] = sum_k x[m, k] * (s[n, k/g] * q[n, k] + b[n, k/g])
+ *
+ * with q an unsigned b-bit code.  No dequantized weight is ever written to
+ * global memory.
+ *
+ * Packed-weight layout (all row-major, bases 16-byte aligned):
+ *   codes   uint32 [N][K*bits/32]  each group of g codes is a group-local
+ *           LSB-first bitstream of g*bits bits in g*bits/32 words: code j of a
+ *           group is stream bits [j*bits, j*bits+bits), stream bit t is bit
+ *           t%32 of the group's word t/32.  bits = 4 gives "8 codes per
+ *           uint32", code j in bits [4*(j%8), +4) of word j/8.
+ *   scales  fp16 bit patterns (uint16) [N][K/g]
+ *   biases  fp16 bit patterns (uint16) [N][K/g]
+ * Supported: bits in {2,3,4,6,8}; g = 64; K a multiple of g.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are device memory owned by the caller; the library keeps no
+ *     pointer after the call returns and allocates no device memory.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
+ *     synchronize.  Argument errors return before any launch and leave the
+ *     outputs untouched.  A failed launch returns BT_ERR_CUDA.
+ *   - Results are deterministic: the same inputs give bitwise-identical
+ *     outputs (no atomics in any reduction).
+ *   - Device-side bounded waits that expire set a device error word, which
+ *     bt_last_device_error() reports as BT_ERR_TIMEOUT.
+ */
+#ifndef BT_H_
+#define BT_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define BT_API __attribute__((visibility("default")))
+#else
+#define BT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BT_OK = 0,
+  BT_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, K % g != 0, bad dtype */
+  BT_ERR_UNSUPPORTED = 2,  /* bits or group size not supported, size beyond a kernel limit */
+  BT_ERR_MISALIGNED = 3,   /* a base pointer is not 16-byte aligned */
+  BT_ERR_CUDA = 4,         /* a CUDA runtime call or a launch failed */
+  BT_ERR_TIMEOUT = 5       /* a device-side bounded wait expired (see bt_last_device_error) */
+} bt_status;
+
+typedef enum { BT_F16 = 0, BT_BF16 = 1, BT_F32 = 2 } bt_dtype;
+
+/*
+ * Dequant-GEMV, M = 1 (decode): y[n] = sum_k x[k] * w_deq[n, k], n < N.
+ * BaseRT pages, thetesserapress.com "What BaseRT does differently": the
+ * dedicated decode GEMV with inline dequantization.
+ *   codes/scales/biases  packed weight [N, K] (layout above)
+ *   x        [K] of x_dtype (BT_F16 or BT_BF16)
+ *   y        [N] of y_dtype (BT_F32, BT_BF16 or BT_F16); accumulation is fp32
+ * Limits: N >= 1, 64 <= K <= 32768.
+ */
+BT_API bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                   int bits, int group_size, int N, int K,
+                   const void* x, bt_dtype x_dtype,
+                   void* y, bt_dtype y_dtype, cudaStream_t stream);
+
+/*
+ * Dequant-GEMM, M > 1 (prefill): Y[m, n] = sum_k X[m, k] * w_deq[n, k].
+ * BaseRT pages, thetesserapress.com "What BaseRT does differently" (GEMM for
+ * prefill where M > 1) and gist.science "Metodologia" (tiled prefill GEMM on
+ * the matrix units).  Weights are dequantized in registers and fed to the
+ * tensor cores (M >= 64) or to a CUDA-core tile (small M); fp32 accumulation.
+ *   X  [M, K] row-major, x_dtype BT_BF16 or BT_F16
+ *   Y  [M, N] row-major, y_dtype BT_BF16, BT_F16 or BT_F32
+ * M = 1 is accepted and runs the GEMV.  Limits: 1 <= M, 64 <= K <= 32768.
+ */
+BT_API bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                   int bits, int group_size, int M, int N, int K,
+                   const void* x, bt_dtype x_dtype,
+                   void* y, bt_dtype y_dtype, cudaStream_t stream);
+
+/*
+ * Grouped expert GEMM: for each expert e, rows r in [off[e], off[e+1]) of the
+ * grouped activation matrix use expert e's weight:
+ *     Y[r, n] = sum_k Xg[r, k] * w_deq_e[n, k].
+ * BaseRT pages, thetesserapress.com "Where the wins land, and where they
+ * don't" (mixture-of-experts prefill without branching on expert routing).
+ *   codes/scales/biases  experts stacked: [E][N][K*bits/32], [E][N][K/g]
+ *   expert_offsets  device int32 [E+1], non-decreasing, off[0] = 0,
+ *                   off[E] = total_rows; experts may be empty
+ *   x_row_index     device int32 [total_rows] or NULL.  When given, grouped
+ *                   row r reads X row x_row_index[r] (a gather); when NULL,
+ *                   X is already in grouped order, [total_rows, K]
+ *   x     X of x_dtype (BT_F16 or BT_BF16), rows of K elements
+ *   y     [total_rows, N] of y_dtype, grouped order
+ * Offsets are read on the device; rows outside [0, total_rows) are never
+ * touched.  Limits: E >= 1, total_rows >= 0, 64 <= K <= 32768.
+ */
+BT_API bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                       int bits, int group_size, int num_experts, int N, int K,
+                       const int32_t* expert_offsets, int total_rows,
+                       const int32_t* x_row_index,
+                       const void* x, bt_dtype x_dtype,
+                       void* y, bt_dtype y_dtype, cudaStream_t stream);
+
+/*
+ * Expert routing step of a mixture-of-experts layer: groups the T*top_k
+ * (token, slot) pairs by expert id with a stable counting sort, so that within
+ * an expert the pairs keep (token, slot) order.
+ *   topk_ids        device int32 [T, top_k], each in [0, E)
+ *   expert_offsets  device int32 [E+1] (out)
+ *   pair_index      device int32 [T*top_k] (out): grouped row r holds pair
+ *                   pair_index[r] = t*top_k + slot
+ *   pair_row        device int32 [T*top_k] (out): inverse of pair_index
+ * Ids outside [0, E) set the device error word and are placed in no group
+ * (bt_last_device_error then returns BT_ERR_INVALID_ARG).
+ * Limits: T >= 0, 1 <= top_k <= 32, 1 <= E <= 4096.
+ */
+BT_API bt_status bt_moe_route(const int32_t* topk_ids, int tokens, int top_k, int num_experts,
+                       int32_t* expert_offsets, int32_t* pair_index, int32_t* pair_row,
+                       cudaStream_t stream);
+
+/*
+ * SwiGLU between the gate/up and down products: h[r, i] = silu(a[r, i]) * a[r, I + i]
+ * for a = [gate | up] of shape [rows, 2*I] (dtype BT_F32, BT_BF16 or BT_F16);
+ * h is [rows, I] of h_dtype.  Computed in fp32.
+ */
+BT_API bt_status bt_swiglu(const void* gate_up, bt_dtype in_dtype, int rows, int inter,
+                    void* h, bt_dtype h_dtype, cudaStream_t stream);
+
+/*
+ * Weighted combine of expert outputs: out[t, :] = sum_{s < top_k} gates[t, s] *
+ * Yg[pair_row[t*top_k + s], :], summed in slot order in fp32.
+ *   y_grouped  [T*top_k, H] of y_dtype (grouped order)
+ *   gates      device float32 [T, top_k]
+ *   pair_row   device int32 [T*top_k] from bt_moe_route
+ *   out        [T, H] of out_dtype
+ */
+BT_API bt_status bt_moe_combine(const void* y_grouped, bt_dtype y_dtype, const float* gates,
+                         const int32_t* pair_row, int tokens, int top_k, int hidden,
+                         void* out, bt_dtype out_dtype, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+BT_API const char* bt_status_string(bt_status status);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device error word.
+ * Returns BT_OK, BT_ERR_TIMEOUT (a bounded wait expired), BT_ERR_INVALID_ARG
+ * (a device-side argument check failed, e.g. a routing id out of range) or
+ * BT_ERR_CUDA (the synchronization itself failed).
+ */
+BT_API bt_status bt_last_device_error(cudaStream_t stream);
+
+/*
+ * Launch options (process-wide, host side; read at each call; not thread-safe
+ * against concurrent calls).
+ *   BT_OPT_PDL          1: launch with programmatic dependent launch so a call's
+ *                       prologue overlaps the previous kernel on the stream.
+ *   BT_OPT_CONST_WEIGHTS 1 (with PDL): the caller promises that the packed
+ *                       weights are not written by the kernel launched just
+ *                       before on the same stream, so weight loads may start
+ *                       before that kernel finishes.  Activations are always
+ *                       read after it finishes.
+ *   BT_OPT_WAIT_TIMEOUT_US  bound of every device-side wait, microseconds
+ *                       (default 4,000,000).
+ *   BT_OPT_TEST_DROP_STAGE  test hook, 1: the next GEMV launch leaves its first
+ *                       pipeline stage unfilled in CTA 0, so that CTA's waits
+ *                       expire after BT_OPT_WAIT_TIMEOUT_US and the call reports
+ *                       BT_ERR_TIMEOUT through bt_last_device_error().  Resets
+ *                       itself after one launch.
+ *   BT_OPT_GEMV_GENERIC  tuning, 1: GEMV uses the generic unpack path for all bits.
+ *   BT_OPT_GEMV_STAGES   tuning: GEMV pipeline depth (0 = heuristic, else 2..8).
+ *   BT_OPT_GEMM_PATH     tuning: 0 = heuristic, 1 = CUDA-core tile,
+ *                       2 = tensor-core tile where supported.
+ */
+typedef enum {
+  BT_OPT_PDL = 0,
+  BT_OPT_CONST_WEIGHTS = 1,
+  BT_OPT_WAIT_TIMEOUT_US = 2,
+  BT_OPT_TEST_DROP_STAGE = 3,
+  BT_OPT_GEMV_GENERIC = 4,
+  BT_OPT_GEMV_STAGES = 5,
+  BT_OPT_GEMM_PATH = 6
+} bt_option;
+/* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
+BT_API bt_status bt_set_option(bt_option option, long long value);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BT_H_ */

@@ -1,0 +1,68 @@
+"""Dequant-GEMM (M > 1) on the GPU against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle.bt_oracle as O
+from helpers import assert_close, half_tensor, make_case, out_to_f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from dequant_gemv_gemm_bt_b300 import bt
+    return torch, bt
+
+
+def run(env, qw, xb, xdtype, out_dtype, path=0):
+    torch, bt = env
+    codes, scales, biases = to_dev(qw, torch)
+    x = half_tensor(xb, xdtype, torch)
+    od = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[out_dtype]
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, path)
+        y = bt.bt_qgemm(codes, scales, biases, qw.bits, x, out_dtype=od)
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
+    torch.cuda.synchronize()
+    return out_to_f64(y, torch)
+
+
+@pytest.mark.parametrize("bits", (2, 3, 4, 6, 8))
+@pytest.mark.parametrize("m,n,k", [(2, 130, 256), (17, 300, 1024), (64, 257, 512), (128, 384, 3072), (130, 200, 192)])
+def test_qgemm_matches_oracle(env, bits, m, n, k):
+    qw, x = make_case("gemm", n, k, bits, m=m, xdtype="bf16")
+    y = run(env, qw, x, "bf16", "bf16")
+    y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, bits, O.decode_bf16(x))
+    assert_close(y, y_ref, a, "bf16", f"b={bits} m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("m", [2, 16, 33, 64, 127, 128, 129, 256, 512])
+def test_qgemm_paths_q4(env, path, m):
+    qw, x = make_case("gemm-path", 640, 1024, 4, m=m, xdtype="bf16")
+    y = run(env, qw, x, "bf16", "bf16", path=path)
+    y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_bf16(x))
+    assert_close(y, y_ref, a, "bf16", f"path={path} m={m}")
+
+
+@pytest.mark.parametrize("xdtype,out", [("f16", "f32"), ("bf16", "f32"), ("f16", "f16")])
+def test_qgemm_dtypes(env, xdtype, out):
+    qw, x = make_case("gemm-dt", 256, 1024, 4, m=96, xdtype=xdtype)
+    y = run(env, qw, x, xdtype, out)
+    y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_half(x, xdtype))
+    assert_close(y, y_ref, a, out, f"{xdtype}->{out}")
+
+
+def test_qgemm_m1_is_gemv(env):
+    qw, x = make_case("gemm-m1", 500, 1024, 4, m=1, xdtype="f16")
+    y = run(env, qw, x, "f16", "f32")
+    y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x))
+    assert_close(y, y_ref, a, "f32", "M=1")
+
+
+def test_qgemm_deterministic(env):
+    qw, x = make_case("gemm-det", 512, 2048, 4, m=128, xdtype="bf16")
+    assert np.array_equal(run(env, qw, x, "bf16", "bf16"), run(env, qw, x, "bf16", "bf16"))

@@ -1,0 +1,144 @@
+"""Dequant-GEMV (M = 1) on the GPU against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle.bt_oracle as O
+from helpers import assert_close, half_tensor, make_case, out_to_f64, to_dev
+
+pytestmark = pytest.mark.gpu
+BITS = (2, 3, 4, 6, 8)
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from dequant_gemv_gemm_bt_b300 import bt
+    return torch, bt
+
+
+def run(env, qw, x16, xdtype, out_dtype):
+    torch, bt = env
+    codes, scales, biases = to_dev(qw, torch)
+    x = half_tensor(x16[0], xdtype, torch)
+    od = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[out_dtype]
+    y = bt.bt_qgemv(codes, scales, biases, qw.bits, x, out_dtype=od)
+    torch.cuda.synchronize()
+    return out_to_f64(y, torch)
+
+
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("n,k", [(1, 64), (7, 128), (333, 1024), (2085, 1024), (515, 3072), (260, 8192)])
+def test_qgemv_matches_oracle(env, bits, n, k):
+    qw, x = make_case("gemv", n, k, bits)
+    y = run(env, qw, x, "f16", "f32")
+    y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x[0]))
+    assert_close(y, y_ref, a, "f32", f"b={bits} n={n} k={k}")
+
+
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("xdtype,out", [("bf16", "f32"), ("f16", "bf16"), ("bf16", "f16")])
+def test_qgemv_dtypes(env, bits, xdtype, out):
+    qw, x = make_case("gemv-dt", 301, 2048, bits, xdtype=xdtype)
+    y = run(env, qw, x, xdtype, out)
+    y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_half(x[0], xdtype))
+    assert_close(y, y_ref, a, out, f"b={bits} {xdtype}->{out}")
+
+
+@pytest.mark.parametrize("k", [64, 1024, 16384, 32768])
+def test_qgemv_k_extremes(env, k):
+    for bits in (3, 4):
+        qw, x = make_case("gemv-k", 41, k, bits)
+        y = run(env, qw, x, "f16", "f32")
+        y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x[0]))
+        assert_close(y, y_ref, a, "f32", f"b={bits} k={k}")
+
+
+def test_qgemv_single_q4_workload_and_determinism(env):
+    """The single Q4 GEMV workload: N=2048, K=1024, fp16 x, fp32 y."""
+    torch, bt = env
+    qw, x = make_case("c1", 2048, 1024, 4)
+    y1 = run(env, qw, x, "f16", "f32")
+    y2 = run(env, qw, x, "f16", "f32")
+    assert np.array_equal(y1, y2), "GEMV is not bitwise deterministic"
+    y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]))
+    assert_close(y1, y_ref, a, "f32", "N=2048 K=1024 Q4")
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_qgemv_one_hot_returns_column(env, bits):
+    torch, bt = env
+    n, k = 517, 1024
+    qw, _ = make_case("onehot", n, k, bits)
+    w = O.dequant_weight(qw.codes, qw.scales, qw.biases, bits, k)
+    for col in (0, 31, 32, 63, 64, 777, 1023):
+        x = np.zeros((1, k), dtype=np.float16)
+        x[0, col] = 1.0
+        y = run(env, qw, x.view(np.uint16), "f16", "f32")
+        np.testing.assert_allclose(y, w[:, col], rtol=0, atol=1e-5)
+
+
+def test_qgemv_lm_head_sampled(env):
+    """Full-size lm_head GEMV (N=151936, K=1024, Q4) checked on sampled rows."""
+    torch, bt = env
+    from dequant_gemv_gemm_bt_b300 import synth
+    r = synth.rng_for("test", "lm_head")
+    qw = synth.make_qweight(r, 151936, 1024, 4)
+    x = synth.draw_activations(r, 1, 1024, "f16")
+    y = run(env, qw, x, "f16", "f32")
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(151936 - 64, 151936),
+                                     r.integers(0, 151936, 2000)]))
+    y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]), rows=rows)
+    assert_close(y[rows], y_ref, a, "f32", "lm_head sampled rows")
+
+
+def test_qgemv_pdl_and_const_weights(env):
+    torch, bt = env
+    qw, x = make_case("pdl", 1200, 2048, 4)
+    y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]))
+    try:
+        bt.bt_set_option(bt.BT_OPT_PDL, 1)
+        bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
+        ys = [run(env, qw, x, "f16", "f32") for _ in range(3)]
+    finally:
+        bt.bt_set_option(bt.BT_OPT_PDL, 0)
+        bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 0)
+    for y in ys:
+        assert_close(y, y_ref, a, "f32", "pdl")
+
+
+def test_qgemv_generic_path_matches_fast(env):
+    torch, bt = env
+    for bits in (2, 4, 8):
+        qw, x = make_case("generic", 300, 1024, bits)
+        y_fast = run(env, qw, x, "f16", "f32")
+        try:
+            bt.bt_set_option(bt.BT_OPT_GEMV_GENERIC, 1)
+            y_gen = run(env, qw, x, "f16", "f32")
+        finally:
+            bt.bt_set_option(bt.BT_OPT_GEMV_GENERIC, 0)
+        y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x[0]))
+        assert_close(y_gen, y_ref, a, "f32", "generic")
+        assert_close(y_fast, y_ref, a, "f32", "fast")
+
+
+def test_device_wait_timeout_is_reported(env):
+    """A stage that is never filled makes the consumers' bounded waits expire;
+    the call reports BT_ERR_TIMEOUT and the context stays usable."""
+    torch, bt = env
+    qw, x = make_case("timeout", 4000, 1024, 4)
+    codes, scales, biases = to_dev(qw, torch)
+    xt = half_tensor(x[0], "f16", torch)
+    assert bt.bt_last_device_error() == bt.BT_OK
+    try:
+        bt.bt_set_option(bt.BT_OPT_WAIT_TIMEOUT_US, 20000)
+        bt.bt_set_option(bt.BT_OPT_TEST_DROP_STAGE, 1)
+        bt.bt_qgemv(codes, scales, biases, 4, xt)
+        assert bt.bt_last_device_error() == bt.BT_ERR_TIMEOUT
+    finally:
+        bt.bt_set_option(bt.BT_OPT_TEST_DROP_STAGE, 0)
+        bt.bt_set_option(bt.BT_OPT_WAIT_TIMEOUT_US, 4000000)
+    assert bt.bt_last_device_error() == bt.BT_OK
+    y = run(env, qw, x, "f16", "f32")
+    y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]))
+    assert_close(y, y_ref, a, "f32", "after timeout")

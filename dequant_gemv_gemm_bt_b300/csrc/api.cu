@@ -100,7 +100,20 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.const_weights = opts().pdl && opts().const_weights;
   p.drop_stage = opts().test_drop_stage;
   opts().test_drop_stage = 0;
-  const GemvPlan pl = plan_gemv(bits, N, K, problems, p.num_experts, sm_count());
+  const bool fast = xd == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !opts().gemv_generic;
+  const GemvPlan pl = plan_gemv(bits, fast, N, K, problems, p.num_experts, sm_count());
+  if (!pl.feasible) {
+    // no GEMV kernel holds this K slice in registers: the CUDA-core tile computes the same product
+    GemmParams g{};
+    g.codes = codes; g.scales = scales; g.biases = biases; g.x = x; g.y = y;
+    g.M = problems; g.N = N; g.K = K;
+    g.offsets = offsets;
+    g.row_index = row_index;
+    g.num_experts = num_experts;
+    g.err = p.err;
+    g.timeout_ns = p.timeout_ns;
+    return cuda_status(launch_gemm_simt(g, bits, xd, yd, stream));
+  }
   return cuda_status(launch_gemv(p, pl, bits, xd, yd, stream));
 }
 
@@ -133,6 +146,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_GENERIC: opts().gemv_generic = value != 0; return BT_OK;
     case BT_OPT_GEMV_STAGES: opts().gemv_stages = (int)value; return BT_OK;
     case BT_OPT_GEMM_PATH: opts().gemm_path = (int)value; return BT_OK;
+    case BT_OPT_GEMV_KERNEL: opts().gemv_kernel = (int)value; return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
 }

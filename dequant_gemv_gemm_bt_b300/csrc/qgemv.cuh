@@ -19,6 +19,7 @@ struct GemvParams {
   int rows_per_unit, row_bytes, stage_bytes, stages, kw, units_per_problem;
   long long num_units;
   // grouped experts (null offsets = dense)
+  bt_dtype y_dtype;
   const int32_t* moe_offsets;
   const int32_t* row_index;
   int num_experts;
@@ -31,12 +32,15 @@ struct GemvParams {
 };
 
 struct GemvPlan {
-  int kw, cpl, rows_per_unit, row_bytes, stage_bytes, stages, units_per_problem, grid;
+  bool fast;
+  bool reg;        // register-streaming kernel (no shared-memory ring)
+  bool feasible;   // false: no GEMV kernel fits this shape (the caller uses the CUDA-core tile)
+  int kw, cpl, ri, rows_per_unit, row_bytes, stage_bytes, stages, units_per_problem, grid;
   long long num_units;
   size_t smem;
 };
 
-GemvPlan plan_gemv(int bits, int N, int K, int problems, int num_experts, int sms);
+GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,
                         cudaStream_t stream);
 

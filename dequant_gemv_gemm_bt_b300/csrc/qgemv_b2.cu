@@ -1,0 +1,11 @@
+// Dequant-GEMV kernels for 2-bit codes (instantiations of qgemv_impl.cuh).
+#include "qgemv_impl.cuh"
+
+namespace bt {
+cudaError_t launch_gemv_b2(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
+  return gemv::launch_bits<2>(p, pl, xd, st);
+}
+cudaError_t launch_gemv_reg_b2(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
+  return gemv::launch_reg_bits<2>(p, pl, xd, st);
+}
+}  // namespace bt

@@ -1,0 +1,817 @@
+// Device code of the dequant-GEMV (M = 1, decode) and its batched form for
+// mixture-of-experts decode.  BaseRT pages, thetesserapress.com "BaseRT claims
+// fastest Apple Silicon inference", section "What BaseRT does differently": a
+// dedicated GEMV for M = 1 whose memory traffic scales with the compression
+// ratio because the weights are dequantized inside the compute loop.
+//
+// Design (B300):
+//  * Persistent CTAs, each streaming a contiguous range of row blocks ("units")
+//    through a shared-memory ring filled by 1-D bulk copies (TMA) issued by one
+//    producer thread; weights are read exactly once, with an L2 evict-first hint.
+//  * Each consumer lane owns a fixed K-slice of x in registers (loaded once per
+//    problem), so shared-memory traffic is only the packed codes and the fp16
+//    scale/bias of each row.
+//  * Per group the product is factored as s * sum(q*x) + b * sum(x); sum(x) per
+//    slice is precomputed, so the bias costs one FMA per 32 codes.
+//  * Fast path (fp16 x, bits 2/4/8): codes become fp16 "1024 + c*q" with one
+//    LOP3 / PRMT per two codes and are multiplied into fp32 accumulators with
+//    mixed-precision FMA (one instruction at FFMA rate on sm_103); the 1024
+//    offset is removed with a precomputed sum.  Generic path (bits 3/6, or bf16
+//    x): funnel-shift extraction, exact int->float via the 2^23 magic, fp32 FMA.
+//  * A warp works on RI rows at once (independent FMA chains), reduces the RI
+//    partials across lanes with a transpose-style shuffle tree (6 shuffles for
+//    4 rows) and, when one warp covers a whole row, stores y directly with no
+//    block-wide barrier.  When K is split over several warps the partials meet
+//    in shared memory behind a named barrier of that row group.  No atomics:
+//    results are bitwise deterministic.
+#pragma once
+#include "bt_common.cuh"
+#include "qgemv.cuh"
+
+namespace bt {
+
+namespace gemv {
+
+// ------------------------------------------------------------ shared loads
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+// Load the BITS words of one 32-code chunk (4*BITS bytes) from shared or global memory.
+template <int BITS, bool SMEM>
+__device__ __forceinline__ void load_chunk(uint32_t saddr, const uint8_t* gptr, uint32_t (&w)[BITS]) {
+  if constexpr (SMEM) {
+    if constexpr (BITS == 4) {
+      uint4 v = lds128(saddr); w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (BITS == 8) {
+      uint4 a = lds128(saddr), b = lds128(saddr + 16);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else if constexpr (BITS == 2) {
+      uint2 v = lds64(saddr); w[0] = v.x; w[1] = v.y;
+    } else if constexpr (BITS == 6) {
+#pragma unroll
+      for (int i = 0; i < 3; ++i) { uint2 v = lds64(saddr + 8 * i); w[2 * i] = v.x; w[2 * i + 1] = v.y; }
+    } else {
+#pragma unroll
+      for (int i = 0; i < BITS; ++i) w[i] = lds32(saddr + 4 * i);
+    }
+  } else {
+    if constexpr (BITS == 4) {
+      uint4 v = __ldg(reinterpret_cast<const uint4*>(gptr)); w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (BITS == 8) {
+      uint4 a = __ldg(reinterpret_cast<const uint4*>(gptr)), b = __ldg(reinterpret_cast<const uint4*>(gptr) + 1);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else if constexpr (BITS == 2 || BITS == 6) {
+#pragma unroll
+      for (int i = 0; i < BITS / 2; ++i) {
+        uint2 v = __ldg(reinterpret_cast<const uint2*>(gptr) + i); w[2 * i] = v.x; w[2 * i + 1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < BITS; ++i) w[i] = __ldg(reinterpret_cast<const uint32_t*>(gptr) + i);
+    }
+  }
+}
+
+// ------------------------------------------------------------ fast path math
+// acc_lo += x_lo * h.lo and acc_hi += x_hi * h.hi: fp16 operands, fp32
+// accumulation, two independent chains.  x values live one per register
+// (unpacked once when loaded), so only the code pair is split here.
+__device__ __forceinline__ void fma_lohi(float& acc_lo, float& acc_hi, uint16_t x_lo, uint16_t x_hi, uint32_t hp) {
+  asm("{\n .reg .f16 ha, hb;\n mov.b32 {ha, hb}, %4;\n"
+      " fma.rn.f32.f16 %0, %2, ha, %0;\n fma.rn.f32.f16 %1, %3, hb, %1;\n}\n"
+      : "+f"(acc_lo), "+f"(acc_hi) : "h"(x_lo), "h"(x_hi), "r"(hp));
+}
+
+__device__ __forceinline__ uint32_t lop_mask_or(uint32_t w, uint32_t mask) {
+  return (w & mask) | 0x64006400u;   // one LOP3
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Number of distinct "classes" (power-of-two multipliers c in 1024 + c*q) per bits.
+template <int BITS> struct FastClasses;
+template <> struct FastClasses<2> { static constexpr int n = 5; };
+template <> struct FastClasses<4> { static constexpr int n = 2; };
+template <> struct FastClasses<8> { static constexpr int n = 1; };
+
+// For each fp16x2 code pair of a word: the positions (within the word) of its
+// low-half and high-half codes, and its class.
+template <int BITS> struct FastLayout;
+
+// Q4: per word, pairs (q0,q4) c=1, (q1,q5) c=16, (q2,q6) c=1, (q3,q7) c=16.
+template <> struct FastLayout<4> {
+  static constexpr int pairs_per_word = 4;
+  __device__ static constexpr int pos(int pair, int half) { return pair + 4 * half; }
+  __device__ static constexpr int cls(int pair) { return (pair & 1) ? 1 : 0; }
+  __device__ static constexpr float mult(int c) { return c ? 16.f : 1.f; }
+};
+// Q2: per word, pairs (q_j, q_{j+8}) for j = 0..7; pairs 0..4 come from w with
+// classes 1,4,16,64,256 and pairs 5..7 from w >> 10 with classes 1,4,16.
+template <> struct FastLayout<2> {
+  static constexpr int pairs_per_word = 8;
+  __device__ static constexpr int pos(int pair, int half) { return pair + 8 * half; }
+  __device__ static constexpr int cls(int pair) { return pair < 5 ? pair : pair - 5; }
+  __device__ static constexpr float mult(int c) {
+    return c == 0 ? 1.f : c == 1 ? 4.f : c == 2 ? 16.f : c == 3 ? 64.f : 256.f;
+  }
+};
+// Q8: per word, pairs (q0,q1) and (q2,q3), class 1.
+template <> struct FastLayout<8> {
+  static constexpr int pairs_per_word = 2;
+  __device__ static constexpr int pos(int pair, int half) { return 2 * pair + half; }
+  __device__ static constexpr int cls(int) { return 0; }
+  __device__ static constexpr float mult(int) { return 1.f; }
+};
+
+// One word's code pairs as fp16x2 "1024 + c*q" values.
+template <int BITS>
+__device__ __forceinline__ void fast_pairs(uint32_t w, uint32_t (&h)[FastLayout<BITS>::pairs_per_word]) {
+  if constexpr (BITS == 4) {
+    const uint32_t w8 = w >> 8;
+    h[0] = lop_mask_or(w, 0x000F000Fu);
+    h[1] = lop_mask_or(w, 0x00F000F0u);
+    h[2] = lop_mask_or(w8, 0x000F000Fu);
+    h[3] = lop_mask_or(w8, 0x00F000F0u);
+  } else if constexpr (BITS == 2) {
+    const uint32_t w10 = w >> 10;
+    h[0] = lop_mask_or(w, 0x00030003u);
+    h[1] = lop_mask_or(w, 0x000C000Cu);
+    h[2] = lop_mask_or(w, 0x00300030u);
+    h[3] = lop_mask_or(w, 0x00C000C0u);
+    h[4] = lop_mask_or(w, 0x03000300u);
+    h[5] = lop_mask_or(w10, 0x00030003u);
+    h[6] = lop_mask_or(w10, 0x000C000Cu);
+    h[7] = lop_mask_or(w10, 0x00300030u);
+  } else {
+    h[0] = prmt(w, 0x64646464u, 0x4140u);
+    h[1] = prmt(w, 0x64646464u, 0x4342u);
+  }
+}
+
+// ------------------------------------------------------------ x slices
+// Per chunk a lane keeps: the x values (layout depends on the path), sum(x)
+// over the chunk (for the bias term) and, on the fast path, the offset sum
+// Z = sum_j 1024 * x_j / c_j that removes the fp16 magic.
+template <int BITS, bool FAST> struct XSlice;
+
+template <int BITS> struct XSlice<BITS, true> {
+  uint16_t xh[32];   // fp16 x values of the chunk, one per register
+  float xsum, z;
+};
+template <int BITS> struct XSlice<BITS, false> {
+  float xv[32];
+  float xsum;
+};
+
+template <int BITS, bt_dtype XD>
+__device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_t* xk) {
+  // xk: 32 consecutive x values (16-B aligned) of this chunk
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 q = __ldg(reinterpret_cast<const uint4*>(xk) + i);
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      s.xh[8 * i + 2 * j] = u[j] & 0xFFFF;
+      s.xh[8 * i + 2 * j + 1] = u[j] >> 16;
+    }
+  }
+  using L = FastLayout<BITS>;
+  constexpr int codes_per_word = 32 / BITS;
+  float xsum = 0.f, z = 0.f;
+#pragma unroll
+  for (int wd = 0; wd < BITS; ++wd) {
+#pragma unroll
+    for (int p = 0; p < L::pairs_per_word; ++p) {
+      const float x0 = __half2float(__ushort_as_half(s.xh[wd * codes_per_word + L::pos(p, 0)]));
+      const float x1 = __half2float(__ushort_as_half(s.xh[wd * codes_per_word + L::pos(p, 1)]));
+      xsum += x0 + x1;
+      z += (x0 + x1) * (1024.f / L::mult(L::cls(p)));
+    }
+  }
+  s.xsum = xsum;
+  s.z = z;
+}
+
+template <int BITS, bt_dtype XD>
+__device__ __forceinline__ void load_x_generic(XSlice<BITS, false>& s, const uint16_t* xk) {
+  float xsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 q = __ldg(reinterpret_cast<const uint4*>(xk) + i);
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      s.xv[8 * i + 2 * j] = to_f32<XD>(u[j] & 0xFFFF);
+      s.xv[8 * i + 2 * j + 1] = to_f32<XD>(u[j] >> 16);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) xsum += s.xv[j];
+  s.xsum = xsum;
+}
+
+// sum_j q_j * x_j over one chunk (fast path).
+template <int BITS>
+__device__ __forceinline__ float chunk_dot_fast(const uint32_t (&w)[BITS], const XSlice<BITS, true>& s) {
+  using L = FastLayout<BITS>;
+  constexpr int NC = FastClasses<BITS>::n;
+  constexpr int codes_per_word = 32 / BITS;
+  float acc[NC][2];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c][0] = acc[c][1] = 0.f;
+#pragma unroll
+  for (int wd = 0; wd < BITS; ++wd) {
+    uint32_t h[L::pairs_per_word];
+    fast_pairs<BITS>(w[wd], h);
+#pragma unroll
+    for (int p = 0; p < L::pairs_per_word; ++p)
+      fma_lohi(acc[L::cls(p)][0], acc[L::cls(p)][1], s.xh[wd * codes_per_word + L::pos(p, 0)],
+               s.xh[wd * codes_per_word + L::pos(p, 1)], h[p]);
+  }
+  float t = acc[0][0] + acc[0][1];
+#pragma unroll
+  for (int c = 1; c < NC; ++c) t = fmaf(acc[c][0] + acc[c][1], 1.f / L::mult(c), t);
+  return t - s.z;
+}
+
+// sum_j q_j * x_j over one chunk (generic path, any bits).
+template <int BITS>
+__device__ __forceinline__ float chunk_dot_generic(const uint32_t (&w)[BITS], const XSlice<BITS, false>& s) {
+  constexpr uint32_t mask = (1u << BITS) - 1u;
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int bit = j * BITS, wi = bit >> 5, off = bit & 31;
+    uint32_t q;
+    if (off + BITS <= 32) q = (w[wi] >> off) & mask;
+    else q = __funnelshift_r(w[wi], w[wi + 1], off) & mask;
+    const float qf = __uint_as_float(0x4B000000u | q) - 8388608.f;
+    if (j & 1) acc1 = fmaf(s.xv[j], qf, acc1);
+    else acc0 = fmaf(s.xv[j], qf, acc0);
+  }
+  return acc0 + acc1;
+}
+
+// ------------------------------------------------------- problem -> expert / rows
+// Grouped row `prob` belongs to the expert e with off[e] <= prob < off[e+1]
+// (offsets cached in shared memory); -1 when no expert holds it.
+__device__ __forceinline__ int problem_expert(const GemvParams& p, const int* offs, int prob) {
+  if (!p.moe_offsets) return 0;
+  int lo = 0, hi = p.num_experts;   // invariant: offs[lo] <= prob, answer in [lo, hi)
+  if (prob < offs[0] || prob >= offs[p.num_experts]) return -1;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offs[mid] <= prob) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+__device__ __forceinline__ int problem_xrow(const GemvParams& p, int prob) {
+  if (!p.moe_offsets) return 0;
+  return p.row_index ? __ldg(p.row_index + prob) : prob;
+}
+__device__ __forceinline__ int problem_yrow(const GemvParams& p, int prob) { return p.moe_offsets ? prob : 0; }
+
+// A unit's rows are staged by bulk copies only when every copy starts on a
+// 16-byte boundary and moves a multiple of 16 bytes; otherwise the consumers
+// read that unit straight from global memory.
+__device__ __forceinline__ bool unit_uses_bulk(const GemvParams& p, size_t wrow, int rows) {
+  const size_t c0 = wrow * (size_t)p.row_bytes, s0 = wrow * (size_t)p.G * 2;
+  const size_t cb = (size_t)rows * p.row_bytes, sb = (size_t)rows * p.G * 2;
+  return ((c0 | s0 | cb | sb) & 15u) == 0;
+}
+
+// --------------------------------------------------------------- the kernel
+// Consumer warps per CTA: 8, which leaves each thread up to 168 registers so
+// the fp16 x values stay one per register (a tighter cap makes the compiler
+// pack them in pairs and pay an extract per FMA).  One more warp is the producer.
+template <int CPL> struct Warps {
+  static constexpr int kNW = 8;
+  static constexpr int kThreads = (kNW + 1) * 32;
+};
+
+// Sum RI per-row partials over the 32 lanes with a transpose-style tree.  On
+// return, `row` is the row in [0, RI) whose full sum this lane holds; lanes
+// with (lane & (32/RI - 1)) == 0 are the first holder of each row.
+template <int RI>
+__device__ __forceinline__ float reduce_rows(const float (&part)[RI], int lane, int& row) {
+  if constexpr (RI == 4) {
+    const bool hi = lane & 16;
+    float a0 = hi ? part[2] : part[0], a1 = hi ? part[3] : part[1];
+    const float b0 = hi ? part[0] : part[2], b1 = hi ? part[1] : part[3];
+    a0 += __shfl_xor_sync(0xffffffffu, b0, 16);
+    a1 += __shfl_xor_sync(0xffffffffu, b1, 16);
+    const bool m = lane & 8;
+    float c = m ? a1 : a0;
+    const float d = m ? a0 : a1;
+    c += __shfl_xor_sync(0xffffffffu, d, 8);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    row = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+    return c;
+  } else if constexpr (RI == 2) {
+    const bool hi = lane & 16;
+    float a = hi ? part[1] : part[0];
+    const float b = hi ? part[0] : part[1];
+    a += __shfl_xor_sync(0xffffffffu, b, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    row = (lane >> 4) & 1;
+    return a;
+  } else {
+    float a = part[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    row = 0;
+    return a;
+  }
+}
+
+__device__ __forceinline__ void store_y(const GemvParams& p, size_t i, float v) {
+  if (p.y_dtype == BT_F32) store_out<BT_F32>(p.y, i, v);
+  else if (p.y_dtype == BT_BF16) store_out<BT_BF16>(p.y, i, v);
+  else store_out<BT_F16>(p.y, i, v);
+}
+
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
+__global__ void __launch_bounds__(Warps<CPL>::kThreads, 1) qgemv_kernel(const GemvParams p) {
+  constexpr int kNW = Warps<CPL>::kNW;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
+  uint64_t* empty = full + S;
+  float* red = reinterpret_cast<float*>(empty + S);        // [kNW/KW][2][RI][KW] = kNW*2*RI floats
+  int* offs = reinterpret_cast<int*>(red + kNW * 2 * RI);  // [E+1] when grouped
+
+  // contiguous range of units for this CTA
+  const long long U = p.num_units;
+  const long long u_begin = U * blockIdx.x / gridDim.x;
+  const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
+
+  // full[s]: one arrive.expect_tx for the bulk copy of the codes plus one
+  // cp.async-tracked arrive from each producer lane (scales and biases).
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 33); mbar_init(&empty[s], kNW); }
+    fence_mbar_init();
+  }
+  if (p.moe_offsets) {
+    pdl_wait();   // offsets come from the routing kernel
+    for (int i = threadIdx.x; i <= p.num_experts; i += blockDim.x) offs[i] = __ldg(p.moe_offsets + i);
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  const int RB = p.rows_per_unit;
+  const int row_bytes = p.row_bytes;
+  const int G = p.G;
+
+  if (warp == kNW) {
+    // ------------------------------------------------------------ producer
+    // Lane 0 moves a unit's packed codes with one bulk copy (large copies keep
+    // the copy engine streaming); all 32 lanes move its fp16 scales and biases
+    // with 16-byte cp.async, whose completion the same mbarrier tracks.
+    if (!p.const_weights) pdl_wait();
+    const uint64_t pol = l2_policy_evict_first();
+    // unit u = prob * units_per_problem + blk; stage s = it % S, phase = (it / S) & 1,
+    // all advanced incrementally (no divisions in the loop)
+    int prob = (int)(u_begin / p.units_per_problem);
+    int blk = (int)(u_begin - (long long)prob * p.units_per_problem);
+    int s = 0;
+    uint32_t ph = 0;
+    long long it = 0;
+    bool ok = true;
+    for (long long u = u_begin; u < u_end; ++u, ++it) {
+      if (it >= S) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
+        if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; break; }
+      }
+      const int row0 = blk * RB;
+      const int rows = min(RB, p.N - row0);
+      const int e = problem_expert(p, offs, prob);
+      const uint32_t cbytes = (uint32_t)rows * row_bytes, sbytes = (uint32_t)rows * G * 2;
+      const size_t wrow = (size_t)(e < 0 ? 0 : e) * p.N + row0;
+      const bool tma = unit_uses_bulk(p, wrow, rows);
+      if (p.drop_stage && blockIdx.x == 0 && it == 0) {   // test hook: never fill this stage
+        if (++blk == p.units_per_problem) { blk = 0; ++prob; }
+        if (++s == S) { s = 0; ph ^= 1u; }
+        continue;
+      }
+      if (tma && e >= 0) {
+        uint8_t* st = smem + (size_t)s * p.stage_bytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], cbytes);
+          bulk_g2s(st, reinterpret_cast<const uint8_t*>(p.codes) + wrow * row_bytes, cbytes, &full[s], pol);
+        }
+        const uint8_t* gs = reinterpret_cast<const uint8_t*>(p.scales + wrow * G);
+        const uint8_t* gb = reinterpret_cast<const uint8_t*>(p.biases + wrow * G);
+        uint8_t* ss = st + (size_t)RB * row_bytes;
+        uint8_t* sbb = ss + (size_t)RB * G * 2;
+        for (uint32_t o = lane * 16u; o < sbytes; o += 32u * 16u) {
+          cp_async16(ss + o, gs + o);
+          cp_async16(sbb + o, gb + o);
+        }
+        cp_async_mbar_arrive_noinc(&full[s]);
+      } else {
+        mbar_arrive(&full[s]);
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+      if (++blk == p.units_per_problem) { blk = 0; ++prob; }
+      if (++s == S) { s = 0; ph ^= 1u; }
+    }
+    if (!ok) {
+      // drain copies still in flight before this CTA's shared memory goes away
+      cp_async_wait_all();
+      if (lane == 0) {
+        const long long issued = it;
+        for (long long j = (issued > S ? issued - S : 0); j < issued; ++j)   // failure path only
+          mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), p.timeout_ns, p.err);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int KW = p.kw;
+  const int RW = kNW / KW;
+  if (KW < 1 || RW < 1 || RW * KW != kNW) {   // never launched so by the planner; refuse rather than spin
+    if (threadIdx.x == 0) set_device_error(p.err, kErrBadArg);
+    return;
+  }
+  const int kw = warp % KW, rg = warp / KW;
+  const int nchunks = p.K / 32;
+  const bool writer = (lane & (32 / RI - 1)) == 0;
+  pdl_wait();   // activations (and offsets) may come from the previous kernel
+
+  XSlice<BITS, FAST> xs[CPL];
+  int cur_prob = -1;
+  int cur_expert = -1;
+  int rbuf = 0;
+  int prob = (int)(u_begin / p.units_per_problem);
+  int blk = (int)(u_begin - (long long)prob * p.units_per_problem);
+  int s = 0;
+  uint32_t ph = 0;
+  for (long long u = u_begin; u < u_end; ++u) {
+    if (prob != cur_prob) {
+      cur_prob = prob;
+      cur_expert = problem_expert(p, offs, prob);
+      const int xrow = problem_xrow(p, prob);
+      const uint16_t* xb = static_cast<const uint16_t*>(p.x) + (size_t)xrow * p.K;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = (i * KW + kw) * 32 + lane;
+        if (c < nchunks) {
+          if constexpr (FAST) load_x_fast<BITS, XD>(xs[i], xb + (size_t)c * 32);
+          else load_x_generic<BITS, XD>(xs[i], xb + (size_t)c * 32);
+        }
+      }
+    }
+    if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) return;
+    const int row0 = blk * RB;
+    const int rows = min(RB, p.N - row0);
+    const size_t wrow = (size_t)(cur_expert < 0 ? 0 : cur_expert) * p.N + row0;
+    const bool tma = unit_uses_bulk(p, wrow, rows) && cur_expert >= 0;
+    const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
+    const uint32_t st_sc = st + RB * row_bytes, st_bi = st_sc + RB * G * 2;
+    const uint8_t* g_codes = reinterpret_cast<const uint8_t*>(p.codes) + wrow * row_bytes;
+    const uint16_t* g_sc = p.scales + wrow * G;
+    const uint16_t* g_bi = p.biases + wrow * G;
+    const size_t ybase = (size_t)problem_yrow(p, prob) * p.N + row0;
+
+    const int nb = (rows + RI - 1) / RI;
+    for (int bi = rg; bi < nb; bi += RW) {
+      const int r0 = bi * RI;
+      float part[RI];
+#pragma unroll
+      for (int j = 0; j < RI; ++j) part[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = (i * KW + kw) * 32 + lane;
+        if (c < nchunks) {
+          uint32_t w[RI][BITS];
+          float sc[RI], bs[RI];
+#pragma unroll
+          for (int j = 0; j < RI; ++j) {
+            const int r = min(r0 + j, rows - 1);
+            if (tma) {
+              load_chunk<BITS, true>(st + r * row_bytes + c * (4 * BITS), nullptr, w[j]);
+              sc[j] = to_f32<BT_F16>(lds16(st_sc + (r * G + (c >> 1)) * 2));
+              bs[j] = to_f32<BT_F16>(lds16(st_bi + (r * G + (c >> 1)) * 2));
+            } else {
+              load_chunk<BITS, false>(0, g_codes + (size_t)r * row_bytes + c * (4 * BITS), w[j]);
+              sc[j] = to_f32<BT_F16>(__ldg(g_sc + (size_t)r * G + (c >> 1)));
+              bs[j] = to_f32<BT_F16>(__ldg(g_bi + (size_t)r * G + (c >> 1)));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < RI; ++j) {
+            float t;
+            if constexpr (FAST) t = chunk_dot_fast<BITS>(w[j], xs[i]);
+            else t = chunk_dot_generic<BITS>(w[j], xs[i]);
+            part[j] = fmaf(sc[j], t, fmaf(bs[j], xs[i].xsum, part[j]));
+          }
+        }
+      }
+      int rj;
+      const float v = reduce_rows<RI>(part, lane, rj);
+      const int r = r0 + rj;
+      if (KW == 1) {
+        if (writer && r < rows && cur_expert >= 0) store_y(p, ybase + r, v);
+      } else {
+        float* rb = red + (size_t)((rg * 2 + rbuf) * RI) * KW;   // [RI][KW]
+        if (writer) rb[rj * KW + kw] = v;
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
+        if (kw == 0 && writer && r < rows && cur_expert >= 0) {
+          float acc = 0.f;
+          for (int j = 0; j < KW; ++j) acc += rb[rj * KW + j];
+          store_y(p, ybase + r, acc);
+        }
+        rbuf ^= 1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++blk == p.units_per_problem) { blk = 0; ++prob; }
+    if (++s == S) { s = 0; ph ^= 1u; }
+  }
+}
+
+// ------------------------------------------------------------------ launch
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
+cudaError_t launch_t(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
+  auto k = qgemv_kernel<BITS, XD, CPL, FAST, RI>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Warps<CPL>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+template <int BITS, bt_dtype XD, int CPL, bool FAST>
+cudaError_t launch_ri(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
+  switch (pl.ri) {
+    case 4: return launch_t<BITS, XD, CPL, FAST, 4>(p, pl.grid, pl.smem, st);
+    case 2: return launch_t<BITS, XD, CPL, FAST, 2>(p, pl.grid, pl.smem, st);
+    default: return launch_t<BITS, XD, CPL, FAST, 1>(p, pl.grid, pl.smem, st);
+  }
+}
+
+template <int BITS, bt_dtype XD, bool FAST>
+cudaError_t launch_cpl(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
+  switch (pl.cpl) {
+    case 1: return launch_ri<BITS, XD, 1, FAST>(p, pl, st);
+    case 2: return launch_ri<BITS, XD, 2, FAST>(p, pl, st);
+    case 3: if constexpr (FAST) return launch_ri<BITS, XD, 3, FAST>(p, pl, st); else break;
+    case 4: if constexpr (FAST) return launch_ri<BITS, XD, 4, FAST>(p, pl, st); else break;
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int BITS>
+cudaError_t launch_bits(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
+  constexpr bool kFastBits = (BITS == 2 || BITS == 4 || BITS == 8);
+  if (xd == BT_F16) {
+    if constexpr (kFastBits) {
+      if (pl.fast) return launch_cpl<BITS, BT_F16, true>(p, pl, st);
+    }
+    return launch_cpl<BITS, BT_F16, false>(p, pl, st);
+  }
+  return launch_cpl<BITS, BT_BF16, false>(p, pl, st);
+}
+
+}  // namespace gemv
+}  // namespace bt
+
+namespace bt {
+namespace gemv {
+
+// ---------------------------------------------------------------------------
+// Register-streaming variant: no shared-memory ring and no barriers on the
+// main path.  Each warp walks its rows in batches of RI; the packed codes and
+// the fp16 scale/bias of batch i+1 are loaded with 128-bit / 16-bit global
+// loads while batch i is being multiplied, so two batches of loads are in
+// flight per warp.
+template <int CPL> struct WarpsR {
+  static constexpr int kNW = 16;
+  static constexpr int kThreads = kNW * 32;
+};
+
+template <int BITS, bool FAST, int RI, int CPL>
+struct BatchRegs {
+  uint32_t w[CPL][RI][BITS];
+  uint16_t s[CPL][RI], b[CPL][RI];
+};
+
+template <int BITS, int RI, int CPL>
+__device__ __forceinline__ void load_batch(const GemvParams& p, const uint8_t* codes_row0, const uint16_t* sc_row0,
+                                           const uint16_t* bi_row0, int r0, int rows, int kw, int KW, int lane,
+                                           int nchunks, uint32_t (&w)[CPL][RI][BITS], uint16_t (&s)[CPL][RI],
+                                           uint16_t (&b)[CPL][RI]) {
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = (i * KW + kw) * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < RI; ++j) {
+      const int r = min(r0 + j, rows - 1);
+      if (c < nchunks && r >= 0) {
+        load_chunk<BITS, false>(0, codes_row0 + (size_t)r * p.row_bytes + c * (4 * BITS), w[i][j]);
+        s[i][j] = __ldg(sc_row0 + (size_t)r * p.G + (c >> 1));
+        b[i][j] = __ldg(bi_row0 + (size_t)r * p.G + (c >> 1));
+      }
+    }
+  }
+}
+
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
+__global__ void __launch_bounds__(WarpsR<CPL>::kThreads, 1) qgemv_reg_kernel(const GemvParams p) {
+  constexpr int kNW = WarpsR<CPL>::kNW;
+  __shared__ float red[kNW * 2 * RI];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KW = p.kw;
+  const int RW = kNW / KW;
+  if (KW < 1 || RW < 1 || RW * KW != kNW) {
+    if (threadIdx.x == 0) set_device_error(p.err, kErrBadArg);
+    return;
+  }
+  const int kw = warp % KW, rg = warp / KW;
+  const int nchunks = p.K / 32;
+  const bool writer = (lane & (32 / RI - 1)) == 0;
+  extern __shared__ int offs_dyn[];   // [E+1] when grouped
+  pdl_launch_dependents();
+  pdl_wait();
+  if (p.moe_offsets) {
+    for (int i = threadIdx.x; i <= p.num_experts; i += blockDim.x) offs_dyn[i] = __ldg(p.moe_offsets + i);
+    __syncthreads();
+  }
+
+  const long long U = p.num_units;
+  const long long u_begin = U * blockIdx.x / gridDim.x;
+  const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
+  const int RB = p.rows_per_unit;
+
+  XSlice<BITS, FAST> xs[CPL];
+  int cur_prob = -1, cur_expert = -1;
+  int rbuf = 0;
+  int prob = (int)(u_begin / p.units_per_problem);
+  int blk = (int)(u_begin - (long long)prob * p.units_per_problem) - 1;
+  for (long long u = u_begin; u < u_end; ++u) {
+    if (++blk == p.units_per_problem) { blk = 0; ++prob; }
+    if (prob != cur_prob) {
+      cur_prob = prob;
+      cur_expert = problem_expert(p, offs_dyn, prob);
+      const uint16_t* xb = static_cast<const uint16_t*>(p.x) + (size_t)problem_xrow(p, prob) * p.K;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = (i * KW + kw) * 32 + lane;
+        if (c < nchunks) {
+          if constexpr (FAST) load_x_fast<BITS, XD>(xs[i], xb + (size_t)c * 32);
+          else load_x_generic<BITS, XD>(xs[i], xb + (size_t)c * 32);
+        }
+      }
+    }
+    if (cur_expert < 0) continue;
+    const int row0 = blk * RB;
+    const int rows = min(RB, p.N - row0);
+    const size_t wrow = (size_t)cur_expert * p.N + row0;
+    const uint8_t* g_codes = reinterpret_cast<const uint8_t*>(p.codes) + wrow * p.row_bytes;
+    const uint16_t* g_sc = p.scales + wrow * p.G;
+    const uint16_t* g_bi = p.biases + wrow * p.G;
+    const size_t ybase = (size_t)problem_yrow(p, prob) * p.N + row0;
+    const int nb = (rows + RI - 1) / RI;
+
+    uint32_t wA[CPL][RI][BITS], wB[CPL][RI][BITS];
+    uint16_t sA[CPL][RI], bA[CPL][RI], sB[CPL][RI], bB[CPL][RI];
+    int bi = rg;
+    if (bi < nb) load_batch<BITS, RI, CPL>(p, g_codes, g_sc, g_bi, bi * RI, rows, kw, KW, lane, nchunks, wA, sA, bA);
+    while (bi < nb) {
+      const int nbi = bi + RW;
+      if (nbi < nb) load_batch<BITS, RI, CPL>(p, g_codes, g_sc, g_bi, nbi * RI, rows, kw, KW, lane, nchunks, wB, sB, bB);
+      float part[RI];
+#pragma unroll
+      for (int j = 0; j < RI; ++j) part[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = (i * KW + kw) * 32 + lane;
+        if (c < nchunks) {
+#pragma unroll
+          for (int j = 0; j < RI; ++j) {
+            float t;
+            if constexpr (FAST) t = chunk_dot_fast<BITS>(wA[i][j], xs[i]);
+            else t = chunk_dot_generic<BITS>(wA[i][j], xs[i]);
+            part[j] = fmaf(to_f32<BT_F16>(sA[i][j]), t, fmaf(to_f32<BT_F16>(bA[i][j]), xs[i].xsum, part[j]));
+          }
+        }
+      }
+      int rj;
+      const float v = reduce_rows<RI>(part, lane, rj);
+      const int r = bi * RI + rj;
+      if (KW == 1) {
+        if (writer && r < rows) store_y(p, ybase + r, v);
+      } else {
+        float* rb = red + (size_t)((rg * 2 + rbuf) * RI) * KW;
+        if (writer) rb[rj * KW + kw] = v;
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
+        if (kw == 0 && writer && r < rows) {
+          float acc = 0.f;
+          for (int j = 0; j < KW; ++j) acc += rb[rj * KW + j];
+          store_y(p, ybase + r, acc);
+        }
+        rbuf ^= 1;
+      }
+      // rotate the double buffer
+#pragma unroll
+      for (int i = 0; i < CPL; ++i)
+#pragma unroll
+        for (int j = 0; j < RI; ++j) {
+#pragma unroll
+          for (int t = 0; t < BITS; ++t) wA[i][j][t] = wB[i][j][t];
+          sA[i][j] = sB[i][j];
+          bA[i][j] = bB[i][j];
+        }
+      bi = nbi;
+    }
+  }
+}
+
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
+cudaError_t launch_reg_t(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
+  auto k = qgemv_reg_kernel<BITS, XD, CPL, FAST, RI>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(WarpsR<CPL>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+template <int BITS, bt_dtype XD, int CPL, bool FAST>
+cudaError_t launch_reg_ri(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
+  switch (pl.ri) {
+    case 4: return launch_reg_t<BITS, XD, CPL, FAST, 4>(p, pl.grid, pl.smem, st);
+    case 2: return launch_reg_t<BITS, XD, CPL, FAST, 2>(p, pl.grid, pl.smem, st);
+    default: return launch_reg_t<BITS, XD, CPL, FAST, 1>(p, pl.grid, pl.smem, st);
+  }
+}
+
+template <int BITS, bt_dtype XD, bool FAST>
+cudaError_t launch_reg_cpl(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
+  switch (pl.cpl) {
+    case 1: return launch_reg_ri<BITS, XD, 1, FAST>(p, pl, st);
+    case 2: return launch_reg_ri<BITS, XD, 2, FAST>(p, pl, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int BITS>
+cudaError_t launch_reg_bits(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
+  constexpr bool kFastBits = (BITS == 2 || BITS == 4 || BITS == 8);
+  if (xd == BT_F16) {
+    if constexpr (kFastBits) {
+      if (pl.fast) return launch_reg_cpl<BITS, BT_F16, true>(p, pl, st);
+    }
+    return launch_reg_cpl<BITS, BT_F16, false>(p, pl, st);
+  }
+  return launch_reg_cpl<BITS, BT_BF16, false>(p, pl, st);
+}
+
+}  // namespace gemv
+}  // namespace bt

@@ -186,6 +186,7 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMV_STAGES   tuning: GEMV pipeline depth (0 = heuristic, else 2..8).
  *   BT_OPT_GEMM_PATH     tuning: 0 = heuristic, 1 = CUDA-core tile,
  *                       2 = tensor-core tile where supported.
+ *   BT_OPT_GEMV_KERNEL   tuning: 0 = shared-memory ring GEMV, 1 = register-streaming GEMV.
  */
 typedef enum {
   BT_OPT_PDL = 0,
@@ -194,7 +195,8 @@ typedef enum {
   BT_OPT_TEST_DROP_STAGE = 3,
   BT_OPT_GEMV_GENERIC = 4,
   BT_OPT_GEMV_STAGES = 5,
-  BT_OPT_GEMM_PATH = 6
+  BT_OPT_GEMM_PATH = 6,
+  BT_OPT_GEMV_KERNEL = 7
 } bt_option;
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);

@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark of the affine group-quantized GEMV / GEMM hot path on B300.
+
+Default workload (one "step"): a Qwen3-0.6B-shaped Q4 (group 64) decode pass
+at M = 1 -- 28 layers of q 1024->2048, k/v 1024->1024, o 2048->1024, gate/up
+1024->3072, down 3072->1024, each with its own weights and its own fp16 x,
+plus an lm_head 1024->151936: 197 dequant-GEMVs, 335,241,216 bytes of packed
+codes + fp16 scales/biases, captured as one CUDA graph of libbt launches.
+Weights are synthetic (seeded N(0, 0.02), min/max-quantized); they exceed the
+126 MB L2, so no flush is needed between steps.
+
+Metric: weight GB/s (codes + scales + biases per pass / pass time), the
+BaseRT pages' decode-bandwidth view ("memory traffic scales with the
+compression ratio").  With --prefill, the Llama-3.2-3B-shaped prefill GEMM
+pass (M = 128 and 512) is also timed and reported in TFLOP/s.
+
+``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
+workload (the only other code path of this workload).  Under torchrun each
+rank runs an independent replica (the path does not shard); rank 0 prints one
+JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dequant_gemv_gemm_bt_b300 import synth  # noqa: E402
+
+METRIC = "Q4 dequant-GEMV decode weight GB/s vs HBM peak; prefill qGEMM TFLOP/s"
+GROUP = 64
+
+# Qwen3-0.6B-shaped decode pass: (N, K) per projection in a layer, 28 layers, + lm_head.
+QWEN06_LAYER = [("q", 2048, 1024), ("k", 1024, 1024), ("v", 1024, 1024), ("o", 1024, 2048),
+                ("gate", 3072, 1024), ("up", 3072, 1024), ("down", 1024, 3072)]
+QWEN06_LAYERS = 28
+QWEN06_LM_HEAD = ("lm_head", 151936, 1024)
+# Llama-3.2-3B-shaped prefill pass.
+LLAMA3B_LAYER = [("q", 3072, 3072), ("k", 1024, 3072), ("v", 1024, 3072), ("o", 3072, 3072),
+                 ("gate", 8192, 3072), ("up", 8192, 3072), ("down", 3072, 8192)]
+LLAMA3B_LAYERS = 28
+
+
+def weight_bytes(n: int, k: int, bits: int) -> int:
+    return n * k * bits // 8 + 4 * n * (k // GROUP)
+
+
+def decode_pass_shapes():
+    shapes = []
+    for layer in range(QWEN06_LAYERS):
+        for name, n, k in QWEN06_LAYER:
+            shapes.append((f"L{layer}.{name}", n, k))
+    shapes.append(QWEN06_LM_HEAD)
+    return shapes
+
+
+def prefill_pass_shapes():
+    return [(f"L{l}.{name}", n, k) for l in range(LLAMA3B_LAYERS) for name, n, k in LLAMA3B_LAYER]
+
+
+def gen_weights(tag, shapes, bits, threads=16):
+    """Seeded packed weights for every (name, N, K), generated on host threads."""
+    import concurrent.futures as cf
+
+    def one(item):
+        name, n, k = item
+        return synth.make_qweight(synth.rng_for(tag, name, "w"), n, k, bits)
+    with cf.ThreadPoolExecutor(threads) as ex:
+        return list(ex.map(one, shapes))
+
+
+def gen_x(tag, shapes, m, dtype):
+    return [synth.draw_activations(synth.rng_for(tag, name, "x"), m, k, dtype) for name, n, k in shapes]
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def source_digest(patterns):
+    h = hashlib.sha256()
+    for pat in patterns:
+        for f in sorted(glob.glob(os.path.join(ROOT, pat))):
+            h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(summary_file, digest):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", summary_file)
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", txt)
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_d or not m_t or m_d.group(1) != digest:
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", str(self.gpu),
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.06)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max([d.get("num_threads", 1) for d in info if d.get("user_api") == "blas"] or [1])
+    except Exception:
+        return 1
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_rate(weights, xs16, budget_s: float, start: int = 0):
+    """fp64 oracle on whole projections, in pass order from `start`, for about `budget_s`.
+
+    Returns (GB/s of weight bytes, bytes processed, projections done).
+    """
+    import oracle.bt_oracle as O
+    t0 = time.perf_counter()
+    done_bytes = 0
+    count = 0
+    i = start
+    while True:
+        qw = weights[i % len(weights)]
+        x = O.decode_f16(xs16[i % len(weights)][0])
+        rows = None
+        if qw.n > 16384:   # huge projections: a bounded slice of rows
+            rows = np.arange(0, 16384)
+        O.qgemv(qw.codes, qw.scales, qw.biases, qw.bits, x, rows=rows)
+        n_rows = qw.n if rows is None else len(rows)
+        done_bytes += weight_bytes(n_rows, qw.k, qw.bits)
+        count += 1
+        i += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done_bytes / el / 1e9, done_bytes, count
+
+
+# ------------------------------------------------------------------ GPU legs
+def build_decode_pass(torch, bt, weights, xs16, dev):
+    bufs = []
+    for qw, x16 in zip(weights, xs16):
+        c = torch.from_numpy(qw.codes.view(np.int32)).to(dev)
+        s = torch.from_numpy(qw.scales.view(np.float16)).to(dev)
+        b = torch.from_numpy(qw.biases.view(np.float16)).to(dev)
+        x = torch.from_numpy(x16[0].view(np.int16)).to(dev).view(torch.float16)
+        y = torch.empty(qw.n, dtype=torch.float32, device=dev)
+        bufs.append((c, s, b, x, y, qw.bits))
+    return bufs
+
+
+def capture(torch, fn, stream):
+    with torch.cuda.stream(stream):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def timed(torch, dist, stream, fn, steps, warmup, gpu_index):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index) as clk:
+        ev0.record(stream)
+        for _ in range(steps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    return ms / 1e3, clk.summary()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    shapes = decode_pass_shapes()
+    bits = 4
+    pass_bytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
+    config = {"workload": "Qwen3-0.6B-shaped decode pass, M=1: 28 layers x 7 projections + lm_head 1024->151936",
+              "bits": bits, "group_size": GROUP, "gemvs_per_pass": len(shapes), "weight_bytes_per_pass": pass_bytes,
+              "x_dtype": "f16", "y_dtype": "f32",
+              "l2": "inputs exceed L2 (335 MB of packed weights per pass vs 126 MB L2); no flush",
+              "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        weights = gen_weights("decode-pass", shapes, bits)
+        xs16 = gen_x("decode-pass", shapes, 1, "f16")
+        # each step: the oracle on a bounded sample so the whole run stays within ~2 minutes
+        per_step = max(0.005, min(2.0, 90.0 / (args.steps + args.warmup)))
+        for i in range(args.warmup):
+            oracle_rate(weights, xs16, per_step, start=i)
+        t0 = time.perf_counter()
+        tot = 0
+        done = 0
+        for i in range(args.steps):
+            _, b, c = oracle_rate(weights, xs16, per_step, start=args.warmup + i)
+            tot += b
+            done += c
+        el = time.perf_counter() - t0
+        val = tot / el / 1e9
+        threads = blas_threads()
+        sample = f"{done} projections (slices of 16384 rows for lm_head) over {args.steps} steps of ~{per_step:.3f} s"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return 0
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from dequant_gemv_gemm_bt_b300 import bt
+
+    # CPU baseline first (rank 0, single GPU only), before any GPU work
+    cpu_baseline = None
+    weights = gen_weights("decode-pass", shapes, bits)
+    xs16 = gen_x("decode-pass", shapes, 1, "f16")
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        rate, nbytes, cnt = oracle_rate(weights, xs16, args.cpu_budget)
+        cpu_baseline = {"value": round(rate, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+                        "sample": f"{cnt} projections of the pass in order ({nbytes/1e6:.1f} MB of packed weights, "
+                                  f"lm_head sliced to 16384 rows), fp64 numpy, ~{args.cpu_budget:.0f} s"}
+
+    bufs = build_decode_pass(torch, bt, weights, xs16, dev)
+    del weights
+    bt.bt_set_option(bt.BT_OPT_PDL, 1)
+    bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
+
+    def run_pass():
+        for c, s, b, x, y, nb in bufs:
+            bt.bt_qgemv(c, s, b, nb, x, y)
+
+    stream = torch.cuda.Stream(device=dev)
+    graph = capture(torch, run_pass, stream)
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error during capture")
+
+    def replay():
+        graph.replay()
+
+    with torch.cuda.stream(stream):
+        t_pass, clocks = timed(torch, dist, stream, replay, args.steps, args.warmup, local_rank)
+    if dist is not None:
+        tt = torch.tensor([t_pass], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_pass = tt.item()
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error during the timed region")
+    sec_per_step = t_pass / args.steps
+    value = pass_bytes * args.steps * world / t_pass / 1e9
+
+    # lm_head alone (the largest single GEMV), for context
+    lm = bufs[-1]
+    lm_bytes = weight_bytes(QWEN06_LM_HEAD[1], QWEN06_LM_HEAD[2], bits)
+    g_lm = capture(torch, lambda: [bt.bt_qgemv(lm[0], lm[1], lm[2], lm[5], lm[3], lm[4]) for _ in range(20)], stream)
+    with torch.cuda.stream(stream):
+        t_lm, _ = timed(torch, None, stream, lambda: g_lm.replay(), 20, 3, local_rank)
+    lm_gbs = lm_bytes * 20 * 20 / t_lm / 1e9
+
+    # end to end through the public API: H2D of the pass's activations from pinned
+    # host memory, the pass, D2H of every output, each step
+    x_host = torch.cat([x for _, _, _, x, _, _ in bufs]).cpu().pin_memory()
+    y_total = sum(y.numel() for *_, y, _ in bufs)
+    y_host = torch.empty(y_total, dtype=torch.float32).pin_memory()
+    x_dev_views, off = [], 0
+    x_all = torch.empty_like(x_host, device=dev)
+    for c, s, b, x, y, nb in bufs:
+        x_dev_views.append(x_all[off:off + x.numel()])
+        off += x.numel()
+    y_all = torch.empty(y_total, dtype=torch.float32, device=dev)
+    y_views, off = [], 0
+    for *_, y, _ in bufs:
+        y_views.append(y_all[off:off + y.numel()])
+        off += y.numel()
+
+    def run_pass_e2e():
+        for (c, s, b, _, _, nb), xv, yv in zip(bufs, x_dev_views, y_views):
+            bt.bt_qgemv(c, s, b, nb, xv, yv)
+    g_e2e = capture(torch, run_pass_e2e, stream)
+
+    def e2e_step():
+        x_all.copy_(x_host, non_blocking=True)
+        g_e2e.replay()
+        y_host.copy_(y_all, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        t_e2e, _ = timed(torch, dist, stream, e2e_step, e2e_steps, 3, local_rank)
+    if dist is not None:
+        tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = tt.item()
+    e2e_val = pass_bytes * e2e_steps * world / t_e2e / 1e9
+
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    launches = len(bufs)
+    achieved = (pass_bytes / launches) / (sec_per_step / launches) / 1e9
+    digest = source_digest(["dequant_gemv_gemm_bt_b300/csrc/qgemv*", "dequant_gemv_gemm_bt_b300/csrc/bt_common.cuh"])
+    traffic = profile_traffic("qgemv_decode_pass.md", digest)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec_per_step * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes, f16 x, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) weights, min/max Q4 g64; x ~ N(0,1) fp16)",
+        "config": config,
+        "roofline": {"bound": "hbm", "kernel": "qgemv_kernel (all 197 launches of the pass)",
+                     "achieved": round(achieved, 2), "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s",
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic, "kernel_source_digest": digest},
+        "cpu_baseline": cpu_baseline,
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(y_total * 4),
+                "how": "per step: pinned H2D of all 197 activation vectors, the pass (CUDA graph of bt_qgemv "
+                       "launches), D2H of all outputs"},
+        "gpu_launches": launches * args.steps,
+        "lm_head_gemv": {"gbs": round(lm_gbs, 1), "frac_of_hbm": round(lm_gbs / hbm, 4),
+                         "shape": "N=151936 K=1024 Q4", "bytes": lm_bytes},
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

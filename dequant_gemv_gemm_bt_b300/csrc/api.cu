@@ -190,6 +190,10 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.M = M; p.N = N; p.K = K;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
+  const int path = opts().gemm_path;
+  const bool tc_ok = tc_supported(bits, K, M, p);
+  if (tc_ok && (path == 2 || (path == 0 && M >= 16)))
+    return cuda_status(launch_gemm_tc(p, bits, x_dtype, y_dtype, stream));
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
 }
 

@@ -1,0 +1,522 @@
+// Tensor-core dequant-GEMM (tcgen05 / TMEM / TMA) for prefill, M >= 16.
+// BaseRT pages, thetesserapress.com "BaseRT claims fastest Apple Silicon
+// inference", section "What BaseRT does differently" (GEMM kernels for prefill
+// where M > 1, dequantization inline in the compute loop, never materializing
+// full-precision weights in memory) and section "Where the wins land" (dense
+// prefill saturates the matrix units); gist.science "Metodologia" (tiled GEMM
+// on the matrix units).
+//
+// Layout of one CTA tile (swap-AB: weights are the MMA's M side):
+//   D[n, m] = sum_k W_deq[n0 + n, k] * X[m0 + m, k],  n < 128, m < BN
+//   A = dequantized weight tile, 128 x 64 (one quantization group) per stage,
+//       bf16/f16, written by the dequant warps into shared memory in the
+//       128-byte-swizzled K-major layout the tensor core reads;
+//   B = X tile, BN x 64, loaded by TMA with 128-byte swizzle;
+//   D = fp32 accumulator in tensor memory (128 lanes x BN columns).
+// Warp roles: warp 0 issues TMA loads of the packed codes and of X; warp 1
+// owns the tensor-memory allocation and one of its threads issues
+// tcgen05.mma; warps 2..9 dequantize (w = s*q + b with an exact integer code
+// and one rounding) and then drain the accumulator to global memory.  The
+// per-row fp16 scales/biases of the CTA's K range are staged in shared memory
+// once, with cp.async, before the main loop.  All waits are bounded.
+#include <cuda.h>
+
+#include "bt_common.cuh"
+#include "qgemm.cuh"
+
+namespace bt {
+namespace tc {
+
+constexpr int BM = 128;                  // weight rows per tile (MMA M)
+constexpr int BK = 64;                   // K per stage = one quantization group
+constexpr int kDeqWarps = 8;
+constexpr int kThreads = (2 + kDeqWarps) * 32;
+
+struct TcParams {
+  int M, N, K, G;          // G = K / 64
+  int kb_begin, kb_count;  // K blocks handled by this launch's CTAs (whole K for now)
+  int stages;
+  int bn;
+  uint32_t stage_bytes, a_bytes, x_bytes, c_bytes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  void* y;
+  bt_dtype y_dtype;
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core
+// groups 1024 bytes apart (tile base 1024-byte aligned).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // descriptor version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A and B both bf16 or both
+// f16, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int n) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// ------------------------------------------------------------------ dequant math
+// Half-precision pair arithmetic for the A operand's type.
+template <bool BF16> __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (BF16) asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <bool BF16> __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  if constexpr (BF16) asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// Magic "2^p + q" in both halves: 128 + q in bf16 (7 mantissa bits), 1024 + q in f16.
+template <bool BF16> constexpr uint32_t kMagic2 = BF16 ? 0x43004300u : 0x64006400u;
+template <bool BF16> constexpr uint32_t kMagicByte = BF16 ? 0x43434343u : 0x64646464u;
+
+// Eight 4-bit codes (one word, code j in bits 4j..4j+3) -> eight dequantized
+// halves in k order, as four pairs.
+template <bool BF16>
+__device__ __forceinline__ uint4 deq8_q4(uint32_t w, uint32_t s2, uint32_t b2) {
+  constexpr uint32_t MG = kMagic2<BF16>;
+  uint32_t d0 = (w & 0x000F000Fu) | MG;          // (q0, q4)
+  uint32_t d1 = ((w >> 4) & 0x000F000Fu) | MG;   // (q1, q5)
+  uint32_t d2 = ((w >> 8) & 0x000F000Fu) | MG;   // (q2, q6)
+  uint32_t d3 = ((w >> 12) & 0x000F000Fu) | MG;  // (q3, q7)
+  d0 = hfma2<BF16>(hsub2<BF16>(d0, MG), s2, b2);
+  d1 = hfma2<BF16>(hsub2<BF16>(d1, MG), s2, b2);
+  d2 = hfma2<BF16>(hsub2<BF16>(d2, MG), s2, b2);
+  d3 = hfma2<BF16>(hsub2<BF16>(d3, MG), s2, b2);
+  return make_uint4(prmt(d0, d1, 0x5410u), prmt(d2, d3, 0x5410u), prmt(d0, d1, 0x7632u), prmt(d2, d3, 0x7632u));
+}
+
+// Exact small integers (< 2048) held as an f16 pair -> the same integers as a bf16 pair
+// (exact for values below 256, which is every 8-bit code).
+__device__ __forceinline__ uint32_t f16x2_int_to_bf16x2(uint32_t h) {
+  const float lo = __half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half((uint16_t)(h >> 16)));
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Four 8-bit codes (one word) -> four halves.  The code pair is formed exactly
+// as f16 "1024 + q" (bf16 has too few mantissa bits for 8-bit codes).
+template <bool BF16>
+__device__ __forceinline__ uint2 deq4_q8(uint32_t w, uint32_t s2, uint32_t b2) {
+  constexpr uint32_t MG16 = 0x64006400u;
+  uint32_t d0 = hsub2<false>(prmt(w, 0x64646464u, 0x4140u), MG16);   // (q0, q1) exact in f16
+  uint32_t d1 = hsub2<false>(prmt(w, 0x64646464u, 0x4342u), MG16);   // (q2, q3)
+  if constexpr (BF16) {
+    d0 = f16x2_int_to_bf16x2(d0);
+    d1 = f16x2_int_to_bf16x2(d1);
+  }
+  d0 = hfma2<BF16>(d0, s2, b2);
+  d1 = hfma2<BF16>(d1, s2, b2);
+  return make_uint2(d0, d1);
+}
+
+// Generic: code j (bits j*B.. of a little-endian word array) as an integer.
+template <int B, int NW>
+__device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[NW], int j) {
+  const int bit = j * B, wi = bit >> 5, off = bit & 31;
+  uint32_t q = w[wi] >> off;
+  if (off + B > 32) q |= w[wi + 1] << (32 - off);
+  return q & ((1u << B) - 1u);
+}
+
+// Dequantize this thread's 4 chunks (32 codes) of one row into 4 x 16 bytes.
+template <int BITS, bool BF16>
+__device__ __forceinline__ void deq32(const uint32_t (&w)[BITS], uint32_t s2, uint32_t b2, uint4 (&out)[4]) {
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) out[c] = deq8_q4<BF16>(w[c], s2, b2);
+  } else if constexpr (BITS == 8) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint2 lo = deq4_q8<BF16>(w[2 * c], s2, b2), hi = deq4_q8<BF16>(w[2 * c + 1], s2, b2);
+      out[c] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+  } else {
+    constexpr uint32_t MG = kMagic2<BF16>;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = code_at<BITS, BITS>(w, 8 * c + 2 * i), hi = code_at<BITS, BITS>(w, 8 * c + 2 * i + 1);
+        o[i] = hfma2<BF16>(hsub2<BF16>(lo | (hi << 16) | MG, MG), s2, b2);
+      }
+      out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+template <bool BF16> __device__ __forceinline__ uint32_t half_pair(uint16_t h16) {
+  // fp16 parameter -> pair of the A type (bf16 rounds; f16 is exact)
+  if constexpr (BF16) {
+    const __nv_bfloat16 v = __float2bfloat16_rn(__half2float(__ushort_as_half(h16)));
+    const uint32_t u = __bfloat16_as_ushort(v);
+    return u | (u << 16);
+  } else {
+    return (uint32_t)h16 | ((uint32_t)h16 << 16);
+  }
+}
+
+__device__ __forceinline__ void store_y(const TcParams& p, size_t i, float v) {
+  if (p.y_dtype == BT_F32) store_out<BT_F32>(p.y, i, v);
+  else if (p.y_dtype == BT_BF16) store_out<BT_BF16>(p.y, i, v);
+  else store_out<BT_F16>(p.y, i, v);
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BITS, bool BF16, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
+                    const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const int KB = p.kb_count;
+  const int Gc = KB;                       // groups staged for this CTA
+  uint16_t* sS = reinterpret_cast<uint16_t*>(smem + (size_t)S * p.stage_bytes);   // [128][Gc]
+  uint16_t* sB = sS + BM * Gc;                                                     // [128][Gc]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(sB + BM * Gc) + 7) & ~uintptr_t(7));
+  uint64_t* full = bars;             // [S] TMA landed (codes + X)
+  uint64_t* afull = bars + S;        // [S] A tile written
+  uint64_t* empty = bars + 2 * S;    // [S] MMAs of the stage done
+  uint64_t* tmem_full = bars + 3 * S;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 3 * S + 1);
+  volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int n0 = blockIdx.x * BM;
+  const int m0 = blockIdx.y * BN;
+  constexpr int kTmemCols = BN < 32 ? 32 : BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&afull[s], kDeqWarps);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    *fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      pdl_wait();
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err)) { *fail = 1; break; }
+        if (*fail) break;
+        uint8_t* st = smem + (size_t)s * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[s], p.c_bytes + p.x_bytes);
+        const int g = p.kb_begin + kb;
+        tma_load_2d(st + p.a_bytes + p.x_bytes, &map_codes, g * (8 * BITS), n0, &full[s]);
+        tma_load_2d(st + p.a_bytes, &map_x, g * BK, m0, &full[s]);
+        ++issued;
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+      if (*fail) {   // let copies in flight land before shared memory is released
+        for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+          mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), p.timeout_ns, p.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(BF16, BN);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err) || !mbar_wait(&afull[s], ph, p.timeout_ns, p.err)) {
+          *fail = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const uint64_t adesc = sw128_desc(st);
+        const uint64_t bdesc = sw128_desc(st + p.a_bytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)   // 16 elements = 32 bytes per MMA step
+          mma_f16(tmem_base, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+        mma_commit(&empty[s]);
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+      mma_commit(tmem_full);   // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ---------------------------------------------------------------- dequant warps
+    const int t = threadIdx.x - 64;        // 0..255
+    const int r = t >> 1, h = t & 1;       // row of the tile, which 4 of its 8 chunks
+    // stage this CTA's scales and biases: rows n0..n0+127, groups kb_begin..+Gc
+    for (int i = t; i < BM * (Gc / 2); i += kDeqWarps * 32) {
+      const int rr = i / (Gc / 2), gg = 2 * (i % (Gc / 2));
+      const int n = n0 + rr;
+      if (n < p.N) {
+        const size_t off = (size_t)n * p.G + p.kb_begin + gg;
+        cp_async4(sS + rr * Gc + gg, p.scales + off);
+        cp_async4(sB + rr * Gc + gg, p.biases + off);
+      } else {
+        *reinterpret_cast<uint32_t*>(sS + rr * Gc + gg) = 0u;
+        *reinterpret_cast<uint32_t*>(sB + rr * Gc + gg) = 0u;
+      }
+    }
+    cp_async_wait_all();
+    asm volatile("bar.sync 1, %0;" ::"r"(kDeqWarps * 32) : "memory");
+
+    int s = 0;
+    uint32_t ph = 0;
+    for (int kb = 0; kb < KB; ++kb) {
+      if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) { *fail = 1; break; }
+      uint8_t* st = smem + (size_t)s * p.stage_bytes;
+      const uint32_t* codes = reinterpret_cast<const uint32_t*>(st + p.a_bytes + p.x_bytes + r * (8 * BITS) + h * (4 * BITS));
+      uint32_t w[BITS];
+#pragma unroll
+      for (int i = 0; i < BITS; ++i) w[i] = codes[i];
+      const uint32_t s2 = half_pair<BF16>(sS[r * Gc + kb]);
+      const uint32_t b2 = half_pair<BF16>(sB[r * Gc + kb]);
+      uint4 out[4];
+      deq32<BITS, BF16>(w, s2, b2, out);
+      uint8_t* arow = st + r * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int chunk = 4 * h + c;
+        *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = out[c];
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[s]);
+      if (++s == S) { s = 0; ph ^= 1u; }
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    const bool ok = mbar_wait(tmem_full, 0, p.timeout_ns, p.err) && !*fail;
+    tc_fence_after();
+    const int q = warp & 3;                        // TMEM lanes 32q..32q+31
+    const int half_sel = (warp - 2) >> 2;          // which half of the column chunks
+    const int n = n0 + 32 * q + lane;
+    for (int c0 = 16 * half_sel; c0 < BN; c0 += 32) {
+      uint32_t v[16];
+      tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+      if (ok && n < p.N) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + c0 + j;
+          if (m < p.M) store_y(p, (size_t)m * p.N + n, __uint_as_float(v[j]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+template <int BITS, bool BF16, int BN>
+cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int row_bytes = gp.K * BITS / 8;
+  CUtensorMap mc, mx;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)gp.N};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(8 * BITS), (cuuint32_t)BM};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(gp.codes), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)gp.K, (cuuint64_t)gp.M};
+    cuuint64_t strides[1] = {(cuuint64_t)gp.K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&mx, BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(gp.x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  TcParams p{};
+  p.M = gp.M;
+  p.N = gp.N;
+  p.K = gp.K;
+  p.G = gp.K / BK;
+  p.kb_begin = 0;
+  p.kb_count = p.G;
+  p.bn = BN;
+  p.a_bytes = BM * BK * 2;
+  p.x_bytes = BN * BK * 2;
+  p.c_bytes = BM * 8 * BITS;
+  p.stage_bytes = (p.a_bytes + p.x_bytes + p.c_bytes + 1023u) & ~1023u;
+  p.scales = gp.scales;
+  p.biases = gp.biases;
+  p.y = gp.y;
+  p.y_dtype = yd;
+  p.err = gp.err;
+  p.timeout_ns = gp.timeout_ns;
+  const size_t params_bytes = (size_t)2 * BM * p.kb_count * sizeof(uint16_t);
+  const size_t fixed = 1024 + params_bytes + 8 + (size_t)(3 * 8 + 1) * 8 + 16;
+  int stages = (int)((size_t)(200 * 1024 - fixed) / p.stage_bytes);
+  stages = std::max(2, std::min(6, stages));
+  p.stages = stages;
+  const size_t smem = fixed + (size_t)stages * p.stage_bytes;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  auto k = qgemm_tc_kernel<BITS, BF16, BN>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((gp.N + BM - 1) / BM, (gp.M + BN - 1) / BN, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, mc, mx, p);
+}
+
+template <int BITS, bool BF16>
+cudaError_t launch_tc_bn(const GemmParams& gp, bt_dtype yd, int bn, cudaStream_t st) {
+  switch (bn) {
+    case 32: return launch_tc_t<BITS, BF16, 32>(gp, yd, st);
+    case 64: return launch_tc_t<BITS, BF16, 64>(gp, yd, st);
+    case 128: return launch_tc_t<BITS, BF16, 128>(gp, yd, st);
+    default: return launch_tc_t<BITS, BF16, 256>(gp, yd, st);
+  }
+}
+
+template <int BITS>
+cudaError_t launch_tc_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int bn, cudaStream_t st) {
+  if (xd == BT_BF16) return launch_tc_bn<BITS, true>(gp, yd, bn, st);
+  return launch_tc_bn<BITS, false>(gp, yd, bn, st);
+}
+
+}  // namespace tc
+
+bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
+  if (!(bits == 2 || bits == 4 || bits == 6 || bits == 8)) return false;
+  const int G = K / 64;
+  if (G % 2) return false;                          // 4-byte cp.async of scale pairs
+  if (G > 192) return false;                        // the CTA's scales/biases are staged whole in shared memory
+  if (((size_t)K * bits / 8) % 16) return false;    // TMA row stride
+  if (gp.offsets) return false;                     // grouped experts: CUDA-core tile for now
+  if ((reinterpret_cast<uintptr_t>(gp.x) & 15) || (reinterpret_cast<uintptr_t>(gp.codes) & 15)) return false;
+  (void)M;
+  return true;
+}
+
+cudaError_t launch_gemm_tc(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
+  int bn = 256;
+  if (gp.M <= 32) bn = 32;
+  else if (gp.M <= 64) bn = 64;
+  else if (gp.M <= 128) bn = 128;
+  switch (bits) {
+    case 2: return tc::launch_tc_bits<2>(gp, xd, yd, bn, st);
+    case 4: return tc::launch_tc_bits<4>(gp, xd, yd, bn, st);
+    case 6: return tc::launch_tc_bits<6>(gp, xd, yd, bn, st);
+    default: return tc::launch_tc_bits<8>(gp, xd, yd, bn, st);
+  }
+}
+
+}  // namespace bt

@@ -48,12 +48,17 @@ def test_qgemm_paths_q4(env, path, m):
     assert_close(y, y_ref, a, "bf16", f"path={path} m={m}")
 
 
-@pytest.mark.parametrize("xdtype,out", [("f16", "f32"), ("bf16", "f32"), ("f16", "f16")])
-def test_qgemm_dtypes(env, xdtype, out):
+# Tolerance follows the arithmetic: products formed from bf16 operands (the
+# tensor-core path with bf16 X dequantizes weights to bf16) carry the bf16
+# bound whatever the output type; f16 operands (exact f16 scale and bias, one
+# rounding per weight) meet the fp32-output bound.
+@pytest.mark.parametrize("xdtype,out,bound", [("f16", "f32", "f32"), ("bf16", "f32", "bf16"), ("f16", "f16", "f16")])
+@pytest.mark.parametrize("path", [1, 2])
+def test_qgemm_dtypes(env, xdtype, out, bound, path):
     qw, x = make_case("gemm-dt", 256, 1024, 4, m=96, xdtype=xdtype)
-    y = run(env, qw, x, xdtype, out)
+    y = run(env, qw, x, xdtype, out, path=path)
     y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_half(x, xdtype))
-    assert_close(y, y_ref, a, out, f"{xdtype}->{out}")
+    assert_close(y, y_ref, a, out if path == 1 else bound, f"{xdtype}->{out} path {path}")
 
 
 def test_qgemm_m1_is_gemv(env):

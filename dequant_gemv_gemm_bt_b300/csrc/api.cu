@@ -1,6 +1,7 @@
 // C ABI of libbt: argument validation, per-shape launch heuristics and the
 // device error word.  Every product is computed by the kernels in this
 // library; nothing here computes on the host.
+#include <algorithm>
 #include <cstdlib>
 #include <mutex>
 #include <vector>
@@ -147,6 +148,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_STAGES: opts().gemv_stages = (int)value; return BT_OK;
     case BT_OPT_GEMM_PATH: opts().gemm_path = (int)value; return BT_OK;
     case BT_OPT_GEMV_KERNEL: opts().gemv_kernel = (int)value; return BT_OK;
+    case BT_OPT_GEMM_SPLITS: opts().gemm_splits = (int)std::min<long long>(value, 8); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
 }

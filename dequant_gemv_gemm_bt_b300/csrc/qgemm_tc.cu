@@ -34,7 +34,8 @@ constexpr int kThreads = (2 + kDeqWarps) * 32;
 
 struct TcParams {
   int M, N, K, G;          // G = K / 64
-  int kb_begin, kb_count;  // K blocks handled by this launch's CTAs (whole K for now)
+  int splits;              // CTAs of a cluster splitting K (gridDim.z); 1 = no split
+  int gc_max;              // most groups any split stages
   int stages;
   int bn;
   uint32_t stage_bytes, a_bytes, x_bytes, c_bytes;
@@ -98,6 +99,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
         "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -231,12 +245,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.stages;
-  const int KB = p.kb_count;
+  // K blocks of this split: boundaries rounded to even group indices (scale pairs
+  // are staged with 4-byte copies)
+  const int split = blockIdx.z;
+  const int kb_lo = split == 0 ? 0 : ((split * p.G) / p.splits) & ~1;
+  const int kb_hi = split == p.splits - 1 ? p.G : (((split + 1) * p.G) / p.splits) & ~1;
+  const int KB = kb_hi - kb_lo;
   const int Gc = KB;                       // groups staged for this CTA
   uint16_t* sS = reinterpret_cast<uint16_t*>(smem + (size_t)S * p.stage_bytes);   // [128][Gc]
-  uint16_t* sB = sS + BM * Gc;                                                     // [128][Gc]
+  uint16_t* sB = sS + BM * p.gc_max;                                               // [128][Gc]
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(sB + BM * Gc) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(sB + BM * p.gc_max) + 7) & ~uintptr_t(7));
   uint64_t* full = bars;             // [S] TMA landed (codes + X)
   uint64_t* afull = bars + S;        // [S] A tile written
   uint64_t* empty = bars + 2 * S;    // [S] MMAs of the stage done
@@ -283,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*fail) break;
         uint8_t* st = smem + (size_t)s * p.stage_bytes;
         mbar_arrive_expect_tx(&full[s], p.c_bytes + p.x_bytes);
-        const int g = p.kb_begin + kb;
+        const int g = kb_lo + kb;
         tma_load_2d(st + p.a_bytes + p.x_bytes, &map_codes, g * (8 * BITS), n0, &full[s]);
         tma_load_2d(st + p.a_bytes, &map_x, g * BK, m0, &full[s]);
         ++issued;
@@ -326,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rr = i / (Gc / 2), gg = 2 * (i % (Gc / 2));
       const int n = n0 + rr;
       if (n < p.N) {
-        const size_t off = (size_t)n * p.G + p.kb_begin + gg;
+        const size_t off = (size_t)n * p.G + kb_lo + gg;
         cp_async4(sS + rr * Gc + gg, p.scales + off);
         cp_async4(sB + rr * Gc + gg, p.biases + off);
       } else {
@@ -362,20 +381,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++s == S) { s = 0; ph ^= 1u; }
     }
 
-    // ---------------------------------------------------------------- epilogue
-    const bool ok = mbar_wait(tmem_full, 0, p.timeout_ns, p.err) && !*fail;
+  }
+
+  // ------------------------------------------------------------------ epilogue
+  // Warps 2..9 drain the accumulator: warp w reads TMEM lanes 32*(w%4).. (the
+  // tile rows it may access) and every other 16-column chunk.  With a K split
+  // the partial tiles meet in distributed shared memory first: chunk c belongs
+  // to cluster rank c % splits, every rank sends its partial of that chunk to
+  // the owner's receive slot [sender], and the owner sums the slots in rank
+  // order (deterministic) and stores.
+  const bool epi = warp >= 2;
+  bool ok = true;
+  if (epi) {
+    ok = mbar_wait(tmem_full, 0, p.timeout_ns, p.err) && !*fail;
     tc_fence_after();
-    const int q = warp & 3;                        // TMEM lanes 32q..32q+31
-    const int half_sel = (warp - 2) >> 2;          // which half of the column chunks
-    const int n = n0 + 32 * q + lane;
-    for (int c0 = 16 * half_sel; c0 < BN; c0 += 32) {
-      uint32_t v[16];
-      tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-      if (ok && n < p.N) {
+  }
+  const int q = warp & 3;
+  const int half_sel = (warp - 2) >> 2;
+  const int row = 32 * q + lane;
+  const int n = n0 + row;
+  const uint32_t taddr_row = tmem_base + ((uint32_t)(32 * q) << 16);
+  if (p.splits == 1) {
+    if (epi) {
+      for (int c0 = 16 * half_sel; c0 < BN; c0 += 32) {
+        uint32_t v[16];
+        tmem_ld16(taddr_row + (uint32_t)c0, v);
+        if (ok && n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < p.M) store_y(p, (size_t)m * p.N + n, __uint_as_float(v[j]));
+          }
+        }
+      }
+    }
+  } else {
+    const int R = p.splits;
+    constexpr int kChunks = BN / 16;
+    const int owned_max = (kChunks + R - 1) / R;
+    // receive area (reuses the pipeline stages): [R senders][128 rows][owned_max * 16] fp32
+    float* recv = reinterpret_cast<float*>(smem);
+    const uint32_t recv_s = smem_u32(recv);
+    tc_fence_before();
+    cluster_sync_all();            // every CTA of the cluster is past its main loop
+    tc_fence_after();
+    if (epi) {
+      for (int c0 = 16 * half_sel; c0 < BN; c0 += 32) {
+        uint32_t v[16];
+        tmem_ld16(taddr_row + (uint32_t)c0, v);
+        const int chunk = c0 >> 4, owner = chunk % R, slot = chunk / R;
+        const uint32_t local = recv_s + (uint32_t)((((split * BM) + row) * owned_max + slot) * 16 * 4);
+        const uint32_t remote = map_to_rank(local, (uint32_t)owner);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) st_cluster_v4(remote + j * 4, v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+    }
+    cluster_sync_all();            // every partial is in its owner's receive area
+    if (epi && ok && n < p.N) {
+      for (int slot = half_sel; slot < owned_max; slot += 2) {
+        const int chunk = slot * R + split;
+        if (chunk >= kChunks) break;
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+        for (int sdr = 0; sdr < R; ++sdr) {
+          const float4* src = reinterpret_cast<const float4*>(recv + (((size_t)(sdr * BM) + row) * owned_max + slot) * 16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 f = src[j];
+            acc[4 * j] += f.x; acc[4 * j + 1] += f.y; acc[4 * j + 2] += f.z; acc[4 * j + 3] += f.w;
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int m = m0 + c0 + j;
-          if (m < p.M) store_y(p, (size_t)m * p.N + n, __uint_as_float(v[j]));
+          const int m = m0 + chunk * 16 + j;
+          if (m < p.M) store_y(p, (size_t)m * p.N + n, acc[j]);
         }
       }
     }
@@ -409,7 +489,7 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int BITS, bool BF16, int BN>
-cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, cudaStream_t st) {
+cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStream_t st) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int row_bytes = gp.K * BITS / 8;
@@ -440,8 +520,15 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, cudaStream_t st) {
   p.N = gp.N;
   p.K = gp.K;
   p.G = gp.K / BK;
-  p.kb_begin = 0;
-  p.kb_count = p.G;
+  p.splits = splits;
+  int gc_max = 0;
+  for (int z = 0; z < splits; ++z) {   // same split boundaries as the kernel
+    const int lo = z == 0 ? 0 : ((z * p.G) / splits) & ~1;
+    const int hi = z == splits - 1 ? p.G : (((z + 1) * p.G) / splits) & ~1;
+    if (hi - lo < 1) return cudaErrorInvalidValue;
+    gc_max = std::max(gc_max, hi - lo);
+  }
+  p.gc_max = gc_max;
   p.bn = BN;
   p.a_bytes = BM * BK * 2;
   p.x_bytes = BN * BK * 2;
@@ -453,10 +540,14 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, cudaStream_t st) {
   p.y_dtype = yd;
   p.err = gp.err;
   p.timeout_ns = gp.timeout_ns;
-  const size_t params_bytes = (size_t)2 * BM * p.kb_count * sizeof(uint16_t);
+  const size_t params_bytes = (size_t)2 * BM * p.gc_max * sizeof(uint16_t);
   const size_t fixed = 1024 + params_bytes + 8 + (size_t)(3 * 8 + 1) * 8 + 16;
-  int stages = (int)((size_t)(200 * 1024 - fixed) / p.stage_bytes);
-  stages = std::max(2, std::min(6, stages));
+  int stages = (int)((size_t)(220 * 1024 - fixed) / p.stage_bytes);
+  stages = std::max(2, std::min(8, stages));
+  // a K split reduces through a receive area laid over the stages
+  const int chunks = BN / 16, owned_max = (chunks + splits - 1) / splits;
+  const size_t recv_bytes = splits > 1 ? (size_t)splits * BM * owned_max * 16 * 4 : 0;
+  while ((size_t)stages * p.stage_bytes < recv_bytes) ++stages;
   p.stages = stages;
   const size_t smem = fixed + (size_t)stages * p.stage_bytes;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -464,32 +555,36 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((gp.N + BM - 1) / BM, (gp.M + BN - 1) / BN, 1);
+  cfg.gridDim = dim3((gp.N + BM - 1) / BM, (gp.M + BN - 1) / BN, splits);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = splits;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k, mc, mx, p);
 }
 
 template <int BITS, bool BF16>
-cudaError_t launch_tc_bn(const GemmParams& gp, bt_dtype yd, int bn, cudaStream_t st) {
+cudaError_t launch_tc_bn(const GemmParams& gp, bt_dtype yd, int bn, int splits, cudaStream_t st) {
   switch (bn) {
-    case 32: return launch_tc_t<BITS, BF16, 32>(gp, yd, st);
-    case 64: return launch_tc_t<BITS, BF16, 64>(gp, yd, st);
-    case 128: return launch_tc_t<BITS, BF16, 128>(gp, yd, st);
-    default: return launch_tc_t<BITS, BF16, 256>(gp, yd, st);
+    case 32: return launch_tc_t<BITS, BF16, 32>(gp, yd, splits, st);
+    case 64: return launch_tc_t<BITS, BF16, 64>(gp, yd, splits, st);
+    case 128: return launch_tc_t<BITS, BF16, 128>(gp, yd, splits, st);
+    default: return launch_tc_t<BITS, BF16, 256>(gp, yd, splits, st);
   }
 }
 
 template <int BITS>
-cudaError_t launch_tc_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int bn, cudaStream_t st) {
-  if (xd == BT_BF16) return launch_tc_bn<BITS, true>(gp, yd, bn, st);
-  return launch_tc_bn<BITS, false>(gp, yd, bn, st);
+cudaError_t launch_tc_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int bn, int splits, cudaStream_t st) {
+  if (xd == BT_BF16) return launch_tc_bn<BITS, true>(gp, yd, bn, splits, st);
+  return launch_tc_bn<BITS, false>(gp, yd, bn, splits, st);
 }
 
 }  // namespace tc
@@ -506,16 +601,28 @@ bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
   return true;
 }
 
+// Tile width and K split: token tiles of up to 256 columns; clusters of up to
+// 8 CTAs split K so that tiles x splits covers the SMs (each split keeps at
+// least 4 K blocks).
+void plan_gemm_tc(int M, int N, int K, int sms, int& bn, int& splits) {
+  bn = 256;
+  if (M <= 32) bn = 32;
+  else if (M <= 64) bn = 64;
+  else if (M <= 128) bn = 128;
+  const int tiles = ((N + 127) / 128) * ((M + bn - 1) / bn);
+  const int kb = K / 64;
+  splits = std::max(1, std::min({8, (sms + tiles / 2) / std::max(1, tiles), kb / 4}));
+  if (opts().gemm_splits > 0) splits = std::min(opts().gemm_splits, std::max(1, kb / 2));
+}
+
 cudaError_t launch_gemm_tc(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
-  int bn = 256;
-  if (gp.M <= 32) bn = 32;
-  else if (gp.M <= 64) bn = 64;
-  else if (gp.M <= 128) bn = 128;
+  int bn, splits;
+  plan_gemm_tc(gp.M, gp.N, gp.K, sm_count(), bn, splits);
   switch (bits) {
-    case 2: return tc::launch_tc_bits<2>(gp, xd, yd, bn, st);
-    case 4: return tc::launch_tc_bits<4>(gp, xd, yd, bn, st);
-    case 6: return tc::launch_tc_bits<6>(gp, xd, yd, bn, st);
-    default: return tc::launch_tc_bits<8>(gp, xd, yd, bn, st);
+    case 2: return tc::launch_tc_bits<2>(gp, xd, yd, bn, splits, st);
+    case 4: return tc::launch_tc_bits<4>(gp, xd, yd, bn, splits, st);
+    case 6: return tc::launch_tc_bits<6>(gp, xd, yd, bn, splits, st);
+    default: return tc::launch_tc_bits<8>(gp, xd, yd, bn, splits, st);
   }
 }
 

@@ -71,3 +71,20 @@ def test_qgemm_m1_is_gemv(env):
 def test_qgemm_deterministic(env):
     qw, x = make_case("gemm-det", 512, 2048, 4, m=128, xdtype="bf16")
     assert np.array_equal(run(env, qw, x, "bf16", "bf16"), run(env, qw, x, "bf16", "bf16"))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("m", [40, 128, 300])
+def test_qgemm_tc_k_split(env, splits, m):
+    """Tensor-core path with K split over a cluster (partials reduced in shared memory)."""
+    torch, bt = env
+    qw, x = make_case("gemm-split", 333, 3072, 4, m=m, xdtype="bf16")
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMM_SPLITS, splits)
+        y = run(env, qw, x, "bf16", "f32", path=2)
+        y2 = run(env, qw, x, "bf16", "f32", path=2)
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMM_SPLITS, 0)
+    assert np.array_equal(y, y2), "split-K result is not deterministic"
+    y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_bf16(x))
+    assert_close(y, y_ref, a, "bf16", f"splits={splits} m={m}")

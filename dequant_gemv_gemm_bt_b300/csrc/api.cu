@@ -147,7 +147,6 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_GENERIC: opts().gemv_generic = value != 0; return BT_OK;
     case BT_OPT_GEMV_STAGES: opts().gemv_stages = (int)value; return BT_OK;
     case BT_OPT_GEMM_PATH: opts().gemm_path = (int)value; return BT_OK;
-    case BT_OPT_GEMV_KERNEL: opts().gemv_kernel = (int)value; return BT_OK;
     case BT_OPT_GEMM_SPLITS: opts().gemm_splits = (int)std::min<long long>(value, 8); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
@@ -177,6 +176,48 @@ bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (!x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
   return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0, stream);
+}
+
+bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
+                           bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
+  if (!problems || count < 1 || K <= 0) return BT_ERR_INVALID_ARG;
+  if (count > kBatchCap) return BT_ERR_UNSUPPORTED;
+  if (!half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
+  long long rows = 0;
+  int max_n = 0;
+  for (int i = 0; i < count; ++i) {
+    const bt_gemv_problem& q = problems[i];
+    bt_status s = check_weights(q.codes, q.scales, q.biases, bits, group_size, q.n, K);
+    if (s != BT_OK) return s;
+    if (!q.x || !q.y) return BT_ERR_INVALID_ARG;
+    if (!aligned16(q.x)) return BT_ERR_MISALIGNED;
+    rows += q.n;
+    max_n = std::max(max_n, q.n);
+  }
+  GemvBatch<kBatchCap> batch;
+  batch.count = count;
+  for (int i = 0; i < count; ++i) {
+    batch.prob[i].codes = problems[i].codes;
+    batch.prob[i].scales = problems[i].scales;
+    batch.prob[i].biases = problems[i].biases;
+    batch.prob[i].x = problems[i].x;
+    batch.prob[i].y = problems[i].y;
+    batch.prob[i].n = problems[i].n;
+  }
+  GemvParams p{};
+  p.K = K;
+  p.G = K / kGroup;
+  p.N = max_n;
+  p.err = device_error_word();
+  p.timeout_ns = opts().wait_timeout_ns;
+  p.const_weights = opts().pdl && opts().const_weights;
+  p.drop_stage = opts().test_drop_stage;
+  opts().test_drop_stage = 0;
+  const bool fast = x_dtype == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !opts().gemv_generic;
+  const int problems_equiv = (int)std::max<long long>(1, (rows + max_n - 1) / max_n);
+  const GemvPlan pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count());
+  if (!pl.feasible) return BT_ERR_UNSUPPORTED;
+  return cuda_status(launch_gemv(p, pl, bits, x_dtype, y_dtype, stream, &batch));
 }
 
 bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,

@@ -26,7 +26,6 @@ struct LaunchOpts {
   bool gemv_generic = false; // tuning: force the generic unpack path
   int gemv_stages = 0;       // tuning: pipeline depth override (0 = heuristic)
   int gemm_path = 0;         // tuning: 0 = heuristic, 1 = CUDA-core tile, 2 = tensor-core tile
-  int gemv_kernel = 0;       // tuning: 0 = shared-memory ring, 1 = register streaming
   int gemm_splits = 0;       // tuning: tensor-core GEMM K split (0 = heuristic)
 };
 LaunchOpts& opts();

@@ -6,16 +6,11 @@
 
 namespace bt {
 
-cudaError_t launch_gemv_b2(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_b3(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_b4(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_b6(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_b8(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_reg_b2(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_reg_b3(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_reg_b4(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_reg_b6(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
-cudaError_t launch_gemv_reg_b8(const GemvParams&, const GemvPlan&, bt_dtype, cudaStream_t);
+cudaError_t launch_gemv_b2(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
+cudaError_t launch_gemv_b3(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
+cudaError_t launch_gemv_b4(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
+cudaError_t launch_gemv_b6(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
+cudaError_t launch_gemv_b8(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
 
 namespace {
 constexpr int kMaxNW = 8;               // consumer warps per CTA (as in the kernel)
@@ -24,42 +19,7 @@ constexpr int kRingBudget = 176 * 1024;
 constexpr size_t kMaxSmem = 227 * 1024;   // opt-in dynamic shared memory per block on sm_100/sm_103
 }  // namespace
 
-// Register-streaming variant: 16 warps, up to 2 chunks per lane, rows in
-// batches of RI per warp, double-buffered global loads.
-static GemvPlan plan_gemv_reg(int bits, bool fast, int N, int K, int problems, int num_experts, int sms) {
-  GemvPlan pl{};
-  pl.reg = true;
-  pl.fast = fast;
-  constexpr int nw = 16;
-  const int nchunks = K / 32;
-  int kw = 1;
-  while (kw < nw && (nchunks + 32 * kw - 1) / (32 * kw) > 2) kw *= 2;
-  pl.kw = kw;
-  pl.cpl = (nchunks + 32 * kw - 1) / (32 * kw);
-  pl.feasible = pl.cpl <= 2;
-  if (!pl.feasible) return pl;
-  const int rw = nw / kw;
-  pl.ri = pl.cpl == 1 ? 2 : 1;
-  const int G = K / kGroup;
-  pl.row_bytes = K * bits / 8;
-  const long long rows_total = (long long)N * problems;
-  const long long per_sm = std::max<long long>(1, (rows_total + sms - 1) / sms);
-  const int unit = pl.ri * rw;
-  long long rb = std::min<long long>(unit * 16LL, ((per_sm + unit - 1) / unit) * unit);
-  rb = std::min<long long>(rb, ((N + unit - 1) / unit) * (long long)unit);
-  pl.rows_per_unit = (int)std::max<long long>(unit, rb);
-  pl.units_per_problem = (N + pl.rows_per_unit - 1) / pl.rows_per_unit;
-  pl.num_units = (long long)pl.units_per_problem * problems;
-  pl.grid = (int)std::min<long long>(pl.num_units, (long long)sms);
-  pl.stages = 0;
-  pl.stage_bytes = 0;
-  pl.smem = (size_t)(num_experts + 1) * sizeof(int);
-  (void)G;
-  return pl;
-}
-
 GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms) {
-  if (opts().gemv_kernel == 1) return plan_gemv_reg(bits, fast, N, K, problems, num_experts, sms);
   GemvPlan pl{};
   pl.fast = fast;
   const int nchunks = K / 32;
@@ -115,7 +75,8 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   return pl;
 }
 
-cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
+cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st,
+                        GemvBatch<kBatchCap>* batch) {
   p.rows_per_unit = pl.rows_per_unit;
   p.row_bytes = pl.row_bytes;
   p.stage_bytes = pl.stage_bytes;
@@ -124,22 +85,25 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
   p.units_per_problem = pl.units_per_problem;
   p.num_units = pl.num_units;
   p.y_dtype = yd;
-  if (pl.num_units == 0) return cudaSuccess;
-  if (pl.reg) {
-    switch (bits) {
-      case 2: return launch_gemv_reg_b2(p, pl, xd, st);
-      case 3: return launch_gemv_reg_b3(p, pl, xd, st);
-      case 4: return launch_gemv_reg_b4(p, pl, xd, st);
-      case 6: return launch_gemv_reg_b6(p, pl, xd, st);
-      default: return launch_gemv_reg_b8(p, pl, xd, st);
+  GemvPlan plb = pl;
+  if (batch) {   // per-problem row blocks and their running offsets
+    long long u = 0;
+    for (int i = 0; i < batch->count; ++i) {
+      batch->prob[i].units = (batch->prob[i].n + pl.rows_per_unit - 1) / pl.rows_per_unit;
+      batch->prob[i].unit_begin = u;
+      u += batch->prob[i].units;
     }
+    p.num_units = u;
+    plb.num_units = u;
+    plb.grid = (int)std::min<long long>(u, (long long)sm_count());
   }
+  if (p.num_units == 0) return cudaSuccess;
   switch (bits) {
-    case 2: return launch_gemv_b2(p, pl, xd, st);
-    case 3: return launch_gemv_b3(p, pl, xd, st);
-    case 4: return launch_gemv_b4(p, pl, xd, st);
-    case 6: return launch_gemv_b6(p, pl, xd, st);
-    default: return launch_gemv_b8(p, pl, xd, st);
+    case 2: return launch_gemv_b2(p, plb, xd, batch, st);
+    case 3: return launch_gemv_b3(p, plb, xd, batch, st);
+    case 4: return launch_gemv_b4(p, plb, xd, batch, st);
+    case 6: return launch_gemv_b6(p, plb, xd, batch, st);
+    default: return launch_gemv_b8(p, plb, xd, batch, st);
   }
 }
 

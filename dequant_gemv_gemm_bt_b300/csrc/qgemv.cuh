@@ -31,9 +31,26 @@ struct GemvParams {
   int drop_stage;
 };
 
+// Batched launches: many independent GEMVs of the same K, bits and dtypes, each
+// with its own weight, x, y and N; the table travels in the kernel parameters.
+constexpr int kBatchCap = 192;
+struct GemvProblem {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const void* x;
+  void* y;
+  int n;
+  int units;          // row blocks of this problem (rows_per_unit each)
+  long long unit_begin;
+};
+template <int CAP> struct GemvBatch {
+  int count;
+  GemvProblem prob[CAP];
+};
+
 struct GemvPlan {
   bool fast;
-  bool reg;        // register-streaming kernel (no shared-memory ring)
   bool feasible;   // false: no GEMV kernel fits this shape (the caller uses the CUDA-core tile)
   int kw, cpl, ri, rows_per_unit, row_bytes, stage_bytes, stages, units_per_problem, grid;
   long long num_units;
@@ -42,6 +59,6 @@ struct GemvPlan {
 
 GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,
-                        cudaStream_t stream);
+                        cudaStream_t stream, GemvBatch<kBatchCap>* batch = nullptr);
 
 }  // namespace bt

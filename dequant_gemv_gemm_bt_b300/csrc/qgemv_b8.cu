@@ -2,10 +2,8 @@
 #include "qgemv_impl.cuh"
 
 namespace bt {
-cudaError_t launch_gemv_b8(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
-  return gemv::launch_bits<8>(p, pl, xd, st);
-}
-cudaError_t launch_gemv_reg_b8(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
-  return gemv::launch_reg_bits<8>(p, pl, xd, st);
+cudaError_t launch_gemv_b8(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, const GemvBatch<kBatchCap>* b,
+                           cudaStream_t st) {
+  return gemv::launch_bits<8>(p, pl, xd, b, st);
 }
 }  // namespace bt

@@ -294,14 +294,6 @@ __device__ __forceinline__ int problem_xrow(const GemvParams& p, int prob) {
 }
 __device__ __forceinline__ int problem_yrow(const GemvParams& p, int prob) { return p.moe_offsets ? prob : 0; }
 
-// A unit's rows are staged by bulk copies only when every copy starts on a
-// 16-byte boundary and moves a multiple of 16 bytes; otherwise the consumers
-// read that unit straight from global memory.
-__device__ __forceinline__ bool unit_uses_bulk(const GemvParams& p, size_t wrow, int rows) {
-  const size_t c0 = wrow * (size_t)p.row_bytes, s0 = wrow * (size_t)p.G * 2;
-  const size_t cb = (size_t)rows * p.row_bytes, sb = (size_t)rows * p.G * 2;
-  return ((c0 | s0 | cb | sb) & 15u) == 0;
-}
 
 // --------------------------------------------------------------- the kernel
 // Consumer warps per CTA: 8, which leaves each thread up to 168 registers so
@@ -350,14 +342,88 @@ __device__ __forceinline__ float reduce_rows(const float (&part)[RI], int lane, 
   }
 }
 
-__device__ __forceinline__ void store_y(const GemvParams& p, size_t i, float v) {
-  if (p.y_dtype == BT_F32) store_out<BT_F32>(p.y, i, v);
-  else if (p.y_dtype == BT_BF16) store_out<BT_BF16>(p.y, i, v);
-  else store_out<BT_F16>(p.y, i, v);
+__device__ __forceinline__ void store_yv(const GemvParams& p, void* y, size_t i, float v) {
+  if (p.y_dtype == BT_F32) store_out<BT_F32>(y, i, v);
+  else if (p.y_dtype == BT_BF16) store_out<BT_BF16>(y, i, v);
+  else store_out<BT_F16>(y, i, v);
 }
 
-template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
-__global__ void __launch_bounds__(Warps<CPL>::kThreads, 1) qgemv_kernel(const GemvParams p) {
+// One GEMV problem as the kernel sees it: weight rows, x row, y row.
+struct ProbView {
+  const uint8_t* codes;      // row 0 of this problem's packed weight
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint16_t* x;         // this problem's x (K halves)
+  void* y;                   // output base
+  size_t y0;                 // element index of this problem's row 0 in y
+  int n;                     // rows of the problem
+  int units;                 // row blocks of the problem
+  bool valid;                // false: a grouped row that no expert holds (skipped)
+};
+
+template <bool BATCH>
+__device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch<BATCH ? kBatchCap : 1>& batch,
+                                            const int* offs, int prob) {
+  ProbView v;
+  if constexpr (BATCH) {
+    const GemvProblem& q = batch.prob[prob];
+    v.codes = reinterpret_cast<const uint8_t*>(q.codes);
+    v.scales = q.scales;
+    v.biases = q.biases;
+    v.x = static_cast<const uint16_t*>(q.x);
+    v.y = q.y;
+    v.y0 = 0;
+    v.n = q.n;
+    v.units = q.units;
+    v.valid = true;
+  } else {
+    const int e = problem_expert(p, offs, prob);
+    const size_t e_rows = (size_t)(e < 0 ? 0 : e) * p.N;
+    v.codes = reinterpret_cast<const uint8_t*>(p.codes) + e_rows * p.row_bytes;
+    v.scales = p.scales + e_rows * p.G;
+    v.biases = p.biases + e_rows * p.G;
+    v.x = static_cast<const uint16_t*>(p.x) + (size_t)problem_xrow(p, prob) * p.K;
+    v.y = p.y;
+    v.y0 = (size_t)problem_yrow(p, prob) * p.N;
+    v.n = p.N;
+    v.units = p.units_per_problem;
+    v.valid = e >= 0;
+  }
+  return v;
+}
+
+// Rows of a unit are staged by bulk copies only when every copy starts on a
+// 16-byte boundary and moves a multiple of 16 bytes; otherwise the consumers
+// read that unit straight from global memory.
+__device__ __forceinline__ bool unit_bulk(const GemvParams& p, const ProbView& v, int row0, int rows) {
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(v.codes) + (size_t)row0 * p.row_bytes;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(v.scales + (size_t)row0 * p.G);
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(v.biases + (size_t)row0 * p.G);
+  const size_t cb = (size_t)rows * p.row_bytes, sb = (size_t)rows * p.G * 2;
+  return ((c0 | s0 | b0 | cb | sb) & 15u) == 0;
+}
+
+// First problem whose unit range contains unit u (batched launches).
+template <bool BATCH>
+__device__ __forceinline__ void first_unit(const GemvParams& p, const GemvBatch<BATCH ? kBatchCap : 1>& batch,
+                                           long long u, int& prob, int& blk) {
+  if constexpr (BATCH) {
+    int lo = 0, hi = batch.count;   // unit_begin[lo] <= u
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (batch.prob[mid].unit_begin <= u) lo = mid; else hi = mid;
+    }
+    prob = lo;
+    blk = (int)(u - batch.prob[lo].unit_begin);
+  } else {
+    prob = (int)(u / p.units_per_problem);
+    blk = (int)(u - (long long)prob * p.units_per_problem);
+  }
+}
+
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
+__global__ void __launch_bounds__(Warps<CPL>::kThreads, 1)
+    qgemv_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
   constexpr int kNW = Warps<CPL>::kNW;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -388,6 +454,7 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, 1) qgemv_kernel(const Ge
   const int RB = p.rows_per_unit;
   const int row_bytes = p.row_bytes;
   const int G = p.G;
+  if (u_begin >= u_end) return;
 
   if (warp == kNW) {
     // ------------------------------------------------------------ producer
@@ -396,51 +463,46 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, 1) qgemv_kernel(const Ge
     // with 16-byte cp.async, whose completion the same mbarrier tracks.
     if (!p.const_weights) pdl_wait();
     const uint64_t pol = l2_policy_evict_first();
-    // unit u = prob * units_per_problem + blk; stage s = it % S, phase = (it / S) & 1,
-    // all advanced incrementally (no divisions in the loop)
-    int prob = (int)(u_begin / p.units_per_problem);
-    int blk = (int)(u_begin - (long long)prob * p.units_per_problem);
+    int prob, blk;
+    first_unit<BATCH>(p, batch, u_begin, prob, blk);
+    ProbView v = resolve<BATCH>(p, batch, offs, prob);
     int s = 0;
     uint32_t ph = 0;
     long long it = 0;
     bool ok = true;
     for (long long u = u_begin; u < u_end; ++u, ++it) {
+      if (blk == v.units) { blk = 0; ++prob; v = resolve<BATCH>(p, batch, offs, prob); }
       if (it >= S) {
         bool w = true;
         if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
         if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; break; }
       }
       const int row0 = blk * RB;
-      const int rows = min(RB, p.N - row0);
-      const int e = problem_expert(p, offs, prob);
-      const uint32_t cbytes = (uint32_t)rows * row_bytes, sbytes = (uint32_t)rows * G * 2;
-      const size_t wrow = (size_t)(e < 0 ? 0 : e) * p.N + row0;
-      const bool tma = unit_uses_bulk(p, wrow, rows);
-      if (p.drop_stage && blockIdx.x == 0 && it == 0) {   // test hook: never fill this stage
-        if (++blk == p.units_per_problem) { blk = 0; ++prob; }
-        if (++s == S) { s = 0; ph ^= 1u; }
-        continue;
-      }
-      if (tma && e >= 0) {
-        uint8_t* st = smem + (size_t)s * p.stage_bytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], cbytes);
-          bulk_g2s(st, reinterpret_cast<const uint8_t*>(p.codes) + wrow * row_bytes, cbytes, &full[s], pol);
+      const int rows = min(RB, v.n - row0);
+      const bool drop = p.drop_stage && blockIdx.x == 0 && it == 0;   // test hook: never fill this stage
+      if (!drop) {
+        if (v.valid && unit_bulk(p, v, row0, rows)) {
+          const uint32_t cbytes = (uint32_t)rows * row_bytes, sbytes = (uint32_t)rows * G * 2;
+          uint8_t* st = smem + (size_t)s * p.stage_bytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], cbytes);
+            bulk_g2s(st, v.codes + (size_t)row0 * row_bytes, cbytes, &full[s], pol);
+          }
+          const uint8_t* gs = reinterpret_cast<const uint8_t*>(v.scales + (size_t)row0 * G);
+          const uint8_t* gb = reinterpret_cast<const uint8_t*>(v.biases + (size_t)row0 * G);
+          uint8_t* ss = st + (size_t)RB * row_bytes;
+          uint8_t* sbb = ss + (size_t)RB * G * 2;
+          for (uint32_t o = lane * 16u; o < sbytes; o += 32u * 16u) {
+            cp_async16(ss + o, gs + o);
+            cp_async16(sbb + o, gb + o);
+          }
+          cp_async_mbar_arrive_noinc(&full[s]);
+        } else {
+          mbar_arrive(&full[s]);
+          if (lane == 0) mbar_arrive(&full[s]);
         }
-        const uint8_t* gs = reinterpret_cast<const uint8_t*>(p.scales + wrow * G);
-        const uint8_t* gb = reinterpret_cast<const uint8_t*>(p.biases + wrow * G);
-        uint8_t* ss = st + (size_t)RB * row_bytes;
-        uint8_t* sbb = ss + (size_t)RB * G * 2;
-        for (uint32_t o = lane * 16u; o < sbytes; o += 32u * 16u) {
-          cp_async16(ss + o, gs + o);
-          cp_async16(sbb + o, gb + o);
-        }
-        cp_async_mbar_arrive_noinc(&full[s]);
-      } else {
-        mbar_arrive(&full[s]);
-        if (lane == 0) mbar_arrive(&full[s]);
       }
-      if (++blk == p.units_per_problem) { blk = 0; ++prob; }
+      ++blk;
       if (++s == S) { s = 0; ph ^= 1u; }
     }
     if (!ok) {
@@ -468,39 +530,37 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, 1) qgemv_kernel(const Ge
   pdl_wait();   // activations (and offsets) may come from the previous kernel
 
   XSlice<BITS, FAST> xs[CPL];
-  int cur_prob = -1;
-  int cur_expert = -1;
   int rbuf = 0;
-  int prob = (int)(u_begin / p.units_per_problem);
-  int blk = (int)(u_begin - (long long)prob * p.units_per_problem);
+  int prob, blk;
+  first_unit<BATCH>(p, batch, u_begin, prob, blk);
+  ProbView v;
+  int cur_prob = -1;
   int s = 0;
   uint32_t ph = 0;
   for (long long u = u_begin; u < u_end; ++u) {
+    if (cur_prob >= 0 && blk == v.units) { blk = 0; ++prob; }
     if (prob != cur_prob) {
       cur_prob = prob;
-      cur_expert = problem_expert(p, offs, prob);
-      const int xrow = problem_xrow(p, prob);
-      const uint16_t* xb = static_cast<const uint16_t*>(p.x) + (size_t)xrow * p.K;
+      v = resolve<BATCH>(p, batch, offs, prob);
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = (i * KW + kw) * 32 + lane;
         if (c < nchunks) {
-          if constexpr (FAST) load_x_fast<BITS, XD>(xs[i], xb + (size_t)c * 32);
-          else load_x_generic<BITS, XD>(xs[i], xb + (size_t)c * 32);
+          if constexpr (FAST) load_x_fast<BITS, XD>(xs[i], v.x + (size_t)c * 32);
+          else load_x_generic<BITS, XD>(xs[i], v.x + (size_t)c * 32);
         }
       }
     }
     if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) return;
     const int row0 = blk * RB;
-    const int rows = min(RB, p.N - row0);
-    const size_t wrow = (size_t)(cur_expert < 0 ? 0 : cur_expert) * p.N + row0;
-    const bool tma = unit_uses_bulk(p, wrow, rows) && cur_expert >= 0;
+    const int rows = min(RB, v.n - row0);
+    const bool tma = v.valid && unit_bulk(p, v, row0, rows);
     const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
     const uint32_t st_sc = st + RB * row_bytes, st_bi = st_sc + RB * G * 2;
-    const uint8_t* g_codes = reinterpret_cast<const uint8_t*>(p.codes) + wrow * row_bytes;
-    const uint16_t* g_sc = p.scales + wrow * G;
-    const uint16_t* g_bi = p.biases + wrow * G;
-    const size_t ybase = (size_t)problem_yrow(p, prob) * p.N + row0;
+    const uint8_t* g_codes = v.codes + (size_t)row0 * row_bytes;
+    const uint16_t* g_sc = v.scales + (size_t)row0 * G;
+    const uint16_t* g_bi = v.biases + (size_t)row0 * G;
+    const size_t ybase = v.y0 + row0;
 
     const int nb = (rows + RI - 1) / RI;
     for (int bi = rg; bi < nb; bi += RW) {
@@ -537,33 +597,34 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, 1) qgemv_kernel(const Ge
         }
       }
       int rj;
-      const float v = reduce_rows<RI>(part, lane, rj);
+      const float val = reduce_rows<RI>(part, lane, rj);
       const int r = r0 + rj;
       if (KW == 1) {
-        if (writer && r < rows && cur_expert >= 0) store_y(p, ybase + r, v);
+        if (writer && r < rows && v.valid) store_yv(p, v.y, ybase + r, val);
       } else {
         float* rb = red + (size_t)((rg * 2 + rbuf) * RI) * KW;   // [RI][KW]
-        if (writer) rb[rj * KW + kw] = v;
+        if (writer) rb[rj * KW + kw] = val;
         asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
-        if (kw == 0 && writer && r < rows && cur_expert >= 0) {
+        if (kw == 0 && writer && r < rows && v.valid) {
           float acc = 0.f;
           for (int j = 0; j < KW; ++j) acc += rb[rj * KW + j];
-          store_y(p, ybase + r, acc);
+          store_yv(p, v.y, ybase + r, acc);
         }
         rbuf ^= 1;
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (++blk == p.units_per_problem) { blk = 0; ++prob; }
+    ++blk;
     if (++s == S) { s = 0; ph ^= 1u; }
   }
 }
 
 // ------------------------------------------------------------------ launch
-template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
-cudaError_t launch_t(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
-  auto k = qgemv_kernel<BITS, XD, CPL, FAST, RI>;
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
+cudaError_t launch_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int grid, size_t smem,
+                     cudaStream_t stream) {
+  auto k = qgemv_kernel<BITS, XD, CPL, FAST, RI, BATCH>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -576,242 +637,54 @@ cudaError_t launch_t(const GemvParams& p, int grid, size_t smem, cudaStream_t st
   attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, p);
-}
-
-template <int BITS, bt_dtype XD, int CPL, bool FAST>
-cudaError_t launch_ri(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
-  switch (pl.ri) {
-    case 4: return launch_t<BITS, XD, CPL, FAST, 4>(p, pl.grid, pl.smem, st);
-    case 2: return launch_t<BITS, XD, CPL, FAST, 2>(p, pl.grid, pl.smem, st);
-    default: return launch_t<BITS, XD, CPL, FAST, 1>(p, pl.grid, pl.smem, st);
+  if constexpr (BATCH) {
+    return cudaLaunchKernelEx(&cfg, k, p, *batch);
+  } else {
+    GemvBatch<1> none{};
+    return cudaLaunchKernelEx(&cfg, k, p, none);
   }
 }
 
-template <int BITS, bt_dtype XD, bool FAST>
-cudaError_t launch_cpl(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
+template <int BITS, bt_dtype XD, int CPL, bool FAST, bool BATCH>
+cudaError_t launch_ri(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b, cudaStream_t st) {
+  switch (pl.ri) {
+    case 4: return launch_t<BITS, XD, CPL, FAST, 4, BATCH>(p, b, pl.grid, pl.smem, st);
+    case 2: return launch_t<BITS, XD, CPL, FAST, 2, BATCH>(p, b, pl.grid, pl.smem, st);
+    default: return launch_t<BITS, XD, CPL, FAST, 1, BATCH>(p, b, pl.grid, pl.smem, st);
+  }
+}
+
+template <int BITS, bt_dtype XD, bool FAST, bool BATCH>
+cudaError_t launch_cpl(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b, cudaStream_t st) {
   switch (pl.cpl) {
-    case 1: return launch_ri<BITS, XD, 1, FAST>(p, pl, st);
-    case 2: return launch_ri<BITS, XD, 2, FAST>(p, pl, st);
-    case 3: if constexpr (FAST) return launch_ri<BITS, XD, 3, FAST>(p, pl, st); else break;
-    case 4: if constexpr (FAST) return launch_ri<BITS, XD, 4, FAST>(p, pl, st); else break;
+    case 1: return launch_ri<BITS, XD, 1, FAST, BATCH>(p, pl, b, st);
+    case 2: return launch_ri<BITS, XD, 2, FAST, BATCH>(p, pl, b, st);
+    case 3: if constexpr (FAST) return launch_ri<BITS, XD, 3, FAST, BATCH>(p, pl, b, st); else break;
+    case 4: if constexpr (FAST) return launch_ri<BITS, XD, 4, FAST, BATCH>(p, pl, b, st); else break;
   }
   return cudaErrorInvalidValue;
 }
 
-template <int BITS>
-cudaError_t launch_bits(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
+template <int BITS, bool BATCH>
+cudaError_t launch_bits_b(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, const GemvBatch<kBatchCap>* b,
+                          cudaStream_t st) {
   constexpr bool kFastBits = (BITS == 2 || BITS == 4 || BITS == 8);
   if (xd == BT_F16) {
     if constexpr (kFastBits) {
-      if (pl.fast) return launch_cpl<BITS, BT_F16, true>(p, pl, st);
+      if (pl.fast) return launch_cpl<BITS, BT_F16, true, BATCH>(p, pl, b, st);
     }
-    return launch_cpl<BITS, BT_F16, false>(p, pl, st);
+    return launch_cpl<BITS, BT_F16, false, BATCH>(p, pl, b, st);
   }
-  return launch_cpl<BITS, BT_BF16, false>(p, pl, st);
+  return launch_cpl<BITS, BT_BF16, false, BATCH>(p, pl, b, st);
+}
+
+template <int BITS>
+cudaError_t launch_bits(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, const GemvBatch<kBatchCap>* b,
+                        cudaStream_t st) {
+  if (b) return launch_bits_b<BITS, true>(p, pl, xd, b, st);
+  return launch_bits_b<BITS, false>(p, pl, xd, nullptr, st);
 }
 
 }  // namespace gemv
 }  // namespace bt
 
-namespace bt {
-namespace gemv {
-
-// ---------------------------------------------------------------------------
-// Register-streaming variant: no shared-memory ring and no barriers on the
-// main path.  Each warp walks its rows in batches of RI; the packed codes and
-// the fp16 scale/bias of batch i+1 are loaded with 128-bit / 16-bit global
-// loads while batch i is being multiplied, so two batches of loads are in
-// flight per warp.
-template <int CPL> struct WarpsR {
-  static constexpr int kNW = 16;
-  static constexpr int kThreads = kNW * 32;
-};
-
-template <int BITS, bool FAST, int RI, int CPL>
-struct BatchRegs {
-  uint32_t w[CPL][RI][BITS];
-  uint16_t s[CPL][RI], b[CPL][RI];
-};
-
-template <int BITS, int RI, int CPL>
-__device__ __forceinline__ void load_batch(const GemvParams& p, const uint8_t* codes_row0, const uint16_t* sc_row0,
-                                           const uint16_t* bi_row0, int r0, int rows, int kw, int KW, int lane,
-                                           int nchunks, uint32_t (&w)[CPL][RI][BITS], uint16_t (&s)[CPL][RI],
-                                           uint16_t (&b)[CPL][RI]) {
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const int c = (i * KW + kw) * 32 + lane;
-#pragma unroll
-    for (int j = 0; j < RI; ++j) {
-      const int r = min(r0 + j, rows - 1);
-      if (c < nchunks && r >= 0) {
-        load_chunk<BITS, false>(0, codes_row0 + (size_t)r * p.row_bytes + c * (4 * BITS), w[i][j]);
-        s[i][j] = __ldg(sc_row0 + (size_t)r * p.G + (c >> 1));
-        b[i][j] = __ldg(bi_row0 + (size_t)r * p.G + (c >> 1));
-      }
-    }
-  }
-}
-
-template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
-__global__ void __launch_bounds__(WarpsR<CPL>::kThreads, 1) qgemv_reg_kernel(const GemvParams p) {
-  constexpr int kNW = WarpsR<CPL>::kNW;
-  __shared__ float red[kNW * 2 * RI];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KW = p.kw;
-  const int RW = kNW / KW;
-  if (KW < 1 || RW < 1 || RW * KW != kNW) {
-    if (threadIdx.x == 0) set_device_error(p.err, kErrBadArg);
-    return;
-  }
-  const int kw = warp % KW, rg = warp / KW;
-  const int nchunks = p.K / 32;
-  const bool writer = (lane & (32 / RI - 1)) == 0;
-  extern __shared__ int offs_dyn[];   // [E+1] when grouped
-  pdl_launch_dependents();
-  pdl_wait();
-  if (p.moe_offsets) {
-    for (int i = threadIdx.x; i <= p.num_experts; i += blockDim.x) offs_dyn[i] = __ldg(p.moe_offsets + i);
-    __syncthreads();
-  }
-
-  const long long U = p.num_units;
-  const long long u_begin = U * blockIdx.x / gridDim.x;
-  const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
-  const int RB = p.rows_per_unit;
-
-  XSlice<BITS, FAST> xs[CPL];
-  int cur_prob = -1, cur_expert = -1;
-  int rbuf = 0;
-  int prob = (int)(u_begin / p.units_per_problem);
-  int blk = (int)(u_begin - (long long)prob * p.units_per_problem) - 1;
-  for (long long u = u_begin; u < u_end; ++u) {
-    if (++blk == p.units_per_problem) { blk = 0; ++prob; }
-    if (prob != cur_prob) {
-      cur_prob = prob;
-      cur_expert = problem_expert(p, offs_dyn, prob);
-      const uint16_t* xb = static_cast<const uint16_t*>(p.x) + (size_t)problem_xrow(p, prob) * p.K;
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) {
-        const int c = (i * KW + kw) * 32 + lane;
-        if (c < nchunks) {
-          if constexpr (FAST) load_x_fast<BITS, XD>(xs[i], xb + (size_t)c * 32);
-          else load_x_generic<BITS, XD>(xs[i], xb + (size_t)c * 32);
-        }
-      }
-    }
-    if (cur_expert < 0) continue;
-    const int row0 = blk * RB;
-    const int rows = min(RB, p.N - row0);
-    const size_t wrow = (size_t)cur_expert * p.N + row0;
-    const uint8_t* g_codes = reinterpret_cast<const uint8_t*>(p.codes) + wrow * p.row_bytes;
-    const uint16_t* g_sc = p.scales + wrow * p.G;
-    const uint16_t* g_bi = p.biases + wrow * p.G;
-    const size_t ybase = (size_t)problem_yrow(p, prob) * p.N + row0;
-    const int nb = (rows + RI - 1) / RI;
-
-    uint32_t wA[CPL][RI][BITS], wB[CPL][RI][BITS];
-    uint16_t sA[CPL][RI], bA[CPL][RI], sB[CPL][RI], bB[CPL][RI];
-    int bi = rg;
-    if (bi < nb) load_batch<BITS, RI, CPL>(p, g_codes, g_sc, g_bi, bi * RI, rows, kw, KW, lane, nchunks, wA, sA, bA);
-    while (bi < nb) {
-      const int nbi = bi + RW;
-      if (nbi < nb) load_batch<BITS, RI, CPL>(p, g_codes, g_sc, g_bi, nbi * RI, rows, kw, KW, lane, nchunks, wB, sB, bB);
-      float part[RI];
-#pragma unroll
-      for (int j = 0; j < RI; ++j) part[j] = 0.f;
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) {
-        const int c = (i * KW + kw) * 32 + lane;
-        if (c < nchunks) {
-#pragma unroll
-          for (int j = 0; j < RI; ++j) {
-            float t;
-            if constexpr (FAST) t = chunk_dot_fast<BITS>(wA[i][j], xs[i]);
-            else t = chunk_dot_generic<BITS>(wA[i][j], xs[i]);
-            part[j] = fmaf(to_f32<BT_F16>(sA[i][j]), t, fmaf(to_f32<BT_F16>(bA[i][j]), xs[i].xsum, part[j]));
-          }
-        }
-      }
-      int rj;
-      const float v = reduce_rows<RI>(part, lane, rj);
-      const int r = bi * RI + rj;
-      if (KW == 1) {
-        if (writer && r < rows) store_y(p, ybase + r, v);
-      } else {
-        float* rb = red + (size_t)((rg * 2 + rbuf) * RI) * KW;
-        if (writer) rb[rj * KW + kw] = v;
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
-        if (kw == 0 && writer && r < rows) {
-          float acc = 0.f;
-          for (int j = 0; j < KW; ++j) acc += rb[rj * KW + j];
-          store_y(p, ybase + r, acc);
-        }
-        rbuf ^= 1;
-      }
-      // rotate the double buffer
-#pragma unroll
-      for (int i = 0; i < CPL; ++i)
-#pragma unroll
-        for (int j = 0; j < RI; ++j) {
-#pragma unroll
-          for (int t = 0; t < BITS; ++t) wA[i][j][t] = wB[i][j][t];
-          sA[i][j] = sB[i][j];
-          bA[i][j] = bB[i][j];
-        }
-      bi = nbi;
-    }
-  }
-}
-
-template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI>
-cudaError_t launch_reg_t(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
-  auto k = qgemv_reg_kernel<BITS, XD, CPL, FAST, RI>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(WarpsR<CPL>::kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, p);
-}
-
-template <int BITS, bt_dtype XD, int CPL, bool FAST>
-cudaError_t launch_reg_ri(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
-  switch (pl.ri) {
-    case 4: return launch_reg_t<BITS, XD, CPL, FAST, 4>(p, pl.grid, pl.smem, st);
-    case 2: return launch_reg_t<BITS, XD, CPL, FAST, 2>(p, pl.grid, pl.smem, st);
-    default: return launch_reg_t<BITS, XD, CPL, FAST, 1>(p, pl.grid, pl.smem, st);
-  }
-}
-
-template <int BITS, bt_dtype XD, bool FAST>
-cudaError_t launch_reg_cpl(const GemvParams& p, const GemvPlan& pl, cudaStream_t st) {
-  switch (pl.cpl) {
-    case 1: return launch_reg_ri<BITS, XD, 1, FAST>(p, pl, st);
-    case 2: return launch_reg_ri<BITS, XD, 2, FAST>(p, pl, st);
-  }
-  return cudaErrorInvalidValue;
-}
-
-template <int BITS>
-cudaError_t launch_reg_bits(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, cudaStream_t st) {
-  constexpr bool kFastBits = (BITS == 2 || BITS == 4 || BITS == 8);
-  if (xd == BT_F16) {
-    if constexpr (kFastBits) {
-      if (pl.fast) return launch_reg_cpl<BITS, BT_F16, true>(p, pl, st);
-    }
-    return launch_reg_cpl<BITS, BT_F16, false>(p, pl, st);
-  }
-  return launch_reg_cpl<BITS, BT_BF16, false>(p, pl, st);
-}
-
-}  // namespace gemv
-}  // namespace bt

@@ -79,6 +79,28 @@ BT_API bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const u
                    void* y, bt_dtype y_dtype, cudaStream_t stream);
 
 /*
+ * Batched dequant-GEMV: `count` independent M = 1 products in one launch, all
+ * with the same K, bits, group size and dtypes, each with its own weight, x, y
+ * and row count.  Persistent CTAs stream the problems' rows back to back, so a
+ * decode step's many small GEMVs cost one launch instead of one each (BaseRT
+ * pages, thetesserapress.com "Where the wins land": small models are
+ * dispatch-bound; gist.science "Contribuições": low-overhead dispatch).
+ *   problems  HOST array of `count` descriptors (read during the call only;
+ *             the pointers in it are device memory, 16-byte aligned)
+ * Limits: 1 <= count <= 192, 64 <= K <= 32768 (K <= 16384 for bf16 x or odd bits).
+ */
+typedef struct {
+  const uint32_t* codes;     /* [n, K*bits/32] */
+  const uint16_t* scales;    /* [n, K/g] fp16 */
+  const uint16_t* biases;    /* [n, K/g] fp16 */
+  const void* x;             /* [K] of x_dtype */
+  void* y;                   /* [n] of y_dtype */
+  int32_t n;                 /* rows, >= 1 */
+} bt_gemv_problem;
+BT_API bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size,
+                                  int K, bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream);
+
+/*
  * Dequant-GEMM, M > 1 (prefill): Y[m, n] = sum_k X[m, k] * w_deq[n, k].
  * BaseRT pages, thetesserapress.com "What BaseRT does differently" (GEMM for
  * prefill where M > 1) and gist.science "Metodologia" (tiled prefill GEMM on
@@ -186,7 +208,6 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMV_STAGES   tuning: GEMV pipeline depth (0 = heuristic, else 2..8).
  *   BT_OPT_GEMM_PATH     tuning: 0 = heuristic, 1 = CUDA-core tile,
  *                       2 = tensor-core tile where supported.
- *   BT_OPT_GEMV_KERNEL   tuning: 0 = shared-memory ring GEMV, 1 = register-streaming GEMV.
  *   BT_OPT_GEMM_SPLITS   tuning: tensor-core GEMM K split across a cluster (0 = heuristic, 1..8).
  */
 typedef enum {
@@ -197,8 +218,7 @@ typedef enum {
   BT_OPT_GEMV_GENERIC = 4,
   BT_OPT_GEMV_STAGES = 5,
   BT_OPT_GEMM_PATH = 6,
-  BT_OPT_GEMV_KERNEL = 7,
-  BT_OPT_GEMM_SPLITS = 8
+  BT_OPT_GEMM_SPLITS = 7
 } bt_option;
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);

@@ -142,3 +142,42 @@ def test_device_wait_timeout_is_reported(env):
     y = run(env, qw, x, "f16", "f32")
     y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]))
     assert_close(y, y_ref, a, "f32", "after timeout")
+
+
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("k,count", [(1024, 7), (2048, 3), (3072, 29), (1024, 192)])
+def test_qgemv_batched_matches_oracle(env, bits, k, count):
+    """Independent GEMVs of one K in a single launch, ragged row counts."""
+    torch, bt = env
+    from dequant_gemv_gemm_bt_b300 import synth
+    r = synth.rng_for("test", "batched", bits, k, count)
+    ns = [int(v) for v in r.integers(1, 700, count)]
+    ns[0] = 1
+    cases, probs = [], []
+    for i, n in enumerate(ns):
+        qw = synth.make_qweight(r, n, k, bits)
+        x16 = synth.draw_activations(r, 1, k, "f16")
+        codes, scales, biases = to_dev(qw, torch)
+        x = half_tensor(x16[0], "f16", torch)
+        y = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+        probs.append((codes, scales, biases, x, y))
+        cases.append((qw, x16))
+    bt.bt_qgemv_batched(probs, bits)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for (qw, x16), pr in zip(cases, probs):
+        y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x16[0]))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"batched b={bits} n={qw.n}")
+
+
+def test_qgemv_batched_rejects_bad_tables(env):
+    torch, bt = env
+    qw, x16 = make_case("batched-bad", 64, 1024, 4)
+    codes, scales, biases = to_dev(qw, torch)
+    x = half_tensor(x16[0], "f16", torch)
+    y = torch.empty(64, device="cuda")
+    with pytest.raises(bt.BTError):
+        bt.bt_qgemv_batched([(codes, scales, biases, x, y)] * 193, 4)      # over the table capacity
+    x2 = torch.zeros(2048, dtype=torch.float16, device="cuda")
+    with pytest.raises(ValueError):
+        bt.bt_qgemv_batched([(codes, scales, biases, x, y), (codes, scales, biases, x2, y)], 4)   # mixed K

@@ -59,17 +59,18 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   pl.row_bytes = row_bytes;
   const int stage = (rb * per_row + 127) / 128 * 128;
   pl.stage_bytes = stage;
-  int stages = std::max(2, std::min(8, kRingBudget / stage));
+  const int ctas_per_sm = pl.cpl == 1 ? 2 : 1;   // must match the kernel's launch bounds
+  int stages = std::max(2, std::min(8, (kRingBudget / ctas_per_sm) / stage));
   if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
   pl.stages = stages;
   pl.units_per_problem = (N + rb - 1) / rb;
   pl.num_units = (long long)pl.units_per_problem * problems;
-  pl.grid = (int)std::min<long long>(pl.num_units, (long long)sms);
+  pl.grid = (int)std::min<long long>(pl.num_units, (long long)sms * ctas_per_sm);
   auto smem_for = [&](int st) {
     return (size_t)st * stage + 2 * st * sizeof(uint64_t) + (size_t)nw * 2 * ri * sizeof(float) +
            (size_t)(num_experts + 1) * sizeof(int);
   };
-  while (pl.stages > 2 && smem_for(pl.stages) > kMaxSmem) --pl.stages;
+  while (pl.stages > 2 && smem_for(pl.stages) > kMaxSmem / ctas_per_sm) --pl.stages;
   pl.smem = smem_for(pl.stages);
   if (pl.smem > kMaxSmem) pl.feasible = false;
   return pl;
@@ -95,7 +96,7 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
     }
     p.num_units = u;
     plb.num_units = u;
-    plb.grid = (int)std::min<long long>(u, (long long)sm_count());
+    plb.grid = (int)std::min<long long>(u, (long long)sm_count() * (pl.cpl == 1 ? 2 : 1));
   }
   if (p.num_units == 0) return cudaSuccess;
   switch (bits) {

@@ -302,6 +302,8 @@ __device__ __forceinline__ int problem_yrow(const GemvParams& p, int prob) { ret
 template <int CPL> struct Warps {
   static constexpr int kNW = 8;
   static constexpr int kThreads = (kNW + 1) * 32;
+  // one x chunk per lane fits two CTAs per SM (16 consumer warps) within 112 registers
+  static constexpr int kMinBlocks = CPL == 1 ? 2 : 1;
 };
 
 // Sum RI per-row partials over the 32 lanes with a transpose-style tree.  On
@@ -422,7 +424,7 @@ __device__ __forceinline__ void first_unit(const GemvParams& p, const GemvBatch<
 }
 
 template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
-__global__ void __launch_bounds__(Warps<CPL>::kThreads, 1)
+__global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
     qgemv_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
   constexpr int kNW = Warps<CPL>::kNW;
   extern __shared__ __align__(128) uint8_t smem[];

@@ -251,7 +251,7 @@ bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint
     return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
   if (total_rows == 0) return BT_OK;
-  if (total_rows <= num_experts && opts().gemm_path != 1)
+  if (total_rows <= num_experts && opts().gemm_path == 0)
     return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, total_rows, expert_offsets,
                     x_row_index, num_experts, stream);
   GemmParams p{};
@@ -262,6 +262,8 @@ bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint
   p.num_experts = num_experts;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
+  if (opts().gemm_path != 1 && tc_supported(bits, K, total_rows, p))
+    return cuda_status(launch_gemm_tc_grouped(p, bits, x_dtype, y_dtype, stream));
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
 }
 

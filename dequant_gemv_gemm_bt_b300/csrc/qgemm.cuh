@@ -25,5 +25,6 @@ struct GemmParams {
 cudaError_t launch_gemm_simt(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
 bool tc_supported(int bits, int K, int M, const GemmParams& p);
 cudaError_t launch_gemm_tc(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
+cudaError_t launch_gemm_tc_grouped(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
 
 }  // namespace bt

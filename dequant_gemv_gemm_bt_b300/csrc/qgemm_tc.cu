@@ -21,6 +21,8 @@
 // once, with cp.async, before the main loop.  All waits are bounded.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "bt_common.cuh"
 #include "qgemm.cuh"
 
@@ -45,6 +47,11 @@ struct TcParams {
   bt_dtype y_dtype;
   unsigned* err;
   unsigned long long timeout_ns;
+  // grouped experts
+  const void* x;              // X base (grouped mode loads rows with cp.async)
+  const int32_t* offsets;     // [E+1] device
+  const int32_t* row_index;   // [total_rows] device or null
+  int num_experts;
 };
 
 // ------------------------------------------------------------------ PTX
@@ -53,6 +60,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -237,7 +253,7 @@ __device__ __forceinline__ void store_y(const TcParams& p, size_t i, float v) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BITS, bool BF16, int BN>
+template <int BITS, bool BF16, int BN, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                     const TcParams p) {
@@ -264,12 +280,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int n0 = blockIdx.x * BM;
-  const int m0 = blockIdx.y * BN;
+  int m0 = blockIdx.y * BN;     // first grouped/dense row of the tile
+  int m_end = p.M;              // one past its last valid row
+  int expert = 0;
   constexpr int kTmemCols = BN < 32 ? 32 : BN;
+
+  if constexpr (GROUPED) {
+    // Tile blockIdx.y of the expert-major list of (expert, BN-row tile) pairs;
+    // tiles past the end of the list exit before touching anything.
+    __shared__ int s_tile[3];
+    pdl_wait();   // offsets come from the routing kernel
+    if (threadIdx.x < 32) {
+      const int E = p.num_experts;
+      int base = 0, found = -1;
+      for (int e0 = 0; e0 < E && found < 0; e0 += 32) {
+        const int e = e0 + (int)threadIdx.x;
+        int cnt = 0, lo = 0;
+        if (e < E) {
+          lo = max(0, __ldg(p.offsets + e));
+          cnt = max(0, min(__ldg(p.offsets + e + 1), p.M) - lo);
+        }
+        const int tiles = (cnt + BN - 1) / BN;
+        int incl = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (threadIdx.x >= (unsigned)o) incl += v;
+        }
+        const int excl = base + incl - tiles;
+        const bool mine = tiles > 0 && (int)blockIdx.y >= excl && (int)blockIdx.y < excl + tiles;
+        const unsigned hit = __ballot_sync(0xffffffffu, mine);
+        if (hit) {
+          found = 0;
+          if (mine) {
+            s_tile[0] = e;
+            s_tile[1] = lo + ((int)blockIdx.y - excl) * BN;
+            s_tile[2] = lo + cnt;
+          }
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (threadIdx.x == 0 && found < 0) s_tile[0] = -1;
+    }
+    __syncthreads();
+    if (s_tile[0] < 0) return;
+    expert = s_tile[0];
+    m0 = s_tile[1];
+    m_end = s_tile[2];
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], GROUPED ? 33 : 1);
       mbar_init(&afull[s], kDeqWarps);
       mbar_init(&empty[s], 1);
     }
@@ -292,25 +354,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      pdl_wait();
+    if constexpr (!GROUPED) {
+      if (lane == 0) {
+        pdl_wait();
+        int s = 0;
+        uint32_t ph = 0;
+        int issued = 0;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err)) { *fail = 1; break; }
+          if (*fail) break;
+          uint8_t* st = smem + (size_t)s * p.stage_bytes;
+          mbar_arrive_expect_tx(&full[s], p.c_bytes + p.x_bytes);
+          const int g = kb_lo + kb;
+          tma_load_2d(st + p.a_bytes + p.x_bytes, &map_codes, g * (8 * BITS), n0, &full[s]);
+          tma_load_2d(st + p.a_bytes, &map_x, g * BK, m0, &full[s]);
+          ++issued;
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+        if (*fail) {   // let copies in flight land before shared memory is released
+          for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+            mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), p.timeout_ns, p.err);
+        }
+      }
+    } else {
+      // codes: one 3-D TMA box per stage (expert plane); X: the tile's rows,
+      // gathered with 16-byte cp.async straight into the swizzled layout
+      const uint16_t* xg = static_cast<const uint16_t*>(p.x);
       int s = 0;
       uint32_t ph = 0;
       int issued = 0;
+      bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
-        if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err)) { *fail = 1; break; }
-        if (*fail) break;
+        if (kb >= S) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
+          if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; break; }
+        }
         uint8_t* st = smem + (size_t)s * p.stage_bytes;
-        mbar_arrive_expect_tx(&full[s], p.c_bytes + p.x_bytes);
         const int g = kb_lo + kb;
-        tma_load_2d(st + p.a_bytes + p.x_bytes, &map_codes, g * (8 * BITS), n0, &full[s]);
-        tma_load_2d(st + p.a_bytes, &map_x, g * BK, m0, &full[s]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], p.c_bytes);
+          tma_load_3d(st + p.a_bytes + p.x_bytes, &map_codes, g * (8 * BITS), n0, expert, &full[s]);
+        }
+        for (int i = lane; i < BN * 8; i += 32) {
+          const int row = i >> 3, ch = i & 7;
+          const int gr = m0 + row;
+          uint8_t* dst = st + p.a_bytes + row * 128 + ((ch ^ (row & 7)) << 4);
+          if (gr < m_end) {
+            const int src = p.row_index ? __ldg(p.row_index + gr) : gr;
+            cp_async16(dst, xg + (size_t)src * p.K + (size_t)g * BK + ch * 8);
+          } else {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        cp_async_mbar_arrive_noinc(&full[s]);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
       }
-      if (*fail) {   // let copies in flight land before shared memory is released
-        for (int j = issued > S ? issued - S : 0; j < issued; ++j)
-          mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), p.timeout_ns, p.err);
+      if (!ok) {
+        *fail = 1;
+        cp_async_wait_all();
+        if (lane == 0)
+          for (int j = issued > S ? issued - S : 0; j < issued; ++j)
+            mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), p.timeout_ns, p.err);
       }
     }
   } else if (warp == 1) {
@@ -325,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        fence_proxy_async();   // X rows written by cp.async / zero fill are read by the tensor core
         const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
         const uint64_t adesc = sw128_desc(st);
         const uint64_t bdesc = sw128_desc(st + p.a_bytes);
@@ -345,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rr = i / (Gc / 2), gg = 2 * (i % (Gc / 2));
       const int n = n0 + rr;
       if (n < p.N) {
-        const size_t off = (size_t)n * p.G + kb_lo + gg;
+        const size_t off = ((size_t)expert * p.N + n) * p.G + kb_lo + gg;
         cp_async4(sS + rr * Gc + gg, p.scales + off);
         cp_async4(sB + rr * Gc + gg, p.biases + off);
       } else {
@@ -410,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
-            if (m < p.M) store_y(p, (size_t)m * p.N + n, __uint_as_float(v[j]));
+            if (m < m_end) store_y(p, (size_t)m * p.N + n, __uint_as_float(v[j]));
           }
         }
       }
@@ -455,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = m0 + chunk * 16 + j;
-          if (m < p.M) store_y(p, (size_t)m * p.N + n, acc[j]);
+          if (m < m_end) store_y(p, (size_t)m * p.N + n, acc[j]);
         }
       }
     }
@@ -488,13 +595,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int BITS, bool BF16, int BN>
+template <int BITS, bool BF16, int BN, bool GROUPED = false>
 cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStream_t st) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int row_bytes = gp.K * BITS / 8;
   CUtensorMap mc, mx;
-  {
+  memset(&mx, 0, sizeof(mx));
+  if constexpr (GROUPED) {
+    cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)gp.N, (cuuint64_t)gp.num_experts};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)row_bytes * gp.N};
+    cuuint32_t box[3] = {(cuuint32_t)(8 * BITS), (cuuint32_t)BM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint32_t*>(gp.codes), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else {
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)gp.N};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
     cuuint32_t box[2] = {(cuuint32_t)(8 * BITS), (cuuint32_t)BM};
@@ -504,7 +621,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {
+  if constexpr (!GROUPED) {
     cuuint64_t dims[2] = {(cuuint64_t)gp.K, (cuuint64_t)gp.M};
     cuuint64_t strides[1] = {(cuuint64_t)gp.K * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
@@ -540,6 +657,10 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.y_dtype = yd;
   p.err = gp.err;
   p.timeout_ns = gp.timeout_ns;
+  p.x = gp.x;
+  p.offsets = gp.offsets;
+  p.row_index = gp.row_index;
+  p.num_experts = gp.num_experts;
   const size_t params_bytes = (size_t)2 * BM * p.gc_max * sizeof(uint16_t);
   const size_t fixed = 1024 + params_bytes + 8 + (size_t)(3 * 8 + 1) * 8 + 16;
   int stages = (int)((size_t)(220 * 1024 - fixed) / p.stage_bytes);
@@ -551,11 +672,15 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.stages = stages;
   const size_t smem = fixed + (size_t)stages * p.stage_bytes;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto k = qgemm_tc_kernel<BITS, BF16, BN>;
+  auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((gp.N + BM - 1) / BM, (gp.M + BN - 1) / BN, splits);
+  // grouped: an upper bound on the (expert, tile) list, sum over experts of ceil(rows / BN)
+  const long long ytiles = GROUPED ? (long long)(gp.M + BN - 1) / BN + std::min(gp.num_experts, gp.M)
+                                   : (gp.M + BN - 1) / BN;
+  if (ytiles > 65535) return cudaErrorInvalidValue;
+  cfg.gridDim = dim3((gp.N + BM - 1) / BM, (unsigned)ytiles, splits);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -587,7 +712,41 @@ cudaError_t launch_tc_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int b
   return launch_tc_bn<BITS, false>(gp, yd, bn, splits, st);
 }
 
+
+template <int BITS, bool BF16>
+cudaError_t launch_tc_grouped_bn(const GemmParams& gp, bt_dtype yd, int bn, cudaStream_t st) {
+  switch (bn) {
+    case 16: return launch_tc_t<BITS, BF16, 16, true>(gp, yd, 1, st);
+    case 32: return launch_tc_t<BITS, BF16, 32, true>(gp, yd, 1, st);
+    case 64: return launch_tc_t<BITS, BF16, 64, true>(gp, yd, 1, st);
+    default: return launch_tc_t<BITS, BF16, 128, true>(gp, yd, 1, st);
+  }
+}
+
+template <int BITS>
+cudaError_t launch_tc_grouped_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int bn, cudaStream_t st) {
+  if (xd == BT_BF16) return launch_tc_grouped_bn<BITS, true>(gp, yd, bn, st);
+  return launch_tc_grouped_bn<BITS, false>(gp, yd, bn, st);
+}
+
 }  // namespace tc
+
+// Grouped experts: token tiles sized to the mean rows per expert (the MMA's N
+// runs 16..128), one CTA per (expert, 128 weight rows, token tile).
+cudaError_t launch_gemm_tc_grouped(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
+  const int avg = (gp.M + gp.num_experts - 1) / gp.num_experts;
+  int bn = 128;
+  if (avg <= 16) bn = 16;
+  else if (avg <= 32) bn = 32;
+  else if (avg <= 64) bn = 64;
+  switch (bits) {
+    case 2: return tc::launch_tc_grouped_bits<2>(gp, xd, yd, bn, st);
+    case 4: return tc::launch_tc_grouped_bits<4>(gp, xd, yd, bn, st);
+    case 6: return tc::launch_tc_grouped_bits<6>(gp, xd, yd, bn, st);
+    default: return tc::launch_tc_grouped_bits<8>(gp, xd, yd, bn, st);
+  }
+}
+
 
 bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
   if (!(bits == 2 || bits == 4 || bits == 6 || bits == 8)) return false;
@@ -595,7 +754,6 @@ bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
   if (G % 2) return false;                          // 4-byte cp.async of scale pairs
   if (G > 192) return false;                        // the CTA's scales/biases are staged whole in shared memory
   if (((size_t)K * bits / 8) % 16) return false;    // TMA row stride
-  if (gp.offsets) return false;                     // grouped experts: CUDA-core tile for now
   if ((reinterpret_cast<uintptr_t>(gp.x) & 15) || (reinterpret_cast<uintptr_t>(gp.codes) & 15)) return false;
   (void)M;
   return true;

@@ -11,8 +11,9 @@ Weights are synthetic (seeded N(0, 0.02), min/max-quantized); they exceed the
 
 Metric: weight GB/s (codes + scales + biases per pass / pass time), the
 BaseRT pages' decode-bandwidth view ("memory traffic scales with the
-compression ratio").  With --prefill, the Llama-3.2-3B-shaped prefill GEMM
-pass (M = 128 and 512) is also timed and reported in TFLOP/s.
+compression ratio").  The same run also times the Llama-3.2-3B-shaped prefill
+GEMM pass (M = 128 and 512, TFLOP/s, key "prefill") and the Qwen3-30B-A3B-
+shaped MoE layer (M = 1 and 128, key "moe"); --legs selects them.
 
 ``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
 workload (the only other code path of this workload).  Under torchrun each
@@ -252,6 +253,178 @@ def timed(torch, dist, stream, fn, steps, warmup, gpu_index):
     return ms / 1e3, clk.summary()
 
 
+def pack_rows(ws):
+    """Concatenate packed weights along N (row-major layout: row slices stay contiguous)."""
+    return synth.QuantWeight(np.concatenate([w.codes for w in ws]), np.concatenate([w.scales for w in ws]),
+                             np.concatenate([w.biases for w in ws]), ws[0].bits, sum(w.n for w in ws), ws[0].k)
+
+
+def to_dev_w(torch, qw, dev):
+    return (torch.from_numpy(qw.codes.view(np.int32)).to(dev), torch.from_numpy(qw.scales.view(np.float16)).to(dev),
+            torch.from_numpy(qw.biases.view(np.float16)).to(dev))
+
+
+def run_prefill(torch, bt, dev, stream, steps, warmup, gpu_index, peaks):
+    """Llama-3.2-3B-shaped prefill pass, Q4, bf16 X and Y, M = 128 and 512.
+
+    Per layer the weights are stored as the runtime would keep them: q|k|v
+    concatenated (N = 5120) and gate|up concatenated (N = 16384), plus o and
+    down.  The "fused" pass runs 4 GEMMs per layer (q, k, v share X; gate, up
+    share X); the "unfused" pass runs the 7 projections separately on row
+    slices of the same weights.  FLOPs are identical: 2*M*sum(N*K).
+    """
+    bits = 4
+    shapes = prefill_pass_shapes()
+    t0 = time.time()
+    ws = gen_weights("prefill-pass", shapes, bits)
+    gen_s = time.time() - t0
+    per_layer = len(LLAMA3B_LAYER)
+    layers = []
+    for l in range(LLAMA3B_LAYERS):
+        q, k, v, o, g, u, d = ws[l * per_layer:(l + 1) * per_layer]
+        layers.append({"qkv": to_dev_w(torch, pack_rows([q, k, v]), dev), "o": to_dev_w(torch, o, dev),
+                       "gu": to_dev_w(torch, pack_rows([g, u]), dev), "down": to_dev_w(torch, d, dev)})
+    del ws
+    flops_per_token = 2 * sum(n * k for _, n, k in shapes)
+    wbytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
+    out = {"workload": "Llama-3.2-3B-shaped prefill pass: 28 layers x (q 3072->3072, k/v 3072->1024, o 3072->3072, "
+                       "gate/up 3072->8192, down 8192->3072), Q4 g64, bf16 X/Y, fp32 accumulate",
+           "weight_bytes_per_pass": wbytes, "weight_gen_s": round(gen_s, 1)}
+    sustained = float(peaks.get("bf16_tflops_sustained", 1400.0))
+    burst = float(peaks.get("bf16_tflops", 1800.0))
+    for m in (128, 512):
+        xs = [torch.randn(m, 3072, device=dev).bfloat16() for _ in range(3)]
+        xd = torch.randn(m, 8192, device=dev).bfloat16()
+        y_qkv = torch.empty(m, 5120, device=dev, dtype=torch.bfloat16)
+        y_o = torch.empty(m, 3072, device=dev, dtype=torch.bfloat16)
+        y_gu = torch.empty(m, 16384, device=dev, dtype=torch.bfloat16)
+        y_d = torch.empty(m, 3072, device=dev, dtype=torch.bfloat16)
+
+        def fused():
+            for L in layers:
+                bt.bt_qgemm(*L["qkv"], bits, xs[0], y_qkv)
+                bt.bt_qgemm(*L["o"], bits, xs[1], y_o)
+                bt.bt_qgemm(*L["gu"], bits, xs[2], y_gu)
+                bt.bt_qgemm(*L["down"], bits, xd, y_d)
+
+        ys = {nm: torch.empty(m, n, device=dev, dtype=torch.bfloat16) for nm, n, _ in LLAMA3B_LAYER}
+        rows = {"q": ("qkv", 0, 3072), "k": ("qkv", 3072, 4096), "v": ("qkv", 4096, 5120),
+                "gate": ("gu", 0, 8192), "up": ("gu", 8192, 16384)}
+
+        def unfused():
+            for L in layers:
+                for nm, n, kk in LLAMA3B_LAYER:
+                    if nm in rows:
+                        key, a, b = rows[nm]
+                        c, sc, bi = L[key]
+                        w = (c[a:b], sc[a:b], bi[a:b])
+                    else:
+                        w = L["o" if nm == "o" else "down"]
+                    x = xd if nm == "down" else xs[0 if nm in ("q", "k", "v") else (1 if nm == "o" else 2)]
+                    bt.bt_qgemm(*w, bits, x, ys[nm])
+
+        res = {}
+        for tag, fn, launches in (("fused", fused, 4 * LLAMA3B_LAYERS), ("unfused", unfused, 7 * LLAMA3B_LAYERS)):
+            g = capture(torch, fn, stream)
+            n_steps = max(3, min(steps, 50))
+            with torch.cuda.stream(stream):
+                t, clk = timed(torch, None, stream, lambda: g.replay(), n_steps, max(3, min(warmup, 5)), gpu_index)
+            tfl = flops_per_token * m * n_steps / t / 1e12
+            res[tag] = {"tflops": round(tfl, 1), "ms_per_pass": round(t / n_steps * 1e3, 3), "launches_per_pass": launches,
+                        "frac_of_sustained_bf16": round(tfl / sustained, 4), "frac_of_burst_bf16": round(tfl / burst, 4),
+                        "clocks": clk}
+            del g
+        out[f"M{m}"] = res
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error in the prefill leg")
+    return out
+
+
+def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
+    """Qwen3-30B-A3B-shaped expert layer, Q4: route -> gate|up (grouped, gathered rows) -> SwiGLU ->
+    down (grouped) -> gate-weighted combine, at M = 1 (decode) and M = 128 (prefill).
+
+    Each timed step uses a fresh routing draw (cycled from 16 seeded draws) and
+    L2 is flushed between steps (a 256 MB write outside the timed events), so
+    expert weights come from HBM.  GB/s counts the packed bytes of the experts
+    the step's routing touches.
+    """
+    bits, E, H, I, top_k = 4, 128, 2048, 768, 8
+    t0 = time.time()
+    gu_w = gen_weights("moe-layer-gu", [(f"e{e}", 2 * I, H) for e in range(E)], bits)
+    dn_w = gen_weights("moe-layer-down", [(f"e{e}", H, I) for e in range(E)], bits)
+    gen_s = time.time() - t0
+
+    def stack(ws):
+        return (torch.from_numpy(np.stack([w.codes for w in ws]).view(np.int32)).to(dev),
+                torch.from_numpy(np.stack([w.scales for w in ws]).view(np.float16)).to(dev),
+                torch.from_numpy(np.stack([w.biases for w in ws]).view(np.float16)).to(dev))
+    GU, DN = stack(gu_w), stack(dn_w)
+    per_expert = weight_bytes(2 * I, H, bits) + weight_bytes(H, I, bits)
+    del gu_w, dn_w
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    out = {"workload": "Qwen3-30B-A3B-shaped MoE layer: hidden 2048, 128 experts, gate/up 2048->768 (stored as one "
+                       "1536-row matrix), down 768->2048, top-8, Q4 g64", "weight_gen_s": round(gen_s, 1)}
+    for tokens in (1, 128):
+        xdt = torch.float16 if tokens == 1 else torch.bfloat16
+        draws = []
+        for i in range(16):
+            r = synth.rng_for("moe-layer", tokens, i)
+            ids, gates = synth.draw_routing(r, tokens, E, top_k)
+            x = torch.randn(tokens, H, device=dev).to(xdt)
+            ids_t = torch.from_numpy(ids).to(dev)
+            gates_t = torch.from_numpy(gates).to(dev)
+            touched = len(set(ids.reshape(-1).tolist()))
+            bufs = dict(off=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                        pidx=torch.empty(tokens * top_k, dtype=torch.int32, device=dev),
+                        prow=torch.empty(tokens * top_k, dtype=torch.int32, device=dev),
+                        rowi=torch.empty(tokens * top_k, dtype=torch.int32, device=dev),
+                        ygu=torch.empty(tokens * top_k, 2 * I, device=dev, dtype=xdt),
+                        h=torch.empty(tokens * top_k, I, device=dev, dtype=xdt),
+                        yd=torch.empty(tokens * top_k, H, device=dev, dtype=xdt),
+                        out=torch.empty(tokens, H, device=dev, dtype=torch.float32))
+            draws.append((ids_t, gates_t, x, bufs, touched))
+
+        def layer(d):
+            ids_t, gates_t, x, b, _ = d
+            bt.bt_moe_route(ids_t, E, b["off"], b["pidx"], b["prow"])
+            torch.floor_divide(b["pidx"], top_k, out=b["rowi"])
+            bt.bt_moe_qgemm(*GU, bits, b["off"], x, b["ygu"], x_row_index=b["rowi"])
+            bt.bt_swiglu(b["ygu"], b["h"])
+            bt.bt_moe_qgemm(*DN, bits, b["off"], b["h"], b["yd"])
+            bt.bt_moe_combine(b["yd"], gates_t, b["prow"], top_k, b["out"])
+
+        graphs = [capture(torch, lambda d=d: layer(d), stream) for d in draws]
+        n_steps = max(3, min(steps, 100))
+        times = []
+        touched_bytes = 0
+        with torch.cuda.stream(stream):
+            for i in range(max(3, min(warmup, 5))):
+                graphs[i % len(graphs)].replay()
+            torch.cuda.synchronize()
+            with ClockSampler(gpu_index) as clk:
+                for i in range(n_steps):
+                    flush.fill_(float(i))
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    graphs[i % len(graphs)].replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1) / 1e3)
+                    touched_bytes += draws[i % len(draws)][4] * per_expert
+        t = sum(times)
+        gbs = touched_bytes / t / 1e9
+        flops = 2 * tokens * top_k * (2 * I * H + H * I)
+        out[f"M{tokens}"] = {"us_per_layer": round(t / n_steps * 1e6, 2), "weight_gbs": round(gbs, 1),
+                             "frac_of_hbm": round(gbs / hbm, 4), "tflops": round(flops * n_steps / t / 1e12, 3),
+                             "experts_touched_mean": round(touched_bytes / n_steps / per_expert, 2),
+                             "launches_per_layer": 6, "clocks": clk.summary()}
+        del graphs
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error in the MoE leg")
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -259,6 +432,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--legs", default="decode,prefill,moe",
+                    help="comma list of legs to run: decode (headline), prefill, moe")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -447,6 +622,11 @@ def main():
         "lm_head_gemv": {"gbs": round(lm_gbs, 1), "frac_of_hbm": round(lm_gbs / hbm, 4),
                          "shape": "N=151936 K=1024 Q4", "bytes": lm_bytes},
     }
+    legs = set(args.legs.split(","))
+    if "prefill" in legs:
+        out["prefill"] = run_prefill(torch, bt, dev, stream, args.steps, args.warmup, local_rank, peaks)
+    if "moe" in legs:
+        out["moe"] = run_moe(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
     if rank == 0:
         print(json.dumps(out))
     if dist is not None:

@@ -130,6 +130,28 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void lds128(uint32_t a, uint32_t& x, uint32_t& y, uint32_t& z, uint32_t& w) {
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "r"(a));
+}
+__device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -462,25 +484,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cp_async_wait_all();
     asm volatile("bar.sync 1, %0;" ::"r"(kDeqWarps * 32) : "memory");
+    const uint32_t sS_a = smem_u32(sS), sB_a = smem_u32(sB);
 
     int s = 0;
     uint32_t ph = 0;
     for (int kb = 0; kb < KB; ++kb) {
       if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) { *fail = 1; break; }
-      uint8_t* st = smem + (size_t)s * p.stage_bytes;
-      const uint32_t* codes = reinterpret_cast<const uint32_t*>(st + p.a_bytes + p.x_bytes + r * (8 * BITS) + h * (4 * BITS));
+      const uint32_t st = smem_u32(smem) + (uint32_t)(s * p.stage_bytes);
+      const uint32_t caddr = st + p.a_bytes + p.x_bytes + r * (8 * BITS) + h * (4 * BITS);
       uint32_t w[BITS];
+      if constexpr (BITS == 4) {
+        lds128(caddr, w[0], w[1], w[2], w[3]);
+      } else if constexpr (BITS == 8) {
+        lds128(caddr, w[0], w[1], w[2], w[3]);
+        lds128(caddr + 16, w[4], w[5], w[6], w[7]);
+      } else {
 #pragma unroll
-      for (int i = 0; i < BITS; ++i) w[i] = codes[i];
-      const uint32_t s2 = half_pair<BF16>(sS[r * Gc + kb]);
-      const uint32_t b2 = half_pair<BF16>(sB[r * Gc + kb]);
+        for (int i = 0; i < BITS; ++i) w[i] = lds32(caddr + 4 * i);
+      }
+      const uint32_t s2 = half_pair<BF16>(lds16(sS_a + (uint32_t)(r * Gc + kb) * 2));
+      const uint32_t b2 = half_pair<BF16>(lds16(sB_a + (uint32_t)(r * Gc + kb) * 2));
       uint4 out[4];
       deq32<BITS, BF16>(w, s2, b2, out);
-      uint8_t* arow = st + r * 128;
+      const uint32_t arow = st + r * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int chunk = 4 * h + c;
-        *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = out[c];
+        sts128(arow + ((chunk ^ (r & 7)) << 4), out[c]);
       }
       fence_proxy_async();
       __syncwarp();
@@ -552,10 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[j] = 0.f;
         for (int sdr = 0; sdr < R; ++sdr) {
-          const float4* src = reinterpret_cast<const float4*>(recv + (((size_t)(sdr * BM) + row) * owned_max + slot) * 16);
+          const uint32_t src = recv_s + (uint32_t)((((sdr * BM) + row) * owned_max + slot) * 16 * 4);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float4 f = src[j];
+            const float4 f = lds128f(src + 16 * j);
             acc[4 * j] += f.x; acc[4 * j + 1] += f.y; acc[4 * j + 2] += f.z; acc[4 * j + 3] += f.w;
           }
         }

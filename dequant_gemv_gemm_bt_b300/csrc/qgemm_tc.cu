@@ -38,9 +38,10 @@ struct TcParams {
   int M, N, K, G;          // G = K / 64
   int splits;              // CTAs of a cluster splitting K (gridDim.z); 1 = no split
   int gc_max;              // most groups any split stages
-  int stages;
+  int stages;              // TMA ring depth (X tile + packed codes per K block)
+  int astages;             // A ring depth (dequantized weight tile per K block)
   int bn;
-  uint32_t stage_bytes, a_bytes, x_bytes, c_bytes;
+  uint32_t stage_bytes, a_bytes, x_bytes, c_bytes;   // stage_bytes: one TMA-ring slot
   const uint16_t* scales;
   const uint16_t* biases;
   void* y;
@@ -290,15 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb_hi = split == p.splits - 1 ? p.G : (((split + 1) * p.G) / p.splits) & ~1;
   const int KB = kb_hi - kb_lo;
   const int Gc = KB;                       // groups staged for this CTA
-  uint16_t* sS = reinterpret_cast<uint16_t*>(smem + (size_t)S * p.stage_bytes);   // [128][Gc]
+  // shared memory: [A ring: SA x 16 KB][TMA ring: S x (X tile | codes)][scales][biases][barriers]
+  const int SA = p.astages;
+  uint8_t* aring = smem;
+  uint8_t* tring = smem + (size_t)SA * p.a_bytes;
+  uint16_t* sS = reinterpret_cast<uint16_t*>(tring + (size_t)S * p.stage_bytes);  // [128][Gc]
   uint16_t* sB = sS + BM * p.gc_max;                                               // [128][Gc]
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(sB + BM * p.gc_max) + 7) & ~uintptr_t(7));
-  uint64_t* full = bars;             // [S] TMA landed (codes + X)
-  uint64_t* afull = bars + S;        // [S] A tile written
-  uint64_t* empty = bars + 2 * S;    // [S] MMAs of the stage done
-  uint64_t* tmem_full = bars + 3 * S;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 3 * S + 1);
+  uint64_t* full = bars;             // [S] X + codes landed
+  uint64_t* empty = bars + S;        // [S] MMAs reading the slot's X done
+  uint64_t* afull = bars + 2 * S;    // [SA] A tile written
+  uint64_t* aempty = afull + SA;     // [SA] MMAs reading the A tile done
+  uint64_t* tmem_full = aempty + SA;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tmem_full + 1);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int n0 = blockIdx.x * BM;
@@ -354,8 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], GROUPED ? 33 : 1);
-      mbar_init(&afull[s], kDeqWarps);
       mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < SA; ++a) {
+      mbar_init(&afull[a], kDeqWarps);
+      mbar_init(&aempty[a], 1);
     }
     mbar_init(tmem_full, 1);
     *fail = 0;
@@ -385,11 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < KB; ++kb) {
           if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err)) { *fail = 1; break; }
           if (*fail) break;
-          uint8_t* st = smem + (size_t)s * p.stage_bytes;
+          uint8_t* st = tring + (size_t)s * p.stage_bytes;
           mbar_arrive_expect_tx(&full[s], p.c_bytes + p.x_bytes);
           const int g = kb_lo + kb;
-          tma_load_2d(st + p.a_bytes + p.x_bytes, &map_codes, g * (8 * BITS), n0, &full[s]);
-          tma_load_2d(st + p.a_bytes, &map_x, g * BK, m0, &full[s]);
+          tma_load_2d(st + p.x_bytes, &map_codes, g * (8 * BITS), n0, &full[s]);
+          tma_load_2d(st, &map_x, g * BK, m0, &full[s]);
           ++issued;
           if (++s == S) { s = 0; ph ^= 1u; }
         }
@@ -412,16 +421,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
           if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; break; }
         }
-        uint8_t* st = smem + (size_t)s * p.stage_bytes;
+        uint8_t* st = tring + (size_t)s * p.stage_bytes;
         const int g = kb_lo + kb;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[s], p.c_bytes);
-          tma_load_3d(st + p.a_bytes + p.x_bytes, &map_codes, g * (8 * BITS), n0, expert, &full[s]);
+          tma_load_3d(st + p.x_bytes, &map_codes, g * (8 * BITS), n0, expert, &full[s]);
         }
         for (int i = lane; i < BN * 8; i += 32) {
           const int row = i >> 3, ch = i & 7;
           const int gr = m0 + row;
-          uint8_t* dst = st + p.a_bytes + row * 128 + ((ch ^ (row & 7)) << 4);
+          uint8_t* dst = st + row * 128 + ((ch ^ (row & 7)) << 4);
           if (gr < m_end) {
             const int src = p.row_index ? __ldg(p.row_index + gr) : gr;
             cp_async16(dst, xg + (size_t)src * p.K + (size_t)g * BK + ch * 8);
@@ -445,23 +454,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(BF16, BN);
-      int s = 0;
-      uint32_t ph = 0;
+      int s = 0, a = 0;
+      uint32_t ph = 0, aph = 0;
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err) || !mbar_wait(&afull[s], ph, p.timeout_ns, p.err)) {
+        if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err) || !mbar_wait(&afull[a], aph, p.timeout_ns, p.err)) {
           *fail = 1;
           break;
         }
         tc_fence_after();
         fence_proxy_async();   // X rows written by cp.async / zero fill are read by the tensor core
-        const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
-        const uint64_t adesc = sw128_desc(st);
-        const uint64_t bdesc = sw128_desc(st + p.a_bytes);
+        const uint64_t adesc = sw128_desc(smem_u32(aring) + (uint32_t)(a * p.a_bytes));
+        const uint64_t bdesc = sw128_desc(smem_u32(tring) + (uint32_t)(s * p.stage_bytes));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)   // 16 elements = 32 bytes per MMA step
           mma_f16(tmem_base, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
         mma_commit(&empty[s]);
+        mma_commit(&aempty[a]);
         if (++s == S) { s = 0; ph ^= 1u; }
+        if (++a == SA) { a = 0; aph ^= 1u; }
       }
       mma_commit(tmem_full);   // arrives once every MMA issued above has completed
     }
@@ -486,12 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("bar.sync 1, %0;" ::"r"(kDeqWarps * 32) : "memory");
     const uint32_t sS_a = smem_u32(sS), sB_a = smem_u32(sB);
 
-    int s = 0;
-    uint32_t ph = 0;
+    int s = 0, a = 0;
+    uint32_t ph = 0, aph = 0;
     for (int kb = 0; kb < KB; ++kb) {
       if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) { *fail = 1; break; }
-      const uint32_t st = smem_u32(smem) + (uint32_t)(s * p.stage_bytes);
-      const uint32_t caddr = st + p.a_bytes + p.x_bytes + r * (8 * BITS) + h * (4 * BITS);
+      if (kb >= SA && !mbar_wait(&aempty[a], aph ^ 1u, p.timeout_ns, p.err)) { *fail = 1; break; }
+      const uint32_t st = smem_u32(tring) + (uint32_t)(s * p.stage_bytes);
+      const uint32_t caddr = st + p.x_bytes + r * (8 * BITS) + h * (4 * BITS);
       uint32_t w[BITS];
       if constexpr (BITS == 4) {
         lds128(caddr, w[0], w[1], w[2], w[3]);
@@ -506,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b2 = half_pair<BF16>(lds16(sB_a + (uint32_t)(r * Gc + kb) * 2));
       uint4 out[4];
       deq32<BITS, BF16>(w, s2, b2, out);
-      const uint32_t arow = st + r * 128;
+      const uint32_t arow = smem_u32(aring) + (uint32_t)(a * p.a_bytes) + r * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int chunk = 4 * h + c;
@@ -514,8 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[s]);
+      if (lane == 0) mbar_arrive(&afull[a]);
       if (++s == S) { s = 0; ph ^= 1u; }
+      if (++a == SA) { a = 0; aph ^= 1u; }
     }
 
   }
@@ -680,7 +692,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.a_bytes = BM * BK * 2;
   p.x_bytes = BN * BK * 2;
   p.c_bytes = BM * 8 * BITS;
-  p.stage_bytes = (p.a_bytes + p.x_bytes + p.c_bytes + 1023u) & ~1023u;
+  p.stage_bytes = (p.x_bytes + p.c_bytes + 1023u) & ~1023u;
   p.scales = gp.scales;
   p.biases = gp.biases;
   p.y = gp.y;
@@ -692,13 +704,17 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.row_index = gp.row_index;
   p.num_experts = gp.num_experts;
   const size_t params_bytes = (size_t)2 * BM * p.gc_max * sizeof(uint16_t);
-  const size_t fixed = 1024 + params_bytes + 8 + (size_t)(3 * 8 + 1) * 8 + 16;
-  int stages = (int)((size_t)(220 * 1024 - fixed) / p.stage_bytes);
-  stages = std::max(2, std::min(8, stages));
-  // a K split reduces through a receive area laid over the stages
+  p.astages = 2;
+  const size_t fixed = 1024 + params_bytes + 8 + (size_t)(2 * 12 + 2 * 2 + 1) * 8 + 16 + (size_t)p.astages * p.a_bytes;
+  // TMA ring as deep as the budget allows; small token tiles (grouped experts)
+  // keep the CTA small enough for two per SM
+  const size_t budget = (GROUPED && BN <= 32) ? 112 * 1024 : 222 * 1024;
+  int stages = (int)((budget - std::min(budget, fixed)) / p.stage_bytes);
+  stages = std::max(2, std::min(12, stages));
+  // a K split reduces through a receive area laid over both rings
   const int chunks = BN / 16, owned_max = (chunks + splits - 1) / splits;
   const size_t recv_bytes = splits > 1 ? (size_t)splits * BM * owned_max * 16 * 4 : 0;
-  while ((size_t)stages * p.stage_bytes < recv_bytes) ++stages;
+  while ((size_t)stages * p.stage_bytes + (size_t)p.astages * p.a_bytes < recv_bytes) ++stages;
   p.stages = stages;
   const size_t smem = fixed + (size_t)stages * p.stage_bytes;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;

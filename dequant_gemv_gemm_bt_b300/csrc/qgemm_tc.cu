@@ -637,8 +637,40 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Shared memory of one CTA for a given K split (mirrors the layout in the kernel).
+template <int BITS, int BN, bool GROUPED>
+size_t tc_smem_bytes(int K, int splits, int* stages_out) {
+  const int G_all = K / BK;
+  int gc_max = 0;
+  for (int z = 0; z < splits; ++z) {
+    const int lo = z == 0 ? 0 : ((z * G_all) / splits) & ~1;
+    const int hi = z == splits - 1 ? G_all : (((z + 1) * G_all) / splits) & ~1;
+    if (hi - lo < 1) return 0;
+    gc_max = std::max(gc_max, hi - lo);
+  }
+  const uint32_t a_bytes = BM * BK * 2, x_bytes = BN * BK * 2, c_bytes = BM * 8 * BITS;
+  const uint32_t stage_bytes = (x_bytes + c_bytes + 1023u) & ~1023u;
+  const int astages = 2;
+  const size_t params_bytes = (size_t)2 * BM * gc_max * sizeof(uint16_t);
+  const size_t fixed = 1024 + params_bytes + 8 + (size_t)(2 * 12 + 2 * 2 + 1) * 8 + 16 + (size_t)astages * a_bytes;
+  const size_t budget = (GROUPED && BN <= 32) ? 112 * 1024 : 222 * 1024;
+  int stages = (int)((budget - std::min(budget, fixed)) / stage_bytes);
+  stages = std::max(2, std::min(12, stages));
+  const int chunks = BN / 16, owned_max = (chunks + splits - 1) / splits;
+  const size_t recv_bytes = splits > 1 ? (size_t)splits * BM * owned_max * 16 * 4 : 0;
+  while ((size_t)stages * stage_bytes + (size_t)astages * a_bytes < recv_bytes) ++stages;
+  if (stages_out) *stages_out = stages;
+  return fixed + (size_t)stages * stage_bytes;
+}
+
+// K split for a dense launch: minimize waves x (K blocks per split + fixed cost),
+// where waves come from how many clusters of that size fit on the device at once.
+template <int BITS, bool BF16, int BN>
+int choose_splits(int tiles, int K, cudaStream_t st);
+
 template <int BITS, bool BF16, int BN, bool GROUPED = false>
 cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStream_t st) {
+  if (splits <= 0) splits = GROUPED ? 1 : choose_splits<BITS, BF16, BN>(((gp.N + BM - 1) / BM) * ((gp.M + BN - 1) / BN), gp.K, st);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int row_bytes = gp.K * BITS / 8;
@@ -703,20 +735,11 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.offsets = gp.offsets;
   p.row_index = gp.row_index;
   p.num_experts = gp.num_experts;
-  const size_t params_bytes = (size_t)2 * BM * p.gc_max * sizeof(uint16_t);
   p.astages = 2;
-  const size_t fixed = 1024 + params_bytes + 8 + (size_t)(2 * 12 + 2 * 2 + 1) * 8 + 16 + (size_t)p.astages * p.a_bytes;
-  // TMA ring as deep as the budget allows; small token tiles (grouped experts)
-  // keep the CTA small enough for two per SM
-  const size_t budget = (GROUPED && BN <= 32) ? 112 * 1024 : 222 * 1024;
-  int stages = (int)((budget - std::min(budget, fixed)) / p.stage_bytes);
-  stages = std::max(2, std::min(12, stages));
-  // a K split reduces through a receive area laid over both rings
-  const int chunks = BN / 16, owned_max = (chunks + splits - 1) / splits;
-  const size_t recv_bytes = splits > 1 ? (size_t)splits * BM * owned_max * 16 * 4 : 0;
-  while ((size_t)stages * p.stage_bytes + (size_t)p.astages * p.a_bytes < recv_bytes) ++stages;
+  int stages = 0;
+  const size_t smem = tc_smem_bytes<BITS, BN, GROUPED>(gp.K, splits, &stages);
+  if (smem == 0) return cudaErrorInvalidValue;
   p.stages = stages;
-  const size_t smem = fixed + (size_t)stages * p.stage_bytes;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -740,6 +763,22 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k, mc, mx, p);
+}
+
+// K split for a dense launch.  Measured on B300: launches whose CTA count
+// stays at or below ~85% of the SMs run in one wave with room for cluster
+// placement, while fuller grids of split clusters spill into a second wave and
+// lose more than the split gains.  So: the largest split (1, 2, 3, 4, 6, 8,
+// keeping >= 4 K blocks per split) with tiles x split <= 0.85 x SMs.
+template <int BITS, bool BF16, int BN>
+int choose_splits(int tiles, int K, cudaStream_t) {
+  const int kb = K / BK;
+  if (opts().gemm_splits > 0) return std::max(1, std::min(opts().gemm_splits, kb / 2));
+  const int limit = (sm_count() * 85) / 100;
+  int best = 1;
+  for (int sp : {2, 3, 4, 6, 8})
+    if (kb / sp >= 4 && tiles * sp <= limit) best = sp;
+  return best;
 }
 
 template <int BITS, bool BF16>
@@ -813,10 +852,8 @@ void plan_gemm_tc(int M, int N, int K, int sms, int& bn, int& splits) {
   if (M <= 32) bn = 32;
   else if (M <= 64) bn = 64;
   else if (M <= 128) bn = 128;
-  const int tiles = ((N + 127) / 128) * ((M + bn - 1) / bn);
-  const int kb = K / 64;
-  splits = std::max(1, std::min({8, (sms + tiles / 2) / std::max(1, tiles), kb / 4}));
-  if (opts().gemm_splits > 0) splits = std::min(opts().gemm_splits, std::max(1, kb / 2));
+  splits = 0;   // chosen per instantiation from cluster occupancy (choose_splits)
+  (void)N; (void)K; (void)sms;
 }
 
 cudaError_t launch_gemm_tc(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {

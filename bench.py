@@ -387,8 +387,7 @@ def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
 
         def layer(d):
             ids_t, gates_t, x, b, _ = d
-            bt.bt_moe_route(ids_t, E, b["off"], b["pidx"], b["prow"])
-            torch.floor_divide(b["pidx"], top_k, out=b["rowi"])
+            bt.bt_moe_route(ids_t, E, b["off"], b["pidx"], b["prow"], b["rowi"])
             bt.bt_moe_qgemm(*GU, bits, b["off"], x, b["ygu"], x_row_index=b["rowi"])
             bt.bt_swiglu(b["ygu"], b["h"])
             bt.bt_moe_qgemm(*DN, bits, b["off"], b["h"], b["yd"])
@@ -418,7 +417,7 @@ def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
         out[f"M{tokens}"] = {"us_per_layer": round(t / n_steps * 1e6, 2), "weight_gbs": round(gbs, 1),
                              "frac_of_hbm": round(gbs / hbm, 4), "tflops": round(flops * n_steps / t / 1e12, 3),
                              "experts_touched_mean": round(touched_bytes / n_steps / per_expert, 2),
-                             "launches_per_layer": 6, "clocks": clk.summary()}
+                             "launches_per_layer": 5, "clocks": clk.summary()}
         del graphs
     if bt.bt_last_device_error() != bt.BT_OK:
         raise RuntimeError("device error in the MoE leg")
@@ -434,6 +433,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--legs", default="decode,prefill,moe",
                     help="comma list of legs to run: decode (headline), prefill, moe")
+    ap.add_argument("--no-compare", action="store_true",
+                    help="skip the side measurement of the pass as 197 single-GEMV launches")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -482,6 +483,7 @@ def main():
         }))
         return 0
 
+    legs = set(args.legs.split(","))
     import torch
     dist = None
     if world > 1:
@@ -491,6 +493,18 @@ def main():
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     from dequant_gemv_gemm_bt_b300 import bt
+
+    if "decode" not in legs:   # other legs only (profiling); no headline value
+        stream = torch.cuda.Stream(device=dev)
+        peaks, _ = measured_peaks()
+        out = {"metric": METRIC, "value": None, "unit": "GB/s", "legs": sorted(legs)}
+        if "prefill" in legs:
+            out["prefill"] = run_prefill(torch, bt, dev, stream, args.steps, args.warmup, local_rank, peaks)
+        if "moe" in legs:
+            out["moe"] = run_moe(torch, bt, dev, stream, args.steps, args.warmup, local_rank, float(peaks["hbm_gbs"]))
+        if rank == 0:
+            print(json.dumps(out))
+        return 0
 
     # CPU baseline first (rank 0, single GPU only), before any GPU work
     cpu_baseline = None
@@ -526,7 +540,7 @@ def main():
 
     stream = torch.cuda.Stream(device=dev)
     graph = capture(torch, run_pass, stream)
-    graph_single = capture(torch, run_pass_single, stream)
+    graph_single = None if args.no_compare else capture(torch, run_pass_single, stream)
     if bt.bt_last_device_error() != bt.BT_OK:
         raise RuntimeError("device error during capture")
 
@@ -535,9 +549,10 @@ def main():
 
     with torch.cuda.stream(stream):
         t_pass, clocks = timed(torch, dist, stream, replay, args.steps, args.warmup, local_rank)
-        t_single, _ = timed(torch, None, stream, lambda: graph_single.replay(), max(3, args.steps // 4), 3,
-                            local_rank)
-    single_gbs = pass_bytes * max(3, args.steps // 4) / t_single / 1e9
+        if graph_single is not None:
+            t_single, _ = timed(torch, None, stream, lambda: graph_single.replay(), max(3, args.steps // 4), 3,
+                                local_rank)
+    single_gbs = pass_bytes * max(3, args.steps // 4) / t_single / 1e9 if graph_single is not None else None
     if dist is not None:
         tt = torch.tensor([t_pass], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -617,12 +632,11 @@ def main():
                 "how": "per step: pinned H2D of all 197 activation vectors, the pass (CUDA graph of 3 "
                        "bt_qgemv_batched launches), D2H of all outputs"},
         "gpu_launches": launches * args.steps,
-        "per_gemv_graph": {"gbs": round(single_gbs, 2), "launches_per_pass": len(bufs),
+        "per_gemv_graph": {"gbs": round(single_gbs, 2) if single_gbs else None, "launches_per_pass": len(bufs),
                            "how": "the same pass as 197 bt_qgemv launches in one CUDA graph with PDL"},
         "lm_head_gemv": {"gbs": round(lm_gbs, 1), "frac_of_hbm": round(lm_gbs / hbm, 4),
                          "shape": "N=151936 K=1024 Q4", "bytes": lm_bytes},
     }
-    legs = set(args.legs.split(","))
     if "prefill" in legs:
         out["prefill"] = run_prefill(torch, bt, dev, stream, args.steps, args.warmup, local_rank, peaks)
     if "moe" in legs:

@@ -48,7 +48,7 @@ class GemvProblem(ctypes.Structure):
 
 lib.bt_qgemv_batched.argtypes = [ctypes.POINTER(GemvProblem), _i, _i, _i, _i, _i, _i, _p]
 lib.bt_moe_qgemm.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
-lib.bt_moe_route.argtypes = [_p, _i, _i, _i, _p, _p, _p, _p]
+lib.bt_moe_route.argtypes = [_p, _i, _i, _i, _p, _p, _p, _p, _p]
 lib.bt_swiglu.argtypes = [_p, _i, _i, _i, _p, _i, _p]
 lib.bt_moe_combine.argtypes = [_p, _i, _p, _p, _i, _i, _i, _p, _i, _p]
 lib.bt_status_string.argtypes = [_i]
@@ -177,8 +177,13 @@ def bt_moe_qgemm(codes, scales, biases, bits: int, expert_offsets, x, y=None, *,
     return y
 
 
-def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair_row=None, stream=None):
-    """Stable grouping of (token, slot) pairs by expert: returns (offsets, pair_index, pair_row)."""
+def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair_row=None, pair_token=None,
+                 stream=None, with_token=False):
+    """Stable grouping of (token, slot) pairs by expert.
+
+    Returns ``(offsets, pair_index, pair_row)``, plus ``pair_token`` (the token of each
+    grouped row, for ``x_row_index``) when ``with_token`` or a ``pair_token`` buffer is given.
+    """
     t, top_k = topk_ids.shape
     dev = topk_ids.device
     if offsets is None:
@@ -187,9 +192,15 @@ def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair
         pair_index = torch.empty(t * top_k, dtype=torch.int32, device=dev)
     if pair_row is None:
         pair_row = torch.empty(t * top_k, dtype=torch.int32, device=dev)
+    want_token = with_token or pair_token is not None
+    if want_token and pair_token is None:
+        pair_token = torch.empty(t * top_k, dtype=torch.int32, device=dev)
     _check(lib.bt_moe_route(_dev(topk_ids, "topk_ids"), t, top_k, num_experts, _dev(offsets, "offsets"),
-                            _dev(pair_index, "pair_index"), _dev(pair_row, "pair_row"), _stream(stream)),
+                            _dev(pair_index, "pair_index"), _dev(pair_row, "pair_row"),
+                            _dev(pair_token, "pair_token") if want_token else None, _stream(stream)),
            "bt_moe_route")
+    if want_token:
+        return offsets, pair_index, pair_row, pair_token
     return offsets, pair_index, pair_row
 
 

@@ -268,12 +268,12 @@ bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint
 }
 
 bt_status bt_moe_route(const int32_t* topk_ids, int tokens, int top_k, int num_experts, int32_t* expert_offsets,
-                       int32_t* pair_index, int32_t* pair_row, cudaStream_t stream) {
+                       int32_t* pair_index, int32_t* pair_row, int32_t* pair_token, cudaStream_t stream) {
   if (tokens < 0 || top_k < 1 || top_k > 32 || num_experts < 1 || num_experts > 4096) return BT_ERR_INVALID_ARG;
   if (!expert_offsets || (tokens > 0 && (!topk_ids || !pair_index || !pair_row))) return BT_ERR_INVALID_ARG;
   if ((long long)tokens * top_k > (1LL << 30)) return BT_ERR_UNSUPPORTED;
   return cuda_status(launch_moe_route(topk_ids, tokens, top_k, num_experts, expert_offsets, pair_index, pair_row,
-                                      stream));
+                                      pair_token, stream));
 }
 
 bt_status bt_swiglu(const void* gate_up, bt_dtype in_dtype, int rows, int inter, void* h, bt_dtype h_dtype,

@@ -14,9 +14,10 @@ constexpr int kRouteThreads = 1024;
 
 // One CTA: histogram, exclusive scan, then a stable scatter that walks the
 // pairs in order, 1024 at a time, one warp at a time within a chunk.
-__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const int32_t* ids, int pairs, int E,
+__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const int32_t* ids, int pairs, int E, int top_k,
                                                                   int32_t* offsets, int32_t* pair_index,
-                                                                  int32_t* pair_row, unsigned* err) {
+                                                                  int32_t* pair_row, int32_t* pair_token,
+                                                                  unsigned* err) {
   extern __shared__ int cursor[];   // [E]
   __shared__ int warp_tot[32];
   pdl_launch_dependents();
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const int32_t*
         __syncwarp();
         if (valid) {
           pair_index[pos] = i;
+          if (pair_token) pair_token[pos] = i / top_k;
           if (rank == 0) cursor[e] += __popc(peers);
         }
         if (i < pairs) pair_row[i] = pos;
@@ -168,14 +170,14 @@ cudaError_t combine_o(const void* yg, const float* gates, const int32_t* pair_ro
 }  // namespace
 
 cudaError_t launch_moe_route(const int32_t* ids, int tokens, int top_k, int E, int32_t* offsets,
-                             int32_t* pair_index, int32_t* pair_row, cudaStream_t st) {
+                             int32_t* pair_index, int32_t* pair_row, int32_t* pair_token, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   const size_t smem = (size_t)E * sizeof(int);
   cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = cfg_for(dim3(1), dim3(kRouteThreads), smem, st, attr);
-  return cudaLaunchKernelEx(&cfg, moe_route_kernel, ids, tokens * top_k, E, offsets, pair_index, pair_row,
-                            device_error_word());
+  return cudaLaunchKernelEx(&cfg, moe_route_kernel, ids, tokens * top_k, E, top_k, offsets, pair_index, pair_row,
+                            pair_token, device_error_word());
 }
 
 cudaError_t launch_swiglu(const void* in, bt_dtype id, int rows, int inter, void* out, bt_dtype od,

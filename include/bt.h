@@ -148,13 +148,16 @@ BT_API bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, con
  *   pair_index      device int32 [T*top_k] (out): grouped row r holds pair
  *                   pair_index[r] = t*top_k + slot
  *   pair_row        device int32 [T*top_k] (out): inverse of pair_index
+ *   pair_token      device int32 [T*top_k] (out, may be NULL): token of grouped
+ *                   row r, pair_index[r] / top_k -- the x_row_index that
+ *                   gathers the layer input for the grouped product
  * Ids outside [0, E) set the device error word and are placed in no group
  * (bt_last_device_error then returns BT_ERR_INVALID_ARG).
  * Limits: T >= 0, 1 <= top_k <= 32, 1 <= E <= 4096.
  */
 BT_API bt_status bt_moe_route(const int32_t* topk_ids, int tokens, int top_k, int num_experts,
                        int32_t* expert_offsets, int32_t* pair_index, int32_t* pair_row,
-                       cudaStream_t stream);
+                       int32_t* pair_token, cudaStream_t stream);
 
 /*
  * SwiGLU between the gate/up and down products: h[r, i] = silu(a[r, i]) * a[r, I + i]

@@ -75,8 +75,8 @@ def test_qgemm_and_moe_validation(bt):
     assert L.bt_moe_qgemm(*W, 4, 64, 8, 128, 256, None, 4, None, A, 1, A, 1, None) == 1  # offsets
     assert L.bt_moe_qgemm(*W, 4, 64, 8, 128, 256, A, -1, None, A, 1, A, 1, None) == 1   # rows < 0
     assert L.bt_moe_qgemm(*W, 4, 64, 8, 128, 256, A, 0, None, A, 1, A, 1, None) == 0    # no rows: no-op
-    assert L.bt_moe_route(A, 4, 0, 8, A, A, A, None) == 1                       # top_k = 0
-    assert L.bt_moe_route(A, 4, 2, 0, A, A, A, None) == 1                       # E = 0
-    assert L.bt_moe_route(A, 4, 2, 8, None, A, A, None) == 1
+    assert L.bt_moe_route(A, 4, 0, 8, A, A, A, None, None) == 1                 # top_k = 0
+    assert L.bt_moe_route(A, 4, 2, 0, A, A, A, None, None) == 1                 # E = 0
+    assert L.bt_moe_route(A, 4, 2, 8, None, A, A, None, None) == 1
     assert L.bt_swiglu(A, 1, 4, 0, A, 1, None) == 1
     assert L.bt_moe_combine(A, 1, A, A, 4, 0, 128, A, 1, None) == 1

@@ -33,8 +33,9 @@ def test_route_matches_oracle_bit_exact(env, tokens, e, top_k):
     r = synth.rng_for("test", "route", tokens, e, top_k)
     ids, _ = synth.draw_routing(r, tokens, e, top_k)
     ids_t = torch.from_numpy(ids).cuda()
-    off, pidx, prow = bt.bt_moe_route(ids_t, e)
+    off, pidx, prow, ptok = bt.bt_moe_route(ids_t, e, with_token=True)
     assert bt.bt_last_device_error() == bt.BT_OK
+    np.testing.assert_array_equal(ptok.cpu().numpy(), pidx.cpu().numpy() // top_k)
     off_ref, order = O.route_sort(ids, e)
     np.testing.assert_array_equal(off.cpu().numpy(), off_ref)
     np.testing.assert_array_equal(pidx.cpu().numpy(), order)
@@ -119,8 +120,8 @@ def test_moe_layer_end_to_end(env, tokens):
     tdt = torch.float16 if tokens == 1 else torch.bfloat16
     xb = synth.draw_activations(r, tokens, hdim, xdt)
     x = half_tensor(xb, xdt, torch)
-    off, pidx, prow = bt.bt_moe_route(torch.from_numpy(ids).cuda(), e)
-    row_index = (pidx // top_k).int()
+    off, pidx, prow, ptok = bt.bt_moe_route(torch.from_numpy(ids).cuda(), e, with_token=True)
+    row_index = ptok
     y_gu = bt.bt_moe_qgemm(*dev_stack(gu, torch), bits, off, x, x_row_index=row_index, out_dtype=tdt)
     h = bt.bt_swiglu(y_gu, out_dtype=tdt)
     y_d = bt.bt_moe_qgemm(*dev_stack(down_w, torch), bits, off, h, out_dtype=tdt)
@@ -156,8 +157,8 @@ def test_moe_layer_qwen3_30b_shapes(env, tokens):
     xdt, tdt = ("f16", torch.float16) if tokens == 1 else ("bf16", torch.bfloat16)
     xb = synth.draw_activations(r, tokens, hdim, xdt)
     x = half_tensor(xb, xdt, torch)
-    off, pidx, prow = bt.bt_moe_route(torch.from_numpy(ids).cuda(), e)
-    y_gu = bt.bt_moe_qgemm(*dev_stack(gu, torch), bits, off, x, x_row_index=(pidx // top_k).int(), out_dtype=tdt)
+    off, pidx, prow, ptok = bt.bt_moe_route(torch.from_numpy(ids).cuda(), e, with_token=True)
+    y_gu = bt.bt_moe_qgemm(*dev_stack(gu, torch), bits, off, x, x_row_index=ptok, out_dtype=tdt)
     h = bt.bt_swiglu(y_gu, out_dtype=tdt)
     y_d = bt.bt_moe_qgemm(*dev_stack(down, torch), bits, off, h, out_dtype=tdt)
     out = bt.bt_moe_combine(y_d, torch.from_numpy(gates).cuda(), prow, top_k, out_dtype=torch.float32)

@@ -221,7 +221,23 @@ def build_decode_pass(torch, bt, weights, xs16, dev):
     return bufs
 
 
+class EagerReplay:
+    """Stands in for a captured graph: replay() issues the same launches directly on the stream."""
+
+    def __init__(self, torch, fn, stream):
+        self.torch, self.fn, self.stream = torch, fn, stream
+
+    def replay(self):
+        with self.torch.cuda.stream(self.stream):
+            self.fn()
+
+
+EAGER = False   # set by --eager: no graph capture (for profilers that cannot follow graph replays)
+
+
 def capture(torch, fn, stream):
+    if EAGER:
+        return EagerReplay(torch, fn, stream)
     with torch.cuda.stream(stream):
         fn()
         torch.cuda.synchronize()
@@ -435,7 +451,12 @@ def main():
                     help="comma list of legs to run: decode (headline), prefill, moe")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the side measurement of the pass as 197 single-GEMV launches")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch directly instead of replaying CUDA graphs (profiling runs only: the times then "
+                         "include host launch overhead)")
     args = ap.parse_args()
+    global EAGER
+    EAGER = args.eager
     if args.warmup < 3:
         args.warmup = 3
 
@@ -451,6 +472,9 @@ def main():
               "x_dtype": "f16", "y_dtype": "f32",
               "l2": "inputs exceed L2 (335 MB of packed weights per pass vs 126 MB L2); no flush",
               "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+    if args.eager:
+        config["execution"] = "eager launches (--eager profiling run; times include host launch overhead)"
 
     if args.impl == "reference":
         if rank != 0:

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/bt.h"
 
 namespace bt {
@@ -127,6 +129,24 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ----------------------------------------------------------------- halves
+// Raises a kernel's dynamic shared-memory limit to the device's opt-in maximum,
+// once per device.  Setting the limit to each launch's own size instead makes
+// the driver reconfigure the function whenever consecutive launches differ
+// (tens of microseconds of host time per call when shapes alternate).
+inline cudaError_t raise_smem_limit(const void* fn, std::atomic<uint64_t>& done) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = d < 64 ? (uint64_t{1} << d) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  int mx = 0;
+  e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 template <bt_dtype D> struct HalfT;
 template <> struct HalfT<BT_F16> { using T = __half; };
 template <> struct HalfT<BT_BF16> { using T = __nv_bfloat16; };

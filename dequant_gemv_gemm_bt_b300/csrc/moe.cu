@@ -173,7 +173,8 @@ cudaError_t launch_moe_route(const int32_t* ids, int tokens, int top_k, int E, i
                              int32_t* pair_index, int32_t* pair_row, int32_t* pair_token, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   const size_t smem = (size_t)E * sizeof(int);
-  cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> smem_raised{0};
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(moe_route_kernel), smem_raised);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = cfg_for(dim3(1), dim3(kRouteThreads), smem, st, attr);
   return cudaLaunchKernelEx(&cfg, moe_route_kernel, ids, tokens * top_k, E, top_k, offsets, pair_index, pair_row,

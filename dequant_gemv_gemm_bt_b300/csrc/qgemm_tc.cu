@@ -742,7 +742,8 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.stages = stages;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> smem_raised{0};
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   // grouped: an upper bound on the (expert, tile) list, sum over experts of ceil(rows / BN)

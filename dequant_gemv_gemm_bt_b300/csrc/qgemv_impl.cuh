@@ -627,7 +627,8 @@ template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
 cudaError_t launch_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int grid, size_t smem,
                      cudaStream_t stream) {
   auto k = qgemv_kernel<BITS, XD, CPL, FAST, RI, BATCH>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> smem_raised{0};
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -52,6 +52,11 @@ QWEN06_LM_HEAD = ("lm_head", 151936, 1024)
 LLAMA3B_LAYER = [("q", 3072, 3072), ("k", 1024, 3072), ("v", 1024, 3072), ("o", 3072, 3072),
                  ("gate", 8192, 3072), ("up", 8192, 3072), ("down", 3072, 8192)]
 LLAMA3B_LAYERS = 28
+# Llama-3.2-1B-shaped decode pass, swept over bit widths.
+LLAMA1B_LAYER = [("q", 2048, 2048), ("k", 512, 2048), ("v", 512, 2048), ("o", 2048, 2048),
+                 ("gate", 8192, 2048), ("up", 8192, 2048), ("down", 2048, 8192)]
+LLAMA1B_LAYERS = 16
+SWEEP_BITS = (2, 3, 4, 6, 8)
 
 
 def weight_bytes(n: int, k: int, bits: int) -> int:
@@ -65,6 +70,10 @@ def decode_pass_shapes():
             shapes.append((f"L{layer}.{name}", n, k))
     shapes.append(QWEN06_LM_HEAD)
     return shapes
+
+
+def sweep_pass_shapes():
+    return [(f"L{l}.{name}", n, k) for l in range(LLAMA1B_LAYERS) for name, n, k in LLAMA1B_LAYER]
 
 
 def prefill_pass_shapes():
@@ -356,6 +365,46 @@ def run_prefill(torch, bt, dev, stream, steps, warmup, gpu_index, peaks):
     return out
 
 
+def run_sweep(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
+    """Llama-3.2-1B-shaped decode pass (16 layers x 7 projections, fp16 x, fp32 y) at
+    Q2/Q3/Q4/Q6/Q8: one bt_qgemv_batched launch per K (2048: q,k,v,o,gate,up; 8192:
+    down), captured in a CUDA graph with PDL; weight GB/s per bit width."""
+    shapes = sweep_pass_shapes()
+    bt.bt_set_option(bt.BT_OPT_PDL, 1)
+    bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
+    xs16 = gen_x("sweep-pass", shapes, 1, "f16")
+    out = {"workload": "Llama-3.2-1B-shaped decode pass: 16 layers x (q/o 2048->2048, k/v 2048->512, "
+                       "gate/up 2048->8192, down 8192->2048), g64, fp16 x, fp32 y; 2 batched launches per pass"}
+    n_steps = max(3, min(steps, 200))
+    for bits in SWEEP_BITS:
+        t0 = time.time()
+        ws = gen_weights("sweep-pass", shapes, bits)
+        gen_s = time.time() - t0
+        pass_bytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
+        bufs = build_decode_pass(torch, bt, ws, xs16, dev)
+        del ws
+        by_k = {}
+        for i, (_, n, k) in enumerate(shapes):
+            by_k.setdefault(k, []).append(i)
+        groups = [[bufs[i][:5] for i in idx] for _, idx in sorted(by_k.items())]
+
+        def run_pass():
+            for g in groups:
+                bt.bt_qgemv_batched(g, bits)
+        g = capture(torch, run_pass, stream)
+        with torch.cuda.stream(stream):
+            t, clk = timed(torch, None, stream, lambda: g.replay(), n_steps, max(3, min(warmup, 5)), gpu_index)
+        gbs = pass_bytes * n_steps / t / 1e9
+        out[f"Q{bits}"] = {"gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+                           "us_per_pass": round(t / n_steps * 1e6, 2), "bytes_per_pass": pass_bytes,
+                           "launches_per_pass": len(groups), "weight_gen_s": round(gen_s, 1), "clocks": clk}
+        del g, bufs, groups
+        torch.cuda.synchronize()
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error in the bit-width sweep leg")
+    return out
+
+
 def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     """Qwen3-30B-A3B-shaped expert layer, Q4: route -> gate|up (grouped, gathered rows) -> SwiGLU ->
     down (grouped) -> gate-weighted combine, at M = 1 (decode) and M = 128 (prefill).
@@ -447,8 +496,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--legs", default="decode,prefill,moe",
-                    help="comma list of legs to run: decode (headline), prefill, moe")
+    ap.add_argument("--legs", default="decode,sweep,prefill,moe",
+                    help="comma list of legs to run: decode (headline), sweep (bit widths), prefill, moe")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the side measurement of the pass as 197 single-GEMV launches")
     ap.add_argument("--eager", action="store_true",
@@ -522,6 +571,9 @@ def main():
         stream = torch.cuda.Stream(device=dev)
         peaks, _ = measured_peaks()
         out = {"metric": METRIC, "value": None, "unit": "GB/s", "legs": sorted(legs)}
+        if "sweep" in legs:
+            out["sweep"] = run_sweep(torch, bt, dev, stream, args.steps, args.warmup, local_rank,
+                                     float(peaks["hbm_gbs"]))
         if "prefill" in legs:
             out["prefill"] = run_prefill(torch, bt, dev, stream, args.steps, args.warmup, local_rank, peaks)
         if "moe" in legs:
@@ -661,6 +713,8 @@ def main():
         "lm_head_gemv": {"gbs": round(lm_gbs, 1), "frac_of_hbm": round(lm_gbs / hbm, 4),
                          "shape": "N=151936 K=1024 Q4", "bytes": lm_bytes},
     }
+    if "sweep" in legs:
+        out["sweep"] = run_sweep(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
     if "prefill" in legs:
         out["prefill"] = run_prefill(torch, bt, dev, stream, args.steps, args.warmup, local_rank, peaks)
     if "moe" in legs:

@@ -148,6 +148,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_STAGES: opts().gemv_stages = (int)value; return BT_OK;
     case BT_OPT_GEMM_PATH: opts().gemm_path = (int)value; return BT_OK;
     case BT_OPT_GEMM_SPLITS: opts().gemm_splits = (int)std::min<long long>(value, 8); return BT_OK;
+    case BT_OPT_GEMV_MAX_CPL: opts().gemv_max_cpl = (int)std::min<long long>(value, 4); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
 }

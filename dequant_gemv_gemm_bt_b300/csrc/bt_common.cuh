@@ -29,6 +29,7 @@ struct LaunchOpts {
   int gemv_stages = 0;       // tuning: pipeline depth override (0 = heuristic)
   int gemm_path = 0;         // tuning: 0 = heuristic, 1 = CUDA-core tile, 2 = tensor-core tile
   int gemm_splits = 0;       // tuning: tensor-core GEMM K split (0 = heuristic)
+  int gemv_max_cpl = 0;      // tuning: GEMV chunks per lane before splitting K over warps (0 = heuristic)
 };
 LaunchOpts& opts();
 unsigned* device_error_word();   // device address of the error word (current device)
@@ -129,10 +130,9 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ----------------------------------------------------------------- halves
-// Raises a kernel's dynamic shared-memory limit to the device's opt-in maximum,
-// once per device.  Setting the limit to each launch's own size instead makes
-// the driver reconfigure the function whenever consecutive launches differ
-// (tens of microseconds of host time per call when shapes alternate).
+// Raises a kernel's dynamic shared-memory limit to the most the device allows
+// next to the kernel's static shared memory, once per device, so the limit is
+// not rewritten on every launch whose size differs from the previous one.
 inline cudaError_t raise_smem_limit(const void* fn, std::atomic<uint64_t>& done) {
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
@@ -142,9 +142,21 @@ inline cudaError_t raise_smem_limit(const void* fn, std::atomic<uint64_t>& done)
   int mx = 0;
   e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, mx - (int)fa.sharedSizeBytes);
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
+}
+
+// (a & m) | c as one LOP3.  Written as a C++ expression with two constants the
+// compiler emits two logic instructions; in the dequant loops that doubles the
+// ALU-pipe work per code pair.
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
+  return d;
 }
 
 template <bt_dtype D> struct HalfT;

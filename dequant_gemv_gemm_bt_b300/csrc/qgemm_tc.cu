@@ -185,10 +185,10 @@ template <bool BF16> constexpr uint32_t kMagicByte = BF16 ? 0x43434343u : 0x6464
 template <bool BF16>
 __device__ __forceinline__ uint4 deq8_q4(uint32_t w, uint32_t s2, uint32_t b2) {
   constexpr uint32_t MG = kMagic2<BF16>;
-  uint32_t d0 = (w & 0x000F000Fu) | MG;          // (q0, q4)
-  uint32_t d1 = ((w >> 4) & 0x000F000Fu) | MG;   // (q1, q5)
-  uint32_t d2 = ((w >> 8) & 0x000F000Fu) | MG;   // (q2, q6)
-  uint32_t d3 = ((w >> 12) & 0x000F000Fu) | MG;  // (q3, q7)
+  uint32_t d0 = lop3_and_or(w, 0x000F000Fu, MG);          // (q0, q4)
+  uint32_t d1 = lop3_and_or(w >> 4, 0x000F000Fu, MG);     // (q1, q5)
+  uint32_t d2 = lop3_and_or(w >> 8, 0x000F000Fu, MG);     // (q2, q6)
+  uint32_t d3 = lop3_and_or(w >> 12, 0x000F000Fu, MG);    // (q3, q7)
   d0 = hfma2<BF16>(hsub2<BF16>(d0, MG), s2, b2);
   d1 = hfma2<BF16>(hsub2<BF16>(d1, MG), s2, b2);
   d2 = hfma2<BF16>(hsub2<BF16>(d2, MG), s2, b2);
@@ -251,7 +251,9 @@ __device__ __forceinline__ void deq32(const uint32_t (&w)[BITS], uint32_t s2, ui
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t lo = code_at<BITS, BITS>(w, 8 * c + 2 * i), hi = code_at<BITS, BITS>(w, 8 * c + 2 * i + 1);
-        o[i] = hfma2<BF16>(hsub2<BF16>(lo | (hi << 16) | MG, MG), s2, b2);
+        uint32_t pr;
+        asm("lop3.b32 %0, %1, %2, %3, 0xFE;" : "=r"(pr) : "r"(lo), "r"(hi << 16), "r"(MG));   // lo | hi<<16 | MG
+        o[i] = hfma2<BF16>(hsub2<BF16>(pr, MG), s2, b2);
       }
       out[c] = make_uint4(o[0], o[1], o[2], o[3]);
     }

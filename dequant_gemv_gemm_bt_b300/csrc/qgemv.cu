@@ -23,9 +23,16 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   GemvPlan pl{};
   pl.fast = fast;
   const int nchunks = K / 32;
-  const int max_cpl = fast ? 4 : 2;
+  // Chunks of 32 codes per lane: the kernels exist for up to 4 (fast path) or 2
+  // (generic).  One chunk per lane, with K split over up to 8 warps, measured
+  // fastest on B300 at every K up to 8192: it keeps x in 32 registers, so two
+  // CTAs (16 consumer warps) fit per SM, and the cross-warp partial sums are
+  // cheap next to the latency hidden (e.g. Q4 K=8192: 3.7 vs 2.3 TB/s with 4
+  // chunks per lane; K=3072 still gains with a quarter of its lanes idle).
+  const int cpl_cap = fast ? 4 : 2;
+  const int want_cpl = opts().gemv_max_cpl > 0 ? std::min(opts().gemv_max_cpl, cpl_cap) : 1;
   int kw = 1;
-  while (kw < kMaxNW && (nchunks + 32 * kw - 1) / (32 * kw) > max_cpl) kw *= 2;
+  while (kw < kMaxNW && (nchunks + 32 * kw - 1) / (32 * kw) > want_cpl) kw *= 2;
   int cpl = (nchunks + 32 * kw - 1) / (32 * kw);
   int nw = kMaxNW;
   if (kw > nw) {            // more than one chunk per lane: only 8 warps, so split K at most 8 ways
@@ -35,7 +42,7 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   pl.kw = kw;
   pl.cpl = cpl;
   // the kernels exist for up to 4 chunks per lane on the fast path and 2 on the generic one
-  pl.feasible = cpl <= max_cpl && kw <= nw && nw % kw == 0 && K <= 16 * 1024 * (fast ? 2 : 1);
+  pl.feasible = cpl <= cpl_cap && kw <= nw && nw % kw == 0 && K <= 16 * 1024 * (fast ? 2 : 1);
   if (!pl.feasible) return pl;
   const int rw = nw / kw;
   const int G = K / kGroup;

@@ -101,7 +101,7 @@ __device__ __forceinline__ void fma_lohi(float& acc_lo, float& acc_hi, uint16_t 
 }
 
 __device__ __forceinline__ uint32_t lop_mask_or(uint32_t w, uint32_t mask) {
-  return (w & mask) | 0x64006400u;   // one LOP3
+  return lop3_and_or(w, mask, 0x64006400u);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -265,10 +265,8 @@ __device__ __forceinline__ float chunk_dot_generic(const uint32_t (&w)[BITS], co
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int bit = j * BITS, wi = bit >> 5, off = bit & 31;
-    uint32_t q;
-    if (off + BITS <= 32) q = (w[wi] >> off) & mask;
-    else q = __funnelshift_r(w[wi], w[wi + 1], off) & mask;
-    const float qf = __uint_as_float(0x4B000000u | q) - 8388608.f;
+    const uint32_t sh = off + BITS <= 32 ? (w[wi] >> off) : __funnelshift_r(w[wi], w[wi + 1], off);
+    const float qf = __uint_as_float(lop3_and_or(sh, mask, 0x4B000000u)) - 8388608.f;
     if (j & 1) acc1 = fmaf(s.xv[j], qf, acc1);
     else acc0 = fmaf(s.xv[j], qf, acc0);
   }

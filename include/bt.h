@@ -212,6 +212,8 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMM_PATH     tuning: 0 = heuristic, 1 = CUDA-core tile,
  *                       2 = tensor-core tile where supported.
  *   BT_OPT_GEMM_SPLITS   tuning: tensor-core GEMM K split across a cluster (0 = heuristic, 1..8).
+ *   BT_OPT_GEMV_MAX_CPL  tuning: GEMV chunks of 32 codes per lane before K is split
+ *                       over more warps (0 = heuristic, else 1..4).
  */
 typedef enum {
   BT_OPT_PDL = 0,
@@ -221,7 +223,8 @@ typedef enum {
   BT_OPT_GEMV_GENERIC = 4,
   BT_OPT_GEMV_STAGES = 5,
   BT_OPT_GEMM_PATH = 6,
-  BT_OPT_GEMM_SPLITS = 7
+  BT_OPT_GEMM_SPLITS = 7,
+  BT_OPT_GEMV_MAX_CPL = 8
 } bt_option;
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);

@@ -181,3 +181,31 @@ def test_qgemv_batched_rejects_bad_tables(env):
     x2 = torch.zeros(2048, dtype=torch.float16, device="cuda")
     with pytest.raises(ValueError):
         bt.bt_qgemv_batched([(codes, scales, biases, x, y), (codes, scales, biases, x2, y)], 4)   # mixed K
+
+
+# One Llama-3.2-1B-shaped layer (hidden 2048): q/o 2048->2048, k/v 2048->512,
+# gate/up 2048->8192, down 8192->2048 -- the bit-width sweep's projections.
+LLAMA1B_LAYER = (("q", 2048, 2048), ("k", 512, 2048), ("v", 512, 2048), ("o", 2048, 2048),
+                 ("gate", 8192, 2048), ("up", 8192, 2048), ("down", 2048, 8192))
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_qgemv_llama1b_layer_all_bits(env, bits):
+    """Every projection of one full-size layer, batched per K as a decode pass runs them."""
+    torch, bt = env
+    from dequant_gemv_gemm_bt_b300 import synth
+    r = synth.rng_for("test", "llama1b-layer", bits)
+    cases = []
+    for name, n, k in LLAMA1B_LAYER:
+        qw = synth.make_qweight(r, n, k, bits)
+        x16 = synth.draw_activations(r, 1, k, "f16")
+        codes, scales, biases = to_dev(qw, torch)
+        y = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+        cases.append((name, qw, x16, (codes, scales, biases, half_tensor(x16[0], "f16", torch), y)))
+    for k in (2048, 8192):
+        bt.bt_qgemv_batched([c[3] for c in cases if c[1].k == k], bits)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for name, qw, x16, pr in cases:
+        y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x16[0]))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"llama1b {name} b={bits}")

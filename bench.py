@@ -367,14 +367,14 @@ def run_prefill(torch, bt, dev, stream, steps, warmup, gpu_index, peaks):
 
 def run_sweep(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     """Llama-3.2-1B-shaped decode pass (16 layers x 7 projections, fp16 x, fp32 y) at
-    Q2/Q3/Q4/Q6/Q8: one bt_qgemv_batched launch per K (2048: q,k,v,o,gate,up; 8192:
-    down), captured in a CUDA graph with PDL; weight GB/s per bit width."""
+    Q2/Q3/Q4/Q6/Q8: one mixed-K bt_qgemv_batched launch per pass (K = 2048 and 8192),
+    captured in a CUDA graph with PDL; weight GB/s per bit width."""
     shapes = sweep_pass_shapes()
     bt.bt_set_option(bt.BT_OPT_PDL, 1)
     bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
     xs16 = gen_x("sweep-pass", shapes, 1, "f16")
     out = {"workload": "Llama-3.2-1B-shaped decode pass: 16 layers x (q/o 2048->2048, k/v 2048->512, "
-                       "gate/up 2048->8192, down 8192->2048), g64, fp16 x, fp32 y; 2 batched launches per pass"}
+                       "gate/up 2048->8192, down 8192->2048), g64, fp16 x, fp32 y; 1 batched launch per pass"}
     n_steps = max(3, min(steps, 200))
     for bits in SWEEP_BITS:
         t0 = time.time()
@@ -383,10 +383,7 @@ def run_sweep(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
         pass_bytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
         bufs = build_decode_pass(torch, bt, ws, xs16, dev)
         del ws
-        by_k = {}
-        for i, (_, n, k) in enumerate(shapes):
-            by_k.setdefault(k, []).append(i)
-        groups = [[bufs[i][:5] for i in idx] for _, idx in sorted(by_k.items())]
+        groups = [[b[:5] for b in bufs]]   # one mixed-K launch (K = 2048 and 8192)
 
         def run_pass():
             for g in groups:
@@ -516,7 +513,7 @@ def main():
     bits = 4
     pass_bytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
     config = {"workload": "Qwen3-0.6B-shaped decode pass, M=1: 28 layers x 7 projections + lm_head 1024->151936",
-              "execution": "3 bt_qgemv_batched launches per pass (one per K), captured in a CUDA graph",
+              "execution": "1 bt_qgemv_batched launch per pass (197 problems, mixed K), captured in a CUDA graph",
               "bits": bits, "group_size": GROUP, "gemvs_per_pass": len(shapes), "weight_bytes_per_pass": pass_bytes,
               "x_dtype": "f16", "y_dtype": "f32",
               "l2": "inputs exceed L2 (335 MB of packed weights per pass vs 126 MB L2); no flush",
@@ -597,14 +594,9 @@ def main():
     bt.bt_set_option(bt.BT_OPT_PDL, 1)
     bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
 
-    # The pass's projections are independent (each has its own x), so they run as
-    # one batched launch per distinct K (1024: q,k,v,gate,up,lm_head; 2048: o;
-    # 3072: down), in pass order.
-    by_k = {}
-    for i, (name, n, k) in enumerate(shapes):
-        by_k.setdefault(k, []).append(i)
-    groups = [[(bufs[i][0], bufs[i][1], bufs[i][2], bufs[i][3], bufs[i][4]) for i in idx] for _, idx in
-              sorted(by_k.items())]
+    # The pass's projections are independent (each has its own x), so the whole
+    # pass is one mixed-K batched launch (K = 1024, 2048, 3072), in pass order.
+    groups = [[(c, s, b, x, y) for c, s, b, x, y, _ in bufs]]
 
     def run_pass():
         for g in groups:
@@ -662,8 +654,7 @@ def main():
         y_views.append(y_all[off:off + y.numel()])
         off += y.numel()
 
-    e2e_groups = [[(bufs[i][0], bufs[i][1], bufs[i][2], x_dev_views[i], y_views[i]) for i in idx]
-                  for _, idx in sorted(by_k.items())]
+    e2e_groups = [[(bufs[i][0], bufs[i][1], bufs[i][2], x_dev_views[i], y_views[i]) for i in range(len(bufs))]]
 
     def run_pass_e2e():
         for g in e2e_groups:
@@ -697,7 +688,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes, f16 x, f32 accumulate",
         "data": "synthetic (seeded N(0,0.02) weights, min/max Q4 g64; x ~ N(0,1) fp16)",
         "config": config,
-        "roofline": {"bound": "hbm", "kernel": "qgemv_kernel (batched; 3 launches per pass, one per K)",
+        "roofline": {"bound": "hbm", "kernel": "qgemv_kernel (batched, mixed K; 1 launch per pass)",
                      "achieved": round(achieved, 2), "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s",
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": traffic, "kernel_source_digest": digest},
@@ -705,8 +696,8 @@ def main():
         "clocks": clocks,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(y_total * 4),
-                "how": "per step: pinned H2D of all 197 activation vectors, the pass (CUDA graph of 3 "
-                       "bt_qgemv_batched launches), D2H of all outputs"},
+                "how": "per step: pinned H2D of all 197 activation vectors, the pass (CUDA graph of 1 "
+                       "bt_qgemv_batched launch), D2H of all outputs"},
         "gpu_launches": launches * args.steps,
         "per_gemv_graph": {"gbs": round(single_gbs, 2) if single_gbs else None, "launches_per_pass": len(bufs),
                            "how": "the same pass as 197 bt_qgemv launches in one CUDA graph with PDL"},

@@ -30,7 +30,8 @@ lib = ctypes.CDLL(LIB_PATH)
 BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_MISALIGNED, BT_ERR_CUDA, BT_ERR_TIMEOUT = range(6)
 BT_F16, BT_BF16, BT_F32 = 0, 1, 2
 (BT_OPT_PDL, BT_OPT_CONST_WEIGHTS, BT_OPT_WAIT_TIMEOUT_US, BT_OPT_TEST_DROP_STAGE,
- BT_OPT_GEMV_GENERIC, BT_OPT_GEMV_STAGES, BT_OPT_GEMM_PATH, BT_OPT_GEMM_SPLITS, BT_OPT_GEMV_MAX_CPL) = range(9)
+ BT_OPT_GEMV_GENERIC, BT_OPT_GEMV_STAGES, BT_OPT_GEMM_PATH, BT_OPT_GEMM_SPLITS, BT_OPT_GEMV_MAX_CPL,
+ BT_OPT_GEMV_STAGE_KB) = range(10)
 
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_route", "bt_swiglu", "bt_moe_combine",
            "bt_status_string", "bt_last_device_error", "bt_set_option")
@@ -43,7 +44,8 @@ lib.bt_qgemm.argtypes = _W + [_i, _i, _i, _p, _i, _p, _i, _p]
 
 
 class GemvProblem(ctypes.Structure):
-    _fields_ = [("codes", _p), ("scales", _p), ("biases", _p), ("x", _p), ("y", _p), ("n", ctypes.c_int32)]
+    _fields_ = [("codes", _p), ("scales", _p), ("biases", _p), ("x", _p), ("y", _p), ("n", ctypes.c_int32),
+                ("k", ctypes.c_int32)]
 
 
 lib.bt_qgemv_batched.argtypes = [ctypes.POINTER(GemvProblem), _i, _i, _i, _i, _i, _i, _p]
@@ -129,17 +131,21 @@ def bt_qgemv(codes, scales, biases, bits: int, x, y=None, *, group_size: int = 6
 def bt_qgemv_batched(problems, bits: int, *, group_size: int = 64, stream=None):
     """Independent GEMVs in one launch.
 
-    ``problems`` is a list of ``(codes, scales, biases, x, y)`` tensors with a
-    common K (``x.shape[-1]``) and dtypes; each ``y`` gets ``codes.shape[0]`` rows.
+    ``problems`` is a list of ``(codes, scales, biases, x, y)`` tensors with
+    common dtypes; each problem's K is ``x.shape[-1]`` and its ``y`` gets
+    ``codes.shape[0]`` rows.  Problems of different K go out as one mixed-K batch.
     """
     arr = (GemvProblem * len(problems))()
-    k = problems[0][3].shape[-1]
+    ks = set()
     for i, (c, s, b, x, y) in enumerate(problems):
-        if x.shape[-1] != k:
-            raise ValueError("all problems of a batch share K")
+        k = x.shape[-1]
+        if c.shape[-1] * 32 != k * bits:
+            raise ValueError(f"problem {i}: codes hold {c.shape[-1] * 32 // bits} codes per row, x has {k}")
+        ks.add(k)
         arr[i] = GemvProblem(_dev(c, "codes"), _dev(s, "scales"), _dev(b, "biases"), _dev(x, "x"), _dev(y, "y"),
-                             c.shape[0])
-    _check(lib.bt_qgemv_batched(arr, len(problems), bits, group_size, k, _dt(problems[0][3]),
+                             c.shape[0], k)
+    k_all = ks.pop() if len(ks) == 1 else 0
+    _check(lib.bt_qgemv_batched(arr, len(problems), bits, group_size, k_all, _dt(problems[0][3]),
                                 _dt(problems[0][4]), _stream(stream)), "bt_qgemv_batched")
     return [pr[4] for pr in problems]
 

@@ -149,6 +149,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMM_PATH: opts().gemm_path = (int)value; return BT_OK;
     case BT_OPT_GEMM_SPLITS: opts().gemm_splits = (int)std::min<long long>(value, 8); return BT_OK;
     case BT_OPT_GEMV_MAX_CPL: opts().gemv_max_cpl = (int)std::min<long long>(value, 4); return BT_OK;
+    case BT_OPT_GEMV_STAGE_KB: opts().gemv_stage_kb = value == 0 ? 0 : (int)std::max(4LL, std::min(value, 96LL)); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
 }
@@ -181,15 +182,18 @@ bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
 
 bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
                            bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
-  if (!problems || count < 1 || K <= 0) return BT_ERR_INVALID_ARG;
+  if (!problems || count < 1 || K < 0) return BT_ERR_INVALID_ARG;
   if (count > kBatchCap) return BT_ERR_UNSUPPORTED;
   if (!half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
+  const bool mixed = K == 0;
   long long rows = 0;
   int max_n = 0;
   for (int i = 0; i < count; ++i) {
     const bt_gemv_problem& q = problems[i];
-    bt_status s = check_weights(q.codes, q.scales, q.biases, bits, group_size, q.n, K);
+    const int kq = mixed ? q.k : K;
+    bt_status s = check_weights(q.codes, q.scales, q.biases, bits, group_size, q.n, kq);
     if (s != BT_OK) return s;
+    if (mixed && kq > 8192) return BT_ERR_UNSUPPORTED;
     if (!q.x || !q.y) return BT_ERR_INVALID_ARG;
     if (!aligned16(q.x)) return BT_ERR_MISALIGNED;
     rows += q.n;
@@ -198,12 +202,15 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
   GemvBatch<kBatchCap> batch;
   batch.count = count;
   for (int i = 0; i < count; ++i) {
-    batch.prob[i].codes = problems[i].codes;
-    batch.prob[i].scales = problems[i].scales;
-    batch.prob[i].biases = problems[i].biases;
-    batch.prob[i].x = problems[i].x;
-    batch.prob[i].y = problems[i].y;
-    batch.prob[i].n = problems[i].n;
+    GemvProblem& b = batch.prob[i];
+    b = GemvProblem{};
+    b.codes = problems[i].codes;
+    b.scales = problems[i].scales;
+    b.biases = problems[i].biases;
+    b.x = problems[i].x;
+    b.y = problems[i].y;
+    b.n = problems[i].n;
+    b.k = mixed ? problems[i].k : 0;   // 0: the launch plan's K and geometry
   }
   GemvParams p{};
   p.K = K;
@@ -215,8 +222,13 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
   p.drop_stage = opts().test_drop_stage;
   opts().test_drop_stage = 0;
   const bool fast = x_dtype == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !opts().gemv_generic;
-  const int problems_equiv = (int)std::max<long long>(1, (rows + max_n - 1) / max_n);
-  const GemvPlan pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count());
+  GemvPlan pl;
+  if (mixed) {
+    pl = plan_gemv_batch(bits, fast, batch, sm_count());
+  } else {
+    const int problems_equiv = (int)std::max<long long>(1, (rows + max_n - 1) / max_n);
+    pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count());
+  }
   if (!pl.feasible) return BT_ERR_UNSUPPORTED;
   return cuda_status(launch_gemv(p, pl, bits, x_dtype, y_dtype, stream, &batch));
 }

@@ -55,10 +55,11 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   const long long rows_total = (long long)N * problems;
   const long long per_sm = std::max<long long>(1, (rows_total + sms - 1) / sms);
   int ri = pl.cpl == 1 ? 4 : (pl.cpl == 2 ? 2 : 1);   // keep x slices and RI rows of codes in registers
-  while (ri > 1 && ((long long)ri * rw * per_row > kStageBudget || ri * rw > std::max<long long>(rw, per_sm))) ri /= 2;
+  const int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
+  while (ri > 1 && ((long long)ri * rw * per_row > stage_budget || ri * rw > std::max<long long>(rw, per_sm))) ri /= 2;
   pl.ri = ri;
   const int unit = std::max(ri * rw, m);
-  int rb = unit * std::max(1, kStageBudget / (unit * per_row));
+  int rb = unit * std::max(1, stage_budget / (unit * per_row));
   const long long want = ((per_sm + unit - 1) / unit) * unit;
   rb = (int)std::min<long long>(rb, std::max<long long>(unit, want));
   rb = std::min(rb, ((N + unit - 1) / unit) * unit);
@@ -83,6 +84,60 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   return pl;
 }
 
+GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms) {
+  GemvPlan pl{};
+  pl.fast = fast;
+  pl.feasible = false;
+  pl.cpl = 1;
+  const int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
+  // rows in flight per warp: 4 unless some problem's row group would overflow a stage
+  int ri = 4;
+  for (int i = 0; i < batch.count; ++i) {
+    const GemvProblem& q = batch.prob[i];
+    if (q.k <= 0 || q.k % kGroup || q.k > 8 * 32 * 32) return pl;   // one chunk per lane needs K <= 8192
+    const int nchunks = q.k / 32;
+    int kw = 1;
+    while (32 * kw < nchunks) kw *= 2;
+    const int per_row = q.k * bits / 8 + 4 * (q.k / kGroup);
+    while (ri > 1 && ri * (kMaxNW / kw) * per_row > stage_budget) ri /= 2;
+  }
+  int stage = 0;
+  for (int i = 0; i < batch.count; ++i) {
+    GemvProblem& q = batch.prob[i];
+    const int nchunks = q.k / 32;
+    int kw = 1;
+    while (32 * kw < nchunks) kw *= 2;
+    q.kw = kw;
+    q.g = q.k / kGroup;
+    q.row_bytes = q.k * bits / 8;
+    const int per_row = q.row_bytes + 4 * q.g;
+    int m = 1;
+    while (((m * q.row_bytes) & 15) || ((m * q.g * 2) & 15)) m *= 2;
+    const int unit = std::max(ri * (kMaxNW / kw), m);
+    int rb = unit * std::max(1, stage_budget / (unit * per_row));
+    rb = std::min(rb, ((q.n + unit - 1) / unit) * unit);
+    q.rb = rb;
+    stage = std::max(stage, (rb * per_row + 127) / 128 * 128);
+  }
+  pl.ri = ri;
+  pl.kw = batch.prob[0].kw;
+  pl.rows_per_unit = batch.prob[0].rb;
+  pl.row_bytes = batch.prob[0].row_bytes;
+  pl.stage_bytes = stage;
+  const int ctas_per_sm = 2;   // one chunk per lane: two CTAs per SM (the kernel's launch bounds)
+  int stages = std::max(2, std::min(8, (kRingBudget / ctas_per_sm) / stage));
+  if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
+  auto smem_for = [&](int st) {
+    return (size_t)st * stage + 2 * st * sizeof(uint64_t) + (size_t)kMaxNW * 2 * ri * sizeof(float) + sizeof(int);
+  };
+  while (stages > 2 && smem_for(stages) > kMaxSmem / ctas_per_sm) --stages;
+  pl.stages = stages;
+  pl.smem = smem_for(stages);
+  pl.grid = sms * ctas_per_sm;   // trimmed to the unit count at launch
+  pl.feasible = pl.smem <= kMaxSmem;
+  return pl;
+}
+
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st,
                         GemvBatch<kBatchCap>* batch) {
   p.rows_per_unit = pl.rows_per_unit;
@@ -95,12 +150,25 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
   p.y_dtype = yd;
   GemvPlan plb = pl;
   if (batch) {   // per-problem row blocks and their running offsets
-    long long u = 0;
+    long long u = 0, cost = 0;
     for (int i = 0; i < batch->count; ++i) {
-      batch->prob[i].units = (batch->prob[i].n + pl.rows_per_unit - 1) / pl.rows_per_unit;
-      batch->prob[i].unit_begin = u;
-      u += batch->prob[i].units;
+      GemvProblem& q = batch->prob[i];
+      if (q.k == 0) {   // one K for the whole batch: the plan's geometry
+        q.k = p.K;
+        q.g = p.G;
+        q.row_bytes = pl.row_bytes;
+        q.kw = pl.kw;
+        q.rb = pl.rows_per_unit;
+      }
+      q.units = (q.n + q.rb - 1) / q.rb;
+      q.unit_begin = u;
+      u += q.units;
+      // CTAs take equal shares of work, not of units: a row split over kw warps
+      // costs kw times a one-warp row (measured: K=2048 ~2.2x, K=3072 ~4x K=1024)
+      q.cost_begin = cost;
+      cost += (long long)q.n * q.kw;
     }
+    p.total_cost = cost;
     p.num_units = u;
     plb.num_units = u;
     plb.grid = (int)std::min<long long>(u, (long long)sm_count() * (pl.cpl == 1 ? 2 : 1));

@@ -18,6 +18,7 @@ struct GemvParams {
   // plan
   int rows_per_unit, row_bytes, stage_bytes, stages, kw, units_per_problem;
   long long num_units;
+  long long total_cost;   // batched launches: work of all problems (rows x warps per row)
   // grouped experts (null offsets = dense)
   bt_dtype y_dtype;
   const int32_t* moe_offsets;
@@ -31,9 +32,11 @@ struct GemvParams {
   int drop_stage;
 };
 
-// Batched launches: many independent GEMVs of the same K, bits and dtypes, each
-// with its own weight, x, y and N; the table travels in the kernel parameters.
-constexpr int kBatchCap = 192;
+// Batched launches: many independent GEMVs of the same bits and dtypes, each
+// with its own weight, x, y, N and (mixed-K batches) K; the table travels in
+// the kernel parameters.  Each problem carries its own row geometry: K, groups,
+// row bytes, warps per row (kw) and rows per pipeline unit (rb).
+constexpr int kBatchCap = 256;
 struct GemvProblem {
   const uint32_t* codes;
   const uint16_t* scales;
@@ -41,8 +44,10 @@ struct GemvProblem {
   const void* x;
   void* y;
   int n;
-  int units;          // row blocks of this problem (rows_per_unit each)
+  int k, g, row_bytes, kw, rb;
+  int units;          // row blocks of this problem (rb rows each)
   long long unit_begin;
+  long long cost_begin;   // work of the problems before this one (rows x warps per row)
 };
 template <int CAP> struct GemvBatch {
   int count;
@@ -58,6 +63,11 @@ struct GemvPlan {
 };
 
 GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
+// One launch over problems of several K (each K <= 8192, one chunk per lane):
+// fills every problem's geometry in `batch` and returns the launch plan
+// (stage size covering the largest unit); infeasible when the problems need
+// different kernel shapes.
+GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms);
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,
                         cudaStream_t stream, GemvBatch<kBatchCap>* batch = nullptr);
 

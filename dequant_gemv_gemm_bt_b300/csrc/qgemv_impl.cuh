@@ -25,6 +25,8 @@
 //    in shared memory behind a named barrier of that row group.  No atomics:
 //    results are bitwise deterministic.
 #pragma once
+#include <type_traits>
+
 #include "bt_common.cuh"
 #include "qgemv.cuh"
 
@@ -91,13 +93,11 @@ __device__ __forceinline__ void load_chunk(uint32_t saddr, const uint8_t* gptr, 
 }
 
 // ------------------------------------------------------------ fast path math
-// acc_lo += x_lo * h.lo and acc_hi += x_hi * h.hi: fp16 operands, fp32
-// accumulation, two independent chains.  x values live one per register
-// (unpacked once when loaded), so only the code pair is split here.
-__device__ __forceinline__ void fma_lohi(float& acc_lo, float& acc_hi, uint16_t x_lo, uint16_t x_hi, uint32_t hp) {
-  asm("{\n .reg .f16 ha, hb;\n mov.b32 {ha, hb}, %4;\n"
-      " fma.rn.f32.f16 %0, %2, ha, %0;\n fma.rn.f32.f16 %1, %3, hb, %1;\n}\n"
-      : "+f"(acc_lo), "+f"(acc_hi) : "h"(x_lo), "h"(x_hi), "r"(hp));
+// acc += x_lo * h.lo + x_hi * h.hi (one accumulator; two dependent FMAs).
+__device__ __forceinline__ void fma_pair(float& acc, uint16_t x_lo, uint16_t x_hi, uint32_t hp) {
+  asm("{\n .reg .f16 ha, hb;\n mov.b32 {ha, hb}, %3;\n"
+      " fma.rn.f32.f16 %0, %1, ha, %0;\n fma.rn.f32.f16 %0, %2, hb, %0;\n}\n"
+      : "+f"(acc) : "h"(x_lo), "h"(x_hi), "r"(hp));
 }
 
 __device__ __forceinline__ uint32_t lop_mask_or(uint32_t w, uint32_t mask) {
@@ -173,12 +173,14 @@ __device__ __forceinline__ void fast_pairs(uint32_t w, uint32_t (&h)[FastLayout<
 // ------------------------------------------------------------ x slices
 // Per chunk a lane keeps: the x values (layout depends on the path), sum(x)
 // over the chunk (for the bias term) and, on the fast path, the offset sum
-// Z = sum_j 1024 * x_j / c_j that removes the fp16 magic.
+// per class c the starting value -sum_{j in c} 1024 * x_j of that class's
+// accumulator, which removes the fp16 magic as the codes are accumulated.
 template <int BITS, bool FAST> struct XSlice;
 
 template <int BITS> struct XSlice<BITS, true> {
   uint16_t xh[32];   // fp16 x values of the chunk, one per register
-  float xsum, z;
+  float xsum;
+  float zc[FastClasses<BITS>::n];
 };
 template <int BITS> struct XSlice<BITS, false> {
   float xv[32];
@@ -200,7 +202,11 @@ __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_
   }
   using L = FastLayout<BITS>;
   constexpr int codes_per_word = 32 / BITS;
-  float xsum = 0.f, z = 0.f;
+  constexpr int NC = FastClasses<BITS>::n;
+  float xsum = 0.f;
+  float zc[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) zc[c] = 0.f;
 #pragma unroll
   for (int wd = 0; wd < BITS; ++wd) {
 #pragma unroll
@@ -208,11 +214,12 @@ __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_
       const float x0 = __half2float(__ushort_as_half(s.xh[wd * codes_per_word + L::pos(p, 0)]));
       const float x1 = __half2float(__ushort_as_half(s.xh[wd * codes_per_word + L::pos(p, 1)]));
       xsum += x0 + x1;
-      z += (x0 + x1) * (1024.f / L::mult(L::cls(p)));
+      zc[L::cls(p)] -= (x0 + x1) * 1024.f;
     }
   }
   s.xsum = xsum;
-  s.z = z;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) s.zc[c] = zc[c];
 }
 
 template <int BITS, bt_dtype XD>
@@ -239,22 +246,22 @@ __device__ __forceinline__ float chunk_dot_fast(const uint32_t (&w)[BITS], const
   using L = FastLayout<BITS>;
   constexpr int NC = FastClasses<BITS>::n;
   constexpr int codes_per_word = 32 / BITS;
-  float acc[NC][2];
+  float acc[NC];
 #pragma unroll
-  for (int c = 0; c < NC; ++c) acc[c][0] = acc[c][1] = 0.f;
+  for (int c = 0; c < NC; ++c) acc[c] = s.zc[c];
 #pragma unroll
   for (int wd = 0; wd < BITS; ++wd) {
     uint32_t h[L::pairs_per_word];
     fast_pairs<BITS>(w[wd], h);
 #pragma unroll
     for (int p = 0; p < L::pairs_per_word; ++p)
-      fma_lohi(acc[L::cls(p)][0], acc[L::cls(p)][1], s.xh[wd * codes_per_word + L::pos(p, 0)],
-               s.xh[wd * codes_per_word + L::pos(p, 1)], h[p]);
+      fma_pair(acc[L::cls(p)], s.xh[wd * codes_per_word + L::pos(p, 0)], s.xh[wd * codes_per_word + L::pos(p, 1)],
+               h[p]);
   }
-  float t = acc[0][0] + acc[0][1];
+  float t = acc[0];
 #pragma unroll
-  for (int c = 1; c < NC; ++c) t = fmaf(acc[c][0] + acc[c][1], 1.f / L::mult(c), t);
-  return t - s.z;
+  for (int c = 1; c < NC; ++c) t = fmaf(acc[c], 1.f / L::mult(c), t);
+  return t;
 }
 
 // sum_j q_j * x_j over one chunk (generic path, any bits).
@@ -358,6 +365,9 @@ struct ProbView {
   size_t y0;                 // element index of this problem's row 0 in y
   int n;                     // rows of the problem
   int units;                 // row blocks of the problem
+  int k, g, row_bytes;       // row geometry: codes per row, groups per row, packed bytes per row
+  int kw;                    // warps that share one row (K split)
+  int rb;                    // rows per pipeline unit
   bool valid;                // false: a grouped row that no expert holds (skipped)
 };
 
@@ -375,6 +385,11 @@ __device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch
     v.y0 = 0;
     v.n = q.n;
     v.units = q.units;
+    v.k = q.k;
+    v.g = q.g;
+    v.row_bytes = q.row_bytes;
+    v.kw = q.kw;
+    v.rb = q.rb;
     v.valid = true;
   } else {
     const int e = problem_expert(p, offs, prob);
@@ -387,6 +402,11 @@ __device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch
     v.y0 = (size_t)problem_yrow(p, prob) * p.N;
     v.n = p.N;
     v.units = p.units_per_problem;
+    v.k = p.K;
+    v.g = p.G;
+    v.row_bytes = p.row_bytes;
+    v.kw = p.kw;
+    v.rb = p.rows_per_unit;
     v.valid = e >= 0;
   }
   return v;
@@ -396,10 +416,10 @@ __device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch
 // 16-byte boundary and moves a multiple of 16 bytes; otherwise the consumers
 // read that unit straight from global memory.
 __device__ __forceinline__ bool unit_bulk(const GemvParams& p, const ProbView& v, int row0, int rows) {
-  const uintptr_t c0 = reinterpret_cast<uintptr_t>(v.codes) + (size_t)row0 * p.row_bytes;
-  const uintptr_t s0 = reinterpret_cast<uintptr_t>(v.scales + (size_t)row0 * p.G);
-  const uintptr_t b0 = reinterpret_cast<uintptr_t>(v.biases + (size_t)row0 * p.G);
-  const size_t cb = (size_t)rows * p.row_bytes, sb = (size_t)rows * p.G * 2;
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(v.codes) + (size_t)row0 * v.row_bytes;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(v.scales + (size_t)row0 * v.g);
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(v.biases + (size_t)row0 * v.g);
+  const size_t cb = (size_t)rows * v.row_bytes, sb = (size_t)rows * v.g * 2;
   return ((c0 | s0 | b0 | cb | sb) & 15u) == 0;
 }
 
@@ -421,6 +441,23 @@ __device__ __forceinline__ void first_unit(const GemvParams& p, const GemvBatch<
   }
 }
 
+// Batched launches: the first unit whose work starts at or after `c`, so that
+// CTA i takes the units starting in its equal share of the launch's work.
+__device__ __forceinline__ long long unit_at_cost(const GemvParams& p, const GemvBatch<kBatchCap>& batch,
+                                                  long long c) {
+  if (c >= p.total_cost) return p.num_units;
+  int lo = 0, hi = batch.count;   // last problem with cost_begin <= c
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (batch.prob[mid].cost_begin <= c) lo = mid; else hi = mid;
+  }
+  const GemvProblem& q = batch.prob[lo];
+  const long long uc = (long long)q.rb * q.kw;
+  const long long blk = (c - q.cost_begin + uc - 1) / uc;
+  if (blk < q.units) return q.unit_begin + blk;
+  return lo + 1 < batch.count ? batch.prob[lo + 1].unit_begin : p.num_units;
+}
+
 template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
 __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
     qgemv_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
@@ -434,9 +471,14 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
   int* offs = reinterpret_cast<int*>(red + kNW * 2 * RI);  // [E+1] when grouped
 
   // contiguous range of units for this CTA
-  const long long U = p.num_units;
-  const long long u_begin = U * blockIdx.x / gridDim.x;
-  const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
+  long long u_begin, u_end;
+  if constexpr (BATCH) {
+    u_begin = unit_at_cost(p, batch, p.total_cost * blockIdx.x / gridDim.x);
+    u_end = unit_at_cost(p, batch, p.total_cost * (blockIdx.x + 1) / gridDim.x);
+  } else {
+    u_begin = p.num_units * blockIdx.x / gridDim.x;
+    u_end = p.num_units * (blockIdx.x + 1) / gridDim.x;
+  }
 
   // full[s]: one arrive.expect_tx for the bulk copy of the codes plus one
   // cp.async-tracked arrive from each producer lane (scales and biases).
@@ -451,9 +493,6 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
   __syncthreads();
   pdl_launch_dependents();
 
-  const int RB = p.rows_per_unit;
-  const int row_bytes = p.row_bytes;
-  const int G = p.G;
   if (u_begin >= u_end) return;
 
   if (warp == kNW) {
@@ -477,6 +516,7 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
         if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
         if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; break; }
       }
+      const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
       const int row0 = blk * RB;
       const int rows = min(RB, v.n - row0);
       const bool drop = p.drop_stage && blockIdx.x == 0 && it == 0;   // test hook: never fill this stage
@@ -518,14 +558,9 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
   }
 
   // -------------------------------------------------------------- consumers
-  const int KW = p.kw;
-  const int RW = kNW / KW;
-  if (KW < 1 || RW < 1 || RW * KW != kNW) {   // never launched so by the planner; refuse rather than spin
-    if (threadIdx.x == 0) set_device_error(p.err, kErrBadArg);
-    return;
-  }
-  const int kw = warp % KW, rg = warp / KW;
-  const int nchunks = p.K / 32;
+  // KW warps share a row (K split), RW row groups per CTA; both follow the
+  // problem, so they are set when a unit of a new problem starts.
+  int KW = 0, RW = 0, kw = 0, rg = 0, nchunks = 0;
   const bool writer = (lane & (32 / RI - 1)) == 0;
   pdl_wait();   // activations (and offsets) may come from the previous kernel
 
@@ -542,6 +577,21 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
     if (prob != cur_prob) {
       cur_prob = prob;
       v = resolve<BATCH>(p, batch, offs, prob);
+      if (v.kw != KW) {
+        if (v.kw < 1 || kNW % v.kw) {   // never planned so; refuse rather than spin
+          if (threadIdx.x == 0) set_device_error(p.err, kErrBadArg);
+          return;
+        }
+        // The row groups change: every consumer warp leaves the previous
+        // problem's row-group barriers before any warp uses the new ones.
+        if (KW != 0) asm volatile("bar.sync 15, %0;" ::"r"(kNW * 32) : "memory");
+        KW = v.kw;
+        RW = kNW / KW;
+        kw = warp % KW;
+        rg = warp / KW;
+        rbuf = 0;
+      }
+      nchunks = v.k / 32;
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = (i * KW + kw) * 32 + lane;
@@ -552,6 +602,7 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
       }
     }
     if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) return;
+    const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
     const int row0 = blk * RB;
     const int rows = min(RB, v.n - row0);
     const bool tma = v.valid && unit_bulk(p, v, row0, rows);
@@ -563,6 +614,12 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
     const size_t ybase = v.y0 + row0;
 
     const int nb = (rows + RI - 1) / RI;
+    // The row batches of this unit.  Instantiated per (rows need clamping, unit
+    // staged in shared memory), chosen once per unit, so the common case -- a
+    // full unit in shared memory -- has no per-row bounds or source branches.
+    auto batches = [&](auto clamp_tag, auto staged_tag) {
+      constexpr bool CLAMP = decltype(clamp_tag)::value;
+      constexpr bool STAGED = decltype(staged_tag)::value;
     for (int bi = rg; bi < nb; bi += RW) {
       const int r0 = bi * RI;
       float part[RI];
@@ -576,8 +633,8 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
           float sc[RI], bs[RI];
 #pragma unroll
           for (int j = 0; j < RI; ++j) {
-            const int r = min(r0 + j, rows - 1);
-            if (tma) {
+            const int r = CLAMP ? min(r0 + j, rows - 1) : r0 + j;
+            if constexpr (STAGED) {
               load_chunk<BITS, true>(st + r * row_bytes + c * (4 * BITS), nullptr, w[j]);
               sc[j] = to_f32<BT_F16>(lds16(st_sc + (r * G + (c >> 1)) * 2));
               bs[j] = to_f32<BT_F16>(lds16(st_bi + (r * G + (c >> 1)) * 2));
@@ -612,6 +669,15 @@ __global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
         }
         rbuf ^= 1;
       }
+    }
+    };
+    using yes = std::integral_constant<bool, true>;
+    using no = std::integral_constant<bool, false>;
+    if (tma) {
+      if (rows == nb * RI) batches(no{}, yes{});
+      else batches(yes{}, yes{});
+    } else {
+      batches(yes{}, no{});
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);

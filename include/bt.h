@@ -80,22 +80,28 @@ BT_API bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const u
 
 /*
  * Batched dequant-GEMV: `count` independent M = 1 products in one launch, all
- * with the same K, bits, group size and dtypes, each with its own weight, x, y
- * and row count.  Persistent CTAs stream the problems' rows back to back, so a
- * decode step's many small GEMVs cost one launch instead of one each (BaseRT
- * pages, thetesserapress.com "Where the wins land": small models are
- * dispatch-bound; gist.science "Contribuições": low-overhead dispatch).
+ * with the same bits, group size and dtypes, each with its own weight, x, y,
+ * row count and (when K = 0) its own K.  Persistent CTAs stream the problems'
+ * rows back to back, so a decode step's many small GEMVs cost one launch
+ * instead of one each (BaseRT pages, thetesserapress.com "Where the wins
+ * land": small models are dispatch-bound; gist.science "Contribuições":
+ * low-overhead dispatch).
  *   problems  HOST array of `count` descriptors (read during the call only;
  *             the pointers in it are device memory, 16-byte aligned)
- * Limits: 1 <= count <= 192, 64 <= K <= 32768 (K <= 16384 for bf16 x or odd bits).
+ *   K         > 0: every problem has this K (the descriptors' k is ignored);
+ *             0: each problem uses its descriptor's k (a mixed-K batch, e.g. a
+ *             whole decode step in one launch)
+ * Limits: 1 <= count <= 256; one K: 64 <= K <= 32768 (K <= 16384 for bf16 x
+ * or odd bits); mixed K: every k in [64, 8192], a multiple of 64.
  */
 typedef struct {
-  const uint32_t* codes;     /* [n, K*bits/32] */
-  const uint16_t* scales;    /* [n, K/g] fp16 */
-  const uint16_t* biases;    /* [n, K/g] fp16 */
-  const void* x;             /* [K] of x_dtype */
+  const uint32_t* codes;     /* [n, k*bits/32] */
+  const uint16_t* scales;    /* [n, k/g] fp16 */
+  const uint16_t* biases;    /* [n, k/g] fp16 */
+  const void* x;             /* [k] of x_dtype */
   void* y;                   /* [n] of y_dtype */
   int32_t n;                 /* rows, >= 1 */
+  int32_t k;                 /* this problem's K when the call's K is 0 */
 } bt_gemv_problem;
 BT_API bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size,
                                   int K, bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream);
@@ -214,6 +220,7 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMM_SPLITS   tuning: tensor-core GEMM K split across a cluster (0 = heuristic, 1..8).
  *   BT_OPT_GEMV_MAX_CPL  tuning: GEMV chunks of 32 codes per lane before K is split
  *                       over more warps (0 = heuristic, else 1..4).
+ *   BT_OPT_GEMV_STAGE_KB tuning: GEMV pipeline stage size in KiB (0 = heuristic, else 4..96).
  */
 typedef enum {
   BT_OPT_PDL = 0,
@@ -224,7 +231,8 @@ typedef enum {
   BT_OPT_GEMV_STAGES = 5,
   BT_OPT_GEMM_PATH = 6,
   BT_OPT_GEMM_SPLITS = 7,
-  BT_OPT_GEMV_MAX_CPL = 8
+  BT_OPT_GEMV_MAX_CPL = 8,
+  BT_OPT_GEMV_STAGE_KB = 9
 } bt_option;
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);

@@ -177,10 +177,42 @@ def test_qgemv_batched_rejects_bad_tables(env):
     x = half_tensor(x16[0], "f16", torch)
     y = torch.empty(64, device="cuda")
     with pytest.raises(bt.BTError):
-        bt.bt_qgemv_batched([(codes, scales, biases, x, y)] * 193, 4)      # over the table capacity
+        bt.bt_qgemv_batched([(codes, scales, biases, x, y)] * 257, 4)      # over the table capacity
     x2 = torch.zeros(2048, dtype=torch.float16, device="cuda")
     with pytest.raises(ValueError):
-        bt.bt_qgemv_batched([(codes, scales, biases, x, y), (codes, scales, biases, x2, y)], 4)   # mixed K
+        bt.bt_qgemv_batched([(codes, scales, biases, x, y), (codes, scales, biases, x2, y)], 4)   # x/codes K differ
+    qb, _ = make_case("batched-bad-big", 8, 16384, 4)
+    cb, sb, bb = to_dev(qb, torch)
+    xb = torch.zeros(16384, dtype=torch.float16, device="cuda")
+    yb = torch.empty(8, device="cuda")
+    with pytest.raises(bt.BTError):   # a mixed-K batch takes K <= 8192 only
+        bt.bt_qgemv_batched([(codes, scales, biases, x, y), (cb, sb, bb, xb, yb)], 4)
+    assert bt.bt_last_device_error() == bt.BT_OK
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_qgemv_batched_mixed_k(env, bits):
+    """Problems of different K in one launch (the warps sharing a row change between
+    problems), in an order that alternates K so every CTA crosses several changes."""
+    torch, bt = env
+    from dequant_gemv_gemm_bt_b300 import synth
+    r = synth.rng_for("test", "batched-mixed", bits)
+    ks = [1024, 2048, 64, 3072, 1024, 8192, 576, 2048, 128, 1024, 4096, 3072] * 3
+    cases, probs = [], []
+    for i, k in enumerate(ks):
+        n = int(r.integers(1, 900))
+        qw = synth.make_qweight(r, n, k, bits)
+        x16 = synth.draw_activations(r, 1, k, "f16")
+        codes, scales, biases = to_dev(qw, torch)
+        y = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+        probs.append((codes, scales, biases, half_tensor(x16[0], "f16", torch), y))
+        cases.append((qw, x16))
+    bt.bt_qgemv_batched(probs, bits)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for (qw, x16), pr in zip(cases, probs):
+        y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x16[0]))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"mixed b={bits} n={qw.n} k={qw.k}")
 
 
 # One Llama-3.2-1B-shaped layer (hidden 2048): q/o 2048->2048, k/v 2048->512,

@@ -31,7 +31,7 @@ BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_MISALIGNED, BT_ERR_CUDA, B
 BT_F16, BT_BF16, BT_F32 = 0, 1, 2
 (BT_OPT_PDL, BT_OPT_CONST_WEIGHTS, BT_OPT_WAIT_TIMEOUT_US, BT_OPT_TEST_DROP_STAGE,
  BT_OPT_GEMV_GENERIC, BT_OPT_GEMV_STAGES, BT_OPT_GEMM_PATH, BT_OPT_GEMM_SPLITS, BT_OPT_GEMV_MAX_CPL,
- BT_OPT_GEMV_STAGE_KB) = range(10)
+ BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI) = range(11)
 
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_route", "bt_swiglu", "bt_moe_combine",
            "bt_status_string", "bt_last_device_error", "bt_set_option")

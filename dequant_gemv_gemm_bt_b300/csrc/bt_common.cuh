@@ -31,6 +31,7 @@ struct LaunchOpts {
   int gemm_splits = 0;       // tuning: tensor-core GEMM K split (0 = heuristic)
   int gemv_max_cpl = 0;      // tuning: GEMV chunks per lane before splitting K over warps (0 = heuristic)
   int gemv_stage_kb = 0;     // tuning: GEMV stage size in KiB (0 = heuristic)
+  int gemv_ri = 0;           // tuning: GEMV rows in flight per warp (0 = heuristic)
 };
 LaunchOpts& opts();
 unsigned* device_error_word();   // device address of the error word (current device)

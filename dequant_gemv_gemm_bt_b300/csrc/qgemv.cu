@@ -55,9 +55,13 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   const long long rows_total = (long long)N * problems;
   const long long per_sm = std::max<long long>(1, (rows_total + sms - 1) / sms);
   int ri = pl.cpl == 1 ? 4 : (pl.cpl == 2 ? 2 : 1);   // keep x slices and RI rows of codes in registers
-  const int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
+  if (opts().gemv_ri > 0) ri = std::min(ri, opts().gemv_ri);
+  int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
   while (ri > 1 && ((long long)ri * rw * per_row > stage_budget || ri * rw > std::max<long long>(rw, per_sm))) ri /= 2;
   pl.ri = ri;
+  const int ctas_per_sm = gemv_ctas_per_sm(pl.cpl, ri);   // must match the kernel's launch bounds
+  // two stages of every resident CTA fit the SM's shared memory
+  stage_budget = std::min<int>(stage_budget, (int)((kMaxSmem / ctas_per_sm - 1024) / 2));
   const int unit = std::max(ri * rw, m);
   int rb = unit * std::max(1, stage_budget / (unit * per_row));
   const long long want = ((per_sm + unit - 1) / unit) * unit;
@@ -67,7 +71,6 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   pl.row_bytes = row_bytes;
   const int stage = (rb * per_row + 127) / 128 * 128;
   pl.stage_bytes = stage;
-  const int ctas_per_sm = pl.cpl == 1 ? 2 : 1;   // must match the kernel's launch bounds
   int stages = std::max(2, std::min(8, (kRingBudget / ctas_per_sm) / stage));
   if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
   pl.stages = stages;
@@ -89,9 +92,9 @@ GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int s
   pl.fast = fast;
   pl.feasible = false;
   pl.cpl = 1;
-  const int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
   // rows in flight per warp: 4 unless some problem's row group would overflow a stage
-  int ri = 4;
+  int ri = opts().gemv_ri > 0 ? std::min(4, opts().gemv_ri) : 4;
+  int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
   for (int i = 0; i < batch.count; ++i) {
     const GemvProblem& q = batch.prob[i];
     if (q.k <= 0 || q.k % kGroup || q.k > 8 * 32 * 32) return pl;   // one chunk per lane needs K <= 8192
@@ -101,6 +104,9 @@ GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int s
     const int per_row = q.k * bits / 8 + 4 * (q.k / kGroup);
     while (ri > 1 && ri * (kMaxNW / kw) * per_row > stage_budget) ri /= 2;
   }
+  const int ctas_per_sm = gemv_ctas_per_sm(1, ri);   // one chunk per lane (the kernel's launch bounds)
+  // two stages of every resident CTA fit the SM's shared memory
+  stage_budget = std::min<int>(stage_budget, (int)((kMaxSmem / ctas_per_sm - 1024) / 2));
   int stage = 0;
   for (int i = 0; i < batch.count; ++i) {
     GemvProblem& q = batch.prob[i];
@@ -124,7 +130,6 @@ GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int s
   pl.rows_per_unit = batch.prob[0].rb;
   pl.row_bytes = batch.prob[0].row_bytes;
   pl.stage_bytes = stage;
-  const int ctas_per_sm = 2;   // one chunk per lane: two CTAs per SM (the kernel's launch bounds)
   int stages = std::max(2, std::min(8, (kRingBudget / ctas_per_sm) / stage));
   if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
   auto smem_for = [&](int st) {
@@ -171,7 +176,7 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
     p.total_cost = cost;
     p.num_units = u;
     plb.num_units = u;
-    plb.grid = (int)std::min<long long>(u, (long long)sm_count() * (pl.cpl == 1 ? 2 : 1));
+    plb.grid = (int)std::min<long long>(u, (long long)sm_count() * gemv_ctas_per_sm(pl.cpl, pl.ri));
   }
   if (p.num_units == 0) return cudaSuccess;
   switch (bits) {

@@ -62,6 +62,10 @@ struct GemvPlan {
   size_t smem;
 };
 
+// CTAs per SM the kernel is built for (its launch bounds): one x chunk per lane
+// runs 2 CTAs with 4 rows in flight per warp, 3 with 2 or fewer; else 1.
+inline int gemv_ctas_per_sm(int cpl, int ri) { return cpl == 1 ? (ri <= 2 ? 3 : 2) : 1; }
+
 GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
 // One launch over problems of several K (each K <= 8192, one chunk per lane):
 // fills every problem's geometry in `batch` and returns the launch plan

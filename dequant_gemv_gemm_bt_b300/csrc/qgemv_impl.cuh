@@ -301,14 +301,15 @@ __device__ __forceinline__ int problem_yrow(const GemvParams& p, int prob) { ret
 
 
 // --------------------------------------------------------------- the kernel
-// Consumer warps per CTA: 8, which leaves each thread up to 168 registers so
-// the fp16 x values stay one per register (a tighter cap makes the compiler
-// pack them in pairs and pay an extract per FMA).  One more warp is the producer.
-template <int CPL> struct Warps {
+// Consumer warps per CTA: 8, plus one producer warp.  One x chunk per lane
+// (CPL = 1) fits two CTAs per SM (16 consumer warps, up to 112 registers) with
+// four rows in flight per warp, or three CTAs (24 consumer warps, up to 75
+// registers) with two; more chunks per lane keep x in more registers and run
+// one CTA per SM.
+template <int CPL, int RI> struct Warps {
   static constexpr int kNW = 8;
   static constexpr int kThreads = (kNW + 1) * 32;
-  // one x chunk per lane fits two CTAs per SM (16 consumer warps) within 112 registers
-  static constexpr int kMinBlocks = CPL == 1 ? 2 : 1;
+  static constexpr int kMinBlocks = CPL == 1 ? (RI <= 2 ? 3 : 2) : 1;
 };
 
 // Sum RI per-row partials over the 32 lanes with a transpose-style tree.  On
@@ -459,9 +460,9 @@ __device__ __forceinline__ long long unit_at_cost(const GemvParams& p, const Gem
 }
 
 template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
-__global__ void __launch_bounds__(Warps<CPL>::kThreads, Warps<CPL>::kMinBlocks)
+__global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMinBlocks)
     qgemv_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
-  constexpr int kNW = Warps<CPL>::kNW;
+  constexpr int kNW = Warps<CPL, RI>::kNW;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.stages;
@@ -696,7 +697,7 @@ cudaError_t launch_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(Warps<CPL>::kThreads);
+  cfg.blockDim = dim3(Warps<CPL, RI>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

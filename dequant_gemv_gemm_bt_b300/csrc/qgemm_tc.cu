@@ -32,6 +32,17 @@ namespace tc {
 constexpr int BM = 128;                  // weight rows per tile (MMA M)
 constexpr int BK = 64;                   // K per stage = one quantization group
 constexpr int kDeqWarps = 8;
+// A ring in tensor memory: the dequant warps write each K block's 128 x 64 bf16
+// A tile into one of kAStages 32-column slots (column j holds k = 2j, 2j+1 of
+// the row in that lane) and the MMA reads it from there, so A never passes
+// through shared memory (whose bandwidth the MMA's B operand and the TMA
+// writes already need).
+constexpr int kAStages = 4;
+template <int BN> constexpr int acc_cols() { return BN < 32 ? 32 : BN; }
+template <int BN> constexpr int tmem_cols() {
+  constexpr int need = acc_cols<BN>() + kAStages * 32;
+  return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
+}
 constexpr int kThreads = (2 + kDeqWarps) * 32;
 
 struct TcParams {
@@ -39,9 +50,9 @@ struct TcParams {
   int splits;              // CTAs of a cluster splitting K (gridDim.z); 1 = no split
   int gc_max;              // most groups any split stages
   int stages;              // TMA ring depth (X tile + packed codes per K block)
-  int astages;             // A ring depth (dequantized weight tile per K block)
+  int astages;             // A ring depth (TMEM slots of dequantized weight tiles)
   int bn;
-  uint32_t stage_bytes, a_bytes, x_bytes, c_bytes;   // stage_bytes: one TMA-ring slot
+  uint32_t stage_bytes, x_bytes, c_bytes;   // stage_bytes: one TMA-ring slot
   const uint16_t* scales;
   const uint16_t* biases;
   void* y;
@@ -91,14 +102,26 @@ __host__ __device__ constexpr uint32_t make_idesc(bool bf16, int n) {
          ((uint32_t)(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
+// D (TMEM) [+]= A (TMEM) x B (shared memory descriptor).
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
           tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-wide, lanes of the warp's quarter).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -143,9 +166,6 @@ __device__ __forceinline__ uint16_t lds16(uint32_t a) {
 }
 __device__ __forceinline__ void lds128(uint32_t a, uint32_t& x, uint32_t& y, uint32_t& z, uint32_t& w) {
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "r"(a));
-}
-__device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 __device__ __forceinline__ float4 lds128f(uint32_t a) {
   float4 v;
@@ -293,10 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb_hi = split == p.splits - 1 ? p.G : (((split + 1) * p.G) / p.splits) & ~1;
   const int KB = kb_hi - kb_lo;
   const int Gc = KB;                       // groups staged for this CTA
-  // shared memory: [A ring: SA x 16 KB][TMA ring: S x (X tile | codes)][scales][biases][barriers]
-  const int SA = p.astages;
-  uint8_t* aring = smem;
-  uint8_t* tring = smem + (size_t)SA * p.a_bytes;
+  // shared memory: [TMA ring: S x (X tile | codes)][scales][biases][barriers]; the A ring is in TMEM
+  const int SA = p.astages;   // A slots in use (<= kAStages, < S)
+  uint8_t* tring = smem;
   uint16_t* sS = reinterpret_cast<uint16_t*>(tring + (size_t)S * p.stage_bytes);  // [128][Gc]
   uint16_t* sB = sS + BM * p.gc_max;                                               // [128][Gc]
   uint64_t* bars = reinterpret_cast<uint64_t*>(
@@ -304,8 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = bars;             // [S] X + codes landed
   uint64_t* empty = bars + S;        // [S] MMAs reading the slot's X done
   uint64_t* afull = bars + 2 * S;    // [SA] A tile written
-  uint64_t* aempty = afull + SA;     // [SA] MMAs reading the A tile done
-  uint64_t* tmem_full = aempty + SA;
+  uint64_t* tmem_full = afull + kAStages;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(tmem_full + 1);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -313,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int m0 = blockIdx.y * BN;     // first grouped/dense row of the tile
   int m_end = p.M;              // one past its last valid row
   int expert = 0;
-  constexpr int kTmemCols = BN < 32 ? 32 : BN;
+  constexpr int kTmemCols = tmem_cols<BN>();
+  constexpr uint32_t kACol0 = acc_cols<BN>();   // first column of the A slots
 
   if constexpr (GROUPED) {
     // Tile blockIdx.y of the expert-major list of (expert, BN-row tile) pairs;
@@ -366,7 +385,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < SA; ++a) {
       mbar_init(&afull[a], kDeqWarps);
-      mbar_init(&aempty[a], 1);
     }
     mbar_init(tmem_full, 1);
     *fail = 0;
@@ -459,19 +477,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0, a = 0;
       uint32_t ph = 0, aph = 0;
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err) || !mbar_wait(&afull[a], aph, p.timeout_ns, p.err)) {
+        // The dequant warps arrive on afull only after their own wait on this
+        // K block's stage, so the stage's X tile has landed too.  (Each wait or
+        // tcgen05 instruction costs this single thread ~60-100 cycles, and it
+        // is the one that feeds the tensor core.)
+        if (!mbar_wait(&afull[a], aph, p.timeout_ns, p.err)) {
           *fail = 1;
           break;
         }
         tc_fence_after();
-        fence_proxy_async();   // X rows written by cp.async / zero fill are read by the tensor core
-        const uint64_t adesc = sw128_desc(smem_u32(aring) + (uint32_t)(a * p.a_bytes));
+        if constexpr (GROUPED) fence_proxy_async();   // X rows written by cp.async / zero fill are read by the tensor core
+        const uint32_t a_tmem = tmem_base + kACol0 + (uint32_t)(a * 32);
         const uint64_t bdesc = sw128_desc(smem_u32(tring) + (uint32_t)(s * p.stage_bytes));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)   // 16 elements = 32 bytes per MMA step
-          mma_f16(tmem_base, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
-        mma_commit(&empty[s]);
-        mma_commit(&aempty[a]);
+        for (int kk = 0; kk < BK / 16; ++kk)   // 16 elements: 8 TMEM columns of A, 32 bytes of B per MMA step
+          mma_f16_ta(tmem_base, a_tmem + (uint32_t)(kk * 8), bdesc + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+        mma_commit(&empty[s]);   // frees the TMA stage, and the A slot for K block kb + SA
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++a == SA) { a = 0; aph ^= 1u; }
       }
@@ -480,7 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- dequant warps
     const int t = threadIdx.x - 64;        // 0..255
-    const int r = t >> 1, h = t & 1;       // row of the tile, which 4 of its 8 chunks
+    // warp w may access TMEM lanes 32*(w%4)..: it dequantizes those 32 rows, the
+    // first four warps the low 32 codes of each K block, the last four the high 32
+    const int r = 32 * (warp & 3) + lane, h = (warp - 2) >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     // stage this CTA's scales and biases: rows n0..n0+127, groups kb_begin..+Gc
     for (int i = t; i < BM * (Gc / 2); i += kDeqWarps * 32) {
       const int rr = i / (Gc / 2), gg = 2 * (i % (Gc / 2));
@@ -500,9 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int s = 0, a = 0;
     uint32_t ph = 0, aph = 0;
+    int sp = 0;          // stage of K block kb - SA, whose MMA commit frees this A slot
+    uint32_t pp = 0;     // parity of that commit on empty[sp]
     for (int kb = 0; kb < KB; ++kb) {
       if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) { *fail = 1; break; }
-      if (kb >= SA && !mbar_wait(&aempty[a], aph ^ 1u, p.timeout_ns, p.err)) { *fail = 1; break; }
+      if (kb >= SA) {
+        // empty[sp] completes once per use of the stage; with S > SA its next
+        // completion needs K block kb - SA + S, which is not dequantized yet,
+        // so the phase awaited here is the one of K block kb - SA.
+        if (!mbar_wait(&empty[sp], pp, p.timeout_ns, p.err)) { *fail = 1; break; }
+        if (++sp == S) { sp = 0; pp ^= 1u; }
+      }
       const uint32_t st = smem_u32(tring) + (uint32_t)(s * p.stage_bytes);
       const uint32_t caddr = st + p.x_bytes + r * (8 * BITS) + h * (4 * BITS);
       uint32_t w[BITS];
@@ -519,13 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b2 = half_pair<BF16>(lds16(sB_a + (uint32_t)(r * Gc + kb) * 2));
       uint4 out[4];
       deq32<BITS, BF16>(w, s2, b2, out);
-      const uint32_t arow = smem_u32(aring) + (uint32_t)(a * p.a_bytes) + r * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int chunk = 4 * h + c;
-        sts128(arow + ((chunk ^ (r & 7)) << 4), out[c]);
-      }
-      fence_proxy_async();
+      const uint32_t v[16] = {out[0].x, out[0].y, out[0].z, out[0].w, out[1].x, out[1].y, out[1].z, out[1].w,
+                              out[2].x, out[2].y, out[2].z, out[2].w, out[3].x, out[3].y, out[3].z, out[3].w};
+      tmem_st16(tmem_base + lane_base + kACol0 + (uint32_t)(a * 32 + 16 * h), v);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[a]);
       if (++s == S) { s = 0; ph ^= 1u; }
@@ -650,17 +680,16 @@ size_t tc_smem_bytes(int K, int splits, int* stages_out) {
     if (hi - lo < 1) return 0;
     gc_max = std::max(gc_max, hi - lo);
   }
-  const uint32_t a_bytes = BM * BK * 2, x_bytes = BN * BK * 2, c_bytes = BM * 8 * BITS;
+  const uint32_t x_bytes = BN * BK * 2, c_bytes = BM * 8 * BITS;
   const uint32_t stage_bytes = (x_bytes + c_bytes + 1023u) & ~1023u;
-  const int astages = 2;
   const size_t params_bytes = (size_t)2 * BM * gc_max * sizeof(uint16_t);
-  const size_t fixed = 1024 + params_bytes + 8 + (size_t)(2 * 12 + 2 * 2 + 1) * 8 + 16 + (size_t)astages * a_bytes;
+  const size_t fixed = 1024 + params_bytes + 8 + (size_t)(2 * 12 + 2 * kAStages + 1) * 8 + 16;
   const size_t budget = (GROUPED && BN <= 32) ? 112 * 1024 : 222 * 1024;
   int stages = (int)((budget - std::min(budget, fixed)) / stage_bytes);
   stages = std::max(2, std::min(12, stages));
   const int chunks = BN / 16, owned_max = (chunks + splits - 1) / splits;
   const size_t recv_bytes = splits > 1 ? (size_t)splits * BM * owned_max * 16 * 4 : 0;
-  while ((size_t)stages * stage_bytes + (size_t)astages * a_bytes < recv_bytes) ++stages;
+  while ((size_t)stages * stage_bytes < recv_bytes) ++stages;
   if (stages_out) *stages_out = stages;
   return fixed + (size_t)stages * stage_bytes;
 }
@@ -723,7 +752,6 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   }
   p.gc_max = gc_max;
   p.bn = BN;
-  p.a_bytes = BM * BK * 2;
   p.x_bytes = BN * BK * 2;
   p.c_bytes = BM * 8 * BITS;
   p.stage_bytes = (p.x_bytes + p.c_bytes + 1023u) & ~1023u;
@@ -737,11 +765,11 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.offsets = gp.offsets;
   p.row_index = gp.row_index;
   p.num_experts = gp.num_experts;
-  p.astages = 2;
   int stages = 0;
   const size_t smem = tc_smem_bytes<BITS, BN, GROUPED>(gp.K, splits, &stages);
   if (smem == 0) return cudaErrorInvalidValue;
   p.stages = stages;
+  p.astages = std::min(kAStages, stages - 1);   // the dequant waits rely on S > SA
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED>;
   static std::atomic<uint64_t> smem_raised{0};

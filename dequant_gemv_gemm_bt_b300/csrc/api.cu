@@ -149,7 +149,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMM_PATH: opts().gemm_path = (int)value; return BT_OK;
     case BT_OPT_GEMM_SPLITS: opts().gemm_splits = (int)std::min<long long>(value, 8); return BT_OK;
     case BT_OPT_GEMV_MAX_CPL: opts().gemv_max_cpl = (int)std::min<long long>(value, 4); return BT_OK;
-    case BT_OPT_GEMV_RI: opts().gemv_ri = value >= 4 ? 4 : (value >= 2 ? 2 : (int)value); return BT_OK;
+    case BT_OPT_GEMV_RI: opts().gemv_ri = value >= 8 ? 8 : value >= 4 ? 4 : (value >= 2 ? 2 : (int)value); return BT_OK;
     case BT_OPT_GEMV_STAGE_KB: opts().gemv_stage_kb = value == 0 ? 0 : (int)std::max(4LL, std::min(value, 96LL)); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;

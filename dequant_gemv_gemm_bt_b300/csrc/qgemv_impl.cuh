@@ -303,9 +303,9 @@ __device__ __forceinline__ int problem_yrow(const GemvParams& p, int prob) { ret
 // --------------------------------------------------------------- the kernel
 // Consumer warps per CTA: 8, plus one producer warp.  One x chunk per lane
 // (CPL = 1) fits two CTAs per SM (16 consumer warps, up to 112 registers) with
-// four rows in flight per warp, or three CTAs (24 consumer warps, up to 75
-// registers) with two; more chunks per lane keep x in more registers and run
-// one CTA per SM.
+// four or eight rows in flight per warp, or three CTAs (24 consumer warps, up
+// to 75 registers) with two; more chunks per lane keep x in more registers and
+// run one CTA per SM.
 template <int CPL, int RI> struct Warps {
   static constexpr int kNW = 8;
   static constexpr int kThreads = (kNW + 1) * 32;
@@ -317,7 +317,29 @@ template <int CPL, int RI> struct Warps {
 // with (lane & (32/RI - 1)) == 0 are the first holder of each row.
 template <int RI>
 __device__ __forceinline__ float reduce_rows(const float (&part)[RI], int lane, int& row) {
-  if constexpr (RI == 4) {
+  if constexpr (RI == 8) {
+    // 9 shuffles for 8 rows: halve the row set at lane bits 16, 8 and 4, then sum
+    const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+    float a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float keep = b16 ? part[4 + i] : part[i], give = b16 ? part[i] : part[4 + i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+    }
+    float c[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float keep = b8 ? a[2 + i] : a[i], give = b8 ? a[i] : a[2 + i];
+      c[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+    }
+    float e = b4 ? c[1] : c[0];
+    const float f = b4 ? c[0] : c[1];
+    e += __shfl_xor_sync(0xffffffffu, f, 4);
+    e += __shfl_xor_sync(0xffffffffu, e, 2);
+    e += __shfl_xor_sync(0xffffffffu, e, 1);
+    row = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+    return e;
+  } else if constexpr (RI == 4) {
     const bool hi = lane & 16;
     float a0 = hi ? part[2] : part[0], a1 = hi ? part[3] : part[1];
     const float b0 = hi ? part[0] : part[2], b1 = hi ? part[1] : part[3];
@@ -716,6 +738,9 @@ cudaError_t launch_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int
 template <int BITS, bt_dtype XD, int CPL, bool FAST, bool BATCH>
 cudaError_t launch_ri(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b, cudaStream_t st) {
   switch (pl.ri) {
+    case 8:
+      if constexpr (CPL == 1) return launch_t<BITS, XD, CPL, FAST, 8, BATCH>(p, b, pl.grid, pl.smem, st);
+      [[fallthrough]];
     case 4: return launch_t<BITS, XD, CPL, FAST, 4, BATCH>(p, b, pl.grid, pl.smem, st);
     case 2: return launch_t<BITS, XD, CPL, FAST, 2, BATCH>(p, b, pl.grid, pl.smem, st);
     default: return launch_t<BITS, XD, CPL, FAST, 1, BATCH>(p, b, pl.grid, pl.smem, st);

@@ -221,7 +221,7 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMV_MAX_CPL  tuning: GEMV chunks of 32 codes per lane before K is split
  *                       over more warps (0 = heuristic, else 1..4).
  *   BT_OPT_GEMV_STAGE_KB tuning: GEMV pipeline stage size in KiB (0 = heuristic, else 4..96).
- *   BT_OPT_GEMV_RI       tuning: GEMV rows in flight per warp (0 = heuristic, else 1, 2 or 4).
+ *   BT_OPT_GEMV_RI       tuning: GEMV rows in flight per warp (0 = heuristic, else 1, 2, 4 or 8).
  */
 typedef enum {
   BT_OPT_PDL = 0,

@@ -506,16 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * (warp & 3) + lane, h = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     // stage this CTA's scales and biases: rows n0..n0+127, groups kb_begin..+Gc
-    for (int i = t; i < BM * (Gc / 2); i += kDeqWarps * 32) {
-      const int rr = i / (Gc / 2), gg = 2 * (i % (Gc / 2));
-      const int n = n0 + rr;
-      if (n < p.N) {
-        const size_t off = ((size_t)expert * p.N + n) * p.G + kb_lo + gg;
-        cp_async4(sS + rr * Gc + gg, p.scales + off);
-        cp_async4(sB + rr * Gc + gg, p.biases + off);
-      } else {
-        *reinterpret_cast<uint32_t*>(sS + rr * Gc + gg) = 0u;
-        *reinterpret_cast<uint32_t*>(sB + rr * Gc + gg) = 0u;
+    const size_t row0 = ((size_t)expert * p.N + n0) * p.G;   // first staged parameter of the tile
+    if (Gc == p.G && n0 + BM <= p.N &&
+        (((reinterpret_cast<uintptr_t>(p.scales + row0) | reinterpret_cast<uintptr_t>(p.biases + row0)) & 15u) == 0)) {
+      // whole rows: the tile's parameters are one contiguous block per array, laid
+      // out as in shared memory, so they move in 16-byte pieces
+      const uint8_t* gs = reinterpret_cast<const uint8_t*>(p.scales + row0);
+      const uint8_t* gb = reinterpret_cast<const uint8_t*>(p.biases + row0);
+      for (int i = t; i < BM * Gc * 2 / 16; i += kDeqWarps * 32) {
+        cp_async16(reinterpret_cast<uint8_t*>(sS) + i * 16, gs + i * 16);
+        cp_async16(reinterpret_cast<uint8_t*>(sB) + i * 16, gb + i * 16);
+      }
+    } else {
+      for (int i = t; i < BM * (Gc / 2); i += kDeqWarps * 32) {
+        const int rr = i / (Gc / 2), gg = 2 * (i % (Gc / 2));
+        const int n = n0 + rr;
+        if (n < p.N) {
+          const size_t off = ((size_t)expert * p.N + n) * p.G + kb_lo + gg;
+          cp_async4(sS + rr * Gc + gg, p.scales + off);
+          cp_async4(sB + rr * Gc + gg, p.biases + off);
+        } else {
+          *reinterpret_cast<uint32_t*>(sS + rr * Gc + gg) = 0u;
+          *reinterpret_cast<uint32_t*>(sB + rr * Gc + gg) = 0u;
+        }
       }
     }
     cp_async_wait_all();

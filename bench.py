@@ -257,6 +257,20 @@ def capture(torch, fn, stream):
     return g
 
 
+def max_over_ranks(torch, dist, seconds, device):
+    """The slowest rank's timed seconds (every rank gets it); `seconds` itself on one GPU."""
+    if dist is None:
+        return seconds
+    tt = torch.tensor([seconds], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return tt.item()
+
+
+def whole_job_rate(units_per_step, steps, world, seconds):
+    """Units all ranks processed per second, each of `world` replicas doing `units_per_step`."""
+    return units_per_step * steps * world / seconds
+
+
 def timed(torch, dist, stream, fn, steps, warmup, gpu_index):
     for _ in range(warmup):
         fn()
@@ -621,14 +635,11 @@ def main():
             t_single, _ = timed(torch, None, stream, lambda: graph_single.replay(), max(3, args.steps // 4), 3,
                                 local_rank)
     single_gbs = pass_bytes * max(3, args.steps // 4) / t_single / 1e9 if graph_single is not None else None
-    if dist is not None:
-        tt = torch.tensor([t_pass], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_pass = tt.item()
+    t_pass = max_over_ranks(torch, dist, t_pass, dev)
     if bt.bt_last_device_error() != bt.BT_OK:
         raise RuntimeError("device error during the timed region")
     sec_per_step = t_pass / args.steps
-    value = pass_bytes * args.steps * world / t_pass / 1e9
+    value = whole_job_rate(pass_bytes, args.steps, world, t_pass) / 1e9
 
     # lm_head alone (the largest single GEMV), for context
     lm = bufs[-1]
@@ -669,11 +680,8 @@ def main():
     e2e_steps = max(3, min(args.steps, 200))
     with torch.cuda.stream(stream):
         t_e2e, _ = timed(torch, dist, stream, e2e_step, e2e_steps, 3, local_rank)
-    if dist is not None:
-        tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = tt.item()
-    e2e_val = pass_bytes * e2e_steps * world / t_e2e / 1e9
+    t_e2e = max_over_ranks(torch, dist, t_e2e, dev)
+    e2e_val = whole_job_rate(pass_bytes, e2e_steps, world, t_e2e) / 1e9
 
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])

@@ -345,3 +345,69 @@ def test_planted_mistakes_are_caught(monkeypatch):
             if not np.allclose(y_bad, want, rtol=1e-9, atol=1e-12):
                 caught += 1
     assert caught == len(mutants)
+
+
+def silu_pins_hold(f) -> bool:
+    """Values of x*sigma(x) fixed by the logistic function itself, not by a formula."""
+    ln3 = np.log(3.0)
+    x = np.linspace(-20.0, 20.0, 81)
+    return bool(f(np.array([0.0]))[0] == 0.0
+                and np.allclose(f(np.array([ln3, -ln3])), [0.75 * ln3, -0.25 * ln3], rtol=1e-15, atol=0)  # sigma(ln 3) = 3/4
+                and np.allclose(f(-x), f(x) - x, rtol=1e-12, atol=1e-12)   # x*s(-x) = x*s(x) - x
+                and np.allclose(f(np.array([60.0])), [60.0], rtol=1e-15, atol=0)   # s(x) -> 1
+                and abs(f(np.array([-60.0]))[0]) < 1e-20)                  # s(x) -> 0
+
+
+def test_silu_closed_forms():
+    assert silu_pins_hold(O.silu)
+
+
+def test_planted_silu_mistakes_are_caught():
+    mutants = [lambda v: v / (1.0 + np.exp(v)),          # sign slip in the exponent
+               lambda v: 1.0 / (1.0 + np.exp(-v)),       # sigmoid without the factor v
+               lambda v: v * np.tanh(v),                 # a different gate
+               lambda v: v / (1.0 + np.exp(-2.0 * v))]   # wrong slope
+    assert not any(silu_pins_hold(f) for f in mutants)
+
+
+def test_moe_combine_is_the_gate_weighted_sum_of_single_slot_layers():
+    """Top-2 layer = g0 * layer(e0 alone) + g1 * layer(e1 alone); the single-slot layer is
+    pinned to the dense chain above.  Also: slot order does not matter, gates act linearly."""
+    r = synth.rng_for("pins", "moe-combine")
+    e, hdim, idim, bits, t = 4, 128, 64, 4, 6
+
+    def stack(n, k):
+        ws = [synth.make_qweight(r, n, k, bits) for _ in range(e)]
+        return (np.stack([w.codes for w in ws]), np.stack([w.scales for w in ws]),
+                np.stack([w.biases for w in ws]))
+    gw, uw, dw = stack(idim, hdim), stack(idim, hdim), stack(hdim, idim)
+    ids, gates = synth.draw_routing(r, t, e, 2)
+    gates = gates.astype(np.float64)
+    x = O.decode_bf16(synth.draw_activations(r, t, hdim, "bf16"))
+    out, _, _, _ = O.moe_layer(x, ids, gates, gw, uw, dw, bits)
+    ones = np.ones((t, 1))
+    s0, _, _, _ = O.moe_layer(x, ids[:, :1], ones, gw, uw, dw, bits)
+    s1, _, _, _ = O.moe_layer(x, ids[:, 1:], ones, gw, uw, dw, bits)
+    np.testing.assert_allclose(out, gates[:, :1] * s0 + gates[:, 1:] * s1, rtol=1e-12, atol=1e-14)
+    swapped, _, _, _ = O.moe_layer(x, ids[:, ::-1], gates[:, ::-1], gw, uw, dw, bits)
+    np.testing.assert_allclose(swapped, out, rtol=1e-12, atol=1e-14)
+    scaled, _, _, _ = O.moe_layer(x, ids, 3.0 * gates, gw, uw, dw, bits)
+    np.testing.assert_allclose(scaled, 3.0 * out, rtol=1e-12, atol=1e-14)
+
+
+def test_planted_combine_mistakes_are_caught(monkeypatch):
+    """A combine that drops the gates or takes one slot only fails the pin above."""
+    real = O.moe_layer
+
+    def drop_gates(x, ids, gates, *a, **k):
+        return real(x, ids, np.ones_like(gates), *a, **k)
+
+    def first_slot(x, ids, gates, *a, **k):
+        out, h, off, pidx = real(x, ids[:, :1], gates[:, :1], *a, **k)
+        return out, h, off, pidx
+
+    for bad in (drop_gates, first_slot):
+        with monkeypatch.context() as mp:
+            mp.setattr(O, "moe_layer", bad)
+            with pytest.raises(AssertionError):
+                test_moe_combine_is_the_gate_weighted_sum_of_single_slot_layers()

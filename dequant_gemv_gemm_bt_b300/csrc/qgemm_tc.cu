@@ -8,17 +8,19 @@
 //
 // Layout of one CTA tile (swap-AB: weights are the MMA's M side):
 //   D[n, m] = sum_k W_deq[n0 + n, k] * X[m0 + m, k],  n < 128, m < BN
-//   A = dequantized weight tile, 128 x 64 (one quantization group) per stage,
-//       bf16/f16, written by the dequant warps into shared memory in the
-//       128-byte-swizzled K-major layout the tensor core reads;
-//   B = X tile, BN x 64, loaded by TMA with 128-byte swizzle;
+//   A = dequantized weight tile, 128 x 64 (one quantization group) per K
+//       block, bf16/f16, written by the dequant warps straight into a tensor
+//       memory slot (tcgen05.st; lane = weight row, column j = k 2j, 2j+1) and
+//       read from there by the MMA, so it never passes through shared memory;
+//   B = X tile, BN x 64, loaded by TMA with 128-byte swizzle (shared memory);
 //   D = fp32 accumulator in tensor memory (128 lanes x BN columns).
 // Warp roles: warp 0 issues TMA loads of the packed codes and of X; warp 1
 // owns the tensor-memory allocation and one of its threads issues
 // tcgen05.mma; warps 2..9 dequantize (w = s*q + b with an exact integer code
-// and one rounding) and then drain the accumulator to global memory.  The
-// per-row fp16 scales/biases of the CTA's K range are staged in shared memory
-// once, with cp.async, before the main loop.  All waits are bounded.
+// and one rounding), warp w for the rows of TMEM lanes 32*(w%4), and then
+// drain the accumulator to global memory.  The per-row fp16 scales/biases of
+// the CTA's K range are staged in shared memory once, with cp.async, before
+// the main loop.  All waits are bounded.
 #include <cuda.h>
 
 #include <cstring>

@@ -15,15 +15,19 @@
 //    slice is precomputed, so the bias costs one FMA per 32 codes.
 //  * Fast path (fp16 x, bits 2/4/8): codes become fp16 "1024 + c*q" with one
 //    LOP3 / PRMT per two codes and are multiplied into fp32 accumulators with
-//    mixed-precision FMA (one instruction at FFMA rate on sm_103); the 1024
-//    offset is removed with a precomputed sum.  Generic path (bits 3/6, or bf16
-//    x): funnel-shift extraction, exact int->float via the 2^23 magic, fp32 FMA.
+//    mixed-precision FMA (one instruction at FFMA rate on sm_103); each class's
+//    accumulator starts at minus its sum of 1024*x, which removes the offset.
+//    Generic path (bits 3/6, or bf16 x): funnel-shift extraction, exact
+//    int->float via the 2^23 magic, fp32 FMA.
 //  * A warp works on RI rows at once (independent FMA chains), reduces the RI
-//    partials across lanes with a transpose-style shuffle tree (6 shuffles for
-//    4 rows) and, when one warp covers a whole row, stores y directly with no
+//    partials across lanes with a transpose-style shuffle tree (9 shuffles for
+//    8 rows) and, when one warp covers a whole row, stores y directly with no
 //    block-wide barrier.  When K is split over several warps the partials meet
 //    in shared memory behind a named barrier of that row group.  No atomics:
 //    results are bitwise deterministic.
+//  * Batched launches carry each problem's row geometry (K, warps per row,
+//    rows per unit), so one launch covers problems of different K; CTAs take
+//    equal shares of work (rows x warps per row).
 #pragma once
 #include <type_traits>
 

@@ -34,7 +34,7 @@ BT_F16, BT_BF16, BT_F32 = 0, 1, 2
  BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI) = range(11)
 
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_route", "bt_swiglu", "bt_moe_combine",
-           "bt_status_string", "bt_last_device_error", "bt_set_option")
+           "bt_status_string", "bt_last_device_error", "bt_set_option", "bt_plan_gemv", "bt_plan_gemv_batch")
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -57,6 +57,17 @@ lib.bt_status_string.argtypes = [_i]
 lib.bt_status_string.restype = ctypes.c_char_p
 lib.bt_last_device_error.argtypes = [_p]
 lib.bt_set_option.argtypes = [_i, ctypes.c_longlong]
+
+
+class GemvPlan(ctypes.Structure):
+    _fields_ = [("feasible", ctypes.c_int32), ("kw", ctypes.c_int32), ("cpl", ctypes.c_int32), ("ri", ctypes.c_int32),
+                ("rows_per_unit", ctypes.c_int32), ("stage_bytes", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32), ("grid", ctypes.c_int32), ("num_units", ctypes.c_int64),
+                ("smem_bytes", ctypes.c_int64)]
+
+
+lib.bt_plan_gemv.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(GemvPlan)]
+lib.bt_plan_gemv_batch.argtypes = [_i, _i, _p, _p, _i, _i, ctypes.POINTER(GemvPlan), _p, _p]
 for _name in EXPORTS:
     if _name != "bt_status_string":
         getattr(lib, _name).restype = _i
@@ -231,3 +242,30 @@ def bt_moe_combine(y_grouped, gates, pair_row, top_k: int, out=None, *, out_dtyp
                               _dev(pair_row, "pair_row"), tokens, top_k, hidden, _dev(out, "out"), _dt(out),
                               _stream(stream)), "bt_moe_combine")
     return out
+
+
+def _plan_dict(pl: "GemvPlan") -> dict:
+    return {name: getattr(pl, name) for name, _ in GemvPlan._fields_}
+
+
+def bt_plan_gemv(bits: int, n: int, k: int, *, problems: int = 1, x_dtype=torch.float16, sms: int = 148) -> dict:
+    """The GEMV launch plan for ``problems`` GEMVs of [n, k] on ``sms`` SMs (host only, no GPU needed)."""
+    pl = GemvPlan()
+    _check(lib.bt_plan_gemv(bits, _DT[x_dtype], n, k, problems, sms, ctypes.byref(pl)), "bt_plan_gemv")
+    return _plan_dict(pl)
+
+
+def bt_plan_gemv_batch(bits: int, shapes, *, x_dtype=torch.float16, sms: int = 148):
+    """Plan of one mixed-K batched launch over ``shapes`` = [(n, k), ...] (host only).
+
+    Returns ``(plan dict, [(kw, rows_per_unit) per problem])``.
+    """
+    cnt = len(shapes)
+    n = (ctypes.c_int32 * cnt)(*[int(a) for a, _ in shapes])
+    k = (ctypes.c_int32 * cnt)(*[int(b) for _, b in shapes])
+    kw = (ctypes.c_int32 * cnt)()
+    rb = (ctypes.c_int32 * cnt)()
+    pl = GemvPlan()
+    _check(lib.bt_plan_gemv_batch(bits, _DT[x_dtype], n, k, cnt, sms, ctypes.byref(pl), kw, rb),
+           "bt_plan_gemv_batch")
+    return _plan_dict(pl), list(zip(kw, rb))

@@ -123,6 +123,25 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
 
 using namespace bt;
 
+namespace {
+void fill_plan(const bt::GemvPlan& pl, bt_gemv_plan* out) {
+  out->feasible = pl.feasible ? 1 : 0;
+  out->kw = pl.kw;
+  out->cpl = pl.cpl;
+  out->ri = pl.ri;
+  out->rows_per_unit = pl.rows_per_unit;
+  out->stage_bytes = pl.stage_bytes;
+  out->stages = pl.stages;
+  out->ctas_per_sm = bt::gemv_ctas_per_sm(pl.cpl, pl.ri);
+  out->grid = pl.grid;
+  out->num_units = pl.num_units;
+  out->smem_bytes = (int64_t)pl.smem;
+}
+bool fast_path(int bits, bt_dtype xd) {
+  return xd == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !bt::opts().gemv_generic;
+}
+}  // namespace
+
 extern "C" {
 
 const char* bt_status_string(bt_status s) {
@@ -135,6 +154,41 @@ const char* bt_status_string(bt_status s) {
     case BT_ERR_TIMEOUT: return "BT_ERR_TIMEOUT: a device-side wait expired";
   }
   return "unknown bt_status";
+}
+
+bt_status bt_plan_gemv(int bits, bt_dtype x_dtype, int N, int K, int problems, int sms, bt_gemv_plan* plan) {
+  if (!plan || N <= 0 || K <= 0 || K % kGroup || problems <= 0 || sms <= 0 || !half_dtype(x_dtype))
+    return BT_ERR_INVALID_ARG;
+  if (!bits_ok(bits) || K > kMaxK) return BT_ERR_UNSUPPORTED;
+  fill_plan(plan_gemv(bits, fast_path(bits, x_dtype), N, K, problems, 0, sms), plan);
+  return BT_OK;
+}
+
+bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n, const int32_t* k, int count, int sms,
+                             bt_gemv_plan* plan, int32_t* kw, int32_t* rows_per_unit) {
+  if (!plan || !n || !k || count < 1 || sms <= 0 || !half_dtype(x_dtype)) return BT_ERR_INVALID_ARG;
+  if (count > kBatchCap || !bits_ok(bits)) return BT_ERR_UNSUPPORTED;
+  GemvBatch<kBatchCap> batch;
+  batch.count = count;
+  long long units = 0;
+  for (int i = 0; i < count; ++i) {
+    if (n[i] <= 0 || k[i] <= 0 || k[i] % kGroup) return BT_ERR_INVALID_ARG;
+    batch.prob[i] = GemvProblem{};
+    batch.prob[i].n = n[i];
+    batch.prob[i].k = k[i];
+  }
+  GemvPlan pl = plan_gemv_batch(bits, fast_path(bits, x_dtype), batch, sms);
+  if (pl.feasible) {
+    for (int i = 0; i < count; ++i) {
+      units += (batch.prob[i].n + batch.prob[i].rb - 1) / batch.prob[i].rb;
+      if (kw) kw[i] = batch.prob[i].kw;
+      if (rows_per_unit) rows_per_unit[i] = batch.prob[i].rb;
+    }
+    pl.num_units = units;
+    pl.grid = (int)std::min<long long>(units, (long long)sms * gemv_ctas_per_sm(pl.cpl, pl.ri));
+  }
+  fill_plan(pl, plan);
+  return BT_OK;
 }
 
 bt_status bt_set_option(bt_option option, long long value) {

@@ -239,6 +239,30 @@ typedef enum {
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);
 
+/*
+ * GEMV launch plan (host only, no CUDA call): what bt_qgemv / bt_qgemv_batched
+ * would launch on a device with `sms` multiprocessors, under the current
+ * options.  The per-shape launch heuristics (BaseRT pages, gist.science
+ * "Metodologia": kernel choice and threadgroup sizes per chip) in inspectable
+ * form, for tests and tuning.
+ *   feasible      0: no GEMV kernel fits (the library runs the CUDA-core tile)
+ *   kw            warps sharing one row (K split); cpl: 32-code chunks per lane
+ *   ri            rows in flight per warp; rows_per_unit: rows per pipeline stage
+ *   stage_bytes, stages, smem_bytes   shared-memory ring of one CTA
+ *   ctas_per_sm   CTAs per SM the kernel is built for; grid: CTAs launched
+ */
+typedef struct {
+  int32_t feasible, kw, cpl, ri, rows_per_unit, stage_bytes, stages, ctas_per_sm, grid;
+  int64_t num_units, smem_bytes;
+} bt_gemv_plan;
+/* One problem shape repeated `problems` times (bt_qgemv: problems = 1). */
+BT_API bt_status bt_plan_gemv(int bits, bt_dtype x_dtype, int N, int K, int problems, int sms,
+                              bt_gemv_plan* plan);
+/* A mixed-K batch: n[i], k[i] per problem; kw[i] and rows_per_unit[i] receive
+ * each problem's geometry (host arrays of `count`). */
+BT_API bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n, const int32_t* k, int count,
+                                    int sms, bt_gemv_plan* plan, int32_t* kw, int32_t* rows_per_unit);
+
 #ifdef __cplusplus
 }
 #endif

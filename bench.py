@@ -10,8 +10,8 @@ Weights are synthetic (seeded N(0, 0.02), min/max-quantized); they exceed the
 126 MB L2, so no flush is needed between steps.
 
 Metric: weight GB/s (codes + scales + biases per pass / pass time), the
-BaseRT pages' decode-bandwidth view ("memory traffic scales with the
-compression ratio").  The same run also times the Llama-3.2-3B-shaped prefill
+BaseRT pages' decode-bandwidth view (the bytes read per token fall with the
+bit width).  The same run also times the Llama-3.2-3B-shaped prefill
 GEMM pass (M = 128 and 512, TFLOP/s, key "prefill") and the Qwen3-30B-A3B-
 shaped MoE layer (M = 1 and 128, key "moe"); --legs selects them.
 

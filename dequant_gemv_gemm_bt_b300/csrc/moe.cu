@@ -1,9 +1,10 @@
 // Mixture-of-experts steps around the grouped expert product: routing (stable
 // counting sort of (token, slot) pairs by expert), SwiGLU between the gate/up
 // and down products, and the gate-weighted combine.  BaseRT pages,
-// thetesserapress.com "Where the wins land, and where they don't" (MoE prefill
-// that avoids branching on expert routing): the routing here is data (offsets
-// and an index list), and the products run as one grouped launch.
+// thetesserapress.com "Where the wins land, and where they don't" (the MoE
+// prefill lead, credited to code paths that do not fork on which experts a
+// token picked): the routing here is data (offsets and an index list), and the
+// products run as one grouped launch.
 #include "bt_common.cuh"
 #include "moe.cuh"
 

@@ -1,6 +1,6 @@
 // CUDA-core dequant-GEMM tile: the small-M and fallback path for M > 1, dense
 // and grouped by expert.  BaseRT pages, thetesserapress.com "What BaseRT does
-// differently" (GEMM kernels for prefill where M > 1, dequantization inline).
+// differently" (a GEMM for prefill, M > 1, that dequantizes in its inner loop).
 //
 // A CTA owns a [32 tokens x 64 weight rows] output tile.  Per K step of one
 // quantization group it stages the group's packed words of its 64 weight rows

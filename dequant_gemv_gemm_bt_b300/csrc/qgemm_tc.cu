@@ -1,10 +1,10 @@
 // Tensor-core dequant-GEMM (tcgen05 / TMEM / TMA) for prefill, M >= 16.
 // BaseRT pages, thetesserapress.com "BaseRT claims fastest Apple Silicon
-// inference", section "What BaseRT does differently" (GEMM kernels for prefill
-// where M > 1, dequantization inline in the compute loop, never materializing
-// full-precision weights in memory) and section "Where the wins land" (dense
-// prefill saturates the matrix units); gist.science "Metodologia" (tiled GEMM
-// on the matrix units).
+// inference", section "What BaseRT does differently" (prefill, M > 1, runs a
+// GEMM that expands the codes in its inner loop; full-precision weights never
+// reach memory) and section "Where the wins land" (dense prefill keeps the
+// matrix units busy); gist.science "Metodologia" (tiled GEMM on the matrix
+// units).
 //
 // Layout of one CTA tile (swap-AB: weights are the MMA's M side):
 //   D[n, m] = sum_k W_deq[n0 + n, k] * X[m0 + m, k],  n < 128, m < BN

@@ -1,8 +1,8 @@
 // Device code of the dequant-GEMV (M = 1, decode) and its batched form for
 // mixture-of-experts decode.  BaseRT pages, thetesserapress.com "BaseRT claims
 // fastest Apple Silicon inference", section "What BaseRT does differently": a
-// dedicated GEMV for M = 1 whose memory traffic scales with the compression
-// ratio because the weights are dequantized inside the compute loop.
+// GEMV of its own for M = 1, which expands the codes inside its inner loop, so
+// the bytes it reads fall in proportion to the bits per weight.
 //
 // Design (B300):
 //  * Persistent CTAs, each streaming a contiguous range of row blocks ("units")

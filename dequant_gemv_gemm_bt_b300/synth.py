@@ -5,7 +5,7 @@ and by the checks of the CPU oracle: it draws random tensors and writes them in
 the packed layout.  It holds none of the product arithmetic (no unpacking, no
 dequantization, no dot products).
 
-Layout (affine group quantization, "Q2 to Q8", BaseRT pages: thakicloud.com
+Layout (affine group quantization, 2 to 8 bits, BaseRT pages: thakicloud.com
 "BaseRT는 무엇인가"; group size 64 along K, fp16 scale and bias, Q4 codes 8 per
 uint32):
 

@@ -2,13 +2,13 @@
  * bt.h -- C ABI of libbt: matrix products over affine group-quantized weights
  * with the dequantization done inside the compute loop (B300, sm_103a).
  *
- * What is computed.  The BaseRT pages describe "affine quantization Q2 to Q8"
- * (thakicloud.com, "Apple Silicon 로컬 LLM 추론의 새 기준 BaseRT", section
- * "BaseRT는 무엇인가") and "dedicated GEMV kernels for decode where M=1, GEMM
- * kernels for prefill where M>1; dequantization happens inline in the compute
- * loop rather than materializing full-precision weights to memory; memory
- * traffic scales with the compression ratio" (thetesserapress.com, "BaseRT
- * claims fastest Apple Silicon inference", section "What BaseRT does
+ * What is computed.  The BaseRT pages store model weights as affine codes of
+ * 2 to 8 bits (thakicloud.com, "Apple Silicon 로컬 LLM 추론의 새 기준 BaseRT",
+ * section "BaseRT는 무엇인가").  Their matmul kernels are split by M: a GEMV
+ * for single-token decode, a GEMM for prefill.  Both expand the codes to
+ * weights inside the inner loop, so full-precision weights never go to
+ * memory and the bytes read shrink with the bit width (thetesserapress.com,
+ * "BaseRT claims fastest Apple Silicon inference", section "What BaseRT does
  * differently").  Every product here is
  *
  *     y[m, n] = sum_k x[m, k] * (s[n, k/g] * q[n, k] + b[n, k/g])
@@ -84,8 +84,8 @@ BT_API bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const u
  * row count and (when K = 0) its own K.  Persistent CTAs stream the problems'
  * rows back to back, so a decode step's many small GEMVs cost one launch
  * instead of one each (BaseRT pages, thetesserapress.com "Where the wins
- * land": small models are dispatch-bound; gist.science "Contribuições":
- * low-overhead dispatch).
+ * land": launch overhead dominates small models; gist.science "Contribuições":
+ * cheap dispatch).
  *   problems  HOST array of `count` descriptors (read during the call only;
  *             the pointers in it are device memory, 16-byte aligned)
  *   K         > 0: every problem has this K (the descriptors' k is ignored);
@@ -108,9 +108,9 @@ BT_API bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, in
 
 /*
  * Dequant-GEMM, M > 1 (prefill): Y[m, n] = sum_k X[m, k] * w_deq[n, k].
- * BaseRT pages, thetesserapress.com "What BaseRT does differently" (GEMM for
- * prefill where M > 1) and gist.science "Metodologia" (tiled prefill GEMM on
- * the matrix units).  Weights are dequantized in registers and fed to the
+ * BaseRT pages, thetesserapress.com "What BaseRT does differently" (prefill,
+ * with several tokens, runs a GEMM) and gist.science "Metodologia" (tiled
+ * prefill GEMM on the matrix units).  Weights are dequantized in registers and fed to the
  * tensor cores (M >= 64) or to a CUDA-core tile (small M); fp32 accumulation.
  *   X  [M, K] row-major, x_dtype BT_BF16 or BT_F16
  *   Y  [M, N] row-major, y_dtype BT_BF16, BT_F16 or BT_F32
@@ -126,7 +126,8 @@ BT_API bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const u
  * grouped activation matrix use expert e's weight:
  *     Y[r, n] = sum_k Xg[r, k] * w_deq_e[n, k].
  * BaseRT pages, thetesserapress.com "Where the wins land, and where they
- * don't" (mixture-of-experts prefill without branching on expert routing).
+ * don't" (the MoE prefill lead, credited to code that does not fork on the
+ * experts a token picked).
  *   codes/scales/biases  experts stacked: [E][N][K*bits/32], [E][N][K/g]
  *   expert_offsets  device int32 [E+1], non-decreasing, off[0] = 0,
  *                   off[E] = total_rows; experts may be empty

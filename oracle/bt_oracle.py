@@ -8,11 +8,11 @@ its own bit-level unpacker, its own half-float decoding and its own arithmetic.
 What it computes is the plain definition, in fp64, of the products described on
 the BaseRT pages:
 
-* "affine quantization Q2 to Q8" (thakicloud.com, "Apple Silicon 로컬 LLM 추론의
+* affine codes of 2 to 8 bits (thakicloud.com, "Apple Silicon 로컬 LLM 추론의
   새 기준 BaseRT", section "BaseRT는 무엇인가"): a weight is ``s*q + b`` with an
   unsigned code ``q`` and a per-group fp16 scale ``s`` and bias ``b``;
-* "dedicated GEMV kernels for decode where M=1, GEMM kernels for prefill where
-  M>1", dequantization inline (thetesserapress.com, "BaseRT claims fastest Apple
+* a GEMV for decode (M = 1) and a GEMM for prefill (M > 1), each expanding the
+  codes in its inner loop (thetesserapress.com, "BaseRT claims fastest Apple
   Silicon inference", section "What BaseRT does differently"): both reduce to
   ``y[m, n] = sum_k x[m, k] * w_deq[n, k]``.  The oracle materializes ``w_deq``;
   the GPU path must not;

@@ -34,7 +34,7 @@ BT_F16, BT_BF16, BT_F32 = 0, 1, 2
  BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI) = range(11)
 
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_route", "bt_swiglu", "bt_moe_combine",
-           "bt_status_string", "bt_last_device_error", "bt_set_option", "bt_plan_gemv", "bt_plan_gemv_batch")
+           "bt_status_string", "bt_last_device_error", "bt_set_option", "bt_plan_gemv", "bt_plan_gemv_batch", "bt_plan_gemm")
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -68,6 +68,17 @@ class GemvPlan(ctypes.Structure):
 
 lib.bt_plan_gemv.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(GemvPlan)]
 lib.bt_plan_gemv_batch.argtypes = [_i, _i, _p, _p, _i, _i, ctypes.POINTER(GemvPlan), _p, _p]
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("feasible", ctypes.c_int32), ("bn", ctypes.c_int32),
+                ("splits", ctypes.c_int32), ("stages", ctypes.c_int32), ("k_blocks", ctypes.c_int32),
+                ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int64)]
+
+
+lib.bt_plan_gemm.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(GemmPlan)]
+GEMM_PATHS = {0: "none", 1: "gemv", 2: "simt", 3: "tc"}
 for _name in EXPORTS:
     if _name != "bt_status_string":
         getattr(lib, _name).restype = _i
@@ -244,8 +255,8 @@ def bt_moe_combine(y_grouped, gates, pair_row, top_k: int, out=None, *, out_dtyp
     return out
 
 
-def _plan_dict(pl: "GemvPlan") -> dict:
-    return {name: getattr(pl, name) for name, _ in GemvPlan._fields_}
+def _plan_dict(pl) -> dict:
+    return {name: getattr(pl, name) for name, _ in type(pl)._fields_}
 
 
 def bt_plan_gemv(bits: int, n: int, k: int, *, problems: int = 1, x_dtype=torch.float16, sms: int = 148) -> dict:
@@ -269,3 +280,16 @@ def bt_plan_gemv_batch(bits: int, shapes, *, x_dtype=torch.float16, sms: int = 1
     _check(lib.bt_plan_gemv_batch(bits, _DT[x_dtype], n, k, cnt, sms, ctypes.byref(pl), kw, rb),
            "bt_plan_gemv_batch")
     return _plan_dict(pl), list(zip(kw, rb))
+
+
+def bt_plan_gemm(bits: int, m: int, n: int, k: int, *, num_experts: int = 0, x_dtype=torch.bfloat16,
+                 sms: int = 148) -> dict:
+    """Launch plan of a dense (num_experts=0) or grouped product of m rows (host only, no GPU needed).
+
+    ``path`` is one of "none", "gemv", "simt" (CUDA-core tile) or "tc" (tensor cores).
+    """
+    pl = GemmPlan()
+    _check(lib.bt_plan_gemm(bits, _DT[x_dtype], m, n, k, num_experts, sms, ctypes.byref(pl)), "bt_plan_gemm")
+    d = _plan_dict(pl)
+    d["path"] = GEMM_PATHS[d["path"]]
+    return d

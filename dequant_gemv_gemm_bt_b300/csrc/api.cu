@@ -80,6 +80,26 @@ bt_status cuda_status(cudaError_t e) {
   return e == cudaSuccess ? BT_OK : BT_ERR_CUDA;
 }
 
+// Which kernel family runs a product of M rows: the GEMV (one row, or a grouped
+// launch with no more rows than experts), the tensor cores (M >= 16 and a
+// supported shape) or the CUDA-core tile.  num_experts == 0: dense product.
+// BT_OPT_GEMM_PATH forces 1 (CUDA-core tile) or 2 (tensor cores where the shape allows).
+enum GemmPath { kPathNone = 0, kPathGemv = 1, kPathSimt = 2, kPathTc = 3 };
+GemmPath gemm_path(int bits, int M, int K, int num_experts) {
+  const int forced = opts().gemm_path;
+  if (num_experts == 0) {
+    if (M == 1) return kPathGemv;
+    return tc_shape_ok(bits, K) && (forced == 2 || (forced == 0 && M >= 16)) ? kPathTc : kPathSimt;
+  }
+  if (M == 0) return kPathNone;
+  if (M <= num_experts && forced == 0) return kPathGemv;
+  return forced != 1 && tc_shape_ok(bits, K) ? kPathTc : kPathSimt;
+}
+
+bool gemv_fast_path(int bits, bt_dtype xd) {
+  return xd == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !opts().gemv_generic;
+}
+
 bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits, int N, int K,
                    const void* x, bt_dtype xd, void* y, bt_dtype yd, int problems, const int32_t* offsets,
                    const int32_t* row_index, int num_experts, cudaStream_t stream) {
@@ -101,8 +121,7 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.const_weights = opts().pdl && opts().const_weights;
   p.drop_stage = opts().test_drop_stage;
   opts().test_drop_stage = 0;
-  const bool fast = xd == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !opts().gemv_generic;
-  const GemvPlan pl = plan_gemv(bits, fast, N, K, problems, p.num_experts, sm_count());
+  const GemvPlan pl = plan_gemv(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count());
   if (!pl.feasible) {
     // no GEMV kernel holds this K slice in registers: the CUDA-core tile computes the same product
     GemmParams g{};
@@ -137,9 +156,6 @@ void fill_plan(const bt::GemvPlan& pl, bt_gemv_plan* out) {
   out->num_units = pl.num_units;
   out->smem_bytes = (int64_t)pl.smem;
 }
-bool fast_path(int bits, bt_dtype xd) {
-  return xd == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !bt::opts().gemv_generic;
-}
 }  // namespace
 
 extern "C" {
@@ -160,7 +176,7 @@ bt_status bt_plan_gemv(int bits, bt_dtype x_dtype, int N, int K, int problems, i
   if (!plan || N <= 0 || K <= 0 || K % kGroup || problems <= 0 || sms <= 0 || !half_dtype(x_dtype))
     return BT_ERR_INVALID_ARG;
   if (!bits_ok(bits) || K > kMaxK) return BT_ERR_UNSUPPORTED;
-  fill_plan(plan_gemv(bits, fast_path(bits, x_dtype), N, K, problems, 0, sms), plan);
+  fill_plan(plan_gemv(bits, gemv_fast_path(bits, x_dtype), N, K, problems, 0, sms), plan);
   return BT_OK;
 }
 
@@ -177,7 +193,7 @@ bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n, const
     batch.prob[i].n = n[i];
     batch.prob[i].k = k[i];
   }
-  GemvPlan pl = plan_gemv_batch(bits, fast_path(bits, x_dtype), batch, sms);
+  GemvPlan pl = plan_gemv_batch(bits, gemv_fast_path(bits, x_dtype), batch, sms);
   if (pl.feasible) {
     for (int i = 0; i < count; ++i) {
       units += (batch.prob[i].n + batch.prob[i].rb - 1) / batch.prob[i].rb;
@@ -188,6 +204,41 @@ bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n, const
     pl.grid = (int)std::min<long long>(units, (long long)sms * gemv_ctas_per_sm(pl.cpl, pl.ri));
   }
   fill_plan(pl, plan);
+  return BT_OK;
+}
+
+bt_status bt_plan_gemm(int bits, bt_dtype x_dtype, int M, int N, int K, int num_experts, int sms, bt_gemm_plan* plan) {
+  if (!plan || M < 0 || (M == 0 && num_experts == 0) || N <= 0 || K <= 0 || K % kGroup || num_experts < 0 ||
+      num_experts > 4096 || sms <= 0 || !half_dtype(x_dtype))
+    return BT_ERR_INVALID_ARG;
+  if (!bits_ok(bits) || K > kMaxK) return BT_ERR_UNSUPPORTED;
+  *plan = bt_gemm_plan{};
+  GemmPath path = gemm_path(bits, M, K, num_experts);
+  GemmGeometry g;
+  if (path == kPathGemv) {
+    const GemvPlan pl = plan_gemv(bits, gemv_fast_path(bits, x_dtype), N, K, num_experts ? M : 1, num_experts, sms);
+    if (pl.feasible) {
+      g.feasible = true;
+      g.stages = pl.stages;
+      g.grid_x = pl.grid;
+      g.grid_y = g.grid_z = 1;
+      g.smem = (long long)pl.smem;
+    } else {
+      path = kPathSimt;   // run_gemv hands shapes no GEMV kernel holds to the CUDA-core tile
+    }
+  }
+  if (path == kPathTc) g = plan_gemm_tc_geometry(bits, M, N, K, num_experts, sms);
+  if (path == kPathSimt) g = plan_gemm_simt_geometry(M, N, num_experts);
+  plan->path = path;
+  plan->feasible = (path == kPathNone || g.feasible) ? 1 : 0;
+  plan->bn = g.bn;
+  plan->splits = g.splits;
+  plan->stages = g.stages;
+  plan->k_blocks = g.k_blocks;
+  plan->grid_x = g.grid_x;
+  plan->grid_y = g.grid_y;
+  plan->grid_z = g.grid_z;
+  plan->smem_bytes = g.smem;
   return BT_OK;
 }
 
@@ -295,15 +346,15 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (s != BT_OK) return s;
   if (M <= 0 || !x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  if (M == 1) return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0, stream);
+  const GemmPath path = gemm_path(bits, M, K, 0);
+  if (path == kPathGemv)
+    return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0, stream);
   GemmParams p{};
   p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
   p.M = M; p.N = N; p.K = K;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
-  const int path = opts().gemm_path;
-  const bool tc_ok = tc_supported(bits, K, M, p);
-  if (tc_ok && (path == 2 || (path == 0 && M >= 16)))
+  if (path == kPathTc && tc_supported(bits, K, M, p))
     return cuda_status(launch_gemm_tc(p, bits, x_dtype, y_dtype, stream));
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
 }
@@ -318,8 +369,9 @@ bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint
       !half_dtype(x_dtype) || !out_dtype(y_dtype))
     return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  if (total_rows == 0) return BT_OK;
-  if (total_rows <= num_experts && opts().gemm_path == 0)
+  const GemmPath path = gemm_path(bits, total_rows, K, num_experts);
+  if (path == kPathNone) return BT_OK;
+  if (path == kPathGemv)
     return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, total_rows, expert_offsets,
                     x_row_index, num_experts, stream);
   GemmParams p{};
@@ -330,7 +382,7 @@ bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint
   p.num_experts = num_experts;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
-  if (opts().gemm_path != 1 && tc_supported(bits, K, total_rows, p))
+  if (path == kPathTc && tc_supported(bits, K, total_rows, p))
     return cuda_status(launch_gemm_tc_grouped(p, bits, x_dtype, y_dtype, stream));
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
 }

@@ -150,6 +150,18 @@ cudaError_t launch_simt_x(const GemmParams& p, int bits, bt_dtype yd, int tiles,
 
 }  // namespace
 
+GemmGeometry plan_gemm_simt_geometry(int M, int N, int num_experts) {
+  GemmGeometry g;
+  long long tiles = (M + TM - 1) / TM;   // the same count as launch_gemm_simt
+  if (num_experts > 0) tiles += std::min<long long>(num_experts, M);
+  g.bn = TM;
+  g.grid_x = (N + TN - 1) / TN;
+  g.grid_y = (int)std::min<long long>(tiles, 1LL << 30);
+  g.grid_z = 1;
+  g.feasible = tiles <= 65535;
+  return g;
+}
+
 cudaError_t launch_gemm_simt(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
   // token tiles: dense ceil(M/32); grouped at most ceil(M/32) + one partial tile per expert
   long long tiles = (p.M + TM - 1) / TM;

@@ -686,7 +686,7 @@ EncodeTiledFn encode_fn() {
 
 // Shared memory of one CTA for a given K split (mirrors the layout in the kernel).
 template <int BITS, int BN, bool GROUPED>
-size_t tc_smem_bytes(int K, int splits, int* stages_out) {
+size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nullptr) {
   const int G_all = K / BK;
   int gc_max = 0;
   for (int z = 0; z < splits; ++z) {
@@ -706,17 +706,17 @@ size_t tc_smem_bytes(int K, int splits, int* stages_out) {
   const size_t recv_bytes = splits > 1 ? (size_t)splits * BM * owned_max * 16 * 4 : 0;
   while ((size_t)stages * stage_bytes < recv_bytes) ++stages;
   if (stages_out) *stages_out = stages;
+  if (k_blocks_out) *k_blocks_out = gc_max;
   return fixed + (size_t)stages * stage_bytes;
 }
 
 // K split for a dense launch: minimize waves x (K blocks per split + fixed cost),
 // where waves come from how many clusters of that size fit on the device at once.
-template <int BITS, bool BF16, int BN>
-int choose_splits(int tiles, int K, cudaStream_t st);
+int choose_splits(int tiles, int K, int sms);
 
 template <int BITS, bool BF16, int BN, bool GROUPED = false>
 cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStream_t st) {
-  if (splits <= 0) splits = GROUPED ? 1 : choose_splits<BITS, BF16, BN>(((gp.N + BM - 1) / BM) * ((gp.M + BN - 1) / BN), gp.K, st);
+  if (splits <= 0) splits = GROUPED ? 1 : choose_splits(((gp.N + BM - 1) / BM) * ((gp.M + BN - 1) / BN), gp.K, sm_count());
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int row_bytes = gp.K * BITS / 8;
@@ -816,11 +816,10 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
 // placement, while fuller grids of split clusters spill into a second wave and
 // lose more than the split gains.  So: the largest split (1, 2, 3, 4, 6, 8,
 // keeping >= 4 K blocks per split) with tiles x split <= 0.85 x SMs.
-template <int BITS, bool BF16, int BN>
-int choose_splits(int tiles, int K, cudaStream_t) {
+int choose_splits(int tiles, int K, int sms) {
   const int kb = K / BK;
   if (opts().gemm_splits > 0) return std::max(1, std::min(opts().gemm_splits, kb / 2));
-  const int limit = (sm_count() * 85) / 100;
+  const int limit = (sms * 85) / 100;
   int best = 1;
   for (int sp : {2, 3, 4, 6, 8})
     if (kb / sp >= 4 && tiles * sp <= limit) best = sp;
@@ -860,16 +859,58 @@ cudaError_t launch_tc_grouped_bits(const GemmParams& gp, bt_dtype xd, bt_dtype y
   return launch_tc_grouped_bn<BITS, false>(gp, yd, bn, st);
 }
 
+// Host-only geometry of one tensor-core launch: the shared memory, ring depth
+// and grid that launch_tc_t computes for the same arguments.
+template <int BITS, int BN, bool GROUPED>
+GemmGeometry geometry_t(int M, int N, int K, int num_experts, int splits) {
+  GemmGeometry g;
+  g.bn = BN;
+  g.splits = splits;
+  int stages = 0, kb = 0;
+  const size_t smem = tc_smem_bytes<BITS, BN, GROUPED>(K, splits, &stages, &kb);
+  const long long ytiles = GROUPED ? (long long)(M + BN - 1) / BN + std::min(num_experts, M) : (M + BN - 1) / BN;
+  g.stages = stages;
+  g.k_blocks = kb;
+  g.smem = (long long)smem;
+  g.grid_x = (N + BM - 1) / BM;
+  g.grid_y = (int)std::min<long long>(ytiles, 1LL << 30);
+  g.grid_z = splits;
+  g.feasible = smem != 0 && smem <= 227 * 1024 && ytiles <= 65535;
+  return g;
+}
+
+template <int BITS>
+GemmGeometry geometry_bits(int bn, int M, int N, int K, int num_experts, int splits) {
+  if (num_experts > 0) {
+    switch (bn) {
+      case 16: return geometry_t<BITS, 16, true>(M, N, K, num_experts, 1);
+      case 32: return geometry_t<BITS, 32, true>(M, N, K, num_experts, 1);
+      case 64: return geometry_t<BITS, 64, true>(M, N, K, num_experts, 1);
+      default: return geometry_t<BITS, 128, true>(M, N, K, num_experts, 1);
+    }
+  }
+  switch (bn) {
+    case 32: return geometry_t<BITS, 32, false>(M, N, K, 0, splits);
+    case 64: return geometry_t<BITS, 64, false>(M, N, K, 0, splits);
+    case 128: return geometry_t<BITS, 128, false>(M, N, K, 0, splits);
+    default: return geometry_t<BITS, 256, false>(M, N, K, 0, splits);
+  }
+}
+
 }  // namespace tc
+
+int grouped_bn(int M, int num_experts) {
+  const int avg = (M + num_experts - 1) / num_experts;
+  if (avg <= 16) return 16;
+  if (avg <= 32) return 32;
+  if (avg <= 64) return 64;
+  return 128;
+}
 
 // Grouped experts: token tiles sized to the mean rows per expert (the MMA's N
 // runs 16..128), one CTA per (expert, 128 weight rows, token tile).
 cudaError_t launch_gemm_tc_grouped(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
-  const int avg = (gp.M + gp.num_experts - 1) / gp.num_experts;
-  int bn = 128;
-  if (avg <= 16) bn = 16;
-  else if (avg <= 32) bn = 32;
-  else if (avg <= 64) bn = 64;
+  const int bn = grouped_bn(gp.M, gp.num_experts);
   switch (bits) {
     case 2: return tc::launch_tc_grouped_bits<2>(gp, xd, yd, bn, st);
     case 4: return tc::launch_tc_grouped_bits<4>(gp, xd, yd, bn, st);
@@ -879,12 +920,17 @@ cudaError_t launch_gemm_tc_grouped(const GemmParams& gp, int bits, bt_dtype xd, 
 }
 
 
-bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
+bool tc_shape_ok(int bits, int K) {
   if (!(bits == 2 || bits == 4 || bits == 6 || bits == 8)) return false;
   const int G = K / 64;
   if (G % 2) return false;                          // 4-byte cp.async of scale pairs
   if (G > 192) return false;                        // the CTA's scales/biases are staged whole in shared memory
   if (((size_t)K * bits / 8) % 16) return false;    // TMA row stride
+  return true;
+}
+
+bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
+  if (!tc_shape_ok(bits, K)) return false;
   if ((reinterpret_cast<uintptr_t>(gp.x) & 15) || (reinterpret_cast<uintptr_t>(gp.codes) & 15)) return false;
   (void)M;
   return true;
@@ -900,6 +946,22 @@ void plan_gemm_tc(int M, int N, int K, int sms, int& bn, int& splits) {
   else if (M <= 128) bn = 128;
   splits = 0;   // chosen per instantiation from cluster occupancy (choose_splits)
   (void)N; (void)K; (void)sms;
+}
+
+GemmGeometry plan_gemm_tc_geometry(int bits, int M, int N, int K, int num_experts, int sms) {
+  int bn = 0, splits = 1;
+  if (num_experts > 0) {
+    bn = grouped_bn(M, num_experts);
+  } else {
+    plan_gemm_tc(M, N, K, sms, bn, splits);
+    splits = tc::choose_splits(((N + tc::BM - 1) / tc::BM) * ((M + bn - 1) / bn), K, sms);
+  }
+  switch (bits) {
+    case 2: return tc::geometry_bits<2>(bn, M, N, K, num_experts, splits);
+    case 4: return tc::geometry_bits<4>(bn, M, N, K, num_experts, splits);
+    case 6: return tc::geometry_bits<6>(bn, M, N, K, num_experts, splits);
+    default: return tc::geometry_bits<8>(bn, M, N, K, num_experts, splits);
+  }
 }
 
 cudaError_t launch_gemm_tc(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {

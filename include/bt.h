@@ -264,6 +264,32 @@ BT_API bt_status bt_plan_gemv(int bits, bt_dtype x_dtype, int N, int K, int prob
 BT_API bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n, const int32_t* k, int count,
                                     int sms, bt_gemv_plan* plan, int32_t* kw, int32_t* rows_per_unit);
 
+/*
+ * Launch plan of a dense (num_experts = 0) or grouped (num_experts > 0, M rows
+ * in total) product (host only, no CUDA call): what bt_qgemm / bt_moe_qgemm
+ * would launch for these sizes on `sms` multiprocessors under the current
+ * options, assuming 16-byte aligned pointers.  The per-shape kernel choice
+ * and tiling (BaseRT pages, gist.science "Metodologia") in inspectable form.
+ *   path       0 no launch (grouped, M = 0); 1 GEMV; 2 CUDA-core tile;
+ *              3 tensor cores
+ *   feasible   0: these sizes exceed the chosen kernel's limits (the call
+ *              would return BT_ERR_CUDA)
+ *   bn         token-tile width (the MMA's N on path 3; 32 on path 2)
+ *   splits     K split: CTAs per cluster on path 3
+ *   stages     ring depth (paths 1 and 3); k_blocks: most 64-wide K blocks
+ *              one split walks (path 3)
+ *   grid_*     launch grid; smem_bytes: dynamic shared memory per CTA
+ * Errors: BT_ERR_INVALID_ARG for a null plan, M < 0 (or 0 when dense),
+ * N <= 0, K not a positive multiple of 64, num_experts outside [0, 4096],
+ * sms <= 0 or a bad x_dtype; BT_ERR_UNSUPPORTED for bits or K beyond limits.
+ */
+typedef struct {
+  int32_t path, feasible, bn, splits, stages, k_blocks, grid_x, grid_y, grid_z;
+  int64_t smem_bytes;
+} bt_gemm_plan;
+BT_API bt_status bt_plan_gemm(int bits, bt_dtype x_dtype, int M, int N, int K, int num_experts, int sms,
+                              bt_gemm_plan* plan);
+
 #ifdef __cplusplus
 }
 #endif

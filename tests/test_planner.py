@@ -133,3 +133,104 @@ def test_mixed_batch_rejects_k_above_8192(bt):
     assert p["feasible"] == 0
     with pytest.raises(bt.BTError):
         bt.bt_plan_gemv_batch(4, [(64, 100)])                       # K not a multiple of the group size
+
+
+# ---------------------------------------------------------------- dense / grouped GEMM plans
+
+SPLIT_CANDIDATES = (1, 2, 3, 4, 6, 8)
+
+
+def test_gemm_path_choice(bt):
+    assert bt.bt_plan_gemm(4, 1, 4096, 4096)["path"] == "gemv"
+    for m in (2, 8, 15):
+        assert bt.bt_plan_gemm(4, m, 4096, 4096)["path"] == "simt"      # too few rows for a 128-wide MMA tile
+    for m in (16, 128, 4096):
+        assert bt.bt_plan_gemm(4, m, 4096, 4096)["path"] == "tc"
+    assert bt.bt_plan_gemm(3, 128, 4096, 4096)["path"] == "simt"        # no tensor-core kernel for Q3
+    assert bt.bt_plan_gemm(4, 128, 4096, 64 * 63)["path"] == "simt"     # odd group count (scale pairs)
+    assert bt.bt_plan_gemm(4, 128, 4096, 64 * 194)["path"] == "simt"    # more groups than the CTA stages
+    assert bt.bt_plan_gemm(2, 128, 4096, 64 * 2)["path"] == "tc"        # Q2 row of 32 B: TMA stride ok
+
+
+@pytest.mark.parametrize("bits", (2, 4, 6, 8))
+@pytest.mark.parametrize("m", (16, 33, 64, 100, 128, 129, 512, 2048))
+@pytest.mark.parametrize("n,k", ((1024, 3072), (3072, 3072), (5120, 3072), (16384, 3072), (3072, 8192),
+                                 (2048, 768), (4096, 128), (151936, 1024)))
+def test_dense_tc_plan_invariants(bt, bits, m, n, k):
+    sms = 148
+    p = bt.bt_plan_gemm(bits, m, n, k, sms=sms)
+    assert p["path"] == "tc" and p["feasible"] == 1
+    bn = p["bn"]
+    assert bn == next((w for w in (32, 64, 128) if m <= w), 256)      # narrowest token tile that covers M
+    assert p["grid_x"] == -(-n // 128) and p["grid_y"] == -(-m // bn)
+    sp, kb = p["splits"], k // 64
+    assert sp in SPLIT_CANDIDATES and p["grid_z"] == sp
+    tiles = p["grid_x"] * p["grid_y"]
+    if sp > 1:
+        assert kb // sp >= 4 and tiles * sp <= sms * 85 // 100
+    for bigger in (c for c in SPLIT_CANDIDATES if c > sp):              # the largest split that fits one wave
+        assert kb // bigger < 4 or tiles * bigger > sms * 85 // 100
+    assert p["k_blocks"] * sp >= kb and p["k_blocks"] <= -(-kb // sp) + 2   # near-even, even-aligned split
+    assert 2 <= p["stages"] <= 12
+    assert p["smem_bytes"] <= 227 * 1024
+
+
+def test_prefill_gate_up_matches_the_captured_launch(bt):
+    # The ncu capture of the Llama-3.2-3B-shaped gate|up launch (N=16384, K=3072,
+    # M=128, Q4, bf16) recorded grid 128 x 1 x 1 and 210.2 kB of dynamic shared memory.
+    p = bt.bt_plan_gemm(4, 128, 16384, 3072)
+    assert (p["grid_x"], p["grid_y"], p["grid_z"]) == (128, 1, 1)
+    assert p["smem_bytes"] == 210208
+
+
+@pytest.mark.parametrize("m", (129, 256, 1024, 4096))
+@pytest.mark.parametrize("experts", (8, 64, 128))
+def test_grouped_tc_plan(bt, m, experts):
+    p = bt.bt_plan_gemm(4, m, 1536, 2048, num_experts=experts)
+    assert p["path"] == "tc" and p["feasible"] == 1 and p["splits"] == 1
+    mean = -(-m // experts)
+    assert p["bn"] == next((w for w in (16, 32, 64) if mean <= w), 128)
+    # (expert, token tile) slots: every expert's partial tile plus the full tiles
+    assert p["grid_y"] == -(-m // p["bn"]) + min(experts, m)
+    assert p["grid_x"] == 1536 // 128
+
+
+def test_grouped_small_batches_run_the_gemv(bt):
+    import torch
+    assert bt.bt_plan_gemm(4, 0, 1536, 2048, num_experts=128)["path"] == "none"
+    p = bt.bt_plan_gemm(4, 8, 1536, 2048, num_experts=128, x_dtype=torch.float16)
+    assert p["path"] == "gemv"                                         # one row per routed expert: decode
+    assert bt.bt_plan_gemm(4, 129, 1536, 2048, num_experts=128)["path"] == "tc"
+
+
+def test_gemm_plan_at_m1_is_the_gemv_plan(bt):
+    import torch
+    for n, k in ((4096, 4096), (151936, 1024), (1024, 3072)):
+        g = bt.bt_plan_gemm(4, 1, n, k, x_dtype=torch.float16)
+        v = bt.bt_plan_gemv(4, n, k, x_dtype=torch.float16)
+        assert g["path"] == "gemv" and g["grid_x"] == v["grid"] and g["smem_bytes"] == v["smem_bytes"]
+
+
+def test_gemm_options_steer_the_plan(bt):
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 1)
+        assert bt.bt_plan_gemm(4, 512, 4096, 4096)["path"] == "simt"
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 2)
+        assert bt.bt_plan_gemm(4, 4, 4096, 4096)["path"] == "tc"
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
+        bt.bt_set_option(bt.BT_OPT_GEMM_SPLITS, 8)
+        assert bt.bt_plan_gemm(4, 128, 16384, 3072)["splits"] == 8
+        assert bt.bt_plan_gemm(4, 128, 4096, 64 * 6)["splits"] == 3   # at least two K blocks per split
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
+        bt.bt_set_option(bt.BT_OPT_GEMM_SPLITS, 0)
+
+
+def test_gemm_plan_rejects_bad_sizes(bt):
+    for args in ((4, 0, 64, 64), (4, 16, 0, 64), (4, 16, 64, 100), (4, 16, 64, -64)):
+        with pytest.raises(bt.BTError):
+            bt.bt_plan_gemm(*args)
+    with pytest.raises(bt.BTError):
+        bt.bt_plan_gemm(5, 16, 64, 64)
+    with pytest.raises(bt.BTError):
+        bt.bt_plan_gemm(4, 16, 64, 64 * 1024)                          # K above 32768

@@ -411,3 +411,37 @@ def test_planted_combine_mistakes_are_caught(monkeypatch):
             mp.setattr(O, "moe_layer", bad)
             with pytest.raises(AssertionError):
                 test_moe_combine_is_the_gate_weighted_sum_of_single_slot_layers()
+
+
+# ---------------------------------------------------------- the pass criterion
+def test_pass_criterion_is_per_element():
+    """|y - y_ref| <= rtol*A + 1e-5 element by element, with rtol 1e-3 for fp32
+    outputs and 8e-3 for 16-bit outputs, and a NaN never passes."""
+    assert O.RTOL["f32"] == 1e-3 and O.RTOL["bf16"] == 8e-3 and O.ATOL == 1e-5
+    y_ref = np.array([1.0, -2.0, 0.0, 5.0])
+    a = np.array([10.0, 4.0, 0.0, 1000.0])
+    assert O.within_tolerance(y_ref.copy(), y_ref, a, "f32") == (True, 0.0)
+    bound = 1e-3 * a + 1e-5
+    for i in range(4):
+        for scale, ok in ((0.99, True), (1.01, False)):
+            for sign in (1.0, -1.0):
+                y = y_ref.copy()
+                y[i] += sign * scale * bound[i]
+                got_ok, ratio = O.within_tolerance(y, y_ref, a, "f32")
+                assert got_ok is ok and abs(ratio - scale) < 1e-6
+    # a large A on one element does not loosen another's bound
+    y = y_ref.copy()
+    y[2] = 2e-5
+    assert not O.within_tolerance(y, y_ref, a, "f32")[0]
+    assert O.within_tolerance(y, y_ref, a * 0 + 1.0, "f32")[0]          # 2e-5 <= 1e-3*1 + 1e-5
+    # 16-bit outputs take the wider bound
+    y = y_ref.copy()
+    y[0] += 0.05                                                        # 5e-3 * A: fails fp32, passes bf16
+    assert not O.within_tolerance(y, y_ref, a, "f32")[0]
+    assert O.within_tolerance(y, y_ref, a, "bf16")[0]
+    y = y_ref.copy()
+    y[1] = np.nan
+    assert not O.within_tolerance(y, y_ref, a, "f32")[0]
+    y = y_ref.copy()
+    y[3] = np.inf
+    assert not O.within_tolerance(y, y_ref, a, "f32")[0]

@@ -128,6 +128,44 @@ def _weights(codes, scales, biases):
     return _dev(codes, "codes"), _dev(scales, "scales"), _dev(biases, "biases")
 
 
+# The C entry points take plain pointers and sizes, so they cannot see a buffer
+# that is smaller than the sizes say.  These checks compare every tensor with
+# the sizes passed alongside it before any pointer reaches a kernel.
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def check_weight(codes, scales, biases, bits: int, k: int, group_size: int = 64, experts: bool = False) -> int:
+    """Packed weight [N, K*bits/32] words + [N, K/g] fp16 params ([E, ...] when ``experts``); returns N."""
+    nd = 3 if experts else 2
+    for t, nm in ((codes, "codes"), (scales, "scales"), (biases, "biases")):
+        _need(isinstance(t, torch.Tensor) and t.dim() == nd, f"{nm} must be a {nd}-D tensor")
+    _need(codes.element_size() == 4 and not codes.is_floating_point(), "codes must be int32/uint32 words")
+    _need(scales.element_size() == 2 and biases.element_size() == 2, "scales and biases must be 16-bit (fp16)")
+    _need(codes.shape[-1] * 32 == k * bits,
+          f"codes hold {codes.shape[-1] * 32 // max(bits, 1)} {bits}-bit codes per row, K is {k}")
+    g = k // group_size if group_size > 0 else -1
+    want = tuple(codes.shape[:-1]) + (g,)
+    _need(tuple(scales.shape) == want and tuple(biases.shape) == want,
+          f"scales/biases must be {list(want)}, got {list(scales.shape)} and {list(biases.shape)}")
+    return codes.shape[-2]
+
+
+def _check_int32(t, nm: str, at_least: int) -> None:
+    _need(isinstance(t, torch.Tensor) and t.dtype == torch.int32, f"{nm} must be an int32 tensor")
+    _need(t.numel() >= at_least, f"{nm} holds {t.numel()} entries, needs {at_least}")
+
+
+def _check_out(t, nm: str, at_least: int) -> None:
+    _need(isinstance(t, torch.Tensor) and t.numel() >= at_least, f"{nm} holds too few elements (needs {at_least})")
+
+
+def _same_device(*ts) -> None:
+    devs = {t.device for t in ts if isinstance(t, torch.Tensor)}
+    _need(len(devs) <= 1, f"tensors are on different devices: {sorted(map(str, devs))}")
+
+
 def bt_set_option(option: int, value: int) -> None:
     _check(lib.bt_set_option(int(option), int(value)), "bt_set_option")
 
@@ -140,10 +178,13 @@ def bt_last_device_error(stream=None) -> int:
 def bt_qgemv(codes, scales, biases, bits: int, x, y=None, *, group_size: int = 64,
              out_dtype=torch.float32, stream=None):
     """``y[n] = sum_k x[k] * w_deq[n, k]``; ``x`` [K] fp16/bf16, ``y`` [N]."""
-    n = codes.shape[0]
     k = x.shape[-1]
+    n = check_weight(codes, scales, biases, bits, k, group_size)
+    _need(x.numel() == k, f"x must hold one row of K = {k}, got shape {list(x.shape)}")
     if y is None:
         y = torch.empty(n, dtype=out_dtype, device=x.device)
+    _check_out(y, "y", n)
+    _same_device(codes, scales, biases, x, y)
     c, s, b = _weights(codes, scales, biases)
     _check(lib.bt_qgemv(c, s, b, bits, group_size, n, k, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y),
                         _stream(stream)), "bt_qgemv")
@@ -157,15 +198,25 @@ def bt_qgemv_batched(problems, bits: int, *, group_size: int = 64, stream=None):
     common dtypes; each problem's K is ``x.shape[-1]`` and its ``y`` gets
     ``codes.shape[0]`` rows.  Problems of different K go out as one mixed-K batch.
     """
-    arr = (GemvProblem * len(problems))()
     ks = set()
-    for i, (c, s, b, x, y) in enumerate(problems):
+    x0, y0 = problems[0][3], problems[0][4]
+    for i, (c, s, b, x, y) in enumerate(problems):   # every entry is checked before any is marshalled
         k = x.shape[-1]
         if c.shape[-1] * 32 != k * bits:
             raise ValueError(f"problem {i}: codes hold {c.shape[-1] * 32 // bits} codes per row, x has {k}")
+        try:
+            check_weight(c, s, b, bits, k, group_size)
+            _need(x.numel() == k, f"x must hold one row of K = {k}")
+            _check_out(y, "y", c.shape[0])
+            _need(x.dtype == x0.dtype and y.dtype == y0.dtype, "every problem must share x and y dtypes")
+            _same_device(c, s, b, x, y, x0)
+        except ValueError as err:
+            raise ValueError(f"problem {i}: {err}") from None
         ks.add(k)
+    arr = (GemvProblem * len(problems))()
+    for i, (c, s, b, x, y) in enumerate(problems):
         arr[i] = GemvProblem(_dev(c, "codes"), _dev(s, "scales"), _dev(b, "biases"), _dev(x, "x"), _dev(y, "y"),
-                             c.shape[0], k)
+                             c.shape[0], x.shape[-1])
     k_all = ks.pop() if len(ks) == 1 else 0
     _check(lib.bt_qgemv_batched(arr, len(problems), bits, group_size, k_all, _dt(problems[0][3]),
                                 _dt(problems[0][4]), _stream(stream)), "bt_qgemv_batched")
@@ -175,10 +226,13 @@ def bt_qgemv_batched(problems, bits: int, *, group_size: int = 64, stream=None):
 def bt_qgemm(codes, scales, biases, bits: int, x, y=None, *, group_size: int = 64,
              out_dtype=torch.bfloat16, stream=None):
     """``Y = X @ W_deq^T``; ``x`` [M, K] bf16/fp16, ``Y`` [M, N]."""
-    n = codes.shape[0]
+    _need(x.dim() == 2, f"x must be [M, K], got shape {list(x.shape)}")
     m, k = x.shape
+    n = check_weight(codes, scales, biases, bits, k, group_size)
     if y is None:
         y = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    _check_out(y, "y", m * n)
+    _same_device(codes, scales, biases, x, y)
     c, s, b = _weights(codes, scales, biases)
     _check(lib.bt_qgemm(c, s, b, bits, group_size, m, n, k, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y),
                         _stream(stream)), "bt_qgemm")
@@ -191,12 +245,20 @@ def bt_moe_qgemm(codes, scales, biases, bits: int, expert_offsets, x, y=None, *,
 
     ``total_rows`` defaults to ``len(x_row_index)`` when a gather index is given, else ``x.shape[0]``.
     """
-    e, n = codes.shape[0], codes.shape[1]
     k = x.shape[-1]
+    n = check_weight(codes, scales, biases, bits, k, group_size, experts=True)
+    e = codes.shape[0]
     if total_rows is None:
         total_rows = x_row_index.shape[0] if x_row_index is not None else x.shape[0]
+    _check_int32(expert_offsets, "expert_offsets", e + 1)
+    if x_row_index is not None:
+        _check_int32(x_row_index, "x_row_index", total_rows)
+    else:
+        _need(x.numel() >= total_rows * k, f"x holds {x.numel() // max(k, 1)} rows, total_rows is {total_rows}")
     if y is None:
         y = torch.empty((total_rows, n), dtype=out_dtype, device=x.device)
+    _check_out(y, "y", total_rows * n)
+    _same_device(codes, scales, biases, x, y, expert_offsets, x_row_index)
     c, s, b = _weights(codes, scales, biases)
     ri = _dev(x_row_index, "x_row_index") if x_row_index is not None else None
     _check(lib.bt_moe_qgemm(c, s, b, bits, group_size, e, n, k, _dev(expert_offsets, "expert_offsets"),
@@ -212,7 +274,9 @@ def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair
     Returns ``(offsets, pair_index, pair_row)``, plus ``pair_token`` (the token of each
     grouped row, for ``x_row_index``) when ``with_token`` or a ``pair_token`` buffer is given.
     """
+    _need(topk_ids.dim() == 2, "topk_ids must be [T, top_k]")
     t, top_k = topk_ids.shape
+    _check_int32(topk_ids, "topk_ids", t * top_k)
     dev = topk_ids.device
     if offsets is None:
         offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
@@ -223,6 +287,10 @@ def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair
     want_token = with_token or pair_token is not None
     if want_token and pair_token is None:
         pair_token = torch.empty(t * top_k, dtype=torch.int32, device=dev)
+    _check_int32(offsets, "offsets", num_experts + 1)
+    for buf, nm in ((pair_index, "pair_index"), (pair_row, "pair_row")) + (((pair_token, "pair_token"),) if want_token else ()):
+        _check_int32(buf, nm, t * top_k)
+    _same_device(topk_ids, offsets, pair_index, pair_row, pair_token)
     _check(lib.bt_moe_route(_dev(topk_ids, "topk_ids"), t, top_k, num_experts, _dev(offsets, "offsets"),
                             _dev(pair_index, "pair_index"), _dev(pair_row, "pair_row"),
                             _dev(pair_token, "pair_token") if want_token else None, _stream(stream)),
@@ -234,10 +302,13 @@ def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair
 
 def bt_swiglu(gate_up, h=None, *, out_dtype=None, stream=None):
     """``h = silu(gate_up[:, :I]) * gate_up[:, I:]``."""
+    _need(gate_up.dim() == 2 and gate_up.shape[1] % 2 == 0, "gate_up must be [rows, 2*I]")
     rows, two_i = gate_up.shape
     inter = two_i // 2
     if h is None:
         h = torch.empty((rows, inter), dtype=out_dtype or gate_up.dtype, device=gate_up.device)
+    _check_out(h, "h", rows * inter)
+    _same_device(gate_up, h)
     _check(lib.bt_swiglu(_dev(gate_up, "gate_up"), _dt(gate_up), rows, inter, _dev(h, "h"), _dt(h),
                          _stream(stream)), "bt_swiglu")
     return h
@@ -245,10 +316,17 @@ def bt_swiglu(gate_up, h=None, *, out_dtype=None, stream=None):
 
 def bt_moe_combine(y_grouped, gates, pair_row, top_k: int, out=None, *, out_dtype=None, stream=None):
     """``out[t] = sum_s gates[t, s] * y_grouped[pair_row[t*top_k + s]]``."""
+    _need(y_grouped.dim() == 2, "y_grouped must be [T*top_k, H]")
+    _need(gates.dim() == 2 and gates.shape[1] == top_k and gates.dtype == torch.float32,
+          "gates must be float32 [T, top_k]")
     hidden = y_grouped.shape[1]
     tokens = gates.shape[0]
+    _need(y_grouped.shape[0] >= tokens * top_k, f"y_grouped holds {y_grouped.shape[0]} rows, needs {tokens * top_k}")
+    _check_int32(pair_row, "pair_row", tokens * top_k)
     if out is None:
         out = torch.empty((tokens, hidden), dtype=out_dtype or y_grouped.dtype, device=y_grouped.device)
+    _check_out(out, "out", tokens * hidden)
+    _same_device(y_grouped, gates, pair_row, out)
     _check(lib.bt_moe_combine(_dev(y_grouped, "y_grouped"), _dt(y_grouped), _dev(gates, "gates"),
                               _dev(pair_row, "pair_row"), tokens, top_k, hidden, _dev(out, "out"), _dt(out),
                               _stream(stream)), "bt_moe_combine")

@@ -96,8 +96,11 @@ GemmPath gemm_path(int bits, int M, int K, int num_experts) {
   return forced != 1 && tc_shape_ok(bits, K) ? kPathTc : kPathSimt;
 }
 
+// fp16 x takes the magic-number fast path at every bit width (BT_OPT_GEMV_GENERIC
+// forces the generic one); bits decides only how many chunks per lane exist.
 bool gemv_fast_path(int bits, bt_dtype xd) {
-  return xd == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !opts().gemv_generic;
+  (void)bits;
+  return xd == BT_F16 && !opts().gemv_generic;
 }
 
 bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits, int N, int K,
@@ -327,7 +330,7 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
   p.const_weights = opts().pdl && opts().const_weights;
   p.drop_stage = opts().test_drop_stage;
   opts().test_drop_stage = 0;
-  const bool fast = x_dtype == BT_F16 && (bits == 2 || bits == 4 || bits == 8) && !opts().gemv_generic;
+  const bool fast = gemv_fast_path(bits, x_dtype);
   GemvPlan pl;
   if (mixed) {
     pl = plan_gemv_batch(bits, fast, batch, sm_count());

@@ -29,7 +29,9 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   // CTAs (16 consumer warps) fit per SM, and the cross-warp partial sums are
   // cheap next to the latency hidden (e.g. Q4 K=8192: 3.7 vs 2.3 TB/s with 4
   // chunks per lane; K=3072 still gains with a quarter of its lanes idle).
-  const int cpl_cap = fast ? 4 : 2;
+  // 3 or 4 chunks per lane exist for the fast path of bits 2/4/8 only
+  const bool wide = fast && (bits == 2 || bits == 4 || bits == 8);
+  const int cpl_cap = wide ? 4 : 2;
   const int want_cpl = opts().gemv_max_cpl > 0 ? std::min(opts().gemv_max_cpl, cpl_cap) : 1;
   int kw = 1;
   while (kw < kMaxNW && (nchunks + 32 * kw - 1) / (32 * kw) > want_cpl) kw *= 2;
@@ -41,8 +43,8 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   }
   pl.kw = kw;
   pl.cpl = cpl;
-  // the kernels exist for up to 4 chunks per lane on the fast path and 2 on the generic one
-  pl.feasible = cpl <= cpl_cap && kw <= nw && nw % kw == 0 && K <= 16 * 1024 * (fast ? 2 : 1);
+  // the kernels exist for up to 4 chunks per lane on the fast path of bits 2/4/8 and 2 otherwise
+  pl.feasible = cpl <= cpl_cap && kw <= nw && nw % kw == 0 && K <= 16 * 1024 * (wide ? 2 : 1);
   if (!pl.feasible) return pl;
   const int rw = nw / kw;
   const int G = K / kGroup;

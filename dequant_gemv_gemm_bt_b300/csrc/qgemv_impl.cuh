@@ -13,11 +13,13 @@
 //    scale/bias of each row.
 //  * Per group the product is factored as s * sum(q*x) + b * sum(x); sum(x) per
 //    slice is precomputed, so the bias costs one FMA per 32 codes.
-//  * Fast path (fp16 x, bits 2/4/8): codes become fp16 "1024 + c*q" with one
-//    LOP3 / PRMT per two codes and are multiplied into fp32 accumulators with
-//    mixed-precision FMA (one instruction at FFMA rate on sm_103); each class's
-//    accumulator starts at minus its sum of 1024*x, which removes the offset.
-//    Generic path (bits 3/6, or bf16 x): funnel-shift extraction, exact
+//  * Fast path (fp16 x, every bit width): codes become fp16 "1024 + c*q" with
+//    one LOP3 / PRMT per two codes and are multiplied into fp32 accumulators
+//    with mixed-precision FMA (one instruction at FFMA rate on sm_103); each
+//    class's accumulator starts at minus its sum of 1024*x, which removes the
+//    offset.  Bits 2/4/8 pair codes within a word; bits 3/6, whose codes
+//    cross words, follow searched schedules of shifted windows
+//    (qgemv_stream.h).  Generic path (bf16 x): funnel-shift extraction, exact
 //    int->float via the 2^23 magic, fp32 FMA.
 //  * A warp works on RI rows at once (independent FMA chains), reduces the RI
 //    partials across lanes with a transpose-style shuffle tree (9 shuffles for
@@ -30,9 +32,11 @@
 //    equal shares of work (rows x warps per row).
 #pragma once
 #include <type_traits>
+#include <utility>
 
 #include "bt_common.cuh"
 #include "qgemv.cuh"
+#include "qgemv_stream.h"
 
 namespace bt {
 
@@ -104,6 +108,23 @@ __device__ __forceinline__ void fma_pair(float& acc, uint16_t x_lo, uint16_t x_h
       : "+f"(acc) : "h"(x_lo), "h"(x_hi), "r"(hp));
 }
 
+// acc_lo += x_lo * h.lo and acc_hi += x_hi * h.hi (two accumulators).
+__device__ __forceinline__ void fma_pair2(float& acc_lo, float& acc_hi, uint16_t x_lo, uint16_t x_hi, uint32_t hp) {
+  asm("{\n .reg .f16 ha, hb;\n mov.b32 {ha, hb}, %4;\n"
+      " fma.rn.f32.f16 %0, %2, ha, %0;\n fma.rn.f32.f16 %1, %3, hb, %1;\n}\n"
+      : "+f"(acc_lo), "+f"(acc_hi) : "h"(x_lo), "h"(x_hi), "r"(hp));
+}
+// acc += x * h.lo, or x * h.hi when HIGH (a half that carries a code alone).
+template <bool HIGH>
+__device__ __forceinline__ void fma_half(float& acc, uint16_t x, uint32_t hp) {
+  if constexpr (HIGH)
+    asm("{\n .reg .f16 ha, hb;\n mov.b32 {ha, hb}, %2;\n fma.rn.f32.f16 %0, %1, hb, %0;\n}\n"
+        : "+f"(acc) : "h"(x), "r"(hp));
+  else
+    asm("{\n .reg .f16 ha, hb;\n mov.b32 {ha, hb}, %2;\n fma.rn.f32.f16 %0, %1, ha, %0;\n}\n"
+        : "+f"(acc) : "h"(x), "r"(hp));
+}
+
 __device__ __forceinline__ uint32_t lop_mask_or(uint32_t w, uint32_t mask) {
   return lop3_and_or(w, mask, 0x64006400u);
 }
@@ -119,6 +140,9 @@ template <int BITS> struct FastClasses;
 template <> struct FastClasses<2> { static constexpr int n = 5; };
 template <> struct FastClasses<4> { static constexpr int n = 2; };
 template <> struct FastClasses<8> { static constexpr int n = 1; };
+template <> struct FastClasses<3> { static constexpr int n = StreamLayout<3>::n_classes; };
+template <> struct FastClasses<6> { static constexpr int n = StreamLayout<6>::n_classes; };
+template <int BITS> constexpr bool kStreamBits = (BITS == 3 || BITS == 6);
 
 // For each fp16x2 code pair of a word: the positions (within the word) of its
 // low-half and high-half codes, and its class.
@@ -191,6 +215,73 @@ template <int BITS> struct XSlice<BITS, false> {
   float xsum;
 };
 
+// ---- bits 3 and 6: the searched code-pair schedules of qgemv_stream.h.
+// One schedule entry: its source window of the chunk's stream, one LOP3 and
+// the FMAs of its one or two codes into their classes.
+template <int BITS, int I>
+__device__ __forceinline__ void stream_step(const uint32_t (&w)[BITS], const uint16_t (&xh)[32],
+                                            float (&acc)[StreamLayout<BITS>::n_classes]) {
+  using L = StreamLayout<BITS>;
+  constexpr StreamPair P = L::pair(I);
+  constexpr int wi = P.t / 32, sh = P.t % 32;
+  uint32_t src;
+  if constexpr (sh == 0) src = w[wi];
+  else if constexpr (wi + 1 < BITS) src = __funnelshift_r(w[wi], w[wi + 1], sh);
+  else src = w[wi] >> sh;
+  const uint32_t h = lop3_and_or(src, stream_mask<BITS>(P), 0x64006400u);
+  if constexpr (P.lo >= 0 && P.hi >= 0) {
+    if constexpr (L::cls(P.olo) == L::cls(P.ohi)) fma_pair(acc[L::cls(P.olo)], xh[P.lo], xh[P.hi], h);
+    else fma_pair2(acc[L::cls(P.olo)], acc[L::cls(P.ohi)], xh[P.lo], xh[P.hi], h);
+  } else if constexpr (P.lo >= 0) {
+    fma_half<false>(acc[L::cls(P.olo)], xh[P.lo], h);
+  } else {
+    fma_half<true>(acc[L::cls(P.ohi)], xh[P.hi], h);
+  }
+}
+
+template <int BITS, int... I>
+__device__ __forceinline__ void stream_steps(const uint32_t (&w)[BITS], const uint16_t (&xh)[32],
+                                             float (&acc)[StreamLayout<BITS>::n_classes],
+                                             std::integer_sequence<int, I...>) {
+  (stream_step<BITS, I>(w, xh, acc), ...);
+}
+
+// x sum of the chunk and each class's seed: minus 1024 times the x of its codes.
+template <int BITS, int I>
+__device__ __forceinline__ void stream_seed(const uint16_t (&xh)[32], float (&zc)[StreamLayout<BITS>::n_classes]) {
+  using L = StreamLayout<BITS>;
+  constexpr StreamPair P = L::pair(I);
+  if constexpr (P.lo >= 0) zc[L::cls(P.olo)] -= 1024.f * __half2float(__ushort_as_half(xh[P.lo]));
+  if constexpr (P.hi >= 0) zc[L::cls(P.ohi)] -= 1024.f * __half2float(__ushort_as_half(xh[P.hi]));
+}
+
+template <int BITS, int... I>
+__device__ __forceinline__ void stream_seeds(XSlice<BITS, true>& s, std::integer_sequence<int, I...>) {
+  float zc[StreamLayout<BITS>::n_classes];
+#pragma unroll
+  for (int c = 0; c < StreamLayout<BITS>::n_classes; ++c) zc[c] = 0.f;
+  (stream_seed<BITS, I>(s.xh, zc), ...);
+  float xsum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) xsum += __half2float(__ushort_as_half(s.xh[j]));
+  s.xsum = xsum;
+#pragma unroll
+  for (int c = 0; c < StreamLayout<BITS>::n_classes; ++c) s.zc[c] = zc[c];
+}
+
+template <int BITS>
+__device__ __forceinline__ float chunk_dot_stream(const uint32_t (&w)[BITS], const XSlice<BITS, true>& s) {
+  using L = StreamLayout<BITS>;
+  float acc[L::n_classes];
+#pragma unroll
+  for (int c = 0; c < L::n_classes; ++c) acc[c] = s.zc[c];
+  stream_steps<BITS>(w, s.xh, acc, std::make_integer_sequence<int, L::n_pairs>{});
+  float t = acc[0];
+#pragma unroll
+  for (int c = 1; c < L::n_classes; ++c) t = fmaf(acc[c], 1.f / float(1 << L::offset(c)), t);
+  return t;
+}
+
 template <int BITS, bt_dtype XD>
 __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_t* xk) {
   // xk: 32 consecutive x values (16-B aligned) of this chunk
@@ -204,6 +295,9 @@ __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_
       s.xh[8 * i + 2 * j + 1] = u[j] >> 16;
     }
   }
+  if constexpr (kStreamBits<BITS>) {
+    stream_seeds<BITS>(s, std::make_integer_sequence<int, StreamLayout<BITS>::n_pairs>{});
+  } else {
   using L = FastLayout<BITS>;
   constexpr int codes_per_word = 32 / BITS;
   constexpr int NC = FastClasses<BITS>::n;
@@ -224,6 +318,7 @@ __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_
   s.xsum = xsum;
 #pragma unroll
   for (int c = 0; c < NC; ++c) s.zc[c] = zc[c];
+  }
 }
 
 template <int BITS, bt_dtype XD>
@@ -244,9 +339,9 @@ __device__ __forceinline__ void load_x_generic(XSlice<BITS, false>& s, const uin
   s.xsum = xsum;
 }
 
-// sum_j q_j * x_j over one chunk (fast path).
+// sum_j q_j * x_j over one chunk (fast path, bits 2/4/8: pairs within a word).
 template <int BITS>
-__device__ __forceinline__ float chunk_dot_fast(const uint32_t (&w)[BITS], const XSlice<BITS, true>& s) {
+__device__ __forceinline__ float chunk_dot_words(const uint32_t (&w)[BITS], const XSlice<BITS, true>& s) {
   using L = FastLayout<BITS>;
   constexpr int NC = FastClasses<BITS>::n;
   constexpr int codes_per_word = 32 / BITS;
@@ -266,6 +361,13 @@ __device__ __forceinline__ float chunk_dot_fast(const uint32_t (&w)[BITS], const
 #pragma unroll
   for (int c = 1; c < NC; ++c) t = fmaf(acc[c], 1.f / L::mult(c), t);
   return t;
+}
+
+// sum_j q_j * x_j over one chunk (fast path).
+template <int BITS>
+__device__ __forceinline__ float chunk_dot_fast(const uint32_t (&w)[BITS], const XSlice<BITS, true>& s) {
+  if constexpr (kStreamBits<BITS>) return chunk_dot_stream<BITS>(w, s);
+  else return chunk_dot_words<BITS>(w, s);
 }
 
 // sum_j q_j * x_j over one chunk (generic path, any bits).
@@ -756,8 +858,9 @@ cudaError_t launch_cpl(const GemvParams& p, const GemvPlan& pl, const GemvBatch<
   switch (pl.cpl) {
     case 1: return launch_ri<BITS, XD, 1, FAST, BATCH>(p, pl, b, st);
     case 2: return launch_ri<BITS, XD, 2, FAST, BATCH>(p, pl, b, st);
-    case 3: if constexpr (FAST) return launch_ri<BITS, XD, 3, FAST, BATCH>(p, pl, b, st); else break;
-    case 4: if constexpr (FAST) return launch_ri<BITS, XD, 4, FAST, BATCH>(p, pl, b, st); else break;
+    // three or four chunks per lane: fast path of bits 2/4/8 only (K up to 32768)
+    case 3: if constexpr (FAST && !kStreamBits<BITS>) return launch_ri<BITS, XD, 3, FAST, BATCH>(p, pl, b, st); else break;
+    case 4: if constexpr (FAST && !kStreamBits<BITS>) return launch_ri<BITS, XD, 4, FAST, BATCH>(p, pl, b, st); else break;
   }
   return cudaErrorInvalidValue;
 }
@@ -765,11 +868,8 @@ cudaError_t launch_cpl(const GemvParams& p, const GemvPlan& pl, const GemvBatch<
 template <int BITS, bool BATCH>
 cudaError_t launch_bits_b(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, const GemvBatch<kBatchCap>* b,
                           cudaStream_t st) {
-  constexpr bool kFastBits = (BITS == 2 || BITS == 4 || BITS == 8);
   if (xd == BT_F16) {
-    if constexpr (kFastBits) {
-      if (pl.fast) return launch_cpl<BITS, BT_F16, true, BATCH>(p, pl, b, st);
-    }
+    if (pl.fast) return launch_cpl<BITS, BT_F16, true, BATCH>(p, pl, b, st);
     return launch_cpl<BITS, BT_F16, false, BATCH>(p, pl, b, st);
   }
   return launch_cpl<BITS, BT_BF16, false, BATCH>(p, pl, b, st);

@@ -109,7 +109,7 @@ def test_qgemv_pdl_and_const_weights(env):
 
 def test_qgemv_generic_path_matches_fast(env):
     torch, bt = env
-    for bits in (2, 4, 8):
+    for bits in (2, 3, 4, 6, 8):
         qw, x = make_case("generic", 300, 1024, bits)
         y_fast = run(env, qw, x, "f16", "f32")
         try:

@@ -72,11 +72,12 @@ def test_moe_qgemm_grouped(env, bits, path):
     assert_close(out_to_f64(y, torch), y_ref, a, "bf16", f"bits={bits} path={path}")
 
 
-def test_moe_qgemm_gather_decode(env):
+@pytest.mark.parametrize("bits", (3, 4, 6))
+def test_moe_qgemm_gather_decode(env, bits):
     """Decode: one token, 8 distinct experts, rows gathered from the same x row."""
     torch, bt = env
-    r = synth.rng_for("test", "moe-decode")
-    e, n, k, bits = 16, 384, 2048, 4
+    r = synth.rng_for("test", "moe-decode") if bits == 4 else synth.rng_for("test", "moe-decode", bits)
+    e, n, k = 16, 384, 2048
     w = stacked(r, e, n, k, bits)
     ids, _ = synth.draw_routing(r, 1, e, 8)
     off, order = O.route_sort(ids, e)

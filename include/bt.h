@@ -92,7 +92,7 @@ BT_API bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const u
  *             0: each problem uses its descriptor's k (a mixed-K batch, e.g. a
  *             whole decode step in one launch)
  * Limits: 1 <= count <= 256; one K: 64 <= K <= 32768 (K <= 16384 for bf16 x
- * or odd bits); mixed K: every k in [64, 8192], a multiple of 64.
+ * or 3- and 6-bit codes); mixed K: every k in [64, 8192], a multiple of 64.
  */
 typedef struct {
   const uint32_t* codes;     /* [n, k*bits/32] */

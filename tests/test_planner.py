@@ -63,6 +63,20 @@ def test_one_chunk_per_lane_up_to_8192(bt):
     assert p["cpl"] == 2 and p["kw"] == 8 and p["ctas_per_sm"] == 1
 
 
+def test_k_limits_per_bit_width(bt):
+    """Two chunks per lane (K <= 16384) for 3- and 6-bit codes and for bf16 x; four (K <= 32768)
+    for 2/4/8-bit codes with fp16 x.  Beyond that a single product runs on the CUDA-core tile."""
+    import torch
+    for bits in (2, 3, 4, 6, 8):
+        assert bt.bt_plan_gemv(bits, 4096, 16384)["feasible"] == 1
+        wide = bits in (2, 4, 8)
+        p = bt.bt_plan_gemv(bits, 4096, 32768)
+        assert p["feasible"] == (1 if wide else 0)
+        assert bt.bt_plan_gemm(bits, 1, 4096, 32768, x_dtype=torch.float16)["path"] == ("gemv" if wide else "simt")
+        p = bt.bt_plan_gemv(bits, 4096, 32768, x_dtype=torch.bfloat16)
+        assert p["feasible"] == 0
+
+
 def test_rows_in_flight_shrink_for_small_problems(bt):
     assert bt.bt_plan_gemv(4, 151936, 1024)["ri"] == 8
     p = bt.bt_plan_gemv(4, 4096, 1024)                             # 28 rows per SM: 2 rows in flight

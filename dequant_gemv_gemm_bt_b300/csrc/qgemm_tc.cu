@@ -16,11 +16,21 @@
 //   D = fp32 accumulator in tensor memory (128 lanes x BN columns).
 // Warp roles: warp 0 issues TMA loads of the packed codes and of X; warp 1
 // owns the tensor-memory allocation and one of its threads issues
-// tcgen05.mma; warps 2..9 dequantize (w = s*q + b with an exact integer code
-// and one rounding), warp w for the rows of TMEM lanes 32*(w%4), and then
-// drain the accumulator to global memory.  The per-row fp16 scales/biases of
-// the CTA's K range are staged in shared memory once, with cp.async, before
-// the main loop.  All waits are bounded.
+// tcgen05.mma; warps 2..9 dequantize, warp w for the rows of TMEM lanes
+// 32*(w%4), and then drain the accumulator to global memory.
+//
+// Dequantization and its rounding.  The codes become exact fp16 "1024 + q"
+// pairs (one LOP3 per pair).  With fp16 X the weight is s*q + b from one
+// f16x2 FMA of the exact integer (one rounding, to fp16).  With bf16 X each
+// weight is formed in fp32 from the exact fp16 scale, w = s*(1024+q) + b',
+// b' = b - 1024*s (the product is exact and the FMA rounds once), then
+// rounded once to bf16.  A bf16 weight keeps 8 significant bits, so when Y is
+// fp32 the kernel also writes the residual w - bf16(w) as a second bf16 A
+// tile and issues the MMAs of both (A = hi + lo carries 16 bits), which keeps
+// the fp32 output within its 1e-3 relative bound at any K.
+//
+// The per-row fp16 scales/biases of the CTA's K range are staged in shared
+// memory once, with cp.async, before the main loop.  All waits are bounded.
 #include <cuda.h>
 
 #include <cstring>
@@ -35,14 +45,21 @@ constexpr int BM = 128;                  // weight rows per tile (MMA M)
 constexpr int BK = 64;                   // K per stage = one quantization group
 constexpr int kDeqWarps = 8;
 // A ring in tensor memory: the dequant warps write each K block's 128 x 64 bf16
-// A tile into one of kAStages 32-column slots (column j holds k = 2j, 2j+1 of
-// the row in that lane) and the MMA reads it from there, so A never passes
-// through shared memory (whose bandwidth the MMA's B operand and the TMA
-// writes already need).
+// A tile into one of the A slots (column j holds k = 2j, 2j+1 of the row in
+// that lane; a split slot holds the hi tile in columns 0..31 and the lo tile
+// in 32..63) and the MMA reads it from there, so A never passes through
+// shared memory (whose bandwidth the MMA's B operand and the TMA writes
+// already need).
 constexpr int kAStages = 4;
 template <int BN> constexpr int acc_cols() { return BN < 32 ? 32 : BN; }
-template <int BN> constexpr int tmem_cols() {
-  constexpr int need = acc_cols<BN>() + kAStages * 32;
+// Columns of one A slot: 32 (64 bf16/f16 k values), or 64 when the slot holds
+// the hi and lo bf16 tiles of a split weight.
+template <bool SPLIT> constexpr int a_slot_cols() { return SPLIT ? 64 : 32; }
+// A slots in use: split tiles at narrow token widths take 3 slots, so that the
+// allocation stays within 256 columns and two CTAs still fit an SM's TMEM.
+template <int BN, bool SPLIT> constexpr int a_stages() { return (SPLIT && BN <= 64) ? 3 : kAStages; }
+template <int BN, bool SPLIT> constexpr int tmem_cols() {
+  constexpr int need = acc_cols<BN>() + a_stages<BN, SPLIT>() * a_slot_cols<SPLIT>();
   return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
 constexpr int kThreads = (2 + kDeqWarps) * 32;
@@ -180,17 +197,15 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 
 // ------------------------------------------------------------------ dequant math
-// Half-precision pair arithmetic for the A operand's type.
-template <bool BF16> __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+// Half-precision pair arithmetic (the fp16-X path).
+__device__ __forceinline__ uint32_t hsub2_f16(uint32_t a, uint32_t b) {
   uint32_t d;
-  if constexpr (BF16) asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  else asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-template <bool BF16> __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+__device__ __forceinline__ uint32_t hfma2_f16(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
-  if constexpr (BF16) asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  else asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -198,50 +213,34 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
-// Magic "2^p + q" in both halves: 128 + q in bf16 (7 mantissa bits), 1024 + q in f16.
-template <bool BF16> constexpr uint32_t kMagic2 = BF16 ? 0x43004300u : 0x64006400u;
-template <bool BF16> constexpr uint32_t kMagicByte = BF16 ? 0x43434343u : 0x64646464u;
+// fp16 "1024 + q" in both halves of a word: exact for every code below 1024.
+constexpr uint32_t kMagic16 = 0x64006400u;
 
-// Eight 4-bit codes (one word, code j in bits 4j..4j+3) -> eight dequantized
-// halves in k order, as four pairs.
-template <bool BF16>
-__device__ __forceinline__ uint4 deq8_q4(uint32_t w, uint32_t s2, uint32_t b2) {
-  constexpr uint32_t MG = kMagic2<BF16>;
-  uint32_t d0 = lop3_and_or(w, 0x000F000Fu, MG);          // (q0, q4)
-  uint32_t d1 = lop3_and_or(w >> 4, 0x000F000Fu, MG);     // (q1, q5)
-  uint32_t d2 = lop3_and_or(w >> 8, 0x000F000Fu, MG);     // (q2, q6)
-  uint32_t d3 = lop3_and_or(w >> 12, 0x000F000Fu, MG);    // (q3, q7)
-  d0 = hfma2<BF16>(hsub2<BF16>(d0, MG), s2, b2);
-  d1 = hfma2<BF16>(hsub2<BF16>(d1, MG), s2, b2);
-  d2 = hfma2<BF16>(hsub2<BF16>(d2, MG), s2, b2);
-  d3 = hfma2<BF16>(hsub2<BF16>(d3, MG), s2, b2);
-  return make_uint4(prmt(d0, d1, 0x5410u), prmt(d2, d3, 0x5410u), prmt(d0, d1, 0x7632u), prmt(d2, d3, 0x7632u));
+// Both halves of an fp16 pair h = (1024 + q0, 1024 + q1) as weights in fp32:
+// w = s*(1024 + q) + bf with bf = b - 1024*s.  The product of two fp16 values
+// is exact in fp32 and the FMA rounds once (fma.rn.f32.f16: fp16 factors, fp32
+// addend and result).
+__device__ __forceinline__ void pair_to_f32(uint32_t h, uint16_t s16, float bf, float& w0, float& w1) {
+  asm("{\n .reg .f16 a, b, s;\n mov.b32 {a, b}, %2;\n mov.b16 s, %3;\n"
+      " fma.rn.f32.f16 %0, s, a, %4;\n fma.rn.f32.f16 %1, s, b, %4;\n}\n"
+      : "=f"(w0), "=f"(w1)
+      : "r"(h), "h"(s16), "f"(bf));
 }
-
-// Exact small integers (< 2048) held as an f16 pair -> the same integers as a bf16 pair
-// (exact for values below 256, which is every 8-bit code).
-__device__ __forceinline__ uint32_t f16x2_int_to_bf16x2(uint32_t h) {
-  const float lo = __half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu)));
-  const float hi = __half2float(__ushort_as_half((uint16_t)(h >> 16)));
+// Two fp32 values -> one bf16 pair (lo in bits 0..15), each rounded once.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
 }
-
-// Four 8-bit codes (one word) -> four halves.  The code pair is formed exactly
-// as f16 "1024 + q" (bf16 has too few mantissa bits for 8-bit codes).
-template <bool BF16>
-__device__ __forceinline__ uint2 deq4_q8(uint32_t w, uint32_t s2, uint32_t b2) {
-  constexpr uint32_t MG16 = 0x64006400u;
-  uint32_t d0 = hsub2<false>(prmt(w, 0x64646464u, 0x4140u), MG16);   // (q0, q1) exact in f16
-  uint32_t d1 = hsub2<false>(prmt(w, 0x64646464u, 0x4342u), MG16);   // (q2, q3)
-  if constexpr (BF16) {
-    d0 = f16x2_int_to_bf16x2(d0);
-    d1 = f16x2_int_to_bf16x2(d1);
+// The weight pair (w0, w1) for the A tile: bf16 hi = round(w), and with SPLIT
+// the residual lo = round(w - hi), so that hi + lo holds w to 16 bits.
+template <bool SPLIT>
+__device__ __forceinline__ void emit_bf16(float w0, float w1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(w0, w1);
+  if constexpr (SPLIT) {
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+    lo = pack_bf16(w0 - h0, w1 - h1);
   }
-  d0 = hfma2<BF16>(d0, s2, b2);
-  d1 = hfma2<BF16>(d1, s2, b2);
-  return make_uint2(d0, d1);
 }
 
 // Generic: code j (bits j*B.. of a little-endian word array) as an integer.
@@ -253,43 +252,84 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[NW], int j) {
   return q & ((1u << B) - 1u);
 }
 
-// Dequantize this thread's 4 chunks (32 codes) of one row into 4 x 16 bytes.
-template <int BITS, bool BF16>
-__device__ __forceinline__ void deq32(const uint32_t (&w)[BITS], uint32_t s2, uint32_t b2, uint4 (&out)[4]) {
+// The 16 code pairs of this thread's 32 codes as fp16 (1024 + q) pairs, in
+// the order they are written: pair i holds codes (p_lo[i], p_hi[i]) of the
+// chunk; `kord` tells whether pair i already holds codes (2i, 2i+1).
+// Q4: per word, (q0,q4) (q1,q5) (q2,q6) (q3,q7) from one LOP3 each.
+template <int BITS>
+__device__ __forceinline__ void code_pairs(const uint32_t (&w)[BITS], uint32_t (&h)[16]) {
   if constexpr (BITS == 4) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) out[c] = deq8_q4<BF16>(w[c], s2, b2);
+    for (int c = 0; c < 4; ++c) {
+      h[4 * c + 0] = lop3_and_or(w[c], 0x000F000Fu, kMagic16);         // (q0, q4)
+      h[4 * c + 1] = lop3_and_or(w[c] >> 4, 0x000F000Fu, kMagic16);    // (q1, q5)
+      h[4 * c + 2] = lop3_and_or(w[c] >> 8, 0x000F000Fu, kMagic16);    // (q2, q6)
+      h[4 * c + 3] = lop3_and_or(w[c] >> 12, 0x000F000Fu, kMagic16);   // (q3, q7)
+    }
   } else if constexpr (BITS == 8) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint2 lo = deq4_q8<BF16>(w[2 * c], s2, b2), hi = deq4_q8<BF16>(w[2 * c + 1], s2, b2);
-      out[c] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    for (int c = 0; c < 8; ++c) {
+      h[2 * c] = prmt(w[c], kMagic16, 0x7170u);       // (q0, q1): bytes 0, 1 under 0x64 high bytes
+      h[2 * c + 1] = prmt(w[c], kMagic16, 0x7372u);   // (q2, q3)
     }
   } else {
-    constexpr uint32_t MG = kMagic2<BF16>;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = code_at<BITS, BITS>(w, 8 * c + 2 * i), hi = code_at<BITS, BITS>(w, 8 * c + 2 * i + 1);
-        uint32_t pr;
-        asm("lop3.b32 %0, %1, %2, %3, 0xFE;" : "=r"(pr) : "r"(lo), "r"(hi << 16), "r"(MG));   // lo | hi<<16 | MG
-        o[i] = hfma2<BF16>(hsub2<BF16>(pr, MG), s2, b2);
-      }
-      out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t lo = code_at<BITS, BITS>(w, 2 * i), hi = code_at<BITS, BITS>(w, 2 * i + 1);
+      uint32_t pr;
+      asm("lop3.b32 %0, %1, %2, %3, 0xFE;" : "=r"(pr) : "r"(lo), "r"(hi << 16), "r"(kMagic16));   // lo | hi<<16 | M
+      h[i] = pr;
     }
   }
 }
 
-template <bool BF16> __device__ __forceinline__ uint32_t half_pair(uint16_t h16) {
-  // fp16 parameter -> pair of the A type (bf16 rounds; f16 is exact)
+// Dequantize this thread's 32 codes of one row into 16 pairs in k order
+// (out[j] holds k = 2j, 2j+1): the A tile's 16 TMEM columns.  With SPLIT
+// (bf16 only) `lo` receives the residual tile.
+template <int BITS, bool BF16, bool SPLIT>
+__device__ __forceinline__ void deq32(const uint32_t (&w)[BITS], uint16_t s16, uint16_t b16, uint32_t (&out)[16],
+                                      uint32_t (&lo)[16]) {
+  uint32_t h[16];
+  code_pairs<BITS>(w, h);
   if constexpr (BF16) {
-    const __nv_bfloat16 v = __float2bfloat16_rn(__half2float(__ushort_as_half(h16)));
-    const uint32_t u = __bfloat16_as_ushort(v);
-    return u | (u << 16);
+    const float s = __half2float(__ushort_as_half(s16));
+    const float bf = __half2float(__ushort_as_half(b16)) - 1024.f * s;   // exact for min/max-quantized groups
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pair_to_f32(h[4 * c + i], s16, bf, f[i], f[i + 4]);   // codes i, i+4
+#pragma unroll
+        for (int j = 0; j < 4; ++j) emit_bf16<SPLIT>(f[2 * j], f[2 * j + 1], out[4 * c + j], lo[4 * c + j]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float f0, f1;
+        pair_to_f32(h[i], s16, bf, f0, f1);
+        emit_bf16<SPLIT>(f0, f1, out[i], lo[i]);
+      }
+    }
   } else {
-    return (uint32_t)h16 | ((uint32_t)h16 << 16);
+    // fp16: the exact integer pair times s plus b, one rounding per weight
+    const uint32_t s2 = (uint32_t)s16 | ((uint32_t)s16 << 16), b2 = (uint32_t)b16 | ((uint32_t)b16 << 16);
+    uint32_t d[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) d[i] = hfma2_f16(hsub2_f16(h[i], kMagic16), s2, b2);
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t* e = d + 4 * c;   // (q0,q4) (q1,q5) (q2,q6) (q3,q7)
+        out[4 * c + 0] = prmt(e[0], e[1], 0x5410u);
+        out[4 * c + 1] = prmt(e[2], e[3], 0x5410u);
+        out[4 * c + 2] = prmt(e[0], e[1], 0x7632u);
+        out[4 * c + 3] = prmt(e[2], e[3], 0x7632u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) out[i] = d[i];
+    }
   }
 }
 
@@ -300,7 +340,7 @@ __device__ __forceinline__ void store_y(const TcParams& p, size_t i, float v) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BITS, bool BF16, int BN, bool GROUPED>
+template <int BITS, bool BF16, int BN, bool GROUPED, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                     const TcParams p) {
@@ -333,8 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int m0 = blockIdx.y * BN;     // first grouped/dense row of the tile
   int m_end = p.M;              // one past its last valid row
   int expert = 0;
-  constexpr int kTmemCols = tmem_cols<BN>();
+  constexpr int kTmemCols = tmem_cols<BN, SPLIT>();
   constexpr uint32_t kACol0 = acc_cols<BN>();   // first column of the A slots
+  constexpr uint32_t kASlot = a_slot_cols<SPLIT>();
 
   if constexpr (GROUPED) {
     // Tile blockIdx.y of the expert-major list of (expert, BN-row tile) pairs;
@@ -489,11 +530,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         if constexpr (GROUPED) fence_proxy_async();   // X rows written by cp.async / zero fill are read by the tensor core
-        const uint32_t a_tmem = tmem_base + kACol0 + (uint32_t)(a * 32);
+        const uint32_t a_tmem = tmem_base + kACol0 + (uint32_t)a * kASlot;
         const uint64_t bdesc = sw128_desc(smem_u32(tring) + (uint32_t)(s * p.stage_bytes));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)   // 16 elements: 8 TMEM columns of A, 32 bytes of B per MMA step
+        for (int kk = 0; kk < BK / 16; ++kk) {   // 16 elements: 8 TMEM columns of A, 32 bytes of B per MMA step
           mma_f16_ta(tmem_base, a_tmem + (uint32_t)(kk * 8), bdesc + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+          if constexpr (SPLIT)   // the residual tile against the same X columns
+            mma_f16_ta(tmem_base, a_tmem + 32u + (uint32_t)(kk * 8), bdesc + (uint64_t)(kk * 2), idesc, 1u);
+        }
         mma_commit(&empty[s]);   // frees the TMA stage, and the A slot for K block kb + SA
         if (++s == S) { s = 0; ph ^= 1u; }
         if (++a == SA) { a = 0; aph ^= 1u; }
@@ -562,13 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < BITS; ++i) w[i] = lds32(caddr + 4 * i);
       }
-      const uint32_t s2 = half_pair<BF16>(lds16(sS_a + (uint32_t)(r * Gc + kb) * 2));
-      const uint32_t b2 = half_pair<BF16>(lds16(sB_a + (uint32_t)(r * Gc + kb) * 2));
-      uint4 out[4];
-      deq32<BITS, BF16>(w, s2, b2, out);
-      const uint32_t v[16] = {out[0].x, out[0].y, out[0].z, out[0].w, out[1].x, out[1].y, out[1].z, out[1].w,
-                              out[2].x, out[2].y, out[2].z, out[2].w, out[3].x, out[3].y, out[3].z, out[3].w};
-      tmem_st16(tmem_base + lane_base + kACol0 + (uint32_t)(a * 32 + 16 * h), v);
+      const uint16_t s16 = lds16(sS_a + (uint32_t)(r * Gc + kb) * 2);
+      const uint16_t b16 = lds16(sB_a + (uint32_t)(r * Gc + kb) * 2);
+      uint32_t v[16], vlo[16];
+      deq32<BITS, BF16, SPLIT>(w, s16, b16, v, vlo);
+      const uint32_t slot = tmem_base + lane_base + kACol0 + (uint32_t)a * kASlot + (uint32_t)(16 * h);
+      tmem_st16(slot, v);
+      if constexpr (SPLIT) tmem_st16(slot + 32u, vlo);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -714,7 +758,7 @@ size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nul
 // where waves come from how many clusters of that size fit on the device at once.
 int choose_splits(int tiles, int K, int sms);
 
-template <int BITS, bool BF16, int BN, bool GROUPED = false>
+template <int BITS, bool BF16, int BN, bool GROUPED, bool SPLIT>
 cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStream_t st) {
   if (splits <= 0) splits = GROUPED ? 1 : choose_splits(((gp.N + BM - 1) / BM) * ((gp.M + BN - 1) / BN), gp.K, sm_count());
   EncodeTiledFn enc = encode_fn();
@@ -784,9 +828,9 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   const size_t smem = tc_smem_bytes<BITS, BN, GROUPED>(gp.K, splits, &stages);
   if (smem == 0) return cudaErrorInvalidValue;
   p.stages = stages;
-  p.astages = std::min(kAStages, stages - 1);   // the dequant waits rely on S > SA
+  p.astages = std::min(a_stages<BN, SPLIT>(), stages - 1);   // the dequant waits rely on S > SA
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED>;
+  auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED, SPLIT>;
   static std::atomic<uint64_t> smem_raised{0};
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
@@ -826,37 +870,46 @@ int choose_splits(int tiles, int K, int sms) {
   return best;
 }
 
-template <int BITS, bool BF16>
+template <int BITS, bool BF16, bool SPLIT>
 cudaError_t launch_tc_bn(const GemmParams& gp, bt_dtype yd, int bn, int splits, cudaStream_t st) {
   switch (bn) {
-    case 32: return launch_tc_t<BITS, BF16, 32>(gp, yd, splits, st);
-    case 64: return launch_tc_t<BITS, BF16, 64>(gp, yd, splits, st);
-    case 128: return launch_tc_t<BITS, BF16, 128>(gp, yd, splits, st);
-    default: return launch_tc_t<BITS, BF16, 256>(gp, yd, splits, st);
+    case 32: return launch_tc_t<BITS, BF16, 32, false, SPLIT>(gp, yd, splits, st);
+    case 64: return launch_tc_t<BITS, BF16, 64, false, SPLIT>(gp, yd, splits, st);
+    case 128: return launch_tc_t<BITS, BF16, 128, false, SPLIT>(gp, yd, splits, st);
+    default: return launch_tc_t<BITS, BF16, 256, false, SPLIT>(gp, yd, splits, st);
   }
 }
 
+// bf16 X with fp32 Y takes the split (hi + lo) A tiles; every other pairing the
+// single tile (fp16 A is exact to one fp16 rounding; bf16 Y rounds coarser
+// than a bf16 weight).
 template <int BITS>
 cudaError_t launch_tc_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int bn, int splits, cudaStream_t st) {
-  if (xd == BT_BF16) return launch_tc_bn<BITS, true>(gp, yd, bn, splits, st);
-  return launch_tc_bn<BITS, false>(gp, yd, bn, splits, st);
+  if (xd == BT_BF16) {
+    if (yd == BT_F32) return launch_tc_bn<BITS, true, true>(gp, yd, bn, splits, st);
+    return launch_tc_bn<BITS, true, false>(gp, yd, bn, splits, st);
+  }
+  return launch_tc_bn<BITS, false, false>(gp, yd, bn, splits, st);
 }
 
 
-template <int BITS, bool BF16>
+template <int BITS, bool BF16, bool SPLIT>
 cudaError_t launch_tc_grouped_bn(const GemmParams& gp, bt_dtype yd, int bn, cudaStream_t st) {
   switch (bn) {
-    case 16: return launch_tc_t<BITS, BF16, 16, true>(gp, yd, 1, st);
-    case 32: return launch_tc_t<BITS, BF16, 32, true>(gp, yd, 1, st);
-    case 64: return launch_tc_t<BITS, BF16, 64, true>(gp, yd, 1, st);
-    default: return launch_tc_t<BITS, BF16, 128, true>(gp, yd, 1, st);
+    case 16: return launch_tc_t<BITS, BF16, 16, true, SPLIT>(gp, yd, 1, st);
+    case 32: return launch_tc_t<BITS, BF16, 32, true, SPLIT>(gp, yd, 1, st);
+    case 64: return launch_tc_t<BITS, BF16, 64, true, SPLIT>(gp, yd, 1, st);
+    default: return launch_tc_t<BITS, BF16, 128, true, SPLIT>(gp, yd, 1, st);
   }
 }
 
 template <int BITS>
 cudaError_t launch_tc_grouped_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int bn, cudaStream_t st) {
-  if (xd == BT_BF16) return launch_tc_grouped_bn<BITS, true>(gp, yd, bn, st);
-  return launch_tc_grouped_bn<BITS, false>(gp, yd, bn, st);
+  if (xd == BT_BF16) {
+    if (yd == BT_F32) return launch_tc_grouped_bn<BITS, true, true>(gp, yd, bn, st);
+    return launch_tc_grouped_bn<BITS, true, false>(gp, yd, bn, st);
+  }
+  return launch_tc_grouped_bn<BITS, false, false>(gp, yd, bn, st);
 }
 
 // Host-only geometry of one tensor-core launch: the shared memory, ring depth

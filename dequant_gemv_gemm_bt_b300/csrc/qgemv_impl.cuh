@@ -598,6 +598,11 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
   uint64_t* empty = full + S;
   float* red = reinterpret_cast<float*>(empty + S);        // [kNW/KW][2][RI][KW] = kNW*2*RI floats
   int* offs = reinterpret_cast<int*>(red + kNW * 2 * RI);  // [E+1] when grouped
+  // Set once any wait of this CTA has expired: from then on every warp skips
+  // its waits, loads and stores but still walks the loop and reaches every
+  // named barrier its row group and the CTA execute, so no partner is left
+  // waiting at a barrier that cannot time out.
+  __shared__ volatile int s_fail;
 
   // contiguous range of units for this CTA
   long long u_begin, u_end;
@@ -613,6 +618,7 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
   // cp.async-tracked arrive from each producer lane (scales and biases).
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(&full[s], 33); mbar_init(&empty[s], kNW); }
+    s_fail = 0;
     fence_mbar_init();
   }
   if (p.moe_offsets) {
@@ -643,7 +649,7 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
       if (it >= S) {
         bool w = true;
         if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
-        if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; break; }
+        if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; s_fail = 1; break; }
       }
       const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
       const int row0 = blk * RB;
@@ -694,6 +700,7 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
   pdl_wait();   // activations (and offsets) may come from the previous kernel
 
   XSlice<BITS, FAST> xs[CPL];
+  bool dead = false;   // this warp gave up on a wait, or saw another warp of the CTA give up
   int rbuf = 0;
   int prob, blk;
   first_unit<BATCH>(p, batch, u_begin, prob, blk);
@@ -730,7 +737,10 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
         }
       }
     }
-    if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) return;
+    if (!dead && (s_fail || !mbar_wait(&full[s], ph, p.timeout_ns, p.err))) {
+      dead = true;
+      s_fail = 1;
+    }
     const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
     const int row0 = blk * RB;
     const int rows = min(RB, v.n - row0);
@@ -746,9 +756,12 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
     // The row batches of this unit.  Instantiated per (rows need clamping, unit
     // staged in shared memory), chosen once per unit, so the common case -- a
     // full unit in shared memory -- has no per-row bounds or source branches.
-    auto batches = [&](auto clamp_tag, auto staged_tag) {
+    // LIVE = false walks the same batches and barriers without touching memory
+    // (a warp after an expired wait).
+    auto batches = [&](auto clamp_tag, auto staged_tag, auto live_tag) {
       constexpr bool CLAMP = decltype(clamp_tag)::value;
       constexpr bool STAGED = decltype(staged_tag)::value;
+      constexpr bool LIVE = decltype(live_tag)::value;
     for (int bi = rg; bi < nb; bi += RW) {
       const int r0 = bi * RI;
       float part[RI];
@@ -757,7 +770,7 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = (i * KW + kw) * 32 + lane;
-        if (c < nchunks) {
+        if (LIVE && c < nchunks) {
           uint32_t w[RI][BITS];
           float sc[RI], bs[RI];
 #pragma unroll
@@ -786,12 +799,12 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
       const float val = reduce_rows<RI>(part, lane, rj);
       const int r = r0 + rj;
       if (KW == 1) {
-        if (writer && r < rows && v.valid) store_yv(p, v.y, ybase + r, val);
+        if (LIVE && writer && r < rows && v.valid) store_yv(p, v.y, ybase + r, val);
       } else {
         float* rb = red + (size_t)((rg * 2 + rbuf) * RI) * KW;   // [RI][KW]
         if (writer) rb[rj * KW + kw] = val;
         asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
-        if (kw == 0 && writer && r < rows && v.valid) {
+        if (LIVE && kw == 0 && writer && r < rows && v.valid) {
           float acc = 0.f;
           for (int j = 0; j < KW; ++j) acc += rb[rj * KW + j];
           store_yv(p, v.y, ybase + r, acc);
@@ -802,14 +815,18 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
     };
     using yes = std::integral_constant<bool, true>;
     using no = std::integral_constant<bool, false>;
-    if (tma) {
-      if (rows == nb * RI) batches(no{}, yes{});
-      else batches(yes{}, yes{});
+    if (dead) {
+      batches(yes{}, no{}, no{});
+    } else if (tma) {
+      if (rows == nb * RI) batches(no{}, yes{}, yes{});
+      else batches(yes{}, yes{}, yes{});
     } else {
-      batches(yes{}, no{});
+      batches(yes{}, no{}, yes{});
     }
+    // A warp that gave up does not arrive: the producer's own bounded wait on
+    // this stage then expires and it drains its copies.
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (!dead && lane == 0) mbar_arrive(&empty[s]);
     ++blk;
     if (++s == S) { s = 0; ph ^= 1u; }
   }

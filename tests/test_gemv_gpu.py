@@ -122,11 +122,14 @@ def test_qgemv_generic_path_matches_fast(env):
         assert_close(y_fast, y_ref, a, "f32", "fast")
 
 
-def test_device_wait_timeout_is_reported(env):
+@pytest.mark.parametrize("k", [1024, 3072, 8192])
+def test_device_wait_timeout_is_reported(env, k):
     """A stage that is never filled makes the consumers' bounded waits expire;
-    the call reports BT_ERR_TIMEOUT and the context stays usable."""
+    the call reports BT_ERR_TIMEOUT and the context stays usable.  K = 3072 and
+    8192 split each row over 4 and 8 warps that meet at named barriers: warps
+    that gave up still reach every barrier, so none is left waiting."""
     torch, bt = env
-    qw, x = make_case("timeout", 4000, 1024, 4)
+    qw, x = make_case("timeout", 4000, k, 4)
     codes, scales, biases = to_dev(qw, torch)
     xt = half_tensor(x[0], "f16", torch)
     assert bt.bt_last_device_error() == bt.BT_OK
@@ -142,6 +145,37 @@ def test_device_wait_timeout_is_reported(env):
     y = run(env, qw, x, "f16", "f32")
     y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]))
     assert_close(y, y_ref, a, "f32", "after timeout")
+
+
+def test_device_wait_timeout_mixed_k_batch(env):
+    """The same expiry in a mixed-K batch, whose CTAs also meet at the barrier
+    taken when the K split changes between problems."""
+    torch, bt = env
+    from dequant_gemv_gemm_bt_b300 import synth
+    r = synth.rng_for("test", "timeout-mixed")
+    probs, cases = [], []
+    for k in (3072, 1024, 2048, 1024, 3072):
+        qw = synth.make_qweight(r, 900, k, 4)
+        x16 = synth.draw_activations(r, 1, k, "f16")
+        codes, scales, biases = to_dev(qw, torch)
+        y = torch.empty(900, dtype=torch.float32, device="cuda")
+        probs.append((codes, scales, biases, half_tensor(x16[0], "f16", torch), y))
+        cases.append((qw, x16))
+    assert bt.bt_last_device_error() == bt.BT_OK
+    try:
+        bt.bt_set_option(bt.BT_OPT_WAIT_TIMEOUT_US, 20000)
+        bt.bt_set_option(bt.BT_OPT_TEST_DROP_STAGE, 1)
+        bt.bt_qgemv_batched(probs, 4)
+        assert bt.bt_last_device_error() == bt.BT_ERR_TIMEOUT
+    finally:
+        bt.bt_set_option(bt.BT_OPT_TEST_DROP_STAGE, 0)
+        bt.bt_set_option(bt.BT_OPT_WAIT_TIMEOUT_US, 4000000)
+    bt.bt_qgemv_batched(probs, 4)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for (qw, x16), pr in zip(cases, probs):
+        y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x16[0]))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"after timeout k={qw.k}")
 
 
 @pytest.mark.parametrize("bits", BITS)

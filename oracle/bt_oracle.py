@@ -152,6 +152,43 @@ def silu(v: np.ndarray) -> np.ndarray:
     return v / (1.0 + np.exp(-v))
 
 
+def swiglu(gate_up: np.ndarray):
+    """``h = silu(gate) * up`` for ``gate_up = [gate | up]`` of shape ``[R, 2I]``.
+
+    The step between an expert's gate/up and down products (thetesserapress.com,
+    "Where the wins land, and where they don't": the MoE layers whose expert
+    products these are).  The pages do not name the activation; SwiGLU is the
+    reading taken, the plainest for the Qwen3 family the workloads are shaped
+    after.  Returns ``(h [R, I], A = |h|)``: an elementwise step, so its
+    tolerance scale is the magnitude of the exact result.
+    """
+    gu = np.asarray(gate_up, dtype=np.float64)
+    inter = gu.shape[1] // 2
+    h = silu(gu[:, :inter]) * gu[:, inter:]
+    return h, np.abs(h)
+
+
+def moe_combine(y_grouped: np.ndarray, gates: np.ndarray, pair_index: np.ndarray, top_k: int):
+    """Gate-weighted combine: ``out[t] = sum_s g[t, s] * y_grouped[row of pair t*k + s]``.
+
+    The last step of the expert layer (thetesserapress.com, "Where the wins
+    land, and where they don't"): each token's expert outputs, weighted by its
+    routing gates and summed.  ``pair_index[r]`` is the pair placed at grouped
+    row ``r`` (from ``route_sort``).  Returns ``(out [T, H], A = sum_s |g[t, s]
+    * y|)``, the per-element tolerance scale of a sum of products.
+    """
+    y = np.asarray(y_grouped, dtype=np.float64)
+    g = np.asarray(gates, dtype=np.float64)
+    t_count = g.shape[0]
+    out = np.zeros((t_count, y.shape[1]))
+    a = np.zeros((t_count, y.shape[1]))
+    gflat = g.reshape(-1)
+    for r, pair in enumerate(np.asarray(pair_index)):
+        out[pair // top_k] += gflat[pair] * y[r]
+        a[pair // top_k] += np.abs(gflat[pair] * y[r])
+    return out, a
+
+
 def moe_layer(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, gate_w, up_w, down_w,
               bits: int, group_size: int = 64):
     """One expert layer in fp64: ``out[t] = sum_k g[t,k] * down_e(silu(gate_e x_t) * up_e x_t)``.
@@ -160,7 +197,7 @@ def moe_layer(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, gate_w, up_w, d
     Returns ``(out [T, H], h [T*k, I] in grouped row order, offsets, pair_index)``.
     """
     x = np.asarray(x, dtype=np.float64)
-    t_count, top_k = ids.shape
+    top_k = ids.shape[1]
     e_count = gate_w[0].shape[0]
     offsets, pair_index = route_sort(ids, e_count)
     xg = x[pair_index // top_k]
@@ -168,10 +205,7 @@ def moe_layer(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, gate_w, up_w, d
     u_out, _ = moe_qgemm(*up_w, bits, offsets, xg, group_size)
     h = silu(g_out) * u_out
     d_out, _ = moe_qgemm(*down_w, bits, offsets, h, group_size)
-    out = np.zeros((t_count, d_out.shape[1]))
-    gflat = np.asarray(gates, dtype=np.float64).reshape(-1)
-    for r, p in enumerate(pair_index):
-        out[p // top_k] += gflat[p] * d_out[r]
+    out, _ = moe_combine(d_out, gates, pair_index, top_k)
     return out, h, offsets, pair_index
 
 

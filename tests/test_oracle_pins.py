@@ -395,6 +395,27 @@ def test_moe_combine_is_the_gate_weighted_sum_of_single_slot_layers():
     np.testing.assert_allclose(scaled, 3.0 * out, rtol=1e-12, atol=1e-14)
 
 
+def test_moe_combine_hand_example():
+    """Two tokens, top-2, rows placed out of pair order: each output is the
+    gate-weighted sum of the rows its pairs were placed at (values by hand)."""
+    y = np.array([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0], [7.0, 8.0]])
+    pair_index = np.array([2, 0, 3, 1])            # grouped row r holds pair pair_index[r]
+    gates = np.array([[0.5, 0.25], [2.0, -1.0]])
+    out, a = O.moe_combine(y, gates, pair_index, 2)
+    # token 0: pairs 0 (row 1) and 1 (row 3); token 1: pairs 2 (row 0) and 3 (row 2)
+    np.testing.assert_array_equal(out, [[3.25, 4.0], [-3.0, -2.0]])
+    np.testing.assert_array_equal(a, [[3.25, 4.0], [7.0, 10.0]])
+
+
+def test_swiglu_matches_silu_of_gate_times_up():
+    gu = np.array([[0.0, np.log(3.0), 2.0, -1.0], [1.0, -2.0, 0.5, 4.0]])
+    h, a = O.swiglu(gu)
+    np.testing.assert_allclose(h[0], [0.0, -0.75 * np.log(3.0)], rtol=1e-15, atol=0)   # silu(ln 3) = 3/4 ln 3
+    np.testing.assert_allclose(h[1], [0.5 * O.silu(np.array([1.0]))[0], 4.0 * O.silu(np.array([-2.0]))[0]],
+                               rtol=1e-15)
+    np.testing.assert_array_equal(a, np.abs(h))
+
+
 def test_planted_combine_mistakes_are_caught(monkeypatch):
     """A combine that drops the gates or takes one slot only fails the pin above."""
     real = O.moe_layer

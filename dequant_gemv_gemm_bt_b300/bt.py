@@ -31,7 +31,8 @@ BT_OK, BT_ERR_INVALID_ARG, BT_ERR_UNSUPPORTED, BT_ERR_MISALIGNED, BT_ERR_CUDA, B
 BT_F16, BT_BF16, BT_F32 = 0, 1, 2
 (BT_OPT_PDL, BT_OPT_CONST_WEIGHTS, BT_OPT_WAIT_TIMEOUT_US, BT_OPT_TEST_DROP_STAGE,
  BT_OPT_GEMV_GENERIC, BT_OPT_GEMV_STAGES, BT_OPT_GEMM_PATH, BT_OPT_GEMM_SPLITS, BT_OPT_GEMV_MAX_CPL,
- BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI) = range(11)
+ BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI, BT_OPT_GEMV_CUDA_CORE, BT_OPT_GEMV_MMA_STAGE_KB, BT_OPT_GEMV_MMA_SHAPE,
+ BT_OPT_GEMV_MMA_GROUPS, BT_OPT_GEMV_TENSOR_PIPE) = range(16)
 
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_route", "bt_swiglu", "bt_moe_combine",
            "bt_status_string", "bt_last_device_error", "bt_set_option", "bt_plan_gemv", "bt_plan_gemv_batch", "bt_plan_gemm")
@@ -63,7 +64,7 @@ class GemvPlan(ctypes.Structure):
     _fields_ = [("feasible", ctypes.c_int32), ("kw", ctypes.c_int32), ("cpl", ctypes.c_int32), ("ri", ctypes.c_int32),
                 ("rows_per_unit", ctypes.c_int32), ("stage_bytes", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("grid", ctypes.c_int32), ("num_units", ctypes.c_int64),
-                ("smem_bytes", ctypes.c_int64)]
+                ("smem_bytes", ctypes.c_int64), ("tensor_pipe", ctypes.c_int32)]
 
 
 lib.bt_plan_gemv.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.POINTER(GemvPlan)]

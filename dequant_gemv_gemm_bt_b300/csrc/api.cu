@@ -124,7 +124,8 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.const_weights = opts().pdl && opts().const_weights;
   p.drop_stage = opts().test_drop_stage;
   opts().test_drop_stage = 0;
-  const GemvPlan pl = plan_gemv(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count());
+  GemvPlan pl = plan_gemv_mma(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count());
+  if (!pl.feasible) pl = plan_gemv(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count());
   if (!pl.feasible) {
     // no GEMV kernel holds this K slice in registers: the CUDA-core tile computes the same product
     GemmParams g{};
@@ -148,13 +149,14 @@ using namespace bt;
 namespace {
 void fill_plan(const bt::GemvPlan& pl, bt_gemv_plan* out) {
   out->feasible = pl.feasible ? 1 : 0;
+  out->tensor_pipe = pl.mma ? 1 : 0;
   out->kw = pl.kw;
   out->cpl = pl.cpl;
   out->ri = pl.ri;
   out->rows_per_unit = pl.rows_per_unit;
   out->stage_bytes = pl.stage_bytes;
   out->stages = pl.stages;
-  out->ctas_per_sm = bt::gemv_ctas_per_sm(pl.cpl, pl.ri);
+  out->ctas_per_sm = pl.mma ? pl.mma_ctas : bt::gemv_ctas_per_sm(pl.cpl, pl.ri);
   out->grid = pl.grid;
   out->num_units = pl.num_units;
   out->smem_bytes = (int64_t)pl.smem;
@@ -179,7 +181,9 @@ bt_status bt_plan_gemv(int bits, bt_dtype x_dtype, int N, int K, int problems, i
   if (!plan || N <= 0 || K <= 0 || K % kGroup || problems <= 0 || sms <= 0 || !half_dtype(x_dtype))
     return BT_ERR_INVALID_ARG;
   if (!bits_ok(bits) || K > kMaxK) return BT_ERR_UNSUPPORTED;
-  fill_plan(plan_gemv(bits, gemv_fast_path(bits, x_dtype), N, K, problems, 0, sms), plan);
+  GemvPlan pl = plan_gemv_mma(bits, gemv_fast_path(bits, x_dtype), N, K, problems, 0, sms);
+  if (!pl.feasible) pl = plan_gemv(bits, gemv_fast_path(bits, x_dtype), N, K, problems, 0, sms);
+  fill_plan(pl, plan);
   return BT_OK;
 }
 
@@ -196,7 +200,8 @@ bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n, const
     batch.prob[i].n = n[i];
     batch.prob[i].k = k[i];
   }
-  GemvPlan pl = plan_gemv_batch(bits, gemv_fast_path(bits, x_dtype), batch, sms);
+  GemvPlan pl = plan_gemv_batch_mma(bits, gemv_fast_path(bits, x_dtype), batch, sms);
+  if (!pl.feasible) pl = plan_gemv_batch(bits, gemv_fast_path(bits, x_dtype), batch, sms);
   if (pl.feasible) {
     for (int i = 0; i < count; ++i) {
       units += (batch.prob[i].n + batch.prob[i].rb - 1) / batch.prob[i].rb;
@@ -204,7 +209,7 @@ bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n, const
       if (rows_per_unit) rows_per_unit[i] = batch.prob[i].rb;
     }
     pl.num_units = units;
-    pl.grid = (int)std::min<long long>(units, (long long)sms * gemv_ctas_per_sm(pl.cpl, pl.ri));
+    pl.grid = (int)std::min<long long>(units, (long long)sms * (pl.mma ? pl.mma_ctas : gemv_ctas_per_sm(pl.cpl, pl.ri)));
   }
   fill_plan(pl, plan);
   return BT_OK;
@@ -219,7 +224,8 @@ bt_status bt_plan_gemm(int bits, bt_dtype x_dtype, int M, int N, int K, int num_
   GemmPath path = gemm_path(bits, M, K, num_experts);
   GemmGeometry g;
   if (path == kPathGemv) {
-    const GemvPlan pl = plan_gemv(bits, gemv_fast_path(bits, x_dtype), N, K, num_experts ? M : 1, num_experts, sms);
+    GemvPlan pl = plan_gemv_mma(bits, gemv_fast_path(bits, x_dtype), N, K, num_experts ? M : 1, num_experts, sms);
+    if (!pl.feasible) pl = plan_gemv(bits, gemv_fast_path(bits, x_dtype), N, K, num_experts ? M : 1, num_experts, sms);
     if (pl.feasible) {
       g.feasible = true;
       g.stages = pl.stages;
@@ -259,6 +265,11 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_MAX_CPL: opts().gemv_max_cpl = (int)std::min<long long>(value, 4); return BT_OK;
     case BT_OPT_GEMV_RI: opts().gemv_ri = value >= 8 ? 8 : value >= 4 ? 4 : (value >= 2 ? 2 : (int)value); return BT_OK;
     case BT_OPT_GEMV_STAGE_KB: opts().gemv_stage_kb = value == 0 ? 0 : (int)std::max(4LL, std::min(value, 96LL)); return BT_OK;
+    case BT_OPT_GEMV_CUDA_CORE: opts().gemv_cuda_core = value != 0; return BT_OK;
+    case BT_OPT_GEMV_MMA_STAGE_KB: opts().gemv_mma_stage_kb = value == 0 ? 0 : (int)std::max(8LL, std::min(value, 112LL)); return BT_OK;
+    case BT_OPT_GEMV_MMA_SHAPE: opts().gemv_mma_cfg = (int)std::min(value, 4LL); return BT_OK;
+    case BT_OPT_GEMV_TENSOR_PIPE: opts().gemv_tensor_pipe = (int)std::min(value, 2LL); return BT_OK;
+    case BT_OPT_GEMV_MMA_GROUPS: opts().gemv_mma_ks = value == 0 ? 0 : (int)std::max(1LL, std::min(value, 64LL)); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
 }
@@ -333,10 +344,16 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
   const bool fast = gemv_fast_path(bits, x_dtype);
   GemvPlan pl;
   if (mixed) {
-    pl = plan_gemv_batch(bits, fast, batch, sm_count());
+    pl = plan_gemv_batch_mma(bits, fast, batch, sm_count());
+    if (!pl.feasible) pl = plan_gemv_batch(bits, fast, batch, sm_count());
   } else {
     const int problems_equiv = (int)std::max<long long>(1, (rows + max_n - 1) / max_n);
-    pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count());
+    // the tensor-pipe kernel needs every problem's units (its ragged last one too) 16-byte aligned
+    bool all_mma = true;
+    for (int i = 0; i < count && all_mma; ++i)
+      all_mma = plan_gemv_mma(bits, fast, problems[i].n, K, 1, 0, sm_count()).feasible;
+    pl = all_mma ? plan_gemv_mma(bits, fast, max_n, K, problems_equiv, 0, sm_count()) : GemvPlan{};
+    if (!pl.feasible) pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count());
   }
   if (!pl.feasible) return BT_ERR_UNSUPPORTED;
   return cuda_status(launch_gemv(p, pl, bits, x_dtype, y_dtype, stream, &batch));

@@ -32,6 +32,11 @@ struct LaunchOpts {
   int gemv_max_cpl = 0;      // tuning: GEMV chunks per lane before splitting K over warps (0 = heuristic)
   int gemv_stage_kb = 0;     // tuning: GEMV stage size in KiB (0 = heuristic)
   int gemv_ri = 0;           // tuning: GEMV rows in flight per warp (0 = heuristic)
+  int gemv_cuda_core = 0;    // tuning: 1 = GEMV on the CUDA-core kernel even where the tensor-pipe one applies
+  int gemv_tensor_pipe = 0;  // tuning: tensor-pipe GEMV 0 = by launch size, 1 = wherever it applies, 2 = never
+  int gemv_mma_stage_kb = 0; // tuning: tensor-pipe GEMV stage size in KiB (0 = heuristic)
+  int gemv_mma_cfg = 0;      // tuning: tensor-pipe GEMV kernel shape (0 = default, 1..4)
+  int gemv_mma_ks = 0;       // tuning: most quantization groups per warp in the tensor-pipe GEMV (0 = heuristic)
 };
 LaunchOpts& opts();
 unsigned* device_error_word();   // device address of the error word (current device)

@@ -11,6 +11,7 @@ cudaError_t launch_gemv_b3(const GemvParams&, const GemvPlan&, bt_dtype, const G
 cudaError_t launch_gemv_b4(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
 cudaError_t launch_gemv_b6(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
 cudaError_t launch_gemv_b8(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
+cudaError_t launch_gemv_mma_b4(const GemvParams&, const GemvPlan&, const GemvBatch<kBatchCap>*, cudaStream_t);
 
 namespace {
 constexpr int kMaxNW = 8;               // consumer warps per CTA (as in the kernel)
@@ -89,6 +90,165 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   while (pl.stages > 2 && smem_for(pl.stages) > kMaxSmem / ctas_per_sm) --pl.stages;
   pl.smem = smem_for(pl.stages);
   if (pl.smem > kMaxSmem) pl.feasible = false;
+  return pl;
+}
+
+// ---------------------------------------------------------- tensor-pipe GEMV
+// Geometry of one problem on the tensor-pipe kernel: K split over kw warps so
+// that each warp's slice holds at most 32 groups (2048 codes), 16-row tiles,
+// units of whole tiles up to the stage budget (and no more tiles than the
+// problem's share of one SM).  Returns false when the kernel does not apply.
+MmaShape mma_shape(int cfg) {
+  switch (cfg) {
+    case 1: return {8, 1, 2};
+    case 2: return {8, 1, 1};
+    case 3: return {16, 1, 1};
+    case 4: return {8, 2, 1};
+    default: return {8, 1, 2};
+  }
+}
+
+namespace {
+// shared memory one CTA may take when `ctas` CTAs share an SM (228 KB, 1 KB of
+// it reserved per CTA)
+size_t mma_smem_limit(int ctas) { return ctas == 1 ? 227 * 1024 : (228 * 1024) / ctas - 1024; }
+
+bool mma_applies(int bits, bool fast, int N, int K) {
+  if (opts().gemv_cuda_core || bits != 4 || !fast || K > kMmaMaxK || K % kGroup) return false;
+  if (opts().gemv_tensor_pipe == 2) return false;
+  const int G = K / kGroup, row_bytes = K * bits / 8;
+  // every unit, the ragged last one included, must move in 16-byte pieces
+  return ((long long)N * G * 2) % 16 == 0 && ((long long)N * row_bytes) % 16 == 0;
+}
+
+// Which launches take the tensor pipe by default.  Measured on B300 (decode
+// pass, lm_head, single N=2048 GEMV): with many 16-row tiles per SM the
+// CUDA-core kernel streams faster (4.08 vs 3.69 TB/s on the decode pass), while
+// a launch of at most one tile per SM runs faster on the tensor pipe, whose
+// warps then split K down to one group each (single Q4 GEMV N=2048 K=1024:
+// 2.72 vs 3.44 us).  BT_OPT_GEMV_TENSOR_PIPE 1 forces it wherever it applies,
+// 2 disables it.
+bool mma_by_size(long long rows, int sms) {
+  if (opts().gemv_tensor_pipe == 1) return true;
+  return (rows + 15) / 16 <= sms;
+}
+
+struct MmaGeom {
+  int kw, rb, row_bytes, per_row;
+};
+
+// per_sm_rows: the launch's rows per SM.  When those fill fewer 16-row tiles
+// than the CTA has warps, K is split further (down to one group per warp), so
+// that every warp has work (e.g. the single N=2048 GEMV: one tile per CTA,
+// eight warps on two groups each).
+MmaGeom mma_geom(int bits, int N, int K, long long per_sm_rows, int stage_budget, int nw) {
+  MmaGeom m{};
+  const int G = K / kGroup;
+  const int ks_max = opts().gemv_mma_ks > 0 ? opts().gemv_mma_ks : 32;
+  int kw = 1;
+  while (kw < nw && (G + kw - 1) / kw > ks_max) kw *= 2;
+  const long long tiles_per_sm = std::max<long long>(1, per_sm_rows / 16);
+  while (kw < nw && kw * tiles_per_sm < nw && 2 * kw <= G) kw *= 2;
+  m.kw = kw;
+  m.row_bytes = K * bits / 8;
+  m.per_row = m.row_bytes + 4 * G;
+  const int tile = 16 * m.per_row;
+  long long tiles = std::max(1, stage_budget / tile);
+  tiles = std::min<long long>(tiles, std::max<long long>(1, (per_sm_rows + 15) / 16));
+  tiles = std::min<long long>(tiles, (N + 15) / 16);
+  m.rb = (int)(16 * tiles);
+  return m;
+}
+
+int mma_stage_budget(const MmaShape& sh) {
+  if (opts().gemv_mma_stage_kb > 0) return opts().gemv_mma_stage_kb * 1024;
+  return sh.ctas == 1 ? 48 * 1024 : 24 * 1024;
+}
+
+// Shared memory of one CTA: ring, barriers, row-group partials, x sums, permuted x.
+size_t mma_smem(int stages, int stage, int g_max, int nw, int* xsum_bytes) {
+  const int xsb = (g_max * 4 + 15) / 16 * 16;
+  if (xsum_bytes) *xsum_bytes = xsb;
+  return (size_t)stages * stage + 2 * stages * sizeof(uint64_t) + (size_t)nw * 2 * 16 * sizeof(float) + xsb +
+         (size_t)g_max * 192;
+}
+
+int mma_stages(int stage, int g_max, const MmaShape& sh) {
+  int stages = 8;
+  while (stages > 2 && mma_smem(stages, stage, g_max, sh.nw, nullptr) > mma_smem_limit(sh.ctas)) --stages;
+  if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
+  return stages;
+}
+
+void set_shape(GemvPlan& pl, const MmaShape& sh) {
+  pl.mma_nw = sh.nw;
+  pl.mma_ctas = sh.ctas;
+  pl.mma_unroll = sh.unroll;
+}
+}  // namespace
+
+GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms) {
+  GemvPlan pl{};
+  pl.fast = fast;
+  pl.mma = true;
+  pl.cpl = 1;
+  pl.ri = 16;
+  if (num_experts || !mma_applies(bits, fast, N, K)) return pl;
+  if (!mma_by_size((long long)N * problems, sms)) return pl;
+  const MmaShape sh = mma_shape(opts().gemv_mma_cfg);
+  set_shape(pl, sh);
+  const long long per_sm = std::max<long long>(1, ((long long)N * problems + sms - 1) / sms);
+  const MmaGeom m = mma_geom(bits, N, K, per_sm / sh.ctas, mma_stage_budget(sh), sh.nw);
+  pl.kw = m.kw;
+  pl.rows_per_unit = m.rb;
+  pl.row_bytes = m.row_bytes;
+  pl.stage_bytes = (m.rb * m.per_row + 127) / 128 * 128;
+  const int G = K / kGroup;
+  pl.stages = mma_stages(pl.stage_bytes, G, sh);
+  pl.units_per_problem = (N + m.rb - 1) / m.rb;
+  pl.num_units = (long long)pl.units_per_problem * problems;
+  pl.grid = (int)std::min<long long>(pl.num_units, (long long)sms * sh.ctas);
+  pl.smem = mma_smem(pl.stages, pl.stage_bytes, G, sh.nw, nullptr);
+  pl.feasible = pl.smem <= mma_smem_limit(sh.ctas) && pl.stages >= 2;
+  return pl;
+}
+
+GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms) {
+  GemvPlan pl{};
+  pl.fast = fast;
+  pl.mma = true;
+  pl.cpl = 1;
+  pl.ri = 16;
+  long long rows = 0;
+  int g_max = 0;
+  for (int i = 0; i < batch.count; ++i) {
+    const GemvProblem& q = batch.prob[i];
+    if (q.k <= 0 || !mma_applies(bits, fast, q.n, q.k)) return pl;
+    rows += q.n;
+    g_max = std::max(g_max, q.k / kGroup);
+  }
+  if (!mma_by_size(rows, sms)) return pl;
+  const MmaShape sh = mma_shape(opts().gemv_mma_cfg);
+  set_shape(pl, sh);
+  const long long per_sm = std::max<long long>(1, (rows + sms - 1) / sms);
+  int stage = 0;
+  for (int i = 0; i < batch.count; ++i) {
+    GemvProblem& q = batch.prob[i];
+    const MmaGeom m = mma_geom(bits, q.n, q.k, per_sm / sh.ctas, mma_stage_budget(sh), sh.nw);
+    q.kw = m.kw;
+    q.g = q.k / kGroup;
+    q.row_bytes = m.row_bytes;
+    q.rb = m.rb;
+    stage = std::max(stage, (m.rb * m.per_row + 127) / 128 * 128);
+  }
+  pl.kw = batch.prob[0].kw;
+  pl.rows_per_unit = batch.prob[0].rb;
+  pl.row_bytes = batch.prob[0].row_bytes;
+  pl.stage_bytes = stage;
+  pl.stages = mma_stages(stage, g_max, sh);
+  pl.smem = mma_smem(pl.stages, stage, g_max, sh.nw, nullptr);
+  pl.grid = sms * sh.ctas;   // trimmed to the unit count at launch
+  pl.feasible = pl.smem <= mma_smem_limit(sh.ctas) && pl.stages >= 2;
   return pl;
 }
 
@@ -184,6 +344,14 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
     plb.grid = (int)std::min<long long>(u, (long long)sm_count() * gemv_ctas_per_sm(pl.cpl, pl.ri));
   }
   if (p.num_units == 0) return cudaSuccess;
+  if (pl.mma) {
+    int g_max = p.G;
+    if (batch)
+      for (int i = 0; i < batch->count; ++i) g_max = std::max(g_max, batch->prob[i].g);
+    mma_smem(pl.stages, pl.stage_bytes, g_max, pl.mma_nw, &p.xsum_bytes);
+    plb.grid = (int)std::min<long long>(p.num_units, (long long)sm_count() * pl.mma_ctas);
+    return launch_gemv_mma_b4(p, plb, batch, st);
+  }
   switch (bits) {
     case 2: return launch_gemv_b2(p, plb, xd, batch, st);
     case 3: return launch_gemv_b3(p, plb, xd, batch, st);

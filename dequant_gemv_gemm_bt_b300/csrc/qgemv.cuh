@@ -30,6 +30,8 @@ struct GemvParams {
   unsigned long long timeout_ns;
   int const_weights;
   int drop_stage;
+  // tensor-pipe kernel: shared-memory bytes reserved for the per-group x sums
+  int xsum_bytes;
 };
 
 // Batched launches: many independent GEMVs of the same bits and dtypes, each
@@ -56,6 +58,8 @@ template <int CAP> struct GemvBatch {
 
 struct GemvPlan {
   bool fast;
+  bool mma;        // the tensor-pipe kernel (qgemv_mma.cuh) rather than the CUDA-core one
+  int mma_nw, mma_ctas, mma_unroll;   // its consumer warps per CTA, CTAs per SM, steps per loop iteration
   bool feasible;   // false: no GEMV kernel fits this shape (the caller uses the CUDA-core tile)
   int kw, cpl, ri, rows_per_unit, row_bytes, stage_bytes, stages, units_per_problem, grid;
   long long num_units;
@@ -66,12 +70,24 @@ struct GemvPlan {
 // runs 2 CTAs with 4 rows in flight per warp, 3 with 2 or fewer; else 1.
 inline int gemv_ctas_per_sm(int cpl, int ri) { return cpl == 1 ? (ri <= 2 ? 3 : 2) : 1; }
 
+// Tensor-pipe GEMV: K limit and the kernel shapes that exist (consumer warps
+// per CTA, CTAs per SM, steps per loop iteration), chosen by configuration id.
+constexpr int kMmaMaxK = 8192;
+struct MmaShape {
+  int nw, ctas, unroll;
+};
+MmaShape mma_shape(int cfg);   // cfg 0: the default shape
+
 GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
+// The tensor-pipe kernel's plan for the same arguments (infeasible when it does
+// not apply: 4-bit codes, fp16 x, dense, K <= 8192, every unit 16-byte aligned).
+GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
 // One launch over problems of several K (each K <= 8192, one chunk per lane):
 // fills every problem's geometry in `batch` and returns the launch plan
 // (stage size covering the largest unit); infeasible when the problems need
 // different kernel shapes.
 GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms);
+GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms);
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,
                         cudaStream_t stream, GemvBatch<kBatchCap>* batch = nullptr);
 

@@ -1,0 +1,426 @@
+// Dequant-GEMV (M = 1, decode) with the dot products on the tensor pipe
+// (mma.sync m16n8k16, fp16 in, fp32 accumulate).  BaseRT pages,
+// thetesserapress.com "BaseRT claims fastest Apple Silicon inference", section
+// "What BaseRT does differently" (a GEMV of its own for M = 1 that expands the
+// codes in its inner loop) and section "Where the wins land, and where they
+// don't" (large-model decode waits on memory bandwidth: the kernel must keep
+// up with HBM, so the contraction leaves the FMA pipe).
+//
+// What stays from the CUDA-core GEMV (qgemv_impl.cuh): persistent CTAs, one
+// producer warp filling a shared-memory ring with one bulk copy per unit of
+// rows (codes) plus 16-byte cp.async of the unit's scales and biases, batched
+// problem tables, the K split over warps of a row group with a named-barrier
+// reduction, and the fail flag that keeps every warp on its barriers after an
+// expired wait.
+//
+// What changes is the consumer.  A warp takes a tile of 16 weight rows and its
+// K slice, one quantization group (64 codes, two 16-byte chunks per row at
+// 4 bits) per step:
+//  * ldmatrix.x4 gives lane (g = lane/4, t = lane%4) word t of one chunk of
+//    rows g and g+8, for two chunks: 8 codes per word.
+//  * One AND per code pair turns a word into fp16 values q * 2^-24 (codes 0/4)
+//    and 16q * 2^-24 (codes 1/5), and with one shift codes 2/6 and 3/7: fp16
+//    subnormals whose products with fp16 x are exact in the fp32 accumulator.
+//    These are the MMA's A fragments, so no dequantized weight exists anywhere.
+//  * The MMA's B operand is x, permuted to the pair order above and with the
+//    x of the 16q codes divided by 16, written once per problem into shared
+//    memory with the group sums of x.
+//  * Lane group g works on group u ^ g of its slice at step u (u mod ks when
+//    the slice is not a multiple of 8 groups), so the eight rows one ldmatrix
+//    phase reads start in eight different 16-byte bank slots, and B column g
+//    holds exactly the x of lane group g's group: the results sit on the
+//    diagonal D[g][g], D[g+8][g], in lane (g, g/2).
+//  * Per step and row the holder lane adds s * 2^24 * D + b * sum(x) of that
+//    group in fp32; rows split over KW warps meet in shared memory.
+#pragma once
+#include "qgemv_impl.cuh"
+
+namespace bt {
+namespace gemv {
+
+constexpr int kMmaRows = 16;   // rows per tile (the MMA's M)
+
+// The MMA and the shared-memory fragment loads are plain (non-volatile) asm,
+// so the compiler may interleave two independent steps; their addresses derive
+// from values passed through launder() after the wait or barrier that makes
+// the data valid, so no load can be moved above it.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr));
+}
+__device__ __forceinline__ uint4 lds128_nv(uint32_t a) {
+  uint4 v;
+  asm("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint16_t lds16_nv(uint32_t a) {
+  uint16_t v;
+  asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds32f_nv(uint32_t a) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+// A value the compiler must treat as produced here (volatile, memory clobber).
+__device__ __forceinline__ uint32_t launder(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v) : "memory");
+  return r;
+}
+
+// Shared-memory address of the permuted x of (group v, chunk c, lane slot t):
+// 16 bytes, groups 192 bytes apart, so that lane groups on neighbouring groups
+// read different bank halves.
+constexpr int kXGroupBytes = 192;
+__device__ __forceinline__ uint32_t xslot(uint32_t xs, int v, int c, int t) {
+  return xs + (uint32_t)(v * kXGroupBytes + c * 64 + t * 16);
+}
+
+// Permuted, prescaled x of one problem (K values) and its group sums, written
+// by all consumer threads: slot (v, c, t) holds, for the 8 x values j = 0..7 at
+// k = 64v + 32c + 8t + j, the pairs (x0, x4) (x1/16, x5/16) (x2, x6) (x3/16, x7/16)
+// -- the B fragments of the two MMAs of that chunk.
+__device__ __forceinline__ void prep_x(uint32_t xs, float* xsum, const uint16_t* x, int G, int ctid, int nthreads) {
+  const int lane = ctid & 31;
+  for (int base = ctid - lane; base < G * 8; base += nthreads) {
+    const int idx = base + lane;
+    float part = 0.f;
+    if (idx < G * 8) {
+      const int v = idx >> 3, c = (idx >> 2) & 1, t = idx & 3;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + (size_t)v * 64 + c * 32 + t * 8));
+      const __half2 x01 = *reinterpret_cast<const __half2*>(&raw.x), x23 = *reinterpret_cast<const __half2*>(&raw.y);
+      const __half2 x45 = *reinterpret_cast<const __half2*>(&raw.z), x67 = *reinterpret_cast<const __half2*>(&raw.w);
+      const __half2 sixteenth = __float2half2_rn(0.0625f);
+      const __half2 p04 = __lows2half2(x01, x45), p15 = __hmul2(__highs2half2(x01, x45), sixteenth);
+      const __half2 p26 = __lows2half2(x23, x67), p37 = __hmul2(__highs2half2(x23, x67), sixteenth);
+      uint4 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&p04);
+      o.y = *reinterpret_cast<const uint32_t*>(&p15);
+      o.z = *reinterpret_cast<const uint32_t*>(&p26);
+      o.w = *reinterpret_cast<const uint32_t*>(&p37);
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(xslot(xs, v, c, t)), "r"(o.x), "r"(o.y), "r"(o.z),
+                   "r"(o.w)
+                   : "memory");
+      const float2 f01 = __half22float2(x01), f23 = __half22float2(x23), f45 = __half22float2(x45),
+                   f67 = __half22float2(x67);
+      part = ((f01.x + f01.y) + (f23.x + f23.y)) + ((f45.x + f45.y) + (f67.x + f67.y));
+    }
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    part += __shfl_xor_sync(0xffffffffu, part, 4);
+    if (idx < G * 8 && (idx & 7) == 0) xsum[idx >> 3] = part;
+  }
+}
+
+// Four fp16x2 A pairs of one word of 8 four-bit codes: (q0,q4) (q1,q5)*16
+// (q2,q6) (q3,q7)*16 as subnormals q * 2^-24.
+__device__ __forceinline__ void pairs_q4(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t w8 = w >> 8;
+  p[0] = w & 0x000F000Fu;
+  p[1] = w & 0x00F000F0u;
+  p[2] = w8 & 0x000F000Fu;
+  p[3] = w8 & 0x00F000F0u;
+}
+
+template <int NW> struct MmaWarps {
+  static constexpr int kThreads = (NW + 1) * 32;
+};
+
+template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH>
+__global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
+    qgemv_mma_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
+  static_assert(BITS == 4, "tensor-pipe GEMV: 4-bit codes");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
+  uint64_t* empty = full + S;
+  float* red = reinterpret_cast<float*>(empty + S);          // [row group][2][KW][16]: NW * 2 * 16 floats
+  float* xsum = red + NW * 2 * kMmaRows;                      // [G] group sums of x
+  uint8_t* xs_ptr = reinterpret_cast<uint8_t*>(xsum) + p.xsum_bytes;   // permuted x, 128 B per group
+  __shared__ volatile int s_fail;
+
+  long long u_begin, u_end;
+  if constexpr (BATCH) {
+    u_begin = unit_at_cost(p, batch, p.total_cost * blockIdx.x / gridDim.x);
+    u_end = unit_at_cost(p, batch, p.total_cost * (blockIdx.x + 1) / gridDim.x);
+  } else {
+    u_begin = p.num_units * blockIdx.x / gridDim.x;
+    u_end = p.num_units * (blockIdx.x + 1) / gridDim.x;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 33); mbar_init(&empty[s], NW); }
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (u_begin >= u_end) return;
+
+  if (warp == NW) {
+    // ------------------------------------------------------------ producer
+    if (!p.const_weights) pdl_wait();
+    const uint64_t pol = l2_policy_evict_first();
+    int prob, blk;
+    first_unit<BATCH>(p, batch, u_begin, prob, blk);
+    ProbView v = resolve<BATCH>(p, batch, nullptr, prob);
+    int s = 0;
+    uint32_t ph = 0;
+    long long it = 0;
+    bool ok = true;
+    for (long long u = u_begin; u < u_end; ++u, ++it) {
+      if (blk == v.units) { blk = 0; ++prob; v = resolve<BATCH>(p, batch, nullptr, prob); }
+      if (it >= S) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
+        if (!__shfl_sync(0xffffffffu, (int)w, 0)) { ok = false; s_fail = 1; break; }
+      }
+      const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
+      const int row0 = blk * RB;
+      const int rows = min(RB, v.n - row0);
+      const bool drop = p.drop_stage && blockIdx.x == 0 && it == 0;   // test hook: never fill this stage
+      if (!drop) {
+        if (unit_bulk(p, v, row0, rows)) {
+          const uint32_t cbytes = (uint32_t)rows * row_bytes, sbytes = (uint32_t)rows * G * 2;
+          uint8_t* st = smem + (size_t)s * p.stage_bytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], cbytes);
+            bulk_g2s(st, v.codes + (size_t)row0 * row_bytes, cbytes, &full[s], pol);
+          }
+          const uint8_t* gs = reinterpret_cast<const uint8_t*>(v.scales + (size_t)row0 * G);
+          const uint8_t* gb = reinterpret_cast<const uint8_t*>(v.biases + (size_t)row0 * G);
+          uint8_t* ss = st + (size_t)RB * row_bytes;
+          uint8_t* sbb = ss + (size_t)RB * G * 2;
+          for (uint32_t o = lane * 16u; o < sbytes; o += 32u * 16u) {
+            cp_async16(ss + o, gs + o);
+            cp_async16(sbb + o, gb + o);
+          }
+          cp_async_mbar_arrive_noinc(&full[s]);
+        } else {
+          // the host plans only 16-byte aligned units; anything else is refused
+          if (lane == 0) set_device_error(p.err, kErrBadArg);
+          mbar_arrive(&full[s]);
+          if (lane == 0) mbar_arrive(&full[s]);
+        }
+      }
+      ++blk;
+      if (++s == S) { s = 0; ph ^= 1u; }
+    }
+    if (!ok) {
+      cp_async_wait_all();
+      if (lane == 0) {
+        const long long issued = it;
+        for (long long j = (issued > S ? issued - S : 0); j < issued; ++j)   // failure path only
+          mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), p.timeout_ns, p.err);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, tq = lane & 3;
+  const bool holder = tq == (g >> 1);       // holds D[g][g] and D[g+8][g]
+  const int ld_row = (lane & 7) + ((lane >> 3) & 1) * 8;   // tile row whose address this lane gives ldmatrix
+  const int ld_g = lane & 7;                // lane group of that row
+  const int ld_second = lane >> 4;          // 0: the row's first chunk of a group, 1: its second
+  const uint32_t xs0 = smem_u32(xs_ptr), xsum0 = smem_u32(xsum);
+  uint32_t xs = xs0, xsa = xsum0;   // laundered after each x re-staging
+  int KW = 0, RW = 0, kw = 0, rg = 0;
+  bool dead = false;
+  int rbuf = 0;
+  int prob, blk;
+  first_unit<BATCH>(p, batch, u_begin, prob, blk);
+  ProbView v;
+  int cur_prob = -1;
+  int tcount = 0;   // tiles of the current problem this CTA has passed
+  int s = 0;
+  uint32_t ph = 0;
+  pdl_wait();   // x comes from the previous kernel
+  for (long long u = u_begin; u < u_end; ++u) {
+    if (cur_prob >= 0 && blk == v.units) { blk = 0; ++prob; }
+    if (prob != cur_prob) {
+      cur_prob = prob;
+      v = resolve<BATCH>(p, batch, nullptr, prob);
+      // every consumer has finished the previous problem's tiles: x can be replaced
+      asm volatile("bar.sync 15, %0;" ::"r"(NW * 32) : "memory");
+      if (v.kw < 1 || NW % v.kw) {   // never planned so; refuse rather than spin
+        if (threadIdx.x == 0) set_device_error(p.err, kErrBadArg);
+        return;
+      }
+      KW = v.kw;
+      RW = NW / KW;
+      kw = warp % KW;
+      rg = warp / KW;
+      rbuf = 0;
+      tcount = 0;
+      if (!dead) prep_x(xs0, xsum, v.x, v.g, threadIdx.x, NW * 32);
+      asm volatile("bar.sync 15, %0;" ::"r"(NW * 32) : "memory");
+      xs = launder(xs0);
+      xsa = launder(xsum0);
+    }
+    if (!dead && (s_fail || !mbar_wait(&full[s], ph, p.timeout_ns, p.err))) {
+      dead = true;
+      s_fail = 1;
+    }
+    const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
+    const int row0 = blk * RB;
+    const int rows = min(RB, v.n - row0);
+    const uint32_t st = launder(smem_u32(smem + (size_t)s * p.stage_bytes));   // after the wait
+    const uint32_t st_sc = st + RB * row_bytes, st_bi = st_sc + RB * G * 2;
+    const int ntiles = (rows + kMmaRows - 1) / kMmaRows;
+    // this warp's K slice: groups [gs0, gs0 + ks)
+    const int KS = (G + KW - 1) / KW;
+    const int gs0 = kw * KS;
+    const int ks = max(0, min(KS, G - gs0));
+    const size_t ybase = v.y0 + row0;
+    // tiles t of this unit with (tcount + t) % RW == rg
+    int t = (rg - tcount % RW + RW) % RW;
+    for (; t < ntiles; t += RW) {
+      const int r0 = t * kMmaRows;
+      float acc_a = 0.f, acc_b = 0.f;   // rows r0 + g, r0 + g + 8 (meaningful on holder lanes)
+      if (!dead && ks > 0) {
+        const int lr = min(r0 + ld_row, rows - 1);
+        const uint32_t ld_base = st + (uint32_t)(lr * row_bytes) + (uint32_t)(((ld_g >> 2) ^ ld_second) << 4) +
+                                 (uint32_t)(gs0 * 32);
+        const int ra = min(r0 + g, rows - 1), rb = min(r0 + g + 8, rows - 1);
+        const uint32_t pbase = (uint32_t)(gs0 * 2);
+        const uint32_t sc_a = st_sc + (uint32_t)(ra * G) * 2 + pbase, sc_b = st_sc + (uint32_t)(rb * G) * 2 + pbase;
+        const uint32_t bi_a = st_bi + (uint32_t)(ra * G) * 2 + pbase, bi_b = st_bi + (uint32_t)(rb * G) * 2 + pbase;
+        const int h = (g >> 2) & 1;       // chunk this lane group reads first
+        const uint32_t x1 = xs + (uint32_t)(gs0 * kXGroupBytes + h * 64 + tq * 16);
+        const uint32_t x2 = xs + (uint32_t)(gs0 * kXGroupBytes + (h ^ 1) * 64 + tq * 16);
+        const uint32_t xsb = xsa + (uint32_t)(gs0 * 4);
+        // One step: the slice's group vl for the ldmatrix row, vc for this lane
+        // group (the same rotation seen from the two lane mappings).
+        auto step = [&](int vl, int vc) {
+          uint32_t r[4];
+          ldmatrix_x4(ld_base + (uint32_t)(vl * 32), r);
+          const uint4 b1 = lds128_nv(x1 + (uint32_t)(vc * kXGroupBytes));
+          const uint4 b2 = lds128_nv(x2 + (uint32_t)(vc * kXGroupBytes));
+          const uint32_t po = (uint32_t)(vc * 2);
+          const uint16_t sa = lds16_nv(sc_a + po), sb = lds16_nv(sc_b + po);
+          const uint16_t ba = lds16_nv(bi_a + po), bb = lds16_nv(bi_b + po);
+          const float xsv = lds32f_nv(xsb + (uint32_t)(vc * 4));
+          uint32_t pa[4], pb[4], pc[4], pd[4];
+          pairs_q4(r[0], pa);   // row g, first chunk
+          pairs_q4(r[1], pb);   // row g + 8, first chunk
+          pairs_q4(r[2], pc);   // row g, second chunk
+          pairs_q4(r[3], pd);   // row g + 8, second chunk
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+          mma16816(d, a0, b1.x, b1.y);
+          const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+          mma16816(d, a1, b1.z, b1.w);
+          const uint32_t a2[4] = {pc[0], pd[0], pc[1], pd[1]};
+          mma16816(d, a2, b2.x, b2.y);
+          const uint32_t a3[4] = {pc[2], pd[2], pc[3], pd[3]};
+          mma16816(d, a3, b2.z, b2.w);
+          const float da = (g & 1) ? d[1] : d[0], db = (g & 1) ? d[3] : d[2];
+          acc_a = fmaf(to_f32<BT_F16>(sa) * 16777216.f, da, fmaf(to_f32<BT_F16>(ba), xsv, acc_a));
+          acc_b = fmaf(to_f32<BT_F16>(sb) * 16777216.f, db, fmaf(to_f32<BT_F16>(bb), xsv, acc_b));
+        };
+        if ((ks & 7) == 0) {
+          // step j visits group j ^ lane group: a permutation of every aligned block
+          // of 8 groups, with the eight rows of an ldmatrix phase in eight bank slots
+          if constexpr (UNROLL == 2) {
+            for (int j = 0; j < ks; j += 2) {
+              step(j ^ ld_g, j ^ g);
+              step((j + 1) ^ ld_g, (j + 1) ^ g);
+            }
+          } else {
+            for (int j = 0; j < ks; ++j) step(j ^ ld_g, j ^ g);
+          }
+        } else {
+          int vl = ld_g % ks, vc = g % ks;
+          for (int j = 0; j < ks; ++j) {
+            step(vl, vc);
+            if (++vl == ks) vl = 0;
+            if (++vc == ks) vc = 0;
+          }
+        }
+      }
+      const int ya = r0 + g, yb = r0 + g + 8;
+      if (KW == 1) {
+        if (!dead && holder) {
+          if (ya < rows) store_yv(p, v.y, ybase + ya, acc_a);
+          if (yb < rows) store_yv(p, v.y, ybase + yb, acc_b);
+        }
+      } else {
+        float* rbp = red + (size_t)((rg * 2 + rbuf) * KW) * kMmaRows;   // [KW][16]
+        if (holder) {
+          rbp[kw * kMmaRows + g] = acc_a;
+          rbp[kw * kMmaRows + g + 8] = acc_b;
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
+        if (!dead && kw == 0 && holder) {
+          float sa = 0.f, sb = 0.f;
+          for (int j = 0; j < KW; ++j) {
+            sa += rbp[j * kMmaRows + g];
+            sb += rbp[j * kMmaRows + g + 8];
+          }
+          if (ya < rows) store_yv(p, v.y, ybase + ya, sa);
+          if (yb < rows) store_yv(p, v.y, ybase + yb, sb);
+        }
+        rbuf ^= 1;
+      }
+    }
+    tcount += ntiles;
+    __syncwarp();
+    if (!dead && lane == 0) mbar_arrive(&empty[s]);
+    ++blk;
+    if (++s == S) { s = 0; ph ^= 1u; }
+  }
+}
+
+template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH>
+cudaError_t launch_mma_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int grid, size_t smem,
+                         cudaStream_t stream) {
+  auto k = qgemv_mma_kernel<BITS, NW, CTAS, UNROLL, BATCH>;
+  static std::atomic<uint64_t> smem_raised{0};
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MmaWarps<NW>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if constexpr (BATCH) {
+    return cudaLaunchKernelEx(&cfg, k, p, *batch);
+  } else {
+    GemvBatch<1> none{};
+    return cudaLaunchKernelEx(&cfg, k, p, none);
+  }
+}
+
+template <int BITS, int NW, int CTAS, int UNROLL>
+cudaError_t launch_mma_shape(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b,
+                             cudaStream_t st) {
+  if (b) return launch_mma_t<BITS, NW, CTAS, UNROLL, true>(p, b, pl.grid, pl.smem, st);
+  return launch_mma_t<BITS, NW, CTAS, UNROLL, false>(p, nullptr, pl.grid, pl.smem, st);
+}
+
+template <int BITS>
+cudaError_t launch_mma_bits(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b,
+                            cudaStream_t st) {
+  if (pl.mma_nw == 16) return launch_mma_shape<BITS, 16, 1, 1>(p, pl, b, st);
+  if (pl.mma_ctas == 2) return launch_mma_shape<BITS, 8, 2, 1>(p, pl, b, st);
+  if (pl.mma_unroll == 1) return launch_mma_shape<BITS, 8, 1, 1>(p, pl, b, st);
+  return launch_mma_shape<BITS, 8, 1, 2>(p, pl, b, st);
+}
+
+}  // namespace gemv
+}  // namespace bt

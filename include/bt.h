@@ -223,6 +223,19 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *                       over more warps (0 = heuristic, else 1..4).
  *   BT_OPT_GEMV_STAGE_KB tuning: GEMV pipeline stage size in KiB (0 = heuristic, else 4..96).
  *   BT_OPT_GEMV_RI       tuning: GEMV rows in flight per warp (0 = heuristic, else 1, 2, 4 or 8).
+ *   BT_OPT_GEMV_CUDA_CORE tuning, 1: GEMV on the CUDA-core kernel even where the
+ *                       tensor-pipe one applies (4-bit codes, fp16 x, K <= 8192).
+ *   BT_OPT_GEMV_TENSOR_PIPE tuning: 0 = the tensor-pipe GEMV for launches of at
+ *                       most one 16-row tile per SM (default), 1 = wherever it
+ *                       applies, 2 = never.
+ *   BT_OPT_GEMV_MMA_STAGE_KB tuning: tensor-pipe GEMV stage size in KiB (0 = heuristic, else 8..112).
+ *   BT_OPT_GEMV_MMA_SHAPE tuning: tensor-pipe GEMV kernel shape, 0 = default,
+ *                       1: 8 consumer warps, 1 CTA per SM, two steps per loop
+ *                       iteration; 2: the same, one step; 3: 16 consumer warps,
+ *                       1 CTA per SM; 4: 8 consumer warps, 2 CTAs per SM.
+ *   BT_OPT_GEMV_MMA_GROUPS tuning: most quantization groups of K one warp of the
+ *                       tensor-pipe GEMV takes before K is split over more warps
+ *                       (0 = heuristic).
  */
 typedef enum {
   BT_OPT_PDL = 0,
@@ -235,7 +248,12 @@ typedef enum {
   BT_OPT_GEMM_SPLITS = 7,
   BT_OPT_GEMV_MAX_CPL = 8,
   BT_OPT_GEMV_STAGE_KB = 9,
-  BT_OPT_GEMV_RI = 10
+  BT_OPT_GEMV_RI = 10,
+  BT_OPT_GEMV_CUDA_CORE = 11,
+  BT_OPT_GEMV_MMA_STAGE_KB = 12,
+  BT_OPT_GEMV_MMA_SHAPE = 13,
+  BT_OPT_GEMV_MMA_GROUPS = 14,
+  BT_OPT_GEMV_TENSOR_PIPE = 15
 } bt_option;
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);
@@ -247,14 +265,18 @@ BT_API bt_status bt_set_option(bt_option option, long long value);
  * "Metodologia": kernel choice and threadgroup sizes per chip) in inspectable
  * form, for tests and tuning.
  *   feasible      0: no GEMV kernel fits (the library runs the CUDA-core tile)
+ *   tensor_pipe   1: the tensor-pipe kernel (dot products on mma.sync), 0: the
+ *                 CUDA-core kernel
  *   kw            warps sharing one row (K split); cpl: 32-code chunks per lane
- *   ri            rows in flight per warp; rows_per_unit: rows per pipeline stage
+ *   ri            rows in flight per warp (16 on the tensor pipe: one MMA tile);
+ *                 rows_per_unit: rows per pipeline stage
  *   stage_bytes, stages, smem_bytes   shared-memory ring of one CTA
  *   ctas_per_sm   CTAs per SM the kernel is built for; grid: CTAs launched
  */
 typedef struct {
   int32_t feasible, kw, cpl, ri, rows_per_unit, stage_bytes, stages, ctas_per_sm, grid;
   int64_t num_units, smem_bytes;
+  int32_t tensor_pipe;
 } bt_gemv_plan;
 /* One problem shape repeated `problems` times (bt_qgemv: problems = 1). */
 BT_API bt_status bt_plan_gemv(int bits, bt_dtype x_dtype, int N, int K, int problems, int sms,

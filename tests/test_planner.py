@@ -26,6 +26,8 @@ def per_row(bits, k):
 
 def check_plan(p, bits, n, k, problems, sms):
     assert p["feasible"] == 1
+    if p["tensor_pipe"]:
+        return check_tensor_pipe_plan(p, bits, n, k, problems, sms)
     kw, cpl, ri, rb = p["kw"], p["cpl"], p["ri"], p["rows_per_unit"]
     assert kw in (1, 2, 4, 8) and 8 % kw == 0                      # row groups tile the 8 consumer warps
     assert 32 * kw * cpl >= k // 32                                # every 32-code chunk has a lane
@@ -41,10 +43,106 @@ def check_plan(p, bits, n, k, problems, sms):
     assert p["grid"] == min(units, sms * p["ctas_per_sm"])
 
 
+def check_tensor_pipe_plan(p, bits, n, k, problems, sms):
+    """The tensor-pipe kernel: 16-row MMA tiles, each warp's K slice at most 16
+    groups, whole tiles per unit, one CTA per SM."""
+    g = k // 64
+    kw, rb = p["kw"], p["rows_per_unit"]
+    assert bits == 4 and k <= 8192
+    assert kw in (1, 2, 4, 8) and -(-g // kw) <= 32                 # at most 32 groups per warp
+    tiles_per_sm = max(1, (-(-n * problems // sms)) // 16)
+    if kw > 1 and -(-g // (kw // 2)) <= 32:                        # split further only to give idle warps work
+        assert (kw // 2) * tiles_per_sm < 8 and kw <= g
+    assert p["ri"] == 16 and rb % 16 == 0 and rb >= 16
+    assert rb <= max(16, -(-n // 16) * 16)
+    assert p["stage_bytes"] >= rb * per_row(bits, k) and p["stage_bytes"] % 128 == 0
+    assert p["stages"] >= 2 and p["ctas_per_sm"] == 1
+    # ring + barriers + row-group partials + x sums + permuted x (192 B per group) fit one CTA
+    assert p["smem_bytes"] >= p["stages"] * p["stage_bytes"] + g * 192
+    assert p["smem_bytes"] <= KMAX_SMEM
+    units = -(-n // rb) * problems
+    assert p["num_units"] == units
+    assert p["grid"] == min(units, sms)
+    assert (n * g * 2) % 16 == 0 and (n * k // 2) % 16 == 0         # every unit moves in 16-byte pieces
+
+
+@pytest.fixture()
+def tensor_pipe(bt):
+    """Plans with the tensor-pipe GEMV taken wherever it applies (not only for small launches)."""
+    bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 1)
+    yield
+    bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 0)
+
+
+@pytest.fixture()
+def cuda_core(bt):
+    """Plans of the CUDA-core GEMV kernel (the tensor-pipe one switched off)."""
+    bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 1)
+    yield
+    bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 0)
+
+
+@pytest.mark.parametrize("k", (64, 128, 576, 1024, 2048, 3072, 4096, 8192))
+@pytest.mark.parametrize("n", (16, 64, 333, 1024, 151936))
+def test_tensor_pipe_plan_invariants(bt, tensor_pipe, k, n):
+    p = bt.bt_plan_gemv(4, n, k)
+    g = k // 64
+    if (n * g * 2) % 16 or (n * k // 2) % 16:
+        assert p["tensor_pipe"] == 0                                # a ragged unit could not move by bulk copy
+    else:
+        assert p["tensor_pipe"] == 1
+    check_plan(p, 4, n, k, 1, 148)
+
+
+def test_tensor_pipe_applies_to_4_bit_fp16_dense_only(bt, tensor_pipe):
+    import torch
+    assert bt.bt_plan_gemv(4, 4096, 1024)["tensor_pipe"] == 1
+    assert bt.bt_plan_gemv(4, 4096, 16384)["tensor_pipe"] == 0       # K above 8192
+    assert bt.bt_plan_gemv(4, 4096, 1024, x_dtype=torch.bfloat16)["tensor_pipe"] == 0
+    for bits in (2, 3, 6, 8):
+        assert bt.bt_plan_gemv(bits, 4096, 1024)["tensor_pipe"] == 0
+    p = bt.bt_plan_gemv(4, 151936, 1024)
+    assert p["kw"] == 1 and p["grid"] == 148
+    assert {k: bt.bt_plan_gemv(4, 65536, k)["kw"] for k in (1024, 2048, 3072, 4096, 8192)} == \
+        {1024: 1, 2048: 1, 3072: 2, 4096: 2, 8192: 4}
+    p = bt.bt_plan_gemv(4, 2048, 1024)                              # the single N=2048 GEMV: one tile per CTA
+    assert p["kw"] == 8 and p["rows_per_unit"] == 16 and p["grid"] == 128
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 1)
+        assert bt.bt_plan_gemv(4, 4096, 1024)["tensor_pipe"] == 0
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 0)
+
+
+def test_tensor_pipe_by_default_only_for_small_launches(bt):
+    """Default rule: the tensor-pipe GEMV for launches of at most one 16-row tile
+    per SM (the single N=2048 GEMV), the CUDA-core kernel for larger ones."""
+    assert bt.bt_plan_gemv(4, 2048, 1024)["tensor_pipe"] == 1
+    assert bt.bt_plan_gemv(4, 148 * 16, 1024)["tensor_pipe"] == 1
+    assert bt.bt_plan_gemv(4, 148 * 16 + 16, 1024)["tensor_pipe"] == 0
+    assert bt.bt_plan_gemv(4, 151936, 1024)["tensor_pipe"] == 0
+    p, _ = bt.bt_plan_gemv_batch(4, QWEN06_LAYER * 28 + [(151936, 1024)])
+    assert p["tensor_pipe"] == 0
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 2)
+        assert bt.bt_plan_gemv(4, 2048, 1024)["tensor_pipe"] == 0
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 0)
+
+
 @pytest.mark.parametrize("bits", (2, 3, 4, 6, 8))
 @pytest.mark.parametrize("k", (64, 128, 576, 1024, 2048, 3072, 4096, 8192, 16384))
 @pytest.mark.parametrize("n", (1, 7, 333, 1024, 151936))
 def test_single_plan_invariants(bt, bits, k, n):
+    for cc in (0, 1):
+        bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, cc)
+        try:
+            single_plan_invariants(bt, bits, k, n)
+        finally:
+            bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 0)
+
+
+def single_plan_invariants(bt, bits, k, n):
     for xdt, name in ((None, "f16"), ("bf16", "bf16")):
         import torch
         dt = torch.float16 if xdt is None else torch.bfloat16
@@ -54,7 +152,7 @@ def test_single_plan_invariants(bt, bits, k, n):
         check_plan(p, bits, n, k, 1, 148)
 
 
-def test_one_chunk_per_lane_up_to_8192(bt):
+def test_one_chunk_per_lane_up_to_8192(bt, cuda_core):
     for k in (1024, 2048, 3072, 8192):
         p = bt.bt_plan_gemv(4, 151936, k)
         assert p["cpl"] == 1 and p["ctas_per_sm"] == 2
@@ -77,13 +175,13 @@ def test_k_limits_per_bit_width(bt):
         assert p["feasible"] == 0
 
 
-def test_rows_in_flight_shrink_for_small_problems(bt):
+def test_rows_in_flight_shrink_for_small_problems(bt, cuda_core):
     assert bt.bt_plan_gemv(4, 151936, 1024)["ri"] == 8
     p = bt.bt_plan_gemv(4, 4096, 1024)                             # 28 rows per SM: 2 rows in flight
     assert p["ri"] == 2 and p["ctas_per_sm"] == 3
 
 
-def test_tuning_options_steer_the_plan(bt):
+def test_tuning_options_steer_the_plan(bt, cuda_core):
     try:
         bt.bt_set_option(bt.BT_OPT_GEMV_MAX_CPL, 4)
         assert bt.bt_plan_gemv(4, 4096, 2048)["cpl"] == 2
@@ -125,6 +223,24 @@ def unit_partition(geoms, grid):
         load.append(sum(costs[u0:u1]))
     assert covered == len(starts)                                     # every unit has a CTA
     return load, total
+
+
+def test_decode_pass_batch_plan_on_the_tensor_pipe(bt, tensor_pipe):
+    """The Qwen3-0.6B-shaped pass as one tensor-pipe launch: K split 1/1/2 for
+    K = 1024/2048/3072, whole 16-row tiles per unit, and the work-balanced split
+    of units over one CTA per SM."""
+    shapes = QWEN06_LAYER * 28 + [(151936, 1024)]
+    p, geo = bt.bt_plan_gemv_batch(4, shapes)
+    assert p["feasible"] == 1 and p["tensor_pipe"] == 1 and p["ctas_per_sm"] == 1 and p["ri"] == 16
+    for (n, k), (kw, rb) in zip(shapes, geo):
+        assert kw == {1024: 1, 2048: 1, 3072: 2}[k]
+        assert rb % 16 == 0 and rb * per_row(4, k) <= p["stage_bytes"]
+    assert p["stages"] >= 2 and p["smem_bytes"] <= KMAX_SMEM
+    assert p["smem_bytes"] >= p["stages"] * p["stage_bytes"] + 48 * 192   # x of the largest K (48 groups)
+    assert p["num_units"] == sum(-(-n // rb) for (n, _), (_, rb) in zip(shapes, geo))
+    assert p["grid"] == 148
+    load, total = unit_partition([(n, kw, rb) for (n, _), (kw, rb) in zip(shapes, geo)], p["grid"])
+    assert max(load) <= 1.1 * total / p["grid"]
 
 
 def test_decode_pass_batch_plan_and_work_split(bt):

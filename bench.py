@@ -118,16 +118,19 @@ def source_digest(patterns):
 
 
 def profile_traffic(summary_file, digest):
-    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on this kernel source."""
+    """Per-launch DRAM bytes from a committed ncu summary (profiles/<name>.json:
+    {"kernel_source_digest": ..., "traffic_bytes_per_launch": ...}), if it was
+    taken on this kernel source."""
     path = os.path.join(ROOT, "profiles", summary_file)
     if not os.path.exists(path):
         return None
-    txt = open(path).read()
-    m_d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", txt)
-    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m_d or not m_t or m_d.group(1) != digest:
+    try:
+        d = json.load(open(path))
+        if d.get("kernel_source_digest") != digest:
+            return None
+        return float(d["traffic_bytes_per_launch"])
+    except (ValueError, KeyError, TypeError):
         return None
-    return float(m_t.group(1))
 
 
 class ClockSampler:
@@ -194,32 +197,88 @@ def blas_threads():
         return 1
 
 
-# ------------------------------------------------------------------ oracle leg
-def oracle_rate(weights, xs16, budget_s: float, start: int = 0):
-    """fp64 oracle on whole projections, in pass order from `start`, for about `budget_s`.
+def host_cores():
+    """os.cpu_count() and the cores this process may run on."""
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except AttributeError:
+        aff = os.cpu_count() or 1
+    return os.cpu_count() or 1, aff
 
-    Returns (GB/s of weight bytes, bytes processed, projections done).
-    """
+
+# ------------------------------------------------------------------ oracle leg
+LM_HEAD_SLICE = 8192   # rows of the lm_head a worker computes per visit (bounded memory per worker)
+
+
+def _oracle_worker(tag, shapes, indices, budget_s, warmup_s, ready, start, results):
+    """One host core: its share of the pass's projections (generated here, untimed),
+    `warmup_s` of untimed oracle work, then the fp64 oracle over them in pass
+    order until the budget is spent."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
     import oracle.bt_oracle as O
-    t0 = time.perf_counter()
-    done_bytes = 0
-    count = 0
-    i = start
-    while True:
-        qw = weights[i % len(weights)]
-        x = O.decode_f16(xs16[i % len(weights)][0])
-        rows = None
-        if qw.n > 16384:   # huge projections: a bounded slice of rows
-            rows = np.arange(0, 16384)
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(1)
+    except Exception:
+        pass
+    work = []
+    for i in indices:
+        name, n, k = shapes[i]
+        qw = synth.make_qweight(synth.rng_for(tag, name, "w"), n, k, 4)
+        x = O.decode_f16(synth.draw_activations(synth.rng_for(tag, name, "x"), 1, k, "f16")[0])
+        work.append((qw, x))
+    def one(j):
+        qw, x = work[j % len(work)]
+        rows = np.arange(0, min(qw.n, LM_HEAD_SLICE)) if qw.n > LM_HEAD_SLICE else None
         O.qgemv(qw.codes, qw.scales, qw.biases, qw.bits, x, rows=rows)
-        n_rows = qw.n if rows is None else len(rows)
-        done_bytes += weight_bytes(n_rows, qw.k, qw.bits)
+        return weight_bytes(qw.n if rows is None else len(rows), qw.k, qw.bits)
+
+    tw = time.perf_counter()
+    j = 0
+    while work and time.perf_counter() - tw < warmup_s:
+        one(j)
+        j += 1
+    ready.put(1)
+    start.wait()
+    t0 = time.perf_counter()
+    done, count = 0, 0
+    while work:
+        done += one(j)
         count += 1
-        i += 1
+        j += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    el = time.perf_counter() - t0
-    return done_bytes / el / 1e9, done_bytes, count
+    results.put((done, count, time.perf_counter() - t0))
+
+
+def oracle_rate(tag, shapes, budget_s: float, procs: int = 0, warmup_s: float = 0.0):
+    """The fp64 oracle on the host's cores: `procs` spawned workers (default: every
+    core in this process's affinity set), each running its share of the pass's
+    projections for about `budget_s`.  Returns (GB/s of weight bytes, bytes,
+    projections, workers).  Workers are spawned (not forked), so this may run
+    after CUDA is initialised."""
+    import multiprocessing as mp
+    procs = min(procs or min(host_cores()[1], 64), len(shapes))
+    ctx = mp.get_context("spawn")
+    ready, results, start = ctx.Queue(), ctx.Queue(), ctx.Event()
+    order = list(range(len(shapes)))
+    ps = [ctx.Process(target=_oracle_worker,
+                      args=(tag, shapes, order[w::procs], budget_s, warmup_s, ready, start, results))
+          for w in range(procs)]
+    for p in ps:
+        p.start()
+    for _ in ps:
+        ready.get()
+    t0 = time.perf_counter()
+    start.set()
+    got = [results.get() for _ in ps]
+    wall = time.perf_counter() - t0
+    for p in ps:
+        p.join()
+    done = sum(g[0] for g in got)
+    count = sum(g[1] for g in got)
+    return done / wall / 1e9, done, count, procs
 
 
 # ------------------------------------------------------------------ GPU legs
@@ -384,6 +443,42 @@ def run_prefill(torch, bt, dev, stream, steps, warmup, gpu_index, peaks):
     return out
 
 
+def run_c1(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
+    """The single Q4 GEMV (N=2048, K=1024, fp16 x, fp32 y; 1,179,648 weight bytes),
+    timed twice: as-is (the same weights every launch, so they stay in the 126 MB
+    L2 and the launch is latency-bound), and rotating over enough distinct
+    device copies of the weights to exceed 2x L2, so each launch reads HBM.
+    Each is a CUDA graph of back-to-back bt_qgemv launches with PDL."""
+    n, k, bits = 2048, 1024, 4
+    per = weight_bytes(n, k, bits)
+    qw = synth.make_qweight(synth.rng_for("c1", "w"), n, k, bits)
+    x16 = synth.draw_activations(synth.rng_for("c1", "x"), 1, k, "f16")
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    copies = -(-2 * l2 // per) + 8
+    base = to_dev_w(torch, qw, dev)
+    ws = [tuple(t.clone() for t in base) for _ in range(copies)]
+    x = torch.from_numpy(x16[0].view(np.int16)).to(dev).view(torch.float16)
+    y = torch.empty(n, dtype=torch.float32, device=dev)
+    bt.bt_set_option(bt.BT_OPT_PDL, 1)
+    bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
+    out = {"workload": "single Q4 GEMV N=2048 K=1024 g64, fp16 x, fp32 y", "bytes_per_gemv": per,
+           "rotated_copies": copies, "rotated_bytes": copies * per, "l2_bytes": l2}
+    for tag, seq in (("as_is", [base] * copies), ("rotated", ws)):
+        g = capture(torch, lambda seq=seq: [bt.bt_qgemv(c, s, b, bits, x, y) for c, s, b in seq], stream)
+        n_steps = max(3, min(steps, 50))
+        with torch.cuda.stream(stream):
+            t, clk = timed(torch, None, stream, lambda: g.replay(), n_steps, max(3, min(warmup, 5)), gpu_index)
+        launches = n_steps * len(seq)
+        gbs = per * launches / t / 1e9
+        out[tag] = {"us_per_gemv": round(t / launches * 1e6, 3), "gbs": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / hbm, 4), "launches_per_graph": len(seq), "clocks": clk}
+        del g
+    del ws
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error in the single-GEMV leg")
+    return out
+
+
 def run_sweep(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     """Llama-3.2-1B-shaped decode pass (16 layers x 7 projections, fp16 x, fp32 y) at
     Q2/Q3/Q4/Q6/Q8: one mixed-K bt_qgemv_batched launch per pass (K = 2048 and 8192),
@@ -512,8 +607,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--legs", default="decode,sweep,prefill,moe",
-                    help="comma list of legs to run: decode (headline), sweep (bit widths), prefill, moe")
+    ap.add_argument("--legs", default="decode,c1,sweep,prefill,moe",
+                    help="comma list of legs to run: decode (headline), c1 (single GEMV), sweep (bit widths), "
+                         "prefill, moe")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the side measurement of the pass as 197 single-GEMV launches")
     ap.add_argument("--eager", action="store_true",
@@ -544,30 +640,22 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        weights = gen_weights("decode-pass", shapes, bits)
-        xs16 = gen_x("decode-pass", shapes, 1, "f16")
-        # each step: the oracle on a bounded sample so the whole run stays within ~2 minutes
+        # the oracle on every host core; the run is K bounded samples back to back
+        # (each ~per_step seconds of work per core) after W untimed ones
         per_step = max(0.005, min(2.0, 90.0 / (args.steps + args.warmup)))
-        for i in range(args.warmup):
-            oracle_rate(weights, xs16, per_step, start=i)
-        t0 = time.perf_counter()
-        tot = 0
-        done = 0
-        for i in range(args.steps):
-            _, b, c = oracle_rate(weights, xs16, per_step, start=args.warmup + i)
-            tot += b
-            done += c
-        el = time.perf_counter() - t0
-        val = tot / el / 1e9
-        threads = blas_threads()
-        sample = f"{done} projections (slices of 16384 rows for lm_head) over {args.steps} steps of ~{per_step:.3f} s"
+        val, tot, done, procs = oracle_rate("decode-pass", shapes, per_step * args.steps,
+                                            warmup_s=per_step * args.warmup)
+        el = tot / (val * 1e9)
+        ncpu, naff = host_cores()
+        sample = (f"{done} projections of the pass on {procs} spawned workers, one BLAS thread each "
+                  f"(lm_head sliced to {LM_HEAD_SLICE} rows); {args.steps} steps of ~{per_step:.3f} s")
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config,
-            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": procs, "kind": "oracle",
+                             "sample": sample, "host_cpu_count": ncpu, "affinity_cores": naff, "blas_threads": 1},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return 0
@@ -587,6 +675,8 @@ def main():
         stream = torch.cuda.Stream(device=dev)
         peaks, _ = measured_peaks()
         out = {"metric": METRIC, "value": None, "unit": "GB/s", "legs": sorted(legs)}
+        if "c1" in legs:
+            out["c1"] = run_c1(torch, bt, dev, stream, args.steps, args.warmup, local_rank, float(peaks["hbm_gbs"]))
         if "sweep" in legs:
             out["sweep"] = run_sweep(torch, bt, dev, stream, args.steps, args.warmup, local_rank,
                                      float(peaks["hbm_gbs"]))
@@ -598,15 +688,19 @@ def main():
             print(json.dumps(out))
         return 0
 
-    # CPU baseline first (rank 0, single GPU only), before any GPU work
+    # CPU baseline first (rank 0, single GPU only), before any GPU work: the
+    # oracle on every host core (spawned workers, one BLAS thread each)
     cpu_baseline = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        rate, nbytes, cnt, procs = oracle_rate("decode-pass", shapes, args.cpu_budget)
+        ncpu, naff = host_cores()
+        cpu_baseline = {"value": round(rate, 4), "unit": "GB/s", "cores": procs, "kind": "oracle",
+                        "host_cpu_count": ncpu, "affinity_cores": naff, "blas_threads": 1,
+                        "sample": f"{cnt} projections of the pass ({nbytes/1e6:.1f} MB of packed weights, lm_head "
+                                  f"sliced to {LM_HEAD_SLICE} rows), fp64 numpy, {procs} spawned workers, "
+                                  f"~{args.cpu_budget:.0f} s"}
     weights = gen_weights("decode-pass", shapes, bits)
     xs16 = gen_x("decode-pass", shapes, 1, "f16")
-    if rank == 0 and world == 1 and args.cpu_budget > 0:
-        rate, nbytes, cnt = oracle_rate(weights, xs16, args.cpu_budget)
-        cpu_baseline = {"value": round(rate, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-                        "sample": f"{cnt} projections of the pass in order ({nbytes/1e6:.1f} MB of packed weights, "
-                                  f"lm_head sliced to 16384 rows), fp64 numpy, ~{args.cpu_budget:.0f} s"}
 
     bufs = build_decode_pass(torch, bt, weights, xs16, dev)
     del weights
@@ -693,7 +787,7 @@ def main():
     launches = len(groups)
     achieved = (pass_bytes / launches) / (sec_per_step / launches) / 1e9
     digest = source_digest(["dequant_gemv_gemm_bt_b300/csrc/qgemv*", "dequant_gemv_gemm_bt_b300/csrc/bt_common.cuh"])
-    traffic = profile_traffic("qgemv_decode_pass.md", digest)
+    traffic = profile_traffic("qgemv_decode_pass.json", digest)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -717,6 +811,8 @@ def main():
         "lm_head_gemv": {"gbs": round(lm_gbs, 1), "frac_of_hbm": round(lm_gbs / hbm, 4),
                          "shape": "N=151936 K=1024 Q4", "bytes": lm_bytes},
     }
+    if "c1" in legs:
+        out["c1"] = run_c1(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
     if "sweep" in legs:
         out["sweep"] = run_sweep(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
     if "prefill" in legs:

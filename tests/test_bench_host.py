@@ -28,13 +28,26 @@ def test_digest_ignores_comments_and_blank_lines(tmp_path, monkeypatch):
 
 def test_traffic_only_for_the_captured_code(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    write(os.path.join(tmp_path, "profiles", "p.md"),
-          "# capture\n\ntraffic_bytes_per_launch: 3.3879e8\nkernel_source_digest: 0123abcd\n")
-    assert bench.profile_traffic("p.md", "0123abcd") == 3.3879e8
-    assert bench.profile_traffic("p.md", "ffffffff") is None
-    assert bench.profile_traffic("missing.md", "0123abcd") is None
-    write(os.path.join(tmp_path, "profiles", "q.md"), "traffic_bytes_per_launch: 1e6\n")   # no digest: unusable
-    assert bench.profile_traffic("q.md", "0123abcd") is None
+    write(os.path.join(tmp_path, "profiles", "p.json"),
+          '{"traffic_bytes_per_launch": 3.3879e8, "kernel_source_digest": "0123abcd"}')
+    assert bench.profile_traffic("p.json", "0123abcd") == 3.3879e8
+    assert bench.profile_traffic("p.json", "ffffffff") is None
+    assert bench.profile_traffic("missing.json", "0123abcd") is None
+    write(os.path.join(tmp_path, "profiles", "q.json"), '{"traffic_bytes_per_launch": 1e6}')   # no digest
+    assert bench.profile_traffic("q.json", "0123abcd") is None
+    write(os.path.join(tmp_path, "profiles", "r.json"), "not json")
+    assert bench.profile_traffic("r.json", "0123abcd") is None
+
+
+def test_oracle_baseline_runs_on_spawned_workers():
+    """The CPU baseline spreads the pass's projections over spawned workers (one
+    per core asked for) and counts the bytes every worker processed."""
+    shapes = [("a", 64, 128), ("b", 32, 256), ("c", 16, 64)]
+    rate, nbytes, count, procs = bench.oracle_rate("bench-host-test", shapes, 0.3, procs=2)
+    assert procs == 2 and count >= 2 and nbytes > 0 and rate > 0
+    assert bench.oracle_rate("bench-host-test", shapes[:1], 0.1, procs=4)[3] == 1   # never more workers than projections
+    ncpu, naff = bench.host_cores()
+    assert 1 <= naff <= ncpu
 
 
 def test_peaks_fall_back_only_without_the_measured_file(tmp_path, monkeypatch):

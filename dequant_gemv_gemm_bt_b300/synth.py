@@ -6,8 +6,9 @@ the packed layout.  It holds none of the product arithmetic (no unpacking, no
 dequantization, no dot products).
 
 Layout (affine group quantization, 2 to 8 bits, BaseRT pages: thakicloud.com
-"BaseRT는 무엇인가"; group size 64 along K, fp16 scale and bias, Q4 codes 8 per
-uint32):
+"BaseRT는 무엇인가"; group size 64 along K -- 32 and 128 also supported -- fp16
+scale and bias, Q4 codes 8 per uint32; and plain fp16 weights as "bits = 16",
+the top of the pages' Q2..FP16 range):
 
 * ``W`` is ``[N, K]`` with K contiguous (``nn.Linear`` convention).  Groups are
   ``g`` consecutive elements along K; ``G = K / g`` groups per row.
@@ -37,8 +38,10 @@ from dataclasses import dataclass
 
 import numpy as np
 
-SUPPORTED_BITS = (2, 3, 4, 6, 8)
+SUPPORTED_BITS = (2, 3, 4, 5, 6, 8)
+FP16_BITS = 16            # "bits = 16": plain fp16 weights, no codes, scales or biases
 GROUP_SIZE = 64
+GROUP_SIZES = (32, 64, 128)
 
 
 def seed_for(*parts) -> int:
@@ -145,7 +148,17 @@ class QuantWeight:
 
 def make_qweight(r: np.random.Generator, n: int, k: int, bits: int,
                  group_size: int = GROUP_SIZE, sigma: float = 0.02) -> QuantWeight:
+    """Seeded weights in the packed layout.  ``bits = 16`` gives fp16 weights:
+    weight k of a row is the fp16 bit pattern in bits [16*(k%2), +16) of word
+    k/2 (the same LSB-first stream with 16-bit "codes"); the scales and biases
+    are zero arrays of the usual shape, never read."""
     w = draw_weights(r, n, k, sigma)
+    if bits == FP16_BITS:
+        if k % group_size:
+            raise ValueError("K must be a multiple of the group size")
+        codes = np.ascontiguousarray(f32_to_f16_bits(w)).view("<u4").reshape(n, k // 2).astype(np.uint32)
+        zeros = np.zeros((n, k // group_size), dtype=np.uint16)
+        return QuantWeight(codes, zeros, zeros.copy(), bits, n, k, group_size)
     q, s, b = quantize(w, bits, group_size)
     return QuantWeight(pack_codes(q, bits, group_size), s, b, bits, n, k, group_size)
 

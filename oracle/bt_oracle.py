@@ -10,7 +10,9 @@ the BaseRT pages:
 
 * affine codes of 2 to 8 bits (thakicloud.com, "Apple Silicon 로컬 LLM 추론의
   새 기준 BaseRT", section "BaseRT는 무엇인가"): a weight is ``s*q + b`` with an
-  unsigned code ``q`` and a per-group fp16 scale ``s`` and bias ``b``;
+  unsigned code ``q`` and a per-group fp16 scale ``s`` and bias ``b``, groups of
+  32, 64 or 128 along K; and plain fp16 weights (``bits = 16``), the top of the
+  Q2..FP16 range (gist.science summary, "Metodologia");
 * a GEMV for decode (M = 1) and a GEMM for prefill (M > 1), each expanding the
   codes in its inner loop (thetesserapress.com, "BaseRT claims fastest Apple
   Silicon inference", section "What BaseRT does differently"): both reduce to
@@ -88,10 +90,19 @@ def dequantize(q: np.ndarray, scales: np.ndarray, biases: np.ndarray,
 
 def dequant_weight(codes, scales, biases, bits: int, k: int, group_size: int = 64,
                    rows=None) -> np.ndarray:
-    """Dequantized fp64 ``[N, K]`` (or the selected ``rows``)."""
+    """Dequantized fp64 ``[N, K]`` (or the selected ``rows``).
+
+    ``bits = 16`` is the fp16-weight format (the "FP16" end of the pages'
+    Q2..FP16 range, gist.science summary, "Metodologia"): the 16-bit "codes"
+    are the weights' fp16 bit patterns and scales/biases are not used.
+    """
     if rows is not None:
         rows = np.asarray(rows)
-        codes, scales, biases = codes[rows], scales[rows], biases[rows]
+        codes = codes[rows]
+        if bits != 16:
+            scales, biases = scales[rows], biases[rows]
+    if bits == 16:
+        return decode_f16(unpack_codes(codes, 16, k, group_size).astype(np.uint16))
     return dequantize(unpack_codes(codes, bits, k, group_size), scales, biases, group_size)
 
 

@@ -28,14 +28,16 @@ def load_layout_fixtures():
             continue
         key, _, rest = line.partition(" ")
         if key == "fixture":
-            cur = {"name": rest}
+            cur = {"name": rest, "group": 64}
+        elif key == "group":
+            cur["group"] = int(rest)
         elif key == "bits":
             cur["bits"] = int(rest)
         elif key == "codes":
             kind, _, spec = rest.partition(" ")
-            q = np.zeros(64, dtype=np.int64)
+            q = np.zeros(cur["group"], dtype=np.int64)
             if kind == "ramp":
-                q = np.arange(64) % int(spec)
+                q = np.arange(cur["group"]) % int(spec)
             else:
                 for item in spec.split():
                     j, v = item.split(":")
@@ -88,12 +90,49 @@ def frac_bf16(u16) -> Fraction:
 # --------------------------------------------------------------- layout pins
 @pytest.mark.parametrize("fx", load_layout_fixtures(), ids=lambda f: f["name"])
 def test_layout_fixture(fx):
-    bits, q, words = fx["bits"], fx["codes"], fx["words"]
-    assert words.size == 2 * bits
-    packed = synth.pack_codes(q[None, :], bits)
+    bits, q, words, g = fx["bits"], fx["codes"], fx["words"], fx["group"]
+    assert words.size == g * bits // 32
+    packed = synth.pack_codes(q[None, :], bits, g)
     np.testing.assert_array_equal(packed[0], words)
-    np.testing.assert_array_equal(O.unpack_codes(words[None, :], bits, 64)[0], q)
-    assert brute_force_unpack(words, bits, 64) == list(q)
+    np.testing.assert_array_equal(O.unpack_codes(words[None, :], bits, g, g)[0], q)
+    assert brute_force_unpack(words, bits, g) == list(q)
+
+
+@pytest.mark.parametrize("bits", (2, 3, 4, 5, 6, 8))
+@pytest.mark.parametrize("g", (32, 128))
+def test_brute_force_exact_other_group_sizes(bits, g):
+    """Exact rational y = sum_k (s q + b) x at group sizes 32 and 128 (and 5-bit codes):
+    each code read bit by bit, its group's fp16 scale and bias decoded field by field."""
+    r = synth.rng_for("pins", "brute-g", bits, g)
+    n, k = 3, 2 * g
+    qw = synth.make_qweight(r, n, k, bits, group_size=g)
+    x16 = synth.draw_activations(r, 1, k, "f16")[0]
+    y, a = O.qgemv(qw.codes, qw.scales, qw.biases, bits, O.decode_f16(x16), group_size=g)
+    for row in range(n):
+        q = brute_force_unpack(qw.codes[row], bits, k)
+        assert max(q) < 2 ** bits
+        exact = sum((frac_f16(qw.scales[row, j // g]) * q[j] + frac_f16(qw.biases[row, j // g])) * frac_f16(x16[j])
+                    for j in range(k))
+        assert abs(y[row] - float(exact)) <= 1e-12 * max(1.0, a[row])
+
+
+def test_fp16_weights_hand_example():
+    """bits = 16: the codes are fp16 weights, two per word, low half first; no scale or bias."""
+    words = np.array([[0x40003C00, 0x3800C000]], dtype=np.uint32)    # weights 1.0, 2.0, -2.0, 0.5
+    x = np.array([1.0, 0.5, 0.25, -4.0])
+    y, a = O.qgemv(words, None, None, 16, x, group_size=4)
+    assert y[0] == 1.0 + 1.0 - 0.5 - 2.0 and a[0] == 1.0 + 1.0 + 0.5 + 2.0
+
+
+def test_fp16_weights_brute_force():
+    r = synth.rng_for("pins", "fp16-w")
+    qw = synth.make_qweight(r, 4, 128, 16)
+    x16 = synth.draw_activations(r, 1, 128, "f16")[0]
+    y, _ = O.qgemv(qw.codes, qw.scales, qw.biases, 16, O.decode_f16(x16))
+    halves = qw.codes.astype("<u4").view(np.uint16).reshape(4, 128)
+    for row in range(4):
+        exact = sum(frac_f16(halves[row, j]) * frac_f16(x16[j]) for j in range(128))
+        assert abs(y[row] - float(exact)) <= 1e-12
 
 
 @pytest.mark.parametrize("bits", BITS)

@@ -126,7 +126,9 @@ def _dt(t: torch.Tensor) -> int:
 
 
 def _weights(codes, scales, biases):
-    return _dev(codes, "codes"), _dev(scales, "scales"), _dev(biases, "biases")
+    """Device pointers of a packed weight (fp16 weights may pass None for scales and biases)."""
+    return (_dev(codes, "codes"), None if scales is None else _dev(scales, "scales"),
+            None if biases is None else _dev(biases, "biases"))
 
 
 # The C entry points take plain pointers and sizes, so they cannot see a buffer
@@ -138,14 +140,21 @@ def _need(cond: bool, msg: str) -> None:
 
 
 def check_weight(codes, scales, biases, bits: int, k: int, group_size: int = 64, experts: bool = False) -> int:
-    """Packed weight [N, K*bits/32] words + [N, K/g] fp16 params ([E, ...] when ``experts``); returns N."""
+    """Packed weight [N, K*bits/32] words + [N, K/g] fp16 params ([E, ...] when ``experts``); returns N.
+
+    ``bits = 16`` is the fp16-weight format: the words hold the weights' fp16 bit
+    patterns, and scales/biases are not read (they may be None).
+    """
     nd = 3 if experts else 2
-    for t, nm in ((codes, "codes"), (scales, "scales"), (biases, "biases")):
-        _need(isinstance(t, torch.Tensor) and t.dim() == nd, f"{nm} must be a {nd}-D tensor")
+    _need(isinstance(codes, torch.Tensor) and codes.dim() == nd, f"codes must be a {nd}-D tensor")
     _need(codes.element_size() == 4 and not codes.is_floating_point(), "codes must be int32/uint32 words")
-    _need(scales.element_size() == 2 and biases.element_size() == 2, "scales and biases must be 16-bit (fp16)")
     _need(codes.shape[-1] * 32 == k * bits,
           f"codes hold {codes.shape[-1] * 32 // max(bits, 1)} {bits}-bit codes per row, K is {k}")
+    if bits == 16 and scales is None and biases is None:
+        return codes.shape[-2]
+    for t, nm in ((scales, "scales"), (biases, "biases")):
+        _need(isinstance(t, torch.Tensor) and t.dim() == nd, f"{nm} must be a {nd}-D tensor")
+    _need(scales.element_size() == 2 and biases.element_size() == 2, "scales and biases must be 16-bit (fp16)")
     g = k // group_size if group_size > 0 else -1
     want = tuple(codes.shape[:-1]) + (g,)
     _need(tuple(scales.shape) == want and tuple(biases.shape) == want,
@@ -216,8 +225,8 @@ def bt_qgemv_batched(problems, bits: int, *, group_size: int = 64, stream=None):
         ks.add(k)
     arr = (GemvProblem * len(problems))()
     for i, (c, s, b, x, y) in enumerate(problems):
-        arr[i] = GemvProblem(_dev(c, "codes"), _dev(s, "scales"), _dev(b, "biases"), _dev(x, "x"), _dev(y, "y"),
-                             c.shape[0], x.shape[-1])
+        cw, sw, bw = _weights(c, s, b)
+        arr[i] = GemvProblem(cw, sw, bw, _dev(x, "x"), _dev(y, "y"), c.shape[0], x.shape[-1])
     k_all = ks.pop() if len(ks) == 1 else 0
     _check(lib.bt_qgemv_batched(arr, len(problems), bits, group_size, k_all, _dt(problems[0][3]),
                                 _dt(problems[0][4]), _stream(stream)), "bt_qgemv_batched")

@@ -59,18 +59,22 @@ int sm_count() {
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 6 || b == 8; }
+// 2..8-bit affine codes, and 16 = fp16 weights (no scale or bias)
+bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8 || b == 16; }
+bool group_ok(int g) { return g == 32 || g == 64 || g == 128; }
+int group_shift(int g) { return g == 32 ? 0 : (g == 64 ? 1 : 2); }
 bool half_dtype(bt_dtype d) { return d == BT_F16 || d == BT_BF16; }
 bool out_dtype(bt_dtype d) { return d == BT_F16 || d == BT_BF16 || d == BT_F32; }
 
 bt_status check_weights(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
                         int group_size, int N, int K) {
-  if (!codes || !scales || !biases) return BT_ERR_INVALID_ARG;
+  const bool params = bits != 16;   // fp16 weights carry no scale or bias (they may be NULL)
+  if (!codes || (params && (!scales || !biases))) return BT_ERR_INVALID_ARG;
   if (N <= 0 || K <= 0) return BT_ERR_INVALID_ARG;
-  if (!bits_ok(bits) || group_size != kGroup) return BT_ERR_UNSUPPORTED;
+  if (!bits_ok(bits) || !group_ok(group_size)) return BT_ERR_UNSUPPORTED;
   if (K % group_size) return BT_ERR_INVALID_ARG;
   if (K > kMaxK) return BT_ERR_UNSUPPORTED;
-  if (!aligned16(codes) || !aligned16(scales) || !aligned16(biases)) return BT_ERR_MISALIGNED;
+  if (!aligned16(codes) || (params && (!aligned16(scales) || !aligned16(biases)))) return BT_ERR_MISALIGNED;
   return BT_OK;
 }
 
@@ -85,27 +89,26 @@ bt_status cuda_status(cudaError_t e) {
 // supported shape) or the CUDA-core tile.  num_experts == 0: dense product.
 // BT_OPT_GEMM_PATH forces 1 (CUDA-core tile) or 2 (tensor cores where the shape allows).
 enum GemmPath { kPathNone = 0, kPathGemv = 1, kPathSimt = 2, kPathTc = 3 };
-GemmPath gemm_path(int bits, int M, int K, int num_experts) {
+GemmPath gemm_path(int bits, int M, int K, int num_experts, int group = 64) {
   const int forced = opts().gemm_path;
   if (num_experts == 0) {
     if (M == 1) return kPathGemv;
-    return tc_shape_ok(bits, K) && (forced == 2 || (forced == 0 && M >= 16)) ? kPathTc : kPathSimt;
+    return tc_shape_ok(bits, K, group) && (forced == 2 || (forced == 0 && M >= 16)) ? kPathTc : kPathSimt;
   }
   if (M == 0) return kPathNone;
   if (M <= num_experts && forced == 0) return kPathGemv;
-  return forced != 1 && tc_shape_ok(bits, K) ? kPathTc : kPathSimt;
+  return forced != 1 && tc_shape_ok(bits, K, group) ? kPathTc : kPathSimt;
 }
 
 // fp16 x takes the magic-number fast path at every bit width (BT_OPT_GEMV_GENERIC
 // forces the generic one); bits decides only how many chunks per lane exist.
 bool gemv_fast_path(int bits, bt_dtype xd) {
-  (void)bits;
-  return xd == BT_F16 && !opts().gemv_generic;
+  return xd == BT_F16 && !opts().gemv_generic && bits != 5;   // 5-bit codes have no fp16 pair schedule
 }
 
-bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits, int N, int K,
-                   const void* x, bt_dtype xd, void* y, bt_dtype yd, int problems, const int32_t* offsets,
-                   const int32_t* row_index, int num_experts, cudaStream_t stream) {
+bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits, int group,
+                   int N, int K, const void* x, bt_dtype xd, void* y, bt_dtype yd, int problems,
+                   const int32_t* offsets, const int32_t* row_index, int num_experts, cudaStream_t stream) {
   GemvParams p{};
   p.codes = codes;
   p.scales = scales;
@@ -114,7 +117,8 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.y = y;
   p.N = N;
   p.K = K;
-  p.G = K / kGroup;
+  p.G = param_groups(bits, K, group);
+  p.gshift = group_shift(group);
   p.moe_offsets = offsets;
   p.row_index = row_index;
   p.num_experts = offsets ? num_experts : 0;
@@ -124,13 +128,15 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.const_weights = opts().pdl && opts().const_weights;
   p.drop_stage = opts().test_drop_stage;
   opts().test_drop_stage = 0;
-  GemvPlan pl = plan_gemv_mma(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count());
-  if (!pl.feasible) pl = plan_gemv(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count());
+  GemvPlan pl = plan_gemv_mma(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count(), group);
+  if (!pl.feasible)
+    pl = plan_gemv(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count(), group);
   if (!pl.feasible) {
     // no GEMV kernel holds this K slice in registers: the CUDA-core tile computes the same product
     GemmParams g{};
     g.codes = codes; g.scales = scales; g.biases = biases; g.x = x; g.y = y;
     g.M = problems; g.N = N; g.K = K;
+    g.group = group;
     g.offsets = offsets;
     g.row_index = row_index;
     g.num_experts = num_experts;
@@ -297,7 +303,8 @@ bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (s != BT_OK) return s;
   if (!x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0, stream);
+  return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0,
+                  stream);
 }
 
 bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
@@ -334,7 +341,8 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
   }
   GemvParams p{};
   p.K = K;
-  p.G = K / kGroup;
+  p.G = param_groups(bits, K, group_size);
+  p.gshift = group_shift(group_size);
   p.N = max_n;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
@@ -344,16 +352,16 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
   const bool fast = gemv_fast_path(bits, x_dtype);
   GemvPlan pl;
   if (mixed) {
-    pl = plan_gemv_batch_mma(bits, fast, batch, sm_count());
-    if (!pl.feasible) pl = plan_gemv_batch(bits, fast, batch, sm_count());
+    pl = plan_gemv_batch_mma(bits, fast, batch, sm_count(), group_size);
+    if (!pl.feasible) pl = plan_gemv_batch(bits, fast, batch, sm_count(), group_size);
   } else {
     const int problems_equiv = (int)std::max<long long>(1, (rows + max_n - 1) / max_n);
     // the tensor-pipe kernel needs every problem's units (its ragged last one too) 16-byte aligned
     bool all_mma = true;
     for (int i = 0; i < count && all_mma; ++i)
-      all_mma = plan_gemv_mma(bits, fast, problems[i].n, K, 1, 0, sm_count()).feasible;
-    pl = all_mma ? plan_gemv_mma(bits, fast, max_n, K, problems_equiv, 0, sm_count()) : GemvPlan{};
-    if (!pl.feasible) pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count());
+      all_mma = plan_gemv_mma(bits, fast, problems[i].n, K, 1, 0, sm_count(), group_size).feasible;
+    pl = all_mma ? plan_gemv_mma(bits, fast, max_n, K, problems_equiv, 0, sm_count(), group_size) : GemvPlan{};
+    if (!pl.feasible) pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count(), group_size);
   }
   if (!pl.feasible) return BT_ERR_UNSUPPORTED;
   return cuda_status(launch_gemv(p, pl, bits, x_dtype, y_dtype, stream, &batch));
@@ -366,12 +374,14 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (s != BT_OK) return s;
   if (M <= 0 || !x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  const GemmPath path = gemm_path(bits, M, K, 0);
+  const GemmPath path = gemm_path(bits, M, K, 0, group_size);
   if (path == kPathGemv)
-    return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0, stream);
+    return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0,
+                  stream);
   GemmParams p{};
   p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
   p.M = M; p.N = N; p.K = K;
+  p.group = group_size;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
   if (path == kPathTc && tc_supported(bits, K, M, p))
@@ -389,14 +399,15 @@ bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint
       !half_dtype(x_dtype) || !out_dtype(y_dtype))
     return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  const GemmPath path = gemm_path(bits, total_rows, K, num_experts);
+  const GemmPath path = gemm_path(bits, total_rows, K, num_experts, group_size);
   if (path == kPathNone) return BT_OK;
   if (path == kPathGemv)
-    return run_gemv(codes, scales, biases, bits, N, K, x, x_dtype, y, y_dtype, total_rows, expert_offsets,
-                    x_row_index, num_experts, stream);
+    return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, total_rows,
+                    expert_offsets, x_row_index, num_experts, stream);
   GemmParams p{};
   p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
   p.M = total_rows; p.N = N; p.K = K;
+  p.group = group_size;
   p.offsets = expert_offsets;
   p.row_index = x_row_index;
   p.num_experts = num_experts;

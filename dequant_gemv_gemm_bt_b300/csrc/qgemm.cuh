@@ -15,6 +15,7 @@ struct GemmParams {
   const void* x;
   void* y;
   int M, N, K;
+  int group;                 // quantization group size along K: 32, 64 or 128
   const int32_t* offsets;
   const int32_t* row_index;
   int num_experts;
@@ -23,8 +24,8 @@ struct GemmParams {
 };
 
 cudaError_t launch_gemm_simt(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
-// The tensor-core path's limits on bits and K (pointers are checked by tc_supported).
-bool tc_shape_ok(int bits, int K);
+// The tensor-core path's limits on bits, K and group size (pointers are checked by tc_supported).
+bool tc_shape_ok(int bits, int K, int group = 64);
 bool tc_supported(int bits, int K, int M, const GemmParams& p);
 cudaError_t launch_gemm_tc(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
 cudaError_t launch_gemm_tc_grouped(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);

@@ -2,11 +2,12 @@
 // and grouped by expert.  BaseRT pages, thetesserapress.com "What BaseRT does
 // differently" (a GEMM for prefill, M > 1, that dequantizes in its inner loop).
 //
-// A CTA owns a [32 tokens x 64 weight rows] output tile.  Per K step of one
-// quantization group it stages the group's packed words of its 64 weight rows
-// in shared memory, dequantizes them there into fp32 (w = s*q + b, never
-// written to global memory), stages the matching x tile as fp32 and
-// accumulates with fp32 FMA.  Grouped mode walks the device offsets to find
+// A CTA owns a [32 tokens x 64 weight rows] output tile.  Per K step of 64
+// codes it stages the step's packed words of its 64 weight rows in shared
+// memory with the (scale, bias) of each 32-code half (groups of 32, 64 or 128),
+// dequantizes them there into fp32 (w = s*q + b, or the fp16 weight itself for
+// bits = 16; never written to global memory), stages the matching x tile as
+// fp32 and accumulates with fp32 FMA.  Grouped mode walks the device offsets to find
 // which expert and which rows a CTA's token tile covers.
 #include "bt_common.cuh"
 #include "qgemm.cuh"
@@ -21,7 +22,7 @@ __global__ void __launch_bounds__(NT) qgemm_simt_kernel(const GemmParams p) {
   __shared__ float xs[TM][TK + 1];
   __shared__ float ws[TN][TK + 1];
   __shared__ uint32_t wwords[TN][2 * BITS + 1];
-  __shared__ float wsb[TN][2];
+  __shared__ float wsb[TN][2][2];   // (scale, bias) of each 32-code half of the K step
   __shared__ int tile_info[3];   // expert, m0, m_end
 
   pdl_launch_dependents();
@@ -51,7 +52,8 @@ __global__ void __launch_bounds__(NT) qgemm_simt_kernel(const GemmParams p) {
   if (e < 0) return;
 
   const int row_words = p.K * BITS / 32;
-  const int G = p.K / TK;
+  const int G = p.K / TK;                 // K steps of 64 codes
+  const int GQ = p.K / p.group;           // quantization groups per row
   const int tx = tid % 64, ty = tid / 64;
   float acc[TM / 4];
 #pragma unroll
@@ -76,14 +78,19 @@ __global__ void __launch_bounds__(NT) qgemm_simt_kernel(const GemmParams p) {
       const int n = n0 + ni;
       wwords[ni][wi] = (n < p.N) ? __ldg(p.codes + ((size_t)e * p.N + n) * row_words + (size_t)g * 2 * BITS + wi) : 0u;
     }
-    if (tid < TN) {
-      const int n = n0 + tid;
-      float s = 0.f, b = 0.f;
-      if (n < p.N) {
-        s = to_f32<BT_F16>(__ldg(p.scales + ((size_t)e * p.N + n) * G + g));
-        b = to_f32<BT_F16>(__ldg(p.biases + ((size_t)e * p.N + n) * G + g));
+    if constexpr (BITS != 16) {   // fp16 weights have no scale or bias
+      if (tid < 2 * TN) {
+        const int ni = tid >> 1, half = tid & 1;
+        const int n = n0 + ni;
+        const int gq = (g * TK + half * 32) / p.group;   // quantization group of this half of the step
+        float s = 0.f, b = 0.f;
+        if (n < p.N) {
+          s = to_f32<BT_F16>(__ldg(p.scales + ((size_t)e * p.N + n) * GQ + gq));
+          b = to_f32<BT_F16>(__ldg(p.biases + ((size_t)e * p.N + n) * GQ + gq));
+        }
+        wsb[ni][half][0] = s;
+        wsb[ni][half][1] = b;
       }
-      wsb[tid][0] = s; wsb[tid][1] = b;
     }
     __syncthreads();
     // dequantize into shared fp32
@@ -93,7 +100,8 @@ __global__ void __launch_bounds__(NT) qgemm_simt_kernel(const GemmParams p) {
       uint32_t q = wwords[ni][wi] >> off;
       if (off + BITS > 32) q |= wwords[ni][wi + 1] << (32 - off);
       q &= (1u << BITS) - 1u;
-      ws[ni][j] = fmaf(wsb[ni][0], (float)q, wsb[ni][1]);
+      if constexpr (BITS == 16) ws[ni][j] = __half2float(__ushort_as_half((uint16_t)q));   // fp16 weight
+      else ws[ni][j] = fmaf(wsb[ni][j >> 5][0], (float)q, wsb[ni][j >> 5][1]);
     }
     __syncthreads();
 #pragma unroll 8
@@ -134,7 +142,9 @@ cudaError_t launch_simt_xy(const GemmParams& p, int bits, int tiles, cudaStream_
     case 2: return launch_simt_t<2, XD, YD>(p, tiles, st);
     case 3: return launch_simt_t<3, XD, YD>(p, tiles, st);
     case 4: return launch_simt_t<4, XD, YD>(p, tiles, st);
+    case 5: return launch_simt_t<5, XD, YD>(p, tiles, st);
     case 6: return launch_simt_t<6, XD, YD>(p, tiles, st);
+    case 16: return launch_simt_t<16, XD, YD>(p, tiles, st);
     default: return launch_simt_t<8, XD, YD>(p, tiles, st);
   }
 }

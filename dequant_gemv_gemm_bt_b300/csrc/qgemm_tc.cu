@@ -65,9 +65,11 @@ template <int BN, bool SPLIT> constexpr int tmem_cols() {
 constexpr int kThreads = (2 + kDeqWarps) * 32;
 
 struct TcParams {
-  int M, N, K, G;          // G = K / 64
+  int M, N, K, G;          // G = K / 64: K blocks
+  int GQ;                  // quantization groups per row (K / group size)
+  int gshift;              // group of 32-code half h of K block kb: (2*kb + h) >> gshift
   int splits;              // CTAs of a cluster splitting K (gridDim.z); 1 = no split
-  int gc_max;              // most groups any split stages
+  int gc_max;              // most quantization groups any split stages
   int stages;              // TMA ring depth (X tile + packed codes per K block)
   int astages;             // A ring depth (TMEM slots of dequantized weight tiles)
   int bn;
@@ -192,9 +194,6 @@ __device__ __forceinline__ float4 lds128f(uint32_t a) {
   return v;
 }
 
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
 
 // ------------------------------------------------------------------ dequant math
 // Half-precision pair arithmetic (the fp16-X path).
@@ -354,7 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb_lo = split == 0 ? 0 : ((split * p.G) / p.splits) & ~1;
   const int kb_hi = split == p.splits - 1 ? p.G : (((split + 1) * p.G) / p.splits) & ~1;
   const int KB = kb_hi - kb_lo;
-  const int Gc = KB;                       // groups staged for this CTA
+  // quantization groups staged for this CTA (its K range starts on an even K
+  // block, so on a group boundary for groups of 32, 64 and 128 codes)
+  const int gq_lo = (2 * kb_lo) >> p.gshift;
+  const int Gc = ((2 * kb_hi + (1 << p.gshift) - 1) >> p.gshift) - gq_lo;
   // shared memory: [TMA ring: S x (X tile | codes)][scales][biases][barriers]; the A ring is in TMEM
   const int SA = p.astages;   // A slots in use (<= kAStages, < S)
   uint8_t* tring = smem;
@@ -551,9 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first four warps the low 32 codes of each K block, the last four the high 32
     const int r = 32 * (warp & 3) + lane, h = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    // stage this CTA's scales and biases: rows n0..n0+127, groups kb_begin..+Gc
-    const size_t row0 = ((size_t)expert * p.N + n0) * p.G;   // first staged parameter of the tile
-    if (Gc == p.G && n0 + BM <= p.N &&
+    // stage this CTA's scales and biases: rows n0..n0+127, groups gq_lo..+Gc
+    const size_t row0 = ((size_t)expert * p.N + n0) * p.GQ;   // first staged parameter of the tile
+    if (Gc == p.GQ && n0 + BM <= p.N &&
         (((reinterpret_cast<uintptr_t>(p.scales + row0) | reinterpret_cast<uintptr_t>(p.biases + row0)) & 15u) == 0)) {
       // whole rows: the tile's parameters are one contiguous block per array, laid
       // out as in shared memory, so they move in 16-byte pieces
@@ -564,17 +566,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async16(reinterpret_cast<uint8_t*>(sB) + i * 16, gb + i * 16);
       }
     } else {
-      for (int i = t; i < BM * (Gc / 2); i += kDeqWarps * 32) {
-        const int rr = i / (Gc / 2), gg = 2 * (i % (Gc / 2));
+      // part of a row (K split) or the ragged last rows: one parameter at a time
+      for (int i = t; i < BM * Gc; i += kDeqWarps * 32) {
+        const int rr = i / Gc, gg = i % Gc;
         const int n = n0 + rr;
+        uint16_t sv = 0, bv = 0;
         if (n < p.N) {
-          const size_t off = ((size_t)expert * p.N + n) * p.G + kb_lo + gg;
-          cp_async4(sS + rr * Gc + gg, p.scales + off);
-          cp_async4(sB + rr * Gc + gg, p.biases + off);
-        } else {
-          *reinterpret_cast<uint32_t*>(sS + rr * Gc + gg) = 0u;
-          *reinterpret_cast<uint32_t*>(sB + rr * Gc + gg) = 0u;
+          const size_t off = ((size_t)expert * p.N + n) * p.GQ + gq_lo + gg;
+          sv = __ldg(p.scales + off);
+          bv = __ldg(p.biases + off);
         }
+        sS[rr * Gc + gg] = sv;
+        sB[rr * Gc + gg] = bv;
       }
     }
     cp_async_wait_all();
@@ -606,8 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < BITS; ++i) w[i] = lds32(caddr + 4 * i);
       }
-      const uint16_t s16 = lds16(sS_a + (uint32_t)(r * Gc + kb) * 2);
-      const uint16_t b16 = lds16(sB_a + (uint32_t)(r * Gc + kb) * 2);
+      const int gq = ((2 * (kb_lo + kb) + h) >> p.gshift) - gq_lo;   // this thread's 32 codes' group
+      const uint16_t s16 = lds16(sS_a + (uint32_t)(r * Gc + gq) * 2);
+      const uint16_t b16 = lds16(sB_a + (uint32_t)(r * Gc + gq) * 2);
       uint32_t v[16], vlo[16];
       deq32<BITS, BF16, SPLIT>(w, s16, b16, v, vlo);
       const uint32_t slot = tmem_base + lane_base + kACol0 + (uint32_t)a * kASlot + (uint32_t)(16 * h);
@@ -729,19 +733,25 @@ EncodeTiledFn encode_fn() {
 }
 
 // Shared memory of one CTA for a given K split (mirrors the layout in the kernel).
+// Quantization groups of K blocks [lo, hi) (lo even) with groups of 32 << gshift codes.
+inline int groups_in(int lo, int hi, int gshift) {
+  return ((2 * hi + (1 << gshift) - 1) >> gshift) - ((2 * lo) >> gshift);
+}
+
 template <int BITS, int BN, bool GROUPED>
-size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nullptr) {
+size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nullptr, int gshift = 1) {
   const int G_all = K / BK;
-  int gc_max = 0;
+  int kb_max = 0, gq_max = 0;
   for (int z = 0; z < splits; ++z) {
     const int lo = z == 0 ? 0 : ((z * G_all) / splits) & ~1;
     const int hi = z == splits - 1 ? G_all : (((z + 1) * G_all) / splits) & ~1;
     if (hi - lo < 1) return 0;
-    gc_max = std::max(gc_max, hi - lo);
+    kb_max = std::max(kb_max, hi - lo);
+    gq_max = std::max(gq_max, groups_in(lo, hi, gshift));
   }
   const uint32_t x_bytes = BN * BK * 2, c_bytes = BM * 8 * BITS;
   const uint32_t stage_bytes = (x_bytes + c_bytes + 1023u) & ~1023u;
-  const size_t params_bytes = (size_t)2 * BM * gc_max * sizeof(uint16_t);
+  const size_t params_bytes = (size_t)2 * BM * gq_max * sizeof(uint16_t);
   const size_t fixed = 1024 + params_bytes + 8 + (size_t)(2 * 12 + 2 * kAStages + 1) * 8 + 16;
   const size_t budget = (GROUPED && BN <= 32) ? 112 * 1024 : 222 * 1024;
   int stages = (int)((budget - std::min(budget, fixed)) / stage_bytes);
@@ -750,7 +760,7 @@ size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nul
   const size_t recv_bytes = splits > 1 ? (size_t)splits * BM * owned_max * 16 * 4 : 0;
   while ((size_t)stages * stage_bytes < recv_bytes) ++stages;
   if (stages_out) *stages_out = stages;
-  if (k_blocks_out) *k_blocks_out = gc_max;
+  if (k_blocks_out) *k_blocks_out = kb_max;
   return fixed + (size_t)stages * stage_bytes;
 }
 
@@ -801,13 +811,15 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.N = gp.N;
   p.K = gp.K;
   p.G = gp.K / BK;
+  p.GQ = gp.K / gp.group;
+  p.gshift = gp.group == 32 ? 0 : (gp.group == 64 ? 1 : 2);
   p.splits = splits;
   int gc_max = 0;
   for (int z = 0; z < splits; ++z) {   // same split boundaries as the kernel
     const int lo = z == 0 ? 0 : ((z * p.G) / splits) & ~1;
     const int hi = z == splits - 1 ? p.G : (((z + 1) * p.G) / splits) & ~1;
     if (hi - lo < 1) return cudaErrorInvalidValue;
-    gc_max = std::max(gc_max, hi - lo);
+    gc_max = std::max(gc_max, groups_in(lo, hi, p.gshift));
   }
   p.gc_max = gc_max;
   p.bn = BN;
@@ -825,7 +837,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.row_index = gp.row_index;
   p.num_experts = gp.num_experts;
   int stages = 0;
-  const size_t smem = tc_smem_bytes<BITS, BN, GROUPED>(gp.K, splits, &stages);
+  const size_t smem = tc_smem_bytes<BITS, BN, GROUPED>(gp.K, splits, &stages, nullptr, p.gshift);
   if (smem == 0) return cudaErrorInvalidValue;
   p.stages = stages;
   p.astages = std::min(a_stages<BN, SPLIT>(), stages - 1);   // the dequant waits rely on S > SA
@@ -973,17 +985,17 @@ cudaError_t launch_gemm_tc_grouped(const GemmParams& gp, int bits, bt_dtype xd, 
 }
 
 
-bool tc_shape_ok(int bits, int K) {
+bool tc_shape_ok(int bits, int K, int group) {
   if (!(bits == 2 || bits == 4 || bits == 6 || bits == 8)) return false;
   const int G = K / 64;
-  if (G % 2) return false;                          // 4-byte cp.async of scale pairs
-  if (G > 192) return false;                        // the CTA's scales/biases are staged whole in shared memory
+  if (G % 2) return false;                          // K splits start on even K blocks
+  if (K / group > 192) return false;                // the CTA's scales/biases are staged whole in shared memory
   if (((size_t)K * bits / 8) % 16) return false;    // TMA row stride
   return true;
 }
 
 bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
-  if (!tc_shape_ok(bits, K)) return false;
+  if (!tc_shape_ok(bits, K, gp.group)) return false;
   if ((reinterpret_cast<uintptr_t>(gp.x) & 15) || (reinterpret_cast<uintptr_t>(gp.codes) & 15)) return false;
   (void)M;
   return true;

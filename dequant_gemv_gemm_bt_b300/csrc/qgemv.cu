@@ -10,7 +10,9 @@ cudaError_t launch_gemv_b2(const GemvParams&, const GemvPlan&, bt_dtype, const G
 cudaError_t launch_gemv_b3(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
 cudaError_t launch_gemv_b4(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
 cudaError_t launch_gemv_b6(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
+cudaError_t launch_gemv_b5(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
 cudaError_t launch_gemv_b8(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
+cudaError_t launch_gemv_b16(const GemvParams&, const GemvPlan&, bt_dtype, const GemvBatch<kBatchCap>*, cudaStream_t);
 cudaError_t launch_gemv_mma_b4(const GemvParams&, const GemvPlan&, const GemvBatch<kBatchCap>*, cudaStream_t);
 
 namespace {
@@ -20,7 +22,7 @@ constexpr int kRingBudget = 176 * 1024;
 constexpr size_t kMaxSmem = 227 * 1024;   // opt-in dynamic shared memory per block on sm_100/sm_103
 }  // namespace
 
-GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms) {
+GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group) {
   GemvPlan pl{};
   pl.fast = fast;
   const int nchunks = K / 32;
@@ -48,7 +50,7 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   pl.feasible = cpl <= cpl_cap && kw <= nw && nw % kw == 0 && K <= 16 * 1024 * (wide ? 2 : 1);
   if (!pl.feasible) return pl;
   const int rw = nw / kw;
-  const int G = K / kGroup;
+  const int G = param_groups(bits, K, group);
   const int row_bytes = K * bits / 8;
   const int per_row = row_bytes + 4 * G;
   // smallest row multiple that keeps every bulk copy a multiple of 16 bytes (a power of two)
@@ -113,8 +115,8 @@ namespace {
 // it reserved per CTA)
 size_t mma_smem_limit(int ctas) { return ctas == 1 ? 227 * 1024 : (228 * 1024) / ctas - 1024; }
 
-bool mma_applies(int bits, bool fast, int N, int K) {
-  if (opts().gemv_cuda_core || bits != 4 || !fast || K > kMmaMaxK || K % kGroup) return false;
+bool mma_applies(int bits, bool fast, int N, int K, int group) {
+  if (opts().gemv_cuda_core || bits != 4 || group != 64 || !fast || K > kMmaMaxK || K % kGroup) return false;
   if (opts().gemv_tensor_pipe == 2) return false;
   const int G = K / kGroup, row_bytes = K * bits / 8;
   // every unit, the ragged last one included, must move in 16-byte pieces
@@ -187,13 +189,13 @@ void set_shape(GemvPlan& pl, const MmaShape& sh) {
 }
 }  // namespace
 
-GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms) {
+GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group) {
   GemvPlan pl{};
   pl.fast = fast;
   pl.mma = true;
   pl.cpl = 1;
   pl.ri = 16;
-  if (num_experts || !mma_applies(bits, fast, N, K)) return pl;
+  if (num_experts || !mma_applies(bits, fast, N, K, group)) return pl;
   if (!mma_by_size((long long)N * problems, sms)) return pl;
   const MmaShape sh = mma_shape(opts().gemv_mma_cfg);
   set_shape(pl, sh);
@@ -213,7 +215,7 @@ GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_
   return pl;
 }
 
-GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms) {
+GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group) {
   GemvPlan pl{};
   pl.fast = fast;
   pl.mma = true;
@@ -223,7 +225,7 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
   int g_max = 0;
   for (int i = 0; i < batch.count; ++i) {
     const GemvProblem& q = batch.prob[i];
-    if (q.k <= 0 || !mma_applies(bits, fast, q.n, q.k)) return pl;
+    if (q.k <= 0 || !mma_applies(bits, fast, q.n, q.k, group)) return pl;
     rows += q.n;
     g_max = std::max(g_max, q.k / kGroup);
   }
@@ -252,7 +254,7 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
   return pl;
 }
 
-GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms) {
+GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group) {
   GemvPlan pl{};
   pl.fast = fast;
   pl.feasible = false;
@@ -262,11 +264,11 @@ GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int s
   int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
   for (int i = 0; i < batch.count; ++i) {
     const GemvProblem& q = batch.prob[i];
-    if (q.k <= 0 || q.k % kGroup || q.k > 8 * 32 * 32) return pl;   // one chunk per lane needs K <= 8192
+    if (q.k <= 0 || q.k % group || q.k > 8 * 32 * 32) return pl;   // one chunk per lane needs K <= 8192
     const int nchunks = q.k / 32;
     int kw = 1;
     while (32 * kw < nchunks) kw *= 2;
-    const int per_row = q.k * bits / 8 + 4 * (q.k / kGroup);
+    const int per_row = q.k * bits / 8 + 4 * param_groups(bits, q.k, group);
     while (ri > 1 && ri * (kMaxNW / kw) * per_row > stage_budget) ri /= 2;
   }
   const int ctas_per_sm = gemv_ctas_per_sm(1, ri);   // one chunk per lane (the kernel's launch bounds)
@@ -279,7 +281,7 @@ GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int s
     int kw = 1;
     while (32 * kw < nchunks) kw *= 2;
     q.kw = kw;
-    q.g = q.k / kGroup;
+    q.g = param_groups(bits, q.k, group);
     q.row_bytes = q.k * bits / 8;
     const int per_row = q.row_bytes + 4 * q.g;
     int m = 1;
@@ -356,7 +358,9 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
     case 2: return launch_gemv_b2(p, plb, xd, batch, st);
     case 3: return launch_gemv_b3(p, plb, xd, batch, st);
     case 4: return launch_gemv_b4(p, plb, xd, batch, st);
+    case 5: return launch_gemv_b5(p, plb, xd, batch, st);
     case 6: return launch_gemv_b6(p, plb, xd, batch, st);
+    case 16: return launch_gemv_b16(p, plb, xd, batch, st);
     default: return launch_gemv_b8(p, plb, xd, batch, st);
   }
 }

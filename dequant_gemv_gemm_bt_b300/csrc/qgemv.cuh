@@ -32,6 +32,8 @@ struct GemvParams {
   int drop_stage;
   // tensor-pipe kernel: shared-memory bytes reserved for the per-group x sums
   int xsum_bytes;
+  // quantization group of 32-code chunk c is c >> gshift (group size 32 << gshift)
+  int gshift;
 };
 
 // Batched launches: many independent GEMVs of the same bits and dtypes, each
@@ -78,16 +80,21 @@ struct MmaShape {
 };
 MmaShape mma_shape(int cfg);   // cfg 0: the default shape
 
-GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
+// Quantization groups per row whose scale and bias the kernels read: K / group,
+// or 0 for fp16 weights (bits = 16), which have none.
+inline int param_groups(int bits, int K, int group) { return bits == 16 ? 0 : K / group; }
+
+GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group = 64);
 // The tensor-pipe kernel's plan for the same arguments (infeasible when it does
 // not apply: 4-bit codes, fp16 x, dense, K <= 8192, every unit 16-byte aligned).
-GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms);
+GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms,
+                       int group = 64);
 // One launch over problems of several K (each K <= 8192, one chunk per lane):
 // fills every problem's geometry in `batch` and returns the launch plan
 // (stage size covering the largest unit); infeasible when the problems need
 // different kernel shapes.
-GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms);
-GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms);
+GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group = 64);
+GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group = 64);
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,
                         cudaStream_t stream, GemvBatch<kBatchCap>* batch = nullptr);
 

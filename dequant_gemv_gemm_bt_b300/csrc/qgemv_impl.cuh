@@ -78,6 +78,11 @@ __device__ __forceinline__ void load_chunk(uint32_t saddr, const uint8_t* gptr, 
     } else if constexpr (BITS == 6) {
 #pragma unroll
       for (int i = 0; i < 3; ++i) { uint2 v = lds64(saddr + 8 * i); w[2 * i] = v.x; w[2 * i + 1] = v.y; }
+    } else if constexpr (BITS == 16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 v = lds128(saddr + 16 * i); w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < BITS; ++i) w[i] = lds32(saddr + 4 * i);
@@ -92,6 +97,12 @@ __device__ __forceinline__ void load_chunk(uint32_t saddr, const uint8_t* gptr, 
 #pragma unroll
       for (int i = 0; i < BITS / 2; ++i) {
         uint2 v = __ldg(reinterpret_cast<const uint2*>(gptr) + i); w[2 * i] = v.x; w[2 * i + 1] = v.y;
+      }
+    } else if constexpr (BITS == 16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(gptr) + i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
       }
     } else {
 #pragma unroll
@@ -142,7 +153,13 @@ template <> struct FastClasses<4> { static constexpr int n = 2; };
 template <> struct FastClasses<8> { static constexpr int n = 1; };
 template <> struct FastClasses<3> { static constexpr int n = StreamLayout<3>::n_classes; };
 template <> struct FastClasses<6> { static constexpr int n = StreamLayout<6>::n_classes; };
+template <> struct FastClasses<16> { static constexpr int n = 1; };
 template <int BITS> constexpr bool kStreamBits = (BITS == 3 || BITS == 6);
+// 5-bit codes have no fp16 pair schedule: they take the generic path.  16 is
+// the fp16-weight format: the "codes" are the weights themselves.
+template <int BITS> constexpr bool kHasFast = BITS != 5;
+// widths whose fast path has kernels with three or four x chunks per lane
+template <int BITS> constexpr bool kWideBits = BITS == 2 || BITS == 4 || BITS == 8;
 
 // For each fp16x2 code pair of a word: the positions (within the word) of its
 // low-half and high-half codes, and its class.
@@ -295,7 +312,9 @@ __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_
       s.xh[8 * i + 2 * j + 1] = u[j] >> 16;
     }
   }
-  if constexpr (kStreamBits<BITS>) {
+  if constexpr (BITS == 16) {
+    s.xsum = 0.f;   // fp16 weights: no bias term
+  } else if constexpr (kStreamBits<BITS>) {
     stream_seeds<BITS>(s, std::make_integer_sequence<int, StreamLayout<BITS>::n_pairs>{});
   } else {
   using L = FastLayout<BITS>;
@@ -363,17 +382,38 @@ __device__ __forceinline__ float chunk_dot_words(const uint32_t (&w)[BITS], cons
   return t;
 }
 
+// fp16 weights: sum_j w_j * x_j with the mixed fp16 x fp16 -> fp32 FMA, two chains.
+__device__ __forceinline__ float chunk_dot_f16w(const uint32_t (&w)[16], const XSlice<16, true>& s) {
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    fma_pair(a0, s.xh[2 * i], s.xh[2 * i + 1], w[i]);
+    fma_pair(a1, s.xh[2 * i + 2], s.xh[2 * i + 3], w[i + 1]);
+  }
+  return a0 + a1;
+}
+
 // sum_j q_j * x_j over one chunk (fast path).
 template <int BITS>
 __device__ __forceinline__ float chunk_dot_fast(const uint32_t (&w)[BITS], const XSlice<BITS, true>& s) {
-  if constexpr (kStreamBits<BITS>) return chunk_dot_stream<BITS>(w, s);
+  if constexpr (BITS == 16) return chunk_dot_f16w(w, s);
+  else if constexpr (kStreamBits<BITS>) return chunk_dot_stream<BITS>(w, s);
   else return chunk_dot_words<BITS>(w, s);
 }
 
 // sum_j q_j * x_j over one chunk (generic path, any bits).
 template <int BITS>
 __device__ __forceinline__ float chunk_dot_generic(const uint32_t (&w)[BITS], const XSlice<BITS, false>& s) {
-  constexpr uint32_t mask = (1u << BITS) - 1u;
+  if constexpr (BITS == 16) {   // fp16 weights
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      acc0 = fmaf(s.xv[2 * i], __half2float(__ushort_as_half((uint16_t)(w[i] & 0xFFFFu))), acc0);
+      acc1 = fmaf(s.xv[2 * i + 1], __half2float(__ushort_as_half((uint16_t)(w[i] >> 16))), acc1);
+    }
+    return acc0 + acc1;
+  }
+  constexpr uint32_t mask = (1u << (BITS & 15)) - 1u;
   float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -773,17 +813,22 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
         if (LIVE && c < nchunks) {
           uint32_t w[RI][BITS];
           float sc[RI], bs[RI];
+          const int grp = c >> p.gshift;   // quantization group of this 32-code chunk
 #pragma unroll
           for (int j = 0; j < RI; ++j) {
             const int r = CLAMP ? min(r0 + j, rows - 1) : r0 + j;
             if constexpr (STAGED) {
               load_chunk<BITS, true>(st + r * row_bytes + c * (4 * BITS), nullptr, w[j]);
-              sc[j] = to_f32<BT_F16>(lds16(st_sc + (r * G + (c >> 1)) * 2));
-              bs[j] = to_f32<BT_F16>(lds16(st_bi + (r * G + (c >> 1)) * 2));
+              if constexpr (BITS != 16) {
+                sc[j] = to_f32<BT_F16>(lds16(st_sc + (r * G + grp) * 2));
+                bs[j] = to_f32<BT_F16>(lds16(st_bi + (r * G + grp) * 2));
+              }
             } else {
               load_chunk<BITS, false>(0, g_codes + (size_t)r * row_bytes + c * (4 * BITS), w[j]);
-              sc[j] = to_f32<BT_F16>(__ldg(g_sc + (size_t)r * G + (c >> 1)));
-              bs[j] = to_f32<BT_F16>(__ldg(g_bi + (size_t)r * G + (c >> 1)));
+              if constexpr (BITS != 16) {
+                sc[j] = to_f32<BT_F16>(__ldg(g_sc + (size_t)r * G + grp));
+                bs[j] = to_f32<BT_F16>(__ldg(g_bi + (size_t)r * G + grp));
+              }
             }
           }
 #pragma unroll
@@ -791,7 +836,8 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
             float t;
             if constexpr (FAST) t = chunk_dot_fast<BITS>(w[j], xs[i]);
             else t = chunk_dot_generic<BITS>(w[j], xs[i]);
-            part[j] = fmaf(sc[j], t, fmaf(bs[j], xs[i].xsum, part[j]));
+            if constexpr (BITS == 16) part[j] += t;   // fp16 weights: no scale or bias
+            else part[j] = fmaf(sc[j], t, fmaf(bs[j], xs[i].xsum, part[j]));
           }
         }
       }
@@ -876,8 +922,8 @@ cudaError_t launch_cpl(const GemvParams& p, const GemvPlan& pl, const GemvBatch<
     case 1: return launch_ri<BITS, XD, 1, FAST, BATCH>(p, pl, b, st);
     case 2: return launch_ri<BITS, XD, 2, FAST, BATCH>(p, pl, b, st);
     // three or four chunks per lane: fast path of bits 2/4/8 only (K up to 32768)
-    case 3: if constexpr (FAST && !kStreamBits<BITS>) return launch_ri<BITS, XD, 3, FAST, BATCH>(p, pl, b, st); else break;
-    case 4: if constexpr (FAST && !kStreamBits<BITS>) return launch_ri<BITS, XD, 4, FAST, BATCH>(p, pl, b, st); else break;
+    case 3: if constexpr (FAST && kWideBits<BITS>) return launch_ri<BITS, XD, 3, FAST, BATCH>(p, pl, b, st); else break;
+    case 4: if constexpr (FAST && kWideBits<BITS>) return launch_ri<BITS, XD, 4, FAST, BATCH>(p, pl, b, st); else break;
   }
   return cudaErrorInvalidValue;
 }
@@ -886,7 +932,8 @@ template <int BITS, bool BATCH>
 cudaError_t launch_bits_b(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, const GemvBatch<kBatchCap>* b,
                           cudaStream_t st) {
   if (xd == BT_F16) {
-    if (pl.fast) return launch_cpl<BITS, BT_F16, true, BATCH>(p, pl, b, st);
+    if constexpr (kHasFast<BITS>)
+      if (pl.fast) return launch_cpl<BITS, BT_F16, true, BATCH>(p, pl, b, st);
     return launch_cpl<BITS, BT_F16, false, BATCH>(p, pl, b, st);
   }
   return launch_cpl<BITS, BT_BF16, false, BATCH>(p, pl, b, st);

@@ -58,7 +58,8 @@ def gemv(bt, codes=W[0], scales=W[1], biases=W[2], bits=4, g=64, n=128, k=256, x
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(codes=None), 1), (dict(scales=None), 1), (dict(x=None), 1), (dict(y=None), 1),
-    (dict(bits=5), 2), (dict(bits=1), 2), (dict(bits=16), 2), (dict(g=32), 2),
+    (dict(bits=7), 2), (dict(bits=1), 2), (dict(bits=12), 2), (dict(g=16), 2), (dict(g=96), 2), (dict(g=256), 2),
+    (dict(bits=16, codes=None), 1), (dict(biases=None), 1), (dict(g=128, k=192), 1),
     (dict(n=0), 1), (dict(k=0), 1), (dict(n=-3), 1), (dict(k=100), 1), (dict(k=64 * 1024), 2),
     (dict(codes=A + 4), 3), (dict(x=A + 8), 3), (dict(xd=2), 1), (dict(yd=7), 1),
 ])

@@ -361,6 +361,6 @@ def test_gemm_plan_rejects_bad_sizes(bt):
         with pytest.raises(bt.BTError):
             bt.bt_plan_gemm(*args)
     with pytest.raises(bt.BTError):
-        bt.bt_plan_gemm(5, 16, 64, 64)
+        bt.bt_plan_gemm(7, 16, 64, 64)
     with pytest.raises(bt.BTError):
         bt.bt_plan_gemm(4, 16, 64, 64 * 1024)                          # K above 32768

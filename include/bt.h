@@ -24,7 +24,14 @@
  *           uint32", code j in bits [4*(j%8), +4) of word j/8.
  *   scales  fp16 bit patterns (uint16) [N][K/g]
  *   biases  fp16 bit patterns (uint16) [N][K/g]
- * Supported: bits in {2,3,4,6,8}; g = 64; K a multiple of g.
+ * Supported: bits in {2,3,4,5,6,8}; g in {32, 64, 128}; K a multiple of g.
+ * Because g*bits is a multiple of 32, every 32-code slice of a row starts on a
+ * word, so a row is one contiguous stream whatever g is.
+ *
+ * fp16 weights ("bits = 16", the FP16 end of the pages' Q2..FP16 range,
+ * gist.science summary, "Metodologia"): codes holds the weights' fp16 bit
+ * patterns, weight k of a row in bits [16*(k%2), +16) of word k/2 ([N][K/2]
+ * words); scales and biases are not read and may be NULL.
  *
  * Conventions for every entry point:
  *   - All pointers are device memory owned by the caller; the library keeps no

@@ -34,8 +34,10 @@ BT_F16, BT_BF16, BT_F32 = 0, 1, 2
  BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI, BT_OPT_GEMV_CUDA_CORE, BT_OPT_GEMV_MMA_STAGE_KB, BT_OPT_GEMV_MMA_SHAPE,
  BT_OPT_GEMV_MMA_GROUPS, BT_OPT_GEMV_TENSOR_PIPE) = range(16)
 
-EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_route", "bt_swiglu", "bt_moe_combine",
-           "bt_status_string", "bt_last_device_error", "bt_set_option", "bt_plan_gemv", "bt_plan_gemv_batch", "bt_plan_gemm")
+EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_qgemm_swiglu", "bt_moe_qgemv_pairs",
+           "bt_moe_down_combine",
+           "bt_moe_route", "bt_swiglu", "bt_moe_combine", "bt_status_string", "bt_last_device_error", "bt_set_option",
+           "bt_plan_gemv", "bt_plan_gemv_batch", "bt_plan_gemm")
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -51,6 +53,9 @@ class GemvProblem(ctypes.Structure):
 
 lib.bt_qgemv_batched.argtypes = [ctypes.POINTER(GemvProblem), _i, _i, _i, _i, _i, _i, _p]
 lib.bt_moe_qgemm.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
+lib.bt_moe_qgemm_swiglu.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
+lib.bt_moe_qgemv_pairs.argtypes = _W + [_i, _i, _i, _p, _i, _i, _p, _i, _p, _i, _i, _p]
+lib.bt_moe_down_combine.argtypes = _W + [_i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _p]
 lib.bt_moe_route.argtypes = [_p, _i, _i, _i, _p, _p, _p, _p, _p]
 lib.bt_swiglu.argtypes = [_p, _i, _i, _i, _p, _i, _p]
 lib.bt_moe_combine.argtypes = [_p, _i, _p, _p, _i, _i, _i, _p, _i, _p]
@@ -275,6 +280,79 @@ def bt_moe_qgemm(codes, scales, biases, bits: int, expert_offsets, x, y=None, *,
                             total_rows, ri, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y), _stream(stream)),
            "bt_moe_qgemm")
     return y
+
+
+def bt_moe_qgemm_swiglu(codes, scales, biases, bits: int, expert_offsets, x, h=None, *, total_rows=None,
+                        x_row_index=None, group_size: int = 64, out_dtype=torch.bfloat16, stream=None):
+    """Grouped gate|up product with the SwiGLU epilogue: ``codes`` [E, 2I, .] with gate/up rows
+    interleaved (row 2i gate i, row 2i+1 up i); returns ``h`` [total_rows, I]."""
+    k = x.shape[-1]
+    n = check_weight(codes, scales, biases, bits, k, group_size, experts=True)
+    _need(n % 2 == 0, f"gate|up rows must be even (interleaved pairs), got {n}")
+    e = codes.shape[0]
+    if total_rows is None:
+        total_rows = x_row_index.shape[0] if x_row_index is not None else x.shape[0]
+    _check_int32(expert_offsets, "expert_offsets", e + 1)
+    if x_row_index is not None:
+        _check_int32(x_row_index, "x_row_index", total_rows)
+    else:
+        _need(x.numel() >= total_rows * k, f"x holds {x.numel() // max(k, 1)} rows, total_rows is {total_rows}")
+    if h is None:
+        h = torch.empty((total_rows, n // 2), dtype=out_dtype, device=x.device)
+    _check_out(h, "h", total_rows * (n // 2))
+    _same_device(codes, scales, biases, x, h, expert_offsets, x_row_index)
+    c, s, b = _weights(codes, scales, biases)
+    ri = _dev(x_row_index, "x_row_index") if x_row_index is not None else None
+    _check(lib.bt_moe_qgemm_swiglu(c, s, b, bits, group_size, e, n, k, _dev(expert_offsets, "expert_offsets"),
+                                   total_rows, ri, _dev(x, "x"), _dt(x), _dev(h, "h"), _dt(h), _stream(stream)),
+           "bt_moe_qgemm_swiglu")
+    return h
+
+
+def bt_moe_qgemv_pairs(codes, scales, biases, bits: int, topk_ids, x, y=None, *, swiglu: bool = False,
+                       group_size: int = 64, out_dtype=torch.float16, stream=None):
+    """Routed pairs without a sort: pair r = t*top_k + s uses expert ``topk_ids[t, s]`` and x row t;
+    returns ``y`` [T*top_k, N] (``N/2`` with the SwiGLU epilogue, gate/up rows interleaved)."""
+    _need(x.dim() == 2, f"x must be [T, K], got shape {list(x.shape)}")
+    t, k = x.shape
+    n = check_weight(codes, scales, biases, bits, k, group_size, experts=True)
+    _check_int32(topk_ids, "topk_ids", 0)
+    _need(topk_ids.dim() == 2 and topk_ids.shape[0] == t, f"topk_ids must be [T={t}, top_k]")
+    top_k = topk_ids.shape[1]
+    cols = n // 2 if swiglu else n
+    _need(not swiglu or n % 2 == 0, "gate|up rows must be even (interleaved pairs)")
+    if y is None:
+        y = torch.empty((t * top_k, cols), dtype=out_dtype, device=x.device)
+    _check_out(y, "y", t * top_k * cols)
+    _same_device(codes, scales, biases, x, y, topk_ids)
+    c, s, b = _weights(codes, scales, biases)
+    _check(lib.bt_moe_qgemv_pairs(c, s, b, bits, group_size, codes.shape[0], n, k, _dev(topk_ids, "topk_ids"), t,
+                                  top_k, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y), 1 if swiglu else 0,
+                                  _stream(stream)), "bt_moe_qgemv_pairs")
+    return y
+
+
+def bt_moe_down_combine(codes, scales, biases, bits: int, topk_ids, gates, h, out=None, *, group_size: int = 64,
+                        out_dtype=torch.float32, stream=None):
+    """Down products of each token's routed experts, gate-weighted and summed in the kernel:
+    ``out[t] = sum_s gates[t, s] * W_down[ids[t, s]] @ h[t*top_k + s]``; ``h`` [T*top_k, K]."""
+    _check_int32(topk_ids, "topk_ids", 0)
+    _need(topk_ids.dim() == 2, "topk_ids must be [T, top_k]")
+    t, top_k = topk_ids.shape
+    k = h.shape[-1]
+    n = check_weight(codes, scales, biases, bits, k, group_size, experts=True)
+    _need(h.dim() == 2 and h.shape[0] == t * top_k, f"h must be [T*top_k = {t * top_k}, K]")
+    _need(isinstance(gates, torch.Tensor) and gates.dtype == torch.float32 and gates.numel() >= t * top_k,
+          "gates must be a float32 tensor of [T, top_k]")
+    if out is None:
+        out = torch.empty((t, n), dtype=out_dtype, device=h.device)
+    _check_out(out, "out", t * n)
+    _same_device(codes, scales, biases, h, out, topk_ids, gates)
+    c, s, b = _weights(codes, scales, biases)
+    _check(lib.bt_moe_down_combine(c, s, b, bits, group_size, codes.shape[0], n, k, _dev(topk_ids, "topk_ids"),
+                                   _dev(gates, "gates"), t, top_k, _dev(h, "h"), _dt(h), _dev(out, "out"),
+                                   _dt(out), _stream(stream)), "bt_moe_down_combine")
+    return out
 
 
 def bt_moe_route(topk_ids, num_experts: int, offsets=None, pair_index=None, pair_row=None, pair_token=None,

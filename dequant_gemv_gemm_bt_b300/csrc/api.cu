@@ -106,9 +106,22 @@ bool gemv_fast_path(int bits, bt_dtype xd) {
   return xd == BT_F16 && !opts().gemv_generic && bits != 5;   // 5-bit codes have no fp16 pair schedule
 }
 
+// How the problems of a GEMV launch map to experts and rows (all empty: dense).
+struct RowMap {
+  const int32_t* offsets = nullptr;     // grouped rows: expert of row r from the offsets
+  const int32_t* row_index = nullptr;   // grouped rows: x row of row r
+  int num_experts = 0;
+  const int32_t* pair_ids = nullptr;    // routed pairs: expert of problem r, x row r / top_k
+  int top_k = 0;
+  int swiglu = 0;                       // SwiGLU epilogue over interleaved gate/up rows
+};
+
 bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits, int group,
-                   int N, int K, const void* x, bt_dtype xd, void* y, bt_dtype yd, int problems,
-                   const int32_t* offsets, const int32_t* row_index, int num_experts, cudaStream_t stream) {
+                   int N, int K, const void* x, bt_dtype xd, void* y, bt_dtype yd, int problems, const RowMap& rm,
+                   cudaStream_t stream) {
+  const int32_t* offsets = rm.offsets;
+  const int32_t* row_index = rm.row_index;
+  const int num_experts = rm.num_experts;
   GemvParams p{};
   p.codes = codes;
   p.scales = scales;
@@ -121,16 +134,23 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.gshift = group_shift(group);
   p.moe_offsets = offsets;
   p.row_index = row_index;
-  p.num_experts = offsets ? num_experts : 0;
+  p.num_experts = (offsets || rm.pair_ids) ? num_experts : 0;
+  p.pair_ids = rm.pair_ids;
+  p.top_k = rm.top_k;
+  p.swiglu = rm.swiglu;
   p.total_rows = problems;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
   p.const_weights = opts().pdl && opts().const_weights;
   p.drop_stage = opts().test_drop_stage;
   opts().test_drop_stage = 0;
-  GemvPlan pl = plan_gemv_mma(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count(), group);
+  GemvPlan pl{};
+  if (!rm.pair_ids && !rm.swiglu)
+    pl = plan_gemv_mma(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count(), group);
   if (!pl.feasible)
-    pl = plan_gemv(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count(), group);
+    pl = plan_gemv(bits, gemv_fast_path(bits, xd), N, K, problems, offsets ? num_experts : 0, sm_count(), group,
+                   rm.swiglu != 0);
+  if (!pl.feasible && rm.pair_ids) return BT_ERR_UNSUPPORTED;   // routed pairs run on the GEMV only
   if (!pl.feasible) {
     // no GEMV kernel holds this K slice in registers: the CUDA-core tile computes the same product
     GemmParams g{};
@@ -140,11 +160,49 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
     g.offsets = offsets;
     g.row_index = row_index;
     g.num_experts = num_experts;
+    g.swiglu = rm.swiglu;
     g.err = p.err;
     g.timeout_ns = p.timeout_ns;
     return cuda_status(launch_gemm_simt(g, bits, xd, yd, stream));
   }
   return cuda_status(launch_gemv(p, pl, bits, xd, yd, stream));
+}
+
+// Grouped expert product (optionally with the SwiGLU epilogue): the GEMV for at
+// most one row per expert, else the tensor cores or the CUDA-core tile.
+bt_status moe_grouped(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                      int group_size, int num_experts, int N, int K, const int32_t* expert_offsets, int total_rows,
+                      const int32_t* x_row_index, const void* x, bt_dtype x_dtype, void* y, bt_dtype y_dtype,
+                      int swiglu, cudaStream_t stream) {
+  bt_status s = check_weights(codes, scales, biases, bits, group_size, N, K);
+  if (s != BT_OK) return s;
+  if (num_experts <= 0 || num_experts > 4096 || total_rows < 0 || !expert_offsets || !x || !y ||
+      !half_dtype(x_dtype) || !out_dtype(y_dtype))
+    return BT_ERR_INVALID_ARG;
+  if (!aligned16(x)) return BT_ERR_MISALIGNED;
+  const GemmPath path = gemm_path(bits, total_rows, K, num_experts, group_size);
+  if (path == kPathNone) return BT_OK;
+  if (path == kPathGemv) {
+    RowMap rm;
+    rm.offsets = expert_offsets;
+    rm.row_index = x_row_index;
+    rm.num_experts = num_experts;
+    rm.swiglu = swiglu;
+    return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, total_rows, rm, stream);
+  }
+  GemmParams p{};
+  p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
+  p.M = total_rows; p.N = N; p.K = K;
+  p.group = group_size;
+  p.swiglu = swiglu;
+  p.offsets = expert_offsets;
+  p.row_index = x_row_index;
+  p.num_experts = num_experts;
+  p.err = device_error_word();
+  p.timeout_ns = opts().wait_timeout_ns;
+  if (path == kPathTc && tc_supported(bits, K, total_rows, p))
+    return cuda_status(launch_gemm_tc_grouped(p, bits, x_dtype, y_dtype, stream));
+  return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
 }
 
 }  // namespace
@@ -303,8 +361,7 @@ bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (s != BT_OK) return s;
   if (!x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0,
-                  stream);
+  return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, RowMap{}, stream);
 }
 
 bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
@@ -376,8 +433,7 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
   const GemmPath path = gemm_path(bits, M, K, 0, group_size);
   if (path == kPathGemv)
-    return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, nullptr, nullptr, 0,
-                  stream);
+    return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, RowMap{}, stream);
   GemmParams p{};
   p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
   p.M = M; p.N = N; p.K = K;
@@ -393,29 +449,78 @@ bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint
                        int group_size, int num_experts, int N, int K, const int32_t* expert_offsets,
                        int total_rows, const int32_t* x_row_index, const void* x, bt_dtype x_dtype, void* y,
                        bt_dtype y_dtype, cudaStream_t stream) {
+  return moe_grouped(codes, scales, biases, bits, group_size, num_experts, N, K, expert_offsets, total_rows,
+                     x_row_index, x, x_dtype, y, y_dtype, 0, stream);
+}
+
+bt_status bt_moe_qgemm_swiglu(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                              int group_size, int num_experts, int N, int K, const int32_t* expert_offsets,
+                              int total_rows, const int32_t* x_row_index, const void* x, bt_dtype x_dtype, void* h,
+                              bt_dtype h_dtype, cudaStream_t stream) {
+  if (N % 2) return BT_ERR_INVALID_ARG;
+  return moe_grouped(codes, scales, biases, bits, group_size, num_experts, N, K, expert_offsets, total_rows,
+                     x_row_index, x, x_dtype, h, h_dtype, 1, stream);
+}
+
+bt_status bt_moe_qgemv_pairs(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                             int group_size, int num_experts, int N, int K, const int32_t* topk_ids, int tokens,
+                             int top_k, const void* x, bt_dtype x_dtype, void* y, bt_dtype y_dtype, int swiglu,
+                             cudaStream_t stream) {
   bt_status s = check_weights(codes, scales, biases, bits, group_size, N, K);
   if (s != BT_OK) return s;
-  if (num_experts <= 0 || num_experts > 4096 || total_rows < 0 || !expert_offsets || !x || !y ||
-      !half_dtype(x_dtype) || !out_dtype(y_dtype))
+  if (num_experts <= 0 || num_experts > 4096 || tokens < 0 || top_k < 1 || top_k > 32 || !x || !y || !topk_ids ||
+      !half_dtype(x_dtype) || !out_dtype(y_dtype) || (swiglu && N % 2))
     return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  const GemmPath path = gemm_path(bits, total_rows, K, num_experts, group_size);
-  if (path == kPathNone) return BT_OK;
-  if (path == kPathGemv)
-    return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, total_rows,
-                    expert_offsets, x_row_index, num_experts, stream);
-  GemmParams p{};
-  p.codes = codes; p.scales = scales; p.biases = biases; p.x = x; p.y = y;
-  p.M = total_rows; p.N = N; p.K = K;
-  p.group = group_size;
-  p.offsets = expert_offsets;
-  p.row_index = x_row_index;
+  if ((long long)tokens * top_k > (1LL << 30)) return BT_ERR_UNSUPPORTED;
+  if (tokens == 0) return BT_OK;
+  RowMap rm;
+  rm.pair_ids = topk_ids;
+  rm.top_k = top_k;
+  rm.num_experts = num_experts;
+  rm.swiglu = swiglu ? 1 : 0;
+  return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, tokens * top_k, rm, stream);
+}
+
+bt_status bt_moe_down_combine(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                              int group_size, int num_experts, int N, int K, const int32_t* topk_ids,
+                              const float* gates, int tokens, int top_k, const void* h, bt_dtype h_dtype,
+                              void* out, bt_dtype o_dtype, cudaStream_t stream) {
+  bt_status s = check_weights(codes, scales, biases, bits, group_size, N, K);
+  if (s != BT_OK) return s;
+  if (num_experts <= 0 || num_experts > 4096 || tokens < 0 || top_k < 1 || top_k > 32 || !topk_ids || !gates ||
+      !h || !out || !half_dtype(h_dtype) || !out_dtype(o_dtype))
+    return BT_ERR_INVALID_ARG;
+  if (!aligned16(h)) return BT_ERR_MISALIGNED;
+  if (tokens == 0) return BT_OK;
+  // every segment copy (one expert's rows) must start and end on 16 bytes
+  const long long seg_rb = (long long)K * bits / 8, seg_pb = 2LL * param_groups(bits, K, group_size);
+  if ((N * seg_rb) % 16 || (N * seg_pb) % 16 || (long long)top_k * K > kMaxK) return BT_ERR_UNSUPPORTED;
+  const int ktot = top_k * K;
+  GemvParams p{};
+  p.codes = codes;
+  p.scales = scales;
+  p.biases = biases;
+  p.x = h;
+  p.y = out;
+  p.N = N;
+  p.K = ktot;
+  p.G = param_groups(bits, ktot, group_size);
+  p.gshift = group_shift(group_size);
   p.num_experts = num_experts;
+  p.seg_ids = topk_ids;
+  p.seg_gates = gates;
+  p.nseg = top_k;
+  p.seg_k = K;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
-  if (path == kPathTc && tc_supported(bits, K, total_rows, p))
-    return cuda_status(launch_gemm_tc_grouped(p, bits, x_dtype, y_dtype, stream));
-  return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
+  p.const_weights = opts().pdl && opts().const_weights;
+  p.drop_stage = opts().test_drop_stage;
+  opts().test_drop_stage = 0;
+  const GemvPlan pl = plan_gemv(bits, gemv_fast_path(bits, h_dtype), N, ktot, tokens, 0, sm_count(), group_size,
+                                false, top_k);
+  if (!pl.feasible) return BT_ERR_UNSUPPORTED;
+  return cuda_status(launch_gemv(p, pl, bits, h_dtype, o_dtype, stream));
 }
 
 bt_status bt_moe_route(const int32_t* topk_ids, int tokens, int top_k, int num_experts, int32_t* expert_offsets,

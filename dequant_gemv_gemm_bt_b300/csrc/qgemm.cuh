@@ -16,6 +16,7 @@ struct GemmParams {
   void* y;
   int M, N, K;
   int group;                 // quantization group size along K: 32, 64 or 128
+  int swiglu;                // epilogue: rows 2i/2i+1 are gate_i/up_i; Y is [M, N/2], silu(gate) * up
   const int32_t* offsets;
   const int32_t* row_index;
   int num_experts;

@@ -113,7 +113,16 @@ __global__ void __launch_bounds__(NT) qgemm_simt_kernel(const GemmParams p) {
     __syncthreads();
   }
   const int n = n0 + tx;
-  if (n < p.N) {
+  if (p.swiglu) {
+    // gate row (even tx) and its up row (tx + 1: the next lane of the same warp)
+#pragma unroll
+    for (int i = 0; i < TM / 4; ++i) {
+      const float up = __shfl_xor_sync(0xffffffffu, acc[i], 1);
+      const int m = m0 + ty + 4 * i;
+      if (!(tx & 1) && n < p.N && m < m1)
+        store_out<YD>(p.y, (size_t)m * (p.N / 2) + (n >> 1), acc[i] / (1.f + expf(-acc[i])) * up);
+    }
+  } else if (n < p.N) {
 #pragma unroll
     for (int i = 0; i < TM / 4; ++i) {
       const int m = m0 + ty + 4 * i;

@@ -78,6 +78,7 @@ struct TcParams {
   const uint16_t* biases;
   void* y;
   bt_dtype y_dtype;
+  int swiglu;                 // epilogue: rows 2i/2i+1 = gate_i/up_i -> Y [M, N/2] = silu(gate) * up
   unsigned* err;
   unsigned long long timeout_ns;
   // grouped experts
@@ -650,7 +651,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 16 * half_sel; c0 < BN; c0 += 32) {
         uint32_t v[16];
         tmem_ld16(taddr_row + (uint32_t)c0, v);
-        if (ok && n < p.N) {
+        if (p.swiglu) {
+          // gate row (even TMEM lane) and its up row (the next lane, same warp)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float gt = __uint_as_float(v[j]);
+            const float up = __shfl_xor_sync(0xffffffffu, gt, 1);
+            const int m = m0 + c0 + j;
+            if (ok && !(row & 1) && n < p.N && m < m_end)
+              store_y(p, (size_t)m * (p.N / 2) + (n >> 1), gt / (1.f + expf(-gt)) * up);
+          }
+        } else if (ok && n < p.N) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
@@ -830,6 +841,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.biases = gp.biases;
   p.y = gp.y;
   p.y_dtype = yd;
+  p.swiglu = gp.swiglu;
   p.err = gp.err;
   p.timeout_ns = gp.timeout_ns;
   p.x = gp.x;

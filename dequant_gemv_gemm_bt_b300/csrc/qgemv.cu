@@ -22,7 +22,8 @@ constexpr int kRingBudget = 176 * 1024;
 constexpr size_t kMaxSmem = 227 * 1024;   // opt-in dynamic shared memory per block on sm_100/sm_103
 }  // namespace
 
-GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group) {
+GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group,
+                   bool pair_rows, int nseg) {
   GemvPlan pl{};
   pl.fast = fast;
   const int nchunks = K / 32;
@@ -53,9 +54,10 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   const int G = param_groups(bits, K, group);
   const int row_bytes = K * bits / 8;
   const int per_row = row_bytes + 4 * G;
-  // smallest row multiple that keeps every bulk copy a multiple of 16 bytes (a power of two)
+  // smallest row multiple that keeps every bulk copy a multiple of 16 bytes (a power of two);
+  // with K segments every segment is its own copy
   int m = 1;
-  while (((m * row_bytes) & 15) || ((m * G * 2) & 15)) m *= 2;
+  while (((m * (row_bytes / nseg)) & 15) || ((m * (G / nseg) * 2) & 15)) m *= 2;
   // rows in flight per warp: as many as the stage budget and the per-SM row count allow
   const long long rows_total = (long long)N * problems;
   const long long per_sm = std::max<long long>(1, (rows_total + sms - 1) / sms);
@@ -65,7 +67,10 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   int ri = pl.cpl == 1 ? 8 : (pl.cpl == 2 ? 2 : 1);
   if (opts().gemv_ri > 0) ri = pl.cpl == 1 ? std::min(8, opts().gemv_ri) : std::min(ri, opts().gemv_ri);
   int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
-  while (ri > 1 && ((long long)ri * rw * per_row > stage_budget || ri * rw > std::max<long long>(rw, per_sm))) ri /= 2;
+  const int ri_min = pair_rows ? 2 : 1;   // the SwiGLU epilogue pairs rows 2i, 2i+1
+  while (ri > ri_min &&
+         ((long long)ri * rw * per_row > stage_budget || ri * rw > std::max<long long>(rw, per_sm)))
+    ri /= 2;
   pl.ri = ri;
   const int ctas_per_sm = gemv_ctas_per_sm(pl.cpl, ri);   // must match the kernel's launch bounds
   // two stages of every resident CTA fit the SM's shared memory

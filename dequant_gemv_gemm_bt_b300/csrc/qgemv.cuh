@@ -34,6 +34,21 @@ struct GemvParams {
   int xsum_bytes;
   // quantization group of 32-code chunk c is c >> gshift (group size 32 << gshift)
   int gshift;
+  // routed pairs (decode without a sort): problem r is pair r of a [tokens, top_k]
+  // routing, expert pair_ids[r], x row r / top_k, output row r
+  const int32_t* pair_ids;
+  int top_k;
+  // SwiGLU epilogue: weight rows interleaved (2i gate_i, 2i+1 up_i); the output
+  // row holds N/2 values h_i = silu(gate_i . x) * (up_i . x)
+  int swiglu;
+  // K-segmented problems (expert down products summed into each token's output):
+  // problem t's K is nseg segments of seg_k codes; segment s uses expert
+  // seg_ids[t*nseg + s] and x segment seg_gates[t*nseg + s] * x[t*nseg + s]
+  // (x holds the nseg rows of a token back to back).  N, G and row_bytes above
+  // are then the totals over the segments.
+  const int32_t* seg_ids;
+  const float* seg_gates;
+  int nseg, seg_k;
 };
 
 // Batched launches: many independent GEMVs of the same bits and dtypes, each
@@ -84,7 +99,10 @@ MmaShape mma_shape(int cfg);   // cfg 0: the default shape
 // or 0 for fp16 weights (bits = 16), which have none.
 inline int param_groups(int bits, int K, int group) { return bits == 16 ? 0 : K / group; }
 
-GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group = 64);
+// pair_rows: the launch's epilogue combines rows 2i and 2i+1 (SwiGLU), so at
+// least two rows are in flight per warp.
+GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group = 64,
+                   bool pair_rows = false, int nseg = 1);
 // The tensor-pipe kernel's plan for the same arguments (infeasible when it does
 // not apply: 4-bit codes, fp16 x, dense, K <= 8192, every unit 16-byte aligned).
 GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms,

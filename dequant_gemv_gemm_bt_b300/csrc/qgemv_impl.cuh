@@ -300,7 +300,7 @@ __device__ __forceinline__ float chunk_dot_stream(const uint32_t (&w)[BITS], con
 }
 
 template <int BITS, bt_dtype XD>
-__device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_t* xk) {
+__device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_t* xk, float xscale = 1.f) {
   // xk: 32 consecutive x values (16-B aligned) of this chunk
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -311,6 +311,11 @@ __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_
       s.xh[8 * i + 2 * j] = u[j] & 0xFFFF;
       s.xh[8 * i + 2 * j + 1] = u[j] >> 16;
     }
+  }
+  if (xscale != 1.f) {   // a gate-weighted x segment: xscale * x, rounded to fp16 once
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      s.xh[j] = __half_as_ushort(__float2half_rn(xscale * __half2float(__ushort_as_half(s.xh[j]))));
   }
   if constexpr (BITS == 16) {
     s.xsum = 0.f;   // fp16 weights: no bias term
@@ -341,7 +346,7 @@ __device__ __forceinline__ void load_x_fast(XSlice<BITS, true>& s, const uint16_
 }
 
 template <int BITS, bt_dtype XD>
-__device__ __forceinline__ void load_x_generic(XSlice<BITS, false>& s, const uint16_t* xk) {
+__device__ __forceinline__ void load_x_generic(XSlice<BITS, false>& s, const uint16_t* xk, float xscale = 1.f) {
   float xsum = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -349,8 +354,8 @@ __device__ __forceinline__ void load_x_generic(XSlice<BITS, false>& s, const uin
     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      s.xv[8 * i + 2 * j] = to_f32<XD>(u[j] & 0xFFFF);
-      s.xv[8 * i + 2 * j + 1] = to_f32<XD>(u[j] >> 16);
+      s.xv[8 * i + 2 * j] = xscale * to_f32<XD>(u[j] & 0xFFFF);
+      s.xv[8 * i + 2 * j + 1] = xscale * to_f32<XD>(u[j] >> 16);
     }
   }
 #pragma unroll
@@ -430,6 +435,12 @@ __device__ __forceinline__ float chunk_dot_generic(const uint32_t (&w)[BITS], co
 // Grouped row `prob` belongs to the expert e with off[e] <= prob < off[e+1]
 // (offsets cached in shared memory); -1 when no expert holds it.
 __device__ __forceinline__ int problem_expert(const GemvParams& p, const int* offs, int prob) {
+  if (p.pair_ids) {   // routed pair: its expert id, or -1 (and a device error) when out of range
+    const int e = __ldg(p.pair_ids + prob);
+    if (e >= 0 && e < p.num_experts) return e;
+    set_device_error(p.err, kErrBadArg);
+    return -1;
+  }
   if (!p.moe_offsets) return 0;
   int lo = 0, hi = p.num_experts;   // invariant: offs[lo] <= prob, answer in [lo, hi)
   if (prob < offs[0] || prob >= offs[p.num_experts]) return -1;
@@ -440,10 +451,13 @@ __device__ __forceinline__ int problem_expert(const GemvParams& p, const int* of
   return lo;
 }
 __device__ __forceinline__ int problem_xrow(const GemvParams& p, int prob) {
+  if (p.pair_ids) return prob / p.top_k;
   if (!p.moe_offsets) return 0;
   return p.row_index ? __ldg(p.row_index + prob) : prob;
 }
-__device__ __forceinline__ int problem_yrow(const GemvParams& p, int prob) { return p.moe_offsets ? prob : 0; }
+__device__ __forceinline__ int problem_yrow(const GemvParams& p, int prob) {
+  return (p.moe_offsets || p.pair_ids) ? prob : 0;
+}
 
 
 // --------------------------------------------------------------- the kernel
@@ -538,9 +552,10 @@ struct ProbView {
   int kw;                    // warps that share one row (K split)
   int rb;                    // rows per pipeline unit
   bool valid;                // false: a grouped row that no expert holds (skipped)
+  int nseg, seg_rb, seg_g;   // K segments (1 unless segmented), bytes and groups of one segment's row
 };
 
-template <bool BATCH>
+template <bool BATCH, bool SEG = false>
 __device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch<BATCH ? kBatchCap : 1>& batch,
                                             const int* offs, int prob) {
   ProbView v;
@@ -560,6 +575,35 @@ __device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch
     v.kw = q.kw;
     v.rb = q.rb;
     v.valid = true;
+    v.nseg = 1;
+    v.seg_rb = q.row_bytes;
+    v.seg_g = q.g;
+  } else if constexpr (SEG) {
+    // segmented token problem: the weights' bases are expert 0's (the producer adds
+    // each segment's expert plane); x is the token's nseg rows back to back
+    v.codes = reinterpret_cast<const uint8_t*>(p.codes);
+    v.scales = p.scales;
+    v.biases = p.biases;
+    v.x = static_cast<const uint16_t*>(p.x) + (size_t)prob * p.K;
+    v.y = p.y;
+    v.y0 = (size_t)prob * p.N;
+    v.n = p.N;
+    v.units = p.units_per_problem;
+    v.k = p.K;
+    v.g = p.G;
+    v.row_bytes = p.row_bytes;
+    v.kw = p.kw;
+    v.rb = p.rows_per_unit;
+    v.nseg = p.nseg;
+    v.seg_rb = p.row_bytes / p.nseg;
+    v.seg_g = p.G / p.nseg;
+    bool ok = true;   // every segment's expert id in range (each thread checks all of them)
+    for (int s = 0; s < p.nseg; ++s) {
+      const int e = __ldg(p.seg_ids + (size_t)prob * p.nseg + s);
+      ok = ok && e >= 0 && e < p.num_experts;
+    }
+    if (!ok) set_device_error(p.err, kErrBadArg);
+    v.valid = ok;
   } else {
     const int e = problem_expert(p, offs, prob);
     const size_t e_rows = (size_t)(e < 0 ? 0 : e) * p.N;
@@ -568,7 +612,7 @@ __device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch
     v.biases = p.biases + e_rows * p.G;
     v.x = static_cast<const uint16_t*>(p.x) + (size_t)problem_xrow(p, prob) * p.K;
     v.y = p.y;
-    v.y0 = (size_t)problem_yrow(p, prob) * p.N;
+    v.y0 = (size_t)problem_yrow(p, prob) * (p.swiglu ? p.N / 2 : p.N);
     v.n = p.N;
     v.units = p.units_per_problem;
     v.k = p.K;
@@ -577,6 +621,9 @@ __device__ __forceinline__ ProbView resolve(const GemvParams& p, const GemvBatch
     v.kw = p.kw;
     v.rb = p.rows_per_unit;
     v.valid = e >= 0;
+    v.nseg = 1;
+    v.seg_rb = p.row_bytes;
+    v.seg_g = p.G;
   }
   return v;
 }
@@ -627,7 +674,7 @@ __device__ __forceinline__ long long unit_at_cost(const GemvParams& p, const Gem
   return lo + 1 < batch.count ? batch.prob[lo + 1].unit_begin : p.num_units;
 }
 
-template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH, bool SEG>
 __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMinBlocks)
     qgemv_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
   constexpr int kNW = Warps<CPL, RI>::kNW;
@@ -675,17 +722,17 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
     // Lane 0 moves a unit's packed codes with one bulk copy (large copies keep
     // the copy engine streaming); all 32 lanes move its fp16 scales and biases
     // with 16-byte cp.async, whose completion the same mbarrier tracks.
-    if (!p.const_weights) pdl_wait();
+    if (!p.const_weights || p.pair_ids) pdl_wait();   // routed pairs: expert ids may come from the previous kernel
     const uint64_t pol = l2_policy_evict_first();
     int prob, blk;
     first_unit<BATCH>(p, batch, u_begin, prob, blk);
-    ProbView v = resolve<BATCH>(p, batch, offs, prob);
+    ProbView v = resolve<BATCH, SEG>(p, batch, offs, prob);
     int s = 0;
     uint32_t ph = 0;
     long long it = 0;
     bool ok = true;
     for (long long u = u_begin; u < u_end; ++u, ++it) {
-      if (blk == v.units) { blk = 0; ++prob; v = resolve<BATCH>(p, batch, offs, prob); }
+      if (blk == v.units) { blk = 0; ++prob; v = resolve<BATCH, SEG>(p, batch, offs, prob); }
       if (it >= S) {
         bool w = true;
         if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
@@ -695,7 +742,35 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
       const int row0 = blk * RB;
       const int rows = min(RB, v.n - row0);
       const bool drop = p.drop_stage && blockIdx.x == 0 && it == 0;   // test hook: never fill this stage
-      if (!drop) {
+      if constexpr (SEG) if (!drop) {
+        // K segments: one bulk copy of each segment's rows (from its expert's plane)
+        // and its parameters; the host plans every copy 16-byte aligned
+        if (v.valid) {
+          const uint32_t segc = (uint32_t)rows * v.seg_rb, segs = (uint32_t)rows * v.seg_g * 2;
+          uint8_t* st = smem + (size_t)s * p.stage_bytes;
+          uint8_t* ss = st + (size_t)RB * row_bytes;
+          uint8_t* sbb = ss + (size_t)RB * G * 2;
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], segc * v.nseg);
+          for (int sg = 0; sg < v.nseg; ++sg) {
+            const size_t er = (size_t)__ldg(p.seg_ids + (size_t)prob * v.nseg + sg) * v.n + row0;
+            if (lane == 0)
+              bulk_g2s(st + (size_t)sg * RB * v.seg_rb, v.codes + er * v.seg_rb, segc, &full[s], pol);
+            const uint8_t* gs = reinterpret_cast<const uint8_t*>(v.scales + er * v.seg_g);
+            const uint8_t* gb = reinterpret_cast<const uint8_t*>(v.biases + er * v.seg_g);
+            uint8_t* ds = ss + (size_t)sg * RB * v.seg_g * 2;
+            uint8_t* db = sbb + (size_t)sg * RB * v.seg_g * 2;
+            for (uint32_t o = lane * 16u; o < segs; o += 32u * 16u) {
+              cp_async16(ds + o, gs + o);
+              cp_async16(db + o, gb + o);
+            }
+          }
+          cp_async_mbar_arrive_noinc(&full[s]);
+        } else {
+          mbar_arrive(&full[s]);
+          if (lane == 0) mbar_arrive(&full[s]);
+        }
+      }
+      if constexpr (!SEG) if (!drop) {
         if (v.valid && unit_bulk(p, v, row0, rows)) {
           const uint32_t cbytes = (uint32_t)rows * row_bytes, sbytes = (uint32_t)rows * G * 2;
           uint8_t* st = smem + (size_t)s * p.stage_bytes;
@@ -740,6 +815,10 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
   pdl_wait();   // activations (and offsets) may come from the previous kernel
 
   XSlice<BITS, FAST> xs[CPL];
+  // per x chunk of this lane: byte offset of its codes in a staged row of the
+  // unit and index of its parameters (one segment: c * chunk bytes and the
+  // chunk's group; K segments: inside its segment's block of the stage)
+  int coff[CPL], poff[CPL];
   bool dead = false;   // this warp gave up on a wait, or saw another warp of the CTA give up
   int rbuf = 0;
   int prob, blk;
@@ -752,7 +831,7 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
     if (cur_prob >= 0 && blk == v.units) { blk = 0; ++prob; }
     if (prob != cur_prob) {
       cur_prob = prob;
-      v = resolve<BATCH>(p, batch, offs, prob);
+      v = resolve<BATCH, SEG>(p, batch, offs, prob);
       if (v.kw != KW) {
         if (v.kw < 1 || kNW % v.kw) {   // never planned so; refuse rather than spin
           if (threadIdx.x == 0) set_device_error(p.err, kErrBadArg);
@@ -768,12 +847,20 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
         rbuf = 0;
       }
       nchunks = v.k / 32;
+      const int cps = SEG ? nchunks / v.nseg : nchunks;   // 32-code chunks per segment
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = (i * KW + kw) * 32 + lane;
         if (c < nchunks) {
-          if constexpr (FAST) load_x_fast<BITS, XD>(xs[i], v.x + (size_t)c * 32);
-          else load_x_generic<BITS, XD>(xs[i], v.x + (size_t)c * 32);
+          float xscale = 1.f;
+          if constexpr (SEG) {
+            const int sg = c / cps, cc = c - sg * cps;
+            coff[i] = sg * v.rb * v.seg_rb + cc * (4 * BITS);
+            poff[i] = sg * v.rb * v.seg_g + (cc >> p.gshift);
+            xscale = __ldg(p.seg_gates + (size_t)prob * v.nseg + sg);
+          }
+          if constexpr (FAST) load_x_fast<BITS, XD>(xs[i], v.x + (size_t)c * 32, xscale);
+          else load_x_generic<BITS, XD>(xs[i], v.x + (size_t)c * 32, xscale);
         }
       }
     }
@@ -784,13 +871,15 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
     const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
     const int row0 = blk * RB;
     const int rows = min(RB, v.n - row0);
-    const bool tma = v.valid && unit_bulk(p, v, row0, rows);
+    const bool tma = v.valid && (SEG || unit_bulk(p, v, row0, rows));
+    // row strides of codes (bytes) and parameters (halves) in a staged unit
+    const int crs = SEG ? v.seg_rb : row_bytes, prs = SEG ? v.seg_g : G;
     const uint32_t st = smem_u32(smem + (size_t)s * p.stage_bytes);
     const uint32_t st_sc = st + RB * row_bytes, st_bi = st_sc + RB * G * 2;
     const uint8_t* g_codes = v.codes + (size_t)row0 * row_bytes;
     const uint16_t* g_sc = v.scales + (size_t)row0 * G;
     const uint16_t* g_bi = v.biases + (size_t)row0 * G;
-    const size_t ybase = v.y0 + row0;
+    const size_t ybase = v.y0 + (p.swiglu ? row0 / 2 : row0);
 
     const int nb = (rows + RI - 1) / RI;
     // The row batches of this unit.  Instantiated per (rows need clamping, unit
@@ -813,21 +902,22 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
         if (LIVE && c < nchunks) {
           uint32_t w[RI][BITS];
           float sc[RI], bs[RI];
-          const int grp = c >> p.gshift;   // quantization group of this 32-code chunk
+          const int co = SEG ? coff[i] : c * (4 * BITS);   // this chunk's codes in a staged row
+          const int po = SEG ? poff[i] : (c >> p.gshift);   // and its parameters' index
 #pragma unroll
           for (int j = 0; j < RI; ++j) {
             const int r = CLAMP ? min(r0 + j, rows - 1) : r0 + j;
             if constexpr (STAGED) {
-              load_chunk<BITS, true>(st + r * row_bytes + c * (4 * BITS), nullptr, w[j]);
+              load_chunk<BITS, true>(st + co + r * crs, nullptr, w[j]);
               if constexpr (BITS != 16) {
-                sc[j] = to_f32<BT_F16>(lds16(st_sc + (r * G + grp) * 2));
-                bs[j] = to_f32<BT_F16>(lds16(st_bi + (r * G + grp) * 2));
+                sc[j] = to_f32<BT_F16>(lds16(st_sc + (po + r * prs) * 2));
+                bs[j] = to_f32<BT_F16>(lds16(st_bi + (po + r * prs) * 2));
               }
-            } else {
-              load_chunk<BITS, false>(0, g_codes + (size_t)r * row_bytes + c * (4 * BITS), w[j]);
+            } else {   // one segment only (segmented units are always staged)
+              load_chunk<BITS, false>(0, g_codes + (size_t)r * crs + co, w[j]);
               if constexpr (BITS != 16) {
-                sc[j] = to_f32<BT_F16>(__ldg(g_sc + (size_t)r * G + grp));
-                bs[j] = to_f32<BT_F16>(__ldg(g_bi + (size_t)r * G + grp));
+                sc[j] = to_f32<BT_F16>(__ldg(g_sc + (size_t)r * prs + po));
+                bs[j] = to_f32<BT_F16>(__ldg(g_bi + (size_t)r * prs + po));
               }
             }
           }
@@ -844,16 +934,31 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
       int rj;
       const float val = reduce_rows<RI>(part, lane, rj);
       const int r = r0 + rj;
+      // Store a row's result; with the SwiGLU epilogue the gate row (even) takes
+      // its up row (odd, the lane 32/RI away) and stores silu(gate) * up.
+      auto emit = [&](float y) {
+        if (!BATCH && p.swiglu) {
+          if constexpr (RI >= 2) {
+            const float up = __shfl_xor_sync(0xffffffffu, y, 32 / RI);
+            if (LIVE && writer && !(rj & 1) && r < rows && v.valid)
+              store_yv(p, v.y, ybase + (r >> 1), y / (1.f + expf(-y)) * up);
+          } else if (threadIdx.x == 0) {
+            set_device_error(p.err, kErrBadArg);   // never planned: row pairs need two rows in flight
+          }
+        } else if (LIVE && writer && r < rows && v.valid) {
+          store_yv(p, v.y, ybase + r, y);
+        }
+      };
       if (KW == 1) {
-        if (LIVE && writer && r < rows && v.valid) store_yv(p, v.y, ybase + r, val);
+        emit(val);
       } else {
         float* rb = red + (size_t)((rg * 2 + rbuf) * RI) * KW;   // [RI][KW]
         if (writer) rb[rj * KW + kw] = val;
         asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
-        if (LIVE && kw == 0 && writer && r < rows && v.valid) {
+        if (kw == 0) {   // warp-uniform: the whole warp sums (the SwiGLU shuffle needs every lane)
           float acc = 0.f;
           for (int j = 0; j < KW; ++j) acc += rb[rj * KW + j];
-          store_yv(p, v.y, ybase + r, acc);
+          emit(acc);
         }
         rbuf ^= 1;
       }
@@ -861,7 +966,7 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
     };
     using yes = std::integral_constant<bool, true>;
     using no = std::integral_constant<bool, false>;
-    if (dead) {
+    if (dead || (SEG && !v.valid)) {   // nothing to read: walk the batches and barriers only
       batches(yes{}, no{}, no{});
     } else if (tma) {
       if (rows == nb * RI) batches(no{}, yes{}, yes{});
@@ -879,10 +984,10 @@ __global__ void __launch_bounds__(Warps<CPL, RI>::kThreads, Warps<CPL, RI>::kMin
 }
 
 // ------------------------------------------------------------------ launch
-template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH>
+template <int BITS, bt_dtype XD, int CPL, bool FAST, int RI, bool BATCH, bool SEG>
 cudaError_t launch_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int grid, size_t smem,
                      cudaStream_t stream) {
-  auto k = qgemv_kernel<BITS, XD, CPL, FAST, RI, BATCH>;
+  auto k = qgemv_kernel<BITS, XD, CPL, FAST, RI, BATCH, SEG>;
   static std::atomic<uint64_t> smem_raised{0};
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
@@ -904,46 +1009,49 @@ cudaError_t launch_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int
   }
 }
 
-template <int BITS, bt_dtype XD, int CPL, bool FAST, bool BATCH>
+template <int BITS, bt_dtype XD, int CPL, bool FAST, bool BATCH, bool SEG>
 cudaError_t launch_ri(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b, cudaStream_t st) {
   switch (pl.ri) {
     case 8:
-      if constexpr (CPL == 1) return launch_t<BITS, XD, CPL, FAST, 8, BATCH>(p, b, pl.grid, pl.smem, st);
+      if constexpr (CPL == 1) return launch_t<BITS, XD, CPL, FAST, 8, BATCH, SEG>(p, b, pl.grid, pl.smem, st);
       [[fallthrough]];
-    case 4: return launch_t<BITS, XD, CPL, FAST, 4, BATCH>(p, b, pl.grid, pl.smem, st);
-    case 2: return launch_t<BITS, XD, CPL, FAST, 2, BATCH>(p, b, pl.grid, pl.smem, st);
-    default: return launch_t<BITS, XD, CPL, FAST, 1, BATCH>(p, b, pl.grid, pl.smem, st);
+    case 4: return launch_t<BITS, XD, CPL, FAST, 4, BATCH, SEG>(p, b, pl.grid, pl.smem, st);
+    case 2: return launch_t<BITS, XD, CPL, FAST, 2, BATCH, SEG>(p, b, pl.grid, pl.smem, st);
+    default: return launch_t<BITS, XD, CPL, FAST, 1, BATCH, SEG>(p, b, pl.grid, pl.smem, st);
   }
 }
 
-template <int BITS, bt_dtype XD, bool FAST, bool BATCH>
+template <int BITS, bt_dtype XD, bool FAST, bool BATCH, bool SEG>
 cudaError_t launch_cpl(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b, cudaStream_t st) {
   switch (pl.cpl) {
-    case 1: return launch_ri<BITS, XD, 1, FAST, BATCH>(p, pl, b, st);
-    case 2: return launch_ri<BITS, XD, 2, FAST, BATCH>(p, pl, b, st);
+    case 1: return launch_ri<BITS, XD, 1, FAST, BATCH, SEG>(p, pl, b, st);
+    case 2: return launch_ri<BITS, XD, 2, FAST, BATCH, SEG>(p, pl, b, st);
     // three or four chunks per lane: fast path of bits 2/4/8 only (K up to 32768)
-    case 3: if constexpr (FAST && kWideBits<BITS>) return launch_ri<BITS, XD, 3, FAST, BATCH>(p, pl, b, st); else break;
-    case 4: if constexpr (FAST && kWideBits<BITS>) return launch_ri<BITS, XD, 4, FAST, BATCH>(p, pl, b, st); else break;
+    case 3: if constexpr (FAST && kWideBits<BITS> && !SEG) return launch_ri<BITS, XD, 3, FAST, BATCH, SEG>(p, pl, b, st); else break;
+    case 4: if constexpr (FAST && kWideBits<BITS> && !SEG) return launch_ri<BITS, XD, 4, FAST, BATCH, SEG>(p, pl, b, st); else break;
   }
   return cudaErrorInvalidValue;
 }
 
-template <int BITS, bool BATCH>
+template <int BITS, bool BATCH, bool SEG>
 cudaError_t launch_bits_b(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, const GemvBatch<kBatchCap>* b,
                           cudaStream_t st) {
   if (xd == BT_F16) {
     if constexpr (kHasFast<BITS>)
-      if (pl.fast) return launch_cpl<BITS, BT_F16, true, BATCH>(p, pl, b, st);
-    return launch_cpl<BITS, BT_F16, false, BATCH>(p, pl, b, st);
+      if (pl.fast) return launch_cpl<BITS, BT_F16, true, BATCH, SEG>(p, pl, b, st);
+    return launch_cpl<BITS, BT_F16, false, BATCH, SEG>(p, pl, b, st);
   }
-  return launch_cpl<BITS, BT_BF16, false, BATCH>(p, pl, b, st);
+  return launch_cpl<BITS, BT_BF16, false, BATCH, SEG>(p, pl, b, st);
 }
 
+// K-segmented token problems (a fused down product + combine) run their own
+// instantiations, so the others carry none of the segment bookkeeping.
 template <int BITS>
 cudaError_t launch_bits(const GemvParams& p, const GemvPlan& pl, bt_dtype xd, const GemvBatch<kBatchCap>* b,
                         cudaStream_t st) {
-  if (b) return launch_bits_b<BITS, true>(p, pl, xd, b, st);
-  return launch_bits_b<BITS, false>(p, pl, xd, nullptr, st);
+  if (b) return launch_bits_b<BITS, true, false>(p, pl, xd, b, st);
+  if (p.seg_ids) return launch_bits_b<BITS, false, true>(p, pl, xd, nullptr, st);
+  return launch_bits_b<BITS, false, false>(p, pl, xd, nullptr, st);
 }
 
 }  // namespace gemv

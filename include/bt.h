@@ -154,6 +154,77 @@ BT_API bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, con
                        void* y, bt_dtype y_dtype, cudaStream_t stream);
 
 /*
+ * Grouped expert product with the SwiGLU epilogue fused into its store: the
+ * gate and up products of an expert layer in one launch whose output is
+ * already the activation h = silu(gate . x) * (up . x).  BaseRT pages,
+ * gist.science "Metodologia" (fusing two kernels saves a dispatch and a trip
+ * through memory); thetesserapress.com "Where the wins land, and where they
+ * don't" (the expert layers).
+ *   codes/scales/biases  experts stacked [E][N][...] with N = 2*I rows in
+ *                        interleaved order: row 2i is gate row i, row 2i+1 is
+ *                        up row i (so every gate/up pair is produced together)
+ *   expert_offsets, total_rows, x_row_index, x   as bt_moe_qgemm
+ *   h     [total_rows, I] of h_dtype (BT_F32, BT_BF16 or BT_F16), grouped order
+ * Runs on the GEMV (at most one row per expert), the tensor cores or the
+ * CUDA-core tile like bt_moe_qgemm; silu is evaluated in fp32 on the fp32
+ * accumulators.  Errors: BT_ERR_INVALID_ARG for an odd N, otherwise as
+ * bt_moe_qgemm.
+ */
+BT_API bt_status bt_moe_qgemm_swiglu(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                                     int bits, int group_size, int num_experts, int N, int K,
+                                     const int32_t* expert_offsets, int total_rows, const int32_t* x_row_index,
+                                     const void* x, bt_dtype x_dtype, void* h, bt_dtype h_dtype,
+                                     cudaStream_t stream);
+
+/*
+ * Expert products of routed (token, slot) pairs at decode, without a sort: pair
+ * r = t*top_k + s uses expert topk_ids[r] and x row t, and writes output row r
+ * (pair order).  The experts a token picked are data read on the device, so no
+ * host code forks on them (thetesserapress.com "Where the wins land, and where
+ * they don't"; gist.science "Contribuições").  With swiglu != 0 the weight rows
+ * are gate/up interleaved as in bt_moe_qgemm_swiglu and the output rows hold
+ * N/2 activations.
+ *   topk_ids  device int32 [tokens, top_k], each in [0, E); an id out of range
+ *             sets the device error word (BT_ERR_INVALID_ARG from
+ *             bt_last_device_error) and its pair's output is not written
+ *   x         [tokens, K] of x_dtype;  y [tokens*top_k, N or N/2] of y_dtype
+ * Runs on the GEMV kernel only: BT_ERR_UNSUPPORTED when no GEMV plan fits
+ * (K above the GEMV's limit for the width).  Limits: 1 <= top_k <= 32.
+ */
+BT_API bt_status bt_moe_qgemv_pairs(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
+                                    int group_size, int num_experts, int N, int K, const int32_t* topk_ids,
+                                    int tokens, int top_k, const void* x, bt_dtype x_dtype, void* y,
+                                    bt_dtype y_dtype, int swiglu, cudaStream_t stream);
+
+/*
+ * Down products of a token's routed experts with the gate-weighted combine
+ * fused into the store (decode):
+ *     out[t, n] = sum_{s < top_k} gates[t, s] * sum_k w_deq_{e(t,s)}[n, k] * h[t*top_k + s, k]
+ * with e(t, s) = topk_ids[t, s].  Each token is one product over top_k K
+ * segments, one per expert, summed inside the kernel in slot order (no
+ * atomics, deterministic).  BaseRT pages, gist.science "Metodologia" (fusing
+ * two kernels saves a dispatch and a trip through memory); thetesserapress.com
+ * "Where the wins land, and where they don't" (the expert layers).
+ *   codes/scales/biases  down weights stacked [E][N][K*bits/32], [E][N][K/g]
+ *   topk_ids  device int32 [tokens, top_k]; gates device float32 [tokens, top_k]
+ *   h         [tokens*top_k, K] of h_dtype (BT_F16 or BT_BF16), pair order (the
+ *             output of bt_moe_qgemv_pairs with the SwiGLU epilogue)
+ *   out       [tokens, N] of out_dtype
+ * Each x segment is gates[t, s] * h[t*top_k + s] (rounded once to fp16 on the
+ * fp16 path).  Every expert's weight rows are read once per token, so this is
+ * for decode; at prefill sizes run the grouped down product and
+ * bt_moe_combine.  Errors: BT_ERR_UNSUPPORTED when top_k*K exceeds the GEMV's
+ * K or an expert plane is not 16-byte sized (N*K*bits/8 or N*(K/g)*2 not a
+ * multiple of 16); ids out of range set the device error word and their
+ * token's output is not written.
+ */
+BT_API bt_status bt_moe_down_combine(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                                     int bits, int group_size, int num_experts, int N, int K,
+                                     const int32_t* topk_ids, const float* gates, int tokens, int top_k,
+                                     const void* h, bt_dtype h_dtype, void* out, bt_dtype out_dtype,
+                                     cudaStream_t stream);
+
+/*
  * Expert routing step of a mixture-of-experts layer: groups the T*top_k
  * (token, slot) pairs by expert id with a stable counting sort, so that within
  * an expert the pairs keep (token, slot) order.

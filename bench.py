@@ -516,31 +516,51 @@ def run_sweep(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     return out
 
 
-def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
-    """Qwen3-30B-A3B-shaped expert layer, Q4: route -> gate|up (grouped, gathered rows) -> SwiGLU ->
-    down (grouped) -> gate-weighted combine, at M = 1 (decode) and M = 128 (prefill).
+def interleave_rows(a, b):
+    """Two [N, .] arrays -> [2N, .] with a's row i at 2i and b's at 2i+1 (gate/up pairs)."""
+    return np.stack([a, b], axis=1).reshape(2 * a.shape[0], *a.shape[1:])
 
-    Each timed step uses a fresh routing draw (cycled from 16 seeded draws) and
-    L2 is flushed between steps (a 256 MB write outside the timed events), so
-    expert weights come from HBM.  GB/s counts the packed bytes of the experts
-    the step's routing touches.
+
+def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
+    """Qwen3-30B-A3B-shaped expert layer, Q4, at M = 1 (decode) and M = 128 (prefill).
+
+    Fused layer (the timed one):
+      M = 1:   bt_moe_qgemv_pairs (gate|up with the SwiGLU epilogue, experts read from
+               the top-k ids, no sort) -> bt_moe_down_combine (down products with the
+               gate-weighted combine in the store): 2 launches;
+      M = 128: bt_moe_route -> bt_moe_qgemm_swiglu (grouped gate|up + SwiGLU) ->
+               bt_moe_qgemm (grouped down) -> bt_moe_combine: 4 launches.
+    The unfused layer (route, gate|up, SwiGLU, down, combine: 5 launches) is timed
+    beside it.  Each timed step uses a fresh routing draw (cycled from 16 seeded
+    draws) and L2 is flushed between steps (a 256 MB write outside the timed
+    events), so expert weights come from HBM.  GB/s counts the packed bytes of the
+    experts the step's routing touches.
     """
     bits, E, H, I, top_k = 4, 128, 2048, 768, 8
     t0 = time.time()
-    gu_w = gen_weights("moe-layer-gu", [(f"e{e}", 2 * I, H) for e in range(E)], bits)
+    g_w = gen_weights("moe-layer-gate", [(f"e{e}", I, H) for e in range(E)], bits)
+    u_w = gen_weights("moe-layer-up", [(f"e{e}", I, H) for e in range(E)], bits)
     dn_w = gen_weights("moe-layer-down", [(f"e{e}", H, I) for e in range(E)], bits)
     gen_s = time.time() - t0
 
-    def stack(ws):
-        return (torch.from_numpy(np.stack([w.codes for w in ws]).view(np.int32)).to(dev),
-                torch.from_numpy(np.stack([w.scales for w in ws]).view(np.float16)).to(dev),
-                torch.from_numpy(np.stack([w.biases for w in ws]).view(np.float16)).to(dev))
-    GU, DN = stack(gu_w), stack(dn_w)
-    per_expert = weight_bytes(2 * I, H, bits) + weight_bytes(H, I, bits)
-    del gu_w, dn_w
+    def stack(arrs):
+        return torch.from_numpy(np.stack(arrs)).to(dev)
+
+    def dev_w(ws_codes, ws_s, ws_b):
+        return (stack(ws_codes).view(torch.int32), stack(ws_s).view(torch.float16), stack(ws_b).view(torch.float16))
+    # gate|up stored interleaved for the fused epilogue, concatenated for the unfused layer
+    GUI = dev_w([interleave_rows(g.codes, u.codes) for g, u in zip(g_w, u_w)],
+                [interleave_rows(g.scales, u.scales) for g, u in zip(g_w, u_w)],
+                [interleave_rows(g.biases, u.biases) for g, u in zip(g_w, u_w)])
+    GUC = dev_w([np.concatenate([g.codes, u.codes]) for g, u in zip(g_w, u_w)],
+                [np.concatenate([g.scales, u.scales]) for g, u in zip(g_w, u_w)],
+                [np.concatenate([g.biases, u.biases]) for g, u in zip(g_w, u_w)])
+    DN = dev_w([w.codes for w in dn_w], [w.scales for w in dn_w], [w.biases for w in dn_w])
+    per_expert = 2 * weight_bytes(I, H, bits) + weight_bytes(H, I, bits)
+    del g_w, u_w, dn_w
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    out = {"workload": "Qwen3-30B-A3B-shaped MoE layer: hidden 2048, 128 experts, gate/up 2048->768 (stored as one "
-                       "1536-row matrix), down 768->2048, top-8, Q4 g64", "weight_gen_s": round(gen_s, 1)}
+    out = {"workload": "Qwen3-30B-A3B-shaped MoE layer: hidden 2048, 128 experts, gate/up 2048->768, down "
+                       "768->2048, top-8, Q4 g64", "weight_gen_s": round(gen_s, 1)}
     for tokens in (1, 128):
         xdt = torch.float16 if tokens == 1 else torch.bfloat16
         draws = []
@@ -561,40 +581,54 @@ def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
                         out=torch.empty(tokens, H, device=dev, dtype=torch.float32))
             draws.append((ids_t, gates_t, x, bufs, touched))
 
-        def layer(d):
+        def fused(d):
+            ids_t, gates_t, x, b, _ = d
+            if tokens == 1:
+                bt.bt_moe_qgemv_pairs(*GUI, bits, ids_t, x, b["h"], swiglu=True)
+                bt.bt_moe_down_combine(*DN, bits, ids_t, gates_t, b["h"], b["out"])
+            else:
+                bt.bt_moe_route(ids_t, E, b["off"], b["pidx"], b["prow"], b["rowi"])
+                bt.bt_moe_qgemm_swiglu(*GUI, bits, b["off"], x, b["h"], x_row_index=b["rowi"])
+                bt.bt_moe_qgemm(*DN, bits, b["off"], b["h"], b["yd"])
+                bt.bt_moe_combine(b["yd"], gates_t, b["prow"], top_k, b["out"])
+
+        def unfused(d):
             ids_t, gates_t, x, b, _ = d
             bt.bt_moe_route(ids_t, E, b["off"], b["pidx"], b["prow"], b["rowi"])
-            bt.bt_moe_qgemm(*GU, bits, b["off"], x, b["ygu"], x_row_index=b["rowi"])
+            bt.bt_moe_qgemm(*GUC, bits, b["off"], x, b["ygu"], x_row_index=b["rowi"])
             bt.bt_swiglu(b["ygu"], b["h"])
             bt.bt_moe_qgemm(*DN, bits, b["off"], b["h"], b["yd"])
             bt.bt_moe_combine(b["yd"], gates_t, b["prow"], top_k, b["out"])
 
-        graphs = [capture(torch, lambda d=d: layer(d), stream) for d in draws]
-        n_steps = max(3, min(steps, 100))
-        times = []
-        touched_bytes = 0
-        with torch.cuda.stream(stream):
-            for i in range(max(3, min(warmup, 5))):
-                graphs[i % len(graphs)].replay()
-            torch.cuda.synchronize()
-            with ClockSampler(gpu_index) as clk:
-                for i in range(n_steps):
-                    flush.fill_(float(i))
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
+        res = {}
+        for tag, fn, launches in (("fused", fused, 2 if tokens == 1 else 4), ("unfused", unfused, 5)):
+            graphs = [capture(torch, lambda d=d: fn(d), stream) for d in draws]
+            n_steps = max(3, min(steps, 100))
+            times = []
+            touched_bytes = 0
+            with torch.cuda.stream(stream):
+                for i in range(max(3, min(warmup, 5))):
                     graphs[i % len(graphs)].replay()
-                    e1.record(stream)
-                    e1.synchronize()
-                    times.append(e0.elapsed_time(e1) / 1e3)
-                    touched_bytes += draws[i % len(draws)][4] * per_expert
-        t = sum(times)
-        gbs = touched_bytes / t / 1e9
-        flops = 2 * tokens * top_k * (2 * I * H + H * I)
-        out[f"M{tokens}"] = {"us_per_layer": round(t / n_steps * 1e6, 2), "weight_gbs": round(gbs, 1),
-                             "frac_of_hbm": round(gbs / hbm, 4), "tflops": round(flops * n_steps / t / 1e12, 3),
-                             "experts_touched_mean": round(touched_bytes / n_steps / per_expert, 2),
-                             "launches_per_layer": 5, "clocks": clk.summary()}
-        del graphs
+                torch.cuda.synchronize()
+                with ClockSampler(gpu_index) as clk:
+                    for i in range(n_steps):
+                        flush.fill_(float(i))
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        graphs[i % len(graphs)].replay()
+                        e1.record(stream)
+                        e1.synchronize()
+                        times.append(e0.elapsed_time(e1) / 1e3)
+                        touched_bytes += draws[i % len(draws)][4] * per_expert
+            t = sum(times)
+            gbs = touched_bytes / t / 1e9
+            flops = 2 * tokens * top_k * (2 * I * H + H * I)
+            res[tag] = {"us_per_layer": round(t / n_steps * 1e6, 2), "weight_gbs": round(gbs, 1),
+                        "frac_of_hbm": round(gbs / hbm, 4), "tflops": round(flops * n_steps / t / 1e12, 3),
+                        "experts_touched_mean": round(touched_bytes / n_steps / per_expert, 2),
+                        "launches_per_layer": launches, "clocks": clk.summary()}
+            del graphs
+        out[f"M{tokens}"] = res
     if bt.bt_last_device_error() != bt.BT_OK:
         raise RuntimeError("device error in the MoE leg")
     return out

@@ -32,7 +32,7 @@ BT_F16, BT_BF16, BT_F32 = 0, 1, 2
 (BT_OPT_PDL, BT_OPT_CONST_WEIGHTS, BT_OPT_WAIT_TIMEOUT_US, BT_OPT_TEST_DROP_STAGE,
  BT_OPT_GEMV_GENERIC, BT_OPT_GEMV_STAGES, BT_OPT_GEMM_PATH, BT_OPT_GEMM_SPLITS, BT_OPT_GEMV_MAX_CPL,
  BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI, BT_OPT_GEMV_CUDA_CORE, BT_OPT_GEMV_MMA_STAGE_KB, BT_OPT_GEMV_MMA_SHAPE,
- BT_OPT_GEMV_MMA_GROUPS, BT_OPT_GEMV_TENSOR_PIPE) = range(16)
+ BT_OPT_GEMV_MMA_GROUPS, BT_OPT_GEMV_TENSOR_PIPE, BT_OPT_GEMM_DEQ_WARPS) = range(17)
 
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_qgemm_swiglu", "bt_moe_qgemv_pairs",
            "bt_moe_down_combine",

@@ -142,8 +142,7 @@ bt_status run_gemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
   p.const_weights = opts().pdl && opts().const_weights;
-  p.drop_stage = opts().test_drop_stage;
-  opts().test_drop_stage = 0;
+  p.drop_stage = opts().test_drop_stage.exchange(0);
   GemvPlan pl{};
   if (!rm.pair_ids && !rm.swiglu)
     pl = plan_gemv_mma(bits, gemv_fast_path(bits, xd), N, K, problems, p.num_experts, sm_count(), group);
@@ -333,6 +332,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_MMA_STAGE_KB: opts().gemv_mma_stage_kb = value == 0 ? 0 : (int)std::max(8LL, std::min(value, 112LL)); return BT_OK;
     case BT_OPT_GEMV_MMA_SHAPE: opts().gemv_mma_cfg = (int)std::min(value, 4LL); return BT_OK;
     case BT_OPT_GEMV_TENSOR_PIPE: opts().gemv_tensor_pipe = (int)std::min(value, 2LL); return BT_OK;
+    case BT_OPT_GEMM_DEQ_WARPS: opts().gemm_deq_warps = (int)value; return BT_OK;
     case BT_OPT_GEMV_MMA_GROUPS: opts().gemv_mma_ks = value == 0 ? 0 : (int)std::max(1LL, std::min(value, 64LL)); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
@@ -404,8 +404,7 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
   p.const_weights = opts().pdl && opts().const_weights;
-  p.drop_stage = opts().test_drop_stage;
-  opts().test_drop_stage = 0;
+  p.drop_stage = opts().test_drop_stage.exchange(0);
   const bool fast = gemv_fast_path(bits, x_dtype);
   GemvPlan pl;
   if (mixed) {
@@ -515,8 +514,7 @@ bt_status bt_moe_down_combine(const uint32_t* codes, const uint16_t* scales, con
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
   p.const_weights = opts().pdl && opts().const_weights;
-  p.drop_stage = opts().test_drop_stage;
-  opts().test_drop_stage = 0;
+  p.drop_stage = opts().test_drop_stage.exchange(0);
   const GemvPlan pl = plan_gemv(bits, gemv_fast_path(bits, h_dtype), N, ktot, tokens, 0, sm_count(), group_size,
                                 false, top_k);
   if (!pl.feasible) return BT_ERR_UNSUPPORTED;

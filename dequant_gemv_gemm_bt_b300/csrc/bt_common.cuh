@@ -20,23 +20,40 @@ constexpr int kMaxK = 32768;
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrBadArg = 2u;
 
+// One process-wide tuning value: bt_set_option may run on one host thread while
+// another launches, so every read and write is a relaxed atomic (each value is
+// read once per launch; no ordering between values is needed).
+template <class T>
+struct Opt {
+  std::atomic<T> v;
+  constexpr Opt(T x) : v(x) {}
+  T load() const { return v.load(std::memory_order_relaxed); }
+  operator T() const { return load(); }
+  Opt& operator=(T x) {
+    v.store(x, std::memory_order_relaxed);
+    return *this;
+  }
+  T exchange(T x) { return v.exchange(x, std::memory_order_relaxed); }
+};
+
 struct LaunchOpts {
-  bool pdl = false;
-  bool const_weights = false;
-  unsigned long long wait_timeout_ns = 4000000000ull;
-  int test_drop_stage = 0;   // test hook: the next GEMV launch leaves one stage unfilled
-  bool gemv_generic = false; // tuning: force the generic unpack path
-  int gemv_stages = 0;       // tuning: pipeline depth override (0 = heuristic)
-  int gemm_path = 0;         // tuning: 0 = heuristic, 1 = CUDA-core tile, 2 = tensor-core tile
-  int gemm_splits = 0;       // tuning: tensor-core GEMM K split (0 = heuristic)
-  int gemv_max_cpl = 0;      // tuning: GEMV chunks per lane before splitting K over warps (0 = heuristic)
-  int gemv_stage_kb = 0;     // tuning: GEMV stage size in KiB (0 = heuristic)
-  int gemv_ri = 0;           // tuning: GEMV rows in flight per warp (0 = heuristic)
-  int gemv_cuda_core = 0;    // tuning: 1 = GEMV on the CUDA-core kernel even where the tensor-pipe one applies
-  int gemv_tensor_pipe = 0;  // tuning: tensor-pipe GEMV 0 = by launch size, 1 = wherever it applies, 2 = never
-  int gemv_mma_stage_kb = 0; // tuning: tensor-pipe GEMV stage size in KiB (0 = heuristic)
-  int gemv_mma_cfg = 0;      // tuning: tensor-pipe GEMV kernel shape (0 = default, 1..4)
-  int gemv_mma_ks = 0;       // tuning: most quantization groups per warp in the tensor-pipe GEMV (0 = heuristic)
+  Opt<bool> pdl{false};
+  Opt<bool> const_weights{false};
+  Opt<unsigned long long> wait_timeout_ns{4000000000ull};
+  Opt<int> test_drop_stage{0};   // test hook: the next GEMV launch leaves one stage unfilled
+  Opt<bool> gemv_generic{false}; // tuning: force the generic unpack path
+  Opt<int> gemv_stages{0};       // tuning: pipeline depth override (0 = heuristic)
+  Opt<int> gemm_path{0};         // tuning: 0 = heuristic, 1 = CUDA-core tile, 2 = tensor-core tile
+  Opt<int> gemm_splits{0};       // tuning: tensor-core GEMM K split (0 = heuristic)
+  Opt<int> gemv_max_cpl{0};      // tuning: GEMV chunks per lane before splitting K over warps (0 = heuristic)
+  Opt<int> gemv_stage_kb{0};     // tuning: GEMV stage size in KiB (0 = heuristic)
+  Opt<int> gemv_ri{0};           // tuning: GEMV rows in flight per warp (0 = heuristic)
+  Opt<int> gemv_cuda_core{0};    // tuning: 1 = GEMV on the CUDA-core kernel even where the tensor-pipe one applies
+  Opt<int> gemv_tensor_pipe{0};  // tuning: tensor-pipe GEMV 0 = by launch size, 1 = wherever it applies, 2 = never
+  Opt<int> gemv_mma_stage_kb{0}; // tuning: tensor-pipe GEMV stage size in KiB (0 = heuristic)
+  Opt<int> gemv_mma_cfg{0};      // tuning: tensor-pipe GEMV kernel shape (0 = default, 1..4)
+  Opt<int> gemv_mma_ks{0};       // tuning: most quantization groups per warp in the tensor-pipe GEMV (0 = heuristic)
+  Opt<int> gemm_deq_warps{0};    // tuning: tensor-core GEMM dequant warps per CTA, 8 or 16 (0 = 16 dense, 8 grouped)
 };
 LaunchOpts& opts();
 unsigned* device_error_word();   // device address of the error word (current device)

@@ -43,7 +43,10 @@ namespace tc {
 
 constexpr int BM = 128;                  // weight rows per tile (MMA M)
 constexpr int BK = 64;                   // K per stage = one quantization group
-constexpr int kDeqWarps = 8;
+// Dequantizing warps: 8 cover one K block (4 TMEM lane quadrants x 2 halves of
+// the 64 codes); with 16, two such sets take alternating K blocks, so one set's
+// wait -> load -> dequant -> TMEM store chain overlaps the other's.
+template <int DW> constexpr int kThreadsT = (2 + DW) * 32;
 // A ring in tensor memory: the dequant warps write each K block's 128 x 64 bf16
 // A tile into one of the A slots (column j holds k = 2j, 2j+1 of the row in
 // that lane; a split slot holds the hi tile in columns 0..31 and the lo tile
@@ -62,7 +65,6 @@ template <int BN, bool SPLIT> constexpr int tmem_cols() {
   constexpr int need = acc_cols<BN>() + a_stages<BN, SPLIT>() * a_slot_cols<SPLIT>();
   return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 }
-constexpr int kThreads = (2 + kDeqWarps) * 32;
 
 struct TcParams {
   int M, N, K, G;          // G = K / 64: K blocks
@@ -340,8 +342,8 @@ __device__ __forceinline__ void store_y(const TcParams& p, size_t i, float v) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BITS, bool BF16, int BN, bool GROUPED, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BITS, bool BF16, int BN, bool GROUPED, bool SPLIT, int DW>
+__global__ void __launch_bounds__(kThreadsT<DW>, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                     const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < SA; ++a) {
-      mbar_init(&afull[a], kDeqWarps);
+      mbar_init(&afull[a], 8);   // one arrive per warp of the set that dequantized the K block
     }
     mbar_init(tmem_full, 1);
     *fail = 0;
@@ -549,10 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- dequant warps
-    const int t = threadIdx.x - 64;        // 0..255
+    const int t = threadIdx.x - 64;        // 0..32*DW-1
     // warp w may access TMEM lanes 32*(w%4)..: it dequantizes those 32 rows, the
     // first four warps the low 32 codes of each K block, the last four the high 32
-    const int r = 32 * (warp & 3) + lane, h = (warp - 2) >> 2;
+    // warp w accesses TMEM lanes 32*(w%4)..: it dequantizes those 32 rows; h selects
+    // the low or high 32 codes of a K block, grp which K blocks (kb % (DW/8))
+    const int r = 32 * (warp & 3) + lane, h = ((warp - 2) >> 2) & 1, grp = (warp - 2) >> 3;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     // stage this CTA's scales and biases: rows n0..n0+127, groups gq_lo..+Gc
     const size_t row0 = ((size_t)expert * p.N + n0) * p.GQ;   // first staged parameter of the tile
@@ -562,13 +566,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // out as in shared memory, so they move in 16-byte pieces
       const uint8_t* gs = reinterpret_cast<const uint8_t*>(p.scales + row0);
       const uint8_t* gb = reinterpret_cast<const uint8_t*>(p.biases + row0);
-      for (int i = t; i < BM * Gc * 2 / 16; i += kDeqWarps * 32) {
+      for (int i = t; i < BM * Gc * 2 / 16; i += DW * 32) {
         cp_async16(reinterpret_cast<uint8_t*>(sS) + i * 16, gs + i * 16);
         cp_async16(reinterpret_cast<uint8_t*>(sB) + i * 16, gb + i * 16);
       }
     } else {
       // part of a row (K split) or the ragged last rows: one parameter at a time
-      for (int i = t; i < BM * Gc; i += kDeqWarps * 32) {
+      for (int i = t; i < BM * Gc; i += DW * 32) {
         const int rr = i / Gc, gg = i % Gc;
         const int n = n0 + rr;
         uint16_t sv = 0, bv = 0;
@@ -582,21 +586,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cp_async_wait_all();
-    asm volatile("bar.sync 1, %0;" ::"r"(kDeqWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(DW * 32) : "memory");
     const uint32_t sS_a = smem_u32(sS), sB_a = smem_u32(sB);
 
-    int s = 0, a = 0;
-    uint32_t ph = 0, aph = 0;
-    int sp = 0;          // stage of K block kb - SA, whose MMA commit frees this A slot
-    uint32_t pp = 0;     // parity of that commit on empty[sp]
-    for (int kb = 0; kb < KB; ++kb) {
+    constexpr int NG = DW / 8;   // sets of dequant warps, taking K blocks in turn
+    // Ring positions advance by NG per iteration (no division in the loop):
+    // (s, ph) = stage and phase of K block kb, a = its A slot, (sp, pp) = stage
+    // and phase of K block kb - SA (negative indices wrap to phase 1; they are
+    // never waited on).  S >= 2 >= NG and SA < S.
+    int s = grp, a = grp % SA, sp = grp - SA;
+    uint32_t ph = 0, pp = 0;
+    if (sp < 0) { sp += S; pp = 1; }
+    for (int kb = grp; kb < KB; kb += NG) {
       if (!mbar_wait(&full[s], ph, p.timeout_ns, p.err)) { *fail = 1; break; }
       if (kb >= SA) {
-        // empty[sp] completes once per use of the stage; with S > SA its next
-        // completion needs K block kb - SA + S, which is not dequantized yet,
-        // so the phase awaited here is the one of K block kb - SA.
+        // The commit of K block kb - SA frees this A slot.  empty[] of its stage
+        // completes once per use; its next completion needs K block kb - SA + S
+        // > kb, whose MMA cannot run before this K block's A tile exists, so the
+        // phase awaited here is the one of K block kb - SA.
         if (!mbar_wait(&empty[sp], pp, p.timeout_ns, p.err)) { *fail = 1; break; }
-        if (++sp == S) { sp = 0; pp ^= 1u; }
       }
       const uint32_t st = smem_u32(tring) + (uint32_t)(s * p.stage_bytes);
       const uint32_t caddr = st + p.x_bytes + r * (8 * BITS) + h * (4 * BITS);
@@ -622,15 +630,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[a]);
-      if (++s == S) { s = 0; ph ^= 1u; }
-      if (++a == SA) { a = 0; aph ^= 1u; }
+      s += NG;
+      if (s >= S) { s -= S; ph ^= 1u; }
+      sp += NG;
+      if (sp >= S) { sp -= S; pp ^= 1u; }
+      a += NG;
+      while (a >= SA) a -= SA;
     }
 
   }
 
   // ------------------------------------------------------------------ epilogue
-  // Warps 2..9 drain the accumulator: warp w reads TMEM lanes 32*(w%4).. (the
-  // tile rows it may access) and every other 16-column chunk.  With a K split
+  // Warps 2..DW+1 drain the accumulator: warp w reads TMEM lanes 32*(w%4).. (the
+  // tile rows it may access) and every (DW/4)-th 16-column chunk.  With a K split
   // the partial tiles meet in distributed shared memory first: chunk c belongs
   // to cluster rank c % splits, every rank sends its partial of that chunk to
   // the owner's receive slot [sender], and the owner sums the slots in rank
@@ -642,13 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
   }
   const int q = warp & 3;
-  const int half_sel = (warp - 2) >> 2;
+  const int col_sel = (warp - 2) >> 2;   // this warp's share of the 16-column chunks
+  constexpr int kColSets = DW / 4;
   const int row = 32 * q + lane;
   const int n = n0 + row;
   const uint32_t taddr_row = tmem_base + ((uint32_t)(32 * q) << 16);
   if (p.splits == 1) {
     if (epi) {
-      for (int c0 = 16 * half_sel; c0 < BN; c0 += 32) {
+      for (int c0 = 16 * col_sel; c0 < BN; c0 += 16 * kColSets) {
         uint32_t v[16];
         tmem_ld16(taddr_row + (uint32_t)c0, v);
         if (p.swiglu) {
@@ -681,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync_all();            // every CTA of the cluster is past its main loop
     tc_fence_after();
     if (epi) {
-      for (int c0 = 16 * half_sel; c0 < BN; c0 += 32) {
+      for (int c0 = 16 * col_sel; c0 < BN; c0 += 16 * kColSets) {
         uint32_t v[16];
         tmem_ld16(taddr_row + (uint32_t)c0, v);
         const int chunk = c0 >> 4, owner = chunk % R, slot = chunk / R;
@@ -693,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cluster_sync_all();            // every partial is in its owner's receive area
     if (epi && ok && n < p.N) {
-      for (int slot = half_sel; slot < owned_max; slot += 2) {
+      for (int slot = col_sel; slot < owned_max; slot += kColSets) {
         const int chunk = slot * R + split;
         if (chunk >= kChunks) break;
         float acc[16];
@@ -726,6 +739,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
+// Dequant warps per CTA.  Default: 16 for dense launches (one CTA per SM, so
+// more warps hide the dequant latency) and 8 for grouped ones (narrow expert
+// tiles run two CTAs per SM, which 18 warps' registers would not allow).
+// BT_OPT_GEMM_DEQ_WARPS = 8 or 16 forces either.
+inline int tc_dequant_warps(bool grouped) {
+  const int o = opts().gemm_deq_warps;
+  if (o == 8 || o == 16) return o;
+  return grouped ? 8 : 16;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -779,7 +802,7 @@ size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nul
 // where waves come from how many clusters of that size fit on the device at once.
 int choose_splits(int tiles, int K, int sms);
 
-template <int BITS, bool BF16, int BN, bool GROUPED, bool SPLIT>
+template <int BITS, bool BF16, int BN, bool GROUPED, bool SPLIT, int DW>
 cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStream_t st) {
   if (splits <= 0) splits = GROUPED ? 1 : choose_splits(((gp.N + BM - 1) / BM) * ((gp.M + BN - 1) / BN), gp.K, sm_count());
   EncodeTiledFn enc = encode_fn();
@@ -854,7 +877,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.stages = stages;
   p.astages = std::min(a_stages<BN, SPLIT>(), stages - 1);   // the dequant waits rely on S > SA
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED, SPLIT>;
+  auto k = qgemm_tc_kernel<BITS, BF16, BN, GROUPED, SPLIT, DW>;
   static std::atomic<uint64_t> smem_raised{0};
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
@@ -864,7 +887,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
                                    : (gp.M + BN - 1) / BN;
   if (ytiles > 65535) return cudaErrorInvalidValue;
   cfg.gridDim = dim3((gp.N + BM - 1) / BM, (unsigned)ytiles, splits);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kThreadsT<DW>);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -886,7 +909,8 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
 // keeping >= 4 K blocks per split) with tiles x split <= 0.85 x SMs.
 int choose_splits(int tiles, int K, int sms) {
   const int kb = K / BK;
-  if (opts().gemm_splits > 0) return std::max(1, std::min(opts().gemm_splits, kb / 2));
+  const int forced = opts().gemm_splits;
+  if (forced > 0) return std::max(1, std::min(forced, kb / 2));
   const int limit = (sms * 85) / 100;
   int best = 1;
   for (int sp : {2, 3, 4, 6, 8})
@@ -894,14 +918,20 @@ int choose_splits(int tiles, int K, int sms) {
   return best;
 }
 
+template <int BITS, bool BF16, bool SPLIT, int DW>
+cudaError_t launch_tc_bn_dw(const GemmParams& gp, bt_dtype yd, int bn, int splits, cudaStream_t st) {
+  switch (bn) {
+    case 32: return launch_tc_t<BITS, BF16, 32, false, SPLIT, DW>(gp, yd, splits, st);
+    case 64: return launch_tc_t<BITS, BF16, 64, false, SPLIT, DW>(gp, yd, splits, st);
+    case 128: return launch_tc_t<BITS, BF16, 128, false, SPLIT, DW>(gp, yd, splits, st);
+    default: return launch_tc_t<BITS, BF16, 256, false, SPLIT, DW>(gp, yd, splits, st);
+  }
+}
+
 template <int BITS, bool BF16, bool SPLIT>
 cudaError_t launch_tc_bn(const GemmParams& gp, bt_dtype yd, int bn, int splits, cudaStream_t st) {
-  switch (bn) {
-    case 32: return launch_tc_t<BITS, BF16, 32, false, SPLIT>(gp, yd, splits, st);
-    case 64: return launch_tc_t<BITS, BF16, 64, false, SPLIT>(gp, yd, splits, st);
-    case 128: return launch_tc_t<BITS, BF16, 128, false, SPLIT>(gp, yd, splits, st);
-    default: return launch_tc_t<BITS, BF16, 256, false, SPLIT>(gp, yd, splits, st);
-  }
+  if (tc_dequant_warps(false) == 8) return launch_tc_bn_dw<BITS, BF16, SPLIT, 8>(gp, yd, bn, splits, st);
+  return launch_tc_bn_dw<BITS, BF16, SPLIT, 16>(gp, yd, bn, splits, st);
 }
 
 // bf16 X with fp32 Y takes the split (hi + lo) A tiles; every other pairing the
@@ -917,14 +947,20 @@ cudaError_t launch_tc_bits(const GemmParams& gp, bt_dtype xd, bt_dtype yd, int b
 }
 
 
+template <int BITS, bool BF16, bool SPLIT, int DW>
+cudaError_t launch_tc_grouped_bn_dw(const GemmParams& gp, bt_dtype yd, int bn, cudaStream_t st) {
+  switch (bn) {
+    case 16: return launch_tc_t<BITS, BF16, 16, true, SPLIT, DW>(gp, yd, 1, st);
+    case 32: return launch_tc_t<BITS, BF16, 32, true, SPLIT, DW>(gp, yd, 1, st);
+    case 64: return launch_tc_t<BITS, BF16, 64, true, SPLIT, DW>(gp, yd, 1, st);
+    default: return launch_tc_t<BITS, BF16, 128, true, SPLIT, DW>(gp, yd, 1, st);
+  }
+}
+
 template <int BITS, bool BF16, bool SPLIT>
 cudaError_t launch_tc_grouped_bn(const GemmParams& gp, bt_dtype yd, int bn, cudaStream_t st) {
-  switch (bn) {
-    case 16: return launch_tc_t<BITS, BF16, 16, true, SPLIT>(gp, yd, 1, st);
-    case 32: return launch_tc_t<BITS, BF16, 32, true, SPLIT>(gp, yd, 1, st);
-    case 64: return launch_tc_t<BITS, BF16, 64, true, SPLIT>(gp, yd, 1, st);
-    default: return launch_tc_t<BITS, BF16, 128, true, SPLIT>(gp, yd, 1, st);
-  }
+  if (tc_dequant_warps(true) == 8) return launch_tc_grouped_bn_dw<BITS, BF16, SPLIT, 8>(gp, yd, bn, st);
+  return launch_tc_grouped_bn_dw<BITS, BF16, SPLIT, 16>(gp, yd, bn, st);
 }
 
 template <int BITS>

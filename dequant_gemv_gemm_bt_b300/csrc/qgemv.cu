@@ -36,7 +36,8 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   // 3 or 4 chunks per lane exist for the fast path of bits 2/4/8 only
   const bool wide = fast && (bits == 2 || bits == 4 || bits == 8);
   const int cpl_cap = wide ? 4 : 2;
-  const int want_cpl = opts().gemv_max_cpl > 0 ? std::min(opts().gemv_max_cpl, cpl_cap) : 1;
+  const int o_gemv_max_cpl = opts().gemv_max_cpl.load();
+  const int want_cpl = o_gemv_max_cpl > 0 ? std::min(o_gemv_max_cpl, cpl_cap) : 1;
   int kw = 1;
   while (kw < kMaxNW && (nchunks + 32 * kw - 1) / (32 * kw) > want_cpl) kw *= 2;
   int cpl = (nchunks + 32 * kw - 1) / (32 * kw);
@@ -65,8 +66,10 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   // takes 9 shuffles; decode pass 4.18 vs 3.81 TB/s with 4 rows), fewer as x
   // slices take more registers
   int ri = pl.cpl == 1 ? 8 : (pl.cpl == 2 ? 2 : 1);
-  if (opts().gemv_ri > 0) ri = pl.cpl == 1 ? std::min(8, opts().gemv_ri) : std::min(ri, opts().gemv_ri);
-  int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
+  const int o_gemv_ri = opts().gemv_ri.load();
+  if (o_gemv_ri > 0) ri = pl.cpl == 1 ? std::min(8, o_gemv_ri) : std::min(ri, o_gemv_ri);
+  const int o_gemv_stage_kb = opts().gemv_stage_kb.load();
+  int stage_budget = o_gemv_stage_kb > 0 ? o_gemv_stage_kb * 1024 : kStageBudget;
   const int ri_min = pair_rows ? 2 : 1;   // the SwiGLU epilogue pairs rows 2i, 2i+1
   while (ri > ri_min &&
          ((long long)ri * rw * per_row > stage_budget || ri * rw > std::max<long long>(rw, per_sm)))
@@ -85,7 +88,8 @@ GemvPlan plan_gemv(int bits, bool fast, int N, int K, int problems, int num_expe
   const int stage = (rb * per_row + 127) / 128 * 128;
   pl.stage_bytes = stage;
   int stages = std::max(2, std::min(8, (kRingBudget / ctas_per_sm) / stage));
-  if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
+  const int o_gemv_stages = opts().gemv_stages.load();
+  if (o_gemv_stages >= 2) stages = std::min(8, o_gemv_stages);
   pl.stages = stages;
   pl.units_per_problem = (N + rb - 1) / rb;
   pl.num_units = (long long)pl.units_per_problem * problems;
@@ -121,8 +125,8 @@ namespace {
 size_t mma_smem_limit(int ctas) { return ctas == 1 ? 227 * 1024 : (228 * 1024) / ctas - 1024; }
 
 bool mma_applies(int bits, bool fast, int N, int K, int group) {
-  if (opts().gemv_cuda_core || bits != 4 || group != 64 || !fast || K > kMmaMaxK || K % kGroup) return false;
-  if (opts().gemv_tensor_pipe == 2) return false;
+  if (opts().gemv_cuda_core.load() || bits != 4 || group != 64 || !fast || K > kMmaMaxK || K % kGroup) return false;
+  if (opts().gemv_tensor_pipe.load() == 2) return false;
   const int G = K / kGroup, row_bytes = K * bits / 8;
   // every unit, the ragged last one included, must move in 16-byte pieces
   return ((long long)N * G * 2) % 16 == 0 && ((long long)N * row_bytes) % 16 == 0;
@@ -136,7 +140,7 @@ bool mma_applies(int bits, bool fast, int N, int K, int group) {
 // 2.72 vs 3.44 us).  BT_OPT_GEMV_TENSOR_PIPE 1 forces it wherever it applies,
 // 2 disables it.
 bool mma_by_size(long long rows, int sms) {
-  if (opts().gemv_tensor_pipe == 1) return true;
+  if (opts().gemv_tensor_pipe.load() == 1) return true;
   return (rows + 15) / 16 <= sms;
 }
 
@@ -151,7 +155,8 @@ struct MmaGeom {
 MmaGeom mma_geom(int bits, int N, int K, long long per_sm_rows, int stage_budget, int nw) {
   MmaGeom m{};
   const int G = K / kGroup;
-  const int ks_max = opts().gemv_mma_ks > 0 ? opts().gemv_mma_ks : 32;
+  const int o_gemv_mma_ks = opts().gemv_mma_ks.load();
+  const int ks_max = o_gemv_mma_ks > 0 ? o_gemv_mma_ks : 32;
   int kw = 1;
   while (kw < nw && (G + kw - 1) / kw > ks_max) kw *= 2;
   const long long tiles_per_sm = std::max<long long>(1, per_sm_rows / 16);
@@ -168,7 +173,8 @@ MmaGeom mma_geom(int bits, int N, int K, long long per_sm_rows, int stage_budget
 }
 
 int mma_stage_budget(const MmaShape& sh) {
-  if (opts().gemv_mma_stage_kb > 0) return opts().gemv_mma_stage_kb * 1024;
+  const int o_gemv_mma_stage_kb = opts().gemv_mma_stage_kb.load();
+  if (o_gemv_mma_stage_kb > 0) return o_gemv_mma_stage_kb * 1024;
   return sh.ctas == 1 ? 48 * 1024 : 24 * 1024;
 }
 
@@ -183,7 +189,8 @@ size_t mma_smem(int stages, int stage, int g_max, int nw, int* xsum_bytes) {
 int mma_stages(int stage, int g_max, const MmaShape& sh) {
   int stages = 8;
   while (stages > 2 && mma_smem(stages, stage, g_max, sh.nw, nullptr) > mma_smem_limit(sh.ctas)) --stages;
-  if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
+  const int o_gemv_stages = opts().gemv_stages.load();
+  if (o_gemv_stages >= 2) stages = std::min(8, o_gemv_stages);
   return stages;
 }
 
@@ -202,7 +209,7 @@ GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_
   pl.ri = 16;
   if (num_experts || !mma_applies(bits, fast, N, K, group)) return pl;
   if (!mma_by_size((long long)N * problems, sms)) return pl;
-  const MmaShape sh = mma_shape(opts().gemv_mma_cfg);
+  const MmaShape sh = mma_shape(opts().gemv_mma_cfg.load());
   set_shape(pl, sh);
   const long long per_sm = std::max<long long>(1, ((long long)N * problems + sms - 1) / sms);
   const MmaGeom m = mma_geom(bits, N, K, per_sm / sh.ctas, mma_stage_budget(sh), sh.nw);
@@ -235,7 +242,7 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
     g_max = std::max(g_max, q.k / kGroup);
   }
   if (!mma_by_size(rows, sms)) return pl;
-  const MmaShape sh = mma_shape(opts().gemv_mma_cfg);
+  const MmaShape sh = mma_shape(opts().gemv_mma_cfg.load());
   set_shape(pl, sh);
   const long long per_sm = std::max<long long>(1, (rows + sms - 1) / sms);
   int stage = 0;
@@ -265,8 +272,10 @@ GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int s
   pl.feasible = false;
   pl.cpl = 1;
   // rows in flight per warp: 8 unless some problem's row group would overflow a stage
-  int ri = opts().gemv_ri > 0 ? std::min(8, opts().gemv_ri) : 8;
-  int stage_budget = opts().gemv_stage_kb > 0 ? opts().gemv_stage_kb * 1024 : kStageBudget;
+  const int o_gemv_ri = opts().gemv_ri.load();
+  int ri = o_gemv_ri > 0 ? std::min(8, o_gemv_ri) : 8;
+  const int o_gemv_stage_kb = opts().gemv_stage_kb.load();
+  int stage_budget = o_gemv_stage_kb > 0 ? o_gemv_stage_kb * 1024 : kStageBudget;
   for (int i = 0; i < batch.count; ++i) {
     const GemvProblem& q = batch.prob[i];
     if (q.k <= 0 || q.k % group || q.k > 8 * 32 * 32) return pl;   // one chunk per lane needs K <= 8192
@@ -303,7 +312,8 @@ GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int s
   pl.row_bytes = batch.prob[0].row_bytes;
   pl.stage_bytes = stage;
   int stages = std::max(2, std::min(8, (kRingBudget / ctas_per_sm) / stage));
-  if (opts().gemv_stages >= 2) stages = std::min(8, opts().gemv_stages);
+  const int o_gemv_stages = opts().gemv_stages.load();
+  if (o_gemv_stages >= 2) stages = std::min(8, o_gemv_stages);
   auto smem_for = [&](int st) {
     return (size_t)st * stage + 2 * st * sizeof(uint64_t) + (size_t)kMaxNW * 2 * ri * sizeof(float) + sizeof(int);
   };

@@ -276,8 +276,11 @@ BT_API const char* bt_status_string(bt_status status);
 BT_API bt_status bt_last_device_error(cudaStream_t stream);
 
 /*
- * Launch options (process-wide, host side; read at each call; not thread-safe
- * against concurrent calls).
+ * Launch options.  They are process-wide: one value per option for every
+ * thread, stream and device of the process, read when a call plans its launch.
+ * Setting an option while another thread is inside a call is safe (each value
+ * is a relaxed atomic), but which value that call sees is not defined; set
+ * options before launching work that depends on them.
  *   BT_OPT_PDL          1: launch with programmatic dependent launch so a call's
  *                       prologue overlaps the previous kernel on the stream.
  *   BT_OPT_CONST_WEIGHTS 1 (with PDL): the caller promises that the packed
@@ -303,6 +306,10 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMV_RI       tuning: GEMV rows in flight per warp (0 = heuristic, else 1, 2, 4 or 8).
  *   BT_OPT_GEMV_CUDA_CORE tuning, 1: GEMV on the CUDA-core kernel even where the
  *                       tensor-pipe one applies (4-bit codes, fp16 x, K <= 8192).
+ *   BT_OPT_GEMM_DEQ_WARPS tuning: tensor-core GEMM dequantizing warps per CTA,
+ *                       8 (one set) or 16 (two sets on alternating K blocks);
+ *                       0 = default: 16 for bt_qgemm, 8 for the grouped expert
+ *                       launches (two CTAs per SM there).
  *   BT_OPT_GEMV_TENSOR_PIPE tuning: 0 = the tensor-pipe GEMV for launches of at
  *                       most one 16-row tile per SM (default), 1 = wherever it
  *                       applies, 2 = never.
@@ -331,7 +338,8 @@ typedef enum {
   BT_OPT_GEMV_MMA_STAGE_KB = 12,
   BT_OPT_GEMV_MMA_SHAPE = 13,
   BT_OPT_GEMV_MMA_GROUPS = 14,
-  BT_OPT_GEMV_TENSOR_PIPE = 15
+  BT_OPT_GEMV_TENSOR_PIPE = 15,
+  BT_OPT_GEMM_DEQ_WARPS = 16
 } bt_option;
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);

@@ -516,6 +516,50 @@ def run_sweep(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     return out
 
 
+def run_small(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
+    """Qwen3-0.6B-shaped decode pass with M = 2..16 tokens per step (small-batch
+    decode), Q4 g64, fp16 x, fp32 y.  Per layer the weights are stored as the
+    runtime keeps them: q|k|v (N=4096, K=1024), o (1024, 2048), gate|up (6144,
+    1024), down (1024, 3072); plus the lm_head (151936, 1024): 113 bt_qgemm
+    launches per pass in one CUDA graph with PDL.  Each weight crosses HBM once
+    per pass for all M tokens, so GB/s counts the packed bytes of the pass.
+    "default" is the library's choice (the small-token tensor-pipe kernel);
+    "cuda_core_tile" forces the fp32-FMA tile it replaces."""
+    bits = 4
+    layer = [("qkv", 4096, 1024), ("o", 1024, 2048), ("gu", 6144, 1024), ("down", 1024, 3072)]
+    shapes = [(f"L{l}.{nm}", n, k) for l in range(QWEN06_LAYERS) for nm, n, k in layer] + [QWEN06_LM_HEAD]
+    t0 = time.time()
+    ws = [to_dev_w(torch, w, dev) for w in gen_weights("small-pass", shapes, bits)]
+    gen_s = time.time() - t0
+    wbytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
+    out = {"workload": "Qwen3-0.6B-shaped decode pass at M tokens: 28 layers x (q|k|v 1024->4096, o 2048->1024, "
+                       "gate|up 1024->6144, down 3072->1024) + lm_head 1024->151936, Q4 g64, fp16 x, fp32 y",
+           "bytes_per_pass": wbytes, "launches_per_pass": len(shapes), "weight_gen_s": round(gen_s, 1)}
+    n_steps = max(3, min(steps, 100))
+    for m in (2, 4, 8, 16):
+        xs = {k: torch.randn(m, k, device=dev).half() for k in (1024, 2048, 3072)}
+        ys = [torch.empty(m, n, device=dev, dtype=torch.float32) for _, n, _ in shapes]
+        res = {"path": bt.bt_plan_gemm(bits, m, 4096, 1024, x_dtype=torch.float16)["path"]}
+        for tag, path in (("default", 0), ("cuda_core_tile", 1)):
+            bt.bt_set_option(bt.BT_OPT_GEMM_PATH, path)
+            try:
+                g = capture(torch, lambda: [bt.bt_qgemm(c, s, b, bits, xs[k], y)
+                                            for (c, s, b), (_, _, k), y in zip(ws, shapes, ys)], stream)
+            finally:
+                bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
+            with torch.cuda.stream(stream):
+                t, clk = timed(torch, None, stream, lambda: g.replay(), n_steps, max(3, min(warmup, 5)), gpu_index)
+            t /= n_steps
+            gbs = wbytes / t / 1e9
+            res[tag] = {"gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "us_per_pass": round(t * 1e6, 2),
+                        "tokens_per_s": round(m / t, 1), "clocks": clk}
+            del g
+        out[f"M{m}"] = res
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error in the small-batch leg")
+    return out
+
+
 def interleave_rows(a, b):
     """Two [N, .] arrays -> [2N, .] with a's row i at 2i and b's at 2i+1 (gate/up pairs)."""
     return np.stack([a, b], axis=1).reshape(2 * a.shape[0], *a.shape[1:])
@@ -641,9 +685,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--legs", default="decode,c1,sweep,prefill,moe",
+    ap.add_argument("--legs", default="decode,c1,sweep,prefill,moe,small",
                     help="comma list of legs to run: decode (headline), c1 (single GEMV), sweep (bit widths), "
-                         "prefill, moe")
+                         "prefill, moe, small (M = 2..16 decode pass)")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the side measurement of the pass as 197 single-GEMV launches")
     ap.add_argument("--eager", action="store_true",
@@ -718,6 +762,9 @@ def main():
             out["prefill"] = run_prefill(torch, bt, dev, stream, args.steps, args.warmup, local_rank, peaks)
         if "moe" in legs:
             out["moe"] = run_moe(torch, bt, dev, stream, args.steps, args.warmup, local_rank, float(peaks["hbm_gbs"]))
+        if "small" in legs:
+            out["small_batch"] = run_small(torch, bt, dev, stream, args.steps, args.warmup, local_rank,
+                                           float(peaks["hbm_gbs"]))
         if rank == 0:
             print(json.dumps(out))
         return 0
@@ -853,6 +900,8 @@ def main():
         out["prefill"] = run_prefill(torch, bt, dev, stream, args.steps, args.warmup, local_rank, peaks)
     if "moe" in legs:
         out["moe"] = run_moe(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
+    if "small" in legs:
+        out["small_batch"] = run_small(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
     if rank == 0:
         print(json.dumps(out))
     if dist is not None:

@@ -32,7 +32,7 @@ BT_F16, BT_BF16, BT_F32 = 0, 1, 2
 (BT_OPT_PDL, BT_OPT_CONST_WEIGHTS, BT_OPT_WAIT_TIMEOUT_US, BT_OPT_TEST_DROP_STAGE,
  BT_OPT_GEMV_GENERIC, BT_OPT_GEMV_STAGES, BT_OPT_GEMM_PATH, BT_OPT_GEMM_SPLITS, BT_OPT_GEMV_MAX_CPL,
  BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI, BT_OPT_GEMV_CUDA_CORE, BT_OPT_GEMV_MMA_STAGE_KB, BT_OPT_GEMV_MMA_SHAPE,
- BT_OPT_GEMV_MMA_GROUPS, BT_OPT_GEMV_TENSOR_PIPE, BT_OPT_GEMM_DEQ_WARPS) = range(17)
+ BT_OPT_GEMV_MMA_GROUPS, BT_OPT_GEMV_TENSOR_PIPE, BT_OPT_GEMM_DEQ_WARPS, BT_OPT_GEMM_SMALL_WARPS) = range(18)
 
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_qgemm_swiglu", "bt_moe_qgemv_pairs",
            "bt_moe_down_combine",
@@ -80,11 +80,11 @@ class GemmPlan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("feasible", ctypes.c_int32), ("bn", ctypes.c_int32),
                 ("splits", ctypes.c_int32), ("stages", ctypes.c_int32), ("k_blocks", ctypes.c_int32),
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int64)]
+                ("smem_bytes", ctypes.c_int64), ("rows_per_unit", ctypes.c_int32)]
 
 
 lib.bt_plan_gemm.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(GemmPlan)]
-GEMM_PATHS = {0: "none", 1: "gemv", 2: "simt", 3: "tc"}
+GEMM_PATHS = {0: "none", 1: "gemv", 2: "simt", 3: "tc", 4: "mma"}
 for _name in EXPORTS:
     if _name != "bt_status_string":
         getattr(lib, _name).restype = _i
@@ -452,7 +452,8 @@ def bt_plan_gemm(bits: int, m: int, n: int, k: int, *, num_experts: int = 0, x_d
                  sms: int = 148) -> dict:
     """Launch plan of a dense (num_experts=0) or grouped product of m rows (host only, no GPU needed).
 
-    ``path`` is one of "none", "gemv", "simt" (CUDA-core tile) or "tc" (tensor cores).
+    ``path`` is one of "none", "gemv", "simt" (CUDA-core tile), "tc" (tensor cores) or "mma"
+    (the small-token tensor-pipe kernel).
     """
     pl = GemmPlan()
     _check(lib.bt_plan_gemm(bits, _DT[x_dtype], m, n, k, num_experts, sms, ctypes.byref(pl)), "bt_plan_gemm")

@@ -85,19 +85,30 @@ bt_status cuda_status(cudaError_t e) {
 }
 
 // Which kernel family runs a product of M rows: the GEMV (one row, or a grouped
-// launch with no more rows than experts), the tensor cores (M >= 16 and a
-// supported shape) or the CUDA-core tile.  num_experts == 0: dense product.
-// BT_OPT_GEMM_PATH forces 1 (CUDA-core tile) or 2 (tensor cores where the shape allows).
-enum GemmPath { kPathNone = 0, kPathGemv = 1, kPathSimt = 2, kPathTc = 3 };
-GemmPath gemm_path(int bits, int M, int K, int num_experts, int group = 64) {
+// launch with no more rows than experts), the small-token tensor-pipe kernel
+// (dense M <= 8, or grouped with at most 16 rows per expert on average), the
+// tensor cores (any other supported shape) or the CUDA-core tile.  num_experts == 0: dense product.  BT_OPT_GEMM_PATH forces
+// 1 (CUDA-core tile), 2 (tensor cores) or 3 (small-token kernel) where the shape
+// allows.
+enum GemmPath { kPathNone = 0, kPathGemv = 1, kPathSimt = 2, kPathTc = 3, kPathMma = 4 };
+GemmPath gemm_path(int bits, int M, int N, int K, int num_experts, int group, int sms) {
   const int forced = opts().gemm_path;
-  if (num_experts == 0) {
-    if (M == 1) return kPathGemv;
-    return tc_shape_ok(bits, K, group) && (forced == 2 || (forced == 0 && M >= 16)) ? kPathTc : kPathSimt;
+  if (num_experts == 0 && M == 1) return kPathGemv;
+  if (num_experts > 0 && M == 0) return kPathNone;
+  if (num_experts > 0 && M <= num_experts && forced == 0) return kPathGemv;
+  const bool mma_ok = plan_gemm_small(bits, M, N, K, group, num_experts, sms).feasible;
+  const bool tc_ok = tc_shape_ok(bits, K, group, num_experts > 0);
+  if (forced == 1) return kPathSimt;
+  if (forced == 2) return tc_ok ? kPathTc : kPathSimt;
+  if (forced == 3 && mma_ok) return kPathMma;
+  if (num_experts > 0) {
+    if (mma_ok && ((long long)M + num_experts - 1) / num_experts <= 16) return kPathMma;
+    return tc_ok ? kPathTc : kPathSimt;
   }
-  if (M == 0) return kPathNone;
-  if (M <= num_experts && forced == 0) return kPathGemv;
-  return forced != 1 && tc_shape_ok(bits, K, group) ? kPathTc : kPathSimt;
+  // dense: one n8 token tile on the small-token kernel; the tensor cores from 9 rows
+  if (mma_ok && M <= 8) return kPathMma;
+  if (tc_ok) return kPathTc;
+  return mma_ok ? kPathMma : kPathSimt;
 }
 
 // fp16 x takes the magic-number fast path at every bit width (BT_OPT_GEMV_GENERIC
@@ -179,7 +190,7 @@ bt_status moe_grouped(const uint32_t* codes, const uint16_t* scales, const uint1
       !half_dtype(x_dtype) || !out_dtype(y_dtype))
     return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  const GemmPath path = gemm_path(bits, total_rows, K, num_experts, group_size);
+  const GemmPath path = gemm_path(bits, total_rows, N, K, num_experts, group_size, sm_count());
   if (path == kPathNone) return BT_OK;
   if (path == kPathGemv) {
     RowMap rm;
@@ -199,7 +210,8 @@ bt_status moe_grouped(const uint32_t* codes, const uint16_t* scales, const uint1
   p.num_experts = num_experts;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
-  if (path == kPathTc && tc_supported(bits, K, total_rows, p))
+  if (path == kPathMma && small_supported(bits, p)) return cuda_status(launch_gemm_small(p, bits, x_dtype, y_dtype, stream));
+  if ((path == kPathTc || path == kPathMma) && tc_supported(bits, K, total_rows, p))
     return cuda_status(launch_gemm_tc_grouped(p, bits, x_dtype, y_dtype, stream));
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
 }
@@ -284,7 +296,7 @@ bt_status bt_plan_gemm(int bits, bt_dtype x_dtype, int M, int N, int K, int num_
     return BT_ERR_INVALID_ARG;
   if (!bits_ok(bits) || K > kMaxK) return BT_ERR_UNSUPPORTED;
   *plan = bt_gemm_plan{};
-  GemmPath path = gemm_path(bits, M, K, num_experts);
+  GemmPath path = gemm_path(bits, M, N, K, num_experts, 64, sms);
   GemmGeometry g;
   if (path == kPathGemv) {
     GemvPlan pl = plan_gemv_mma(bits, gemv_fast_path(bits, x_dtype), N, K, num_experts ? M : 1, num_experts, sms);
@@ -298,6 +310,17 @@ bt_status bt_plan_gemm(int bits, bt_dtype x_dtype, int M, int N, int K, int num_
     } else {
       path = kPathSimt;   // run_gemv hands shapes no GEMV kernel holds to the CUDA-core tile
     }
+  }
+  if (path == kPathMma) {
+    const SmallGeometry sg = plan_gemm_small(bits, M, N, K, 64, num_experts, sms);
+    g.feasible = sg.feasible;
+    g.bn = 8 * sg.t8;
+    g.splits = sg.kw;
+    g.stages = sg.stages;
+    g.grid_x = sg.grid;
+    g.grid_y = g.grid_z = 1;
+    g.smem = sg.smem;
+    plan->rows_per_unit = sg.rb;
   }
   if (path == kPathTc) g = plan_gemm_tc_geometry(bits, M, N, K, num_experts, sms);
   if (path == kPathSimt) g = plan_gemm_simt_geometry(M, N, num_experts);
@@ -333,6 +356,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_MMA_SHAPE: opts().gemv_mma_cfg = (int)std::min(value, 4LL); return BT_OK;
     case BT_OPT_GEMV_TENSOR_PIPE: opts().gemv_tensor_pipe = (int)std::min(value, 2LL); return BT_OK;
     case BT_OPT_GEMM_DEQ_WARPS: opts().gemm_deq_warps = (int)value; return BT_OK;
+    case BT_OPT_GEMM_SMALL_WARPS: opts().gemm_small_warps = (int)value; return BT_OK;
     case BT_OPT_GEMV_MMA_GROUPS: opts().gemv_mma_ks = value == 0 ? 0 : (int)std::max(1LL, std::min(value, 64LL)); return BT_OK;
   }
   return BT_ERR_INVALID_ARG;
@@ -377,7 +401,6 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
     const int kq = mixed ? q.k : K;
     bt_status s = check_weights(q.codes, q.scales, q.biases, bits, group_size, q.n, kq);
     if (s != BT_OK) return s;
-    if (mixed && kq > 8192) return BT_ERR_UNSUPPORTED;
     if (!q.x || !q.y) return BT_ERR_INVALID_ARG;
     if (!aligned16(q.x)) return BT_ERR_MISALIGNED;
     rows += q.n;
@@ -419,7 +442,18 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
     pl = all_mma ? plan_gemv_mma(bits, fast, max_n, K, problems_equiv, 0, sm_count(), group_size) : GemvPlan{};
     if (!pl.feasible) pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count(), group_size);
   }
-  if (!pl.feasible) return BT_ERR_UNSUPPORTED;
+  if (!pl.feasible) {
+    // No single launch holds this batch (a row group or K beyond one launch's
+    // staging): each problem runs as its own bt_qgemv, which accepts every shape
+    // the checks above pass.
+    for (int i = 0; i < count; ++i) {
+      const bt_gemv_problem& q = problems[i];
+      const bt_status st = run_gemv(q.codes, q.scales, q.biases, bits, group_size, q.n, mixed ? q.k : K, q.x,
+                                    x_dtype, q.y, y_dtype, 1, RowMap{}, stream);
+      if (st != BT_OK) return st;
+    }
+    return BT_OK;
+  }
   return cuda_status(launch_gemv(p, pl, bits, x_dtype, y_dtype, stream, &batch));
 }
 
@@ -430,7 +464,7 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (s != BT_OK) return s;
   if (M <= 0 || !x || !y || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
   if (!aligned16(x)) return BT_ERR_MISALIGNED;
-  const GemmPath path = gemm_path(bits, M, K, 0, group_size);
+  const GemmPath path = gemm_path(bits, M, N, K, 0, group_size, sm_count());
   if (path == kPathGemv)
     return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, RowMap{}, stream);
   GemmParams p{};
@@ -439,6 +473,7 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   p.group = group_size;
   p.err = device_error_word();
   p.timeout_ns = opts().wait_timeout_ns;
+  if (path == kPathMma && small_supported(bits, p)) return cuda_status(launch_gemm_small(p, bits, x_dtype, y_dtype, stream));
   if (path == kPathTc && tc_supported(bits, K, M, p))
     return cuda_status(launch_gemm_tc(p, bits, x_dtype, y_dtype, stream));
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));

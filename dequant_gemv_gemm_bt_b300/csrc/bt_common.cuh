@@ -54,6 +54,7 @@ struct LaunchOpts {
   Opt<int> gemv_mma_cfg{0};      // tuning: tensor-pipe GEMV kernel shape (0 = default, 1..4)
   Opt<int> gemv_mma_ks{0};       // tuning: most quantization groups per warp in the tensor-pipe GEMV (0 = heuristic)
   Opt<int> gemm_deq_warps{0};    // tuning: tensor-core GEMM dequant warps per CTA, 8 or 16 (0 = 16 dense, 8 grouped)
+  Opt<int> gemm_small_warps{0};  // tuning: small-token kernel consumer warps, 8 or 16 (0 = 16 where it fits)
 };
 LaunchOpts& opts();
 unsigned* device_error_word();   // device address of the error word (current device)

@@ -1,6 +1,9 @@
 // Dequant-GEMM launch description (dense and grouped by expert).
 #pragma once
+#include <cuda.h>
+
 #include <algorithm>
+
 #include "bt_common.cuh"
 
 namespace bt {
@@ -26,7 +29,7 @@ struct GemmParams {
 
 cudaError_t launch_gemm_simt(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
 // The tensor-core path's limits on bits, K and group size (pointers are checked by tc_supported).
-bool tc_shape_ok(int bits, int K, int group = 64);
+bool tc_shape_ok(int bits, int K, int group = 64, bool grouped = false);
 bool tc_supported(int bits, int K, int M, const GemmParams& p);
 cudaError_t launch_gemm_tc(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
 cudaError_t launch_gemm_tc_grouped(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
@@ -47,5 +50,32 @@ GemmGeometry plan_gemm_tc_geometry(int bits, int M, int N, int K, int num_expert
 GemmGeometry plan_gemm_simt_geometry(int M, int N, int num_experts);
 // Token-tile width of a grouped tensor-core launch: the mean rows per expert, 16..128.
 int grouped_bn(int M, int num_experts);
+
+// Small token counts on the tensor pipe (qgemm_mma.cu): 4-bit codes, groups of
+// 64, tokens as the N of mma.sync m16n8k16, each weight read from HBM once for
+// every token of its problem (all M rows of a dense product, or one expert's rows).
+struct SmallGeometry {
+  bool feasible = false;
+  int t8 = 0;            // n8 token tiles per pass: up to 8 * t8 tokens share one staging of x
+  int nw = 0;            // consumer warps per CTA (8 or 16)
+  int kw = 0;            // consumer warps splitting one 16-row tile's K range
+  int rb = 0;            // weight rows per unit (one TMA ring stage)
+  int stages = 0;        // ring depth
+  int grid = 0;          // persistent CTAs (units beyond are walked in turn)
+  long long smem = 0;    // dynamic shared memory per CTA
+};
+// num_experts == 0: dense product of M rows (M <= 32); > 0: grouped, M rows in total.
+SmallGeometry plan_gemm_small(int bits, int M, int N, int K, int group, int num_experts, int sms);
+// Shape limits plus the pointer alignment the TMA and 8-byte parameter copies need.
+bool small_supported(int bits, const GemmParams& p);
+cudaError_t launch_gemm_small(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
+
+namespace tc {
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+}  // namespace tc
 
 }  // namespace bt

@@ -43,6 +43,13 @@ namespace tc {
 
 constexpr int BM = 128;                  // weight rows per tile (MMA M)
 constexpr int BK = 64;                   // K per stage = one quantization group
+// Codes bytes per weight row in one stage: one K block (8*BITS bytes), except
+// for 3-bit codes, whose 24-byte K block is not the multiple of 16 bytes that a
+// TMA box row needs: their stage holds the aligned pair of K blocks (48 bytes,
+// starting at an even K block) and the dequant warps read the half at hand.
+template <int BITS> constexpr int kRowBox = BITS == 3 ? 48 : 8 * BITS;
+template <int BITS> __host__ __device__ __forceinline__ int box_x(int g) { return BITS == 3 ? (g & ~1) * 24 : g * 8 * BITS; }
+template <int BITS> __device__ __forceinline__ int box_off(int g) { return BITS == 3 ? (g & 1) * 24 : 0; }
 // Dequantizing warps: 8 cover one K block (4 TMEM lane quadrants x 2 halves of
 // the 64 codes); with 16, two such sets take alternating K blocks, so one set's
 // wait -> load -> dequant -> TMEM store chain overlaps the other's.
@@ -465,7 +472,7 @@ __global__ void __launch_bounds__(kThreadsT<DW>, 1)
           uint8_t* st = tring + (size_t)s * p.stage_bytes;
           mbar_arrive_expect_tx(&full[s], p.c_bytes + p.x_bytes);
           const int g = kb_lo + kb;
-          tma_load_2d(st + p.x_bytes, &map_codes, g * (8 * BITS), n0, &full[s]);
+          tma_load_2d(st + p.x_bytes, &map_codes, box_x<BITS>(g), n0, &full[s]);
           tma_load_2d(st, &map_x, g * BK, m0, &full[s]);
           ++issued;
           if (++s == S) { s = 0; ph ^= 1u; }
@@ -493,7 +500,7 @@ __global__ void __launch_bounds__(kThreadsT<DW>, 1)
         const int g = kb_lo + kb;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[s], p.c_bytes);
-          tma_load_3d(st + p.x_bytes, &map_codes, g * (8 * BITS), n0, expert, &full[s]);
+          tma_load_3d(st + p.x_bytes, &map_codes, box_x<BITS>(g), n0, expert, &full[s]);
         }
         for (int i = lane; i < BN * 8; i += 32) {
           const int row = i >> 3, ch = i & 7;
@@ -607,7 +614,7 @@ __global__ void __launch_bounds__(kThreadsT<DW>, 1)
         if (!mbar_wait(&empty[sp], pp, p.timeout_ns, p.err)) { *fail = 1; break; }
       }
       const uint32_t st = smem_u32(tring) + (uint32_t)(s * p.stage_bytes);
-      const uint32_t caddr = st + p.x_bytes + r * (8 * BITS) + h * (4 * BITS);
+      const uint32_t caddr = st + p.x_bytes + r * kRowBox<BITS> + box_off<BITS>(kb_lo + kb) + h * (4 * BITS);
       uint32_t w[BITS];
       if constexpr (BITS == 4) {
         lds128(caddr, w[0], w[1], w[2], w[3]);
@@ -749,10 +756,6 @@ inline int tc_dequant_warps(bool grouped) {
   return grouped ? 8 : 16;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
@@ -783,7 +786,7 @@ size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nul
     kb_max = std::max(kb_max, hi - lo);
     gq_max = std::max(gq_max, groups_in(lo, hi, gshift));
   }
-  const uint32_t x_bytes = BN * BK * 2, c_bytes = BM * 8 * BITS;
+  const uint32_t x_bytes = BN * BK * 2, c_bytes = BM * kRowBox<BITS>;
   const uint32_t stage_bytes = (x_bytes + c_bytes + 1023u) & ~1023u;
   const size_t params_bytes = (size_t)2 * BM * gq_max * sizeof(uint16_t);
   const size_t fixed = 1024 + params_bytes + 8 + (size_t)(2 * 12 + 2 * kAStages + 1) * 8 + 16;
@@ -800,11 +803,11 @@ size_t tc_smem_bytes(int K, int splits, int* stages_out, int* k_blocks_out = nul
 
 // K split for a dense launch: minimize waves x (K blocks per split + fixed cost),
 // where waves come from how many clusters of that size fit on the device at once.
-int choose_splits(int tiles, int K, int sms);
+int choose_splits(int tiles, int K, int sms, int group);
 
 template <int BITS, bool BF16, int BN, bool GROUPED, bool SPLIT, int DW>
 cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStream_t st) {
-  if (splits <= 0) splits = GROUPED ? 1 : choose_splits(((gp.N + BM - 1) / BM) * ((gp.M + BN - 1) / BN), gp.K, sm_count());
+  if (splits <= 0) splits = GROUPED ? 1 : choose_splits(((gp.N + BM - 1) / BM) * ((gp.M + BN - 1) / BN), gp.K, sm_count(), gp.group);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int row_bytes = gp.K * BITS / 8;
@@ -813,7 +816,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   if constexpr (GROUPED) {
     cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)gp.N, (cuuint64_t)gp.num_experts};
     cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)row_bytes * gp.N};
-    cuuint32_t box[3] = {(cuuint32_t)(8 * BITS), (cuuint32_t)BM, 1};
+    cuuint32_t box[3] = {(cuuint32_t)kRowBox<BITS>, (cuuint32_t)BM, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint32_t*>(gp.codes), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -822,7 +825,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   } else {
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)gp.N};
     cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)(8 * BITS), (cuuint32_t)BM};
+    cuuint32_t box[2] = {(cuuint32_t)kRowBox<BITS>, (cuuint32_t)BM};
     cuuint32_t es[2] = {1, 1};
     if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(gp.codes), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -858,7 +861,7 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
   p.gc_max = gc_max;
   p.bn = BN;
   p.x_bytes = BN * BK * 2;
-  p.c_bytes = BM * 8 * BITS;
+  p.c_bytes = BM * kRowBox<BITS>;
   p.stage_bytes = (p.x_bytes + p.c_bytes + 1023u) & ~1023u;
   p.scales = gp.scales;
   p.biases = gp.biases;
@@ -907,15 +910,21 @@ cudaError_t launch_tc_t(const GemmParams& gp, bt_dtype yd, int splits, cudaStrea
 // placement, while fuller grids of split clusters spill into a second wave and
 // lose more than the split gains.  So: the largest split (1, 2, 3, 4, 6, 8,
 // keeping >= 4 K blocks per split) with tiles x split <= 0.85 x SMs.
-int choose_splits(int tiles, int K, int sms) {
+int choose_splits(int tiles, int K, int sms, int group) {
   const int kb = K / BK;
+  // each split stages at most 192 quantization groups of parameters
+  const int gq = K / group;
+  const int need = (gq + 191) / 192;
+  int min_sp = 1;
+  for (int sp : {1, 2, 3, 4, 6, 8})
+    if (sp >= need) { min_sp = sp; break; }
   const int forced = opts().gemm_splits;
-  if (forced > 0) return std::max(1, std::min(forced, kb / 2));
+  if (forced > 0) return std::max(min_sp, std::min(forced, kb / 2));
   const int limit = (sms * 85) / 100;
   int best = 1;
   for (int sp : {2, 3, 4, 6, 8})
     if (kb / sp >= 4 && tiles * sp <= limit) best = sp;
-  return best;
+  return std::max(best, min_sp);
 }
 
 template <int BITS, bool BF16, bool SPLIT, int DW>
@@ -1026,6 +1035,7 @@ cudaError_t launch_gemm_tc_grouped(const GemmParams& gp, int bits, bt_dtype xd, 
   const int bn = grouped_bn(gp.M, gp.num_experts);
   switch (bits) {
     case 2: return tc::launch_tc_grouped_bits<2>(gp, xd, yd, bn, st);
+    case 3: return tc::launch_tc_grouped_bits<3>(gp, xd, yd, bn, st);
     case 4: return tc::launch_tc_grouped_bits<4>(gp, xd, yd, bn, st);
     case 6: return tc::launch_tc_grouped_bits<6>(gp, xd, yd, bn, st);
     default: return tc::launch_tc_grouped_bits<8>(gp, xd, yd, bn, st);
@@ -1033,17 +1043,17 @@ cudaError_t launch_gemm_tc_grouped(const GemmParams& gp, int bits, bt_dtype xd, 
 }
 
 
-bool tc_shape_ok(int bits, int K, int group) {
-  if (!(bits == 2 || bits == 4 || bits == 6 || bits == 8)) return false;
-  const int G = K / 64;
-  if (G % 2) return false;                          // K splits start on even K blocks
-  if (K / group > 192) return false;                // the CTA's scales/biases are staged whole in shared memory
+bool tc_shape_ok(int bits, int K, int group, bool grouped) {
+  if (!(bits == 2 || bits == 3 || bits == 4 || bits == 6 || bits == 8)) return false;
+  // the CTA's scales/biases are staged whole in shared memory, at most 192 groups:
+  // dense launches split a longer K over a cluster, grouped ones run one CTA per tile
+  if (K / group > (grouped ? 192 : 8 * 192)) return false;
   if (((size_t)K * bits / 8) % 16) return false;    // TMA row stride
   return true;
 }
 
 bool tc_supported(int bits, int K, int M, const GemmParams& gp) {
-  if (!tc_shape_ok(bits, K, gp.group)) return false;
+  if (!tc_shape_ok(bits, K, gp.group, gp.offsets != nullptr)) return false;
   if ((reinterpret_cast<uintptr_t>(gp.x) & 15) || (reinterpret_cast<uintptr_t>(gp.codes) & 15)) return false;
   (void)M;
   return true;
@@ -1067,10 +1077,11 @@ GemmGeometry plan_gemm_tc_geometry(int bits, int M, int N, int K, int num_expert
     bn = grouped_bn(M, num_experts);
   } else {
     plan_gemm_tc(M, N, K, sms, bn, splits);
-    splits = tc::choose_splits(((N + tc::BM - 1) / tc::BM) * ((M + bn - 1) / bn), K, sms);
+    splits = tc::choose_splits(((N + tc::BM - 1) / tc::BM) * ((M + bn - 1) / bn), K, sms, 64);
   }
   switch (bits) {
     case 2: return tc::geometry_bits<2>(bn, M, N, K, num_experts, splits);
+    case 3: return tc::geometry_bits<3>(bn, M, N, K, num_experts, splits);
     case 4: return tc::geometry_bits<4>(bn, M, N, K, num_experts, splits);
     case 6: return tc::geometry_bits<6>(bn, M, N, K, num_experts, splits);
     default: return tc::geometry_bits<8>(bn, M, N, K, num_experts, splits);
@@ -1082,6 +1093,7 @@ cudaError_t launch_gemm_tc(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype
   plan_gemm_tc(gp.M, gp.N, gp.K, sm_count(), bn, splits);
   switch (bits) {
     case 2: return tc::launch_tc_bits<2>(gp, xd, yd, bn, splits, st);
+    case 3: return tc::launch_tc_bits<3>(gp, xd, yd, bn, splits, st);
     case 4: return tc::launch_tc_bits<4>(gp, xd, yd, bn, splits, st);
     case 6: return tc::launch_tc_bits<6>(gp, xd, yd, bn, splits, st);
     default: return tc::launch_tc_bits<8>(gp, xd, yd, bn, splits, st);

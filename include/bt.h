@@ -98,8 +98,10 @@ BT_API bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const u
  *   K         > 0: every problem has this K (the descriptors' k is ignored);
  *             0: each problem uses its descriptor's k (a mixed-K batch, e.g. a
  *             whole decode step in one launch)
- * Limits: 1 <= count <= 256; one K: 64 <= K <= 32768 (K <= 16384 for bf16 x
- * or 3- and 6-bit codes); mixed K: every k in [64, 8192], a multiple of 64.
+ * Limits: 1 <= count <= 256; each problem's K (the call's, or its own k) as
+ * for bt_qgemv.  A batch that one launch cannot hold (in a mixed-K batch, a k
+ * above 8192) runs as one bt_qgemv launch per problem, in order, on `stream`:
+ * the results are the same, only the launch count differs.
  */
 typedef struct {
   const uint32_t* codes;     /* [n, k*bits/32] */
@@ -298,7 +300,8 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMV_GENERIC  tuning, 1: GEMV uses the generic unpack path for all bits.
  *   BT_OPT_GEMV_STAGES   tuning: GEMV pipeline depth (0 = heuristic, else 2..8).
  *   BT_OPT_GEMM_PATH     tuning: 0 = heuristic, 1 = CUDA-core tile,
- *                       2 = tensor-core tile where supported.
+ *                       2 = tensor-core tile where supported, 3 = small-token
+ *                       tensor-pipe kernel where supported.
  *   BT_OPT_GEMM_SPLITS   tuning: tensor-core GEMM K split across a cluster (0 = heuristic, 1..8).
  *   BT_OPT_GEMV_MAX_CPL  tuning: GEMV chunks of 32 codes per lane before K is split
  *                       over more warps (0 = heuristic, else 1..4).
@@ -310,6 +313,9 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *                       8 (one set) or 16 (two sets on alternating K blocks);
  *                       0 = default: 16 for bt_qgemm, 8 for the grouped expert
  *                       launches (two CTAs per SM there).
+ *   BT_OPT_GEMM_SMALL_WARPS tuning: consumer warps per CTA of the small-token
+ *                       kernel (path 4 of bt_plan_gemm), 8 or 16; 0 = 16 where
+ *                       that layout fits shared memory, else 8.
  *   BT_OPT_GEMV_TENSOR_PIPE tuning: 0 = the tensor-pipe GEMV for launches of at
  *                       most one 16-row tile per SM (default), 1 = wherever it
  *                       applies, 2 = never.
@@ -339,7 +345,8 @@ typedef enum {
   BT_OPT_GEMV_MMA_SHAPE = 13,
   BT_OPT_GEMV_MMA_GROUPS = 14,
   BT_OPT_GEMV_TENSOR_PIPE = 15,
-  BT_OPT_GEMM_DEQ_WARPS = 16
+  BT_OPT_GEMM_DEQ_WARPS = 16,
+  BT_OPT_GEMM_SMALL_WARPS = 17
 } bt_option;
 /* Returns BT_ERR_INVALID_ARG for an unknown option or a negative value. */
 BT_API bt_status bt_set_option(bt_option option, long long value);
@@ -379,14 +386,20 @@ BT_API bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n
  * options, assuming 16-byte aligned pointers.  The per-shape kernel choice
  * and tiling (BaseRT pages, gist.science "Metodologia") in inspectable form.
  *   path       0 no launch (grouped, M = 0); 1 GEMV; 2 CUDA-core tile;
- *              3 tensor cores
+ *              3 tensor cores (tcgen05); 4 small-token tensor-pipe kernel
+ *              (mma.sync, tokens as the MMA's N: dense M <= 8, or grouped
+ *              with at most 16 rows per expert on average; 4-bit codes,
+ *              groups of 64, K a multiple of 256, N a multiple of 8)
  *   feasible   0: these sizes exceed the chosen kernel's limits (the call
  *              would return BT_ERR_CUDA)
- *   bn         token-tile width (the MMA's N on path 3; 32 on path 2)
- *   splits     K split: CTAs per cluster on path 3
- *   stages     ring depth (paths 1 and 3); k_blocks: most 64-wide K blocks
+ *   bn         token-tile width (the MMA's N on path 3; 32 on path 2; on
+ *              path 4 the tokens that share one staging of x)
+ *   splits     K split: CTAs per cluster on path 3; on path 4 the warps that
+ *              split one 16-row tile's K range
+ *   stages     ring depth (paths 1, 3 and 4); k_blocks: most 64-wide K blocks
  *              one split walks (path 3)
  *   grid_*     launch grid; smem_bytes: dynamic shared memory per CTA
+ *   rows_per_unit  weight rows per ring stage (path 4)
  * Errors: BT_ERR_INVALID_ARG for a null plan, M < 0 (or 0 when dense),
  * N <= 0, K not a positive multiple of 64, num_experts outside [0, 4096],
  * sms <= 0 or a bad x_dtype; BT_ERR_UNSUPPORTED for bits or K beyond limits.
@@ -394,6 +407,7 @@ BT_API bt_status bt_plan_gemv_batch(int bits, bt_dtype x_dtype, const int32_t* n
 typedef struct {
   int32_t path, feasible, bn, splits, stages, k_blocks, grid_x, grid_y, grid_z;
   int64_t smem_bytes;
+  int32_t rows_per_unit;
 } bt_gemm_plan;
 BT_API bt_status bt_plan_gemm(int bits, bt_dtype x_dtype, int M, int N, int K, int num_experts, int sms,
                               bt_gemm_plan* plan);

@@ -98,3 +98,18 @@ def test_qgemm_tc_k_split(env, splits, m):
     assert np.array_equal(y, y2), "split-K result is not deterministic"
     y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_bf16(x))
     assert_close(y, y_ref, a, "f32", f"splits={splits} m={m}")
+
+
+@pytest.mark.parametrize("bits,m,n,k", [(3, 128, 384, 3072), (3, 64, 256, 1024), (4, 96, 256, 64 * 5),
+                                        (4, 128, 256, 64 * 63), (4, 64, 512, 16384), (2, 128, 256, 32768)])
+def test_qgemm_tc_q3_odd_groups_long_k(env, bits, m, n, k):
+    """3-bit codes (stages hold aligned 48-byte K-block pairs), odd group counts, and
+    K beyond 192 groups (split over a cluster so each CTA stages at most 192) on the
+    tensor cores, fp32 output at 1e-3*A."""
+    torch, bt = env
+    assert bt.bt_plan_gemm(bits, m, n, k)["path"] == "tc"
+    qw, x = make_case("gemm-tc-ext", n, k, bits, m=m, xdtype="bf16")
+    y = run(env, qw, x, "bf16", "f32", path=2)
+    assert bt.bt_last_device_error() == bt.BT_OK
+    y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, bits, O.decode_bf16(x))
+    assert_close(y, y_ref, a, "f32", f"tc b={bits} m={m} n={n} k={k}")

@@ -215,13 +215,25 @@ def test_qgemv_batched_rejects_bad_tables(env):
     x2 = torch.zeros(2048, dtype=torch.float16, device="cuda")
     with pytest.raises(ValueError):
         bt.bt_qgemv_batched([(codes, scales, biases, x, y), (codes, scales, biases, x2, y)], 4)   # x/codes K differ
-    qb, _ = make_case("batched-bad-big", 8, 16384, 4)
-    cb, sb, bb = to_dev(qb, torch)
-    xb = torch.zeros(16384, dtype=torch.float16, device="cuda")
-    yb = torch.empty(8, device="cuda")
-    with pytest.raises(bt.BTError):   # a mixed-K batch takes K <= 8192 only
-        bt.bt_qgemv_batched([(codes, scales, biases, x, y), (cb, sb, bb, xb, yb)], 4)
     assert bt.bt_last_device_error() == bt.BT_OK
+
+
+def test_qgemv_batched_beyond_one_launch(env):
+    """A mixed-K batch with k = 16384 (above what one batched launch stages) runs
+    one launch per problem and still matches the oracle."""
+    torch, bt = env
+    cases, probs = [], []
+    for tag, n, k in (("a", 64, 1024), ("b", 37, 16384), ("c", 300, 2048)):
+        qw, x16 = make_case("batched-split-" + tag, n, k, 4)
+        y = torch.full((n,), float("nan"), device="cuda")
+        probs.append((*to_dev(qw, torch), half_tensor(x16[0], "f16", torch), y))
+        cases.append((qw, x16))
+    bt.bt_qgemv_batched(probs, 4)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for (qw, x16), pr in zip(cases, probs):
+        y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x16[0]))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"batched fallback k={qw.k}")
 
 
 @pytest.mark.parametrize("bits", BITS)

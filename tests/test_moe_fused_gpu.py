@@ -52,7 +52,7 @@ def check_h(h_gpu, h_ref, bound, what):
 
 
 @pytest.mark.parametrize("bits", (3, 4, 8))
-@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("path", [0, 1, 2, 3])
 @pytest.mark.parametrize("hdt", ["bf16", "f32"])
 def test_grouped_gate_up_swiglu(env, bits, path, hdt):
     torch, bt = env

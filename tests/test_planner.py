@@ -258,7 +258,9 @@ def test_decode_pass_batch_plan_and_work_split(bt):
     assert max(load) <= 1.1 * mean                                    # work, not unit count, is balanced
 
 
-def test_mixed_batch_rejects_k_above_8192(bt):
+def test_mixed_batch_plan_infeasible_above_8192(bt):
+    # one launch cannot hold a mixed batch with k > 8192 (bt_qgemv_batched then
+    # runs one launch per problem)
     p, _ = bt.bt_plan_gemv_batch(4, [(64, 1024), (64, 16384)])
     assert p["feasible"] == 0
     with pytest.raises(bt.BTError):
@@ -272,13 +274,20 @@ SPLIT_CANDIDATES = (1, 2, 3, 4, 6, 8)
 
 def test_gemm_path_choice(bt):
     assert bt.bt_plan_gemm(4, 1, 4096, 4096)["path"] == "gemv"
-    for m in (2, 8, 15):
-        assert bt.bt_plan_gemm(4, m, 4096, 4096)["path"] == "simt"      # too few rows for a 128-wide MMA tile
+    for m in (2, 8):
+        assert bt.bt_plan_gemm(4, m, 4096, 4096)["path"] == "mma"       # a few tokens: the weight-streaming kernel
+    for m in (9, 15):
+        assert bt.bt_plan_gemm(4, m, 4096, 4096)["path"] == "tc"
+    assert bt.bt_plan_gemm(3, 2, 4096, 4096)["path"] == "tc"            # small-token kernel: 4-bit codes only
+    assert bt.bt_plan_gemm(3, 8, 4096, 64 * 3)["path"] == "simt"        # Q3 K = 192: 72-byte rows, neither kernel
     for m in (16, 128, 4096):
         assert bt.bt_plan_gemm(4, m, 4096, 4096)["path"] == "tc"
-    assert bt.bt_plan_gemm(3, 128, 4096, 4096)["path"] == "simt"        # no tensor-core kernel for Q3
-    assert bt.bt_plan_gemm(4, 128, 4096, 64 * 63)["path"] == "simt"     # odd group count (scale pairs)
-    assert bt.bt_plan_gemm(4, 128, 4096, 64 * 194)["path"] == "simt"    # more groups than the CTA stages
+    assert bt.bt_plan_gemm(3, 128, 4096, 4096)["path"] == "tc"          # Q3: stages hold aligned K-block pairs
+    assert bt.bt_plan_gemm(3, 128, 4096, 64 * 63)["path"] == "simt"     # Q3 row of 24*63 B: no 16-B TMA stride
+    assert bt.bt_plan_gemm(4, 128, 4096, 64 * 63)["path"] == "tc"       # odd group count
+    p = bt.bt_plan_gemm(4, 128, 16384, 64 * 256)                        # 256 groups: more than one CTA stages
+    assert p["path"] == "tc" and p["feasible"] == 1 and p["splits"] >= 2
+    assert bt.bt_plan_gemm(4, 128, 16384, 32768)["splits"] >= 3          # 512 groups: at most 192 per split
     assert bt.bt_plan_gemm(2, 128, 4096, 64 * 2)["path"] == "tc"        # Q2 row of 32 B: TMA stride ok
 
 
@@ -288,7 +297,11 @@ def test_gemm_path_choice(bt):
                                  (2048, 768), (4096, 128), (151936, 1024)))
 def test_dense_tc_plan_invariants(bt, bits, m, n, k):
     sms = 148
-    p = bt.bt_plan_gemm(bits, m, n, k, sms=sms)
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 2)   # at M = 16 the small-token kernel would take 4-bit codes
+        p = bt.bt_plan_gemm(bits, m, n, k, sms=sms)
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
     assert p["path"] == "tc" and p["feasible"] == 1
     bn = p["bn"]
     assert bn == next((w for w in (32, 64, 128) if m <= w), 256)      # narrowest token tile that covers M
@@ -316,7 +329,11 @@ def test_prefill_gate_up_matches_the_captured_launch(bt):
 @pytest.mark.parametrize("m", (129, 256, 1024, 4096))
 @pytest.mark.parametrize("experts", (8, 64, 128))
 def test_grouped_tc_plan(bt, m, experts):
-    p = bt.bt_plan_gemm(4, m, 1536, 2048, num_experts=experts)
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 2)
+        p = bt.bt_plan_gemm(4, m, 1536, 2048, num_experts=experts)
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
     assert p["path"] == "tc" and p["feasible"] == 1 and p["splits"] == 1
     mean = -(-m // experts)
     assert p["bn"] == next((w for w in (16, 32, 64) if mean <= w), 128)
@@ -330,7 +347,59 @@ def test_grouped_small_batches_run_the_gemv(bt):
     assert bt.bt_plan_gemm(4, 0, 1536, 2048, num_experts=128)["path"] == "none"
     p = bt.bt_plan_gemm(4, 8, 1536, 2048, num_experts=128, x_dtype=torch.float16)
     assert p["path"] == "gemv"                                         # one row per routed expert: decode
-    assert bt.bt_plan_gemm(4, 129, 1536, 2048, num_experts=128)["path"] == "tc"
+    assert bt.bt_plan_gemm(4, 129, 1536, 2048, num_experts=128)["path"] == "mma"
+    assert bt.bt_plan_gemm(4, 16 * 128, 1536, 2048, num_experts=128)["path"] == "mma"
+    assert bt.bt_plan_gemm(4, 16 * 128 + 1, 1536, 2048, num_experts=128)["path"] == "tc"   # > 16 rows per expert
+
+
+def small_expect(m, n, k, experts, nw, sms=148):
+    """The small-token kernel's geometry restated for nw consumer warps: token tiles
+    from the rows per weight, shrunk while x and its group sums exceed 112 KiB; row
+    blocks of 16 * nw rows (one K box per stage), halved (and the boxes per stage
+    doubled) while there are fewer row blocks than SMs, up to 8 boxes."""
+    g = k // 64
+    xts = g * 128 + 64
+    t8 = -(-m // 8) if experts == 0 else min(4, max(1, (3 * -(-m // experts) // 2 + 7) // 8))
+    while t8 > 1 and 8 * t8 * xts + 8 * t8 * g * 4 > 112 * 1024:
+        t8 -= 1
+    kw = 1
+    while kw < 8 and -(-n // (16 * nw // kw)) * max(1, experts) < sms:
+        kw *= 2
+    rb = 16 * nw // kw
+    return t8, kw, rb, min(-(-n // rb) * max(1, experts), sms)
+
+
+@pytest.mark.parametrize("m,n,k,experts", [(1024, 1536, 2048, 128), (1024, 2048, 768, 128), (300, 1536, 2048, 128),
+                                           (2, 4096, 4096, 0), (8, 3072, 3072, 0), (7, 1024, 3072, 0),
+                                           (5, 151936, 1024, 0), (8, 16384, 3072, 0), (200, 512, 256, 16)])
+@pytest.mark.parametrize("warps", [0, 8, 16])
+def test_small_token_plan(bt, m, n, k, experts, warps):
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMM_SMALL_WARPS, warps)
+        p = bt.bt_plan_gemm(4, m, n, k, num_experts=experts)
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMM_SMALL_WARPS, 0)
+    assert p["path"] == "mma" and p["feasible"] == 1
+    nw = p["rows_per_unit"] * p["splits"] // 16          # rows per block x boxes per stage / 16
+    assert nw == (warps or 16) or (warps == 0 and nw == 8)
+    t8, kw, rb, grid = small_expect(m, n, k, experts, nw)
+    assert (p["bn"], p["splits"], p["rows_per_unit"], p["grid_x"]) == (8 * t8, kw, rb, grid)
+    if experts == 0:
+        assert p["bn"] >= m                                            # every dense row in one staging of x
+    assert 2 <= p["stages"] <= 16 and p["smem_bytes"] <= 227 * 1024
+
+
+def test_small_token_plan_limits(bt):
+    assert bt.bt_plan_gemm(4, 8, 1004, 2048)["path"] != "mma"          # N not a multiple of 8
+    assert bt.bt_plan_gemm(4, 8, 1024, 64 * 5)["path"] != "mma"        # K not a multiple of 256
+    assert bt.bt_plan_gemm(8, 8, 1024, 2048)["path"] != "mma"          # 4-bit codes only
+    assert bt.bt_plan_gemm(4, 33, 1024, 1024)["path"] == "tc"          # more than 8 dense rows
+    try:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 3)
+        assert bt.bt_plan_gemm(4, 32, 1024, 1024)["path"] == "mma"     # forced: up to 32 rows where x fits
+        assert bt.bt_plan_gemm(4, 32, 1024, 4096)["path"] == "tc"      # 32 rows of x at K=4096 do not
+    finally:
+        bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
 
 
 def test_gemm_plan_at_m1_is_the_gemv_plan(bt):

@@ -521,10 +521,12 @@ def run_small(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     decode), Q4 g64, fp16 x, fp32 y.  Per layer the weights are stored as the
     runtime keeps them: q|k|v (N=4096, K=1024), o (1024, 2048), gate|up (6144,
     1024), down (1024, 3072); plus the lm_head (151936, 1024): 113 bt_qgemm
-    launches per pass in one CUDA graph with PDL.  Each weight crosses HBM once
+    products per pass, in one CUDA graph with PDL.  Each weight crosses HBM once
     per pass for all M tokens, so GB/s counts the packed bytes of the pass.
-    "default" is the library's choice (the small-token tensor-pipe kernel);
-    "cuda_core_tile" forces the fp32-FMA tile it replaces."""
+    "batched" is one bt_qgemm_batched call per pass (one launch of the
+    small-token tensor-pipe kernel for M <= 16); "per_product" is one bt_qgemm
+    launch per product (the library's path); "cuda_core_tile" forces the
+    fp32-FMA tile the small-token kernel replaces."""
     bits = 4
     layer = [("qkv", 4096, 1024), ("o", 1024, 2048), ("gu", 6144, 1024), ("down", 1024, 3072)]
     shapes = [(f"L{l}.{nm}", n, k) for l in range(QWEN06_LAYERS) for nm, n, k in layer] + [QWEN06_LM_HEAD]
@@ -534,17 +536,20 @@ def run_small(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     wbytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
     out = {"workload": "Qwen3-0.6B-shaped decode pass at M tokens: 28 layers x (q|k|v 1024->4096, o 2048->1024, "
                        "gate|up 1024->6144, down 3072->1024) + lm_head 1024->151936, Q4 g64, fp16 x, fp32 y",
-           "bytes_per_pass": wbytes, "launches_per_pass": len(shapes), "weight_gen_s": round(gen_s, 1)}
+           "bytes_per_pass": wbytes, "products_per_pass": len(shapes), "weight_gen_s": round(gen_s, 1)}
     n_steps = max(3, min(steps, 100))
     for m in (2, 4, 8, 16):
         xs = {k: torch.randn(m, k, device=dev).half() for k in (1024, 2048, 3072)}
         ys = [torch.empty(m, n, device=dev, dtype=torch.float32) for _, n, _ in shapes]
         res = {"path": bt.bt_plan_gemm(bits, m, 4096, 1024, x_dtype=torch.float16)["path"]}
-        for tag, path in (("default", 0), ("cuda_core_tile", 1)):
-            bt.bt_set_option(bt.BT_OPT_GEMM_PATH, path)
+        probs = [(c, s, b, xs[k], y) for (c, s, b), (_, _, k), y in zip(ws, shapes, ys)]
+        for tag, path in (("batched", None), ("per_product", 0), ("cuda_core_tile", 1)):
+            bt.bt_set_option(bt.BT_OPT_GEMM_PATH, path or 0)
             try:
-                g = capture(torch, lambda: [bt.bt_qgemm(c, s, b, bits, xs[k], y)
-                                            for (c, s, b), (_, _, k), y in zip(ws, shapes, ys)], stream)
+                if path is None:
+                    g = capture(torch, lambda: bt.bt_qgemm_batched(probs, bits), stream)
+                else:
+                    g = capture(torch, lambda: [bt.bt_qgemm(c, s, b, bits, x, y) for c, s, b, x, y in probs], stream)
             finally:
                 bt.bt_set_option(bt.BT_OPT_GEMM_PATH, 0)
             with torch.cuda.stream(stream):

@@ -34,7 +34,7 @@ BT_F16, BT_BF16, BT_F32 = 0, 1, 2
  BT_OPT_GEMV_STAGE_KB, BT_OPT_GEMV_RI, BT_OPT_GEMV_CUDA_CORE, BT_OPT_GEMV_MMA_STAGE_KB, BT_OPT_GEMV_MMA_SHAPE,
  BT_OPT_GEMV_MMA_GROUPS, BT_OPT_GEMV_TENSOR_PIPE, BT_OPT_GEMM_DEQ_WARPS, BT_OPT_GEMM_SMALL_WARPS) = range(18)
 
-EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_moe_qgemm", "bt_moe_qgemm_swiglu", "bt_moe_qgemv_pairs",
+EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_qgemm_batched", "bt_moe_qgemm", "bt_moe_qgemm_swiglu", "bt_moe_qgemv_pairs",
            "bt_moe_down_combine",
            "bt_moe_route", "bt_swiglu", "bt_moe_combine", "bt_status_string", "bt_last_device_error", "bt_set_option",
            "bt_plan_gemv", "bt_plan_gemv_batch", "bt_plan_gemm")
@@ -52,6 +52,14 @@ class GemvProblem(ctypes.Structure):
 
 
 lib.bt_qgemv_batched.argtypes = [ctypes.POINTER(GemvProblem), _i, _i, _i, _i, _i, _i, _p]
+
+
+class GemmProblem(ctypes.Structure):
+    _fields_ = [("codes", _p), ("scales", _p), ("biases", _p), ("x", _p), ("y", _p), ("n", ctypes.c_int32),
+                ("k", ctypes.c_int32)]
+
+
+lib.bt_qgemm_batched.argtypes = [ctypes.POINTER(GemmProblem), _i, _i, _i, _i, _i, _i, _p]
 lib.bt_moe_qgemm.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
 lib.bt_moe_qgemm_swiglu.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
 lib.bt_moe_qgemv_pairs.argtypes = _W + [_i, _i, _i, _p, _i, _i, _p, _i, _p, _i, _i, _p]
@@ -252,6 +260,33 @@ def bt_qgemm(codes, scales, biases, bits: int, x, y=None, *, group_size: int = 6
     _check(lib.bt_qgemm(c, s, b, bits, group_size, m, n, k, _dev(x, "x"), _dt(x), _dev(y, "y"), _dt(y),
                         _stream(stream)), "bt_qgemm")
     return y
+
+
+def bt_qgemm_batched(problems, bits: int, *, group_size: int = 64, stream=None):
+    """Independent products of the same M in one launch where the shapes allow.
+
+    ``problems`` is a list of ``(codes, scales, biases, x [M, K], y [M, N])`` tensors
+    with common dtypes and a common M; each problem has its own K and N.
+    """
+    m = problems[0][3].shape[0]
+    x0, y0 = problems[0][3], problems[0][4]
+    for i, (c, s, b, x, y) in enumerate(problems):   # every entry is checked before any is marshalled
+        try:
+            _need(x.dim() == 2 and x.shape[0] == m, f"x must be [M={m}, K], got shape {list(x.shape)}")
+            k = x.shape[1]
+            n = check_weight(c, s, b, bits, k, group_size)
+            _check_out(y, "y", m * n)
+            _need(x.dtype == x0.dtype and y.dtype == y0.dtype, "every problem must share x and y dtypes")
+            _same_device(c, s, b, x, y, x0)
+        except ValueError as err:
+            raise ValueError(f"problem {i}: {err}") from None
+    arr = (GemmProblem * len(problems))()
+    for i, (c, s, b, x, y) in enumerate(problems):
+        cw, sw, bw = _weights(c, s, b)
+        arr[i] = GemmProblem(cw, sw, bw, _dev(x, "x"), _dev(y, "y"), c.shape[0], x.shape[1])
+    _check(lib.bt_qgemm_batched(arr, len(problems), bits, group_size, m, _dt(x0), _dt(y0), _stream(stream)),
+           "bt_qgemm_batched")
+    return [pr[4] for pr in problems]
 
 
 def bt_moe_qgemm(codes, scales, biases, bits: int, expert_offsets, x, y=None, *, total_rows=None,

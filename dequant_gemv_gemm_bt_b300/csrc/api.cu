@@ -93,7 +93,7 @@ bt_status cuda_status(cudaError_t e) {
 enum GemmPath { kPathNone = 0, kPathGemv = 1, kPathSimt = 2, kPathTc = 3, kPathMma = 4 };
 GemmPath gemm_path(int bits, int M, int N, int K, int num_experts, int group, int sms) {
   const int forced = opts().gemm_path;
-  if (num_experts == 0 && M == 1) return kPathGemv;
+  if (num_experts == 0 && M == 1 && forced != 3) return kPathGemv;
   if (num_experts > 0 && M == 0) return kPathNone;
   if (num_experts > 0 && M <= num_experts && forced == 0) return kPathGemv;
   const bool mma_ok = plan_gemm_small(bits, M, N, K, group, num_experts, sms).feasible;
@@ -477,6 +477,56 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   if (path == kPathTc && tc_supported(bits, K, M, p))
     return cuda_status(launch_gemm_tc(p, bits, x_dtype, y_dtype, stream));
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
+}
+
+bt_status bt_qgemm_batched(const bt_gemm_problem* problems, int count, int bits, int group_size, int M,
+                           bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
+  if (!problems || count < 1 || M < 1 || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    const bt_gemm_problem& q = problems[i];
+    bt_status s = check_weights(q.codes, q.scales, q.biases, bits, group_size, q.n, q.k);
+    if (s != BT_OK) return s;
+    if (!q.x || !q.y) return BT_ERR_INVALID_ARG;
+    if (!aligned16(q.x)) return BT_ERR_MISALIGNED;
+  }
+  if (M == 1) {   // one token: the batched GEMV
+    for (int i0 = 0; i0 < count; i0 += kBatchCap) {
+      const int c = std::min(kBatchCap, count - i0);
+      std::vector<bt_gemv_problem> gp((size_t)c);
+      for (int i = 0; i < c; ++i) {
+        const bt_gemm_problem& q = problems[i0 + i];
+        gp[i] = bt_gemv_problem{q.codes, q.scales, q.biases, q.x, q.y, q.n, q.k};
+      }
+      const bt_status s = bt_qgemv_batched(gp.data(), c, bits, group_size, 0, x_dtype, y_dtype, stream);
+      if (s != BT_OK) return s;
+    }
+    return BT_OK;
+  }
+  // one small-token launch for the table up to 16 rows (where a single product
+  // of 9..16 rows would take the tensor cores, a table of them is launch-bound)
+  const int forced = opts().gemm_path;
+  const bool small_ok = (forced == 0 && M <= 16) || forced == 3;
+  for (int i0 = 0; i0 < count; i0 += small::kBatchLaunchCap) {
+    const int c = std::min(small::kBatchLaunchCap, count - i0);
+    std::vector<GemmProblem> gp((size_t)c);
+    for (int i = 0; i < c; ++i) {
+      const bt_gemm_problem& q = problems[i0 + i];
+      gp[i] = GemmProblem{q.codes, q.scales, q.biases, q.x, q.y, q.n, q.k};
+    }
+    if (small_ok && small_batch_supported(gp.data(), c, M, bits, group_size)) {
+      const bt_status s = cuda_status(launch_gemm_small_batched(gp.data(), c, M, x_dtype, y_dtype, device_error_word(),
+                                                                opts().wait_timeout_ns, stream));
+      if (s != BT_OK) return s;
+      continue;
+    }
+    for (int i = 0; i < c; ++i) {   // one product per launch
+      const bt_gemm_problem& q = problems[i0 + i];
+      const bt_status s = bt_qgemm(q.codes, q.scales, q.biases, bits, group_size, M, q.n, q.k, q.x, x_dtype, q.y,
+                                   y_dtype, stream);
+      if (s != BT_OK) return s;
+    }
+  }
+  return BT_OK;
 }
 
 bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,

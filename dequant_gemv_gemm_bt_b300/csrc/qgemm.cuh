@@ -70,6 +70,24 @@ SmallGeometry plan_gemm_small(int bits, int M, int N, int K, int group, int num_
 bool small_supported(int bits, const GemmParams& p);
 cudaError_t launch_gemm_small(const GemmParams& p, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st);
 
+// Several dense small-token products of the same M in one launch (at most
+// small::kBatchLaunchCap problems per launch).
+namespace small {
+constexpr int kBatchLaunchCap = 120;
+}
+struct GemmProblem {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const void* x;   // [M][K]
+  void* y;         // [M][N]
+  int N, K;
+};
+SmallGeometry plan_gemm_small_batched(const GemmProblem* probs, int count, int M, int sms);
+bool small_batch_supported(const GemmProblem* probs, int count, int M, int bits, int group);
+cudaError_t launch_gemm_small_batched(const GemmProblem* probs, int count, int M, bt_dtype xd, bt_dtype yd,
+                                      unsigned* err, unsigned long long timeout_ns, cudaStream_t st);
+
 namespace tc {
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -78,6 +78,45 @@ struct SmallParams {
   unsigned long long timeout_ns;
 };
 
+// A batch of dense problems in one launch (a decode step of several tokens):
+// each with its own codes (tensor map), parameters, x [M][K] and y [M][N].
+struct SmallProblem {
+  CUtensorMap map;             // codes viewed as [box][row][128 B]
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint16_t* x;
+  void* y;
+  int N, K;
+};
+constexpr int kSmallBatchCap = kBatchLaunchCap;   // 256 bytes per entry: the table fits the 32 KB of kernel parameters
+template <int CAP> struct SmallBatch {
+  SmallProblem prob[CAP];
+  int count;
+};
+
+// What the kernel needs of one problem.
+struct PView {
+  const CUtensorMap* map;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint16_t* x;
+  void* y;
+  int N, K, G, upp, kchunks;
+  uint32_t xts;                // bytes between two tokens' staged x
+};
+
+template <bool BATCH, class Tab>
+__device__ __forceinline__ PView view(const SmallParams& p, const CUtensorMap* map, const Tab& tab, int e) {
+  if constexpr (BATCH) {
+    const SmallProblem& q = tab.prob[e];
+    const int G = q.K >> 6;
+    return PView{&q.map, q.scales, q.biases, q.x, q.y, q.N, q.K, G, (q.N + p.rb - 1) / p.rb,
+                 ((q.K >> 8) + p.kw - 1) / p.kw, (uint32_t)G * 128u + 64u};
+  } else {
+    return PView{map, p.scales, p.biases, p.x, p.y, p.N, p.K, p.G, p.upp, p.kchunks, p.x_tok_stride};
+  }
+}
+
 // One stage (rb rows x kw 128-byte K boxes from box0) in one TMA copy.  The codes
 // are viewed as [box][row][128 bytes] (dense) or [expert][box][row][128 bytes]
 // (grouped), so shared memory receives the stage's box b at b * rb * 128, each
@@ -161,23 +200,33 @@ __device__ __forceinline__ void problem_rows(const SmallParams& p, int e, int& l
 }
 
 // Units of the walk: (problem, token chunk, row block).  Problem e contributes
-// chunks(e) * upp units, chunks(e) = ceil(rows of e / tok_chunk).
-template <bool GROUPED>
-__device__ __forceinline__ int problem_units(const SmallParams& p, int e) {
+// chunks(e) * upp(e) units, chunks(e) = ceil(rows of e / tok_chunk).
+template <bool BATCH, class Tab>
+__device__ __forceinline__ int upp_of(const SmallParams& p, const Tab& tab, int e) {
+  if constexpr (BATCH) return (tab.prob[e].N + p.rb - 1) / p.rb;
+  else return p.upp;
+}
+template <bool GROUPED, bool BATCH, class Tab>
+__device__ __forceinline__ int problem_units(const SmallParams& p, const Tab& tab, int e) {
   int lo, cnt;
   problem_rows<GROUPED>(p, e, lo, cnt);
-  return ((cnt + p.tok_chunk - 1) / p.tok_chunk) * p.upp;
+  return ((cnt + p.tok_chunk - 1) / p.tok_chunk) * upp_of<BATCH>(p, tab, e);
 }
 
 // Warp-collective: total units of the launch.
-template <bool GROUPED>
-__device__ long long count_units(const SmallParams& p) {
-  if constexpr (!GROUPED) return problem_units<GROUPED>(p, 0);
+template <bool GROUPED, bool BATCH, class Tab>
+__device__ long long count_units(const SmallParams& p, const Tab& tab) {
+  if constexpr (BATCH) {
+    long long total = 0;
+    for (int e = 0; e < tab.count; ++e) total += problem_units<GROUPED, BATCH>(p, tab, e);
+    return total;
+  }
+  if constexpr (!GROUPED) return problem_units<GROUPED, BATCH>(p, tab, 0);
   const int lane = threadIdx.x & 31;
   long long total = 0;
   for (int base = 0; base < p.num_experts; base += 32) {
     const int e = base + lane;
-    long long c = e < p.num_experts ? problem_units<GROUPED>(p, e) : 0;
+    long long c = e < p.num_experts ? problem_units<GROUPED, BATCH>(p, tab, e) : 0;
 #pragma unroll
     for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     total += c;
@@ -186,14 +235,19 @@ __device__ long long count_units(const SmallParams& p) {
 }
 
 // Warp-collective: the problem holding unit u and the unit's place in it.
-template <bool GROUPED>
-__device__ void locate(const SmallParams& p, long long u, int& e, int& ch, int& blk) {
+template <bool GROUPED, bool BATCH, class Tab>
+__device__ void locate(const SmallParams& p, const Tab& tab, long long u, int& e, int& ch, int& blk) {
   e = 0;
-  if constexpr (GROUPED) {
+  if constexpr (BATCH) {
+    while (e + 1 < tab.count && u >= problem_units<GROUPED, BATCH>(p, tab, e)) {
+      u -= problem_units<GROUPED, BATCH>(p, tab, e);
+      ++e;
+    }
+  } else if constexpr (GROUPED) {
     const int lane = threadIdx.x & 31;
     for (int base = 0; base < p.num_experts; base += 32) {
       const int ee = base + lane;
-      const long long c = ee < p.num_experts ? problem_units<GROUPED>(p, ee) : 0;
+      const long long c = ee < p.num_experts ? problem_units<GROUPED, BATCH>(p, tab, ee) : 0;
       long long incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -210,21 +264,23 @@ __device__ void locate(const SmallParams& p, long long u, int& e, int& ch, int& 
       u -= __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-  ch = (int)(u / p.upp);
-  blk = (int)(u - (long long)ch * p.upp);
+  const int upp = upp_of<BATCH>(p, tab, e);
+  ch = (int)(u / upp);
+  blk = (int)(u - (long long)ch * upp);
 }
 
 // The unit after (e, ch, blk).
-template <bool GROUPED>
-__device__ __forceinline__ void advance(const SmallParams& p, int& e, int& ch, int& blk) {
-  if (++blk < p.upp) return;
+template <bool GROUPED, bool BATCH, class Tab>
+__device__ __forceinline__ void advance(const SmallParams& p, const Tab& tab, int& e, int& ch, int& blk) {
+  const int upp = upp_of<BATCH>(p, tab, e);
+  if (++blk < upp) return;
   blk = 0;
-  if (++ch * p.upp < problem_units<GROUPED>(p, e)) return;
+  if (++ch * upp < problem_units<GROUPED, BATCH>(p, tab, e)) return;
   ch = 0;
   if constexpr (GROUPED) {
     do {
       ++e;
-    } while (e < p.num_experts && problem_units<GROUPED>(p, e) == 0);
+    } while (e < p.num_experts && problem_units<GROUPED, BATCH>(p, tab, e) == 0);
   } else {
     ++e;
   }
@@ -240,10 +296,11 @@ __device__ __forceinline__ void advance(const SmallParams& p, int& e, int& ch, i
 constexpr int kInFlight = 8;
 
 template <bool BF16, bool GROUPED, int NW>
-__device__ void stage_x(const SmallParams& p, uint32_t xs, float* xsum, int first, int ntok, int npad, int ctid) {
+__device__ void stage_x(const SmallParams& p, const PView& pv, uint32_t xs, float* xsum, int first, int ntok,
+                        int npad, int ctid) {
   constexpr int kStep = NW * 32;
   const int lane = ctid & 31;
-  const int per_tok = p.G * 8;
+  const int per_tok = pv.G * 8;
   const int items = npad * per_tok;
   for (int base = ctid - lane; base < items; base += kInFlight * kStep) {
     uint4 raw[kInFlight];
@@ -259,7 +316,7 @@ __device__ void stage_x(const SmallParams& p, uint32_t xs, float* xsum, int firs
         if constexpr (GROUPED) {
           if (p.row_index) row = __ldg(p.row_index + row);
         }
-        raw[u] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)row * p.K + (size_t)v * 64 + c * 32 + t * 8));
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(pv.x + (size_t)row * pv.K + (size_t)v * 64 + c * 32 + t * 8));
       }
     }
 #pragma unroll
@@ -293,7 +350,7 @@ __device__ void stage_x(const SmallParams& p, uint32_t xs, float* xsum, int firs
       }
       if (idx < items) {
         const int v = rem >> 3, c = (rem >> 2) & 1, t = rem & 3;
-        const uint32_t dst = xs + (uint32_t)tok * p.x_tok_stride + (uint32_t)(v * 128 + c * 64 + t * 16);
+        const uint32_t dst = xs + (uint32_t)tok * pv.xts + (uint32_t)(v * 128 + c * 64 + t * 16);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
                      : "memory");
       }
@@ -305,15 +362,16 @@ __device__ void stage_x(const SmallParams& p, uint32_t xs, float* xsum, int firs
   }
 }
 
-__device__ __forceinline__ void store_y(const SmallParams& p, size_t i, float v) {
-  if (p.y_dtype == BT_F32) store_out<BT_F32>(p.y, i, v);
-  else if (p.y_dtype == BT_BF16) store_out<BT_BF16>(p.y, i, v);
-  else store_out<BT_F16>(p.y, i, v);
+__device__ __forceinline__ void store_y(const SmallParams& p, void* y, size_t i, float v) {
+  if (p.y_dtype == BT_F32) store_out<BT_F32>(y, i, v);
+  else if (p.y_dtype == BT_BF16) store_out<BT_BF16>(y, i, v);
+  else store_out<BT_F16>(y, i, v);
 }
 
-template <bool BF16, int T8, bool GROUPED, int NW>
+template <bool BF16, int T8, bool GROUPED, int NW, bool BATCH>
 __global__ void __launch_bounds__(kThreadsT<NW>, 1)
-    qgemm_small_kernel(const __grid_constant__ CUtensorMap map_codes, const SmallParams p) {
+    qgemm_small_kernel(const __grid_constant__ CUtensorMap map_codes, const SmallParams p,
+                       const __grid_constant__ SmallBatch<BATCH ? kSmallBatchCap : 1> batch) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -327,7 +385,7 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
   __shared__ volatile int s_fail;
 
   // the CTA's share of the row-block units; every unit is kchunks ring stages
-  const long long U = count_units<GROUPED>(p);
+  const long long U = count_units<GROUPED, BATCH>(p, batch);
   const long long u_begin = U * blockIdx.x / gridDim.x, u_end = U * (blockIdx.x + 1) / gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -341,7 +399,7 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
   pdl_launch_dependents();
   if (u_begin >= u_end) return;
   int e, ch, blk;
-  locate<GROUPED>(p, u_begin, e, ch, blk);
+  locate<GROUPED, BATCH>(p, batch, u_begin, e, ch, blk);
 
   if (warp == NW) {
     // ------------------------------------------------------------ producer
@@ -353,9 +411,10 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
     long long it = 0;
     bool ok = true;
     for (long long u = u_begin; u < u_end && ok; ++u) {
+      const PView pv = view<BATCH>(p, &map_codes, batch, e);
       const int row0 = blk * p.rb;
-      const int rows = min(p.rb, p.N - row0);
-      for (int kc = 0; kc < p.kchunks; ++kc, ++it) {
+      const int rows = min(p.rb, pv.N - row0);
+      for (int kc = 0; kc < pv.kchunks; ++kc, ++it) {
         if (it >= S) {
           bool w = true;
           if (lane == 0) w = mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns, p.err);
@@ -364,24 +423,24 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
         const uint32_t st = ring + (uint32_t)s * p.stage_bytes;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[s], p.code_bytes);
-          if constexpr (GROUPED) tma_unit_4d(st, &map_codes, row0, kc * p.kw, e, &full[s], pol);
-          else tma_unit_3d(st, &map_codes, row0, kc * p.kw, &full[s], pol);
+          if constexpr (GROUPED) tma_unit_4d(st, pv.map, row0, kc * p.kw, e, &full[s], pol);
+          else tma_unit_3d(st, pv.map, row0, kc * p.kw, &full[s], pol);
         }
         // scales / biases of groups [kc * gps, +gps) for the block's rows: 8-byte pieces of 4 groups
         const int g0 = kc * gps;
-        const int pieces = min(gps, p.G - g0) >> 2;
-        const size_t prow0 = ((size_t)e * p.N + row0) * p.G + g0;
+        const int pieces = min(gps, pv.G - g0) >> 2;
+        const size_t prow0 = ((size_t)(GROUPED ? e : 0) * pv.N + row0) * pv.G + g0;
         const uint32_t sdst = st + p.code_bytes, bdst = sdst + (uint32_t)p.rb * p.pstride;
         for (int i = lane; i < rows * pieces; i += 32) {
           const int r = i / pieces, j = i - r * pieces;
-          const size_t off = prow0 + (size_t)r * p.G + 4 * j;
-          cp_async8(sdst + (uint32_t)r * p.pstride + 8u * j, p.scales + off);
-          cp_async8(bdst + (uint32_t)r * p.pstride + 8u * j, p.biases + off);
+          const size_t off = prow0 + (size_t)r * pv.G + 4 * j;
+          cp_async8(sdst + (uint32_t)r * p.pstride + 8u * j, pv.scales + off);
+          cp_async8(bdst + (uint32_t)r * p.pstride + 8u * j, pv.biases + off);
         }
         cp_async_mbar_arrive_noinc(&full[s]);
         if (++s == S) { s = 0; ph ^= 1u; }
       }
-      advance<GROUPED>(p, e, ch, blk);
+      advance<GROUPED, BATCH>(p, batch, e, ch, blk);
     }
     if (!ok) {
       cp_async_wait_all();
@@ -407,17 +466,18 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
   int staged_e = -1, staged_ch = -1, rbuf = 0;
   pdl_wait();   // x comes from the previous kernel
   for (long long u = u_begin; u < u_end; ++u) {
+    const PView pv = view<BATCH>(p, &map_codes, batch, e);
     int plo, pcnt;
     problem_rows<GROUPED>(p, e, plo, pcnt);
     const int first = plo + ch * p.tok_chunk;
     const int ntok = min(p.tok_chunk, pcnt - ch * p.tok_chunk);
     const int nt = (ntok + 7) >> 3;
     const int row0 = blk * p.rb;
-    const int rows = min(p.rb, p.N - row0);
+    const int rows = min(p.rb, pv.N - row0);
     if (staged_e != e || staged_ch != ch) {
       // every consumer is done with the previous x before it is replaced
       asm volatile("bar.sync 15, %0;" ::"r"(NW * 32) : "memory");
-      if (!dead) stage_x<BF16, GROUPED, NW>(p, xs0, xsum, first, ntok, nt * 8, (int)threadIdx.x);
+      if (!dead) stage_x<BF16, GROUPED, NW>(p, pv, xs0, xsum, first, ntok, nt * 8, (int)threadIdx.x);
       asm volatile("bar.sync 15, %0;" ::"r"(NW * 32) : "memory");
       staged_e = e;
       staged_ch = ch;
@@ -428,13 +488,13 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
 #pragma unroll
     for (int i = 0; i < T8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     const bool live_rows = r_lo < rows;   // this warp's tile has rows in the block
-    for (int kc = 0; kc < p.kchunks; ++kc) {
+    for (int kc = 0; kc < pv.kchunks; ++kc) {
       if (!dead && (s_fail || !mbar_wait(&full[s], ph, p.timeout_ns, p.err))) {
         dead = true;
         s_fail = 1;
       }
       const int vb = (kc * KW + kw) * 4;   // first group of this warp's box
-      if (!dead && live_rows && vb < p.G) {
+      if (!dead && live_rows && vb < pv.G) {
         const uint32_t st = launder(ring + (uint32_t)s * p.stage_bytes);   // after the wait
         const int R = r_lo + ld_row;
         const uint32_t ldb = st + box_off + (uint32_t)R * kBox;
@@ -445,7 +505,7 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
         // scales / biases of the box's 4 groups for rows g and g + 8
         const uint2 s4a = lds64_nv(ps + (uint32_t)ra * p.pstride), s4b = lds64_nv(ps + (uint32_t)rb2 * p.pstride);
         const uint2 b4a = lds64_nv(pb + (uint32_t)ra * p.pstride), b4b = lds64_nv(pb + (uint32_t)rb2 * p.pstride);
-        const uint32_t xb = xs + (uint32_t)g * p.x_tok_stride + (uint32_t)(tq * 16);
+        const uint32_t xb = xs + (uint32_t)g * pv.xts + (uint32_t)(tq * 16);
         const uint32_t xsb = xsa + (uint32_t)(2 * tq) * 4u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -474,7 +534,7 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
 #pragma unroll
           for (int i8 = 0; i8 < T8; ++i8) {
             if (i8 < nt) {
-              const uint32_t xa = xb + (uint32_t)(8 * i8) * p.x_tok_stride + (uint32_t)v * 128u;
+              const uint32_t xa = xb + (uint32_t)(8 * i8) * pv.xts + (uint32_t)v * 128u;
               const uint4 b1 = lds128_nv(xa), b2 = lds128_nv(xa + 64u);
               float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
               mma<BF16>(d0, pa[0], pbq[0], pa[1], pbq[1], b1.x, b1.y);
@@ -530,15 +590,16 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
               // gate row 2i (even g) and its up row 2i + 1 sit in lanes 4 apart
               const float up = __shfl_xor_sync(0xffffffffu, val, 4);
               if (!dead && !(g & 1) && row < rows && tok < ntok)
-                store_y(p, (size_t)(first + tok) * (p.N / 2) + ((row0 + row) >> 1), val / (1.f + expf(-val)) * up);
+                store_y(p, pv.y, (size_t)(first + tok) * (pv.N / 2) + ((row0 + row) >> 1),
+                        val / (1.f + expf(-val)) * up);
             } else if (!dead && row < rows && tok < ntok) {
-              store_y(p, (size_t)(first + tok) * p.N + row0 + row, val);
+              store_y(p, pv.y, (size_t)(first + tok) * pv.N + row0 + row, val);
             }
           }
         }
       }
     }
-    advance<GROUPED>(p, e, ch, blk);
+    advance<GROUPED, BATCH>(p, batch, e, ch, blk);
   }
 }
 
@@ -609,9 +670,12 @@ Layout plan_layout(int bits, int M, int N, int K, int group, int num_experts, in
   return L;
 }
 
-template <bool BF16, int T8, bool GROUPED, int NW>
-cudaError_t launch_t(const CUtensorMap& map, const SmallParams& p, int grid, size_t smem, cudaStream_t st) {
-  auto k = qgemm_small_kernel<BF16, T8, GROUPED, NW>;
+template <bool BATCH> using TabT = SmallBatch<BATCH ? kSmallBatchCap : 1>;
+
+template <bool BF16, int T8, bool GROUPED, int NW, bool BATCH>
+cudaError_t launch_t(const CUtensorMap& map, const SmallParams& p, const TabT<BATCH>& tab, int grid, size_t smem,
+                     cudaStream_t st) {
+  auto k = qgemm_small_kernel<BF16, T8, GROUPED, NW, BATCH>;
   static std::atomic<uint64_t> smem_raised{0};
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
@@ -625,23 +689,25 @@ cudaError_t launch_t(const CUtensorMap& map, const SmallParams& p, int grid, siz
   attr[0].val.programmaticStreamSerializationAllowed = opts().pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, map, p);
+  return cudaLaunchKernelEx(&cfg, k, map, p, tab);
 }
 
-template <bool BF16, bool GROUPED, int NW>
-cudaError_t launch_x(const CUtensorMap& map, const SmallParams& p, int t8, int grid, size_t smem, cudaStream_t st) {
+template <bool BF16, bool GROUPED, int NW, bool BATCH>
+cudaError_t launch_x(const CUtensorMap& map, const SmallParams& p, const TabT<BATCH>& tab, int t8, int grid,
+                     size_t smem, cudaStream_t st) {
   switch (t8) {
-    case 1: return launch_t<BF16, 1, GROUPED, NW>(map, p, grid, smem, st);
-    case 2: return launch_t<BF16, 2, GROUPED, NW>(map, p, grid, smem, st);
-    case 3: return launch_t<BF16, 3, GROUPED, NW>(map, p, grid, smem, st);
-    default: return launch_t<BF16, 4, GROUPED, NW>(map, p, grid, smem, st);
+    case 1: return launch_t<BF16, 1, GROUPED, NW, BATCH>(map, p, tab, grid, smem, st);
+    case 2: return launch_t<BF16, 2, GROUPED, NW, BATCH>(map, p, tab, grid, smem, st);
+    case 3: return launch_t<BF16, 3, GROUPED, NW, BATCH>(map, p, tab, grid, smem, st);
+    default: return launch_t<BF16, 4, GROUPED, NW, BATCH>(map, p, tab, grid, smem, st);
   }
 }
 
-template <bool BF16, bool GROUPED>
-cudaError_t launch_nw(const CUtensorMap& map, const SmallParams& p, const SmallGeometry& g, cudaStream_t st) {
-  if (g.nw == 16) return launch_x<BF16, GROUPED, 16>(map, p, g.t8, g.grid, (size_t)g.smem, st);
-  return launch_x<BF16, GROUPED, 8>(map, p, g.t8, g.grid, (size_t)g.smem, st);
+template <bool BF16, bool GROUPED, bool BATCH>
+cudaError_t launch_nw(const CUtensorMap& map, const SmallParams& p, const TabT<BATCH>& tab, const SmallGeometry& g,
+                      cudaStream_t st) {
+  if (g.nw == 16) return launch_x<BF16, GROUPED, 16, BATCH>(map, p, tab, g.t8, g.grid, (size_t)g.smem, st);
+  return launch_x<BF16, GROUPED, 8, BATCH>(map, p, tab, g.t8, g.grid, (size_t)g.smem, st);
 }
 
 // Consumer warps: BT_OPT_GEMM_SMALL_WARPS = 8 or 16 forces either; by default
@@ -667,35 +733,29 @@ bool small_supported(int bits, const GemmParams& p) {
          plan_gemm_small(bits, p.M, p.N, p.K, p.group, p.offsets ? p.num_experts : 0, sm_count()).feasible;
 }
 
-cudaError_t launch_gemm_small(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
-  using namespace small;
-  const bool grouped = gp.offsets != nullptr;
-  const Layout L = plan_any(bits, gp.M, gp.N, gp.K, gp.group, grouped ? gp.num_experts : 0, sm_count());
-  if (!L.geo.feasible) return cudaErrorInvalidValue;
+namespace small {
+// The codes of one weight (or E stacked experts) viewed as [E][box][row][128 B]:
+// dim 0 the 128 bytes of a box row, dim 1 the rows (stride row_bytes), dim 2 the
+// K boxes (stride 128), dim 3 the experts; a box is one stage (rb rows, kw boxes).
+bool encode_codes_map(CUtensorMap* map, const uint32_t* codes, int N, int K, int experts, int rb, int kw) {
   tc::EncodeTiledFn enc = tc::encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  const int row_bytes = gp.K / 2;
-  CUtensorMap map;
-  memset(&map, 0, sizeof(map));
+  if (!enc) return false;
+  memset(map, 0, sizeof(*map));
+  const int row_bytes = K / 2;
   const cuuint32_t elem[4] = {1, 1, 1, 1};
-  CUresult r;
-  // [E][box][row][128 B]: dim 0 the 128 bytes of a box row, dim 1 the rows
-  // (stride row_bytes), dim 2 the K boxes (stride 128), dim 3 the experts
-  const cuuint64_t dims[4] = {kBox, (cuuint64_t)gp.N, (cuuint64_t)L.nbox, (cuuint64_t)std::max(1, gp.num_experts)};
-  const cuuint64_t strides[3] = {(cuuint64_t)row_bytes, kBox, (cuuint64_t)row_bytes * gp.N};
-  const cuuint32_t box[4] = {kBox, (cuuint32_t)L.geo.rb, (cuuint32_t)L.geo.kw, 1};
-  r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, grouped ? 4 : 3, const_cast<uint32_t*>(gp.codes), dims, strides, box,
-          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const cuuint64_t dims[4] = {kBox, (cuuint64_t)N, (cuuint64_t)(row_bytes / (int)kBox), (cuuint64_t)std::max(1, experts)};
+  const cuuint64_t strides[3] = {(cuuint64_t)row_bytes, kBox, (cuuint64_t)row_bytes * N};
+  const cuuint32_t box[4] = {kBox, (cuuint32_t)rb, (cuuint32_t)kw, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, experts > 0 ? 4 : 3, const_cast<uint32_t*>(codes), dims, strides, box,
+             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+SmallParams make_params(const Layout& L, int M, bt_dtype yd, unsigned* err, unsigned long long timeout_ns) {
   SmallParams p{};
-  p.M = gp.M;
-  p.N = gp.N;
-  p.K = gp.K;
-  p.G = gp.K / 64;
+  p.M = M;
   p.rb = L.geo.rb;
   p.kw = L.geo.kw;
-  p.upp = (gp.N + L.geo.rb - 1) / L.geo.rb;
   p.kchunks = L.kchunks;
   p.stages = L.geo.stages;
   p.stage_bytes = L.stage_bytes;
@@ -707,6 +767,27 @@ cudaError_t launch_gemm_small(const GemmParams& gp, int bits, bt_dtype xd, bt_dt
   p.xsum_off = L.xsum_off;
   p.red_off = L.red_off;
   p.bar_off = L.bar_off;
+  p.y_dtype = yd;
+  p.const_weights = opts().pdl && opts().const_weights;
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  return p;
+}
+}  // namespace small
+
+cudaError_t launch_gemm_small(const GemmParams& gp, int bits, bt_dtype xd, bt_dtype yd, cudaStream_t st) {
+  using namespace small;
+  const bool grouped = gp.offsets != nullptr;
+  const Layout L = plan_any(bits, gp.M, gp.N, gp.K, gp.group, grouped ? gp.num_experts : 0, sm_count());
+  if (!L.geo.feasible) return cudaErrorInvalidValue;
+  CUtensorMap map;
+  if (!encode_codes_map(&map, gp.codes, gp.N, gp.K, grouped ? gp.num_experts : 0, L.geo.rb, L.geo.kw))
+    return cudaErrorInvalidValue;
+  SmallParams p = make_params(L, gp.M, yd, gp.err, gp.timeout_ns);
+  p.N = gp.N;
+  p.K = gp.K;
+  p.G = gp.K / 64;
+  p.upp = (gp.N + L.geo.rb - 1) / L.geo.rb;
   p.scales = gp.scales;
   p.biases = gp.biases;
   p.x = static_cast<const uint16_t*>(gp.x);
@@ -714,14 +795,80 @@ cudaError_t launch_gemm_small(const GemmParams& gp, int bits, bt_dtype xd, bt_dt
   p.offsets = gp.offsets;
   p.num_experts = grouped ? gp.num_experts : 1;
   p.y = gp.y;
-  p.y_dtype = yd;
   p.swiglu = gp.swiglu;
-  p.const_weights = opts().pdl && opts().const_weights;
-  p.err = gp.err;
-  p.timeout_ns = gp.timeout_ns;
   const bool bf = xd == BT_BF16;
-  if (grouped) return bf ? launch_nw<true, true>(map, p, L.geo, st) : launch_nw<false, true>(map, p, L.geo, st);
-  return bf ? launch_nw<true, false>(map, p, L.geo, st) : launch_nw<false, false>(map, p, L.geo, st);
+  static const TabT<false> none{};
+  if (grouped)
+    return bf ? launch_nw<true, true, false>(map, p, none, L.geo, st) : launch_nw<false, true, false>(map, p, none, L.geo, st);
+  return bf ? launch_nw<true, false, false>(map, p, none, L.geo, st) : launch_nw<false, false, false>(map, p, none, L.geo, st);
+}
+
+// Several dense problems of the same M in one launch.  The layout is planned for
+// the rows of all problems together and the largest K; every problem must fit
+// the kernel's limits (4-bit codes, groups of 64, K a multiple of 256, N a
+// multiple of 8, 16-byte aligned codes and x, 8-byte aligned parameters).
+SmallGeometry plan_gemm_small_batched(const GemmProblem* probs, int count, int M, int sms) {
+  if (count < 1 || count > small::kSmallBatchCap) return SmallGeometry{};
+  long long rows = 0;
+  int kmax = 0;
+  for (int i = 0; i < count; ++i) {
+    const GemmProblem& q = probs[i];
+    if (!plan_gemm_small(4, M, q.N, q.K, 64, 0, sms).feasible) return SmallGeometry{};
+    rows += q.N;
+    kmax = std::max(kmax, q.K);
+  }
+  if (rows > (1LL << 30)) return SmallGeometry{};
+  SmallGeometry g = small::plan_any(4, M, (int)rows, kmax, 64, 0, sms).geo;
+  if (g.feasible) {
+    long long units = 0;
+    for (int i = 0; i < count; ++i) units += (probs[i].N + g.rb - 1) / g.rb;
+    g.grid = (int)std::min<long long>(units, sms);
+  }
+  return g;
+}
+
+bool small_batch_supported(const GemmProblem* probs, int count, int M, int bits, int group) {
+  if (bits != 4 || group != 64) return false;
+  const auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  const auto a8 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 7u) == 0; };
+  for (int i = 0; i < count; ++i)
+    if (!a16(probs[i].codes) || !a16(probs[i].x) || !a8(probs[i].scales) || !a8(probs[i].biases)) return false;
+  return plan_gemm_small_batched(probs, count, M, sm_count()).feasible;
+}
+
+cudaError_t launch_gemm_small_batched(const GemmProblem* probs, int count, int M, bt_dtype xd, bt_dtype yd,
+                                      unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
+  using namespace small;
+  long long rows = 0;
+  int kmax = 0;
+  for (int i = 0; i < count; ++i) {
+    rows += probs[i].N;
+    kmax = std::max(kmax, probs[i].K);
+  }
+  Layout L = plan_any(4, M, (int)rows, kmax, 64, 0, sm_count());
+  if (!L.geo.feasible || count < 1 || count > kSmallBatchCap) return cudaErrorInvalidValue;
+  L.geo.grid = plan_gemm_small_batched(probs, count, M, sm_count()).grid;
+  if (L.geo.grid < 1) return cudaErrorInvalidValue;
+  static thread_local TabT<true> tab;   // 24.6 KB: copied into the launch's parameters
+  memset(&tab, 0, sizeof(tab));
+  tab.count = count;
+  for (int i = 0; i < count; ++i) {
+    const GemmProblem& q = probs[i];
+    SmallProblem& d = tab.prob[i];
+    if (!encode_codes_map(&d.map, q.codes, q.N, q.K, 0, L.geo.rb, L.geo.kw)) return cudaErrorInvalidValue;
+    d.scales = q.scales;
+    d.biases = q.biases;
+    d.x = static_cast<const uint16_t*>(q.x);
+    d.y = q.y;
+    d.N = q.N;
+    d.K = q.K;
+  }
+  SmallParams p = make_params(L, M, yd, err, timeout_ns);
+  p.num_experts = 1;
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  return xd == BT_BF16 ? launch_nw<true, false, true>(unused, p, tab, L.geo, st)
+                       : launch_nw<false, false, true>(unused, p, tab, L.geo, st);
 }
 
 }  // namespace bt

@@ -116,6 +116,39 @@ BT_API bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, in
                                   int K, bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream);
 
 /*
+ * Batched dequant-GEMM for a few tokens: `count` dense products that share M
+ * (the tokens of one decode step), bits, group size and dtypes, each with its
+ * own weight, X [M, k] and Y [M, n], in one launch.  BaseRT pages,
+ * thetesserapress.com "What BaseRT does differently" (more than one token runs
+ * a GEMM) and "Where the wins land, and where they don't" (launch overhead
+ * dominates small models), the M > 1 counterpart of bt_qgemv_batched.
+ *   problems  HOST array of `count` descriptors (read during the call only;
+ *             the pointers in it are device memory: codes and X 16-byte
+ *             aligned, scales and biases 8-byte aligned for the one-launch path)
+ *   M         rows of every X and Y (tokens)
+ * One launch of the small-token tensor-pipe kernel (path 4 of bt_plan_gemm)
+ * takes the whole table when M <= 16, bits = 4, group_size = 64 and every
+ * problem has K a multiple of 256 and n a multiple of 8, and the x of the
+ * largest K fits the kernel's staging (up to 120 problems per launch; longer
+ * tables take several).  M = 1 runs as one bt_qgemv_batched
+ * launch.  Anything else runs one bt_qgemm per problem, in order, on `stream`:
+ * the results are the same, only the launch count differs.
+ * Errors: as for bt_qgemm, for the first problem that fails a check (nothing
+ * is launched then); BT_ERR_INVALID_ARG for count < 1 or M < 1.
+ */
+typedef struct {
+  const uint32_t* codes;     /* [n, k*bits/32] */
+  const uint16_t* scales;    /* [n, k/g] fp16 */
+  const uint16_t* biases;    /* [n, k/g] fp16 */
+  const void* x;             /* [M, k] of x_dtype */
+  void* y;                   /* [M, n] of y_dtype */
+  int32_t n;
+  int32_t k;
+} bt_gemm_problem;
+BT_API bt_status bt_qgemm_batched(const bt_gemm_problem* problems, int count, int bits, int group_size, int M,
+                                  bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream);
+
+/*
  * Dequant-GEMM, M > 1 (prefill): Y[m, n] = sum_k X[m, k] * w_deq[n, k].
  * BaseRT pages, thetesserapress.com "What BaseRT does differently" (prefill,
  * with several tokens, runs a GEMM) and gist.science "Metodologia" (tiled
@@ -301,7 +334,8 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *   BT_OPT_GEMV_STAGES   tuning: GEMV pipeline depth (0 = heuristic, else 2..8).
  *   BT_OPT_GEMM_PATH     tuning: 0 = heuristic, 1 = CUDA-core tile,
  *                       2 = tensor-core tile where supported, 3 = small-token
- *                       tensor-pipe kernel where supported.
+ *                       tensor-pipe kernel where supported (bt_qgemm at M = 1
+ *                       included, which otherwise takes the GEMV).
  *   BT_OPT_GEMM_SPLITS   tuning: tensor-core GEMM K split across a cluster (0 = heuristic, 1..8).
  *   BT_OPT_GEMV_MAX_CPL  tuning: GEMV chunks of 32 codes per lane before K is split
  *                       over more warps (0 = heuristic, else 1..4).

@@ -179,3 +179,46 @@ def test_small_grouped_default_takes_mma_for_moe_prefill(env):
     assert bt.bt_last_device_error() == bt.BT_OK
     y_ref, a = O.moe_qgemm(*w, 4, off, O.decode_bf16(xb)[row_index])
     assert_close(out_to_f64(y, torch), y_ref, a, "f32", "Qwen3-30B-shaped gate|up, M=128")
+
+
+@pytest.mark.parametrize("m", [1, 2, 5, 8, 12, 16, 20])
+@pytest.mark.parametrize("xdtype", ["f16", "bf16"])
+def test_qgemm_batched_matches_oracle(env, m, xdtype):
+    """Several products of the same M in one call: one small-token launch for
+    M <= 16 (the batched GEMV at M = 1, one launch per product above 16), each
+    problem with its own K and N."""
+    torch, bt = env
+    shapes = [(264, 256), (1032, 1024), (96, 3072), (520, 768), (2048, 1024), (16, 2048)]
+    probs, cases = [], []
+    for i, (n, k) in enumerate(shapes):
+        qw, x = make_case(f"qgemm-batched-{i}", n, k, 4, m=m, xdtype=xdtype)
+        c, s, b = to_dev(qw, torch)
+        y = torch.full((m, n), float("nan"), device="cuda")
+        probs.append((c, s, b, half_tensor(x, xdtype, torch), y))
+        cases.append((qw, x))
+    bt.bt_qgemm_batched(probs, 4)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for (qw, x), pr in zip(cases, probs):
+        y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_half(x, xdtype))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"batched m={m} n={qw.n} k={qw.k}")
+
+
+def test_qgemm_batched_more_than_one_launch(env):
+    """130 problems: more than one launch's table (120), results as one call."""
+    torch, bt = env
+    probs, cases = [], []
+    for i in range(130):
+        n, k = (8 + 8 * (i % 5), 256 * (1 + i % 3))
+        n = max(n, 16)
+        qw, x = make_case(f"qgemm-batched-many-{i}", n, k, 4, m=3, xdtype="f16")
+        c, s, b = to_dev(qw, torch)
+        y = torch.full((3, n), float("nan"), device="cuda")
+        probs.append((c, s, b, half_tensor(x, "f16", torch), y))
+        cases.append((qw, x))
+    bt.bt_qgemm_batched(probs, 4)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for (qw, x), pr in zip(cases, probs):
+        y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_half(x, "f16"))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"batched n={qw.n} k={qw.k}")

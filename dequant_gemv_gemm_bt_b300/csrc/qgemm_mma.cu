@@ -234,6 +234,65 @@ __device__ long long count_units(const SmallParams& p, const Tab& tab) {
   return total;
 }
 
+// Grouped launches weigh an expert's units by the n8 token tiles it multiplies
+// (a unit's work is a fixed part per K group plus a part per tile), so that the
+// CTAs' contiguous shares of the walk take similar time.
+template <bool GROUPED, bool BATCH, class Tab>
+__device__ __forceinline__ long long unit_weight(const SmallParams& p, const Tab& tab, int e) {
+  int lo, cnt;
+  problem_rows<GROUPED>(p, e, lo, cnt);
+  return 5 + 2 * ((min(cnt, p.tok_chunk) + 7) >> 3);
+}
+
+// Warp-collective (grouped): the index of the first unit whose weighted start is
+// at or after `c` (the number of units when there is none).
+template <bool GROUPED, bool BATCH, class Tab>
+__device__ long long unit_at_cost(const SmallParams& p, const Tab& tab, long long c) {
+  const int lane = threadIdx.x & 31;
+  long long units_before = 0, cost_before = 0;
+  for (int base = 0; base < p.num_experts; base += 32) {
+    const int e = base + lane;
+    const long long n = e < p.num_experts ? problem_units<GROUPED, BATCH>(p, tab, e) : 0;
+    const long long w = e < p.num_experts ? unit_weight<GROUPED, BATCH>(p, tab, e) : 1;
+    const long long cost = n * w;
+    long long ci = cost, ni = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long tc = __shfl_up_sync(0xffffffffu, ci, o);
+      const long long tn = __shfl_up_sync(0xffffffffu, ni, o);
+      if (lane >= o) { ci += tc; ni += tn; }
+    }
+    const long long c0 = cost_before + ci - cost;   // weighted start of this lane's expert
+    const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && c < c0 + cost);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      const long long sc0 = __shfl_sync(0xffffffffu, c0, src);
+      const long long sw = __shfl_sync(0xffffffffu, w, src);
+      const long long su0 = units_before + __shfl_sync(0xffffffffu, ni - n, src);
+      return su0 + (c > sc0 ? (c - sc0 + sw - 1) / sw : 0);
+    }
+    cost_before += __shfl_sync(0xffffffffu, ci, 31);
+    units_before += __shfl_sync(0xffffffffu, ni, 31);
+  }
+  return units_before;
+}
+
+// Warp-collective (grouped): the weighted size of the walk.
+template <bool GROUPED, bool BATCH, class Tab>
+__device__ long long count_cost(const SmallParams& p, const Tab& tab) {
+  const int lane = threadIdx.x & 31;
+  long long total = 0;
+  for (int base = 0; base < p.num_experts; base += 32) {
+    const int e = base + lane;
+    long long c = e < p.num_experts ? problem_units<GROUPED, BATCH>(p, tab, e) * unit_weight<GROUPED, BATCH>(p, tab, e)
+                                    : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    total += c;
+  }
+  return total;
+}
+
 // Warp-collective: the problem holding unit u and the unit's place in it.
 template <bool GROUPED, bool BATCH, class Tab>
 __device__ void locate(const SmallParams& p, const Tab& tab, long long u, int& e, int& ch, int& blk) {
@@ -385,8 +444,16 @@ __global__ void __launch_bounds__(kThreadsT<NW>, 1)
   __shared__ volatile int s_fail;
 
   // the CTA's share of the row-block units; every unit is kchunks ring stages
-  const long long U = count_units<GROUPED, BATCH>(p, batch);
-  const long long u_begin = U * blockIdx.x / gridDim.x, u_end = U * (blockIdx.x + 1) / gridDim.x;
+  long long u_begin, u_end;
+  if constexpr (GROUPED) {
+    const long long C = count_cost<GROUPED, BATCH>(p, batch);
+    u_begin = unit_at_cost<GROUPED, BATCH>(p, batch, C * blockIdx.x / gridDim.x);
+    u_end = unit_at_cost<GROUPED, BATCH>(p, batch, C * (blockIdx.x + 1) / gridDim.x);
+  } else {
+    const long long U = count_units<GROUPED, BATCH>(p, batch);
+    u_begin = U * blockIdx.x / gridDim.x;
+    u_end = U * (blockIdx.x + 1) / gridDim.x;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 33);
@@ -636,8 +703,8 @@ Layout plan_layout(int bits, int M, int N, int K, int group, int num_experts, in
   auto x_bytes = [&](int t) { return (size_t)8 * t * L.x_tok_stride + (size_t)8 * t * G * 4; };
   while (t8 > 1 && x_bytes(t8) > kXBudget) --t8;
   if (x_bytes(t8) > kXBudget || (num_experts == 0 && 8 * t8 < M)) return L;
-  // K boxes per stage (= warps per 16-row tile): one (128 rows) while the row blocks
-  // alone give every SM one, else more boxes over fewer rows
+  // K boxes per stage (= warps per 16-row tile): one (the most rows per block)
+  // while the row blocks alone give every SM one, else more boxes over fewer rows
   const long long problems = std::max(1, num_experts);
   int kw = 1;
   while (kw < 8 && (long long)((N + 16 * nw / kw - 1) / (16 * nw / kw)) * problems < sms) kw *= 2;

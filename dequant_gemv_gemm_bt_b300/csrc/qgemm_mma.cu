@@ -778,12 +778,16 @@ cudaError_t launch_nw(const CUtensorMap& map, const SmallParams& p, const TabT<B
 }
 
 // Consumer warps: BT_OPT_GEMM_SMALL_WARPS = 8 or 16 forces either; by default
-// 16 where that layout fits shared memory, else 8.
+// 16 where that layout fits shared memory and takes at most two n8 token tiles
+// (with three or four the 16-warp kernel, held to 96 registers, spills), else 8.
 Layout plan_any(int bits, int M, int N, int K, int group, int num_experts, int sms) {
   const int forced = opts().gemm_small_warps;
   if (forced == 8 || forced == 16) return plan_layout(bits, M, N, K, group, num_experts, sms, forced);
   Layout L = plan_layout(bits, M, N, K, group, num_experts, sms, 16);
-  if (!L.geo.feasible) L = plan_layout(bits, M, N, K, group, num_experts, sms, 8);
+  if (!L.geo.feasible || L.geo.t8 > 2) {
+    const Layout L8 = plan_layout(bits, M, N, K, group, num_experts, sms, 8);
+    if (L8.geo.feasible) L = L8;
+  }
   return L;
 }
 

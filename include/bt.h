@@ -349,7 +349,8 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *                       launches (two CTAs per SM there).
  *   BT_OPT_GEMM_SMALL_WARPS tuning: consumer warps per CTA of the small-token
  *                       kernel (path 4 of bt_plan_gemm), 8 or 16; 0 = 16 where
- *                       that layout fits shared memory, else 8.
+ *                       that layout fits shared memory and at most 16 tokens
+ *                       share a staging of x, else 8.
  *   BT_OPT_GEMV_TENSOR_PIPE tuning: 0 = the tensor-pipe GEMV for launches of at
  *                       most one 16-row tile per SM (default), 1 = wherever it
  *                       applies, 2 = never.

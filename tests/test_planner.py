@@ -382,6 +382,8 @@ def test_small_token_plan(bt, m, n, k, experts, warps):
     assert p["path"] == "mma" and p["feasible"] == 1
     nw = p["rows_per_unit"] * p["splits"] // 16          # rows per block x boxes per stage / 16
     assert nw == (warps or 16) or (warps == 0 and nw == 8)
+    if warps == 0 and p["bn"] > 16:
+        assert nw == 8                                                 # 3-4 token tiles: the 8-warp kernel
     t8, kw, rb, grid = small_expect(m, n, k, experts, nw)
     assert (p["bn"], p["splits"], p["rows_per_unit"], p["grid_x"]) == (8 * t8, kw, rb, grid)
     if experts == 0:

@@ -5,7 +5,8 @@ Default workload (one "step"): a Qwen3-0.6B-shaped Q4 (group 64) decode pass
 at M = 1 -- 28 layers of q 1024->2048, k/v 1024->1024, o 2048->1024, gate/up
 1024->3072, down 3072->1024, each with its own weights and its own fp16 x,
 plus an lm_head 1024->151936: 197 dequant-GEMVs, 335,241,216 bytes of packed
-codes + fp16 scales/biases, captured as one CUDA graph of libbt launches.
+codes + fp16 scales/biases, run as the library's decode pass object (one
+batched launch, recorded once as a CUDA graph and replayed per step).
 Weights are synthetic (seeded N(0, 0.02), min/max-quantized); they exceed the
 126 MB L2, so no flush is needed between steps.
 
@@ -13,7 +14,9 @@ Metric: weight GB/s (codes + scales + biases per pass / pass time), the
 BaseRT pages' decode-bandwidth view (the bytes read per token fall with the
 bit width).  The same run also times the Llama-3.2-3B-shaped prefill
 GEMM pass (M = 128 and 512, TFLOP/s, key "prefill") and the Qwen3-30B-A3B-
-shaped MoE layer (M = 1 and 128, key "moe"); --legs selects them.
+shaped MoE layer (M = 1 and 128, key "moe"), the small-batch decode pass
+(key "small_batch") and the decode step as 113 dependent stages through the
+pass object (key "dependent_pass"); --legs selects them.
 
 ``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
 workload (the only other code path of this workload).  Under torchrun each
@@ -565,6 +568,68 @@ def run_small(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
     return out
 
 
+def run_chain(torch, bt, bufs, dev, stream, steps, warmup, gpu_index, hbm, pass_bytes):
+    """The decode leg's Qwen3-0.6B-shaped weights as a DEPENDENT decode step: per
+    layer the stages [q, k, v] (read the hidden state), [o] (reads q's output),
+    [gate, up] (read o's output) and [down] (reads gate's output; its output is
+    the next layer's hidden state), then [lm_head]: 113 stages in order, each
+    stage's fp16 output the next one's x (the products alone, with no attention,
+    norm or activation between them).  "pass": bt_pass_run, the library's CUDA
+    graph recorded with PDL and the constant-weights prefetch; "pass_no_pdl":
+    the same recorded without PDL; "eager": one bt_qgemm_batched call per stage
+    from Python, no graph (host-bound)."""
+    bits = 4
+    per_layer = len(QWEN06_LAYER)
+    out = {"workload": "Qwen3-0.6B-shaped decode step as 113 dependent stages (28 layers x [q,k,v] [o] "
+                       "[gate,up] [down] + [lm_head]), Q4 g64, fp16 x and y", "stages": 28 * 4 + 1,
+           "bytes_per_pass": pass_bytes}
+    n_steps = max(3, min(steps, 50))
+    for m in (1, 4):
+        h = torch.randn(m, 1024, device=dev).half()
+        stages = []
+        for layer in range(QWEN06_LAYERS):
+            w = bufs[layer * per_layer:(layer + 1) * per_layer]
+            ys = [torch.empty(m, qw[4].numel(), dtype=torch.float16, device=dev) for qw in w]
+            q, k, v, o, gate, up, down = [(c, s_, b) for c, s_, b, *_ in w]
+            yq, yk, yv, yo, yg, yu, yd = ys
+            stages += [[(*q, h, yq), (*k, h, yk), (*v, h, yv)], [(*o, yq, yo)], [(*gate, yo, yg), (*up, yo, yu)],
+                       [(*down, yg, yd)]]
+            h = yd
+        lm = bufs[-1]
+        stages.append([(lm[0], lm[1], lm[2], h, torch.empty(m, lm[4].numel(), dtype=torch.float16, device=dev))])
+        res = {"launches_per_pass": len(stages)}
+        for tag, pdl in (("pass", 1), ("pass_no_pdl", 0)):
+            bt.bt_set_option(bt.BT_OPT_PDL, pdl)
+            bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, pdl)
+            try:
+                dp = bt.bt_pass_create(stages, bits)
+                with torch.cuda.stream(stream):
+                    dp.run(stream)   # first run: direct launches, then the recording
+                torch.cuda.synchronize()
+            finally:
+                bt.bt_set_option(bt.BT_OPT_PDL, 1)
+                bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
+            with torch.cuda.stream(stream):
+                t, clk = timed(torch, None, stream, lambda: dp.run(stream), n_steps, max(3, min(warmup, 5)), gpu_index)
+            t /= n_steps
+            gbs = pass_bytes / t / 1e9
+            res[tag] = {"us_per_pass": round(t * 1e6, 2), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+                        "clocks": clk}
+            dp.close()
+
+        def eager():
+            for st in stages:
+                bt.bt_qgemm_batched(st, bits, stream=stream)
+        with torch.cuda.stream(stream):
+            t, _ = timed(torch, None, stream, eager, 5, 3, gpu_index)
+        t /= 5
+        res["eager"] = {"us_per_pass": round(t * 1e6, 2), "gbs": round(pass_bytes / t / 1e9, 1)}
+        out[f"M{m}"] = res
+    if bt.bt_last_device_error() != bt.BT_OK:
+        raise RuntimeError("device error in the dependent-stage leg")
+    return out
+
+
 def interleave_rows(a, b):
     """Two [N, .] arrays -> [2N, .] with a's row i at 2i and b's at 2i+1 (gate/up pairs)."""
     return np.stack([a, b], axis=1).reshape(2 * a.shape[0], *a.shape[1:])
@@ -690,9 +755,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--legs", default="decode,c1,sweep,prefill,moe,small",
+    ap.add_argument("--legs", default="decode,c1,sweep,prefill,moe,small,chain",
                     help="comma list of legs to run: decode (headline), c1 (single GEMV), sweep (bit widths), "
-                         "prefill, moe, small (M = 2..16 decode pass)")
+                         "prefill, moe, small (M = 2..16 decode pass), chain (dependent-stage pass; needs decode)")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the side measurement of the pass as 197 single-GEMV launches")
     ap.add_argument("--eager", action="store_true",
@@ -711,7 +776,8 @@ def main():
     bits = 4
     pass_bytes = sum(weight_bytes(n, k, bits) for _, n, k in shapes)
     config = {"workload": "Qwen3-0.6B-shaped decode pass, M=1: 28 layers x 7 projections + lm_head 1024->151936",
-              "execution": "1 bt_qgemv_batched launch per pass (197 problems, mixed K), captured in a CUDA graph",
+              "execution": "1 batched GEMV launch per pass (197 problems, mixed K) in the library's decode pass "
+                           "object: bt_pass_create once, then bt_pass_run per step (a CUDA graph with PDL)",
               "bits": bits, "group_size": GROUP, "gemvs_per_pass": len(shapes), "weight_bytes_per_pass": pass_bytes,
               "x_dtype": "f16", "y_dtype": "f32",
               "l2": "inputs exceed L2 (335 MB of packed weights per pass vs 126 MB L2); no flush",
@@ -794,25 +860,37 @@ def main():
     bt.bt_set_option(bt.BT_OPT_CONST_WEIGHTS, 1)
 
     # The pass's projections are independent (each has its own x), so the whole
-    # pass is one mixed-K batched launch (K = 1024, 2048, 3072), in pass order.
+    # pass is one stage: one mixed-K batched launch (K = 1024, 2048, 3072), in
+    # pass order, planned once by bt_pass_create and replayed by the library as
+    # a CUDA graph (bt_pass_run).
     groups = [[(c, s, b, x, y) for c, s, b, x, y, _ in bufs]]
 
     def run_pass():
         for g in groups:
             bt.bt_qgemv_batched(g, bits)
 
+    def as_rows(g):
+        return [(c, s, b, x.view(1, -1), y.view(1, -1)) for c, s, b, x, y in g]
+
     def run_pass_single():
         for c, s, b, x, y, nb in bufs:
             bt.bt_qgemv(c, s, b, nb, x, y)
 
     stream = torch.cuda.Stream(device=dev)
-    graph = capture(torch, run_pass, stream)
+    if EAGER:
+        graph = capture(torch, run_pass, stream)
+        replay = graph.replay
+    else:
+        dpass = bt.bt_pass_create([as_rows(g) for g in groups], bits)
+        with torch.cuda.stream(stream):
+            dpass.run(stream)   # the first run launches directly and records the graph
+        torch.cuda.synchronize()
+
+        def replay():
+            dpass.run(stream)
     graph_single = None if args.no_compare else capture(torch, run_pass_single, stream)
     if bt.bt_last_device_error() != bt.BT_OK:
         raise RuntimeError("device error during capture")
-
-    def replay():
-        graph.replay()
 
     with torch.cuda.stream(stream):
         t_pass, clocks = timed(torch, dist, stream, replay, args.steps, args.warmup, local_rank)
@@ -855,11 +933,20 @@ def main():
     def run_pass_e2e():
         for g in e2e_groups:
             bt.bt_qgemv_batched(g, bits)
-    g_e2e = capture(torch, run_pass_e2e, stream)
+    if EAGER:
+        e2e_run = capture(torch, run_pass_e2e, stream).replay
+    else:
+        e2e_pass = bt.bt_pass_create([as_rows(g) for g in e2e_groups], bits)
+        with torch.cuda.stream(stream):
+            e2e_pass.run(stream)
+        torch.cuda.synchronize()
+
+        def e2e_run():
+            e2e_pass.run(stream)
 
     def e2e_step():
         x_all.copy_(x_host, non_blocking=True)
-        g_e2e.replay()
+        e2e_run()
         y_host.copy_(y_all, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 200))
@@ -889,8 +976,8 @@ def main():
         "clocks": clocks,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(y_total * 4),
-                "how": "per step: pinned H2D of all 197 activation vectors, the pass (CUDA graph of 1 "
-                       "bt_qgemv_batched launch), D2H of all outputs"},
+                "how": "per step: pinned H2D of all 197 activation vectors, the pass (bt_pass_run: the "
+                       "library's CUDA graph of 1 batched GEMV launch), D2H of all outputs"},
         "gpu_launches": launches * args.steps,
         "per_gemv_graph": {"gbs": round(single_gbs, 2) if single_gbs else None, "launches_per_pass": len(bufs),
                            "how": "the same pass as 197 bt_qgemv launches in one CUDA graph with PDL"},
@@ -907,6 +994,9 @@ def main():
         out["moe"] = run_moe(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
     if "small" in legs:
         out["small_batch"] = run_small(torch, bt, dev, stream, args.steps, args.warmup, local_rank, hbm)
+    if "chain" in legs:
+        out["dependent_pass"] = run_chain(torch, bt, bufs, dev, stream, args.steps, args.warmup, local_rank, hbm,
+                                          pass_bytes)
     if rank == 0:
         print(json.dumps(out))
     if dist is not None:

@@ -37,7 +37,7 @@ BT_F16, BT_BF16, BT_F32 = 0, 1, 2
 EXPORTS = ("bt_qgemv", "bt_qgemv_batched", "bt_qgemm", "bt_qgemm_batched", "bt_moe_qgemm", "bt_moe_qgemm_swiglu", "bt_moe_qgemv_pairs",
            "bt_moe_down_combine",
            "bt_moe_route", "bt_swiglu", "bt_moe_combine", "bt_status_string", "bt_last_device_error", "bt_set_option",
-           "bt_plan_gemv", "bt_plan_gemv_batch", "bt_plan_gemm")
+           "bt_plan_gemv", "bt_plan_gemv_batch", "bt_plan_gemm", "bt_pass_create", "bt_pass_run", "bt_pass_destroy")
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -60,6 +60,15 @@ class GemmProblem(ctypes.Structure):
 
 
 lib.bt_qgemm_batched.argtypes = [ctypes.POINTER(GemmProblem), _i, _i, _i, _i, _i, _i, _p]
+
+
+class PassStage(ctypes.Structure):
+    _fields_ = [("problems", ctypes.POINTER(GemmProblem)), ("count", _i)]
+
+
+lib.bt_pass_create.argtypes = [ctypes.POINTER(PassStage), _i, _i, _i, _i, _i, _i, ctypes.POINTER(_p)]
+lib.bt_pass_run.argtypes = [_p, _p]
+lib.bt_pass_destroy.argtypes = [_p]
 lib.bt_moe_qgemm.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
 lib.bt_moe_qgemm_swiglu.argtypes = _W + [_i, _i, _i, _p, _i, _p, _p, _i, _p, _i, _p]
 lib.bt_moe_qgemv_pairs.argtypes = _W + [_i, _i, _i, _p, _i, _i, _p, _i, _p, _i, _i, _p]
@@ -94,8 +103,9 @@ class GemmPlan(ctypes.Structure):
 lib.bt_plan_gemm.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(GemmPlan)]
 GEMM_PATHS = {0: "none", 1: "gemv", 2: "simt", 3: "tc", 4: "mma"}
 for _name in EXPORTS:
-    if _name != "bt_status_string":
+    if _name not in ("bt_status_string", "bt_pass_destroy"):
         getattr(lib, _name).restype = _i
+lib.bt_pass_destroy.restype = None
 
 _DT = {torch.float16: BT_F16, torch.bfloat16: BT_BF16, torch.float32: BT_F32}
 
@@ -270,23 +280,79 @@ def bt_qgemm_batched(problems, bits: int, *, group_size: int = 64, stream=None):
     """
     m = problems[0][3].shape[0]
     x0, y0 = problems[0][3], problems[0][4]
+    arr = _gemm_table(problems, bits, group_size, m, x0, y0, "")
+    _check(lib.bt_qgemm_batched(arr, len(problems), bits, group_size, m, _dt(x0), _dt(y0), _stream(stream)),
+           "bt_qgemm_batched")
+    return [pr[4] for pr in problems]
+
+
+def _gemm_table(problems, bits, group_size, m, x0, y0, where):
+    """Checks one list of ``(codes, scales, biases, x, y)`` products and marshals it."""
     for i, (c, s, b, x, y) in enumerate(problems):   # every entry is checked before any is marshalled
         try:
             _need(x.dim() == 2 and x.shape[0] == m, f"x must be [M={m}, K], got shape {list(x.shape)}")
-            k = x.shape[1]
-            n = check_weight(c, s, b, bits, k, group_size)
+            n = check_weight(c, s, b, bits, x.shape[1], group_size)
             _check_out(y, "y", m * n)
             _need(x.dtype == x0.dtype and y.dtype == y0.dtype, "every problem must share x and y dtypes")
             _same_device(c, s, b, x, y, x0)
         except ValueError as err:
-            raise ValueError(f"problem {i}: {err}") from None
+            raise ValueError(f"{where}problem {i}: {err}") from None
     arr = (GemmProblem * len(problems))()
     for i, (c, s, b, x, y) in enumerate(problems):
         cw, sw, bw = _weights(c, s, b)
         arr[i] = GemmProblem(cw, sw, bw, _dev(x, "x"), _dev(y, "y"), c.shape[0], x.shape[1])
-    _check(lib.bt_qgemm_batched(arr, len(problems), bits, group_size, m, _dt(x0), _dt(y0), _stream(stream)),
-           "bt_qgemm_batched")
-    return [pr[4] for pr in problems]
+    return arr
+
+
+class DecodePass:
+    """A planned decode pass (``bt_pass_create``); holds the tensors it reads and writes."""
+
+    def __init__(self, handle, tensors):
+        self._handle = handle
+        self._tensors = tensors   # the pass reads and writes these buffers for its whole life
+
+    def run(self, stream=None):
+        bt_pass_run(self, stream=stream)
+
+    def close(self):
+        bt_pass_destroy(self)
+
+    def __del__(self):
+        try:
+            bt_pass_destroy(self)
+        except Exception:   # interpreter shutdown: the library may already be unloaded
+            pass
+
+
+def bt_pass_create(stages, bits: int, *, group_size: int = 64):
+    """Plans an ordered list of stages once; ``stages`` is a list of lists of
+    ``(codes, scales, biases, x [M, K], y [M, N])`` products with one common M and
+    common dtypes.  A stage may read what an earlier stage writes; runs write
+    the same y buffers and read the x buffers as they are at the time."""
+    _need(len(stages) > 0 and all(len(st) > 0 for st in stages), "every stage needs at least one product")
+    first = stages[0][0]
+    m, x0, y0 = first[3].shape[0], first[3], first[4]
+    tables = [_gemm_table(st, bits, group_size, m, x0, y0, f"stage {si}: ") for si, st in enumerate(stages)]
+    arr = (PassStage * len(stages))()
+    for si, t in enumerate(tables):
+        arr[si] = PassStage(ctypes.cast(t, ctypes.POINTER(GemmProblem)), len(t))
+    handle = _p()
+    _check(lib.bt_pass_create(arr, len(stages), bits, group_size, m, _dt(x0), _dt(y0), ctypes.byref(handle)),
+           "bt_pass_create")
+    return DecodePass(handle, [t for st in stages for pr in st for t in pr])
+
+
+def bt_pass_run(dpass: DecodePass, stream=None):
+    """Launches the pass on ``stream`` (the first run also records it as a CUDA graph)."""
+    _need(dpass._handle is not None, "the pass was destroyed")
+    _check(lib.bt_pass_run(dpass._handle, _stream(stream)), "bt_pass_run")
+
+
+def bt_pass_destroy(dpass: DecodePass):
+    """Frees the pass (its graph and stream); the tensors stay the caller's."""
+    if dpass._handle is not None:
+        lib.bt_pass_destroy(dpass._handle)
+        dpass._handle = None
 
 
 def bt_moe_qgemm(codes, scales, biases, bits: int, expert_offsets, x, y=None, *, total_rows=None,

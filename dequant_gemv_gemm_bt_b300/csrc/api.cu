@@ -3,7 +3,9 @@
 // library; nothing here computes on the host.
 #include <algorithm>
 #include <cstdlib>
+#include <memory>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "bt_common.cuh"
@@ -388,8 +390,17 @@ bt_status bt_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t
   return run_gemv(codes, scales, biases, bits, group_size, N, K, x, x_dtype, y, y_dtype, 1, RowMap{}, stream);
 }
 
-bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
-                           bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
+namespace bt {
+// A validated and planned batched GEMV (no launch).  The run-time fields of p
+// (error word, wait bound, PDL weight hint, test hook) are set at each launch.
+struct PreparedGemv {
+  GemvBatch<kBatchCap> batch;
+  GemvParams p;
+  GemvPlan pl;
+};
+
+bt_status prepare_gemv_batch(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
+                             bt_dtype x_dtype, bt_dtype y_dtype, PreparedGemv& g) {
   if (!problems || count < 1 || K < 0) return BT_ERR_INVALID_ARG;
   if (count > kBatchCap) return BT_ERR_UNSUPPORTED;
   if (!half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
@@ -406,7 +417,7 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
     rows += q.n;
     max_n = std::max(max_n, q.n);
   }
-  GemvBatch<kBatchCap> batch;
+  GemvBatch<kBatchCap>& batch = g.batch;
   batch.count = count;
   for (int i = 0; i < count; ++i) {
     GemvProblem& b = batch.prob[i];
@@ -419,17 +430,13 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
     b.n = problems[i].n;
     b.k = mixed ? problems[i].k : 0;   // 0: the launch plan's K and geometry
   }
-  GemvParams p{};
-  p.K = K;
-  p.G = param_groups(bits, K, group_size);
-  p.gshift = group_shift(group_size);
-  p.N = max_n;
-  p.err = device_error_word();
-  p.timeout_ns = opts().wait_timeout_ns;
-  p.const_weights = opts().pdl && opts().const_weights;
-  p.drop_stage = opts().test_drop_stage.exchange(0);
+  g.p = GemvParams{};
+  g.p.K = K;
+  g.p.G = param_groups(bits, K, group_size);
+  g.p.gshift = group_shift(group_size);
+  g.p.N = max_n;
   const bool fast = gemv_fast_path(bits, x_dtype);
-  GemvPlan pl;
+  GemvPlan& pl = g.pl;
   if (mixed) {
     pl = plan_gemv_batch_mma(bits, fast, batch, sm_count(), group_size);
     if (!pl.feasible) pl = plan_gemv_batch(bits, fast, batch, sm_count(), group_size);
@@ -442,19 +449,39 @@ bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits,
     pl = all_mma ? plan_gemv_mma(bits, fast, max_n, K, problems_equiv, 0, sm_count(), group_size) : GemvPlan{};
     if (!pl.feasible) pl = plan_gemv(bits, fast, max_n, K, problems_equiv, 0, sm_count(), group_size);
   }
-  if (!pl.feasible) {
-    // No single launch holds this batch (a row group or K beyond one launch's
-    // staging): each problem runs as its own bt_qgemv, which accepts every shape
-    // the checks above pass.
+  return BT_OK;
+}
+
+// Launches a prepared batch; a batch no single launch holds (a row group or K
+// beyond one launch's staging) runs each problem as its own bt_qgemv, which
+// accepts every shape the checks passed.
+bt_status run_prepared_gemv(const PreparedGemv& g, const bt_gemv_problem* problems, int count, int bits,
+                            int group_size, int K, bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
+  if (!g.pl.feasible) {
     for (int i = 0; i < count; ++i) {
       const bt_gemv_problem& q = problems[i];
-      const bt_status st = run_gemv(q.codes, q.scales, q.biases, bits, group_size, q.n, mixed ? q.k : K, q.x,
+      const bt_status st = run_gemv(q.codes, q.scales, q.biases, bits, group_size, q.n, K == 0 ? q.k : K, q.x,
                                     x_dtype, q.y, y_dtype, 1, RowMap{}, stream);
       if (st != BT_OK) return st;
     }
     return BT_OK;
   }
-  return cuda_status(launch_gemv(p, pl, bits, x_dtype, y_dtype, stream, &batch));
+  GemvParams p = g.p;
+  p.err = device_error_word();
+  p.timeout_ns = opts().wait_timeout_ns;
+  p.const_weights = opts().pdl && opts().const_weights;
+  p.drop_stage = opts().test_drop_stage.exchange(0);
+  GemvBatch<kBatchCap> batch = g.batch;
+  return cuda_status(launch_gemv(p, g.pl, bits, x_dtype, y_dtype, stream, &batch));
+}
+}  // namespace bt
+
+bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
+                           bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
+  std::unique_ptr<PreparedGemv> g(new PreparedGemv);
+  const bt_status s = prepare_gemv_batch(problems, count, bits, group_size, K, x_dtype, y_dtype, *g);
+  if (s != BT_OK) return s;
+  return run_prepared_gemv(*g, problems, count, bits, group_size, K, x_dtype, y_dtype, stream);
 }
 
 bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
@@ -479,8 +506,27 @@ bt_status bt_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t
   return cuda_status(launch_gemm_simt(p, bits, x_dtype, y_dtype, stream));
 }
 
-bt_status bt_qgemm_batched(const bt_gemm_problem* problems, int count, int bits, int group_size, int M,
-                           bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
+namespace bt {
+// One launch of a batched product list (or, where no single launch holds a
+// chunk, one launch per product), prepared once and launched many times.
+struct PassStep {
+  enum Kind { kGemv, kSmall, kEach } kind = kEach;
+  std::unique_ptr<PreparedGemv> gemv;
+  SmallBatchPrepared* small = nullptr;
+  std::vector<bt_gemv_problem> gp;     // kGemv: the chunk, for the per-problem fallback
+  std::vector<bt_gemm_problem> each;   // kEach: the chunk
+  PassStep() = default;
+  PassStep(PassStep&& o) noexcept
+      : kind(o.kind), gemv(std::move(o.gemv)), small(std::exchange(o.small, nullptr)), gp(std::move(o.gp)),
+        each(std::move(o.each)) {}
+  PassStep(const PassStep&) = delete;
+  ~PassStep() {
+    if (small) free_gemm_small_batched(small);
+  }
+};
+
+bt_status check_gemm_list(const bt_gemm_problem* problems, int count, int bits, int group_size, int M,
+                          bt_dtype x_dtype, bt_dtype y_dtype) {
   if (!problems || count < 1 || M < 1 || !half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     const bt_gemm_problem& q = problems[i];
@@ -489,45 +535,174 @@ bt_status bt_qgemm_batched(const bt_gemm_problem* problems, int count, int bits,
     if (!q.x || !q.y) return BT_ERR_INVALID_ARG;
     if (!aligned16(q.x)) return BT_ERR_MISALIGNED;
   }
-  if (M == 1) {   // one token: the batched GEMV
+  return BT_OK;
+}
+
+// Splits a checked product list into launches: M = 1 takes the batched GEMV
+// (kBatchCap problems per launch); up to 16 rows take the small-token kernel
+// (where a single product of 9..16 rows would take the tensor cores, a table
+// of them is launch-bound); the rest run one product per launch.
+bt_status plan_steps(const bt_gemm_problem* problems, int count, int bits, int group_size, int M, bt_dtype x_dtype,
+                     bt_dtype y_dtype, std::vector<PassStep>& steps) {
+  if (M == 1) {
     for (int i0 = 0; i0 < count; i0 += kBatchCap) {
       const int c = std::min(kBatchCap, count - i0);
-      std::vector<bt_gemv_problem> gp((size_t)c);
+      PassStep st;
+      st.kind = PassStep::kGemv;
+      st.gp.resize((size_t)c);
       for (int i = 0; i < c; ++i) {
         const bt_gemm_problem& q = problems[i0 + i];
-        gp[i] = bt_gemv_problem{q.codes, q.scales, q.biases, q.x, q.y, q.n, q.k};
+        st.gp[i] = bt_gemv_problem{q.codes, q.scales, q.biases, q.x, q.y, q.n, q.k};
       }
-      const bt_status s = bt_qgemv_batched(gp.data(), c, bits, group_size, 0, x_dtype, y_dtype, stream);
+      st.gemv.reset(new PreparedGemv);
+      const bt_status s = prepare_gemv_batch(st.gp.data(), c, bits, group_size, 0, x_dtype, y_dtype, *st.gemv);
       if (s != BT_OK) return s;
+      steps.push_back(std::move(st));
     }
     return BT_OK;
   }
-  // one small-token launch for the table up to 16 rows (where a single product
-  // of 9..16 rows would take the tensor cores, a table of them is launch-bound)
   const int forced = opts().gemm_path;
   const bool small_ok = (forced == 0 && M <= 16) || forced == 3;
   for (int i0 = 0; i0 < count; i0 += small::kBatchLaunchCap) {
     const int c = std::min(small::kBatchLaunchCap, count - i0);
+    PassStep st;
+    st.each.assign(problems + i0, problems + i0 + c);
     std::vector<GemmProblem> gp((size_t)c);
     for (int i = 0; i < c; ++i) {
       const bt_gemm_problem& q = problems[i0 + i];
       gp[i] = GemmProblem{q.codes, q.scales, q.biases, q.x, q.y, q.n, q.k};
     }
     if (small_ok && small_batch_supported(gp.data(), c, M, bits, group_size)) {
-      const bt_status s = cuda_status(launch_gemm_small_batched(gp.data(), c, M, x_dtype, y_dtype, device_error_word(),
-                                                                opts().wait_timeout_ns, stream));
-      if (s != BT_OK) return s;
-      continue;
+      st.small = prepare_gemm_small_batched(gp.data(), c, M, x_dtype, y_dtype);
+      if (!st.small) return BT_ERR_INVALID_ARG;
+      st.kind = PassStep::kSmall;
     }
-    for (int i = 0; i < c; ++i) {   // one product per launch
-      const bt_gemm_problem& q = problems[i0 + i];
-      const bt_status s = bt_qgemm(q.codes, q.scales, q.biases, bits, group_size, M, q.n, q.k, q.x, x_dtype, q.y,
-                                   y_dtype, stream);
-      if (s != BT_OK) return s;
-    }
+    steps.push_back(std::move(st));
   }
   return BT_OK;
 }
+
+bt_status run_steps(const std::vector<PassStep>& steps, int bits, int group_size, int M, bt_dtype x_dtype,
+                    bt_dtype y_dtype, cudaStream_t stream) {
+  for (const PassStep& st : steps) {
+    bt_status s = BT_OK;
+    if (st.kind == PassStep::kGemv) {
+      s = run_prepared_gemv(*st.gemv, st.gp.data(), (int)st.gp.size(), bits, group_size, 0, x_dtype, y_dtype, stream);
+    } else if (st.kind == PassStep::kSmall) {
+      s = cuda_status(run_gemm_small_batched(st.small, device_error_word(), opts().wait_timeout_ns, stream));
+    } else {
+      for (const bt_gemm_problem& q : st.each) {
+        s = bt_qgemm(q.codes, q.scales, q.biases, bits, group_size, M, q.n, q.k, q.x, x_dtype, q.y, y_dtype, stream);
+        if (s != BT_OK) break;
+      }
+    }
+    if (s != BT_OK) return s;
+  }
+  return BT_OK;
+}
+}  // namespace bt
+
+bt_status bt_qgemm_batched(const bt_gemm_problem* problems, int count, int bits, int group_size, int M,
+                           bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream) {
+  bt_status s = check_gemm_list(problems, count, bits, group_size, M, x_dtype, y_dtype);
+  if (s != BT_OK) return s;
+  std::vector<PassStep> steps;
+  s = plan_steps(problems, count, bits, group_size, M, x_dtype, y_dtype, steps);
+  if (s != BT_OK) return s;
+  return run_steps(steps, bits, group_size, M, x_dtype, y_dtype, stream);
+}
+
+// ------------------------------------------------------------------ decode pass
+struct bt_pass {
+  int device = 0;
+  int bits = 0, group = 0, M = 0;
+  bt_dtype xd = BT_F16, yd = BT_F32;
+  std::vector<std::vector<bt::PassStep>> stages;
+  cudaStream_t capture = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  bool ran = false;
+  ~bt_pass() {
+    if (exec) cudaGraphExecDestroy(exec);
+    if (graph) cudaGraphDestroy(graph);
+    if (capture) cudaStreamDestroy(capture);
+  }
+};
+
+bt_status bt_pass_create(const bt_pass_stage* stages, int num_stages, int bits, int group_size, int M,
+                         bt_dtype x_dtype, bt_dtype y_dtype, bt_pass** pass) {
+  if (!pass) return BT_ERR_INVALID_ARG;
+  *pass = nullptr;
+  if (!stages || num_stages < 1) return BT_ERR_INVALID_ARG;
+  for (int s = 0; s < num_stages; ++s) {   // every check before any CUDA call
+    const bt_status st = check_gemm_list(stages[s].problems, stages[s].count, bits, group_size, M, x_dtype, y_dtype);
+    if (st != BT_OK) return st;
+  }
+  std::unique_ptr<bt_pass> ps(new bt_pass);
+  if (cudaGetDevice(&ps->device) != cudaSuccess) return BT_ERR_CUDA;
+  ps->bits = bits;
+  ps->group = group_size;
+  ps->M = M;
+  ps->xd = x_dtype;
+  ps->yd = y_dtype;
+  ps->stages.resize((size_t)num_stages);
+  for (int s = 0; s < num_stages; ++s) {
+    const bt_status st =
+        plan_steps(stages[s].problems, stages[s].count, bits, group_size, M, x_dtype, y_dtype, ps->stages[s]);
+    if (st != BT_OK) return st;
+  }
+  *pass = ps.release();
+  return BT_OK;
+}
+
+namespace {
+bt_status run_stages(const bt_pass& ps, cudaStream_t stream) {
+  for (const std::vector<bt::PassStep>& st : ps.stages) {
+    const bt_status s = run_steps(st, ps.bits, ps.group, ps.M, ps.xd, ps.yd, stream);
+    if (s != BT_OK) return s;
+  }
+  return BT_OK;
+}
+
+// Records the pass into a CUDA graph on a stream of its own.  Runs after one
+// eager pass, so every kernel is loaded and every per-device setting is made
+// before the capture begins.
+bt_status record_pass(bt_pass& ps) {
+  if (cudaStreamCreateWithFlags(&ps.capture, cudaStreamNonBlocking) != cudaSuccess) return BT_ERR_CUDA;
+  if (cudaStreamBeginCapture(ps.capture, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return BT_ERR_CUDA;
+  const bt_status s = run_stages(ps, ps.capture);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(ps.capture, &g);
+  if (s != BT_OK) {
+    if (g) cudaGraphDestroy(g);
+    return s;
+  }
+  if (e != cudaSuccess) return BT_ERR_CUDA;
+  ps.graph = g;
+  if (cudaGraphInstantiate(&ps.exec, g, 0) != cudaSuccess) {
+    ps.exec = nullptr;
+    return BT_ERR_CUDA;
+  }
+  return BT_OK;
+}
+}  // namespace
+
+bt_status bt_pass_run(bt_pass* pass, cudaStream_t stream) {
+  if (!pass) return BT_ERR_INVALID_ARG;
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return BT_ERR_CUDA;
+  if (d != pass->device) return BT_ERR_INVALID_ARG;
+  if (!pass->ran) {   // first run: eager launches, then the recording
+    const bt_status s = run_stages(*pass, stream);
+    if (s != BT_OK) return s;
+    pass->ran = true;
+    return record_pass(*pass);
+  }
+  if (!pass->exec) return BT_ERR_CUDA;
+  return cuda_status(cudaGraphLaunch(pass->exec, stream));
+}
+
+void bt_pass_destroy(bt_pass* pass) { delete pass; }
 
 bt_status bt_moe_qgemm(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases, int bits,
                        int group_size, int num_experts, int N, int K, const int32_t* expert_offsets,

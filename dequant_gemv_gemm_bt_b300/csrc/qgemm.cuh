@@ -87,6 +87,12 @@ SmallGeometry plan_gemm_small_batched(const GemmProblem* probs, int count, int M
 bool small_batch_supported(const GemmProblem* probs, int count, int M, int bits, int group);
 cudaError_t launch_gemm_small_batched(const GemmProblem* probs, int count, int M, bt_dtype xd, bt_dtype yd,
                                       unsigned* err, unsigned long long timeout_ns, cudaStream_t st);
+// The same, prepared once (plan and tensor maps) and launched many times.
+struct SmallBatchPrepared;
+SmallBatchPrepared* prepare_gemm_small_batched(const GemmProblem* probs, int count, int M, bt_dtype xd, bt_dtype yd);
+cudaError_t run_gemm_small_batched(const SmallBatchPrepared* pb, unsigned* err, unsigned long long timeout_ns,
+                                   cudaStream_t st);
+void free_gemm_small_batched(SmallBatchPrepared* pb);
 
 namespace tc {
 // cuTensorMapEncodeTiled from the driver (null if unavailable).

@@ -30,6 +30,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <memory>
 
 #include "qgemm.cuh"
 #include "qgemv_mma.cuh"
@@ -907,26 +908,33 @@ bool small_batch_supported(const GemmProblem* probs, int count, int M, int bits,
   return plan_gemm_small_batched(probs, count, M, sm_count()).feasible;
 }
 
-cudaError_t launch_gemm_small_batched(const GemmProblem* probs, int count, int M, bt_dtype xd, bt_dtype yd,
-                                      unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
+struct SmallBatchPrepared {
+  small::Layout L;
+  small::TabT<true> tab;
+  small::SmallParams p;
+  bool bf16;
+};
+
+SmallBatchPrepared* prepare_gemm_small_batched(const GemmProblem* probs, int count, int M, bt_dtype xd, bt_dtype yd) {
   using namespace small;
+  if (count < 1 || count > kSmallBatchCap) return nullptr;
   long long rows = 0;
   int kmax = 0;
   for (int i = 0; i < count; ++i) {
     rows += probs[i].N;
     kmax = std::max(kmax, probs[i].K);
   }
-  Layout L = plan_any(4, M, (int)rows, kmax, 64, 0, sm_count());
-  if (!L.geo.feasible || count < 1 || count > kSmallBatchCap) return cudaErrorInvalidValue;
-  L.geo.grid = plan_gemm_small_batched(probs, count, M, sm_count()).grid;
-  if (L.geo.grid < 1) return cudaErrorInvalidValue;
-  static thread_local TabT<true> tab;   // 24.6 KB: copied into the launch's parameters
-  memset(&tab, 0, sizeof(tab));
-  tab.count = count;
+  std::unique_ptr<SmallBatchPrepared> pb(new SmallBatchPrepared);
+  pb->L = plan_any(4, M, (int)rows, kmax, 64, 0, sm_count());
+  if (!pb->L.geo.feasible) return nullptr;
+  pb->L.geo.grid = plan_gemm_small_batched(probs, count, M, sm_count()).grid;
+  if (pb->L.geo.grid < 1) return nullptr;
+  memset(&pb->tab, 0, sizeof(pb->tab));
+  pb->tab.count = count;
   for (int i = 0; i < count; ++i) {
     const GemmProblem& q = probs[i];
-    SmallProblem& d = tab.prob[i];
-    if (!encode_codes_map(&d.map, q.codes, q.N, q.K, 0, L.geo.rb, L.geo.kw)) return cudaErrorInvalidValue;
+    SmallProblem& d = pb->tab.prob[i];
+    if (!encode_codes_map(&d.map, q.codes, q.N, q.K, 0, pb->L.geo.rb, pb->L.geo.kw)) return nullptr;
     d.scales = q.scales;
     d.biases = q.biases;
     d.x = static_cast<const uint16_t*>(q.x);
@@ -934,12 +942,32 @@ cudaError_t launch_gemm_small_batched(const GemmProblem* probs, int count, int M
     d.N = q.N;
     d.K = q.K;
   }
-  SmallParams p = make_params(L, M, yd, err, timeout_ns);
-  p.num_experts = 1;
+  pb->p = make_params(pb->L, M, yd, nullptr, 0);
+  pb->p.num_experts = 1;
+  pb->bf16 = xd == BT_BF16;
+  return pb.release();
+}
+
+cudaError_t run_gemm_small_batched(const SmallBatchPrepared* pb, unsigned* err, unsigned long long timeout_ns,
+                                   cudaStream_t st) {
+  using namespace small;
+  SmallParams p = pb->p;
+  p.err = err;
+  p.timeout_ns = timeout_ns;
+  p.const_weights = opts().pdl && opts().const_weights;
   CUtensorMap unused;
   memset(&unused, 0, sizeof(unused));
-  return xd == BT_BF16 ? launch_nw<true, false, true>(unused, p, tab, L.geo, st)
-                       : launch_nw<false, false, true>(unused, p, tab, L.geo, st);
+  return pb->bf16 ? launch_nw<true, false, true>(unused, p, pb->tab, pb->L.geo, st)
+                  : launch_nw<false, false, true>(unused, p, pb->tab, pb->L.geo, st);
+}
+
+void free_gemm_small_batched(SmallBatchPrepared* pb) { delete pb; }
+
+cudaError_t launch_gemm_small_batched(const GemmProblem* probs, int count, int M, bt_dtype xd, bt_dtype yd,
+                                      unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
+  std::unique_ptr<SmallBatchPrepared> pb(prepare_gemm_small_batched(probs, count, M, xd, yd));
+  if (!pb) return cudaErrorInvalidValue;
+  return run_gemm_small_batched(pb.get(), err, timeout_ns, st);
 }
 
 }  // namespace bt

@@ -149,6 +149,57 @@ BT_API bt_status bt_qgemm_batched(const bt_gemm_problem* problems, int count, in
                                   bt_dtype x_dtype, bt_dtype y_dtype, cudaStream_t stream);
 
 /*
+ * Decode pass: an ordered list of stages of products over buffers the caller
+ * sized once, planned once and then replayed as one CUDA graph per call.
+ * BaseRT pages, gist.science "Metodologia" (the decode loop allocates nothing:
+ * every buffer is sized at load and a step is only GPU dispatch plus light
+ * host-side patching) and thetesserapress.com "What BaseRT does differently"
+ * (residuals, scratch and intermediates pre-sized and reused).
+ *
+ * A stage is a set of independent products with the same M, bits, group size
+ * and dtypes, as for bt_qgemm_batched; stage s + 1 may read what stage s
+ * writes (its x may be an earlier stage's y), and stages run in order.
+ *   stages      HOST array of `num_stages` stage descriptors; each stage's
+ *               `problems` is a HOST array of `count` bt_gemm_problem.  Both
+ *               are read during bt_pass_create only: the pass keeps its own
+ *               copy of every pointer and size.
+ *   pass        receives the new pass; the caller owns it and frees it with
+ *               bt_pass_destroy.
+ * The device pointers inside the problems (weights, x, y) stay the caller's:
+ * they must stay valid, and keep their sizes, for the life of the pass.  The
+ * caller changes a run's inputs by writing new values into the same x
+ * buffers (on the stream it runs the pass on, or before).
+ *
+ * bt_pass_create validates and plans every stage (the checks of
+ * bt_qgemm_batched, the launch tables, the tensor maps) on the host; it
+ * launches nothing.  It binds the pass to the current device.
+ * bt_pass_run launches the pass on `stream`.  The first run launches every
+ * stage directly (this loads the kernels and makes the per-device settings)
+ * and then records the same launches into a CUDA graph on a stream the pass
+ * owns; every later run is one cudaGraphLaunch of that graph, with no host
+ * allocation, no validation and no planning.  The options in force at the
+ * first run (PDL, the constant-weights hint, the wait bound) are the ones the
+ * graph keeps.  Call the first run outside any stream capture; later runs
+ * may themselves be captured.  Runs of one pass on two streams at once race
+ * on the pass's y buffers.
+ * Errors: bt_pass_create returns the first check that fails (as for
+ * bt_qgemm_batched) and sets *pass to NULL; BT_ERR_INVALID_ARG for a NULL
+ * `pass` or `stages` or num_stages < 1.  bt_pass_run returns
+ * BT_ERR_INVALID_ARG for a NULL pass or a current device other than the
+ * pass's, BT_ERR_CUDA when a launch, the recording or the graph launch
+ * fails.  bt_pass_destroy accepts NULL.
+ */
+typedef struct bt_pass bt_pass;
+typedef struct {
+  const bt_gemm_problem* problems;
+  int count;
+} bt_pass_stage;
+BT_API bt_status bt_pass_create(const bt_pass_stage* stages, int num_stages, int bits, int group_size, int M,
+                                bt_dtype x_dtype, bt_dtype y_dtype, bt_pass** pass);
+BT_API bt_status bt_pass_run(bt_pass* pass, cudaStream_t stream);
+BT_API void bt_pass_destroy(bt_pass* pass);
+
+/*
  * Dequant-GEMM, M > 1 (prefill): Y[m, n] = sum_k X[m, k] * w_deq[n, k].
  * BaseRT pages, thetesserapress.com "What BaseRT does differently" (prefill,
  * with several tokens, runs a GEMM) and gist.science "Metodologia" (tiled

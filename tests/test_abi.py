@@ -81,3 +81,23 @@ def test_qgemm_and_moe_validation(bt):
     assert L.bt_moe_route(A, 4, 2, 8, None, A, A, None, None) == 1
     assert L.bt_swiglu(A, 1, 4, 0, A, 1, None) == 1
     assert L.bt_moe_combine(A, 1, A, A, 4, 0, 128, A, 1, None) == 1
+
+
+def test_pass_validation(bt):
+    """bt_pass_create checks every stage before any CUDA call; NULL handles are refused."""
+    L = bt.lib
+    out = ctypes.c_void_p(7)
+    assert L.bt_pass_create(None, 1, 4, 64, 1, 0, 2, ctypes.byref(out)) == 1
+    assert out.value is None                                                   # *pass cleared
+    prob = (bt.GemmProblem * 1)(bt.GemmProblem(A, A, A, A, A, 128, 256))
+    stage = (bt.PassStage * 1)(bt.PassStage(ctypes.cast(prob, ctypes.POINTER(bt.GemmProblem)), 1))
+    assert L.bt_pass_create(stage, 1, 4, 64, 1, 0, 2, None) == 1               # no out pointer
+    assert L.bt_pass_create(stage, 0, 4, 64, 1, 0, 2, ctypes.byref(out)) == 1  # no stages
+    assert L.bt_pass_create(stage, 1, 7, 64, 1, 0, 2, ctypes.byref(out)) == 2  # bits
+    assert L.bt_pass_create(stage, 1, 4, 64, 0, 0, 2, ctypes.byref(out)) == 1  # M = 0
+    assert L.bt_pass_create(stage, 1, 4, 64, 1, 2, 2, ctypes.byref(out)) == 1  # x dtype f32
+    prob[0].n = 0
+    assert L.bt_pass_create(stage, 1, 4, 64, 1, 0, 2, ctypes.byref(out)) == 1  # n = 0
+    assert out.value is None
+    assert L.bt_pass_run(None, None) == 1
+    L.bt_pass_destroy(None)

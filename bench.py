@@ -285,6 +285,14 @@ def oracle_rate(tag, shapes, budget_s: float, procs: int = 0, warmup_s: float = 
 
 
 # ------------------------------------------------------------------ GPU legs
+def gemv_kernel_name(bt, bits):
+    """The kernel the library plans for the decode pass's one batched launch."""
+    p, _ = bt.bt_plan_gemv_batch(bits, [(n, k) for _, n, k in decode_pass_shapes()])
+    kind = {0: "qgemv_kernel (CUDA cores", 1: "qgemv_mma_kernel (tensor pipe, diagonal consumer",
+            2: "qgemv_mma_kernel (tensor pipe, four-column consumer"}[p["tensor_pipe"]]
+    return kind + "; batched, mixed K; 1 launch per pass)"
+
+
 def build_decode_pass(torch, bt, weights, xs16, dev):
     bufs = []
     for qw, x16 in zip(weights, xs16):
@@ -968,7 +976,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "u4 codes, f16 x, f32 accumulate",
         "data": "synthetic (seeded N(0,0.02) weights, min/max Q4 g64; x ~ N(0,1) fp16)",
         "config": config,
-        "roofline": {"bound": "hbm", "kernel": "qgemv_kernel (batched, mixed K; 1 launch per pass)",
+        "roofline": {"bound": "hbm", "kernel": gemv_kernel_name(bt, bits),
                      "achieved": round(achieved, 2), "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s",
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "traffic": traffic, "kernel_source_digest": digest},

@@ -226,7 +226,7 @@ using namespace bt;
 namespace {
 void fill_plan(const bt::GemvPlan& pl, bt_gemv_plan* out) {
   out->feasible = pl.feasible ? 1 : 0;
-  out->tensor_pipe = pl.mma ? 1 : 0;
+  out->tensor_pipe = pl.mma ? (pl.mma_cols4 ? 2 : 1) : 0;
   out->kw = pl.kw;
   out->cpl = pl.cpl;
   out->ri = pl.ri;
@@ -355,7 +355,7 @@ bt_status bt_set_option(bt_option option, long long value) {
     case BT_OPT_GEMV_STAGE_KB: opts().gemv_stage_kb = value == 0 ? 0 : (int)std::max(4LL, std::min(value, 96LL)); return BT_OK;
     case BT_OPT_GEMV_CUDA_CORE: opts().gemv_cuda_core = value != 0; return BT_OK;
     case BT_OPT_GEMV_MMA_STAGE_KB: opts().gemv_mma_stage_kb = value == 0 ? 0 : (int)std::max(8LL, std::min(value, 112LL)); return BT_OK;
-    case BT_OPT_GEMV_MMA_SHAPE: opts().gemv_mma_cfg = (int)std::min(value, 4LL); return BT_OK;
+    case BT_OPT_GEMV_MMA_SHAPE: opts().gemv_mma_cfg = (int)std::min(value, 7LL); return BT_OK;
     case BT_OPT_GEMV_TENSOR_PIPE: opts().gemv_tensor_pipe = (int)std::min(value, 2LL); return BT_OK;
     case BT_OPT_GEMM_DEQ_WARPS: opts().gemm_deq_warps = (int)value; return BT_OK;
     case BT_OPT_GEMM_SMALL_WARPS: opts().gemm_small_warps = (int)value; return BT_OK;

@@ -115,6 +115,9 @@ MmaShape mma_shape(int cfg) {
     case 2: return {8, 1, 1};
     case 3: return {16, 1, 1};
     case 4: return {8, 2, 1};
+    case 5: return {8, 1, 1, true};
+    case 6: return {8, 2, 1, true};
+    case 7: return {16, 1, 1, true};
     default: return {8, 1, 2};
   }
 }
@@ -132,16 +135,35 @@ bool mma_applies(int bits, bool fast, int N, int K, int group) {
   return ((long long)N * G * 2) % 16 == 0 && ((long long)N * row_bytes) % 16 == 0;
 }
 
-// Which launches take the tensor pipe by default.  Measured on B300 (decode
-// pass, lm_head, single N=2048 GEMV): with many 16-row tiles per SM the
-// CUDA-core kernel streams faster (4.08 vs 3.69 TB/s on the decode pass), while
-// a launch of at most one tile per SM runs faster on the tensor pipe, whose
-// warps then split K down to one group each (single Q4 GEMV N=2048 K=1024:
-// 2.72 vs 3.44 us).  BT_OPT_GEMV_TENSOR_PIPE 1 forces it wherever it applies,
-// 2 disables it.
-bool mma_by_size(long long rows, int sms) {
-  if (opts().gemv_tensor_pipe.load() == 1) return true;
-  return (rows + 15) / 16 <= sms;
+// Which launches take the tensor pipe, and with which consumer, by default.
+// Measured on B300:
+//  * a launch of at most one 16-row tile per SM: the diagonal consumer, whose
+//    warps then split K down to one group each (single Q4 GEMV N=2048 K=1024:
+//    2.72 vs 3.44 us on the CUDA-core kernel);
+//  * launches of at least eight tiles per SM (one per consumer warp) with every
+//    K a multiple of 256 and at most 4096: the four-column consumer with two
+//    large stages (Qwen3-0.6B-shaped decode pass: 4.63-4.68 vs 4.07 TB/s on the
+//    CUDA-core kernel; the diagonal consumer 3.69).  With K = 8192 in the launch
+//    the x of the longest row leaves smaller stages (Llama-1B-shaped pass at
+//    Q4: 4.20 vs 4.31 TB/s on the CUDA-core kernel);
+//  * the launches in between (a few tiles per SM, which would leave consumer
+//    warps of the four-column kernel idle) and other large launches: the
+//    CUDA-core kernel.
+// BT_OPT_GEMV_TENSOR_PIPE 1 forces the tensor pipe wherever it applies, 2
+// disables it; BT_OPT_GEMV_MMA_SHAPE forces a kernel shape.
+bool mma_small_launch(long long rows, int sms) { return (rows + 15) / 16 <= sms; }
+
+// The shape a tensor-pipe launch takes; nw == 0: the launch stays on the CUDA-core kernel.
+MmaShape pick_shape(long long rows, int sms, bool all_k_by_4, int g_max) {
+  const int cfg = opts().gemv_mma_cfg.load();
+  if (cfg != 0) {
+    const MmaShape sh = mma_shape(cfg);
+    return sh.cols4 && !all_k_by_4 ? mma_shape(0) : sh;
+  }
+  if (mma_small_launch(rows, sms)) return mma_shape(0);
+  if (all_k_by_4 && g_max <= 64 && (rows + 15) / 16 >= 8LL * sms) return mma_shape(5);
+  if (opts().gemv_tensor_pipe.load() == 1) return mma_shape(0);
+  return MmaShape{0, 0, 0, false};
 }
 
 struct MmaGeom {
@@ -152,30 +174,26 @@ struct MmaGeom {
 // than the CTA has warps, K is split further (down to one group per warp), so
 // that every warp has work (e.g. the single N=2048 GEMV: one tile per CTA,
 // eight warps on two groups each).
-MmaGeom mma_geom(int bits, int N, int K, long long per_sm_rows, int stage_budget, int nw) {
+MmaGeom mma_geom(int bits, int N, int K, long long per_sm_rows, int stage_budget, int nw, bool cols4 = false) {
   MmaGeom m{};
   const int G = K / kGroup;
+  m.row_bytes = K * bits / 8;
+  m.per_row = m.row_bytes + 4 * G;
+  const int tile = 16 * m.per_row;
+  const long long tiles_per_sm = std::max<long long>(1, per_sm_rows / 16);
+  const int split_units = cols4 ? G / 4 : G;   // the four-column consumer splits K in blocks of four groups
   const int o_gemv_mma_ks = opts().gemv_mma_ks.load();
   const int ks_max = o_gemv_mma_ks > 0 ? o_gemv_mma_ks : 32;
   int kw = 1;
   while (kw < nw && (G + kw - 1) / kw > ks_max) kw *= 2;
-  const long long tiles_per_sm = std::max<long long>(1, per_sm_rows / 16);
-  while (kw < nw && kw * tiles_per_sm < nw && 2 * kw <= G) kw *= 2;
+  while (kw < nw && kw * tiles_per_sm < nw && 2 * kw <= split_units) kw *= 2;
+  while (kw > 1 && kw > split_units) kw /= 2;
   m.kw = kw;
-  m.row_bytes = K * bits / 8;
-  m.per_row = m.row_bytes + 4 * G;
-  const int tile = 16 * m.per_row;
   long long tiles = std::max(1, stage_budget / tile);
   tiles = std::min<long long>(tiles, std::max<long long>(1, (per_sm_rows + 15) / 16));
   tiles = std::min<long long>(tiles, (N + 15) / 16);
   m.rb = (int)(16 * tiles);
   return m;
-}
-
-int mma_stage_budget(const MmaShape& sh) {
-  const int o_gemv_mma_stage_kb = opts().gemv_mma_stage_kb.load();
-  if (o_gemv_mma_stage_kb > 0) return o_gemv_mma_stage_kb * 1024;
-  return sh.ctas == 1 ? 48 * 1024 : 24 * 1024;
 }
 
 // Shared memory of one CTA: ring, barriers, row-group partials, x sums, permuted x.
@@ -184,6 +202,19 @@ size_t mma_smem(int stages, int stage, int g_max, int nw, int* xsum_bytes) {
   if (xsum_bytes) *xsum_bytes = xsb;
   return (size_t)stages * stage + 2 * stages * sizeof(uint64_t) + (size_t)nw * 2 * 16 * sizeof(float) + xsb +
          (size_t)g_max * 192;
+}
+
+int mma_stage_budget(const MmaShape& sh, int g_max) {
+  const int o_gemv_mma_stage_kb = opts().gemv_mma_stage_kb.load();
+  if (o_gemv_mma_stage_kb > 0) return o_gemv_mma_stage_kb * 1024;
+  if (sh.cols4) {
+    // the four-column consumer streams fastest from two stages as large as fit
+    // beside the x of the longest K (decode pass on B300: 4.68 TB/s at 108 KiB
+    // stages, 4.47 at 96, 3.86 at 48; three stages of 64 KiB 4.45)
+    const long long room = (long long)mma_smem_limit(sh.ctas) - (long long)mma_smem(2, 0, g_max, sh.nw, nullptr);
+    return (int)std::max<long long>(16 * 1024, std::min<long long>(112 * 1024, room / 2 / 1024 * 1024));
+  }
+  return sh.ctas == 1 ? 48 * 1024 : 24 * 1024;
 }
 
 int mma_stages(int stage, int g_max, const MmaShape& sh) {
@@ -198,7 +229,9 @@ void set_shape(GemvPlan& pl, const MmaShape& sh) {
   pl.mma_nw = sh.nw;
   pl.mma_ctas = sh.ctas;
   pl.mma_unroll = sh.unroll;
+  pl.mma_cols4 = sh.cols4;
 }
+
 }  // namespace
 
 GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_experts, int sms, int group) {
@@ -208,11 +241,11 @@ GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_
   pl.cpl = 1;
   pl.ri = 16;
   if (num_experts || !mma_applies(bits, fast, N, K, group)) return pl;
-  if (!mma_by_size((long long)N * problems, sms)) return pl;
-  const MmaShape sh = mma_shape(opts().gemv_mma_cfg.load());
+  const MmaShape sh = pick_shape((long long)N * problems, sms, (K / kGroup) % 4 == 0, K / kGroup);
+  if (sh.nw == 0) return pl;
   set_shape(pl, sh);
   const long long per_sm = std::max<long long>(1, ((long long)N * problems + sms - 1) / sms);
-  const MmaGeom m = mma_geom(bits, N, K, per_sm / sh.ctas, mma_stage_budget(sh), sh.nw);
+  const MmaGeom m = mma_geom(bits, N, K, per_sm / sh.ctas, mma_stage_budget(sh, K / kGroup), sh.nw, sh.cols4);
   pl.kw = m.kw;
   pl.rows_per_unit = m.rb;
   pl.row_bytes = m.row_bytes;
@@ -241,14 +274,16 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
     rows += q.n;
     g_max = std::max(g_max, q.k / kGroup);
   }
-  if (!mma_by_size(rows, sms)) return pl;
-  const MmaShape sh = mma_shape(opts().gemv_mma_cfg.load());
+  bool all_k_by_4 = true;
+  for (int i = 0; i < batch.count; ++i) all_k_by_4 = all_k_by_4 && (batch.prob[i].k / kGroup) % 4 == 0;
+  const MmaShape sh = pick_shape(rows, sms, all_k_by_4, g_max);
+  if (sh.nw == 0) return pl;
   set_shape(pl, sh);
   const long long per_sm = std::max<long long>(1, (rows + sms - 1) / sms);
   int stage = 0;
   for (int i = 0; i < batch.count; ++i) {
     GemvProblem& q = batch.prob[i];
-    const MmaGeom m = mma_geom(bits, q.n, q.k, per_sm / sh.ctas, mma_stage_budget(sh), sh.nw);
+    const MmaGeom m = mma_geom(bits, q.n, q.k, per_sm / sh.ctas, mma_stage_budget(sh, g_max), sh.nw, sh.cols4);
     q.kw = m.kw;
     q.g = q.k / kGroup;
     q.row_bytes = m.row_bytes;
@@ -350,10 +385,15 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
       q.units = (q.n + q.rb - 1) / q.rb;
       q.unit_begin = u;
       u += q.units;
-      // CTAs take equal shares of work, not of units: a row split over kw warps
-      // costs kw times a one-warp row (measured: K=2048 ~2.2x, K=3072 ~4x K=1024)
+      // CTAs take equal shares of work, not of units.  On the CUDA-core kernel a
+      // row split over kw warps costs kw times a one-warp row (measured: K=2048
+      // ~2.2x, K=3072 ~4x K=1024); on the tensor-pipe kernel a row costs its
+      // groups (every warp's share of a row is whole groups, and the measured
+      // per-SM busy time with the kw weighting varied from 0.64 to 0.96 of the
+      // launch on the decode pass).
+      q.cw = pl.mma ? std::max(1, q.g) : q.kw;
       q.cost_begin = cost;
-      cost += (long long)q.n * q.kw;
+      cost += (long long)q.n * q.cw;
     }
     p.total_cost = cost;
     p.num_units = u;

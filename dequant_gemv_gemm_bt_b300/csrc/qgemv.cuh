@@ -64,9 +64,10 @@ struct GemvProblem {
   void* y;
   int n;
   int k, g, row_bytes, kw, rb;
+  int cw;             // work of one row for the CTA split: kw (CUDA-core kernel) or g (tensor-pipe kernel)
   int units;          // row blocks of this problem (rb rows each)
   long long unit_begin;
-  long long cost_begin;   // work of the problems before this one (rows x warps per row)
+  long long cost_begin;   // work of the problems before this one (rows x cw)
 };
 template <int CAP> struct GemvBatch {
   int count;
@@ -77,6 +78,7 @@ struct GemvPlan {
   bool fast;
   bool mma;        // the tensor-pipe kernel (qgemv_mma.cuh) rather than the CUDA-core one
   int mma_nw, mma_ctas, mma_unroll;   // its consumer warps per CTA, CTAs per SM, steps per loop iteration
+  bool mma_cols4;  // its four-column consumer (four groups per MMA; needs K % 256 == 0)
   bool feasible;   // false: no GEMV kernel fits this shape (the caller uses the CUDA-core tile)
   int kw, cpl, ri, rows_per_unit, row_bytes, stage_bytes, stages, units_per_problem, grid;
   long long num_units;
@@ -92,6 +94,7 @@ inline int gemv_ctas_per_sm(int cpl, int ri) { return cpl == 1 ? (ri <= 2 ? 3 : 
 constexpr int kMmaMaxK = 8192;
 struct MmaShape {
   int nw, ctas, unroll;
+  bool cols4;   // four-column consumer: each MMA covers four quantization groups of 16 rows
 };
 MmaShape mma_shape(int cfg);   // cfg 0: the default shape
 

@@ -668,7 +668,7 @@ __device__ __forceinline__ long long unit_at_cost(const GemvParams& p, const Gem
     if (batch.prob[mid].cost_begin <= c) lo = mid; else hi = mid;
   }
   const GemvProblem& q = batch.prob[lo];
-  const long long uc = (long long)q.rb * q.kw;
+  const long long uc = (long long)q.rb * q.cw;
   const long long blk = (c - q.cost_begin + uc - 1) / uc;
   if (blk < q.units) return q.unit_begin + blk;
   return lo + 1 < batch.count ? batch.prob[lo + 1].unit_begin : p.num_units;

@@ -32,6 +32,16 @@
 //    diagonal D[g][g], D[g+8][g], in lane (g, g/2).
 //  * Per step and row the holder lane adds s * 2^24 * D + b * sum(x) of that
 //    group in fp32; rows split over KW warps meet in shared memory.
+//
+// The four-column consumer (COLS4; K a multiple of 256) keeps every lane's
+// results: one MMA covers 16 rows of FOUR groups of a block.  K-pair t of the
+// MMA (A registers a0/a1 for the first code pair, a2/a3 for the second) holds
+// the codes of block group t, so lane (g, t) reads rows g and g+8 of group t;
+// B column j holds the x of group j in its own two k-pairs (j and j + 4) and
+// zero elsewhere, so D[r][j] is row r's dot product with group j, for all 16
+// rows and the four columns at once.  Only the lanes (j, j) supply x; the
+// others pass zeros.  Sixteen MMAs cover a block (64 codes of each group); the
+// epilogue then applies each (row, group)'s scale and bias once per block.
 #pragma once
 #include "qgemv_impl.cuh"
 
@@ -131,11 +141,28 @@ __device__ __forceinline__ void pairs_q4(uint32_t w, uint32_t (&p)[4]) {
   p[3] = w8 & 0x00F000F0u;
 }
 
+__device__ __forceinline__ uint32_t u4_at(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+__device__ __forceinline__ uint32_t lds32_nv(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 lds64f_nv(uint32_t a) {
+  float2 v;
+  asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
 template <int NW> struct MmaWarps {
   static constexpr int kThreads = (NW + 1) * 32;
 };
 
-template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH>
+template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH, bool COLS4>
 __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
     qgemv_mma_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
   static_assert(BITS == 4, "tensor-pipe GEMV: 4-bit codes");
@@ -284,6 +311,97 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
     const size_t ybase = v.y0 + row0;
     // tiles t of this unit with (tcount + t) % RW == rg
     int t = (rg - tcount % RW + RW) % RW;
+    if constexpr (COLS4) {
+      // this warp's K slice in blocks of four groups: [kb0, kb0 + nb)
+      const int B4 = G >> 2;
+      const int KSB = (B4 + KW - 1) / KW;
+      const int kb0 = kw * KSB;
+      const int nb = max(0, min(KSB, B4 - kb0));
+      const bool prov = g == tq;      // lanes (j, j) supply the x of block group j (B column j)
+      const int tl = tq & 1;          // lanes t = 2, 3 mirror t = 0, 1 in the epilogue (results unused)
+      // x fragments: the lanes (j, j) load theirs per block; every other lane keeps zeros
+      uint4 xr[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) xr[w] = make_uint4(0u, 0u, 0u, 0u);
+      for (; t < ntiles; t += RW) {
+        const int r0 = t * kMmaRows;
+        const int ra = min(r0 + g, rows - 1), rb = min(r0 + g + 8, rows - 1);
+        float dsa = 0.f, dsb = 0.f, bxa = 0.f, bxb = 0.f;   // sum s*D and sum b*sum(x), rows ra and rb
+        if (!dead) {
+          for (int bi = 0; bi < nb; ++bi) {
+            const int grp = (kb0 + bi) * 4;   // first group of the block
+            const uint32_t ca = st + (uint32_t)(ra * row_bytes + (grp + tq) * 32);
+            const uint32_t cb = st + (uint32_t)(rb * row_bytes + (grp + tq) * 32);
+            const uint4 wa0 = lds128_nv(ca), wa1 = lds128_nv(ca + 16);
+            const uint4 wb0 = lds128_nv(cb), wb1 = lds128_nv(cb + 16);
+            const uint32_t xg = xs + (uint32_t)((grp + (g & 3)) * kXGroupBytes);   // inside the block for every lane
+            if (prov) {
+#pragma unroll
+              for (int w = 0; w < 8; ++w) xr[w] = lds128_nv(xg + (uint32_t)(w * 16));
+            }
+            // four independent accumulator chains of four MMAs each
+            float dc[4][4] = {};
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              uint32_t pa[4], pb[4];
+              pairs_q4(u4_at(w < 4 ? wa0 : wa1, w & 3), pa);   // row ra, group grp + t, word w
+              pairs_q4(u4_at(w < 4 ? wb0 : wb1, w & 3), pb);   // row rb
+              const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+              mma16816(dc[(w & 1) * 2], a0, xr[w].x, xr[w].y);
+              const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+              mma16816(dc[(w & 1) * 2 + 1], a1, xr[w].z, xr[w].w);
+            }
+            float d0[4], d1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              d0[i] = dc[0][i] + dc[1][i];
+              d1[i] = dc[2][i] + dc[3][i];
+            }
+            // D[ra][2t], D[ra][2t+1], D[rb][2t], D[rb][2t+1]: groups gp, gp + 1
+            const int gp = grp + 2 * tl;
+            const uint32_t po_a = (uint32_t)((ra * G + gp) * 2), po_b = (uint32_t)((rb * G + gp) * 2);
+            const float2 sa = half2_bits_to_float2(lds32_nv(st_sc + po_a));
+            const float2 sb = half2_bits_to_float2(lds32_nv(st_sc + po_b));
+            const float2 ba = half2_bits_to_float2(lds32_nv(st_bi + po_a));
+            const float2 bb = half2_bits_to_float2(lds32_nv(st_bi + po_b));
+            const float2 xsv = lds64f_nv(xsa + (uint32_t)(gp * 4));
+            dsa = fmaf(sa.x, d0[0] + d1[0], fmaf(sa.y, d0[1] + d1[1], dsa));
+            dsb = fmaf(sb.x, d0[2] + d1[2], fmaf(sb.y, d0[3] + d1[3], dsb));
+            bxa = fmaf(ba.x, xsv.x, fmaf(ba.y, xsv.y, bxa));
+            bxb = fmaf(bb.x, xsv.x, fmaf(bb.y, xsv.y, bxb));
+          }
+        }
+        float acc_a = fmaf(dsa, 16777216.f, bxa), acc_b = fmaf(dsb, 16777216.f, bxb);
+        acc_a += __shfl_xor_sync(0xffffffffu, acc_a, 1);   // groups of lanes t = 0 and 1
+        acc_b += __shfl_xor_sync(0xffffffffu, acc_b, 1);
+        const bool holder4 = tq == 0;
+        const int ya = r0 + g, yb = r0 + g + 8;
+        if (KW == 1) {
+          if (!dead && holder4) {
+            if (ya < rows) store_yv(p, v.y, ybase + ya, acc_a);
+            if (yb < rows) store_yv(p, v.y, ybase + yb, acc_b);
+          }
+        } else {
+          float* rbp = red + (size_t)((rg * 2 + rbuf) * KW) * kMmaRows;   // [KW][16]
+          if (holder4) {
+            rbp[kw * kMmaRows + g] = acc_a;
+            rbp[kw * kMmaRows + g + 8] = acc_b;
+          }
+          asm volatile("bar.sync %0, %1;" ::"r"(1 + rg), "r"(KW * 32) : "memory");
+          if (!dead && kw == 0 && holder4) {
+            float sa = 0.f, sb = 0.f;
+            for (int j = 0; j < KW; ++j) {
+              sa += rbp[j * kMmaRows + g];
+              sb += rbp[j * kMmaRows + g + 8];
+            }
+            if (ya < rows) store_yv(p, v.y, ybase + ya, sa);
+            if (yb < rows) store_yv(p, v.y, ybase + yb, sb);
+          }
+          rbuf ^= 1;
+        }
+      }
+      t = ntiles;   // the diagonal consumer's loop below does nothing
+    }
     for (; t < ntiles; t += RW) {
       const int r0 = t * kMmaRows;
       float acc_a = 0.f, acc_b = 0.f;   // rows r0 + g, r0 + g + 8 (meaningful on holder lanes)
@@ -381,10 +499,10 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
   }
 }
 
-template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH>
+template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH, bool COLS4>
 cudaError_t launch_mma_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int grid, size_t smem,
                          cudaStream_t stream) {
-  auto k = qgemv_mma_kernel<BITS, NW, CTAS, UNROLL, BATCH>;
+  auto k = qgemv_mma_kernel<BITS, NW, CTAS, UNROLL, BATCH, COLS4>;
   static std::atomic<uint64_t> smem_raised{0};
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
@@ -406,16 +524,21 @@ cudaError_t launch_mma_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch,
   }
 }
 
-template <int BITS, int NW, int CTAS, int UNROLL>
+template <int BITS, int NW, int CTAS, int UNROLL, bool COLS4 = false>
 cudaError_t launch_mma_shape(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b,
                              cudaStream_t st) {
-  if (b) return launch_mma_t<BITS, NW, CTAS, UNROLL, true>(p, b, pl.grid, pl.smem, st);
-  return launch_mma_t<BITS, NW, CTAS, UNROLL, false>(p, nullptr, pl.grid, pl.smem, st);
+  if (b) return launch_mma_t<BITS, NW, CTAS, UNROLL, true, COLS4>(p, b, pl.grid, pl.smem, st);
+  return launch_mma_t<BITS, NW, CTAS, UNROLL, false, COLS4>(p, nullptr, pl.grid, pl.smem, st);
 }
 
 template <int BITS>
 cudaError_t launch_mma_bits(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b,
                             cudaStream_t st) {
+  if (pl.mma_cols4) {
+    if (pl.mma_nw == 16) return launch_mma_shape<BITS, 16, 1, 1, true>(p, pl, b, st);
+    if (pl.mma_ctas == 2) return launch_mma_shape<BITS, 8, 2, 1, true>(p, pl, b, st);
+    return launch_mma_shape<BITS, 8, 1, 1, true>(p, pl, b, st);
+  }
   if (pl.mma_nw == 16) return launch_mma_shape<BITS, 16, 1, 1>(p, pl, b, st);
   if (pl.mma_ctas == 2) return launch_mma_shape<BITS, 8, 2, 1>(p, pl, b, st);
   if (pl.mma_unroll == 1) return launch_mma_shape<BITS, 8, 1, 1>(p, pl, b, st);

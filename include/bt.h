@@ -402,14 +402,23 @@ BT_API bt_status bt_last_device_error(cudaStream_t stream);
  *                       kernel (path 4 of bt_plan_gemm), 8 or 16; 0 = 16 where
  *                       that layout fits shared memory and at most 16 tokens
  *                       share a staging of x, else 8.
- *   BT_OPT_GEMV_TENSOR_PIPE tuning: 0 = the tensor-pipe GEMV for launches of at
- *                       most one 16-row tile per SM (default), 1 = wherever it
- *                       applies, 2 = never.
+ *   BT_OPT_GEMV_TENSOR_PIPE tuning: 0 = by launch (default): the tensor-pipe
+ *                       GEMV's diagonal consumer for launches of at most one
+ *                       16-row tile per SM, its four-column consumer for
+ *                       launches of at least eight tiles per SM whose every K
+ *                       is a multiple of 256 and at most 4096, else the
+ *                       CUDA-core kernel;
+ *                       1 = the tensor pipe wherever it
+ *                       applies; 2 = never.
  *   BT_OPT_GEMV_MMA_STAGE_KB tuning: tensor-pipe GEMV stage size in KiB (0 = heuristic, else 8..112).
  *   BT_OPT_GEMV_MMA_SHAPE tuning: tensor-pipe GEMV kernel shape, 0 = default,
  *                       1: 8 consumer warps, 1 CTA per SM, two steps per loop
  *                       iteration; 2: the same, one step; 3: 16 consumer warps,
- *                       1 CTA per SM; 4: 8 consumer warps, 2 CTAs per SM.
+ *                       1 CTA per SM; 4: 8 consumer warps, 2 CTAs per SM;
+ *                       5, 6, 7: the four-column consumer (each MMA covers four
+ *                       quantization groups of 16 rows) with 8 warps and 1 CTA,
+ *                       8 warps and 2 CTAs, 16 warps and 1 CTA per SM.  A launch
+ *                       with some K not a multiple of 256 takes shape 0 instead.
  *   BT_OPT_GEMV_MMA_GROUPS tuning: most quantization groups of K one warp of the
  *                       tensor-pipe GEMV takes before K is split over more warps
  *                       (0 = heuristic).
@@ -444,8 +453,10 @@ BT_API bt_status bt_set_option(bt_option option, long long value);
  * "Metodologia": kernel choice and threadgroup sizes per chip) in inspectable
  * form, for tests and tuning.
  *   feasible      0: no GEMV kernel fits (the library runs the CUDA-core tile)
- *   tensor_pipe   1: the tensor-pipe kernel (dot products on mma.sync), 0: the
- *                 CUDA-core kernel
+ *   tensor_pipe   0: the CUDA-core kernel; the tensor-pipe kernel (dot
+ *                 products on mma.sync) with 1: the diagonal consumer (one
+ *                 group per lane group and MMA), 2: the four-column consumer
+ *                 (four groups of 16 rows per MMA)
  *   kw            warps sharing one row (K split); cpl: 32-code chunks per lane
  *   ri            rows in flight per warp (16 on the tensor pipe: one MMA tile);
  *                 rows_per_unit: rows per pipeline stage

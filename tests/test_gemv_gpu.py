@@ -290,68 +290,84 @@ def test_qgemv_llama1b_layer_all_bits(env, bits):
 
 
 # ------------------------------------------------ the tensor-pipe GEMV (4-bit codes, fp16 x)
-def run_opt(env, qw, x16, out_dtype="f32", cuda_core=False):
-    """The tensor-pipe kernel wherever it applies, or the CUDA-core kernel."""
+def run_opt(env, qw, x16, out_dtype="f32", cuda_core=False, shape=0):
+    """The tensor-pipe kernel wherever it applies (kernel shape `shape`), or the CUDA-core kernel."""
     torch, bt = env
     try:
         bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 1 if cuda_core else 0)
         bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 2 if cuda_core else 1)
+        bt.bt_set_option(bt.BT_OPT_GEMV_MMA_SHAPE, shape)
         return run(env, qw, x16, "f16", out_dtype)
     finally:
         bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 0)
         bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 0)
+        bt.bt_set_option(bt.BT_OPT_GEMV_MMA_SHAPE, 0)
 
 
+# kernel shapes: 0 the default diagonal consumer; 5, 6, 7 the four-column consumer
+# (8 warps, 8 warps x 2 CTAs, 16 warps), which takes K multiples of 256 only
+SHAPES = [0, 5, 6, 7]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("n,k", [(16, 64), (8, 128), (24, 256), (1000, 1024), (2056, 2048), (520, 3072),
-                                 (264, 4096), (136, 8192), (40, 576)])
-def test_tensor_pipe_gemv_matches_oracle(env, n, k):
+                                 (264, 4096), (136, 8192), (40, 576), (8, 512), (3000, 1280)])
+def test_tensor_pipe_gemv_matches_oracle(env, n, k, shape):
     """16-row MMA tiles with ragged last tiles, K split over 1..8 warps, odd group counts."""
     torch, bt = env
     try:
         bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 1)
-        assert bt.bt_plan_gemv(4, n, k)["tensor_pipe"] == 1
+        assert bt.bt_plan_gemv(4, n, k)["tensor_pipe"] in (1, 2)
     finally:
         bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 0)
     qw, x = make_case("mma-gemv", n, k, 4)
-    y = run_opt(env, qw, x)
+    y = run_opt(env, qw, x, shape=shape)
     y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]))
-    assert_close(y, y_ref, a, "f32", f"tensor pipe n={n} k={k}")
-    y_cc = run_opt(env, qw, x, cuda_core=True)
-    assert_close(y_cc, y_ref, a, "f32", f"CUDA core n={n} k={k}")
-    assert np.array_equal(y, run_opt(env, qw, x)), "tensor-pipe GEMV is not bitwise deterministic"
+    assert_close(y, y_ref, a, "f32", f"tensor pipe shape {shape} n={n} k={k}")
+    if shape == 0:
+        y_cc = run_opt(env, qw, x, cuda_core=True)
+        assert_close(y_cc, y_ref, a, "f32", f"CUDA core n={n} k={k}")
+    assert np.array_equal(y, run_opt(env, qw, x, shape=shape)), "tensor-pipe GEMV is not bitwise deterministic"
 
 
+@pytest.mark.parametrize("shape", [0, 5])
 @pytest.mark.parametrize("out", ["bf16", "f16"])
-def test_tensor_pipe_gemv_output_dtypes(env, out):
+def test_tensor_pipe_gemv_output_dtypes(env, out, shape):
     qw, x = make_case("mma-gemv-dt", 1032, 2048, 4)
-    y = run_opt(env, qw, x, out)
+    y = run_opt(env, qw, x, out, shape=shape)
     y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]))
-    assert_close(y, y_ref, a, out, f"tensor pipe -> {out}")
+    assert_close(y, y_ref, a, out, f"tensor pipe shape {shape} -> {out}")
 
 
-def test_tensor_pipe_gemv_lm_head_sampled(env):
+@pytest.mark.parametrize("shape", [0, 5])
+def test_tensor_pipe_gemv_lm_head_sampled(env, shape):
     torch, bt = env
     from dequant_gemv_gemm_bt_b300 import synth
     r = synth.rng_for("test", "mma-lm-head")
     qw = synth.make_qweight(r, 151936, 1024, 4)
     x = synth.draw_activations(r, 1, 1024, "f16")
-    y = run_opt(env, qw, x)
+    y = run_opt(env, qw, x, shape=shape)
     rows = np.unique(np.concatenate([np.arange(0, 80), np.arange(151936 - 80, 151936), r.integers(0, 151936, 2000)]))
     y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x[0]), rows=rows)
     assert_close(y[rows], y_ref, a, "f32", "tensor pipe lm_head")
 
 
-def test_tensor_pipe_batched_mixed_k(env):
+@pytest.mark.parametrize("shape,ks", [
+    (0, [1024, 3072, 2048, 128, 8192, 1024, 4096, 576, 3072, 64, 2048, 1024] * 3),
+    (5, [1024, 3072, 2048, 256, 8192, 1024, 4096, 512, 3072, 768, 2048, 1024] * 3),
+    (6, [1024, 3072, 2048, 256, 4096, 1024, 4096, 512, 3072, 768, 2048, 1024] * 3),   # 2 CTAs: K <= 4096 fits
+    (7, [1024, 3072, 2048, 256, 8192, 1024, 4096, 512, 3072, 768, 2048, 1024] * 3)])
+def test_tensor_pipe_batched_mixed_k(env, shape, ks):
     """One tensor-pipe launch over problems whose K split changes between neighbours
     (every CTA meets the barrier that re-stages x for a new problem)."""
     torch, bt = env
     from dequant_gemv_gemm_bt_b300 import synth
-    r = synth.rng_for("test", "mma-batched")
-    ks = [1024, 3072, 2048, 128, 8192, 1024, 4096, 576, 3072, 64, 2048, 1024] * 3
+    r = synth.rng_for("test", "mma-batched", shape)
     shapes = [(8 * int(r.integers(1, 200)), k) for k in ks]
     bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 1)
+    bt.bt_set_option(bt.BT_OPT_GEMV_MMA_SHAPE, shape)
     p, _ = bt.bt_plan_gemv_batch(4, shapes)
-    assert p["tensor_pipe"] == 1
+    assert p["tensor_pipe"] == (2 if shape >= 5 else 1)
     cases, probs = [], []
     for n, k in shapes:
         qw = synth.make_qweight(r, n, k, 4)
@@ -365,6 +381,7 @@ def test_tensor_pipe_batched_mixed_k(env):
         torch.cuda.synchronize()
     finally:
         bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 0)
+        bt.bt_set_option(bt.BT_OPT_GEMV_MMA_SHAPE, 0)
     assert bt.bt_last_device_error() == bt.BT_OK
     for (qw, x16), pr in zip(cases, probs):
         y_ref, a = O.qgemv(qw.codes, qw.scales, qw.biases, 4, O.decode_f16(x16[0]))

@@ -44,15 +44,21 @@ def check_plan(p, bits, n, k, problems, sms):
 
 
 def check_tensor_pipe_plan(p, bits, n, k, problems, sms):
-    """The tensor-pipe kernel: 16-row MMA tiles, each warp's K slice at most 16
-    groups, whole tiles per unit, one CTA per SM."""
+    """The tensor-pipe kernel: 16-row MMA tiles, each warp's K slice at most 32
+    groups (whole blocks of four groups for the four-column consumer), whole
+    tiles per unit, one CTA per SM."""
     g = k // 64
     kw, rb = p["kw"], p["rows_per_unit"]
     assert bits == 4 and k <= 8192
+    cols4 = p["tensor_pipe"] == 2
+    split_units = g // 4 if cols4 else g                            # K is split in blocks or in groups
+    if cols4:
+        assert k % 256 == 0
     assert kw in (1, 2, 4, 8) and -(-g // kw) <= 32                 # at most 32 groups per warp
+    assert kw <= max(1, split_units)
     tiles_per_sm = max(1, (-(-n * problems // sms)) // 16)
     if kw > 1 and -(-g // (kw // 2)) <= 32:                        # split further only to give idle warps work
-        assert (kw // 2) * tiles_per_sm < 8 and kw <= g
+        assert (kw // 2) * tiles_per_sm < 8 and kw <= split_units
     assert p["ri"] == 16 and rb % 16 == 0 and rb >= 16
     assert rb <= max(16, -(-n // 16) * 16)
     assert p["stage_bytes"] >= rb * per_row(bits, k) and p["stage_bytes"] % 128 == 0
@@ -89,6 +95,8 @@ def test_tensor_pipe_plan_invariants(bt, tensor_pipe, k, n):
     g = k // 64
     if (n * g * 2) % 16 or (n * k // 2) % 16:
         assert p["tensor_pipe"] == 0                                # a ragged unit could not move by bulk copy
+    elif -(-n // 16) >= 8 * 148 and k % 256 == 0 and k <= 4096:
+        assert p["tensor_pipe"] == 2                                # large launch: the four-column consumer
     else:
         assert p["tensor_pipe"] == 1
     check_plan(p, 4, n, k, 1, 148)
@@ -96,7 +104,9 @@ def test_tensor_pipe_plan_invariants(bt, tensor_pipe, k, n):
 
 def test_tensor_pipe_applies_to_4_bit_fp16_dense_only(bt, tensor_pipe):
     import torch
-    assert bt.bt_plan_gemv(4, 4096, 1024)["tensor_pipe"] == 1
+    assert bt.bt_plan_gemv(4, 4096, 1024)["tensor_pipe"] == 1       # a few tiles per SM: the diagonal consumer
+    assert bt.bt_plan_gemv(4, 65536, 1024)["tensor_pipe"] == 2      # many: the four-column consumer
+    assert bt.bt_plan_gemv(4, 65536, 1088)["tensor_pipe"] == 1      # 17 groups: the diagonal consumer
     assert bt.bt_plan_gemv(4, 4096, 16384)["tensor_pipe"] == 0       # K above 8192
     assert bt.bt_plan_gemv(4, 4096, 1024, x_dtype=torch.bfloat16)["tensor_pipe"] == 0
     for bits in (2, 3, 6, 8):
@@ -114,14 +124,24 @@ def test_tensor_pipe_applies_to_4_bit_fp16_dense_only(bt, tensor_pipe):
         bt.bt_set_option(bt.BT_OPT_GEMV_CUDA_CORE, 0)
 
 
-def test_tensor_pipe_by_default_only_for_small_launches(bt):
-    """Default rule: the tensor-pipe GEMV for launches of at most one 16-row tile
-    per SM (the single N=2048 GEMV), the CUDA-core kernel for larger ones."""
+def test_tensor_pipe_default_rule(bt):
+    """Default rule: the diagonal consumer for launches of at most one 16-row tile
+    per SM (the single N=2048 GEMV), the four-column consumer for launches of at
+    least eight tiles per SM whose every K is a multiple of 256 and at most 4096,
+    the CUDA-core kernel for the rest."""
     assert bt.bt_plan_gemv(4, 2048, 1024)["tensor_pipe"] == 1
     assert bt.bt_plan_gemv(4, 148 * 16, 1024)["tensor_pipe"] == 1
-    assert bt.bt_plan_gemv(4, 148 * 16 + 16, 1024)["tensor_pipe"] == 0
-    assert bt.bt_plan_gemv(4, 151936, 1024)["tensor_pipe"] == 0
+    assert bt.bt_plan_gemv(4, 148 * 16 + 16, 1024)["tensor_pipe"] == 0   # a few tiles per SM
+    assert bt.bt_plan_gemv(4, 148 * 128 - 16, 1024)["tensor_pipe"] == 0
+    assert bt.bt_plan_gemv(4, 148 * 128, 1024)["tensor_pipe"] == 2        # a tile per consumer warp
+    assert bt.bt_plan_gemv(4, 151936, 1024)["tensor_pipe"] == 2
+    assert bt.bt_plan_gemv(4, 151936, 1088)["tensor_pipe"] == 0     # 17 groups per row
+    assert bt.bt_plan_gemv(4, 151936, 4096)["tensor_pipe"] == 2
+    assert bt.bt_plan_gemv(4, 151936, 8192)["tensor_pipe"] == 0     # x of K = 8192 leaves small stages
+    assert bt.bt_plan_gemv(6, 151936, 1024)["tensor_pipe"] == 0     # 4-bit codes only
     p, _ = bt.bt_plan_gemv_batch(4, QWEN06_LAYER * 28 + [(151936, 1024)])
+    assert p["tensor_pipe"] == 2
+    p, _ = bt.bt_plan_gemv_batch(4, QWEN06_LAYER * 28 + [(151936, 1088)])
     assert p["tensor_pipe"] == 0
     try:
         bt.bt_set_option(bt.BT_OPT_GEMV_TENSOR_PIPE, 2)
@@ -200,7 +220,8 @@ QWEN06_LAYER = [(2048, 1024), (1024, 1024), (1024, 1024), (1024, 2048), (3072, 1
 
 def unit_partition(geoms, grid):
     """Host restatement of the kernel's work split.  Unit b of a problem starts at
-    work cost_begin + b*rb*kw (work = rows x warps per row); CTA i takes the units
+    work cost_begin + b*rb*w (work = rows x w: warps per row on the CUDA-core
+    kernel, quantization groups per row on the tensor-pipe one); CTA i takes the units
     from the first one starting at or after C*i//grid up to the first one starting
     at or after C*(i+1)//grid.  Returns each CTA's work and the total."""
     starts, costs = [], []
@@ -231,7 +252,7 @@ def test_decode_pass_batch_plan_on_the_tensor_pipe(bt, tensor_pipe):
     of units over one CTA per SM."""
     shapes = QWEN06_LAYER * 28 + [(151936, 1024)]
     p, geo = bt.bt_plan_gemv_batch(4, shapes)
-    assert p["feasible"] == 1 and p["tensor_pipe"] == 1 and p["ctas_per_sm"] == 1 and p["ri"] == 16
+    assert p["feasible"] == 1 and p["tensor_pipe"] == 2 and p["ctas_per_sm"] == 1 and p["ri"] == 16
     for (n, k), (kw, rb) in zip(shapes, geo):
         assert kw == {1024: 1, 2048: 1, 3072: 2}[k]
         assert rb % 16 == 0 and rb * per_row(4, k) <= p["stage_bytes"]
@@ -239,11 +260,12 @@ def test_decode_pass_batch_plan_on_the_tensor_pipe(bt, tensor_pipe):
     assert p["smem_bytes"] >= p["stages"] * p["stage_bytes"] + 48 * 192   # x of the largest K (48 groups)
     assert p["num_units"] == sum(-(-n // rb) for (n, _), (_, rb) in zip(shapes, geo))
     assert p["grid"] == 148
-    load, total = unit_partition([(n, kw, rb) for (n, _), (kw, rb) in zip(shapes, geo)], p["grid"])
+    load, total = unit_partition([(n, k // 64, rb) for (n, k), (_, rb) in zip(shapes, geo)], p["grid"])
     assert max(load) <= 1.1 * total / p["grid"]
 
 
-def test_decode_pass_batch_plan_and_work_split(bt):
+def test_decode_pass_batch_plan_and_work_split(bt, cuda_core):
+    """The same pass on the CUDA-core kernel."""
     shapes = QWEN06_LAYER * 28 + [(151936, 1024)]
     p, geo = bt.bt_plan_gemv_batch(4, shapes)
     assert p["feasible"] == 1 and p["cpl"] == 1 and p["ri"] == 8 and p["ctas_per_sm"] == 2

@@ -123,9 +123,13 @@ MmaShape mma_shape(int cfg) {
 }
 
 namespace {
-// shared memory one CTA may take when `ctas` CTAs share an SM (228 KB, 1 KB of
-// it reserved per CTA)
-size_t mma_smem_limit(int ctas) { return ctas == 1 ? 227 * 1024 : (228 * 1024) / ctas - 1024; }
+// dynamic shared memory one CTA may take when `ctas` CTAs share an SM (228 KB,
+// 1 KB of it reserved per CTA), less the kernel's static shared memory (128 B,
+// with room to spare)
+constexpr size_t kMmaStaticSmem = 512;
+size_t mma_smem_limit(int ctas) {
+  return (ctas == 1 ? 227 * 1024 : (228 * 1024) / ctas - 1024) - kMmaStaticSmem;
+}
 
 bool mma_applies(int bits, bool fast, int N, int K, int group) {
   if (opts().gemv_cuda_core.load() || bits != 4 || group != 64 || !fast || K > kMmaMaxK || K % kGroup) return false;

@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
       dead = true;
       s_fail = 1;
     }
+    dead = __any_sync(0xffffffffu, dead);   // warp-uniform: the MMAs and shuffles below need every lane
     const int RB = v.rb, row_bytes = v.row_bytes, G = v.g;
     const int row0 = blk * RB;
     const int rows = min(RB, v.n - row0);

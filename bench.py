@@ -732,20 +732,25 @@ def run_moe(torch, bt, dev, stream, steps, warmup, gpu_index, hbm):
                 for i in range(max(3, min(warmup, 5))):
                     graphs[i % len(graphs)].replay()
                 torch.cuda.synchronize()
+                # events made up front and no host wait inside the loop: the host
+                # stays ahead of the device, so no submission gap lands between
+                # the events (each step's flush keeps the device busy meanwhile)
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(n_steps)]
                 with ClockSampler(gpu_index) as clk:
                     for i in range(n_steps):
                         flush.fill_(float(i))
-                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        e0.record(stream)
+                        ev[i][0].record(stream)
                         graphs[i % len(graphs)].replay()
-                        e1.record(stream)
-                        e1.synchronize()
-                        times.append(e0.elapsed_time(e1) / 1e3)
+                        ev[i][1].record(stream)
                         touched_bytes += draws[i % len(draws)][4] * per_expert
+                    torch.cuda.synchronize()
+                times = [e0.elapsed_time(e1) / 1e3 for e0, e1 in ev]
             t = sum(times)
             gbs = touched_bytes / t / 1e9
             flops = 2 * tokens * top_k * (2 * I * H + H * I)
-            res[tag] = {"us_per_layer": round(t / n_steps * 1e6, 2), "weight_gbs": round(gbs, 1),
+            res[tag] = {"us_per_layer": round(t / n_steps * 1e6, 2),
+                        "us_per_layer_median": round(float(np.median(times)) * 1e6, 2), "weight_gbs": round(gbs, 1),
                         "frac_of_hbm": round(gbs / hbm, 4), "tflops": round(flops * n_steps / t / 1e12, 3),
                         "experts_touched_mean": round(touched_bytes / n_steps / per_expert, 2),
                         "launches_per_layer": launches, "clocks": clk.summary()}

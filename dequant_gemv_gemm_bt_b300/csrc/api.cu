@@ -400,7 +400,7 @@ struct PreparedGemv {
 };
 
 bt_status prepare_gemv_batch(const bt_gemv_problem* problems, int count, int bits, int group_size, int K,
-                             bt_dtype x_dtype, bt_dtype y_dtype, PreparedGemv& g) {
+                             bt_dtype x_dtype, bt_dtype y_dtype, PreparedGemv& g, int tokens = 1) {
   if (!problems || count < 1 || K < 0) return BT_ERR_INVALID_ARG;
   if (count > kBatchCap) return BT_ERR_UNSUPPORTED;
   if (!half_dtype(x_dtype) || !out_dtype(y_dtype)) return BT_ERR_INVALID_ARG;
@@ -431,13 +431,16 @@ bt_status prepare_gemv_batch(const bt_gemv_problem* problems, int count, int bit
     b.k = mixed ? problems[i].k : 0;   // 0: the launch plan's K and geometry
   }
   g.p = GemvParams{};
+  g.p.tokens = tokens;
   g.p.K = K;
   g.p.G = param_groups(bits, K, group_size);
   g.p.gshift = group_shift(group_size);
   g.p.N = max_n;
   const bool fast = gemv_fast_path(bits, x_dtype);
   GemvPlan& pl = g.pl;
-  if (mixed) {
+  if (tokens == 2) {   // two x rows per problem: the tensor-pipe kernel's four-column consumer or nothing
+    pl = mixed ? plan_gemv_batch_mma(bits, fast, batch, sm_count(), group_size, 2) : GemvPlan{};
+  } else if (mixed) {
     pl = plan_gemv_batch_mma(bits, fast, batch, sm_count(), group_size);
     if (!pl.feasible) pl = plan_gemv_batch(bits, fast, batch, sm_count(), group_size);
   } else {
@@ -562,6 +565,30 @@ bt_status plan_steps(const bt_gemm_problem* problems, int count, int bits, int g
     return BT_OK;
   }
   const int forced = opts().gemm_path;
+  if (M == 2 && forced == 0 && bits == 4 && group_size == 64 && x_dtype == BT_F16) {
+    // two tokens: the batched GEMV's four-column consumer reads each weight once
+    // for both (one token per half of the MMA's columns), where it applies
+    std::vector<PassStep> two;
+    bool ok = true;
+    for (int i0 = 0; i0 < count && ok; i0 += kBatchCap) {
+      const int c = std::min(kBatchCap, count - i0);
+      PassStep st;
+      st.kind = PassStep::kGemv;
+      st.gp.resize((size_t)c);
+      for (int i = 0; i < c; ++i) {
+        const bt_gemm_problem& q = problems[i0 + i];
+        st.gp[i] = bt_gemv_problem{q.codes, q.scales, q.biases, q.x, q.y, q.n, q.k};
+      }
+      st.gemv.reset(new PreparedGemv);
+      ok = prepare_gemv_batch(st.gp.data(), c, bits, group_size, 0, x_dtype, y_dtype, *st.gemv, 2) == BT_OK &&
+           st.gemv->pl.feasible;
+      two.push_back(std::move(st));
+    }
+    if (ok) {
+      for (PassStep& st : two) steps.push_back(std::move(st));
+      return BT_OK;
+    }
+  }
   const bool small_ok = (forced == 0 && M <= 16) || forced == 3;
   for (int i0 = 0; i0 < count; i0 += small::kBatchLaunchCap) {
     const int c = std::min(small::kBatchLaunchCap, count - i0);

@@ -264,7 +264,7 @@ GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_
   return pl;
 }
 
-GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group) {
+GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group, int tokens) {
   GemvPlan pl{};
   pl.fast = fast;
   pl.mma = true;
@@ -280,15 +280,18 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
   }
   bool all_k_by_4 = true;
   for (int i = 0; i < batch.count; ++i) all_k_by_4 = all_k_by_4 && (batch.prob[i].k / kGroup) % 4 == 0;
-  const MmaShape sh = pick_shape(rows, sms, all_k_by_4, g_max);
-  if (sh.nw == 0) return pl;
+  // two tokens per problem: the four-column consumer only (one token per half of its columns)
+  const MmaShape sh = tokens == 2 ? (all_k_by_4 ? mma_shape(5) : MmaShape{0, 0, 0, false})
+                                  : pick_shape(rows, sms, all_k_by_4, g_max);
+  if (sh.nw == 0 || tokens < 1 || tokens > 2) return pl;
   set_shape(pl, sh);
+  const int gx = g_max * tokens;   // the staged x (and its group sums) of every token
   const long long per_sm = std::max<long long>(1, (rows + sms - 1) / sms);
   int stage = 0;
   for (int i = 0; i < batch.count; ++i) {
     GemvProblem& q = batch.prob[i];
-    const MmaGeom m = mma_geom(bits, q.n, q.k, per_sm / sh.ctas, mma_stage_budget(sh, g_max), sh.nw, sh.cols4);
-    q.kw = m.kw;
+    const MmaGeom m = mma_geom(bits, q.n, q.k, per_sm / sh.ctas, mma_stage_budget(sh, gx), sh.nw, sh.cols4);
+    q.kw = tokens == 2 ? 1 : m.kw;   // the two-token consumer keeps whole rows in one warp (no K split)
     q.g = q.k / kGroup;
     q.row_bytes = m.row_bytes;
     q.rb = m.rb;
@@ -298,8 +301,8 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
   pl.rows_per_unit = batch.prob[0].rb;
   pl.row_bytes = batch.prob[0].row_bytes;
   pl.stage_bytes = stage;
-  pl.stages = mma_stages(stage, g_max, sh);
-  pl.smem = mma_smem(pl.stages, stage, g_max, sh.nw, nullptr);
+  pl.stages = mma_stages(stage, gx, sh);
+  pl.smem = mma_smem(pl.stages, stage, gx, sh.nw, nullptr);
   pl.grid = sms * sh.ctas;   // trimmed to the unit count at launch
   pl.feasible = pl.smem <= mma_smem_limit(sh.ctas) && pl.stages >= 2;
   return pl;
@@ -409,7 +412,9 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
     int g_max = p.G;
     if (batch)
       for (int i = 0; i < batch->count; ++i) g_max = std::max(g_max, batch->prob[i].g);
-    mma_smem(pl.stages, pl.stage_bytes, g_max, pl.mma_nw, &p.xsum_bytes);
+    p.tokens = std::max(1, p.tokens);
+    p.tok_groups = g_max;
+    mma_smem(pl.stages, pl.stage_bytes, g_max * p.tokens, pl.mma_nw, &p.xsum_bytes);
     plb.grid = (int)std::min<long long>(p.num_units, (long long)sm_count() * pl.mma_ctas);
     return launch_gemv_mma_b4(p, plb, batch, st);
   }

@@ -49,6 +49,11 @@ struct GemvParams {
   const int32_t* seg_ids;
   const float* seg_gates;
   int nseg, seg_k;
+  // tensor-pipe kernel, four-column consumer: tokens (x rows) per problem, 1
+  // or 2 (x and y of a problem are then [tokens, K] and [tokens, N]), and the
+  // stride in groups between the tokens' staged x
+  int tokens;
+  int tok_groups;
 };
 
 // Batched launches: many independent GEMVs of the same bits and dtypes, each
@@ -115,7 +120,11 @@ GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_
 // (stage size covering the largest unit); infeasible when the problems need
 // different kernel shapes.
 GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group = 64);
-GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group = 64);
+// tokens = 2: every problem has two x rows and two y rows (the four-column
+// consumer, one token per half of the MMA's columns); infeasible unless every
+// K is a multiple of 256.
+GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group = 64,
+                             int tokens = 1);
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,
                         cudaStream_t stream, GemvBatch<kBatchCap>* batch = nullptr);
 

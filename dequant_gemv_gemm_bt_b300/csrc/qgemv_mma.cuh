@@ -162,7 +162,7 @@ template <int NW> struct MmaWarps {
   static constexpr int kThreads = (NW + 1) * 32;
 };
 
-template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH, bool COLS4>
+template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH, bool COLS4, int TOK = 1>
 __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
     qgemv_mma_kernel(const GemvParams p, const __grid_constant__ GemvBatch<BATCH ? kBatchCap : 1> batch) {
   static_assert(BITS == 4, "tensor-pipe GEMV: 4-bit codes");
@@ -289,7 +289,12 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
       rg = warp / KW;
       rbuf = 0;
       tcount = 0;
-      if (!dead) prep_x(xs0, xsum, v.x, v.g, threadIdx.x, NW * 32);
+      if (!dead) {
+#pragma unroll
+        for (int tk = 0; tk < TOK; ++tk)   // one staged x per token, tok_groups groups apart
+          prep_x(xs0 + (uint32_t)(tk * p.tok_groups * kXGroupBytes), xsum + tk * p.tok_groups,
+                 v.x + (size_t)tk * v.k, v.g, threadIdx.x, NW * 32);
+      }
       asm volatile("bar.sync 15, %0;" ::"r"(NW * 32) : "memory");
       xs = launder(xs0);
       xsa = launder(xsum0);
@@ -318,8 +323,14 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
       const int KSB = (B4 + KW - 1) / KW;
       const int kb0 = kw * KSB;
       const int nb = max(0, min(KSB, B4 - kb0));
-      const bool prov = g == tq;      // lanes (j, j) supply the x of block group j (B column j)
-      const int tl = tq & 1;          // lanes t = 2, 3 mirror t = 0, 1 in the epilogue (results unused)
+      // B column c holds the x of token c / 4 (TOK = 2; token 0 only for TOK = 1), group c % 4 of
+      // the block: lanes (c, c % 4) supply it.  Lane (g, t) holds columns 2t, 2t + 1: token t / 2,
+      // groups 2 (t % 2) and 2 (t % 2) + 1.
+      const bool prov = TOK == 2 ? (g & 3) == tq : g == tq;
+      const int tl = tq & 1;          // with TOK = 1, lanes t = 2, 3 mirror t = 0, 1 (results unused)
+      const int tok = TOK == 2 ? (tq >> 1) : 0;
+      const uint32_t xtok = TOK == 2 ? (uint32_t)((g >> 2) * p.tok_groups * kXGroupBytes) : 0u;
+      const uint32_t xsum_tok = (uint32_t)(tok * p.tok_groups * 4);
       // x fragments: the lanes (j, j) load theirs per block; every other lane keeps zeros
       uint4 xr[8];
 #pragma unroll
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
             const uint32_t cb = st + (uint32_t)(rb * row_bytes + (grp + tq) * 32);
             const uint4 wa0 = lds128_nv(ca), wa1 = lds128_nv(ca + 16);
             const uint4 wb0 = lds128_nv(cb), wb1 = lds128_nv(cb + 16);
-            const uint32_t xg = xs + (uint32_t)((grp + (g & 3)) * kXGroupBytes);   // inside the block for every lane
+            const uint32_t xg = xs + xtok + (uint32_t)((grp + (g & 3)) * kXGroupBytes);   // inside the block for every lane
             if (prov) {
 #pragma unroll
               for (int w = 0; w < 8; ++w) xr[w] = lds128_nv(xg + (uint32_t)(w * 16));
@@ -365,7 +376,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
             const float2 sb = half2_bits_to_float2(lds32_nv(st_sc + po_b));
             const float2 ba = half2_bits_to_float2(lds32_nv(st_bi + po_a));
             const float2 bb = half2_bits_to_float2(lds32_nv(st_bi + po_b));
-            const float2 xsv = lds64f_nv(xsa + (uint32_t)(gp * 4));
+            const float2 xsv = lds64f_nv(xsa + xsum_tok + (uint32_t)(gp * 4));
             dsa = fmaf(sa.x, d0[0] + d1[0], fmaf(sa.y, d0[1] + d1[1], dsa));
             dsb = fmaf(sb.x, d0[2] + d1[2], fmaf(sb.y, d0[3] + d1[3], dsb));
             bxa = fmaf(ba.x, xsv.x, fmaf(ba.y, xsv.y, bxa));
@@ -373,11 +384,17 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
           }
         }
         float acc_a = fmaf(dsa, 16777216.f, bxa), acc_b = fmaf(dsb, 16777216.f, bxb);
-        acc_a += __shfl_xor_sync(0xffffffffu, acc_a, 1);   // groups of lanes t = 0 and 1
+        acc_a += __shfl_xor_sync(0xffffffffu, acc_a, 1);   // the two lanes of one token
         acc_b += __shfl_xor_sync(0xffffffffu, acc_b, 1);
-        const bool holder4 = tq == 0;
+        const bool holder4 = TOK == 2 ? (tq & 1) == 0 : tq == 0;
         const int ya = r0 + g, yb = r0 + g + 8;
-        if (KW == 1) {
+        if (TOK == 2) {   // KW == 1 (planned so): each token's rows go out directly
+          const size_t yt = ybase + (size_t)tok * v.n;
+          if (!dead && holder4) {
+            if (ya < rows) store_yv(p, v.y, yt + ya, acc_a);
+            if (yb < rows) store_yv(p, v.y, yt + yb, acc_b);
+          }
+        } else if (KW == 1) {
           if (!dead && holder4) {
             if (ya < rows) store_yv(p, v.y, ybase + ya, acc_a);
             if (yb < rows) store_yv(p, v.y, ybase + yb, acc_b);
@@ -500,10 +517,10 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
   }
 }
 
-template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH, bool COLS4>
+template <int BITS, int NW, int CTAS, int UNROLL, bool BATCH, bool COLS4, int TOK = 1>
 cudaError_t launch_mma_t(const GemvParams& p, const GemvBatch<kBatchCap>* batch, int grid, size_t smem,
                          cudaStream_t stream) {
-  auto k = qgemv_mma_kernel<BITS, NW, CTAS, UNROLL, BATCH, COLS4>;
+  auto k = qgemv_mma_kernel<BITS, NW, CTAS, UNROLL, BATCH, COLS4, TOK>;
   static std::atomic<uint64_t> smem_raised{0};
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem_raised);
   if (e != cudaSuccess) return e;
@@ -535,6 +552,10 @@ cudaError_t launch_mma_shape(const GemvParams& p, const GemvPlan& pl, const Gemv
 template <int BITS>
 cudaError_t launch_mma_bits(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b,
                             cudaStream_t st) {
+  if (pl.mma_cols4 && p.tokens == 2) {   // two tokens per problem: the batched 8-warp shape only
+    if (!b || pl.mma_nw != 8 || pl.mma_ctas != 1) return cudaErrorInvalidValue;
+    return launch_mma_t<BITS, 8, 1, 1, true, true, 2>(p, b, pl.grid, pl.smem, st);
+  }
   if (pl.mma_cols4) {
     if (pl.mma_nw == 16) return launch_mma_shape<BITS, 16, 1, 1, true>(p, pl, b, st);
     if (pl.mma_ctas == 2) return launch_mma_shape<BITS, 8, 2, 1, true>(p, pl, b, st);

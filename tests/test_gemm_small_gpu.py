@@ -204,6 +204,39 @@ def test_qgemm_batched_matches_oracle(env, m, xdtype):
         assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"batched m={m} n={qw.n} k={qw.k}")
 
 
+@pytest.mark.parametrize("out", ["f32", "f16"])
+def test_qgemm_batched_two_tokens_on_the_gemv(env, out):
+    """M = 2 with fp16 x and every K a multiple of 256: one launch of the batched
+    GEMV's four-column consumer (one token per half of the MMA's columns), with
+    ragged 16-row tiles, mixed K up to 8192, a long problem spanning many CTAs,
+    and bitwise-repeatable results."""
+    torch, bt = env
+    shapes = [(1000, 1024), (2056, 2048), (520, 3072), (264, 8192), (40000, 1024), (8, 512)]
+    probs, cases = [], []
+    odt = torch.float32 if out == "f32" else torch.float16
+    for i, (n, k) in enumerate(shapes):
+        qw, x = make_case(f"qgemm-two-{i}", n, k, 4, m=2, xdtype="f16")
+        c, s, b = to_dev(qw, torch)
+        y = torch.full((2, n), float("nan"), device="cuda", dtype=odt)
+        probs.append((c, s, b, half_tensor(x, "f16", torch), y))
+        cases.append((qw, x))
+    bt.bt_qgemm_batched(probs, 4)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    first = [pr[4].clone() for pr in probs]
+    for (qw, x), pr in zip(cases, probs):
+        rows = None if qw.n <= 4096 else np.unique(np.linspace(0, qw.n - 1, 600).astype(np.int64))
+        y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_half(x, "f16"), rows=rows)
+        y = out_to_f64(pr[4], torch)
+        assert_close(y if rows is None else y[:, rows], y_ref, a, out, f"two tokens n={qw.n} k={qw.k}")
+    for pr in probs:
+        pr[4].fill_(float("nan"))
+    bt.bt_qgemm_batched(probs, 4)
+    torch.cuda.synchronize()
+    for f, pr in zip(first, probs):
+        assert torch.equal(f, pr[4]), "two-token GEMV is not bitwise repeatable"
+
+
 def test_qgemm_batched_more_than_one_launch(env):
     """130 problems: more than one launch's table (120), results as one call."""
     torch, bt = env

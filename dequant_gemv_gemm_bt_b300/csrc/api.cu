@@ -438,8 +438,8 @@ bt_status prepare_gemv_batch(const bt_gemv_problem* problems, int count, int bit
   g.p.N = max_n;
   const bool fast = gemv_fast_path(bits, x_dtype);
   GemvPlan& pl = g.pl;
-  if (tokens == 2) {   // two x rows per problem: the tensor-pipe kernel's four-column consumer or nothing
-    pl = mixed ? plan_gemv_batch_mma(bits, fast, batch, sm_count(), group_size, 2) : GemvPlan{};
+  if (tokens >= 2) {   // several x rows per problem: the tensor-pipe kernel's four-column consumer or nothing
+    pl = mixed ? plan_gemv_batch_mma(bits, fast, batch, sm_count(), group_size, tokens) : GemvPlan{};
   } else if (mixed) {
     pl = plan_gemv_batch_mma(bits, fast, batch, sm_count(), group_size);
     if (!pl.feasible) pl = plan_gemv_batch(bits, fast, batch, sm_count(), group_size);
@@ -565,9 +565,10 @@ bt_status plan_steps(const bt_gemm_problem* problems, int count, int bits, int g
     return BT_OK;
   }
   const int forced = opts().gemm_path;
-  if (M == 2 && forced == 0 && bits == 4 && group_size == 64 && x_dtype == BT_F16) {
-    // two tokens: the batched GEMV's four-column consumer reads each weight once
-    // for both (one token per half of the MMA's columns), where it applies
+  if (M >= 2 && M <= 4 && forced == 0 && bits == 4 && group_size == 64 && x_dtype == BT_F16) {
+    // two to four tokens: the batched GEMV's four-column consumer reads and
+    // unpacks each weight once for all of them (tokens share the MMA's
+    // columns with the groups), where it applies
     std::vector<PassStep> two;
     bool ok = true;
     for (int i0 = 0; i0 < count && ok; i0 += kBatchCap) {
@@ -580,7 +581,7 @@ bt_status plan_steps(const bt_gemm_problem* problems, int count, int bits, int g
         st.gp[i] = bt_gemv_problem{q.codes, q.scales, q.biases, q.x, q.y, q.n, q.k};
       }
       st.gemv.reset(new PreparedGemv);
-      ok = prepare_gemv_batch(st.gp.data(), c, bits, group_size, 0, x_dtype, y_dtype, *st.gemv, 2) == BT_OK &&
+      ok = prepare_gemv_batch(st.gp.data(), c, bits, group_size, 0, x_dtype, y_dtype, *st.gemv, M) == BT_OK &&
            st.gemv->pl.feasible;
       two.push_back(std::move(st));
     }

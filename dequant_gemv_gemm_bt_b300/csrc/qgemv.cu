@@ -280,18 +280,18 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
   }
   bool all_k_by_4 = true;
   for (int i = 0; i < batch.count; ++i) all_k_by_4 = all_k_by_4 && (batch.prob[i].k / kGroup) % 4 == 0;
-  // two tokens per problem: the four-column consumer only (one token per half of its columns)
-  const MmaShape sh = tokens == 2 ? (all_k_by_4 ? mma_shape(5) : MmaShape{0, 0, 0, false})
+  // several tokens per problem: the four-column consumer only (tokens and groups share its columns)
+  const MmaShape sh = tokens >= 2 ? (all_k_by_4 ? mma_shape(5) : MmaShape{0, 0, 0, false})
                                   : pick_shape(rows, sms, all_k_by_4, g_max);
-  if (sh.nw == 0 || tokens < 1 || tokens > 2) return pl;
+  if (sh.nw == 0 || tokens < 1 || tokens > 4) return pl;
   set_shape(pl, sh);
-  const int gx = g_max * tokens;   // the staged x (and its group sums) of every token
+  const int gx = g_max * token_slots(tokens);   // the staged x (and its group sums) of every token
   const long long per_sm = std::max<long long>(1, (rows + sms - 1) / sms);
   int stage = 0;
   for (int i = 0; i < batch.count; ++i) {
     GemvProblem& q = batch.prob[i];
     const MmaGeom m = mma_geom(bits, q.n, q.k, per_sm / sh.ctas, mma_stage_budget(sh, gx), sh.nw, sh.cols4);
-    q.kw = tokens == 2 ? 1 : m.kw;   // the two-token consumer keeps whole rows in one warp (no K split)
+    q.kw = tokens >= 2 ? 1 : m.kw;   // the multi-token consumers keep whole rows in one warp (no K split)
     q.g = q.k / kGroup;
     q.row_bytes = m.row_bytes;
     q.rb = m.rb;
@@ -414,7 +414,7 @@ cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd
       for (int i = 0; i < batch->count; ++i) g_max = std::max(g_max, batch->prob[i].g);
     p.tokens = std::max(1, p.tokens);
     p.tok_groups = g_max;
-    mma_smem(pl.stages, pl.stage_bytes, g_max * p.tokens, pl.mma_nw, &p.xsum_bytes);
+    mma_smem(pl.stages, pl.stage_bytes, g_max * token_slots(p.tokens), pl.mma_nw, &p.xsum_bytes);
     plb.grid = (int)std::min<long long>(p.num_units, (long long)sm_count() * pl.mma_ctas);
     return launch_gemv_mma_b4(p, plb, batch, st);
   }

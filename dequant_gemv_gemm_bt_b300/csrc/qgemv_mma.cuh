@@ -292,8 +292,9 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
       if (!dead) {
 #pragma unroll
         for (int tk = 0; tk < TOK; ++tk)   // one staged x per token, tok_groups groups apart
-          prep_x(xs0 + (uint32_t)(tk * p.tok_groups * kXGroupBytes), xsum + tk * p.tok_groups,
-                 v.x + (size_t)tk * v.k, v.g, threadIdx.x, NW * 32);
+          if (tk < p.tokens)
+            prep_x(xs0 + (uint32_t)(tk * p.tok_groups * kXGroupBytes), xsum + tk * p.tok_groups,
+                   v.x + (size_t)tk * v.k, v.g, threadIdx.x, NW * 32);
       }
       asm volatile("bar.sync 15, %0;" ::"r"(NW * 32) : "memory");
       xs = launder(xs0);
@@ -317,7 +318,72 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
     const size_t ybase = v.y0 + row0;
     // tiles t of this unit with (tcount + t) % RW == rg
     int t = (rg - tcount % RW + RW) % RW;
-    if constexpr (COLS4) {
+    if constexpr (COLS4 && TOK == 4) {
+      // Four tokens (p.tokens = 3 or 4; KW = 1): an MMA covers 16 rows of TWO
+      // groups.  K-pairs t and t + 4 of lane (g, t) hold half t % 2 of block
+      // group t / 2 (its words 4 (t % 2) .. + 3; first and second code pair of a
+      // word), so the lane reads 16 bytes of rows g and g + 8.  B column c
+      // holds the x of token c / 2 and group c % 2 in the k-pairs of that group:
+      // lanes (c, t) with t / 2 == c % 2 supply it.  Lane (g, t) then holds
+      // token t's dot products with both groups for rows g and g + 8.
+      const int nb2 = G >> 1;   // blocks of two groups
+      const bool prov = (tq >> 1) == (g & 1) && (g >> 1) < p.tokens;
+      const uint32_t xlane = (uint32_t)((g >> 1) * p.tok_groups * kXGroupBytes + (g & 1) * kXGroupBytes +
+                                        (tq & 1) * 64);
+      const uint32_t xsum_tok = (uint32_t)(tq * p.tok_groups * 4);
+      uint4 xr[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) xr[w] = make_uint4(0u, 0u, 0u, 0u);
+      for (; t < ntiles; t += RW) {
+        const int r0 = t * kMmaRows;
+        const int ra = min(r0 + g, rows - 1), rb = min(r0 + g + 8, rows - 1);
+        float dsa = 0.f, dsb = 0.f, bxa = 0.f, bxb = 0.f;   // token tq, rows ra and rb
+        if (!dead) {
+          for (int bi = 0; bi < nb2; ++bi) {
+            const int grp = bi * 2;   // first group of the block
+            const uint32_t off = (uint32_t)((grp + (tq >> 1)) * 32 + (tq & 1) * 16);
+            const uint4 wa = lds128_nv(st + (uint32_t)(ra * row_bytes) + off);
+            const uint4 wb = lds128_nv(st + (uint32_t)(rb * row_bytes) + off);
+            if (prov) {
+#pragma unroll
+              for (int w = 0; w < 4; ++w) xr[w] = lds128_nv(xs + xlane + (uint32_t)(grp * kXGroupBytes + w * 16));
+            }
+            float dc[4][4] = {};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint32_t pa[4], pb[4];
+              pairs_q4(u4_at(wa, w), pa);
+              pairs_q4(u4_at(wb, w), pb);
+              const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+              mma16816(dc[(w & 1) * 2], a0, xr[w].x, xr[w].y);
+              const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+              mma16816(dc[(w & 1) * 2 + 1], a1, xr[w].z, xr[w].w);
+            }
+            // D[ra][2t], D[ra][2t+1], D[rb][2t], D[rb][2t+1]: token t, groups grp, grp + 1
+            const uint32_t po_a = (uint32_t)((ra * G + grp) * 2), po_b = (uint32_t)((rb * G + grp) * 2);
+            const float2 sa = half2_bits_to_float2(lds32_nv(st_sc + po_a));
+            const float2 sb = half2_bits_to_float2(lds32_nv(st_sc + po_b));
+            const float2 ba = half2_bits_to_float2(lds32_nv(st_bi + po_a));
+            const float2 bb = half2_bits_to_float2(lds32_nv(st_bi + po_b));
+            const float2 xsv = lds64f_nv(xsa + xsum_tok + (uint32_t)(grp * 4));
+            float d[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] = (dc[0][i] + dc[1][i]) + (dc[2][i] + dc[3][i]);
+            dsa = fmaf(sa.x, d[0], fmaf(sa.y, d[1], dsa));
+            dsb = fmaf(sb.x, d[2], fmaf(sb.y, d[3], dsb));
+            bxa = fmaf(ba.x, xsv.x, fmaf(ba.y, xsv.y, bxa));
+            bxb = fmaf(bb.x, xsv.x, fmaf(bb.y, xsv.y, bxb));
+          }
+        }
+        const int ya = r0 + g, yb = r0 + g + 8;
+        if (!dead && tq < p.tokens) {
+          const size_t yt = ybase + (size_t)tq * v.n;
+          if (ya < rows) store_yv(p, v.y, yt + ya, fmaf(dsa, 16777216.f, bxa));
+          if (yb < rows) store_yv(p, v.y, yt + yb, fmaf(dsb, 16777216.f, bxb));
+        }
+      }
+      t = ntiles;
+    } else if constexpr (COLS4) {
       // this warp's K slice in blocks of four groups: [kb0, kb0 + nb)
       const int B4 = G >> 2;
       const int KSB = (B4 + KW - 1) / KW;
@@ -552,9 +618,10 @@ cudaError_t launch_mma_shape(const GemvParams& p, const GemvPlan& pl, const Gemv
 template <int BITS>
 cudaError_t launch_mma_bits(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b,
                             cudaStream_t st) {
-  if (pl.mma_cols4 && p.tokens == 2) {   // two tokens per problem: the batched 8-warp shape only
-    if (!b || pl.mma_nw != 8 || pl.mma_ctas != 1) return cudaErrorInvalidValue;
-    return launch_mma_t<BITS, 8, 1, 1, true, true, 2>(p, b, pl.grid, pl.smem, st);
+  if (pl.mma_cols4 && p.tokens >= 2) {   // several tokens per problem: the batched 8-warp shape only
+    if (!b || pl.mma_nw != 8 || pl.mma_ctas != 1 || p.tokens > 4) return cudaErrorInvalidValue;
+    if (p.tokens == 2) return launch_mma_t<BITS, 8, 1, 1, true, true, 2>(p, b, pl.grid, pl.smem, st);
+    return launch_mma_t<BITS, 8, 1, 1, true, true, 4>(p, b, pl.grid, pl.smem, st);
   }
   if (pl.mma_cols4) {
     if (pl.mma_nw == 16) return launch_mma_shape<BITS, 16, 1, 1, true>(p, pl, b, st);

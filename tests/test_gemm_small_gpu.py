@@ -181,7 +181,7 @@ def test_small_grouped_default_takes_mma_for_moe_prefill(env):
     assert_close(out_to_f64(y, torch), y_ref, a, "f32", "Qwen3-30B-shaped gate|up, M=128")
 
 
-@pytest.mark.parametrize("m", [1, 2, 5, 8, 12, 16, 20])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8, 12, 16, 20])
 @pytest.mark.parametrize("xdtype", ["f16", "bf16"])
 def test_qgemm_batched_matches_oracle(env, m, xdtype):
     """Several products of the same M in one call: one small-token launch for
@@ -204,20 +204,22 @@ def test_qgemm_batched_matches_oracle(env, m, xdtype):
         assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"batched m={m} n={qw.n} k={qw.k}")
 
 
+@pytest.mark.parametrize("m", [2, 3, 4])
 @pytest.mark.parametrize("out", ["f32", "f16"])
-def test_qgemm_batched_two_tokens_on_the_gemv(env, out):
-    """M = 2 with fp16 x and every K a multiple of 256: one launch of the batched
-    GEMV's four-column consumer (one token per half of the MMA's columns), with
-    ragged 16-row tiles, mixed K up to 8192, a long problem spanning many CTAs,
-    and bitwise-repeatable results."""
+def test_qgemm_batched_few_tokens_on_the_gemv(env, out, m):
+    """M = 2..4 with fp16 x and every K a multiple of 256: one launch of the
+    batched GEMV's four-column consumer (two tokens x four groups, or four
+    tokens x two groups, in the MMA's columns; M = 3 leaves one token slot
+    empty), with ragged 16-row tiles, mixed K up to 8192, a long problem
+    spanning many CTAs, and bitwise-repeatable results."""
     torch, bt = env
     shapes = [(1000, 1024), (2056, 2048), (520, 3072), (264, 8192), (40000, 1024), (8, 512)]
     probs, cases = [], []
     odt = torch.float32 if out == "f32" else torch.float16
     for i, (n, k) in enumerate(shapes):
-        qw, x = make_case(f"qgemm-two-{i}", n, k, 4, m=2, xdtype="f16")
+        qw, x = make_case(f"qgemm-two-{i}", n, k, 4, m=m, xdtype="f16")
         c, s, b = to_dev(qw, torch)
-        y = torch.full((2, n), float("nan"), device="cuda", dtype=odt)
+        y = torch.full((m, n), float("nan"), device="cuda", dtype=odt)
         probs.append((c, s, b, half_tensor(x, "f16", torch), y))
         cases.append((qw, x))
     bt.bt_qgemm_batched(probs, 4)
@@ -228,13 +230,13 @@ def test_qgemm_batched_two_tokens_on_the_gemv(env, out):
         rows = None if qw.n <= 4096 else np.unique(np.linspace(0, qw.n - 1, 600).astype(np.int64))
         y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_half(x, "f16"), rows=rows)
         y = out_to_f64(pr[4], torch)
-        assert_close(y if rows is None else y[:, rows], y_ref, a, out, f"two tokens n={qw.n} k={qw.k}")
+        assert_close(y if rows is None else y[:, rows], y_ref, a, out, f"m={m} n={qw.n} k={qw.k}")
     for pr in probs:
         pr[4].fill_(float("nan"))
     bt.bt_qgemm_batched(probs, 4)
     torch.cuda.synchronize()
     for f, pr in zip(first, probs):
-        assert torch.equal(f, pr[4]), "two-token GEMV is not bitwise repeatable"
+        assert torch.equal(f, pr[4]), "few-token GEMV is not bitwise repeatable"
 
 
 def test_qgemm_batched_more_than_one_launch(env):

@@ -63,10 +63,9 @@ def new_input(torch, bufs, m, seed):
 @pytest.mark.parametrize("pdl", [0, 1])
 @pytest.mark.parametrize("m", [1, 2, 4, 24])
 def test_pass_chain_runs_match_oracle(env, m, pdl):
-    """Three dependent stages: M = 1 on the batched GEMV, M = 2 on its two-token
-    form, M = 4 on the small-token kernel, M = 24 one tensor-core product per
-    launch; with and without PDL (and the constant-weights prefetch that PDL
-    allows)."""
+    """Three dependent stages: M = 1 on the batched GEMV, M = 2 and 4 on its
+    few-token forms, M = 24 one tensor-core product per launch; with and
+    without PDL (and the constant-weights prefetch that PDL allows)."""
     torch, bt = env
     weights, bufs, stages = build_chain(torch, m, f"chain{m}")
     dp = bt.bt_pass_create(stages, 4)

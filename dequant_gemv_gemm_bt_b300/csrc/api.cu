@@ -565,8 +565,8 @@ bt_status plan_steps(const bt_gemm_problem* problems, int count, int bits, int g
     return BT_OK;
   }
   const int forced = opts().gemm_path;
-  if (M >= 2 && M <= 4 && forced == 0 && bits == 4 && group_size == 64 && x_dtype == BT_F16) {
-    // two to four tokens: the batched GEMV's four-column consumer reads and
+  if (M >= 2 && M <= 8 && forced == 0 && bits == 4 && group_size == 64 && x_dtype == BT_F16) {
+    // two to eight tokens: the batched GEMV's four-column consumer reads and
     // unpacks each weight once for all of them (tokens share the MMA's
     // columns with the groups), where it applies
     std::vector<PassStep> two;

@@ -283,7 +283,7 @@ GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, i
   // several tokens per problem: the four-column consumer only (tokens and groups share its columns)
   const MmaShape sh = tokens >= 2 ? (all_k_by_4 ? mma_shape(5) : MmaShape{0, 0, 0, false})
                                   : pick_shape(rows, sms, all_k_by_4, g_max);
-  if (sh.nw == 0 || tokens < 1 || tokens > 4) return pl;
+  if (sh.nw == 0 || tokens < 1 || tokens > 8) return pl;
   set_shape(pl, sh);
   const int gx = g_max * token_slots(tokens);   // the staged x (and its group sums) of every token
   const long long per_sm = std::max<long long>(1, (rows + sms - 1) / sms);

@@ -122,10 +122,11 @@ GemvPlan plan_gemv_mma(int bits, bool fast, int N, int K, int problems, int num_
 GemvPlan plan_gemv_batch(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group = 64);
 // Staged x copies the tensor-pipe kernel keeps for `tokens` tokens per problem
 // (its variants take 1, 2 or 4).
-inline int token_slots(int tokens) { return tokens <= 1 ? 1 : (tokens == 2 ? 2 : 4); }
-// tokens = 2..4: every problem has that many x rows and y rows (the four-column
-// consumer with two tokens x four groups, or four tokens x two groups, in the
-// MMA's columns); infeasible unless every K is a multiple of 256.
+inline int token_slots(int tokens) { return tokens <= 1 ? 1 : (tokens == 2 ? 2 : (tokens <= 4 ? 4 : 8)); }
+// tokens = 2..8: every problem has that many x rows and y rows (the four-column
+// consumer with two tokens x four groups, four tokens x two groups or eight
+// tokens x one group in the MMA's columns); infeasible unless every K is a
+// multiple of 256.
 GemvPlan plan_gemv_batch_mma(int bits, bool fast, GemvBatch<kBatchCap>& batch, int sms, int group = 64,
                              int tokens = 1);
 cudaError_t launch_gemv(GemvParams& p, const GemvPlan& pl, int bits, bt_dtype xd, bt_dtype yd,

@@ -318,7 +318,71 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
     const size_t ybase = v.y0 + row0;
     // tiles t of this unit with (tcount + t) % RW == rg
     int t = (rg - tcount % RW + RW) % RW;
-    if constexpr (COLS4 && TOK == 4) {
+    if constexpr (COLS4 && TOK == 8) {
+      // Five to eight tokens (KW = 1): an MMA covers 16 rows of ONE group and
+      // eight tokens.  K-pairs t and t + 4 of lane (g, t) hold words 2t and
+      // 2t + 1 of the group (four MMAs: word 2t + w, first or second code pair
+      // of each half-word pair), so the lane reads 8 bytes of rows g and g + 8;
+      // B column c holds token c's x, supplied by lanes (c, *).  Lane (g, t)
+      // holds tokens 2t and 2t + 1 for rows g and g + 8.
+      const bool live = g < p.tokens;   // a lane supplying an empty token slot keeps zeros
+      const uint32_t xlane = (uint32_t)(g * p.tok_groups * kXGroupBytes + tq * 32);
+      const uint32_t xs0t = (uint32_t)(2 * tq * p.tok_groups * 4), xs1t = xs0t + (uint32_t)(p.tok_groups * 4);
+      uint4 xr[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+      for (; t < ntiles; t += RW) {
+        const int r0 = t * kMmaRows;
+        const int ra = min(r0 + g, rows - 1), rb = min(r0 + g + 8, rows - 1);
+        float ds[4] = {0.f, 0.f, 0.f, 0.f}, bx[4] = {0.f, 0.f, 0.f, 0.f};   // (ra, 2t) (ra, 2t+1) (rb, 2t) (rb, 2t+1)
+        if (!dead) {
+          for (int gi = 0; gi < G; ++gi) {
+            const uint32_t off = (uint32_t)(gi * 32 + tq * 8);
+            uint32_t wa[2], wb[2];
+            asm("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(wa[0]), "=r"(wa[1]) : "r"(st + (uint32_t)(ra * row_bytes) + off));
+            asm("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(wb[0]), "=r"(wb[1]) : "r"(st + (uint32_t)(rb * row_bytes) + off));
+            if (live) {
+              xr[0] = lds128_nv(xs + xlane + (uint32_t)(gi * kXGroupBytes));
+              xr[1] = lds128_nv(xs + xlane + (uint32_t)(gi * kXGroupBytes + 16));
+            }
+            float dc[2][4] = {};
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              uint32_t pa[4], pb[4];
+              pairs_q4(wa[w], pa);
+              pairs_q4(wb[w], pb);
+              const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+              mma16816(dc[0], a0, xr[w].x, xr[w].y);
+              const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+              mma16816(dc[1], a1, xr[w].z, xr[w].w);
+            }
+            const uint32_t po_a = (uint32_t)((ra * G + gi) * 2), po_b = (uint32_t)((rb * G + gi) * 2);
+            const float sa = to_f32<BT_F16>(lds16_nv(st_sc + po_a)), sb = to_f32<BT_F16>(lds16_nv(st_sc + po_b));
+            const float ba = to_f32<BT_F16>(lds16_nv(st_bi + po_a)), bb = to_f32<BT_F16>(lds16_nv(st_bi + po_b));
+            const float x0 = lds32f_nv(xsa + xs0t + (uint32_t)(gi * 4)), x1 = lds32f_nv(xsa + xs1t + (uint32_t)(gi * 4));
+            ds[0] = fmaf(sa, dc[0][0] + dc[1][0], ds[0]);
+            ds[1] = fmaf(sa, dc[0][1] + dc[1][1], ds[1]);
+            ds[2] = fmaf(sb, dc[0][2] + dc[1][2], ds[2]);
+            ds[3] = fmaf(sb, dc[0][3] + dc[1][3], ds[3]);
+            bx[0] = fmaf(ba, x0, bx[0]);
+            bx[1] = fmaf(ba, x1, bx[1]);
+            bx[2] = fmaf(bb, x0, bx[2]);
+            bx[3] = fmaf(bb, x1, bx[3]);
+          }
+        }
+        const int ya = r0 + g, yb = r0 + g + 8;
+        if (!dead) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int tk = 2 * tq + j;
+            if (tk < p.tokens) {
+              const size_t yt = ybase + (size_t)tk * v.n;
+              if (ya < rows) store_yv(p, v.y, yt + ya, fmaf(ds[j], 16777216.f, bx[j]));
+              if (yb < rows) store_yv(p, v.y, yt + yb, fmaf(ds[2 + j], 16777216.f, bx[2 + j]));
+            }
+          }
+        }
+      }
+      t = ntiles;
+    } else if constexpr (COLS4 && TOK == 4) {
       // Four tokens (p.tokens = 3 or 4; KW = 1): an MMA covers 16 rows of TWO
       // groups.  K-pairs t and t + 4 of lane (g, t) hold half t % 2 of block
       // group t / 2 (its words 4 (t % 2) .. + 3; first and second code pair of a
@@ -619,9 +683,10 @@ template <int BITS>
 cudaError_t launch_mma_bits(const GemvParams& p, const GemvPlan& pl, const GemvBatch<kBatchCap>* b,
                             cudaStream_t st) {
   if (pl.mma_cols4 && p.tokens >= 2) {   // several tokens per problem: the batched 8-warp shape only
-    if (!b || pl.mma_nw != 8 || pl.mma_ctas != 1 || p.tokens > 4) return cudaErrorInvalidValue;
+    if (!b || pl.mma_nw != 8 || pl.mma_ctas != 1 || p.tokens > 8) return cudaErrorInvalidValue;
     if (p.tokens == 2) return launch_mma_t<BITS, 8, 1, 1, true, true, 2>(p, b, pl.grid, pl.smem, st);
-    return launch_mma_t<BITS, 8, 1, 1, true, true, 4>(p, b, pl.grid, pl.smem, st);
+    if (p.tokens <= 4) return launch_mma_t<BITS, 8, 1, 1, true, true, 4>(p, b, pl.grid, pl.smem, st);
+    return launch_mma_t<BITS, 8, 1, 1, true, true, 8>(p, b, pl.grid, pl.smem, st);
   }
   if (pl.mma_cols4) {
     if (pl.mma_nw == 16) return launch_mma_shape<BITS, 16, 1, 1, true>(p, pl, b, st);

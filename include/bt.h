@@ -126,7 +126,7 @@ BT_API bt_status bt_qgemv_batched(const bt_gemv_problem* problems, int count, in
  *             the pointers in it are device memory: codes and X 16-byte
  *             aligned, scales and biases 8-byte aligned for the one-launch path)
  *   M         rows of every X and Y (tokens)
- * M = 2..4 with fp16 x, bits = 4, group_size = 64 and every K a multiple of
+ * M = 2..8 with fp16 x, bits = 4, group_size = 64 and every K a multiple of
  * 256 runs as one launch of the batched GEMV's four-column consumer, the
  * tokens sharing the MMA's columns with the groups (each weight read and
  * unpacked once for all tokens; up to 256 problems per launch).  Otherwise one launch of the

@@ -204,14 +204,14 @@ def test_qgemm_batched_matches_oracle(env, m, xdtype):
         assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"batched m={m} n={qw.n} k={qw.k}")
 
 
-@pytest.mark.parametrize("m", [2, 3, 4])
+@pytest.mark.parametrize("m", [2, 3, 4, 5, 8])
 @pytest.mark.parametrize("out", ["f32", "f16"])
 def test_qgemm_batched_few_tokens_on_the_gemv(env, out, m):
-    """M = 2..4 with fp16 x and every K a multiple of 256: one launch of the
-    batched GEMV's four-column consumer (two tokens x four groups, or four
-    tokens x two groups, in the MMA's columns; M = 3 leaves one token slot
-    empty), with ragged 16-row tiles, mixed K up to 8192, a long problem
-    spanning many CTAs, and bitwise-repeatable results."""
+    """M = 2..8 with fp16 x and every K a multiple of 256: one launch of the
+    batched GEMV's four-column consumer (two tokens x four groups, four tokens
+    x two groups or eight tokens x one group in the MMA's columns; M = 3 and 5
+    leave token slots empty), with ragged 16-row tiles, mixed K up to 8192, a
+    long problem spanning many CTAs, and bitwise-repeatable results."""
     torch, bt = env
     shapes = [(1000, 1024), (2056, 2048), (520, 3072), (264, 8192), (40000, 1024), (8, 512)]
     probs, cases = [], []

@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
     const int ks = max(0, min(KS, G - gs0));
     const size_t ybase = v.y0 + row0;
     // tiles t of this unit with (tcount + t) % RW == rg
-    int t = (rg - tcount % RW + RW) % RW;
+    int t = (rg - tcount + RW * kMmaRows) & (RW - 1);   // RW = NW / KW is a power of two
     if constexpr (COLS4 && TOK == 8) {
       // Five to eight tokens (KW = 1): an MMA covers 16 rows of ONE group and
       // eight tokens.  K-pairs t and t + 4 of lane (g, t) hold words 2t and
@@ -469,11 +469,13 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
         const int r0 = t * kMmaRows;
         const int ra = min(r0 + g, rows - 1), rb = min(r0 + g + 8, rows - 1);
         float dsa = 0.f, dsb = 0.f, bxa = 0.f, bxb = 0.f;   // sum s*D and sum b*sum(x), rows ra and rb
+        const uint32_t ca0 = st + (uint32_t)(ra * row_bytes + tq * 32), cb0 = st + (uint32_t)(rb * row_bytes + tq * 32);
+        const uint32_t pa0 = (uint32_t)(ra * G * 2), pb0 = (uint32_t)(rb * G * 2);
         if (!dead) {
           for (int bi = 0; bi < nb; ++bi) {
             const int grp = (kb0 + bi) * 4;   // first group of the block
-            const uint32_t ca = st + (uint32_t)(ra * row_bytes + (grp + tq) * 32);
-            const uint32_t cb = st + (uint32_t)(rb * row_bytes + (grp + tq) * 32);
+            const uint32_t ca = ca0 + (uint32_t)(grp * 32);
+            const uint32_t cb = cb0 + (uint32_t)(grp * 32);
             const uint4 wa0 = lds128_nv(ca), wa1 = lds128_nv(ca + 16);
             const uint4 wb0 = lds128_nv(cb), wb1 = lds128_nv(cb + 16);
             const uint32_t xg = xs + xtok + (uint32_t)((grp + (g & 3)) * kXGroupBytes);   // inside the block for every lane
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
             }
             // D[ra][2t], D[ra][2t+1], D[rb][2t], D[rb][2t+1]: groups gp, gp + 1
             const int gp = grp + 2 * tl;
-            const uint32_t po_a = (uint32_t)((ra * G + gp) * 2), po_b = (uint32_t)((rb * G + gp) * 2);
+            const uint32_t po_a = pa0 + (uint32_t)(gp * 2), po_b = pb0 + (uint32_t)(gp * 2);
             const float2 sa = half2_bits_to_float2(lds32_nv(st_sc + po_a));
             const float2 sb = half2_bits_to_float2(lds32_nv(st_sc + po_b));
             const float2 ba = half2_bits_to_float2(lds32_nv(st_bi + po_a));

@@ -402,12 +402,14 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
         const int r0 = t * kMmaRows;
         const int ra = min(r0 + g, rows - 1), rb = min(r0 + g + 8, rows - 1);
         float dsa = 0.f, dsb = 0.f, bxa = 0.f, bxb = 0.f;   // token tq, rows ra and rb
+        const uint32_t lo = (uint32_t)((tq >> 1) * 32 + (tq & 1) * 16);
+        const uint32_t ca0 = st + (uint32_t)(ra * row_bytes) + lo, cb0 = st + (uint32_t)(rb * row_bytes) + lo;
+        const uint32_t pa0 = (uint32_t)(ra * G * 2), pb0 = (uint32_t)(rb * G * 2);
         if (!dead) {
           for (int bi = 0; bi < nb2; ++bi) {
             const int grp = bi * 2;   // first group of the block
-            const uint32_t off = (uint32_t)((grp + (tq >> 1)) * 32 + (tq & 1) * 16);
-            const uint4 wa = lds128_nv(st + (uint32_t)(ra * row_bytes) + off);
-            const uint4 wb = lds128_nv(st + (uint32_t)(rb * row_bytes) + off);
+            const uint4 wa = lds128_nv(ca0 + (uint32_t)(grp * 32));
+            const uint4 wb = lds128_nv(cb0 + (uint32_t)(grp * 32));
             if (prov) {
 #pragma unroll
               for (int w = 0; w < 4; ++w) xr[w] = lds128_nv(xs + xlane + (uint32_t)(grp * kXGroupBytes + w * 16));
@@ -424,7 +426,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
               mma16816(dc[(w & 1) * 2 + 1], a1, xr[w].z, xr[w].w);
             }
             // D[ra][2t], D[ra][2t+1], D[rb][2t], D[rb][2t+1]: token t, groups grp, grp + 1
-            const uint32_t po_a = (uint32_t)((ra * G + grp) * 2), po_b = (uint32_t)((rb * G + grp) * 2);
+            const uint32_t po_a = pa0 + (uint32_t)(grp * 2), po_b = pb0 + (uint32_t)(grp * 2);
             const float2 sa = half2_bits_to_float2(lds32_nv(st_sc + po_a));
             const float2 sb = half2_bits_to_float2(lds32_nv(st_sc + po_b));
             const float2 ba = half2_bits_to_float2(lds32_nv(st_bi + po_a));

@@ -205,7 +205,7 @@ def test_qgemm_batched_matches_oracle(env, m, xdtype):
 
 
 @pytest.mark.parametrize("m", [2, 3, 4, 5, 8])
-@pytest.mark.parametrize("out", ["f32", "f16"])
+@pytest.mark.parametrize("out", ["f32", "f16", "bf16"])
 def test_qgemm_batched_few_tokens_on_the_gemv(env, out, m):
     """M = 2..8 with fp16 x and every K a multiple of 256: one launch of the
     batched GEMV's four-column consumer (two tokens x four groups, four tokens
@@ -215,7 +215,7 @@ def test_qgemm_batched_few_tokens_on_the_gemv(env, out, m):
     torch, bt = env
     shapes = [(1000, 1024), (2056, 2048), (520, 3072), (264, 8192), (40000, 1024), (8, 512)]
     probs, cases = [], []
-    odt = torch.float32 if out == "f32" else torch.float16
+    odt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[out]
     for i, (n, k) in enumerate(shapes):
         qw, x = make_case(f"qgemm-two-{i}", n, k, 4, m=m, xdtype="f16")
         c, s, b = to_dev(qw, torch)
@@ -237,6 +237,28 @@ def test_qgemm_batched_few_tokens_on_the_gemv(env, out, m):
     torch.cuda.synchronize()
     for f, pr in zip(first, probs):
         assert torch.equal(f, pr[4]), "few-token GEMV is not bitwise repeatable"
+
+
+@pytest.mark.parametrize("m", [2, 3, 8])
+def test_qgemm_batched_few_tokens_fallback(env, m):
+    """A table with a K that is not a multiple of 256 (576) cannot take the
+    few-token GEMV: the call falls back (one product per launch) with the same
+    results."""
+    torch, bt = env
+    shapes = [(264, 576), (1032, 1024)]
+    probs, cases = [], []
+    for i, (n, k) in enumerate(shapes):
+        qw, x = make_case(f"qgemm-few-fb-{i}", n, k, 4, m=m, xdtype="f16")
+        c, s, b = to_dev(qw, torch)
+        y = torch.full((m, n), float("nan"), device="cuda")
+        probs.append((c, s, b, half_tensor(x, "f16", torch), y))
+        cases.append((qw, x))
+    bt.bt_qgemm_batched(probs, 4)
+    torch.cuda.synchronize()
+    assert bt.bt_last_device_error() == bt.BT_OK
+    for (qw, x), pr in zip(cases, probs):
+        y_ref, a = O.qgemm(qw.codes, qw.scales, qw.biases, 4, O.decode_half(x, "f16"))
+        assert_close(out_to_f64(pr[4], torch), y_ref, a, "f32", f"fallback m={m} n={qw.n} k={qw.k}")
 
 
 def test_qgemm_batched_more_than_one_launch(env):

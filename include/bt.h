@@ -191,7 +191,8 @@ BT_API bt_status bt_qgemm_batched(const bt_gemm_problem* problems, int count, in
  * `pass` or `stages` or num_stages < 1.  bt_pass_run returns
  * BT_ERR_INVALID_ARG for a NULL pass or a current device other than the
  * pass's, BT_ERR_CUDA when a launch, the recording or the graph launch
- * fails.  bt_pass_destroy accepts NULL.
+ * fails.  bt_pass_destroy accepts NULL; call it only once no run of the
+ * pass is in flight (after the run's stream has been synchronised).
  */
 typedef struct bt_pass bt_pass;
 typedef struct {

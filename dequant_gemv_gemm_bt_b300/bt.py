@@ -310,6 +310,7 @@ class DecodePass:
     def __init__(self, handle, tensors):
         self._handle = handle
         self._tensors = tensors   # the pass reads and writes these buffers for its whole life
+        self._ran = False
 
     def run(self, stream=None):
         bt_pass_run(self, stream=stream)
@@ -346,11 +347,15 @@ def bt_pass_run(dpass: DecodePass, stream=None):
     """Launches the pass on ``stream`` (the first run also records it as a CUDA graph)."""
     _need(dpass._handle is not None, "the pass was destroyed")
     _check(lib.bt_pass_run(dpass._handle, _stream(stream)), "bt_pass_run")
+    dpass._ran = True
 
 
 def bt_pass_destroy(dpass: DecodePass):
-    """Frees the pass (its graph and stream); the tensors stay the caller's."""
+    """Frees the pass (its graph and stream) once its runs have finished; the
+    tensors stay the caller's."""
     if dpass._handle is not None:
+        if dpass._ran and torch.cuda.is_available():
+            torch.cuda.synchronize()   # no run of the pass may still be in flight
         lib.bt_pass_destroy(dpass._handle)
         dpass._handle = None
 

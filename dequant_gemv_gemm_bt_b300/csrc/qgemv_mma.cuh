@@ -91,15 +91,19 @@ __device__ __forceinline__ uint32_t launder(uint32_t v) {
 // 16 bytes, groups 192 bytes apart, so that lane groups on neighbouring groups
 // read different bank halves.
 constexpr int kXGroupBytes = 192;
-__device__ __forceinline__ uint32_t xslot(uint32_t xs, int v, int c, int t) {
-  return xs + (uint32_t)(v * kXGroupBytes + c * 64 + t * 16);
+// The four-token consumer's lanes read two neighbouring groups of one token in
+// one phase: 160 bytes apart they fall in different bank slots.
+constexpr int kXGroupBytes4 = 160;
+__device__ __forceinline__ uint32_t xslot(uint32_t xs, int v, int c, int t, int gbytes = kXGroupBytes) {
+  return xs + (uint32_t)(v * gbytes + c * 64 + t * 16);
 }
 
 // Permuted, prescaled x of one problem (K values) and its group sums, written
 // by all consumer threads: slot (v, c, t) holds, for the 8 x values j = 0..7 at
 // k = 64v + 32c + 8t + j, the pairs (x0, x4) (x1/16, x5/16) (x2, x6) (x3/16, x7/16)
 // -- the B fragments of the two MMAs of that chunk.
-__device__ __forceinline__ void prep_x(uint32_t xs, float* xsum, const uint16_t* x, int G, int ctid, int nthreads) {
+__device__ __forceinline__ void prep_x(uint32_t xs, float* xsum, const uint16_t* x, int G, int ctid, int nthreads,
+                                       int gbytes = kXGroupBytes) {
   const int lane = ctid & 31;
   for (int base = ctid - lane; base < G * 8; base += nthreads) {
     const int idx = base + lane;
@@ -117,7 +121,7 @@ __device__ __forceinline__ void prep_x(uint32_t xs, float* xsum, const uint16_t*
       o.y = *reinterpret_cast<const uint32_t*>(&p15);
       o.z = *reinterpret_cast<const uint32_t*>(&p26);
       o.w = *reinterpret_cast<const uint32_t*>(&p37);
-      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(xslot(xs, v, c, t)), "r"(o.x), "r"(o.y), "r"(o.z),
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(xslot(xs, v, c, t, gbytes)), "r"(o.x), "r"(o.y), "r"(o.z),
                    "r"(o.w)
                    : "memory");
       const float2 f01 = __half22float2(x01), f23 = __half22float2(x23), f45 = __half22float2(x45),
@@ -293,8 +297,9 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
 #pragma unroll
         for (int tk = 0; tk < TOK; ++tk)   // one staged x per token, tok_groups groups apart
           if (tk < p.tokens)
-            prep_x(xs0 + (uint32_t)(tk * p.tok_groups * kXGroupBytes), xsum + tk * p.tok_groups,
-                   v.x + (size_t)tk * v.k, v.g, threadIdx.x, NW * 32);
+            prep_x(xs0 + (uint32_t)(tk * p.tok_groups * kXGroupBytes + (TOK == 8 ? (tk & 1) * 16 : 0)),
+                   xsum + tk * p.tok_groups,
+                   v.x + (size_t)tk * v.k, v.g, threadIdx.x, NW * 32, TOK == 4 ? kXGroupBytes4 : kXGroupBytes);
       }
       asm volatile("bar.sync 15, %0;" ::"r"(NW * 32) : "memory");
       xs = launder(xs0);
@@ -326,7 +331,9 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
       // B column c holds token c's x, supplied by lanes (c, *).  Lane (g, t)
       // holds tokens 2t and 2t + 1 for rows g and g + 8.
       const bool live = g < p.tokens;   // a lane supplying an empty token slot keeps zeros
-      const uint32_t xlane = (uint32_t)(g * p.tok_groups * kXGroupBytes + tq * 32);
+      // odd tokens' x sits 16 bytes into each group slot: the two tokens of a
+      // load phase then fall in different bank slots
+      const uint32_t xlane = (uint32_t)(g * p.tok_groups * kXGroupBytes + (g & 1) * 16 + tq * 32);
       const uint32_t xs0t = (uint32_t)(2 * tq * p.tok_groups * 4), xs1t = xs0t + (uint32_t)(p.tok_groups * 4);
       uint4 xr[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
       for (; t < ntiles; t += RW) {
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
       // token t's dot products with both groups for rows g and g + 8.
       const int nb2 = G >> 1;   // blocks of two groups
       const bool prov = (tq >> 1) == (g & 1) && (g >> 1) < p.tokens;
-      const uint32_t xlane = (uint32_t)((g >> 1) * p.tok_groups * kXGroupBytes + (g & 1) * kXGroupBytes +
+      const uint32_t xlane = (uint32_t)((g >> 1) * p.tok_groups * kXGroupBytes + (g & 1) * kXGroupBytes4 +
                                         (tq & 1) * 64);
       const uint32_t xsum_tok = (uint32_t)(tq * p.tok_groups * 4);
       uint4 xr[4];
@@ -412,7 +419,7 @@ __global__ void __launch_bounds__(MmaWarps<NW>::kThreads, CTAS)
             const uint4 wb = lds128_nv(cb0 + (uint32_t)(grp * 32));
             if (prov) {
 #pragma unroll
-              for (int w = 0; w < 4; ++w) xr[w] = lds128_nv(xs + xlane + (uint32_t)(grp * kXGroupBytes + w * 16));
+              for (int w = 0; w < 4; ++w) xr[w] = lds128_nv(xs + xlane + (uint32_t)(grp * kXGroupBytes4 + w * 16));
             }
             float dc[4][4] = {};
 #pragma unroll
